@@ -1,0 +1,471 @@
+#!/usr/bin/env python
+"""Benchmark of the dg hot path: one JSON line on rank 0.
+
+A step is one pass of the whole path over one batch of seeded synthetic input:
+  1. FP8 GEMM D = 0.5*(A @ B^T) + C, M = N = K = 4096 (e4m3 in, bf16 out)
+  2. A2A FFN layer forward + backward, P=8 ranks, B=512, T=64, D=1280, k=6
+  3. TP SwiGLU pair, 8 shards, S=8192, d=4096, ffn=14336
+The metric is TFLOP/s over GEMM FLOPs (2*M*N*K per problem; the backward
+counts its own GEMMs).  Every input is far larger than L2 per step (the FFN
+weights alone are 3.8 GB), so L2 holds nothing from one use of an operand
+to its next.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl dg|reference]
+
+Under torchrun (N > 1) every rank runs the same workload on its own GPU
+(replicas: the path needs no exchange between GPUs); value sums the ranks'
+work over the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+FP8 = dict(M=4096, N=4096, K=4096, alpha=0.5, beta=1.0, seed=1)
+FFN = dict(P=8, B=512, T=64, D=1280, k=6, seed=42, dy_seed=43)
+TP = dict(S=8192, d=4096, ffn=14336, W=8, seed=7)
+
+MEASURED_PEAKS = os.path.join(ROOT, "MEASURED_PEAKS.json")
+FALLBACK_PEAKS = dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0)
+
+# Per-launch DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) from
+# one ncu capture of each kernel, with the source file hash it was taken at;
+# a kernel whose source changed since reports null.
+TRAFFIC = {}
+
+
+def gemm_flops():
+    f = {}
+    f["fp8_gemm"] = 2.0 * FP8["M"] * FP8["N"] * FP8["K"]
+    P, B, T, D, k = FFN["P"], FFN["B"], FFN["T"], FFN["D"], FFN["k"]
+    H, M = D * k, P * B
+    fwd = T * (2.0 * M * D * 2 * H + 2.0 * M * H * D)
+    f["ffn_fwd"] = fwd
+    f["ffn_bwd"] = 2.0 * fwd      # dHl, dwout, dX, dw1
+    S, d, ffn = TP["S"], TP["d"], TP["ffn"]
+    f["tp_swiglu"] = 2.0 * S * d * 2 * ffn + 2.0 * S * ffn * d
+    return f
+
+
+def load_peaks():
+    try:
+        with open(MEASURED_PEAKS) as fh:
+            p = json.load(fh)
+        return dict(hbm_gbs=float(p["hbm_gbs"]), bf16_tflops=float(p["bf16_tflops"]),
+                    bf16_tflops_sustained=float(p["bf16_tflops_sustained"]), source="measured")
+    except Exception:
+        return dict(FALLBACK_PEAKS, source="fallback")
+
+
+# ---------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        time.sleep(0.3)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=5)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- workload
+
+class Workload:
+    """Device buffers of one step, inputs drawn once from the seeded generators."""
+
+    def __init__(self, dev):
+        import torch
+
+        import expert_gemm_layers_gb300 as dg
+        from expert_gemm_layers_gb300 import synth
+        self.dg, self.torch, self.dev = dg, torch, dev
+        bf = torch.bfloat16
+        self.A, self.B, self.C = synth.fp8_gemm_inputs(FP8["M"], FP8["N"], FP8["K"], seed=FP8["seed"], device=dev)
+        self.D = torch.empty((FP8["M"], FP8["N"]), dtype=bf, device=dev)
+        P, B, T, D, k = FFN["P"], FFN["B"], FFN["T"], FFN["D"], FFN["k"]
+        t = synth.ffn_inputs(P, B, T, D, k, seed=FFN["seed"], device=dev)
+        self.x = t["inputs"]
+        self.params = {n: t[n] for n in dg.FFN_PARAM_NAMES}
+        self.dY = synth.ffn_grad_output(P, B, T, D, seed=FFN["dy_seed"], device=dev)
+        self.out = torch.empty_like(self.x)
+        sh = dg.ffn_shape(P, B, T, D, k)
+        lib = dg._lib.load()
+        import ctypes
+        self.saved = torch.empty(lib.dg_a2a_ffn_saved_bytes(ctypes.byref(sh)), dtype=torch.uint8, device=dev)
+        self.ws = torch.empty(lib.dg_a2a_ffn_bwd_workspace_bytes(ctypes.byref(sh)), dtype=torch.uint8, device=dev)
+        self.grads = {n: torch.empty_like(v) for n, v in self.params.items()}
+        self.grads["inputs"] = torch.empty_like(self.x)
+        self.xs, self.w13, self.w2 = synth.tp_swiglu_inputs(TP["S"], TP["d"], TP["ffn"], TP["W"], seed=TP["seed"],
+                                                            device=dev)
+        self.y = torch.empty_like(self.xs)
+        self.tp_ws = torch.empty(lib.dg_tp_swiglu_workspace_bytes(TP["S"], TP["d"], TP["ffn"], TP["W"], 1),
+                                 dtype=torch.uint8, device=dev)
+
+    def inputs(self):
+        return [self.A, self.B, self.C, self.x, *self.params.values(), self.dY, self.xs, self.w13, self.w2]
+
+    def outputs(self):
+        return [self.D, self.out, *self.grads.values(), self.y]
+
+    def step(self, marks=None):
+        dg = self.dg
+        dg.gemm_fp8(self.A, self.B, self.C, FP8["alpha"], FP8["beta"], out=self.D)
+        if marks is not None:
+            marks[0].record()
+        dg.a2a_ffn_forward(self.x, self.params, saved=self.saved, out=self.out)
+        if marks is not None:
+            marks[1].record()
+        dg.a2a_ffn_backward(self.x, self.params, self.saved, self.dY, workspace=self.ws, grads=self.grads)
+        if marks is not None:
+            marks[2].record()
+        dg.tp_swiglu(self.xs, self.w13, self.w2, workspace=self.tp_ws, out=self.y)
+
+
+# ---------------------------------------------------------------- oracle sample
+
+class OracleSample:
+    """A bounded sample of the same workload run by the CPU oracle (fp64 numpy).
+
+    Per step: 64 rows of the FP8 GEMM, 32 seeded output rows of the FFN
+    forward, 16 seeded rows of d_inputs, 8 rows of the TP SwiGLU output.
+    Its FLOPs are the GEMM FLOPs of exactly those rows.
+    """
+
+    def __init__(self, host):
+        import oracle as O
+        self.O = O
+        self.h = host
+        rng = np.random.default_rng(0)
+        P, B, T, D, k = FFN["P"], FFN["B"], FFN["T"], FFN["D"], FFN["k"]
+        self.sh = O.FFNShape(P, B, T, D, k)
+        self.fp8_rows = np.arange(64)
+        self.ffn_rows = rng.choice(P * B * T, size=32, replace=False)
+        self.dx_rows = rng.choice(P * B * T, size=16, replace=False)
+        self.tp_rows = rng.choice(TP["S"], size=8, replace=False)
+        H = D * k
+        row_fwd = 2.0 * D * 2 * H + 2.0 * H * D
+        self.flops = (2.0 * len(self.fp8_rows) * FP8["N"] * FP8["K"] + len(self.ffn_rows) * row_fwd
+                      + len(self.dx_rows) * (row_fwd + 2.0 * H * D + 2.0 * 2 * H * D)
+                      + len(self.tp_rows) * (2.0 * TP["d"] * 2 * TP["ffn"] + 2.0 * TP["ffn"] * TP["d"]))
+        self.desc = ("per step: FP8 GEMM rows 0-63 of 4096; 32 seeded FFN output rows; 16 seeded d_inputs rows; "
+                     "8 seeded TP SwiGLU rows (GEMM FLOPs of those rows only)")
+
+    def step(self):
+        O, h = self.O, self.h
+        O.gemm_fp8(h["A"], h["B"], h["C"], FP8["alpha"], FP8["beta"], rows=self.fp8_rows)
+        O.ffn_forward_rows(self.sh, h["inputs"], h, self.ffn_rows)
+        O.ffn_backward_dx_rows(self.sh, h["inputs"], h, h["dY"], self.dx_rows)
+        O.tp_swiglu_rows(h["xs"], h["w13"], h["w2"], TP["W"], self.tp_rows)
+
+
+def host_bits(w):
+    from expert_gemm_layers_gb300 import synth
+    h = dict(A=synth.bits(w.A), B=synth.bits(w.B), C=synth.bits(w.C), inputs=synth.bits(w.x), dY=synth.bits(w.dY),
+             xs=synth.bits(w.xs), w13=synth.bits(w.w13), w2=synth.bits(w.w2))
+    for n, v in w.params.items():
+        h[n] = synth.bits(v)
+    return h
+
+
+def time_oracle(sample, steps, warmup=0):
+    for _ in range(warmup):
+        sample.step()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        sample.step()
+    return (time.perf_counter() - t0) / steps
+
+
+def oracle_threads():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+# ---------------------------------------------------------------- arms
+
+def run_reference(args, rank, world):
+    """The oracle as the reference arm: rank 0 only, host cores only."""
+    if rank != 0:
+        return
+    import torch
+    from expert_gemm_layers_gb300 import synth
+
+    class HostWorkload:
+        pass
+
+    dev = torch.device("cuda", 0) if torch.cuda.is_available() else torch.device("cpu")
+    w = HostWorkload()
+    w.A, w.B, w.C = synth.fp8_gemm_inputs(FP8["M"], FP8["N"], FP8["K"], seed=FP8["seed"], device=dev)
+    t = synth.ffn_inputs(FFN["P"], FFN["B"], FFN["T"], FFN["D"], FFN["k"], seed=FFN["seed"], device=dev)
+    w.x = t["inputs"]
+    w.params = {n: t[n] for n in ("w1", "b1", "wout", "bout", "nx_w", "nx_b", "ng_w", "ng_b")}
+    w.dY = synth.ffn_grad_output(FFN["P"], FFN["B"], FFN["T"], FFN["D"], seed=FFN["dy_seed"], device=dev)
+    w.xs, w.w13, w.w2 = synth.tp_swiglu_inputs(TP["S"], TP["d"], TP["ffn"], TP["W"], seed=TP["seed"], device=dev)
+    h = host_bits(w)
+    del w, t
+    sample = OracleSample(h)
+    sec = time_oracle(sample, args.steps, args.warmup)
+    value = sample.flops / sec / 1e12
+    cores = oracle_threads()
+    line = {
+        "impl": "reference", "metric": "hot-path GEMM TFLOP/s (FP8 GEMM + A2A FFN fwd+bwd + TP SwiGLU)",
+        "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": sec * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic", "config": workload_config(),
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": sample.desc},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def workload_config():
+    return {"workload": "fp8_gemm_4096^3 + a2a_ffn_fwd_bwd(P=8,B=512,T=64,D=1280,k=6) + "
+                        "tp_swiglu(S=8192,d=4096,ffn=14336,W=8)",
+            "fp8_gemm": "M=N=K=4096, alpha=0.5, beta=1, seed 1",
+            "a2a_ffn": "P=8, B=512, T=64, D=1280, k=6, H=7680, L=8, seed 42 (+rank), dY seed 43",
+            "tp_swiglu": "S=8192, d=4096, ffn=14336, W=8, bsz=1, seed 7",
+            "l2": "inputs larger than L2 (5.2 GB of operands per step; no L2 flush)"}
+
+
+def run_dg(args, rank, world):
+    import torch
+    import torch.distributed as dist
+
+    import expert_gemm_layers_gb300 as dg
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    w = Workload(dev)
+    flops = gemm_flops()
+    step_flops = sum(flops.values())
+    stream = torch.cuda.current_stream(dev)
+
+    for _ in range(args.warmup):
+        w.step()
+    torch.cuda.synchronize(dev)
+    st, code = dg.device_status(dev)
+    if st != 0:
+        raise RuntimeError(f"device error word after warm-up: {code:#x}")
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    marks = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    barrier()
+    torch.cuda.synchronize(dev)
+    clocks.start()
+    dg.trace_begin()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for i in range(args.steps):
+        starts[i].record(stream)
+        w.step(marks[i])
+        ends[i].record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize(dev)
+    trace = dg.trace_end()
+    clk = clocks.stop()
+    barrier()
+    ms = t_start.elapsed_time(t_end) / args.steps
+    if world > 1:
+        tt = torch.tensor([ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms = float(tt.item())
+    st, code = dg.device_status(dev)
+    if st != 0:
+        raise RuntimeError(f"device error word after the timed steps: {code:#x}")
+
+    part_ms = {"fp8_gemm": [], "ffn_fwd": [], "ffn_bwd": [], "tp_swiglu": []}
+    for i in range(args.steps):
+        m = marks[i]
+        part_ms["fp8_gemm"].append(starts[i].elapsed_time(m[0]))
+        part_ms["ffn_fwd"].append(m[0].elapsed_time(m[1]))
+        part_ms["ffn_bwd"].append(m[1].elapsed_time(m[2]))
+        part_ms["tp_swiglu"].append(m[2].elapsed_time(ends[i]))
+
+    peaks = load_peaks()
+    parts = {}
+    for name, vals in part_ms.items():
+        pm = statistics.mean(vals)
+        tf = flops[name] / (pm * 1e-3) / 1e12
+        peak = (2.0 * peaks["bf16_tflops"]) if name == "fp8_gemm" else peaks["bf16_tflops"]
+        parts[name] = {"ms": round(pm, 4), "tflops": round(tf, 2), "peak_tflops": peak,
+                       "frac_of_peak": round(tf / peak, 4)}
+    parts["fp8_gemm"]["peak_note"] = "2 x measured bf16 burst (nominal fp8:bf16 ratio 2)"
+
+    # roofline of the dominant kernel (largest share of device time)
+    kernels = {e["name"]: e for e in trace}
+    top = max(trace, key=lambda e: e["total_ms"])
+    per_launch_ms = top["total_ms"] / top["launches"]
+    if top["flops"] > 0:
+        achieved = top["flops"] / top["launches"] / (per_launch_ms * 1e-3) / 1e12
+        peak = peaks["bf16_tflops_sustained"] * (2.0 if top["name"] == "gemm_fp8" else 1.0)
+        roof = {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
+                "frac": round(achieved / peak, 4)}
+    else:
+        achieved = top["bytes"] / top["launches"] / (per_launch_ms * 1e-3) / 1e9
+        peak = peaks["hbm_gbs"]
+        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(achieved / peak, 4)}
+    roof["kernel"] = top["name"]
+    roof["peak_source"] = peaks["source"] + (" sustained bf16" if top["flops"] > 0 else " HBM copy")
+    roof["traffic"] = TRAFFIC.get(top["name"], {}).get("bytes_per_launch")
+    total_ms = sum(e["total_ms"] for e in trace)
+    kernel_table = {e["name"]: {"launches": e["launches"], "ms_per_launch": round(e["total_ms"] / e["launches"], 4),
+                                "share": round(e["total_ms"] / total_ms, 4)} for e in trace}
+    launches = int(sum(e["launches"] for e in trace))
+
+    # end to end: inputs from pinned host memory in, results back to pinned host memory
+    e2e = run_e2e(w, args, dev, step_flops, world)
+
+    value = world * step_flops / (ms * 1e-3) / 1e12
+    line = {
+        "metric": "hot-path GEMM TFLOP/s (FP8 GEMM + A2A FFN fwd+bwd + TP SwiGLU)",
+        "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16+e4m3 (fp32 accumulate)", "data": "synthetic",
+        "config": workload_config(), "parts": parts, "roofline": roof, "kernels": kernel_table,
+        "gpu_launches": launches, "e2e": e2e, "clocks": clk,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        sample = OracleSample(host_bits(w))
+        sec = time_oracle(sample, 1)
+        line["cpu_baseline"] = {"value": round(sample.flops / sec / 1e12, 6), "unit": "TFLOP/s",
+                                "cores": oracle_threads(), "kind": "oracle", "sample": sample.desc,
+                                "seconds": round(sec, 2)}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def run_e2e(w, args, dev, step_flops, world):
+    import torch
+    ins = w.inputs()
+    outs = w.outputs()
+    h_in = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in ins]
+    for h, t in zip(h_in, ins):
+        h.copy_(t)
+    h_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
+    stream = torch.cuda.current_stream(dev)
+    steps = max(1, min(args.steps, 10))
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    e0.record(stream)
+    for _ in range(steps):
+        for h, t in zip(h_in, ins):
+            t.copy_(h, non_blocking=True)
+        w.step()
+        for h, t in zip(h_out, outs):
+            h.copy_(t, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = e0.elapsed_time(e1) / steps
+    if world > 1:
+        import torch.distributed as dist
+        tt = torch.tensor([ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms = float(tt.item())
+    return {"value": round(world * step_flops / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+            "ms_per_step": round(ms, 3), "steps": steps,
+            "h2d_bytes_per_step": int(sum(t.numel() * t.element_size() for t in ins)),
+            "d2h_bytes_per_step": int(sum(t.numel() * t.element_size() for t in outs))}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=("dg", "reference"), default="dg")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+        dist.init_process_group("nccl")
+    try:
+        if args.impl == "reference":
+            run_reference(args, rank, world)
+        else:
+            run_dg(args, rank, world)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

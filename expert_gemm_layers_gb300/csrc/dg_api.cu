@@ -1,0 +1,718 @@
+// The C ABI of libdg (include/dg.h): argument validation, TMA tensor maps,
+// scratch carving and the launch sequence of each operation.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdarg.h>
+#include <stdio.h>
+
+#include <mutex>
+#include <string.h>
+#include <vector>
+
+#include "dg_internal.h"
+
+namespace dg {
+
+// One error word per device, written by kernels whose bounded waits expire.
+__device__ uint32_t g_error_word;
+
+namespace {
+
+thread_local char t_last_error[512] = "";
+
+constexpr int kMaxDevices = 64;
+struct DeviceSlot {
+  std::once_flag once;
+  DeviceInfo info;
+  dg_status status;
+};
+DeviceSlot g_devices[kMaxDevices];
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static std::once_flag once;
+  static EncodeTiledFn fn = nullptr;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+inline size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// True if [a, a+na) and [b, b+nb) overlap.
+inline bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
+  if (!a || !b || na == 0 || nb == 0) return false;
+  const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+  return x < y + nb && y < x + na;
+}
+
+dg_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(DG_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+}  // namespace
+
+dg_status fail(dg_status s, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(t_last_error, sizeof(t_last_error), fmt, ap);
+  va_end(ap);
+  return s;
+}
+
+namespace {
+struct TraceRecord {
+  const char* name;
+  double flops, bytes;
+  cudaEvent_t e0, e1;
+};
+std::mutex g_trace_mu;
+bool g_tracing = false;
+std::vector<TraceRecord> g_trace;
+}  // namespace
+
+TraceScope::TraceScope(const char* name, cudaStream_t s, double flops, double bytes)
+    : stream_(s), name_(name), flops_(flops), bytes_(bytes) {
+  {
+    std::lock_guard<std::mutex> g(g_trace_mu);
+    if (!g_tracing) return;
+  }
+  if (cudaEventCreate(&e0_) != cudaSuccess) return;
+  if (cudaEventCreate(&e1_) != cudaSuccess) {
+    cudaEventDestroy(e0_);
+    return;
+  }
+  cudaEventRecord(e0_, stream_);
+  active_ = true;
+}
+
+TraceScope::~TraceScope() {
+  if (!active_) return;
+  cudaEventRecord(e1_, stream_);
+  std::lock_guard<std::mutex> g(g_trace_mu);
+  g_trace.push_back(TraceRecord{name_, flops_, bytes_, e0_, e1_});
+}
+
+dg_status device_info(DeviceInfo* out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return fail(DG_ERR_UNSUPPORTED, "device ordinal %d out of range", dev);
+  DeviceSlot& slot = g_devices[dev];
+  std::call_once(slot.once, [&] {
+    slot.status = DG_OK;
+    slot.info.device = dev;
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&slot.info.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+      slot.status = DG_ERR_CUDA;
+      return;
+    }
+    if (major != 10 || minor != 3) {
+      slot.status = DG_ERR_UNSUPPORTED;
+      return;
+    }
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_error_word) != cudaSuccess) {
+      slot.status = DG_ERR_CUDA;
+      return;
+    }
+    slot.info.err = static_cast<uint32_t*>(p);
+  });
+  if (slot.status == DG_ERR_UNSUPPORTED)
+    return fail(DG_ERR_UNSUPPORTED, "device %d is not sm_103 (this library is built for sm_103a only)", dev);
+  if (slot.status != DG_OK) return fail(slot.status, "device %d: attribute or symbol query failed", dev);
+  *out = slot.info;
+  return DG_OK;
+}
+
+dg_status make_map_3d(CUtensorMap* map, bool is_bf16, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
+                      uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t b0, uint32_t b1, uint32_t b2,
+                      const char* what) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return fail(DG_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  if (!aligned16(base)) return fail(DG_ERR_INVALID_ARGUMENT, "%s: base address must be 16-byte aligned", what);
+  if ((stride1_bytes & 15u) || (stride2_bytes & 15u))
+    return fail(DG_ERR_INVALID_ARGUMENT, "%s: row strides must be multiples of 16 bytes", what);
+  if (d0 == 0 || d1 == 0 || d2 == 0) return fail(DG_ERR_INVALID_ARGUMENT, "%s: empty dimension", what);
+  const cuuint64_t dims[3] = {d0, d1, d2};
+  const cuuint64_t strides[2] = {stride1_bytes, stride2_bytes};
+  const cuuint32_t box[3] = {b0, b1, b2};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(map, is_bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 3,
+                   const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(DG_ERR_INVALID_ARGUMENT, "%s: tensor map rejected (CUresult %d)", what, (int)r);
+  return DG_OK;
+}
+
+int gemm_tile_m() { return 128; }
+
+int gemm_tile_n(GemmVariant v) { return v == GV_BF16_KK_SWIGLU ? 128 : 256; }
+
+dg_status run_gemm(GemmVariant v, const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& d,
+                   const CUtensorMap& c, GemmParams p, const DeviceInfo& dev, cudaStream_t s, const char* name,
+                   double bytes) {
+  p.tiles_m = (p.M + gemm_tile_m() - 1) / gemm_tile_m();
+  p.tiles_n = (p.N + gemm_tile_n(v) - 1) / gemm_tile_n(v);
+  p.err = dev.err;
+  const int64_t tiles = static_cast<int64_t>(p.G) * p.tiles_m * p.tiles_n;
+  if (tiles == 0) return DG_OK;
+  if (tiles > 0x7fffffff) return fail(DG_ERR_UNSUPPORTED, "too many output tiles (%lld)", (long long)tiles);
+  const int grid = static_cast<int>(tiles < dev.num_sms ? tiles : dev.num_sms);
+  const double n_mma = v == GV_BF16_KK_SWIGLU ? 2.0 * p.N : static_cast<double>(p.N);
+  TraceScope trace(name, s, 2.0 * p.G * static_cast<double>(p.M) * n_mma * p.K, bytes);
+  cudaError_t e;
+  switch (v) {
+    case GV_FP8_KK: e = launch_gemm_fp8_kk(a, b, d, c, p, grid, s); break;
+    case GV_BF16_KK_STORE: e = launch_gemm_bf16_kk_store(a, b, d, c, p, grid, s); break;
+    case GV_BF16_KM_BIAS: e = launch_gemm_bf16_km_bias(a, b, d, c, p, grid, s); break;
+    case GV_BF16_MM_STORE: e = launch_gemm_bf16_mm_store(a, b, d, c, p, grid, s); break;
+    case GV_BF16_KK_SWIGLU: e = launch_gemm_bf16_kk_swiglu(a, b, d, c, p, grid, s); break;
+    default: return fail(DG_ERR_UNSUPPORTED, "unknown GEMM variant");
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "GEMM launch");
+  return DG_OK;
+}
+
+}  // namespace dg
+
+using namespace dg;
+
+namespace {
+
+struct FfnDims {
+  int64_t P, B, T, D, k, H, L, M;
+};
+
+dg_status check_ffn_shape(const dg_ffn_shape* sh, FfnDims* o) {
+  if (!sh) return fail(DG_ERR_INVALID_ARGUMENT, "shape is NULL");
+  if (sh->P < 1 || sh->B < 1 || sh->T < 1 || sh->D < 1 || sh->k < 1)
+    return fail(DG_ERR_INVALID_ARGUMENT, "shape: P, B, T, D, k must all be >= 1 (got %d, %d, %d, %d, %d)", sh->P,
+                sh->B, sh->T, sh->D, sh->k);
+  if (sh->T % sh->P) return fail(DG_ERR_INVALID_ARGUMENT, "shape: T %% P != 0 (T=%d, P=%d)", sh->T, sh->P);
+  if (sh->D % 8) return fail(DG_ERR_INVALID_ARGUMENT, "shape: D must be a multiple of 8 (16-byte rows), got %d", sh->D);
+  if (!(sh->eps > 0.0f)) return fail(DG_ERR_INVALID_ARGUMENT, "shape: eps must be > 0");
+  o->P = sh->P; o->B = sh->B; o->T = sh->T; o->D = sh->D; o->k = sh->k;
+  o->H = o->D * o->k;
+  o->L = o->T / o->P;
+  o->M = o->P * o->B;
+  if (o->H > 8192) return fail(DG_ERR_UNSUPPORTED, "shape: H = D*k = %lld exceeds 8192", (long long)o->H);
+  if (o->M > (1 << 30)) return fail(DG_ERR_UNSUPPORTED, "shape: P*B too large");
+  return DG_OK;
+}
+
+// Carving of the forward's `saved` buffer: Z [T,M,2H] bf16, Hl [T,M,H] bf16, stats [T,M] float4.
+struct SavedLayout {
+  size_t z, hl, stats, total;
+};
+SavedLayout saved_layout(const FfnDims& f) {
+  SavedLayout l;
+  const size_t rows = static_cast<size_t>(f.T) * f.M;
+  l.z = 0;
+  l.hl = round_up(l.z + rows * 2 * f.H * 2, 256);
+  l.stats = round_up(l.hl + rows * f.H * 2, 256);
+  l.total = round_up(l.stats + rows * 16, 256);
+  return l;
+}
+
+// Carving of the backward's workspace: dHl [T,M,H], dZ [T,M,2H], partials [T,nchunk,6,H] fp32.
+struct BwdLayout {
+  size_t dhl, dz, part, total;
+  int nchunk;
+};
+BwdLayout bwd_layout(const FfnDims& f) {
+  BwdLayout l;
+  const size_t rows = static_cast<size_t>(f.T) * f.M;
+  l.nchunk = ffn_bwd_chunks(static_cast<int>(f.T), static_cast<int>(f.M));
+  l.dhl = 0;
+  l.dz = round_up(rows * f.H * 2, 256);
+  l.part = round_up(l.dz + rows * 2 * f.H * 2, 256);
+  l.total = round_up(l.part + static_cast<size_t>(f.T) * l.nchunk * 6 * f.H * 4, 256);
+  return l;
+}
+
+inline const char* ptr_name_null(const void* const* ptrs, const char* const* names, int n) {
+  for (int i = 0; i < n; ++i)
+    if (!ptrs[i]) return names[i];
+  return nullptr;
+}
+
+inline const char* ptr_name_unaligned(const void* const* ptrs, const char* const* names, int n) {
+  for (int i = 0; i < n; ++i)
+    if (!aligned16(ptrs[i])) return names[i];
+  return nullptr;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* dg_last_error(void) { return t_last_error; }
+
+const char* dg_version(void) { return "dg 0.1 (sm_103a)"; }
+
+dg_status dg_device_status(void* stream, uint32_t* site) {
+  DeviceInfo dev;
+  dg_status st = device_info(&dev);
+  if (st != DG_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  uint32_t word = 0;
+  e = cudaMemcpy(&word, dev.err, sizeof(word), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "reading the error word");
+  if (word == 0) return DG_OK;
+  const uint32_t zero = 0;
+  e = cudaMemcpy(dev.err, &zero, sizeof(zero), cudaMemcpyHostToDevice);
+  if (e != cudaSuccess) return cuda_fail(e, "clearing the error word");
+  if (site) *site = word;
+  if (word & kErrTimeout)
+    return fail(DG_ERR_TIMEOUT, "a device-side wait exceeded its limit (site %u)", word & 0xffu);
+  return fail(DG_ERR_DEVICE_CHECK, "device-side check failed (code 0x%x)", word);
+}
+
+dg_status dg_debug_wait_timeout(uint32_t limit_us, void* stream) {
+  DeviceInfo dev;
+  dg_status st = device_info(&dev);
+  if (st != DG_OK) return st;
+  if (limit_us == 0 || limit_us > 10u * 1000u * 1000u)
+    return fail(DG_ERR_INVALID_ARGUMENT, "limit_us must be in (0, 10 s]");
+  cudaError_t e = launch_debug_wait(dev.err, static_cast<uint64_t>(limit_us) * 1000u, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "debug wait launch");
+  return DG_OK;
+}
+
+// ------------------------------------------------------------------ FP8 GEMM
+
+dg_status dg_gemm_fp8(int64_t M, int64_t N, int64_t K, const void* A, const void* B, const void* C, void* D,
+                      float alpha, float beta, void* stream) {
+  if (M < 0 || N < 0 || K < 0) return fail(DG_ERR_INVALID_ARGUMENT, "gemm_fp8: negative size");
+  if (M == 0 || N == 0) return DG_OK;
+  if (M > 0x7fffffff || N > 0x7fffffff || K > 0x7fffffff)
+    return fail(DG_ERR_UNSUPPORTED, "gemm_fp8: sizes beyond 2^31-1");
+  if (K % 16) return fail(DG_ERR_INVALID_ARGUMENT, "gemm_fp8: K must be a multiple of 16 (16-byte rows), got %lld",
+                          (long long)K);
+  if (N % 8) return fail(DG_ERR_INVALID_ARGUMENT, "gemm_fp8: N must be a multiple of 8 (16-byte rows), got %lld",
+                         (long long)N);
+  if (!D) return fail(DG_ERR_INVALID_ARGUMENT, "gemm_fp8: D is NULL");
+  if (K > 0 && (!A || !B)) return fail(DG_ERR_INVALID_ARGUMENT, "gemm_fp8: A or B is NULL");
+  const bool has_c = beta != 0.0f;
+  if (has_c && !C) return fail(DG_ERR_INVALID_ARGUMENT, "gemm_fp8: C is NULL but beta != 0");
+  const size_t dbytes = static_cast<size_t>(M) * N * 2;
+  if (overlaps(D, dbytes, A, static_cast<size_t>(M) * K) || overlaps(D, dbytes, B, static_cast<size_t>(N) * K) ||
+      (has_c && overlaps(D, dbytes, C, dbytes)))
+    return fail(DG_ERR_INVALID_ARGUMENT, "gemm_fp8: D overlaps an input");
+  DeviceInfo dev;
+  dg_status st = device_info(&dev);
+  if (st != DG_OK) return st;
+  CUtensorMap ma, mb, md, mc;
+  // K == 0: the maps still need a valid (non-empty) tensor; the kernel loads nothing.
+  const uint64_t kd = K > 0 ? static_cast<uint64_t>(K) : 16u;
+  const void* a_ptr = K > 0 ? A : D;
+  const void* b_ptr = K > 0 ? B : D;
+  const uint64_t am = K > 0 ? static_cast<uint64_t>(M) : 1u, bn = K > 0 ? static_cast<uint64_t>(N) : 1u;
+  if ((st = make_map_3d(&ma, false, a_ptr, kd, am, 1, kd, kd * am, 128, 128, 1, "A")) != DG_OK) return st;
+  if ((st = make_map_3d(&mb, false, b_ptr, kd, bn, 1, kd, kd * bn, 128, 256, 1, "B")) != DG_OK) return st;
+  if ((st = make_map_3d(&md, true, D, N, M, 1, N * 2, N * 2 * M, 64, 32, 1, "D")) != DG_OK) return st;
+  if (has_c) {
+    if ((st = make_map_3d(&mc, true, C, N, M, 1, N * 2, N * 2 * M, 64, 32, 1, "C")) != DG_OK) return st;
+  } else {
+    mc = md;
+  }
+  GemmParams p{};
+  p.G = 1;
+  p.M = static_cast<int32_t>(M);
+  p.N = static_cast<int32_t>(N);
+  p.K = static_cast<int32_t>(K);
+  p.a_g = p.b_g = p.d_g = G_OUTER;
+  p.alpha = alpha;
+  p.beta = beta;
+  p.has_c = has_c ? 1 : 0;
+  const double bytes = static_cast<double>(M) * K + static_cast<double>(N) * K + (has_c ? 2.0 : 1.0) * 2.0 * M * N;
+  return run_gemm(GV_FP8_KK, ma, mb, md, mc, p, dev, static_cast<cudaStream_t>(stream), "gemm_fp8", bytes);
+}
+
+// ------------------------------------------------------------------ A2A FFN
+
+size_t dg_a2a_ffn_saved_bytes(const dg_ffn_shape* shape) {
+  FfnDims f;
+  if (check_ffn_shape(shape, &f) != DG_OK) return 0;
+  return saved_layout(f).total;
+}
+
+size_t dg_a2a_ffn_bwd_workspace_bytes(const dg_ffn_shape* shape) {
+  FfnDims f;
+  if (check_ffn_shape(shape, &f) != DG_OK) return 0;
+  return bwd_layout(f).total;
+}
+
+dg_status dg_a2a_ffn_fwd(const dg_ffn_shape* shape, const void* inputs, const void* w1, const void* b1,
+                         const void* wout, const void* bout, const void* nx_w, const void* nx_b, const void* ng_w,
+                         const void* ng_b, void* output, void* saved, size_t saved_bytes, void* stream) {
+  FfnDims f;
+  dg_status st = check_ffn_shape(shape, &f);
+  if (st != DG_OK) return st;
+  const void* ptrs[] = {inputs, w1, b1, wout, bout, nx_w, nx_b, ng_w, ng_b, output, saved};
+  const char* names[] = {"inputs", "w1", "b1", "wout", "bout", "nx_w", "nx_b", "ng_w", "ng_b", "output", "saved"};
+  if (const char* n = ptr_name_null(ptrs, names, 11)) return fail(DG_ERR_INVALID_ARGUMENT, "a2a_ffn_fwd: %s is NULL", n);
+  if (const char* n = ptr_name_unaligned(ptrs, names, 11))
+    return fail(DG_ERR_INVALID_ARGUMENT, "a2a_ffn_fwd: %s is not 16-byte aligned", n);
+  const SavedLayout sl = saved_layout(f);
+  if (saved_bytes < sl.total)
+    return fail(DG_ERR_WORKSPACE, "a2a_ffn_fwd: saved buffer has %zu bytes, needs %zu", saved_bytes, sl.total);
+  const size_t act = static_cast<size_t>(f.P) * f.B * f.T * f.D * 2;
+  if (overlaps(output, act, inputs, act) || overlaps(output, act, saved, sl.total) ||
+      overlaps(saved, sl.total, inputs, act))
+    return fail(DG_ERR_INVALID_ARGUMENT, "a2a_ffn_fwd: output / saved / inputs overlap");
+  DeviceInfo dev;
+  if ((st = device_info(&dev)) != DG_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* sv = static_cast<uint8_t*>(saved);
+  void* Z = sv + sl.z;
+  void* Hl = sv + sl.hl;
+  void* stats = sv + sl.stats;
+  const uint64_t T = f.T, M = f.M, D = f.D, H = f.H;
+
+  // GEMM1: Z_t = Xlocal_t @ w1_t + b1_t.  Xlocal_t row n is inputs row n*T + t (dispatch).
+  CUtensorMap mx, mw1, mz;
+  if ((st = make_map_3d(&mx, true, inputs, D, T, M, D * 2, T * D * 2, 64, 1, 128, "inputs")) != DG_OK) return st;
+  if ((st = make_map_3d(&mw1, true, w1, 2 * H, D, T, 2 * H * 2, D * 2 * H * 2, 64, 64, 1, "w1")) != DG_OK) return st;
+  if ((st = make_map_3d(&mz, true, Z, 2 * H, M, T, 2 * H * 2, M * 2 * H * 2, 64, 32, 1, "Z")) != DG_OK) return st;
+  GemmParams p1{};
+  p1.G = static_cast<int32_t>(T);
+  p1.M = static_cast<int32_t>(M);
+  p1.N = static_cast<int32_t>(2 * H);
+  p1.K = static_cast<int32_t>(D);
+  p1.a_g = G_MID;
+  p1.b_g = G_OUTER;
+  p1.d_g = G_OUTER;
+  p1.bias = static_cast<const __nv_bfloat16*>(b1);
+  p1.bias_g_stride = static_cast<int64_t>(2 * H);
+  const double rows = static_cast<double>(T) * M;
+  if ((st = run_gemm(GV_BF16_KM_BIAS, mx, mw1, mz, mz, p1, dev, s, "ffn_gemm1",
+                     2.0 * (rows * D + static_cast<double>(T) * D * 2 * H + rows * 2 * H))) != DG_OK)
+    return st;
+
+  // LayerNorm of both halves, gate: Hl = LN_x(U) * silu(LN_g(G)).
+  cudaError_t e;
+  {
+    TraceScope trace("ffn_ln_gate_fwd", s, 0.0, rows * (2.0 * 2 * H + 2.0 * H + 16.0));
+    e = launch_ln_gate_fwd(Z, nx_w, nx_b, ng_w, ng_b, Hl, stats, static_cast<int64_t>(T * M),
+                                     static_cast<int>(M), static_cast<int>(f.L), static_cast<int>(H), shape->eps, dev, s);
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "LayerNorm-gate launch");
+
+  // GEMM2: output rows (s, b, t) = Hl_t @ wout_t + bout_t at the combine offsets.
+  CUtensorMap mh, mwo, mo;
+  if ((st = make_map_3d(&mh, true, Hl, H, M, T, H * 2, M * H * 2, 64, 128, 1, "Hl")) != DG_OK) return st;
+  if ((st = make_map_3d(&mwo, true, wout, D, H, T, D * 2, H * D * 2, 64, 64, 1, "wout")) != DG_OK) return st;
+  if ((st = make_map_3d(&mo, true, output, D, T, M, D * 2, T * D * 2, 64, 1, 32, "output")) != DG_OK) return st;
+  GemmParams p2{};
+  p2.G = static_cast<int32_t>(T);
+  p2.M = static_cast<int32_t>(M);
+  p2.N = static_cast<int32_t>(D);
+  p2.K = static_cast<int32_t>(H);
+  p2.a_g = G_OUTER;
+  p2.b_g = G_OUTER;
+  p2.d_g = G_MID;
+  p2.bias = static_cast<const __nv_bfloat16*>(bout);
+  p2.bias_g_stride = static_cast<int64_t>(D);
+  return run_gemm(GV_BF16_KM_BIAS, mh, mwo, mo, mo, p2, dev, s, "ffn_gemm2",
+                  2.0 * (rows * H + static_cast<double>(T) * H * D + rows * D));
+}
+
+dg_status dg_a2a_ffn_bwd(const dg_ffn_shape* shape, const void* inputs, const void* w1, const void* b1,
+                         const void* wout, const void* bout, const void* nx_w, const void* nx_b, const void* ng_w,
+                         const void* ng_b, const void* saved, size_t saved_bytes, const void* dY, void* d_inputs,
+                         void* d_w1, void* d_b1, void* d_wout, void* d_bout, void* d_nx_w, void* d_nx_b,
+                         void* d_ng_w, void* d_ng_b, void* ws, size_t ws_bytes, void* stream) {
+  FfnDims f;
+  dg_status st = check_ffn_shape(shape, &f);
+  if (st != DG_OK) return st;
+  (void)b1;
+  (void)bout;
+  const void* ptrs[] = {inputs, w1, wout, nx_w, nx_b, ng_w, ng_b, saved, dY, d_inputs, d_w1, d_b1,
+                        d_wout, d_bout, d_nx_w, d_nx_b, d_ng_w, d_ng_b, ws};
+  const char* names[] = {"inputs", "w1", "wout", "nx_w", "nx_b", "ng_w", "ng_b", "saved", "dY", "d_inputs",
+                         "d_w1", "d_b1", "d_wout", "d_bout", "d_nx_w", "d_nx_b", "d_ng_w", "d_ng_b", "ws"};
+  if (const char* n = ptr_name_null(ptrs, names, 19)) return fail(DG_ERR_INVALID_ARGUMENT, "a2a_ffn_bwd: %s is NULL", n);
+  if (const char* n = ptr_name_unaligned(ptrs, names, 19))
+    return fail(DG_ERR_INVALID_ARGUMENT, "a2a_ffn_bwd: %s is not 16-byte aligned", n);
+  const SavedLayout sl = saved_layout(f);
+  if (saved_bytes < sl.total)
+    return fail(DG_ERR_WORKSPACE, "a2a_ffn_bwd: saved buffer has %zu bytes, needs %zu", saved_bytes, sl.total);
+  const BwdLayout bl = bwd_layout(f);
+  if (ws_bytes < bl.total)
+    return fail(DG_ERR_WORKSPACE, "a2a_ffn_bwd: workspace has %zu bytes, needs %zu", ws_bytes, bl.total);
+  const size_t act = static_cast<size_t>(f.P) * f.B * f.T * f.D * 2;
+  if (overlaps(d_inputs, act, dY, act) || overlaps(d_inputs, act, inputs, act) ||
+      overlaps(ws, bl.total, saved, sl.total) || overlaps(ws, bl.total, dY, act) ||
+      overlaps(ws, bl.total, d_inputs, act))
+    return fail(DG_ERR_INVALID_ARGUMENT, "a2a_ffn_bwd: outputs / workspace / inputs overlap");
+  DeviceInfo dev;
+  if ((st = device_info(&dev)) != DG_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const uint8_t* sv = static_cast<const uint8_t*>(saved);
+  const void* Z = sv + sl.z;
+  const void* Hl = sv + sl.hl;
+  const void* stats = sv + sl.stats;
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  void* dHl = w + bl.dhl;
+  void* dZ = w + bl.dz;
+  float* part = reinterpret_cast<float*>(w + bl.part);
+  const uint64_t T = f.T, M = f.M, D = f.D, H = f.H;
+
+  // (1) dHl_t = dY_t @ wout_t^T      (dY_t: the dispatched rows of dY)
+  CUtensorMap mdy_k, mwo_k, mdh;
+  if ((st = make_map_3d(&mdy_k, true, dY, D, T, M, D * 2, T * D * 2, 64, 1, 128, "dY")) != DG_OK) return st;
+  if ((st = make_map_3d(&mwo_k, true, wout, D, H, T, D * 2, H * D * 2, 64, 256, 1, "wout")) != DG_OK) return st;
+  if ((st = make_map_3d(&mdh, true, dHl, H, M, T, H * 2, M * H * 2, 64, 32, 1, "dHl")) != DG_OK) return st;
+  GemmParams p{};
+  p.G = static_cast<int32_t>(T);
+  p.M = static_cast<int32_t>(M);
+  p.N = static_cast<int32_t>(H);
+  p.K = static_cast<int32_t>(D);
+  p.a_g = G_MID;
+  p.b_g = G_OUTER;
+  p.d_g = G_OUTER;
+  const double rows = static_cast<double>(T) * M;
+  if ((st = run_gemm(GV_BF16_KK_STORE, mdy_k, mwo_k, mdh, mdh, p, dev, s, "ffn_bwd_dhl",
+                     2.0 * (rows * D + static_cast<double>(T) * H * D + rows * H))) != DG_OK)
+    return st;
+
+  // (2) dwout_t = Hl_t^T @ dY_t     [H, D], contraction over the M rows
+  CUtensorMap mhl_t, mdy_n, mdwo;
+  if ((st = make_map_3d(&mhl_t, true, Hl, H, M, T, H * 2, M * H * 2, 64, 64, 1, "Hl^T")) != DG_OK) return st;
+  if ((st = make_map_3d(&mdy_n, true, dY, D, T, M, D * 2, T * D * 2, 64, 1, 64, "dY (N-major)")) != DG_OK) return st;
+  if ((st = make_map_3d(&mdwo, true, d_wout, D, H, T, D * 2, H * D * 2, 64, 32, 1, "d_wout")) != DG_OK) return st;
+  p = GemmParams{};
+  p.G = static_cast<int32_t>(T);
+  p.M = static_cast<int32_t>(H);
+  p.N = static_cast<int32_t>(D);
+  p.K = static_cast<int32_t>(M);
+  p.a_g = G_OUTER;
+  p.b_g = G_MID;
+  p.d_g = G_OUTER;
+  if ((st = run_gemm(GV_BF16_MM_STORE, mhl_t, mdy_n, mdwo, mdwo, p, dev, s, "ffn_bwd_dwout",
+                     2.0 * (rows * H + rows * D + static_cast<double>(T) * H * D))) != DG_OK)
+    return st;
+
+  // (3) dbout_t = sum_n dY_t[n, :]
+  cudaError_t e;
+  {
+    TraceScope trace("ffn_bwd_dbout", s, 0.0, rows * D * 2.0 + static_cast<double>(T) * D * 2.0);
+    e = launch_column_sum(dY, d_bout, static_cast<int>(T), static_cast<int>(M), static_cast<int>(D),
+                                    static_cast<int64_t>(D), static_cast<int64_t>(T * D), dev, s);
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "column-sum launch");
+
+  // (4) gate + LayerNorm backward -> dZ, column partials
+  {
+    TraceScope trace("ffn_bwd_ln_gate", s, 0.0,
+                     rows * (2.0 * 2 * H + 2.0 * H + 16.0 + 2.0 * 2 * H) + static_cast<double>(T) * bl.nchunk * 6 * H * 4);
+    e = launch_ln_gate_bwd(Z, stats, dHl, nx_w, nx_b, ng_w, ng_b, dZ, part, static_cast<int>(T), static_cast<int>(M),
+                         static_cast<int>(f.L), static_cast<int>(H), bl.nchunk, dev, s);
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "LayerNorm-gate backward launch");
+
+  // (5) db1, d(norm_x), d(norm_gate) from the partials
+  {
+    TraceScope trace("ffn_bwd_reduce", s, 0.0, static_cast<double>(T) * bl.nchunk * 6 * H * 4);
+    e = launch_reduce_partials(part, d_b1, d_nx_w, d_nx_b, d_ng_w, d_ng_b, static_cast<int>(f.P), static_cast<int>(f.L),
+                             static_cast<int>(H), bl.nchunk, dev, s);
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "partials reduction launch");
+
+  // (6) dX_t = dZ_t @ w1_t^T, stored at the rows dispatch read from (inverse permutation)
+  CUtensorMap mdz_k, mw1_k, mdx;
+  if ((st = make_map_3d(&mdz_k, true, dZ, 2 * H, M, T, 2 * H * 2, M * 2 * H * 2, 64, 128, 1, "dZ")) != DG_OK) return st;
+  if ((st = make_map_3d(&mw1_k, true, w1, 2 * H, D, T, 2 * H * 2, D * 2 * H * 2, 64, 256, 1, "w1 (K-major)")) != DG_OK)
+    return st;
+  if ((st = make_map_3d(&mdx, true, d_inputs, D, T, M, D * 2, T * D * 2, 64, 1, 32, "d_inputs")) != DG_OK) return st;
+  p = GemmParams{};
+  p.G = static_cast<int32_t>(T);
+  p.M = static_cast<int32_t>(M);
+  p.N = static_cast<int32_t>(D);
+  p.K = static_cast<int32_t>(2 * H);
+  p.a_g = G_OUTER;
+  p.b_g = G_OUTER;
+  p.d_g = G_MID;
+  if ((st = run_gemm(GV_BF16_KK_STORE, mdz_k, mw1_k, mdx, mdx, p, dev, s, "ffn_bwd_dx",
+                     2.0 * (rows * 2 * H + static_cast<double>(T) * D * 2 * H + rows * D))) != DG_OK)
+    return st;
+
+  // (7) dw1_t = Xlocal_t^T @ dZ_t   [D, 2H], contraction over the M rows
+  CUtensorMap mx_t, mdz_n, mdw1;
+  if ((st = make_map_3d(&mx_t, true, inputs, D, T, M, D * 2, T * D * 2, 64, 1, 64, "inputs^T")) != DG_OK) return st;
+  if ((st = make_map_3d(&mdz_n, true, dZ, 2 * H, M, T, 2 * H * 2, M * 2 * H * 2, 64, 64, 1, "dZ (N-major)")) != DG_OK)
+    return st;
+  if ((st = make_map_3d(&mdw1, true, d_w1, 2 * H, D, T, 2 * H * 2, D * 2 * H * 2, 64, 32, 1, "d_w1")) != DG_OK)
+    return st;
+  p = GemmParams{};
+  p.G = static_cast<int32_t>(T);
+  p.M = static_cast<int32_t>(D);
+  p.N = static_cast<int32_t>(2 * H);
+  p.K = static_cast<int32_t>(M);
+  p.a_g = G_MID;
+  p.b_g = G_OUTER;
+  p.d_g = G_OUTER;
+  return run_gemm(GV_BF16_MM_STORE, mx_t, mdz_n, mdw1, mdw1, p, dev, s, "ffn_bwd_dw1",
+                  2.0 * (rows * D + rows * 2 * H + static_cast<double>(T) * D * 2 * H));
+}
+
+dg_status dg_a2a_dispatch(int32_t P, int32_t B, int32_t T, int32_t D, const void* inputs, void* xlocal,
+                          void* stream) {
+  if (P < 1 || B < 1 || T < 1 || D < 1 || T % P || D % 8)
+    return fail(DG_ERR_INVALID_ARGUMENT, "a2a_dispatch: need P,B,T,D >= 1, T %% P == 0, D %% 8 == 0");
+  if (!inputs || !xlocal || !aligned16(inputs) || !aligned16(xlocal))
+    return fail(DG_ERR_INVALID_ARGUMENT, "a2a_dispatch: NULL or unaligned pointer");
+  const size_t bytes = static_cast<size_t>(P) * B * T * D * 2;
+  if (overlaps(inputs, bytes, xlocal, bytes)) return fail(DG_ERR_INVALID_ARGUMENT, "a2a_dispatch: in-place not supported");
+  DeviceInfo dev;
+  dg_status st = device_info(&dev);
+  if (st != DG_OK) return st;
+  TraceScope trace("a2a_dispatch", static_cast<cudaStream_t>(stream), 0.0, 2.0 * bytes);
+  cudaError_t e = launch_dispatch(inputs, xlocal, P, B, T, D, dev, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? DG_OK : cuda_fail(e, "dispatch launch");
+}
+
+dg_status dg_a2a_combine(int32_t P, int32_t B, int32_t T, int32_t D, const void* ylocal, void* output,
+                         void* stream) {
+  if (P < 1 || B < 1 || T < 1 || D < 1 || T % P || D % 8)
+    return fail(DG_ERR_INVALID_ARGUMENT, "a2a_combine: need P,B,T,D >= 1, T %% P == 0, D %% 8 == 0");
+  if (!ylocal || !output || !aligned16(ylocal) || !aligned16(output))
+    return fail(DG_ERR_INVALID_ARGUMENT, "a2a_combine: NULL or unaligned pointer");
+  const size_t bytes = static_cast<size_t>(P) * B * T * D * 2;
+  if (overlaps(ylocal, bytes, output, bytes)) return fail(DG_ERR_INVALID_ARGUMENT, "a2a_combine: in-place not supported");
+  DeviceInfo dev;
+  dg_status st = device_info(&dev);
+  if (st != DG_OK) return st;
+  TraceScope trace("a2a_combine", static_cast<cudaStream_t>(stream), 0.0, 2.0 * bytes);
+  cudaError_t e = launch_combine(ylocal, output, P, B, T, D, dev, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? DG_OK : cuda_fail(e, "combine launch");
+}
+
+// ------------------------------------------------------------------ TP SwiGLU
+
+size_t dg_tp_swiglu_workspace_bytes(int64_t S, int64_t d, int64_t ffn, int32_t W, int32_t bsz) {
+  if (S < 1 || d < 1 || ffn < 1 || W < 1 || bsz < 1 || S % W || ffn % W) return 0;
+  return round_up(static_cast<size_t>(S) * bsz * ffn * 2, 256);
+}
+
+dg_status dg_tp_swiglu(int64_t S, int64_t d, int64_t ffn, int32_t W, int32_t bsz, const void* x_shards,
+                       const void* w13, const void* w2, void* y_shards, void* ws, size_t ws_bytes, void* stream) {
+  if (S < 1 || d < 1 || ffn < 1 || W < 1 || bsz < 1)
+    return fail(DG_ERR_INVALID_ARGUMENT, "tp_swiglu: S, d, ffn, W, bsz must be >= 1");
+  if (S % W || ffn % W) return fail(DG_ERR_INVALID_ARGUMENT, "tp_swiglu: S and ffn must be divisible by W");
+  const int64_t F = ffn / W;
+  if (d % 8 || F % 8) return fail(DG_ERR_INVALID_ARGUMENT, "tp_swiglu: d and ffn/W must be multiples of 8");
+  const int64_t rows = S * bsz;
+  if (rows > 0x7fffffff || ffn > 0x7fffffff || d > 0x7fffffff)
+    return fail(DG_ERR_UNSUPPORTED, "tp_swiglu: sizes beyond 2^31-1");
+  const void* ptrs[] = {x_shards, w13, w2, y_shards, ws};
+  const char* names[] = {"x_shards", "w13", "w2", "y_shards", "ws"};
+  if (const char* n = ptr_name_null(ptrs, names, 5)) return fail(DG_ERR_INVALID_ARGUMENT, "tp_swiglu: %s is NULL", n);
+  if (const char* n = ptr_name_unaligned(ptrs, names, 5))
+    return fail(DG_ERR_INVALID_ARGUMENT, "tp_swiglu: %s is not 16-byte aligned", n);
+  const size_t need = dg_tp_swiglu_workspace_bytes(S, d, ffn, W, bsz);
+  if (ws_bytes < need) return fail(DG_ERR_WORKSPACE, "tp_swiglu: workspace has %zu bytes, needs %zu", ws_bytes, need);
+  const size_t act = static_cast<size_t>(rows) * d * 2;
+  if (overlaps(y_shards, act, x_shards, act) || overlaps(ws, need, y_shards, act) || overlaps(ws, need, x_shards, act))
+    return fail(DG_ERR_INVALID_ARGUMENT, "tp_swiglu: outputs / workspace / inputs overlap");
+  DeviceInfo dev;
+  dg_status st = device_info(&dev);
+  if (st != DG_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const uint64_t R = rows, Dm = d, Fu = F, Wu = W, FF = ffn;
+
+  // GEMM1 over all shards: h[:, s*F + c] = silu(X w1_s[c]) * (X w3_s[c]).  The
+  // gathered X is the rows of x_shards in memory order (rank, batch, seq_local).
+  CUtensorMap mx, mw13, mh;
+  if ((st = make_map_3d(&mx, true, x_shards, Dm, R, 1, Dm * 2, R * Dm * 2, 64, 128, 1, "x_shards")) != DG_OK) return st;
+  if ((st = make_map_3d(&mw13, true, w13, Dm, Fu, 2 * Wu, Dm * 2, Fu * Dm * 2, 64, 128, 1, "w13")) != DG_OK) return st;
+  if ((st = make_map_3d(&mh, true, ws, Fu, Wu, R, Fu * 2, FF * 2, 64, 1, 32, "h")) != DG_OK) return st;
+  GemmParams p{};
+  p.G = W;
+  p.M = static_cast<int32_t>(R);
+  p.N = static_cast<int32_t>(F);
+  p.K = static_cast<int32_t>(d);
+  p.a_g = G_NONE;
+  p.b_g = G_OUTER;  // unused: the paired load addresses w13 directly
+  p.d_g = G_MID;
+  if ((st = run_gemm(GV_BF16_KK_SWIGLU, mx, mw13, mh, mh, p, dev, s, "tp_gemm1_swiglu",
+                     2.0 * (static_cast<double>(R) * Dm + 2.0 * FF * Dm + static_cast<double>(R) * FF))) != DG_OK)
+    return st;
+
+  // GEMM2: y = sum_s h_s @ w2_s^T = h @ w2^T; the shard sum is the K loop.
+  CUtensorMap mh_k, mw2, my;
+  if ((st = make_map_3d(&mh_k, true, ws, FF, R, 1, FF * 2, R * FF * 2, 64, 128, 1, "h (A)")) != DG_OK) return st;
+  if ((st = make_map_3d(&mw2, true, w2, FF, Dm, 1, FF * 2, Dm * FF * 2, 64, 256, 1, "w2")) != DG_OK) return st;
+  if ((st = make_map_3d(&my, true, y_shards, Dm, R, 1, Dm * 2, R * Dm * 2, 64, 32, 1, "y_shards")) != DG_OK) return st;
+  p = GemmParams{};
+  p.G = 1;
+  p.M = static_cast<int32_t>(R);
+  p.N = static_cast<int32_t>(d);
+  p.K = static_cast<int32_t>(ffn);
+  p.a_g = G_OUTER;
+  p.b_g = G_OUTER;
+  p.d_g = G_OUTER;
+  return run_gemm(GV_BF16_KK_STORE, mh_k, mw2, my, my, p, dev, s, "tp_gemm2",
+                  2.0 * (static_cast<double>(R) * FF + static_cast<double>(Dm) * FF + static_cast<double>(R) * Dm));
+}
+
+dg_status dg_trace_begin(void) {
+  std::lock_guard<std::mutex> g(g_trace_mu);
+  g_tracing = true;
+  return DG_OK;
+}
+
+int32_t dg_trace_end(dg_trace_entry* out, int32_t max_entries) {
+  std::vector<TraceRecord> recs;
+  {
+    std::lock_guard<std::mutex> g(g_trace_mu);
+    g_tracing = false;
+    recs.swap(g_trace);
+  }
+  std::vector<dg_trace_entry> agg;
+  bool ok = true;
+  for (const TraceRecord& r : recs) {
+    float ms = 0.0f;
+    if (cudaEventSynchronize(r.e1) != cudaSuccess || cudaEventElapsedTime(&ms, r.e0, r.e1) != cudaSuccess) ok = false;
+    cudaEventDestroy(r.e0);
+    cudaEventDestroy(r.e1);
+    size_t i = 0;
+    while (i < agg.size() && strncmp(agg[i].name, r.name, sizeof(agg[i].name)) != 0) ++i;
+    if (i == agg.size()) {
+      dg_trace_entry e{};
+      strncpy(e.name, r.name, sizeof(e.name) - 1);
+      agg.push_back(e);
+    }
+    agg[i].launches += 1;
+    agg[i].total_ms += ms;
+    agg[i].flops += r.flops;
+    agg[i].bytes += r.bytes;
+  }
+  if (!ok) {
+    fail(DG_ERR_CUDA, "dg_trace_end: event timing failed");
+    return -1;
+  }
+  const int32_t n = static_cast<int32_t>(agg.size());
+  for (int32_t i = 0; i < n && i < max_entries; ++i) out[i] = agg[i];
+  return n;
+}
+
+}  // extern "C"

@@ -1,0 +1,435 @@
+// Persistent, warp-specialised tcgen05 GEMM for sm_103a.
+//
+// One CTA per SM walks a static tile schedule.  Per CTA:
+//   warp 0   TMA producer: fills a STAGES-deep ring of (A, B) K-blocks in
+//            shared memory, 128-byte swizzled, signalling `full[s]`.
+//   warp 1   allocates TMEM (two 128 x BN fp32 accumulators) and one lane
+//            issues tcgen05.mma for every K-block, releasing smem stages
+//            through tcgen05.commit -> `empty[s]` and handing a finished
+//            accumulator to the epilogue through `tfull[a]`.
+//   warps 2-5 epilogue: tcgen05.ld the accumulator (32 rows per warp),
+//            apply the fused epilogue, round to bf16, write 32x64 sub-tiles
+//            into swizzled staging buffers and TMA-store them.  The two
+//            accumulators let the epilogue of tile i overlap the mainloop
+//            of tile i+1.
+//
+// Operands are described by 3-D TMA tensor maps whose coordinates are
+// (x, y, g) or (x, g, y): x is the contiguous dimension, y the other matrix
+// dimension and g the problem ("group") index.  A problem whose rows are
+// strided through a larger tensor -- the dispatched rows of the A2A layer --
+// is therefore just another tensor map: the exchange costs no data movement.
+//
+// Operand majorness: K-major tiles are [rows][64 bf16 | 128 e4m3] (one
+// 128-byte swizzle row per tile row); MN-major tiles are [64 k-rows][64 mn]
+// boxes stacked along MN.  The UMMA smem descriptors below encode those two
+// canonical layouts.
+#pragma once
+
+#include "dg_ptx.cuh"
+
+namespace dg {
+
+enum GMode : int32_t { G_OUTER = 0, G_MID = 1, G_NONE = 2 };
+enum Epi : int32_t { EPI_STORE = 0, EPI_BIAS = 1, EPI_FP8 = 2, EPI_SWIGLU = 3 };
+
+// Wait-site codes recorded with a timeout.
+enum WaitSite : uint32_t {
+  SITE_EMPTY = 1, SITE_FULL = 2, SITE_TEMPTY = 3, SITE_TFULL = 4, SITE_CLOAD = 5, SITE_DRAIN = 6
+};
+
+struct GemmParams {
+  int32_t G, M, N, K;        // problems; rows, output columns, contraction of each problem
+  int32_t tiles_m, tiles_n;  // tiles per problem
+  int32_t a_g, b_g, d_g;     // GMode of the group coordinate of A, B and D (C follows D)
+  const __nv_bfloat16* bias; // EPI_BIAS: bias[g * bias_g_stride + n]
+  int64_t bias_g_stride;
+  float alpha, beta;         // EPI_FP8
+  int32_t has_c;             // EPI_FP8: read C
+  uint32_t* err;             // device error word
+};
+
+template <bool kFp8, bool kAMN, bool kBMN, int kEpi>
+struct GemmCfg {
+  static constexpr int BM = 128;                      // UMMA M (one TMEM lane per row)
+  static constexpr int BN = 256;                      // UMMA N = accumulator columns
+  static constexpr int BN_OUT = (kEpi == EPI_SWIGLU) ? BN / 2 : BN;
+  static constexpr int ROW_BYTES = 128;               // K-block = one 128-byte swizzle row
+  static constexpr int BK = kFp8 ? 128 : 64;          // K elements per stage
+  static constexpr int K_STEPS = 4;                   // UMMA K = 32 bytes: 16 bf16 / 32 e4m3
+  static constexpr int STAGES = 4;
+  static constexpr int A_BYTES = BM * ROW_BYTES;      // 16 KB
+  static constexpr int B_BYTES = BN * ROW_BYTES;      // 32 KB
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int MN_BOX_BYTES = 64 * 64 * 2;    // MN-major box: 64 k-rows x 64 bf16
+  static constexpr int EPI_WARPS = 4;
+  static constexpr int EPI_BUF_BYTES = 32 * 128;      // 32 rows x 64 bf16
+  static constexpr int EPI_BYTES = EPI_WARPS * 2 * EPI_BUF_BYTES;
+  static constexpr int NUM_THREADS = 64 + EPI_WARPS * 32;
+  static constexpr uint32_t TMEM_COLS = 2 * BN;
+  static constexpr int NUM_BARS = 2 * STAGES + 4 + 2 * EPI_WARPS + 1;
+  static constexpr int BAR_BYTES = 256;
+  static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + EPI_BYTES + BAR_BYTES;
+  static constexpr uint32_t IDESC = umma_idesc(kFp8 ? 0u : 1u, kAMN, kBMN, BN, BM);
+  static_assert(NUM_BARS * 8 + 4 <= BAR_BYTES, "barrier area");
+  static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+  static_assert(!(kFp8 && (kAMN || kBMN)), "e4m3 operands are K-major here");
+};
+
+static __device__ __forceinline__ void tma_load_op(void* dst, const CUtensorMap* map, uint64_t* bar, int32_t x,
+                                                   int32_t y, int32_t g, int32_t mode) {
+  if (mode == G_MID) {
+    tma_load_3d(dst, map, bar, x, g, y);
+  } else if (mode == G_OUTER) {
+    tma_load_3d(dst, map, bar, x, y, g);
+  } else {
+    tma_load_3d(dst, map, bar, x, y, 0);
+  }
+}
+
+static __device__ __forceinline__ void tma_store_op(const CUtensorMap* map, const void* src, int32_t x, int32_t y,
+                                                    int32_t g, int32_t mode) {
+  if (mode == G_MID) {
+    tma_store_3d(map, src, x, g, y);
+  } else if (mode == G_OUTER) {
+    tma_store_3d(map, src, x, y, g);
+  } else {
+    tma_store_3d(map, src, x, y, 0);
+  }
+}
+
+static __device__ __forceinline__ float silu_f(float x) { return x / (1.0f + __expf(-x)); }
+
+template <bool kFp8, bool kAMN, bool kBMN, int kEpi>
+__global__ void __launch_bounds__(GemmCfg<kFp8, kAMN, kBMN, kEpi>::NUM_THREADS, 1)
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const __grid_constant__ CUtensorMap tmD, const __grid_constant__ CUtensorMap tmC,
+                   const GemmParams p) {
+  using Cfg = GemmCfg<kFp8, kAMN, kBMN, kEpi>;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ uint32_t s_abort;
+
+  const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
+  uint8_t* smem = smem_raw + pad;
+  uint8_t* stage_base = smem;
+  uint8_t* epi_base = smem + Cfg::STAGES * Cfg::STAGE_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(epi_base + Cfg::EPI_BYTES);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + Cfg::STAGES;
+  uint64_t* tfull = bars + 2 * Cfg::STAGES;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* cbar = tempty + 2;
+  uint64_t* drain = cbar + 2 * Cfg::EPI_WARPS;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  // A sticky device error from an earlier failure: do nothing.
+  if (threadIdx.x == 0) s_abort = ld_volatile_u32(p.err);
+  __syncthreads();
+  if (s_abort != 0u) return;
+
+  if (warp == 0 && lane == 0) {
+    for (int s = 0; s < Cfg::STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], Cfg::EPI_WARPS);
+    }
+    for (int i = 0; i < 2 * Cfg::EPI_WARPS; ++i) mbar_init(&cbar[i], 1);
+    mbar_init(drain, 1);
+    fence_mbar_init();
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+    tma_prefetch_desc(&tmD);
+    if (kEpi == EPI_FP8 && p.has_c) tma_prefetch_desc(&tmC);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_holder, Cfg::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem_base = *tmem_holder;
+
+  const int tiles_per_group = p.tiles_m * p.tiles_n;
+  const int total_tiles = p.G * tiles_per_group;
+  const int num_kb = (p.K + Cfg::BK - 1) / Cfg::BK;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t armed = 0, armed_parity = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x) {
+        const int g = tile / tiles_per_group;
+        const int rem = tile - g * tiles_per_group;
+        const int m0 = (rem % p.tiles_m) * Cfg::BM;
+        const int n0 = (rem / p.tiles_m) * Cfg::BN_OUT;
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!mbar_wait(&empty[stage], phase ^ 1u, p.err, SITE_EMPTY)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&full[stage], Cfg::STAGE_BYTES);
+          uint8_t* sa = stage_base + stage * Cfg::STAGE_BYTES;
+          uint8_t* sb = sa + Cfg::A_BYTES;
+          const int k0 = kb * Cfg::BK;
+          if (!kAMN) {
+            tma_load_op(sa, &tmA, &full[stage], k0, m0, g, p.a_g);
+          } else {
+#pragma unroll
+            for (int i = 0; i < Cfg::BM / 64; ++i)
+              tma_load_op(sa + i * Cfg::MN_BOX_BYTES, &tmA, &full[stage], m0 + 64 * i, k0, g, p.a_g);
+          }
+          if (kEpi == EPI_SWIGLU) {
+            // rows [c0, c0+BN/2) of w1_g, then the same rows of w3_g
+            tma_load_3d(sb, &tmB, &full[stage], k0, n0, 2 * g);
+            tma_load_3d(sb + (Cfg::BN / 2) * Cfg::ROW_BYTES, &tmB, &full[stage], k0, n0, 2 * g + 1);
+          } else if (!kBMN) {
+            tma_load_op(sb, &tmB, &full[stage], k0, n0, g, p.b_g);
+          } else {
+#pragma unroll
+            for (int i = 0; i < Cfg::BN / 64; ++i)
+              tma_load_op(sb + i * Cfg::MN_BOX_BYTES, &tmB, &full[stage], n0 + 64 * i, k0, g, p.b_g);
+          }
+          armed |= 1u << stage;
+          armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
+          if (++stage == Cfg::STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      // Every load this thread issued must land before the CTA exits.
+      for (int s = 0; s < Cfg::STAGES; ++s)
+        if (armed & (1u << s)) {
+          if (!mbar_try_wait(&full[s], (armed_parity >> s) & 1u)) {
+            uint32_t dummy = 0;
+            mbar_wait_slow(&full[s], (armed_parity >> s) & 1u, &dummy, SITE_DRAIN, kWaitLimitNs);
+          }
+        }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0, tphase = 0;
+      bool ok = true;
+      int local = 0;
+      for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x, ++local) {
+        const int acc = local & 1;
+        if (!mbar_wait(&tempty[acc], ((tphase >> acc) & 1u) ^ 1u, p.err, SITE_TEMPTY)) {
+          ok = false;
+          break;
+        }
+        tphase ^= 1u << acc;
+        tc_fence_after_sync();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * Cfg::BN);
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!mbar_wait(&full[stage], phase, p.err, SITE_FULL)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          const uint32_t sa = smem_u32(stage_base + stage * Cfg::STAGE_BYTES);
+          const uint32_t sb = sa + Cfg::A_BYTES;
+#pragma unroll
+          for (int j = 0; j < Cfg::K_STEPS; ++j) {
+            // K-major: advance 32 bytes inside the swizzle row; 8-row groups 1024 B apart.
+            // MN-major: advance 16 k-rows (2048 B); 8-k-row groups 1024 B apart,
+            //           64-wide MN boxes MN_BOX_BYTES apart.
+            const uint64_t ad = kAMN ? smem_desc_sw128(sa + j * 2048, Cfg::MN_BOX_BYTES, 1024)
+                                     : smem_desc_sw128(sa + j * 32, 16, 1024);
+            const uint64_t bd = kBMN ? smem_desc_sw128(sb + j * 2048, Cfg::MN_BOX_BYTES, 1024)
+                                     : smem_desc_sw128(sb + j * 32, 16, 1024);
+            const uint32_t accum = (kb > 0 || j > 0) ? 1u : 0u;
+            if (kFp8)
+              umma_f8(d_tmem, ad, bd, Cfg::IDESC, accum);
+            else
+              umma_bf16(d_tmem, ad, bd, Cfg::IDESC, accum);
+          }
+          tc_commit(&empty[stage]);
+          if (++stage == Cfg::STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        tc_commit(&tfull[acc]);
+      }
+      // Every MMA this thread issued must complete before TMEM is released.
+      tc_commit(drain);
+      if (!mbar_try_wait(drain, 0)) {
+        uint32_t dummy = 0;
+        mbar_wait_slow(drain, 0, &dummy, SITE_DRAIN, kWaitLimitNs);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int ew = warp - 2;  // staging-buffer owner index
+    const int lg = warp & 3;  // TMEM lane quarter this warp may access
+    uint8_t* stg = epi_base + ew * 2 * Cfg::EPI_BUF_BYTES;
+    uint64_t* my_cbar = cbar + 2 * ew;
+    const bool use_c = (kEpi == EPI_FP8) && (p.has_c != 0);
+    uint32_t tphase = 0, cphase = 0, chunk_ctr = 0;
+    int c_pending = -1;  // staging buffer with a C load in flight
+    uint32_t c_pending_parity = 0;
+    bool ok = true;
+    const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(32 * lg) << 16);
+    int local = 0;
+    for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x, ++local) {
+      const int g = tile / tiles_per_group;
+      const int rem = tile - g * tiles_per_group;
+      const int m0 = (rem % p.tiles_m) * Cfg::BM;
+      const int n0 = (rem / p.tiles_m) * Cfg::BN_OUT;
+      const int acc = local & 1;
+      const int row0 = m0 + 32 * lg;
+      int nchunks = (p.N - n0 + 63) / 64;
+      if (nchunks > Cfg::BN_OUT / 64) nchunks = Cfg::BN_OUT / 64;
+      if (row0 >= p.M) nchunks = 0;
+
+      auto issue_c = [&](int j, int buf) {
+        if (lane == 0) {
+          bulk_wait_group_read<0>();
+          mbar_arrive_expect_tx(&my_cbar[buf], Cfg::EPI_BUF_BYTES);
+          tma_load_op(stg + buf * Cfg::EPI_BUF_BYTES, &tmC, &my_cbar[buf], n0 + 64 * j, row0, g, p.d_g);
+        }
+        c_pending = buf;
+        c_pending_parity = (cphase >> buf) & 1u;
+        __syncwarp();
+      };
+
+      if (use_c && nchunks > 0) issue_c(0, static_cast<int>(chunk_ctr & 1u));
+
+      if (!mbar_wait(&tfull[acc], (tphase >> acc) & 1u, p.err, SITE_TFULL)) {
+        ok = false;
+        break;
+      }
+      tphase ^= 1u << acc;
+      tc_fence_after_sync();
+
+      for (int j = 0; j < nchunks; ++j) {
+        const int buf = static_cast<int>((chunk_ctr + j) & 1u);
+        if (use_c && j + 1 < nchunks) issue_c(j + 1, buf ^ 1);
+
+        float v[64];
+        if (kEpi == EPI_SWIGLU) {
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            uint32_t ra[32], rb[32];
+            const uint32_t col = static_cast<uint32_t>(acc * Cfg::BN + 64 * j + 32 * h);
+            tmem_ld_32x32b_x32(lane_addr + col, ra);
+            tmem_ld_32x32b_x32(lane_addr + col + Cfg::BN / 2, rb);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              v[32 * h + i] = silu_f(__uint_as_float(ra[i])) * __uint_as_float(rb[i]);
+          }
+        } else {
+          uint32_t r0[32], r1[32];
+          const uint32_t col = static_cast<uint32_t>(acc * Cfg::BN + 64 * j);
+          tmem_ld_32x32b_x32(lane_addr + col, r0);
+          tmem_ld_32x32b_x32(lane_addr + col + 32, r1);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            v[i] = __uint_as_float(r0[i]);
+            v[32 + i] = __uint_as_float(r1[i]);
+          }
+        }
+        if (num_kb == 0) {
+#pragma unroll
+          for (int i = 0; i < 64; ++i) v[i] = 0.0f;
+        }
+
+        uint8_t* sbuf = stg + buf * Cfg::EPI_BUF_BYTES;
+        if (use_c) {
+          if (!mbar_wait(&my_cbar[buf], (cphase >> buf) & 1u, p.err, SITE_CLOAD)) {
+            ok = false;
+            break;
+          }
+          cphase ^= 1u << buf;
+          if (c_pending == buf) c_pending = -1;
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            const uint4 cv =
+                *reinterpret_cast<const uint4*>(sbuf + lane * 128 + ((q ^ (lane & 7)) << 4));
+            const uint32_t cw[4] = {cv.x, cv.y, cv.z, cv.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float2 c2 = unpack_bf16x2(cw[e]);
+              v[8 * q + 2 * e] = p.alpha * v[8 * q + 2 * e] + p.beta * c2.x;
+              v[8 * q + 2 * e + 1] = p.alpha * v[8 * q + 2 * e + 1] + p.beta * c2.y;
+            }
+          }
+        } else {
+          if (kEpi == EPI_FP8) {
+#pragma unroll
+            for (int i = 0; i < 64; ++i) v[i] *= p.alpha;
+          }
+          if (kEpi == EPI_BIAS) {
+            const __nv_bfloat16* bp = p.bias + static_cast<int64_t>(g) * p.bias_g_stride + n0 + 64 * j;
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+              if (n0 + 64 * j + 8 * q < p.N) {
+                const uint4 bv = __ldg(reinterpret_cast<const uint4*>(bp + 8 * q));
+                const uint32_t bw[4] = {bv.x, bv.y, bv.z, bv.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                  const float2 b2 = unpack_bf16x2(bw[e]);
+                  v[8 * q + 2 * e] += b2.x;
+                  v[8 * q + 2 * e + 1] += b2.y;
+                }
+              }
+            }
+          }
+          // the store that last read this buffer (two chunks ago) must be done
+          if (lane == 0) bulk_wait_group_read<1>();
+          __syncwarp();
+        }
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          uint4 o;
+          o.x = pack_bf16x2(v[8 * q + 0], v[8 * q + 1]);
+          o.y = pack_bf16x2(v[8 * q + 2], v[8 * q + 3]);
+          o.z = pack_bf16x2(v[8 * q + 4], v[8 * q + 5]);
+          o.w = pack_bf16x2(v[8 * q + 6], v[8 * q + 7]);
+          *reinterpret_cast<uint4*>(sbuf + lane * 128 + ((q ^ (lane & 7)) << 4)) = o;
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_op(&tmD, sbuf, n0 + 64 * j, row0, g, p.d_g);
+          bulk_commit_group();
+        }
+      }
+      if (!ok) break;
+      chunk_ctr += static_cast<uint32_t>(nchunks);
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty[acc]);
+    }
+    // Outstanding copies of this warp must finish before the CTA exits.
+    if (lane == 0) bulk_wait_group<0>();
+    if (c_pending >= 0 && !mbar_try_wait(&my_cbar[c_pending], c_pending_parity)) {
+      uint32_t dummy = 0;
+      mbar_wait_slow(&my_cbar[c_pending], c_pending_parity, &dummy, SITE_DRAIN, kWaitLimitNs);
+    }
+    __syncwarp();
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
+  }
+}
+
+}  // namespace dg

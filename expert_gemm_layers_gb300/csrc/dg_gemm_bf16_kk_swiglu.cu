@@ -1,0 +1,11 @@
+// Instantiation unit of the tcgen05 GEMM: bf16 A and B K-major, paired silu(a)*b epilogue.
+#include "dg_internal.h"
+
+namespace dg {
+
+cudaError_t launch_gemm_bf16_kk_swiglu(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& d,
+                                       const CUtensorMap& c, const GemmParams& p, int grid, cudaStream_t s) {
+  return launch_gemm_t<false, false, false, EPI_SWIGLU>(a, b, d, c, p, grid, s);
+}
+
+}  // namespace dg

@@ -1,0 +1,11 @@
+// Instantiation unit of the tcgen05 GEMM: e4m3 A and B K-major, D = alpha*acc + beta*C.
+#include "dg_internal.h"
+
+namespace dg {
+
+cudaError_t launch_gemm_fp8_kk(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& d,
+                               const CUtensorMap& c, const GemmParams& p, int grid, cudaStream_t s) {
+  return launch_gemm_t<true, false, false, EPI_FP8>(a, b, d, c, p, grid, s);
+}
+
+}  // namespace dg

@@ -1,0 +1,122 @@
+// Host-side internals shared by the translation units of libdg.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/dg.h"
+#include "dg_gemm.cuh"
+
+namespace dg {
+
+// Records a thread-local message and returns `s`.
+dg_status fail(dg_status s, const char* fmt, ...);
+
+// Per-device facts, cached on first use of each device.
+struct DeviceInfo {
+  int device;
+  int num_sms;
+  uint32_t* err;  // device address of this device's error word
+};
+dg_status device_info(DeviceInfo* out);
+
+// A 3-D TMA tensor map over a row-major tensor.  dims are in elements,
+// innermost first; strides (bytes) are those of dims 1 and 2; box in
+// elements.  Swizzle is 128 B, out-of-bounds elements read as zero.
+dg_status make_map_3d(CUtensorMap* map, bool is_bf16, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
+                      uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t b0, uint32_t b1, uint32_t b2,
+                      const char* what);
+
+enum GemmVariant : int {
+  GV_FP8_KK = 0,        // e4m3, A and B K-major, alpha/beta/C epilogue
+  GV_BF16_KK_STORE = 1, // bf16, A and B K-major, plain store
+  GV_BF16_KM_BIAS = 2,  // bf16, A K-major, B MN-major, bias epilogue
+  GV_BF16_MM_STORE = 3, // bf16, A and B MN-major, plain store
+  GV_BF16_KK_SWIGLU = 4 // bf16, A and B K-major, paired silu(a)*b epilogue
+};
+
+// Tiles along N of one problem for this variant (output columns per tile).
+int gemm_tile_n(GemmVariant v);
+int gemm_tile_m();
+
+// Enqueue one persistent GEMM launch.  `p.tiles_*` and the grid are filled in
+// here.  `name` and `bytes` (algorithmic HBM bytes) label the launch for tracing.
+dg_status run_gemm(GemmVariant v, const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& d,
+                   const CUtensorMap& c, GemmParams p, const DeviceInfo& dev, cudaStream_t s, const char* name,
+                   double bytes);
+
+// Brackets one kernel launch with CUDA events while tracing is on (dg_trace_begin).
+class TraceScope {
+ public:
+  TraceScope(const char* name, cudaStream_t s, double flops, double bytes);
+  ~TraceScope();
+  TraceScope(const TraceScope&) = delete;
+  TraceScope& operator=(const TraceScope&) = delete;
+
+ private:
+  bool active_ = false;
+  cudaStream_t stream_;
+  const char* name_;
+  double flops_, bytes_;
+  cudaEvent_t e0_{}, e1_{};
+};
+
+// Launchers, one per translation unit.
+cudaError_t launch_gemm_fp8_kk(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
+                               const GemmParams&, int grid, cudaStream_t);
+cudaError_t launch_gemm_bf16_kk_store(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
+                                      const CUtensorMap&, const GemmParams&, int grid, cudaStream_t);
+cudaError_t launch_gemm_bf16_km_bias(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
+                                     const CUtensorMap&, const GemmParams&, int grid, cudaStream_t);
+cudaError_t launch_gemm_bf16_mm_store(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
+                                      const CUtensorMap&, const GemmParams&, int grid, cudaStream_t);
+cudaError_t launch_gemm_bf16_kk_swiglu(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
+                                       const CUtensorMap&, const GemmParams&, int grid, cudaStream_t);
+
+// Host launcher body shared by the instantiation units.
+template <bool kFp8, bool kAMN, bool kBMN, int kEpi>
+cudaError_t launch_gemm_t(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& d, const CUtensorMap& c,
+                          const GemmParams& p, int grid, cudaStream_t s) {
+  using Cfg = GemmCfg<kFp8, kAMN, kBMN, kEpi>;
+  auto kern = gemm_tc_kernel<kFp8, kAMN, kBMN, kEpi>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  kern<<<grid, Cfg::NUM_THREADS, Cfg::SMEM_BYTES, s>>>(a, b, d, c, p);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------- row kernels (dg_rowops.cu)
+
+// LayerNorm-and-gate forward over rows of Z [rows, 2H]: Hl [rows, H], stats [rows] (mu_u, rstd_u, mu_g, rstd_g).
+cudaError_t launch_ln_gate_fwd(const void* Z, const void* nx_w, const void* nx_b, const void* ng_w,
+                               const void* ng_b, void* Hl, void* stats, int64_t rows, int M, int L, int H,
+                               float eps, const DeviceInfo& dev, cudaStream_t s);
+
+// Backward of the gate and both LayerNorms: dZ [rows, 2H] and per-(t, chunk)
+// column partials part [T, nchunk, 6, H] (dU, dG, da*xu, da, ds*xg, ds).
+cudaError_t launch_ln_gate_bwd(const void* Z, const void* stats, const void* dHl, const void* nx_w,
+                               const void* nx_b, const void* ng_w, const void* ng_b, void* dZ, float* part,
+                               int T, int M, int L, int H, int nchunk, const DeviceInfo& dev, cudaStream_t s);
+
+// db1 [T, 2H] and the norm gradients [P, H] from the partials, in a fixed order.
+cudaError_t launch_reduce_partials(const float* part, void* d_b1, void* d_nx_w, void* d_nx_b, void* d_ng_w,
+                                   void* d_ng_b, int P, int L, int H, int nchunk, const DeviceInfo& dev,
+                                   cudaStream_t s);
+
+// out[g, c] = sum_n src[g*g_stride + n*row_stride + c] (bf16 in, fp32 sum, bf16 out [G, ncols]).
+cudaError_t launch_column_sum(const void* src, void* out, int G, int rows, int ncols, int64_t g_stride,
+                              int64_t row_stride, const DeviceInfo& dev, cudaStream_t s);
+
+// Row permutations of the exchange (16-byte vector copies).
+cudaError_t launch_dispatch(const void* in, void* out, int P, int B, int T, int D, const DeviceInfo& dev,
+                            cudaStream_t s);
+cudaError_t launch_combine(const void* in, void* out, int P, int B, int T, int D, const DeviceInfo& dev,
+                           cudaStream_t s);
+
+cudaError_t launch_debug_wait(uint32_t* err, uint64_t limit_ns, cudaStream_t s);
+
+// Number of row chunks per token position used by the backward partials.
+int ffn_bwd_chunks(int T, int M);
+
+}  // namespace dg

@@ -1,0 +1,248 @@
+"""Torch-facing wrappers of the libdg entry points.
+
+Each function checks dtypes/devices, allocates outputs and scratch with
+torch (device memory only) and passes raw pointers plus the current CUDA
+stream to the C ABI.  No arithmetic of the layers happens here.
+"""
+from __future__ import annotations
+
+import ctypes
+
+import torch
+
+from ._lib import FFNShape, TraceEntry, check, load
+
+__all__ = [
+    "gemm_fp8", "ffn_shape", "a2a_ffn_forward", "a2a_ffn_backward", "A2AFFN", "a2a_ffn",
+    "a2a_dispatch", "a2a_combine", "tp_swiglu", "device_status", "debug_wait_timeout",
+    "FFN_PARAM_NAMES", "trace_begin", "trace_end",
+]
+
+FFN_PARAM_NAMES = ("w1", "b1", "wout", "bout", "nx_w", "nx_b", "ng_w", "ng_b")
+
+
+def _stream(dev: torch.device) -> int:
+    return torch.cuda.current_stream(dev).cuda_stream
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _need(t: torch.Tensor, name: str, dtype: torch.dtype, shape=None, device=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be on a CUDA device")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+
+
+# ------------------------------------------------------------------ FP8 GEMM
+
+def gemm_fp8(A: torch.Tensor, B: torch.Tensor, C: torch.Tensor | None = None, alpha: float = 1.0,
+             beta: float = 0.0, out: torch.Tensor | None = None) -> torch.Tensor:
+    """D = alpha * (A @ B^T) + beta * C with A [M,K], B [N,K] in float8_e4m3fn, C/D bf16 [M,N]."""
+    lib = load()
+    M, K = A.shape
+    N = B.shape[0]
+    _need(A, "A", torch.float8_e4m3fn, (M, K))
+    _need(B, "B", torch.float8_e4m3fn, (N, K), A.device)
+    if C is not None:
+        _need(C, "C", torch.bfloat16, (M, N), A.device)
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=A.device)
+    _need(out, "out", torch.bfloat16, (M, N), A.device)
+    with torch.cuda.device(A.device):
+        check(lib.dg_gemm_fp8(M, N, K, _ptr(A), _ptr(B), _ptr(C), _ptr(out), float(alpha), float(beta),
+                              ctypes.c_void_p(_stream(A.device))))
+    return out
+
+
+# ------------------------------------------------------------------ A2A FFN
+
+def ffn_shape(P: int, B: int, T: int, D: int, k: int, eps: float = 1e-5) -> FFNShape:
+    return FFNShape(P, B, T, D, k, eps)
+
+
+def _ffn_param_shapes(P, B, T, D, k):
+    H, L = D * k, T // P
+    return dict(inputs=(P, B, T, D), w1=(P, L, D, 2 * H), b1=(P, L, 2 * H), wout=(P, L, H, D),
+                bout=(P, L, D), nx_w=(P, H), nx_b=(P, H), ng_w=(P, H), ng_b=(P, H))
+
+
+def a2a_ffn_forward(inputs: torch.Tensor, params: dict, eps: float = 1e-5, saved: torch.Tensor | None = None,
+                    out: torch.Tensor | None = None):
+    """The A2A FFN layer for all P ranks at once.
+
+    inputs [P,B,T,D] bf16; params: w1 [P,L,D,2H], b1 [P,L,2H], wout [P,L,H,D],
+    bout [P,L,D], nx_w/nx_b/ng_w/ng_b [P,H] (bf16), where k = 2H/(2D) is read
+    from w1.  Returns (output [P,B,T,D], saved) where `saved` is the opaque
+    byte buffer the backward needs.
+    """
+    lib = load()
+    P, B, T, D = inputs.shape
+    k = params["w1"].shape[-1] // (2 * D)
+    shapes = _ffn_param_shapes(P, B, T, D, k)
+    dev = inputs.device
+    _need(inputs, "inputs", torch.bfloat16, shapes["inputs"])
+    for name in FFN_PARAM_NAMES:
+        _need(params[name], name, torch.bfloat16, shapes[name], dev)
+    sh = FFNShape(P, B, T, D, k, eps)
+    nbytes = lib.dg_a2a_ffn_saved_bytes(ctypes.byref(sh))
+    if nbytes == 0:
+        check(lib.dg_a2a_ffn_fwd(ctypes.byref(sh), *([None] * 10), None, 0, None))
+    if saved is None:
+        saved = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    if out is None:
+        out = torch.empty(shapes["inputs"], dtype=torch.bfloat16, device=dev)
+    _need(out, "out", torch.bfloat16, shapes["inputs"], dev)
+    with torch.cuda.device(dev):
+        check(lib.dg_a2a_ffn_fwd(ctypes.byref(sh), _ptr(inputs), *[_ptr(params[n]) for n in FFN_PARAM_NAMES],
+                                 _ptr(out), _ptr(saved), saved.numel(), ctypes.c_void_p(_stream(dev))))
+    return out, saved
+
+
+def a2a_ffn_backward(inputs: torch.Tensor, params: dict, saved: torch.Tensor, dY: torch.Tensor,
+                     eps: float = 1e-5, workspace: torch.Tensor | None = None, grads: dict | None = None) -> dict:
+    """Gradients of the layer w.r.t. inputs and every parameter (overwritten, bf16).
+
+    Returns a dict with keys "inputs" and the names in FFN_PARAM_NAMES.
+    """
+    lib = load()
+    P, B, T, D = inputs.shape
+    k = params["w1"].shape[-1] // (2 * D)
+    shapes = _ffn_param_shapes(P, B, T, D, k)
+    dev = inputs.device
+    _need(dY, "dY", torch.bfloat16, shapes["inputs"], dev)
+    sh = FFNShape(P, B, T, D, k, eps)
+    wsb = lib.dg_a2a_ffn_bwd_workspace_bytes(ctypes.byref(sh))
+    if workspace is None:
+        workspace = torch.empty(max(wsb, 1), dtype=torch.uint8, device=dev)
+    if grads is None:
+        grads = {name: torch.empty(shapes[name], dtype=torch.bfloat16, device=dev)
+                 for name in ("inputs",) + FFN_PARAM_NAMES}
+    g = grads
+    with torch.cuda.device(dev):
+        check(lib.dg_a2a_ffn_bwd(
+            ctypes.byref(sh), _ptr(inputs), *[_ptr(params[n]) for n in FFN_PARAM_NAMES],
+            _ptr(saved), saved.numel(), _ptr(dY),
+            _ptr(g["inputs"]), _ptr(g["w1"]), _ptr(g["b1"]), _ptr(g["wout"]), _ptr(g["bout"]),
+            _ptr(g["nx_w"]), _ptr(g["nx_b"]), _ptr(g["ng_w"]), _ptr(g["ng_b"]),
+            _ptr(workspace), workspace.numel(), ctypes.c_void_p(_stream(dev))))
+    return grads
+
+
+class A2AFFN(torch.autograd.Function):
+    """Autograd wrapper: gradients reach the input and all eight parameters."""
+
+    @staticmethod
+    def forward(ctx, inputs, w1, b1, wout, bout, nx_w, nx_b, ng_w, ng_b, eps):
+        params = dict(w1=w1, b1=b1, wout=wout, bout=bout, nx_w=nx_w, nx_b=nx_b, ng_w=ng_w, ng_b=ng_b)
+        out, saved = a2a_ffn_forward(inputs, params, eps)
+        ctx.save_for_backward(inputs, w1, b1, wout, bout, nx_w, nx_b, ng_w, ng_b, saved)
+        ctx.eps = eps
+        return out
+
+    @staticmethod
+    def backward(ctx, dY):
+        inputs, w1, b1, wout, bout, nx_w, nx_b, ng_w, ng_b, saved = ctx.saved_tensors
+        params = dict(w1=w1, b1=b1, wout=wout, bout=bout, nx_w=nx_w, nx_b=nx_b, ng_w=ng_w, ng_b=ng_b)
+        g = a2a_ffn_backward(inputs, params, saved, dY.contiguous(), ctx.eps)
+        return (g["inputs"], g["w1"], g["b1"], g["wout"], g["bout"], g["nx_w"], g["nx_b"], g["ng_w"],
+                g["ng_b"], None)
+
+
+def a2a_ffn(inputs, params: dict, eps: float = 1e-5):
+    """Differentiable A2A FFN layer (see A2AFFN)."""
+    return A2AFFN.apply(inputs, *[params[n] for n in FFN_PARAM_NAMES], eps)
+
+
+def a2a_dispatch(inputs: torch.Tensor) -> torch.Tensor:
+    """inputs [P,B,T,D] -> dispatched [P, P*B, T/P, D] (explicit permutation copy)."""
+    lib = load()
+    P, B, T, D = inputs.shape
+    _need(inputs, "inputs", torch.bfloat16)
+    out = torch.empty((P, P * B, T // P, D), dtype=torch.bfloat16, device=inputs.device)
+    with torch.cuda.device(inputs.device):
+        check(lib.dg_a2a_dispatch(P, B, T, D, _ptr(inputs), _ptr(out), ctypes.c_void_p(_stream(inputs.device))))
+    return out
+
+
+def a2a_combine(ylocal: torch.Tensor, B: int) -> torch.Tensor:
+    """ylocal [P, P*B, L, D] -> output [P, B, P*L, D] (explicit permutation copy)."""
+    lib = load()
+    P, PB, L, D = ylocal.shape
+    _need(ylocal, "ylocal", torch.bfloat16)
+    out = torch.empty((P, B, P * L, D), dtype=torch.bfloat16, device=ylocal.device)
+    with torch.cuda.device(ylocal.device):
+        check(lib.dg_a2a_combine(P, B, P * L, D, _ptr(ylocal), _ptr(out), ctypes.c_void_p(_stream(ylocal.device))))
+    return out
+
+
+# ------------------------------------------------------------------ TP SwiGLU
+
+def tp_swiglu(x_shards: torch.Tensor, w13: torch.Tensor, w2: torch.Tensor,
+              workspace: torch.Tensor | None = None, out: torch.Tensor | None = None) -> torch.Tensor:
+    """SwiGLU pair over W shards: x_shards [W, bsz, S/W, d] (or [W, S/W, d]),
+    w13 [W, 2F, d] (rows [w1_s; w3_s]), w2 [d, W*F].  Returns y_shards like x_shards."""
+    lib = load()
+    squeeze = x_shards.dim() == 3
+    xs = x_shards.unsqueeze(1) if squeeze else x_shards
+    W, bsz, sl, d = xs.shape
+    ffn = w2.shape[1]
+    dev = x_shards.device
+    _need(x_shards, "x_shards", torch.bfloat16)
+    _need(w13, "w13", torch.bfloat16, (W, 2 * (ffn // W), d), dev)
+    _need(w2, "w2", torch.bfloat16, (d, ffn), dev)
+    S = W * sl
+    wsb = lib.dg_tp_swiglu_workspace_bytes(S, d, ffn, W, bsz)
+    if workspace is None:
+        workspace = torch.empty(max(wsb, 1), dtype=torch.uint8, device=dev)
+    if out is None:
+        out = torch.empty_like(x_shards)
+    with torch.cuda.device(dev):
+        check(lib.dg_tp_swiglu(S, d, ffn, W, bsz, _ptr(x_shards), _ptr(w13), _ptr(w2), _ptr(out),
+                               _ptr(workspace), workspace.numel(), ctypes.c_void_p(_stream(dev))))
+    return out
+
+
+# ------------------------------------------------------------------ diagnostics
+
+def device_status(device=None):
+    """Synchronise the current stream and read/clear the device error word: (status, raw code)."""
+    lib = load()
+    dev = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
+    site = ctypes.c_uint32(0)
+    with torch.cuda.device(dev):
+        st = lib.dg_device_status(ctypes.c_void_p(_stream(dev)), ctypes.byref(site))
+    return st, site.value
+
+
+def debug_wait_timeout(limit_us: int, device=None) -> None:
+    lib = load()
+    dev = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
+    with torch.cuda.device(dev):
+        check(lib.dg_debug_wait_timeout(int(limit_us), ctypes.c_void_p(_stream(dev))))
+
+
+def trace_begin() -> None:
+    """Start recording every libdg kernel launch with CUDA events."""
+    check(load().dg_trace_begin())
+
+
+def trace_end() -> list[dict]:
+    """Stop recording; per kernel name: launches, total_ms, flops, bytes (algorithmic)."""
+    lib = load()
+    buf = (TraceEntry * 64)()
+    n = lib.dg_trace_end(buf, 64)
+    if n < 0:
+        check(3)
+    return [dict(name=buf[i].name.decode(), launches=int(buf[i].launches), total_ms=buf[i].total_ms,
+                 flops=buf[i].flops, bytes=buf[i].bytes) for i in range(min(n, 64))]

@@ -1,0 +1,217 @@
+/*
+ * dg.h -- C ABI of libdg: the local compute of expert- and tensor-parallel
+ * linear layers on one GB300 (sm_103a).
+ *
+ * Every entry point takes plain pointers and sizes.  Conventions that hold
+ * for all of them:
+ *
+ *  - Tensors are caller-owned DEVICE memory, contiguous (row-major, last
+ *    dimension fastest) in the shapes written beside each argument, and
+ *    16-byte aligned.  bf16 means IEEE bfloat16 bit patterns (uint16),
+ *    e4m3 means OCP E4M3FN bit patterns (uint8, the element format of
+ *    cutlass::float_e4m3_t and torch.float8_e4m3fn).
+ *  - The library never allocates device memory.  Scratch space comes from
+ *    the caller through a (pointer, bytes) pair whose required size is given
+ *    by the matching *_bytes() query; too small a buffer is an error.
+ *  - Inputs are never written.  Outputs must not overlap inputs or scratch.
+ *  - Calls are asynchronous and stream-ordered on `stream` (a cudaStream_t,
+ *    NULL = legacy default stream): they return once the work is enqueued.
+ *  - Every call returns a dg_status.  On failure nothing is enqueued and
+ *    dg_last_error() names the offending argument (thread-local message).
+ *    There is no silent fallback: an unsupported case is an error.
+ *  - Device-side failures (a pipeline wait that exceeded its time limit) are
+ *    recorded in a per-device error word instead of trapping; once set, the
+ *    library's kernels return early without touching memory until
+ *    dg_device_status() reads and clears it.  Poll it after synchronising.
+ *  - Tensor cores accumulate in fp32; bf16 results are rounded to nearest
+ *    even once, at the end.
+ */
+#ifndef DG_H
+#define DG_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  DG_OK = 0,
+  DG_ERR_INVALID_ARGUMENT = 1, /* a size, pointer, alignment or overlap rule was broken */
+  DG_ERR_UNSUPPORTED = 2,      /* a valid request this build does not implement */
+  DG_ERR_CUDA = 3,             /* a CUDA runtime/driver call failed */
+  DG_ERR_TIMEOUT = 4,          /* a device-side wait exceeded its limit (see dg_device_status) */
+  DG_ERR_DEVICE_CHECK = 5,     /* a device-side consistency check failed */
+  DG_ERR_WORKSPACE = 6         /* the scratch buffer is missing or smaller than the query says */
+} dg_status;
+
+/* Thread-local description of the last failure on this thread ("" if none). */
+const char* dg_last_error(void);
+
+/* Library version string. */
+const char* dg_version(void);
+
+/*
+ * Synchronises `stream`, then reads and clears the current device's error
+ * word.  Returns DG_OK, DG_ERR_TIMEOUT (a bounded pipeline wait expired),
+ * DG_ERR_DEVICE_CHECK, or DG_ERR_CUDA.  When not DG_OK, *site (if non-NULL)
+ * receives the raw code, whose low byte names the wait that expired.
+ */
+dg_status dg_device_status(void* stream, uint32_t* site);
+
+/* ------------------------------------------------------------------------
+ * (a) FP8 GEMM   D = alpha * (A @ B^T) + beta * C
+ *
+ * Source: "Pytorch Op for blackwell distributed gemm" (pytorch-distributed-
+ * gemm README), sections "Usage" and "Limitations & Important Notes":
+ * A is [M,K], B is [N,K] row-major (the transpose of torch.matmul's second
+ * operand), C is the [M,N] bias term; elements are e4m3.
+ *
+ *   A      e4m3 [M, K]         K % 16 == 0 (TMA rows must be 16-byte multiples)
+ *   B      e4m3 [N, K]
+ *   C      bf16 [M, N]         may be NULL only when beta == 0; N % 8 == 0
+ *   D      bf16 [M, N]         output, D = bf16_rne(alpha*acc + beta*C),
+ *                              acc = sum_k A[m,k]*B[n,k] exact products, fp32 sum
+ *   M, N >= 0 (0 = nothing to do); K >= 0 (K == 0 gives D = beta*C).
+ * No scratch is needed.
+ * ------------------------------------------------------------------------ */
+dg_status dg_gemm_fp8(int64_t M, int64_t N, int64_t K,
+                      const void* A, const void* B, const void* C, void* D,
+                      float alpha, float beta, void* stream);
+
+/* ------------------------------------------------------------------------
+ * (b) All-to-all expert-parallel FFN layer, P logical ranks on one GPU.
+ *
+ * Source: the A2A-FFN project statement (problems/p04), sections
+ * "Interface, layout, and parameters" and "Computation and communication
+ * example".  With H = D*k, L = T/P and a token position t = r*L + l
+ * (rank r, slice l):
+ *   Xlocal[r][n, l] = inputs[s][b, t]            n = s*B + b   (dispatch)
+ *   Z  = Xlocal[r][:, l] @ w1[r][l] + b1[r][l]                 ([P*B, 2H])
+ *   U, G = Z[:, :H], Z[:, H:]
+ *   LN(z) = (z - mean z) / sqrt(mean((z - mean z)^2) + eps) * gamma + beta
+ *   Hl = LN_x(U) * silu(LN_gate(G))       (LN params: norm_x / norm_gate of rank r)
+ *   Ylocal[r][:, l] = Hl @ wout[r][l] + bout[r][l]
+ *   output[s][b, t] = Ylocal[r][n, l]                           (combine)
+ * The two exchanges are index maps folded into the TMA coordinates of the
+ * GEMMs: no data moves for them.
+ *
+ * Layouts (bf16, leading dimension = rank):
+ *   inputs, output, dY, d_inputs : [P, B, T, D]
+ *   w1 [P, L, D, 2H]   b1 [P, L, 2H]   wout [P, L, H, D]   bout [P, L, D]
+ *   nx_w, nx_b, ng_w, ng_b : [P, H]   (LayerNorm weight/bias for U and G)
+ * Requirements: T % P == 0, D % 8 == 0, P*B >= 1.
+ *
+ * `saved` (size dg_a2a_ffn_saved_bytes) is required: the forward writes Z,
+ * Hl and the per-row LayerNorm statistics there, and the backward reads
+ * them.  It is also the forward's only scratch.
+ * ------------------------------------------------------------------------ */
+typedef struct {
+  int32_t P, B, T, D, k;
+  float eps; /* LayerNorm epsilon, 1e-5 on the page */
+} dg_ffn_shape;
+
+size_t dg_a2a_ffn_saved_bytes(const dg_ffn_shape* shape);
+
+dg_status dg_a2a_ffn_fwd(const dg_ffn_shape* shape,
+                         const void* inputs, const void* w1, const void* b1,
+                         const void* wout, const void* bout,
+                         const void* nx_w, const void* nx_b,
+                         const void* ng_w, const void* ng_b,
+                         void* output, void* saved, size_t saved_bytes,
+                         void* stream);
+
+/*
+ * Backward of dg_a2a_ffn_fwd for the same shape and parameters, given the
+ * upstream gradient dY [P,B,T,D] and the `saved` buffer the forward filled.
+ * Gradient outputs are OVERWRITTEN (not accumulated), bf16, same layouts as
+ * the tensors they belong to; d_nx_* / d_ng_* of rank r sum over its rows
+ * and its L slices.  Scratch: `ws` of dg_a2a_ffn_bwd_workspace_bytes.
+ * All gradient pointers are required.
+ */
+size_t dg_a2a_ffn_bwd_workspace_bytes(const dg_ffn_shape* shape);
+
+dg_status dg_a2a_ffn_bwd(const dg_ffn_shape* shape,
+                         const void* inputs, const void* w1, const void* b1,
+                         const void* wout, const void* bout,
+                         const void* nx_w, const void* nx_b,
+                         const void* ng_w, const void* ng_b,
+                         const void* saved, size_t saved_bytes, const void* dY,
+                         void* d_inputs, void* d_w1, void* d_b1,
+                         void* d_wout, void* d_bout,
+                         void* d_nx_w, void* d_nx_b, void* d_ng_w, void* d_ng_b,
+                         void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * The two exchanges as explicit permutation copies (bit-exact bf16 moves),
+ * for layout checks and for callers that want the dispatched tensors:
+ *   dg_a2a_dispatch: inputs [P,B,T,D] -> xlocal [P, P*B, L, D]
+ *   dg_a2a_combine:  ylocal [P, P*B, L, D] -> output [P,B,T,D]
+ */
+dg_status dg_a2a_dispatch(int32_t P, int32_t B, int32_t T, int32_t D,
+                          const void* inputs, void* xlocal, void* stream);
+dg_status dg_a2a_combine(int32_t P, int32_t B, int32_t T, int32_t D,
+                         const void* ylocal, void* output, void* stream);
+
+/* ------------------------------------------------------------------------
+ * (c) SwiGLU column/row-parallel pair over W tensor-parallel shards.
+ *
+ * Source: "Add dist GEMM attention and FFN backend" (torchtitan PR #4044),
+ * sections "Structure" and "Row ordering": the column-parallel w1/w3 pair
+ * shares one gathered input, h_s = silu(X w1_s^T) * (X w3_s^T), and the
+ * row-parallel w2 sums the shards' partials before scattering rows back.
+ *
+ *   x_shards [W, bsz, S/W, d]   sequence shard of each rank
+ *   w13      [W, 2*ffn/W, d]    rows [w1_s ; w3_s] of shard s
+ *   w2       [d, ffn]           stock layout; shard s = columns s*ffn/W ...
+ *   y_shards [W, bsz, S/W, d]   y = sum_s h_s @ w2_s^T, rows back in place
+ * The layer is row-local, so gathering rows (rank, batch, seq_local) and
+ * scattering them back is the identity on memory order.  The shard sum is
+ * the K loop of one GEMM accumulating in TMEM.
+ * Requirements: S % W == 0, ffn % W == 0, d % 8 == 0, (ffn/W) % 8 == 0.
+ * Scratch: h [W*bsz*S/W, ffn] bf16 in `ws` (dg_tp_swiglu_workspace_bytes).
+ * ------------------------------------------------------------------------ */
+size_t dg_tp_swiglu_workspace_bytes(int64_t S, int64_t d, int64_t ffn, int32_t W, int32_t bsz);
+
+dg_status dg_tp_swiglu(int64_t S, int64_t d, int64_t ffn, int32_t W, int32_t bsz,
+                       const void* x_shards, const void* w13, const void* w2,
+                       void* y_shards, void* ws, size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Diagnostics.
+ * dg_debug_wait_timeout launches one small kernel that waits, with the
+ * library's bounded wait, on a barrier nothing will ever arrive at; after
+ * `limit_us` microseconds the wait gives up and records DG_ERR_TIMEOUT in the
+ * error word, which dg_device_status() then reports.  It exists to test the
+ * failure path without faulting or hanging the GPU.
+ * ------------------------------------------------------------------------ */
+dg_status dg_debug_wait_timeout(uint32_t limit_us, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Launch tracing.
+ * Between dg_trace_begin() and dg_trace_end(), every kernel the library
+ * enqueues (on any stream, from any thread) is bracketed by two CUDA events
+ * and recorded with its name and its algorithmic work: FLOPs (2*M*N*K per
+ * GEMM problem) and the minimum HBM bytes the kernel must move.
+ * dg_trace_end() synchronises the recorded events, aggregates them by kernel
+ * name into `out` (up to `max_entries`, in first-launch order), stops
+ * recording and returns the number of distinct kernels (or -1 on a CUDA
+ * error).  Tracing adds two event records per launch and is off by default.
+ * ------------------------------------------------------------------------ */
+typedef struct {
+  char name[40];
+  int64_t launches;
+  double total_ms;   /* sum of event-timed durations */
+  double flops;      /* algorithmic FLOPs summed over launches */
+  double bytes;      /* algorithmic HBM bytes summed over launches */
+} dg_trace_entry;
+
+dg_status dg_trace_begin(void);
+int32_t dg_trace_end(dg_trace_entry* out, int32_t max_entries);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DG_H */

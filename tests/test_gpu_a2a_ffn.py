@@ -1,0 +1,207 @@
+"""A2A FFN layer parity: libdg's forward/backward against the fp64 oracle.
+
+Small shapes are compared in full (every output and every gradient); the
+full-size workload on seeded row / token-position subsets, which is exact
+per row because each output row and each problem's weight gradients depend
+only on their own rows.  The exchange permutations are compared bit for bit.
+"""
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from expert_gemm_layers_gb300 import (FFN_PARAM_NAMES, a2a_combine, a2a_dispatch, a2a_ffn, a2a_ffn_backward,
+                                      a2a_ffn_forward, synth)
+from _compare import TOL_BF16, assert_close, err_fro
+
+pytestmark = pytest.mark.gpu
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+DEV = torch.device("cuda")
+
+# (P, B, T, D, k): the tiny workload, ragged shapes and a multi-tile one
+SMALL_SHAPES = [
+    (2, 4, 16, 128, 2),     # the tiny workload (H=256, L=8, M=8)
+    (2, 3, 4, 136, 3),      # ragged everything: H=408, 2H=816, D=136 (K not a multiple of 64)
+    (4, 40, 16, 64, 2),     # M=160 rows: two row tiles, the second ragged
+    (1, 5, 16, 128, 6),     # one rank (dispatch/combine are the identity)
+]
+
+
+def _inputs(P, B, T, D, k, seed, device, affine="random"):
+    t = synth.ffn_inputs(P, B, T, D, k, seed=seed, device=device, norm_affine=affine)
+    return t["inputs"], {n: t[n] for n in FFN_PARAM_NAMES}
+
+
+def _bits(inputs, params):
+    b = {n: synth.bits(v) for n, v in params.items()}
+    return synth.bits(inputs), b
+
+
+# ------------------------------------------------------------------ exchange
+
+def test_exchange_example_bit_exact():
+    # the page's P=2, B=1, T=2, D=1 example, widened to D=8 so rows are 16-byte aligned:
+    # element [..., 0] carries the page's values, the rest are zeros
+    x = torch.zeros((2, 1, 2, 8), dtype=torch.bfloat16)
+    x[0, 0, :, 0] = torch.tensor([10.0, 11.0])
+    x[1, 0, :, 0] = torch.tensor([20.0, 21.0])
+    X = a2a_dispatch(x.to(DEV)).cpu()
+    assert X.shape == (2, 2, 1, 8)
+    assert X[0, :, 0, 0].tolist() == [10.0, 20.0]
+    assert X[1, :, 0, 0].tolist() == [11.0, 21.0]
+    assert torch.equal(a2a_combine(X.to(DEV), 1).cpu(), x)
+
+
+@pytest.mark.parametrize("P,B,T,D", [(2, 4, 16, 128), (8, 3, 64, 24), (4, 1, 16, 8)])
+def test_dispatch_combine_bit_exact(P, B, T, D):
+    x = torch.randn((P, B, T, D), generator=torch.Generator().manual_seed(P * B + T)).to(torch.bfloat16)
+    X = a2a_dispatch(x.to(DEV)).cpu()
+    ref = O.a2a_dispatch(synth.bits(x))
+    assert np.array_equal(synth.bits(X), ref)
+    Y = a2a_combine(X.to(DEV), B).cpu()
+    assert np.array_equal(synth.bits(Y), O.a2a_combine(ref, B))
+    assert torch.equal(Y, x)
+
+
+# ------------------------------------------------------------------ forward
+
+@pytest.mark.parametrize("P,B,T,D,k", SMALL_SHAPES)
+def test_forward_small_full(P, B, T, D, k):
+    inputs, params = _inputs(P, B, T, D, k, seed=42, device="cpu")
+    out, saved = a2a_ffn_forward(inputs.to(DEV), {n: v.to(DEV) for n, v in params.items()})
+    torch.cuda.synchronize()
+    xb, pb = _bits(inputs, params)
+    ref = O.ffn_forward(O.FFNShape(P, B, T, D, k), xb, pb)
+    assert_close(out, ref, TOL_BF16, f"forward {P,B,T,D,k}")
+
+
+def test_forward_identity_affine_page_init():
+    # the page's initialisation (gamma = 1, beta = 0) on the tiny workload
+    inputs, params = _inputs(2, 4, 16, 128, 2, seed=42, device="cpu", affine="identity")
+    out, _ = a2a_ffn_forward(inputs.to(DEV), {n: v.to(DEV) for n, v in params.items()})
+    xb, pb = _bits(inputs, params)
+    ref = O.ffn_forward(O.FFNShape(2, 4, 16, 128, 2), xb, pb)
+    assert_close(out, ref, TOL_BF16, "forward, identity affine")
+
+
+def test_forward_closed_form_constant_halves():
+    # w1 = 0, constant b1 halves: every output row is silu(c) * colsum(wout) + bout
+    P, B, T, D, k = 2, 4, 16, 128, 2
+    inputs, params = _inputs(P, B, T, D, k, seed=3, device="cpu")
+    H = D * k
+    params["w1"].zero_()
+    params["b1"][..., :H] = 0.75
+    params["b1"][..., H:] = -1.5
+    params["nx_b"].fill_(1.0)
+    params["ng_b"].fill_(0.625)
+    out, _ = a2a_ffn_forward(inputs.to(DEV), {n: v.to(DEV) for n, v in params.items()})
+    xb, pb = _bits(inputs, params)
+    ref = O.ffn_forward(O.FFNShape(P, B, T, D, k), xb, pb)
+    assert_close(out, ref, 1e-2, "closed form")
+
+
+def test_forward_full_size_row_subset():
+    # the page-3 default workload: P=8, B=512, T=64, D=1280, k=6, seed 42
+    P, B, T, D, k = 8, 512, 64, 1280, 6
+    inputs, params = _inputs(P, B, T, D, k, seed=42, device=DEV, affine="random")
+    out, saved = a2a_ffn_forward(inputs, params)
+    torch.cuda.synchronize()
+    rows = np.random.default_rng(42).choice(P * B * T, size=512, replace=False)
+    xb, pb = _bits(inputs, params)
+    ref = O.ffn_forward_rows(O.FFNShape(P, B, T, D, k), xb, pb, rows)
+    got = out.reshape(-1, D)[torch.from_numpy(rows).to(DEV)]
+    assert_close(got, ref, TOL_BF16, "forward full size (512 rows)")
+
+
+# ------------------------------------------------------------------ backward
+
+def _grads_ref_full(sh, xb, pb, dyb):
+    g = O.ffn_backward(sh, xb, pb, dyb)
+    return {"inputs": g["d_inputs"], "w1": g["dw1"], "b1": g["db1"], "wout": g["dwout"], "bout": g["dbout"],
+            "nx_w": g["dnx_w"], "nx_b": g["dnx_b"], "ng_w": g["dng_w"], "ng_b": g["dng_b"]}
+
+
+@pytest.mark.parametrize("P,B,T,D,k", SMALL_SHAPES)
+def test_backward_small_full(P, B, T, D, k):
+    inputs, params = _inputs(P, B, T, D, k, seed=43, device="cpu")
+    dY = synth.ffn_grad_output(P, B, T, D, seed=44)
+    xd, pd = inputs.to(DEV), {n: v.to(DEV) for n, v in params.items()}
+    out, saved = a2a_ffn_forward(xd, pd)
+    grads = a2a_ffn_backward(xd, pd, saved, dY.to(DEV))
+    torch.cuda.synchronize()
+    xb, pb = _bits(inputs, params)
+    ref = _grads_ref_full(O.FFNShape(P, B, T, D, k), xb, pb, synth.bits(dY))
+    for name, r in ref.items():
+        got = grads[name]
+        assert_close(got.reshape(r.shape), r, TOL_BF16, f"grad {name} {P,B,T,D,k}")
+        assert err_fro(got.reshape(r.shape), r) <= TOL_BF16, name
+
+
+def test_autograd_matches_explicit_backward():
+    P, B, T, D, k = 2, 4, 16, 128, 2
+    inputs, params = _inputs(P, B, T, D, k, seed=5, device=DEV)
+    leaves = {n: v.clone().requires_grad_(True) for n, v in params.items()}
+    x = inputs.clone().requires_grad_(True)
+    out = a2a_ffn(x, leaves)
+    dY = synth.ffn_grad_output(P, B, T, D, seed=6, device=DEV)
+    out.backward(dY)
+    _, saved = a2a_ffn_forward(inputs, params)
+    g = a2a_ffn_backward(inputs, params, saved, dY)
+    assert torch.equal(x.grad, g["inputs"])
+    for n in FFN_PARAM_NAMES:
+        assert torch.equal(leaves[n].grad, g[n]), n
+
+
+def test_backward_deterministic():
+    P, B, T, D, k = 4, 40, 16, 64, 2
+    inputs, params = _inputs(P, B, T, D, k, seed=7, device=DEV)
+    dY = synth.ffn_grad_output(P, B, T, D, seed=8, device=DEV)
+    _, saved = a2a_ffn_forward(inputs, params)
+    g1 = a2a_ffn_backward(inputs, params, saved, dY)
+    g2 = a2a_ffn_backward(inputs, params, saved, dY)
+    for n in g1:
+        assert torch.equal(g1[n], g2[n]), n
+
+
+def test_backward_full_size_subsets():
+    # forward + backward at P=8, B=512, T=64, D=1280, k=6 (upstream gradient seed 43):
+    # d_inputs on 512 seeded rows; dw1, db1, dwout, dbout in full for 2 seeded token positions
+    P, B, T, D, k = 8, 512, 64, 1280, 6
+    sh = O.FFNShape(P, B, T, D, k)
+    inputs, params = _inputs(P, B, T, D, k, seed=42, device=DEV)
+    dY = synth.ffn_grad_output(P, B, T, D, seed=43, device=DEV)
+    out, saved = a2a_ffn_forward(inputs, params)
+    grads = a2a_ffn_backward(inputs, params, saved, dY)
+    torch.cuda.synchronize()
+    xb, pb = _bits(inputs, params)
+    dyb = synth.bits(dY)
+    rng = np.random.default_rng(43)
+    rows = rng.choice(P * B * T, size=512, replace=False)
+    ref_dx = O.ffn_backward_dx_rows(sh, xb, pb, dyb, rows)
+    got_dx = grads["inputs"].reshape(-1, D)[torch.from_numpy(rows).to(DEV)]
+    assert_close(got_dx, ref_dx, TOL_BF16, "d_inputs (512 rows)")
+    for t in rng.choice(T, size=2, replace=False):
+        t = int(t)
+        o = O.ffn_backward_problem(sh, xb, pb, dyb, t)
+        r, l = divmod(t, sh.L)
+        for key, name in (("dw1", "w1"), ("db1", "b1"), ("dwout", "wout"), ("dbout", "bout")):
+            got = grads[name][r, l]
+            assert_close(got, o[key], TOL_BF16, f"{name}[t={t}]")
+            assert err_fro(got, o[key]) <= TOL_BF16, name
+
+
+def test_backward_full_width_one_row_per_rank():
+    # B = 1 variant of the full workload (M = 8 rows per problem): every gradient,
+    # including the LayerNorm weight/bias gradients summed over all 8 slices of a rank
+    P, B, T, D, k = 8, 1, 64, 1280, 6
+    inputs, params = _inputs(P, B, T, D, k, seed=42, device=DEV)
+    dY = synth.ffn_grad_output(P, B, T, D, seed=43, device=DEV)
+    _, saved = a2a_ffn_forward(inputs, params)
+    grads = a2a_ffn_backward(inputs, params, saved, dY)
+    torch.cuda.synchronize()
+    xb, pb = _bits(inputs, params)
+    ref = _grads_ref_full(O.FFNShape(P, B, T, D, k), xb, pb, synth.bits(dY))
+    for name, r in ref.items():
+        assert_close(grads[name].reshape(r.shape), r, TOL_BF16, f"grad {name} (B=1)")
