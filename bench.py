@@ -441,6 +441,51 @@ def run_e2e(w, args, dev, step_flops, world):
             "d2h_bytes_per_step": int(sum(t.numel() * t.element_size() for t in outs))}
 
 
+PROFILE_CASES = {
+    "fp8": "FP8 GEMM 4096^3 (alpha 0.5, beta 1)",
+    "ffn_fwd_small": "A2A FFN forward, P=8, B=512, T=8, D=1280, k=6 (the full shape with 8 token positions)",
+    "ffn_small": "A2A FFN forward + backward, P=8, B=512, T=8, D=1280, k=6",
+    "tp": "TP SwiGLU, S=8192, d=4096, ffn=14336, W=8",
+}
+
+
+def run_profile_case(args):
+    """Runs one part of the path `--steps` times on a case small enough for an ncu capture."""
+    import torch
+
+    import expert_gemm_layers_gb300 as dg
+    from expert_gemm_layers_gb300 import synth
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    case = args.profile_case
+    if case == "fp8":
+        A, B, C = synth.fp8_gemm_inputs(4096, 4096, 4096, seed=1, device=dev)
+        D = torch.empty((4096, 4096), dtype=torch.bfloat16, device=dev)
+        run = lambda: dg.gemm_fp8(A, B, C, 0.5, 1.0, out=D)
+    elif case in ("ffn_fwd_small", "ffn_small"):
+        t = synth.ffn_inputs(8, 512, 8, 1280, 6, seed=42, device=dev)
+        params = {n: t[n] for n in dg.FFN_PARAM_NAMES}
+        x = t["inputs"]
+        dY = synth.ffn_grad_output(8, 512, 8, 1280, seed=43, device=dev)
+
+        def run():
+            out, saved = dg.a2a_ffn_forward(x, params)
+            if case == "ffn_small":
+                dg.a2a_ffn_backward(x, params, saved, dY)
+    elif case == "tp":
+        xs, w13, w2 = synth.tp_swiglu_inputs(8192, 4096, 14336, 8, seed=7, device=dev)
+        run = lambda: dg.tp_swiglu(xs, w13, w2)
+    else:
+        raise SystemExit(f"unknown profile case {case}; one of {sorted(PROFILE_CASES)}")
+    for _ in range(args.steps):
+        run()
+    torch.cuda.synchronize(dev)
+    st, code = dg.device_status(dev)
+    if st != 0:
+        raise SystemExit(f"device error word set: {code:#x}")
+    print(json.dumps({"profile_case": case, "what": PROFILE_CASES[case], "steps": args.steps}))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -448,7 +493,12 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=("dg", "reference"), default="dg")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile-case", choices=sorted(PROFILE_CASES), default=None,
+                    help="run one small part of the path (for ncu captures) instead of the benchmark")
     args = ap.parse_args()
+    if args.profile_case:
+        run_profile_case(args)
+        return
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     if world > 1:

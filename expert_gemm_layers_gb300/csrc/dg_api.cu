@@ -109,6 +109,11 @@ dg_status device_info(DeviceInfo* out) {
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
   if (dev < 0 || dev >= kMaxDevices) return fail(DG_ERR_UNSUPPORTED, "device ordinal %d out of range", dev);
+  // Bind the device's primary context to this thread: driver-API calls such as
+  // tensor-map encoding need a current context, which a fresh thread (an
+  // autograd worker, say) does not have until a runtime call creates it.
+  e = cudaSetDevice(dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaSetDevice");
   DeviceSlot& slot = g_devices[dev];
   std::call_once(slot.once, [&] {
     slot.status = DG_OK;
@@ -229,19 +234,19 @@ SavedLayout saved_layout(const FfnDims& f) {
   return l;
 }
 
-// Carving of the backward's workspace: dHl [T,M,H], dZ [T,M,2H], partials [T,nchunk,6,H] fp32.
+// Carving of the backward's workspace: dHl [T,M,H] bf16, dZ [T,M,2H] bf16,
+// rowsum [T,M] float4, norm_part [T,4,H] fp32.
 struct BwdLayout {
-  size_t dhl, dz, part, total;
-  int nchunk;
+  size_t dhl, dz, rowsum, norm, total;
 };
 BwdLayout bwd_layout(const FfnDims& f) {
   BwdLayout l;
   const size_t rows = static_cast<size_t>(f.T) * f.M;
-  l.nchunk = ffn_bwd_chunks(static_cast<int>(f.T), static_cast<int>(f.M));
   l.dhl = 0;
   l.dz = round_up(rows * f.H * 2, 256);
-  l.part = round_up(l.dz + rows * 2 * f.H * 2, 256);
-  l.total = round_up(l.part + static_cast<size_t>(f.T) * l.nchunk * 6 * f.H * 4, 256);
+  l.rowsum = round_up(l.dz + rows * 2 * f.H * 2, 256);
+  l.norm = round_up(l.rowsum + rows * 16, 256);
+  l.total = round_up(l.norm + static_cast<size_t>(f.T) * 4 * f.H * 4, 256);
   return l;
 }
 
@@ -473,7 +478,8 @@ dg_status dg_a2a_ffn_bwd(const dg_ffn_shape* shape, const void* inputs, const vo
   uint8_t* w = static_cast<uint8_t*>(ws);
   void* dHl = w + bl.dhl;
   void* dZ = w + bl.dz;
-  float* part = reinterpret_cast<float*>(w + bl.part);
+  void* rowsum = w + bl.rowsum;
+  float* norm_part = reinterpret_cast<float*>(w + bl.norm);
   const uint64_t T = f.T, M = f.M, D = f.D, H = f.H;
 
   // (1) dHl_t = dY_t @ wout_t^T      (dY_t: the dispatched rows of dY)
@@ -520,22 +526,30 @@ dg_status dg_a2a_ffn_bwd(const dg_ffn_shape* shape, const void* inputs, const vo
   }
   if (e != cudaSuccess) return cuda_fail(e, "column-sum launch");
 
-  // (4) gate + LayerNorm backward -> dZ, column partials
+  // (4) gate + LayerNorm backward: row sums, then dZ with db1 and the norm column sums
   {
-    TraceScope trace("ffn_bwd_ln_gate", s, 0.0,
-                     rows * (2.0 * 2 * H + 2.0 * H + 16.0 + 2.0 * 2 * H) + static_cast<double>(T) * bl.nchunk * 6 * H * 4);
-    e = launch_ln_gate_bwd(Z, stats, dHl, nx_w, nx_b, ng_w, ng_b, dZ, part, static_cast<int>(T), static_cast<int>(M),
-                         static_cast<int>(f.L), static_cast<int>(H), bl.nchunk, dev, s);
+    TraceScope trace("ffn_bwd_ln_rowsum", s, 0.0, rows * (2.0 * 2 * H + 2.0 * H + 32.0));
+    e = launch_ln_gate_bwd_rowsum(Z, stats, dHl, nx_w, nx_b, ng_w, ng_b, rowsum, static_cast<int>(T),
+                                  static_cast<int>(M), static_cast<int>(f.L), static_cast<int>(H), dev, s);
   }
-  if (e != cudaSuccess) return cuda_fail(e, "LayerNorm-gate backward launch");
+  if (e != cudaSuccess) return cuda_fail(e, "LayerNorm-gate backward (row sums) launch");
+  {
+    TraceScope trace("ffn_bwd_ln_apply", s, 0.0,
+                     rows * (2.0 * 2 * H + 2.0 * H + 32.0 + 2.0 * 2 * H) + static_cast<double>(T) * 2 * H * 2 +
+                         static_cast<double>(T) * 4 * H * 4);
+    e = launch_ln_gate_bwd_apply(Z, stats, rowsum, dHl, nx_w, nx_b, ng_w, ng_b, dZ, d_b1, norm_part,
+                                 static_cast<int>(T), static_cast<int>(M), static_cast<int>(f.L), static_cast<int>(H),
+                                 dev, s);
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "LayerNorm-gate backward (apply) launch");
 
-  // (5) db1, d(norm_x), d(norm_gate) from the partials
+  // (5) d(norm_x), d(norm_gate): each rank's slices summed in order
   {
-    TraceScope trace("ffn_bwd_reduce", s, 0.0, static_cast<double>(T) * bl.nchunk * 6 * H * 4);
-    e = launch_reduce_partials(part, d_b1, d_nx_w, d_nx_b, d_ng_w, d_ng_b, static_cast<int>(f.P), static_cast<int>(f.L),
-                             static_cast<int>(H), bl.nchunk, dev, s);
+    TraceScope trace("ffn_bwd_norm_reduce", s, 0.0, static_cast<double>(T) * 4 * H * 4 + static_cast<double>(f.P) * 4 * H * 2);
+    e = launch_norm_reduce(norm_part, d_nx_w, d_nx_b, d_ng_w, d_ng_b, static_cast<int>(f.P), static_cast<int>(f.L),
+                           static_cast<int>(H), dev, s);
   }
-  if (e != cudaSuccess) return cuda_fail(e, "partials reduction launch");
+  if (e != cudaSuccess) return cuda_fail(e, "norm-gradient reduction launch");
 
   // (6) dX_t = dZ_t @ w1_t^T, stored at the rows dispatch read from (inverse permutation)
   CUtensorMap mdz_k, mw1_k, mdx;

@@ -93,16 +93,22 @@ cudaError_t launch_ln_gate_fwd(const void* Z, const void* nx_w, const void* nx_b
                                const void* ng_b, void* Hl, void* stats, int64_t rows, int M, int L, int H,
                                float eps, const DeviceInfo& dev, cudaStream_t s);
 
-// Backward of the gate and both LayerNorms: dZ [rows, 2H] and per-(t, chunk)
-// column partials part [T, nchunk, 6, H] (dU, dG, da*xu, da, ds*xg, ds).
-cudaError_t launch_ln_gate_bwd(const void* Z, const void* stats, const void* dHl, const void* nx_w,
-                               const void* nx_b, const void* ng_w, const void* ng_b, void* dZ, float* part,
-                               int T, int M, int L, int H, int nchunk, const DeviceInfo& dev, cudaStream_t s);
+// Backward of the gate and both LayerNorms, pass 1: per-row sums
+// rowsum[row] = (sum dx_u, sum dx_u*x_u, sum dx_g, sum dx_g*x_g).
+cudaError_t launch_ln_gate_bwd_rowsum(const void* Z, const void* stats, const void* dHl, const void* nx_w,
+                                      const void* nx_b, const void* ng_w, const void* ng_b, void* rowsum, int T, int M,
+                                      int L, int H, const DeviceInfo& dev, cudaStream_t s);
 
-// db1 [T, 2H] and the norm gradients [P, H] from the partials, in a fixed order.
-cudaError_t launch_reduce_partials(const float* part, void* d_b1, void* d_nx_w, void* d_nx_b, void* d_ng_w,
-                                   void* d_ng_b, int P, int L, int H, int nchunk, const DeviceInfo& dev,
-                                   cudaStream_t s);
+// Pass 2: dZ [rows, 2H], db1 [T, 2H] (bf16) and per-token-position norm column
+// sums norm_part [T, 4, H] (fp32: da*x_u, da, ds*x_g, ds).
+cudaError_t launch_ln_gate_bwd_apply(const void* Z, const void* stats, const void* rowsum, const void* dHl,
+                                     const void* nx_w, const void* nx_b, const void* ng_w, const void* ng_b, void* dZ,
+                                     void* d_b1, float* norm_part, int T, int M, int L, int H, const DeviceInfo& dev,
+                                     cudaStream_t s);
+
+// d_nx_w, d_nx_b, d_ng_w, d_ng_b [P, H] = sums over each rank's L slices of norm_part.
+cudaError_t launch_norm_reduce(const float* norm_part, void* d_nx_w, void* d_nx_b, void* d_ng_w, void* d_ng_b, int P,
+                               int L, int H, const DeviceInfo& dev, cudaStream_t s);
 
 // out[g, c] = sum_n src[g*g_stride + n*row_stride + c] (bf16 in, fp32 sum, bf16 out [G, ncols]).
 cudaError_t launch_column_sum(const void* src, void* out, int G, int rows, int ncols, int64_t g_stride,
@@ -115,8 +121,5 @@ cudaError_t launch_combine(const void* in, void* out, int P, int B, int T, int D
                            cudaStream_t s);
 
 cudaError_t launch_debug_wait(uint32_t* err, uint64_t limit_ns, cudaStream_t s);
-
-// Number of row chunks per token position used by the backward partials.
-int ffn_bwd_chunks(int T, int M);
 
 }  // namespace dg

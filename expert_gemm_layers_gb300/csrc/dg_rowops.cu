@@ -16,6 +16,17 @@ namespace dg {
 namespace {
 
 constexpr int kMaxRowWarps = 16;  // row kernels use up to 512 threads
+constexpr int kRowThreads = 256;  // threads of the per-row kernels
+
+__device__ __forceinline__ void unpack8(const uint4 v, float (&f)[8]) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const float2 t = unpack_bf16x2(w[e]);
+    f[2 * e] = t.x;
+    f[2 * e + 1] = t.y;
+  }
+}
 
 __device__ __forceinline__ void load8(const __nv_bfloat16* p, float (&f)[8]) {
   const uint4 v = __ldg(reinterpret_cast<const uint4*>(p));
@@ -45,11 +56,6 @@ __device__ __forceinline__ void load4(const __nv_bfloat16* p, float (&f)[4]) {
   f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y;
 }
 
-__device__ __forceinline__ void load4_stream(const __nv_bfloat16* p, float (&f)[4]) {
-  const uint2 v = __ldcs(reinterpret_cast<const uint2*>(p));
-  const float2 a = unpack_bf16x2(v.x), b = unpack_bf16x2(v.y);
-  f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y;
-}
 
 __device__ __forceinline__ void store8(__nv_bfloat16* p, const float (&f)[8]) {
   uint4 v;
@@ -58,6 +64,15 @@ __device__ __forceinline__ void store8(__nv_bfloat16* p, const float (&f)[8]) {
   v.z = pack_bf16x2(f[4], f[5]);
   v.w = pack_bf16x2(f[6], f[7]);
   *reinterpret_cast<uint4*>(p) = v;
+}
+
+__device__ __forceinline__ void store8_stream(__nv_bfloat16* p, const float (&f)[8]) {
+  uint4 v;
+  v.x = pack_bf16x2(f[0], f[1]);
+  v.y = pack_bf16x2(f[2], f[3]);
+  v.z = pack_bf16x2(f[4], f[5]);
+  v.w = pack_bf16x2(f[6], f[7]);
+  __stcs(reinterpret_cast<uint4*>(p), v);
 }
 
 __device__ __forceinline__ float sigmoid_f(float x) { return 1.0f / (1.0f + __expf(-x)); }
@@ -97,40 +112,45 @@ __device__ __forceinline__ void block_sum(float (&v)[N], float (*sm)[kMaxRowWarp
 
 // ------------------------------------------------------------------ forward
 //
-// One CTA per row (grid-stride).  Thread i holds 8-column vectors
-// i, i + blockDim, ... of U and G in registers: mean, then the centred
-// second moment (two passes, no cancellation), then the affine and the gate.
+// One 256-thread CTA per row (grid-stride), several CTAs per SM.  Thread i
+// keeps 8-column vectors i, i + 256, ... of U and G as packed bf16 in
+// registers: mean, then the centred second moment (two passes, no
+// cancellation), then the affine and the gate.
 
 template <int VPT>
-__global__ void __launch_bounds__(512) ln_gate_fwd_kernel(
+__global__ void __launch_bounds__(kRowThreads, 2) ln_gate_fwd_kernel(
     const __nv_bfloat16* __restrict__ Z, const __nv_bfloat16* __restrict__ gx, const __nv_bfloat16* __restrict__ bx,
     const __nv_bfloat16* __restrict__ gg, const __nv_bfloat16* __restrict__ bg, __nv_bfloat16* __restrict__ Hl,
     float4* __restrict__ stats, int64_t rows, int M, int L, int H, float eps, const uint32_t* err) {
   __shared__ float sm[2][kMaxRowWarps][4];
   if (block_aborted(err)) return;
   const int nvec = H >> 3;
-  const int nt = blockDim.x;
   const float inv_h = 1.0f / static_cast<float>(H);
   for (int64_t row = blockIdx.x; row < rows; row += gridDim.x) {
     const int r = static_cast<int>(row / M) / L;
     const __nv_bfloat16* zu = Z + row * (2 * static_cast<int64_t>(H));
     const __nv_bfloat16* zg = zu + H;
-    float u[VPT][8], g[VPT][8];
+    uint4 pu[VPT], pg[VPT];
+#pragma unroll
+    for (int j = 0; j < VPT; ++j) {
+      const int v = threadIdx.x + kRowThreads * j;
+      if (v < nvec) {
+        pu[j] = __ldcs(reinterpret_cast<const uint4*>(zu + 8 * v));
+        pg[j] = __ldcs(reinterpret_cast<const uint4*>(zg + 8 * v));
+      } else {
+        pu[j] = pg[j] = make_uint4(0u, 0u, 0u, 0u);
+      }
+    }
     float s[2] = {0.0f, 0.0f};
 #pragma unroll
     for (int j = 0; j < VPT; ++j) {
-      const int v = threadIdx.x + nt * j;
-      if (v < nvec) {
-        load8_stream(zu + 8 * v, u[j]);
-        load8_stream(zg + 8 * v, g[j]);
-      } else {
-#pragma unroll
-        for (int e = 0; e < 8; ++e) u[j][e] = g[j][e] = 0.0f;
-      }
+      float u[8], g[8];
+      unpack8(pu[j], u);
+      unpack8(pg[j], g);
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
-        s[0] += u[j][e];
-        s[1] += g[j][e];
+        s[0] += u[e];
+        s[1] += g[e];
       }
     }
     block_sum<2>(s, sm, 0);
@@ -138,10 +158,13 @@ __global__ void __launch_bounds__(512) ln_gate_fwd_kernel(
     float q[2] = {0.0f, 0.0f};
 #pragma unroll
     for (int j = 0; j < VPT; ++j) {
-      if (threadIdx.x + nt * j < nvec) {
+      if (threadIdx.x + kRowThreads * j < nvec) {
+        float u[8], g[8];
+        unpack8(pu[j], u);
+        unpack8(pg[j], g);
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
-          const float du = u[j][e] - mu_u, dg = g[j][e] - mu_g;
+          const float du = u[e] - mu_u, dg = g[e] - mu_g;
           q[0] += du * du;
           q[1] += dg * dg;
         }
@@ -152,9 +175,11 @@ __global__ void __launch_bounds__(512) ln_gate_fwd_kernel(
     __nv_bfloat16* hrow = Hl + row * static_cast<int64_t>(H);
 #pragma unroll
     for (int j = 0; j < VPT; ++j) {
-      const int v = threadIdx.x + nt * j;
+      const int v = threadIdx.x + kRowThreads * j;
       if (v < nvec) {
-        float wx[8], cx[8], wg[8], cg[8], h[8];
+        float u[8], g[8], wx[8], cx[8], wg[8], cg[8], h[8];
+        unpack8(pu[j], u);
+        unpack8(pg[j], g);
         const int64_t po = static_cast<int64_t>(r) * H + 8 * v;
         load8(gx + po, wx);
         load8(bx + po, cx);
@@ -162,11 +187,11 @@ __global__ void __launch_bounds__(512) ln_gate_fwd_kernel(
         load8(bg + po, cg);
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
-          const float a = (u[j][e] - mu_u) * rs_u * wx[e] + cx[e];
-          const float sg = (g[j][e] - mu_g) * rs_g * wg[e] + cg[e];
+          const float a = (u[e] - mu_u) * rs_u * wx[e] + cx[e];
+          const float sg = (g[e] - mu_g) * rs_g * wg[e] + cg[e];
           h[e] = a * (sg * sigmoid_f(sg));
         }
-        store8(hrow + 8 * v, h);
+        store8_stream(hrow + 8 * v, h);
       }
     }
     if (threadIdx.x == 0) stats[row] = make_float4(mu_u, rs_u, mu_g, rs_g);
@@ -175,159 +200,178 @@ __global__ void __launch_bounds__(512) ln_gate_fwd_kernel(
 
 // ------------------------------------------------------------------ backward
 //
-// One CTA per work item (t, chunk) handles rows [chunk*R, chunk*R + R) of
-// token position t.  Per row it recomputes x_hat, the affines and the gate
-// from Z and the saved statistics, forms da, ds, the two row reductions of
-// the LayerNorm backward and writes dZ.  Column partials of
-// (dU, dG, da*xu, da, ds*xg, ds) accumulate in shared memory (each thread
-// owns fixed 4-column vectors, so no atomics) and are written once per item.
+// With x_u = (U - mu_u) * rstd_u, a = x_u*gx + bx, x_g likewise, s = x_g*gg + bg,
+// q = silu(s), Hl = a*q:  da = dHl*q, ds = dHl*a*sigmoid(s)*(1 + s*(1 - sigmoid(s))),
+// dx_u = da*gx, dU = rstd_u * (dx_u - mean(dx_u) - x_u*mean(dx_u*x_u)), and the
+// same for G with ds and gg.
+//
+// Pass 1 (row sums): one CTA per row computes sum(dx_u), sum(dx_u*x_u),
+// sum(dx_g), sum(dx_g*x_g) -> rowsum[row].
+// Pass 2 (apply): a CTA owns 8*128 columns of one token position t and walks
+// all M rows of t: it writes dZ and keeps the column sums of dU, dG (db1),
+// da*x_u, da (norm_x grads), ds*x_g, ds (norm_gate grads) in registers, so
+// every column sum is complete in one CTA (fixed order, deterministic).
 
-template <int VPT4>
-__global__ void __launch_bounds__(512) ln_gate_bwd_kernel(
+template <int VPT>
+__global__ void __launch_bounds__(kRowThreads, 2) ln_gate_bwd_rowsum_kernel(
     const __nv_bfloat16* __restrict__ Z, const float4* __restrict__ stats, const __nv_bfloat16* __restrict__ dHl,
     const __nv_bfloat16* __restrict__ gx, const __nv_bfloat16* __restrict__ bx, const __nv_bfloat16* __restrict__ gg,
-    const __nv_bfloat16* __restrict__ bg, __nv_bfloat16* __restrict__ dZ, float* __restrict__ part, int T, int M,
-    int L, int H, int nchunk, const uint32_t* err) {
-  extern __shared__ float4 acc4[];  // [6][H/4]
+    const __nv_bfloat16* __restrict__ bg, float4* __restrict__ rowsum, int64_t rows, int M, int L, int H,
+    const uint32_t* err) {
   __shared__ float sm[2][kMaxRowWarps][4];
   if (block_aborted(err)) return;
-  const int nv4 = H >> 2;
-  const int nt = blockDim.x;
-  const float inv_h = 1.0f / static_cast<float>(H);
-  const int R = (M + nchunk - 1) / nchunk;
-  const int items = T * nchunk;
-  for (int item = blockIdx.x; item < items; item += gridDim.x) {
-    const int t = item / nchunk, chunk = item - t * nchunk;
-    const int r = t / L;
-    const int64_t pr = static_cast<int64_t>(r) * H;
-    for (int i = threadIdx.x; i < 6 * nv4; i += nt) acc4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-    __syncthreads();
-    const int n_end = min(M, (chunk + 1) * R);
-    int slot = 0;
-    for (int n = chunk * R; n < n_end; ++n) {
-      const int64_t row = static_cast<int64_t>(t) * M + n;
-      const float4 st = stats[row];
-      const __nv_bfloat16* zu = Z + row * (2 * static_cast<int64_t>(H));
-      const __nv_bfloat16* zg = zu + H;
-      const __nv_bfloat16* dh = dHl + row * static_cast<int64_t>(H);
-      float xu[VPT4][4], xg[VPT4][4], da[VPT4][4], ds[VPT4][4];
-      float rsum[4] = {0.f, 0.f, 0.f, 0.f};
+  const int nvec = H >> 3;
+  int slot = 0;
+  for (int64_t row = blockIdx.x; row < rows; row += gridDim.x) {
+    const int r = static_cast<int>(row / M) / L;
+    const float4 st = stats[row];
+    const __nv_bfloat16* zu = Z + row * (2 * static_cast<int64_t>(H));
+    const __nv_bfloat16* zg = zu + H;
+    const __nv_bfloat16* dh = dHl + row * static_cast<int64_t>(H);
+    uint4 pu[VPT], pg[VPT], ph[VPT];
 #pragma unroll
-      for (int j = 0; j < VPT4; ++j) {
-        const int v = threadIdx.x + nt * j;
-        if (v < nv4) {
-          float uv[4], gv[4], hv[4], wx[4], cx[4], wg[4], cg[4];
-          load4_stream(zu + 4 * v, uv);
-          load4_stream(zg + 4 * v, gv);
-          load4_stream(dh + 4 * v, hv);
-          load4(gx + pr + 4 * v, wx);
-          load4(bx + pr + 4 * v, cx);
-          load4(gg + pr + 4 * v, wg);
-          load4(bg + pr + 4 * v, cg);
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float x_u = (uv[e] - st.x) * st.y;
-            const float x_g = (gv[e] - st.z) * st.w;
-            const float a = x_u * wx[e] + cx[e];
-            const float s = x_g * wg[e] + cg[e];
-            const float sg = sigmoid_f(s);
-            const float d_a = hv[e] * (s * sg);
-            const float d_s = hv[e] * a * (sg * (1.0f + s * (1.0f - sg)));
-            xu[j][e] = x_u;
-            xg[j][e] = x_g;
-            da[j][e] = d_a;
-            ds[j][e] = d_s;
-            const float dxu = d_a * wx[e], dxg = d_s * wg[e];
-            rsum[0] += dxu;
-            rsum[1] += dxu * x_u;
-            rsum[2] += dxg;
-            rsum[3] += dxg * x_g;
-          }
-        } else {
-#pragma unroll
-          for (int e = 0; e < 4; ++e) xu[j][e] = xg[j][e] = da[j][e] = ds[j][e] = 0.0f;
-        }
+    for (int j = 0; j < VPT; ++j) {
+      const int v = threadIdx.x + kRowThreads * j;
+      if (v < nvec) {
+        pu[j] = __ldcs(reinterpret_cast<const uint4*>(zu + 8 * v));
+        pg[j] = __ldcs(reinterpret_cast<const uint4*>(zg + 8 * v));
+        ph[j] = __ldcs(reinterpret_cast<const uint4*>(dh + 8 * v));
       }
-      block_sum<4>(rsum, sm, slot);
-      slot ^= 1;
-      const float m1u = rsum[0] * inv_h, m2u = rsum[1] * inv_h;
-      const float m1g = rsum[2] * inv_h, m2g = rsum[3] * inv_h;
-      __nv_bfloat16* dzu = dZ + row * (2 * static_cast<int64_t>(H));
-      __nv_bfloat16* dzg = dzu + H;
+    }
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int j = 0; j < VPT4; ++j) {
-        const int v = threadIdx.x + nt * j;
-        if (v < nv4) {
-          float wx[4], wg[4], du[4], dg[4];
-          load4(gx + pr + 4 * v, wx);
-          load4(gg + pr + 4 * v, wg);
+    for (int j = 0; j < VPT; ++j) {
+      const int v = threadIdx.x + kRowThreads * j;
+      if (v < nvec) {
+        float u[8], g[8], hv[8], wx[8], cx[8], wg[8], cg[8];
+        unpack8(pu[j], u);
+        unpack8(pg[j], g);
+        unpack8(ph[j], hv);
+        const int64_t po = static_cast<int64_t>(r) * H + 8 * v;
+        load8(gx + po, wx);
+        load8(bx + po, cx);
+        load8(gg + po, wg);
+        load8(bg + po, cg);
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            du[e] = st.y * (da[j][e] * wx[e] - m1u - xu[j][e] * m2u);
-            dg[e] = st.w * (ds[j][e] * wg[e] - m1g - xg[j][e] * m2g);
-          }
-          uint2 o;
-          o.x = pack_bf16x2(du[0], du[1]);
-          o.y = pack_bf16x2(du[2], du[3]);
-          *reinterpret_cast<uint2*>(dzu + 4 * v) = o;
-          o.x = pack_bf16x2(dg[0], dg[1]);
-          o.y = pack_bf16x2(dg[2], dg[3]);
-          *reinterpret_cast<uint2*>(dzg + 4 * v) = o;
-          float4* a0 = acc4 + v;
-          float4 q;
-          q = a0[0 * nv4]; q.x += du[0]; q.y += du[1]; q.z += du[2]; q.w += du[3]; a0[0 * nv4] = q;
-          q = a0[1 * nv4]; q.x += dg[0]; q.y += dg[1]; q.z += dg[2]; q.w += dg[3]; a0[1 * nv4] = q;
-          q = a0[2 * nv4];
-          q.x += da[j][0] * xu[j][0]; q.y += da[j][1] * xu[j][1]; q.z += da[j][2] * xu[j][2]; q.w += da[j][3] * xu[j][3];
-          a0[2 * nv4] = q;
-          q = a0[3 * nv4]; q.x += da[j][0]; q.y += da[j][1]; q.z += da[j][2]; q.w += da[j][3]; a0[3 * nv4] = q;
-          q = a0[4 * nv4];
-          q.x += ds[j][0] * xg[j][0]; q.y += ds[j][1] * xg[j][1]; q.z += ds[j][2] * xg[j][2]; q.w += ds[j][3] * xg[j][3];
-          a0[4 * nv4] = q;
-          q = a0[5 * nv4]; q.x += ds[j][0]; q.y += ds[j][1]; q.z += ds[j][2]; q.w += ds[j][3]; a0[5 * nv4] = q;
+        for (int e = 0; e < 8; ++e) {
+          const float xu = (u[e] - st.x) * st.y, xg = (g[e] - st.z) * st.w;
+          const float a = xu * wx[e] + cx[e], sv = xg * wg[e] + cg[e];
+          const float sgm = sigmoid_f(sv);
+          const float dxu = hv[e] * (sv * sgm) * wx[e];
+          const float dxg = hv[e] * a * (sgm * (1.0f + sv * (1.0f - sgm))) * wg[e];
+          acc[0] += dxu;
+          acc[1] += dxu * xu;
+          acc[2] += dxg;
+          acc[3] += dxg * xg;
         }
       }
     }
-    __syncthreads();
-    float4* dst = reinterpret_cast<float4*>(part + static_cast<int64_t>(item) * 6 * H);
-    for (int i = threadIdx.x; i < 6 * nv4; i += nt) dst[i] = acc4[i];
-    __syncthreads();
+    block_sum<4>(acc, sm, slot);
+    slot ^= 1;
+    if (threadIdx.x == 0) rowsum[row] = make_float4(acc[0], acc[1], acc[2], acc[3]);
   }
 }
 
-// db1[t, c] (c < 2H) and the four norm gradients [P, H], summing the
-// partials in a fixed order (chunks, then slices), so reruns are bit-identical.
-__global__ void reduce_partials_kernel(const float* __restrict__ part, __nv_bfloat16* __restrict__ d_b1,
-                                       __nv_bfloat16* __restrict__ d_nx_w, __nv_bfloat16* __restrict__ d_nx_b,
-                                       __nv_bfloat16* __restrict__ d_ng_w, __nv_bfloat16* __restrict__ d_ng_b, int P,
-                                       int L, int H, int nchunk, const uint32_t* err) {
+constexpr int kApplyThreads = 128;
+constexpr int kApplyCols = 8 * kApplyThreads;
+
+__global__ void __launch_bounds__(kApplyThreads) ln_gate_bwd_apply_kernel(
+    const __nv_bfloat16* __restrict__ Z, const float4* __restrict__ stats, const float4* __restrict__ rowsum,
+    const __nv_bfloat16* __restrict__ dHl, const __nv_bfloat16* __restrict__ gx, const __nv_bfloat16* __restrict__ bx,
+    const __nv_bfloat16* __restrict__ gg, const __nv_bfloat16* __restrict__ bg, __nv_bfloat16* __restrict__ dZ,
+    __nv_bfloat16* __restrict__ d_b1, float* __restrict__ norm_part, int M, int L, int H, const uint32_t* err) {
   if (ld_volatile_u32(err) != 0u) return;
-  const int T = P * L;
-  const int64_t n_b1 = static_cast<int64_t>(T) * 2 * H;
-  const int64_t n_norm = static_cast<int64_t>(P) * 4 * H;
-  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n_b1 + n_norm;
-       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    if (i < n_b1) {
-      const int t = static_cast<int>(i / (2 * H));
-      const int c2 = static_cast<int>(i - static_cast<int64_t>(t) * 2 * H);
-      const int which = c2 >= H ? 1 : 0;
-      const int c = c2 - which * H;
-      float s = 0.0f;
-      for (int k = 0; k < nchunk; ++k)
-        s += part[((static_cast<int64_t>(t) * nchunk + k) * 6 + which) * H + c];
-      d_b1[i] = __float2bfloat16_rn(s);
-    } else {
-      const int64_t j = i - n_b1;
-      const int r = static_cast<int>(j / (4 * H));
-      const int q = static_cast<int>((j / H) % 4);  // 0: nx_w, 1: nx_b, 2: ng_w, 3: ng_b
-      const int c = static_cast<int>(j % H);
-      float s = 0.0f;
-      for (int l = 0; l < L; ++l)
-        for (int k = 0; k < nchunk; ++k)
-          s += part[((static_cast<int64_t>(r * L + l) * nchunk + k) * 6 + 2 + q) * H + c];
-      __nv_bfloat16* out = q == 0 ? d_nx_w : q == 1 ? d_nx_b : q == 2 ? d_ng_w : d_ng_b;
-      out[static_cast<int64_t>(r) * H + c] = __float2bfloat16_rn(s);
+  const int t = blockIdx.y;
+  const int r = t / L;
+  const int c0 = blockIdx.x * kApplyCols + 8 * threadIdx.x;
+  if (c0 >= H) return;
+  const float inv_h = 1.0f / static_cast<float>(H);
+  float wx[8], cx[8], wg[8], cg[8];
+  {
+    const int64_t po = static_cast<int64_t>(r) * H + c0;
+    load8(gx + po, wx);
+    load8(bx + po, cx);
+    load8(gg + po, wg);
+    load8(bg + po, cg);
+  }
+  float s_du[8], s_dg[8], s_gx[8], s_bx[8], s_gg[8], s_bg[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) s_du[e] = s_dg[e] = s_gx[e] = s_bx[e] = s_gg[e] = s_bg[e] = 0.0f;
+  const int64_t row0 = static_cast<int64_t>(t) * M;
+  const int64_t zstride = 2 * static_cast<int64_t>(H);
+  constexpr int U = 2;  // rows in flight per thread
+  for (int n = 0; n < M; n += U) {
+    uint4 pu[U], pg[U], ph[U];
+    float4 st[U], rs[U];
+#pragma unroll
+    for (int i = 0; i < U; ++i) {
+      if (n + i < M) {
+        const int64_t row = row0 + n + i;
+        pu[i] = __ldcs(reinterpret_cast<const uint4*>(Z + row * zstride + c0));
+        pg[i] = __ldcs(reinterpret_cast<const uint4*>(Z + row * zstride + H + c0));
+        ph[i] = __ldcs(reinterpret_cast<const uint4*>(dHl + row * H + c0));
+        st[i] = stats[row];
+        rs[i] = rowsum[row];
+      }
     }
+#pragma unroll
+    for (int i = 0; i < U; ++i) {
+      if (n + i < M) {
+        const int64_t row = row0 + n + i;
+        float u[8], g[8], hv[8], du[8], dg[8];
+        unpack8(pu[i], u);
+        unpack8(pg[i], g);
+        unpack8(ph[i], hv);
+        const float m1u = rs[i].x * inv_h, m2u = rs[i].y * inv_h;
+        const float m1g = rs[i].z * inv_h, m2g = rs[i].w * inv_h;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const float xu = (u[e] - st[i].x) * st[i].y, xg = (g[e] - st[i].z) * st[i].w;
+          const float a = xu * wx[e] + cx[e], sv = xg * wg[e] + cg[e];
+          const float sgm = sigmoid_f(sv);
+          const float da = hv[e] * (sv * sgm);
+          const float ds = hv[e] * a * (sgm * (1.0f + sv * (1.0f - sgm)));
+          du[e] = st[i].y * (da * wx[e] - m1u - xu * m2u);
+          dg[e] = st[i].w * (ds * wg[e] - m1g - xg * m2g);
+          s_du[e] += du[e];
+          s_dg[e] += dg[e];
+          s_gx[e] += da * xu;
+          s_bx[e] += da;
+          s_gg[e] += ds * xg;
+          s_bg[e] += ds;
+        }
+        store8_stream(dZ + row * zstride + c0, du);
+        store8_stream(dZ + row * zstride + H + c0, dg);
+      }
+    }
+  }
+  store8(d_b1 + static_cast<int64_t>(t) * 2 * H + c0, s_du);
+  store8(d_b1 + static_cast<int64_t>(t) * 2 * H + H + c0, s_dg);
+  float* np = norm_part + static_cast<int64_t>(t) * 4 * H + c0;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    np[e] = s_gx[e];
+    np[H + e] = s_bx[e];
+    np[2 * H + e] = s_gg[e];
+    np[3 * H + e] = s_bg[e];
+  }
+}
+
+// Norm gradients of rank r: sum of its L slices' column sums, in slice order.
+__global__ void norm_reduce_kernel(const float* __restrict__ norm_part, __nv_bfloat16* __restrict__ d_nx_w,
+                                   __nv_bfloat16* __restrict__ d_nx_b, __nv_bfloat16* __restrict__ d_ng_w,
+                                   __nv_bfloat16* __restrict__ d_ng_b, int P, int L, int H, const uint32_t* err) {
+  if (ld_volatile_u32(err) != 0u) return;
+  const int64_t n = static_cast<int64_t>(P) * 4 * H;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int r = static_cast<int>(i / (4 * H));
+    const int q = static_cast<int>((i / H) % 4);  // 0: nx_w, 1: nx_b, 2: ng_w, 3: ng_b
+    const int c = static_cast<int>(i % H);
+    float s = 0.0f;
+    for (int l = 0; l < L; ++l) s += norm_part[(static_cast<int64_t>(r * L + l) * 4 + q) * H + c];
+    __nv_bfloat16* out = q == 0 ? d_nx_w : q == 1 ? d_nx_b : q == 2 ? d_ng_w : d_ng_b;
+    out[static_cast<int64_t>(r) * H + c] = __float2bfloat16_rn(s);
   }
 }
 
@@ -416,82 +460,66 @@ int grid_for(const DeviceInfo& dev, const void* kernel, int threads, size_t smem
 
 }  // namespace
 
-int ffn_bwd_chunks(int T, int M) {
-  int want = (1024 + T - 1) / T;
-  int cap = (M + 31) / 32;
-  if (want > cap) want = cap;
-  return want < 1 ? 1 : want;
-}
-
-// Smallest VPT in {1,2,4,8} whose block (rounded to warps) has at most 512 threads.
-static bool row_block(int nvec, int* vpt, int* threads) {
-  for (int v = 1; v <= 8; v *= 2) {
-    int t = (nvec + v - 1) / v;
-    t = ((t + 31) / 32) * 32;
-    if (t <= 512) {
-      *vpt = v;
-      *threads = t < 32 ? 32 : t;
-      return true;
-    }
-  }
-  return false;
-}
-
 cudaError_t launch_ln_gate_fwd(const void* Z, const void* nx_w, const void* nx_b, const void* ng_w,
                                const void* ng_b, void* Hl, void* stats, int64_t rows, int M, int L, int H,
                                float eps, const DeviceInfo& dev, cudaStream_t s) {
-  int vpt = 0, threads = 0;
-  if (!row_block(H / 8, &vpt, &threads)) return cudaErrorInvalidValue;
+  const int vpt = (H / 8 + kRowThreads - 1) / kRowThreads;
   auto run = [&](auto kern) {
-    const int grid = grid_for(dev, reinterpret_cast<const void*>(kern), threads, 0, rows);
-    kern<<<grid, threads, 0, s>>>(static_cast<const __nv_bfloat16*>(Z), static_cast<const __nv_bfloat16*>(nx_w),
-                                  static_cast<const __nv_bfloat16*>(nx_b), static_cast<const __nv_bfloat16*>(ng_w),
-                                  static_cast<const __nv_bfloat16*>(ng_b), static_cast<__nv_bfloat16*>(Hl),
-                                  static_cast<float4*>(stats), rows, M, L, H, eps, dev.err);
+    const int grid = grid_for(dev, reinterpret_cast<const void*>(kern), kRowThreads, 0, rows);
+    kern<<<grid, kRowThreads, 0, s>>>(static_cast<const __nv_bfloat16*>(Z), static_cast<const __nv_bfloat16*>(nx_w),
+                                      static_cast<const __nv_bfloat16*>(nx_b), static_cast<const __nv_bfloat16*>(ng_w),
+                                      static_cast<const __nv_bfloat16*>(ng_b), static_cast<__nv_bfloat16*>(Hl),
+                                      static_cast<float4*>(stats), rows, M, L, H, eps, dev.err);
     return cudaGetLastError();
   };
-  if (vpt == 1) return run(ln_gate_fwd_kernel<1>);
-  if (vpt == 2) return run(ln_gate_fwd_kernel<2>);
-  if (vpt == 4) return run(ln_gate_fwd_kernel<4>);
-  return run(ln_gate_fwd_kernel<8>);
+  if (vpt <= 1) return run(ln_gate_fwd_kernel<1>);
+  if (vpt <= 2) return run(ln_gate_fwd_kernel<2>);
+  if (vpt <= 4) return run(ln_gate_fwd_kernel<4>);
+  return cudaErrorInvalidValue;
 }
 
-size_t ln_gate_bwd_smem(int H) { return static_cast<size_t>(6) * H * sizeof(float); }
-
-cudaError_t launch_ln_gate_bwd(const void* Z, const void* stats, const void* dHl, const void* nx_w,
-                               const void* nx_b, const void* ng_w, const void* ng_b, void* dZ, float* part,
-                               int T, int M, int L, int H, int nchunk, const DeviceInfo& dev, cudaStream_t s) {
-  int vpt = 0, threads = 0;
-  if (!row_block(H / 4, &vpt, &threads)) return cudaErrorInvalidValue;
-  const size_t smem = ln_gate_bwd_smem(H);
+cudaError_t launch_ln_gate_bwd_rowsum(const void* Z, const void* stats, const void* dHl, const void* nx_w,
+                                      const void* nx_b, const void* ng_w, const void* ng_b, void* rowsum, int T, int M,
+                                      int L, int H, const DeviceInfo& dev, cudaStream_t s) {
+  const int64_t rows = static_cast<int64_t>(T) * M;
+  const int vpt = (H / 8 + kRowThreads - 1) / kRowThreads;
   auto run = [&](auto kern) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
-    const int grid = grid_for(dev, reinterpret_cast<const void*>(kern), threads, smem,
-                              static_cast<int64_t>(T) * nchunk);
-    kern<<<grid, threads, smem, s>>>(
-        static_cast<const __nv_bfloat16*>(Z), static_cast<const float4*>(stats),
-        static_cast<const __nv_bfloat16*>(dHl), static_cast<const __nv_bfloat16*>(nx_w),
-        static_cast<const __nv_bfloat16*>(nx_b), static_cast<const __nv_bfloat16*>(ng_w),
-        static_cast<const __nv_bfloat16*>(ng_b), static_cast<__nv_bfloat16*>(dZ), part, T, M, L, H, nchunk, dev.err);
+    const int grid = grid_for(dev, reinterpret_cast<const void*>(kern), kRowThreads, 0, rows);
+    kern<<<grid, kRowThreads, 0, s>>>(static_cast<const __nv_bfloat16*>(Z), static_cast<const float4*>(stats),
+                                      static_cast<const __nv_bfloat16*>(dHl), static_cast<const __nv_bfloat16*>(nx_w),
+                                      static_cast<const __nv_bfloat16*>(nx_b), static_cast<const __nv_bfloat16*>(ng_w),
+                                      static_cast<const __nv_bfloat16*>(ng_b), static_cast<float4*>(rowsum), rows, M,
+                                      L, H, dev.err);
     return cudaGetLastError();
   };
-  if (vpt == 1) return run(ln_gate_bwd_kernel<1>);
-  if (vpt == 2) return run(ln_gate_bwd_kernel<2>);
-  if (vpt == 4) return run(ln_gate_bwd_kernel<4>);
-  return run(ln_gate_bwd_kernel<8>);
+  if (vpt <= 1) return run(ln_gate_bwd_rowsum_kernel<1>);
+  if (vpt <= 2) return run(ln_gate_bwd_rowsum_kernel<2>);
+  if (vpt <= 4) return run(ln_gate_bwd_rowsum_kernel<4>);
+  return cudaErrorInvalidValue;
 }
 
-cudaError_t launch_reduce_partials(const float* part, void* d_b1, void* d_nx_w, void* d_nx_b, void* d_ng_w,
-                                   void* d_ng_b, int P, int L, int H, int nchunk, const DeviceInfo& dev,
-                                   cudaStream_t s) {
-  const int64_t n = static_cast<int64_t>(P) * L * 2 * H + static_cast<int64_t>(P) * 4 * H;
+cudaError_t launch_ln_gate_bwd_apply(const void* Z, const void* stats, const void* rowsum, const void* dHl,
+                                     const void* nx_w, const void* nx_b, const void* ng_w, const void* ng_b, void* dZ,
+                                     void* d_b1, float* norm_part, int T, int M, int L, int H, const DeviceInfo& dev,
+                                     cudaStream_t s) {
+  dim3 grid((H + kApplyCols - 1) / kApplyCols, T);
+  ln_gate_bwd_apply_kernel<<<grid, kApplyThreads, 0, s>>>(
+      static_cast<const __nv_bfloat16*>(Z), static_cast<const float4*>(stats), static_cast<const float4*>(rowsum),
+      static_cast<const __nv_bfloat16*>(dHl), static_cast<const __nv_bfloat16*>(nx_w),
+      static_cast<const __nv_bfloat16*>(nx_b), static_cast<const __nv_bfloat16*>(ng_w),
+      static_cast<const __nv_bfloat16*>(ng_b), static_cast<__nv_bfloat16*>(dZ), static_cast<__nv_bfloat16*>(d_b1),
+      norm_part, M, L, H, dev.err);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_norm_reduce(const float* norm_part, void* d_nx_w, void* d_nx_b, void* d_ng_w, void* d_ng_b, int P,
+                               int L, int H, const DeviceInfo& dev, cudaStream_t s) {
+  const int64_t n = static_cast<int64_t>(P) * 4 * H;
   int64_t blocks = (n + 255) / 256;
   if (blocks > 8 * dev.num_sms) blocks = 8 * dev.num_sms;
-  reduce_partials_kernel<<<static_cast<int>(blocks), 256, 0, s>>>(
-      part, static_cast<__nv_bfloat16*>(d_b1), static_cast<__nv_bfloat16*>(d_nx_w),
-      static_cast<__nv_bfloat16*>(d_nx_b), static_cast<__nv_bfloat16*>(d_ng_w), static_cast<__nv_bfloat16*>(d_ng_b), P,
-      L, H, nchunk, dev.err);
+  norm_reduce_kernel<<<static_cast<int>(blocks), 256, 0, s>>>(
+      norm_part, static_cast<__nv_bfloat16*>(d_nx_w), static_cast<__nv_bfloat16*>(d_nx_b),
+      static_cast<__nv_bfloat16*>(d_ng_w), static_cast<__nv_bfloat16*>(d_ng_b), P, L, H, dev.err);
   return cudaGetLastError();
 }
 
