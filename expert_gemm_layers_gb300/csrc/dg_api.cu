@@ -235,18 +235,20 @@ SavedLayout saved_layout(const FfnDims& f) {
 }
 
 // Carving of the backward's workspace: dHl [T,M,H] bf16, dZ [T,M,2H] bf16,
-// rowsum [T,M] float4, norm_part [T,4,H] fp32.
+// rowsum [T,M] float4, column partials [T,nsplit,6,H] fp32.
 struct BwdLayout {
-  size_t dhl, dz, rowsum, norm, total;
+  size_t dhl, dz, rowsum, part, total;
+  int nsplit;
 };
 BwdLayout bwd_layout(const FfnDims& f) {
   BwdLayout l;
   const size_t rows = static_cast<size_t>(f.T) * f.M;
+  l.nsplit = ffn_bwd_row_splits(static_cast<int>(f.T), static_cast<int>(f.M));
   l.dhl = 0;
   l.dz = round_up(rows * f.H * 2, 256);
   l.rowsum = round_up(l.dz + rows * 2 * f.H * 2, 256);
-  l.norm = round_up(l.rowsum + rows * 16, 256);
-  l.total = round_up(l.norm + static_cast<size_t>(f.T) * 4 * f.H * 4, 256);
+  l.part = round_up(l.rowsum + rows * 16, 256);
+  l.total = round_up(l.part + static_cast<size_t>(f.T) * l.nsplit * 6 * f.H * 4, 256);
   return l;
 }
 
@@ -354,13 +356,13 @@ dg_status dg_gemm_fp8(int64_t M, int64_t N, int64_t K, const void* A, const void
 // ------------------------------------------------------------------ A2A FFN
 
 size_t dg_a2a_ffn_saved_bytes(const dg_ffn_shape* shape) {
-  FfnDims f;
+  FfnDims f{};
   if (check_ffn_shape(shape, &f) != DG_OK) return 0;
   return saved_layout(f).total;
 }
 
 size_t dg_a2a_ffn_bwd_workspace_bytes(const dg_ffn_shape* shape) {
-  FfnDims f;
+  FfnDims f{};
   if (check_ffn_shape(shape, &f) != DG_OK) return 0;
   return bwd_layout(f).total;
 }
@@ -368,7 +370,7 @@ size_t dg_a2a_ffn_bwd_workspace_bytes(const dg_ffn_shape* shape) {
 dg_status dg_a2a_ffn_fwd(const dg_ffn_shape* shape, const void* inputs, const void* w1, const void* b1,
                          const void* wout, const void* bout, const void* nx_w, const void* nx_b, const void* ng_w,
                          const void* ng_b, void* output, void* saved, size_t saved_bytes, void* stream) {
-  FfnDims f;
+  FfnDims f{};
   dg_status st = check_ffn_shape(shape, &f);
   if (st != DG_OK) return st;
   const void* ptrs[] = {inputs, w1, b1, wout, bout, nx_w, nx_b, ng_w, ng_b, output, saved};
@@ -445,7 +447,7 @@ dg_status dg_a2a_ffn_bwd(const dg_ffn_shape* shape, const void* inputs, const vo
                          const void* ng_b, const void* saved, size_t saved_bytes, const void* dY, void* d_inputs,
                          void* d_w1, void* d_b1, void* d_wout, void* d_bout, void* d_nx_w, void* d_nx_b,
                          void* d_ng_w, void* d_ng_b, void* ws, size_t ws_bytes, void* stream) {
-  FfnDims f;
+  FfnDims f{};
   dg_status st = check_ffn_shape(shape, &f);
   if (st != DG_OK) return st;
   (void)b1;
@@ -479,7 +481,7 @@ dg_status dg_a2a_ffn_bwd(const dg_ffn_shape* shape, const void* inputs, const vo
   void* dHl = w + bl.dhl;
   void* dZ = w + bl.dz;
   void* rowsum = w + bl.rowsum;
-  float* norm_part = reinterpret_cast<float*>(w + bl.norm);
+  float* part = reinterpret_cast<float*>(w + bl.part);
   const uint64_t T = f.T, M = f.M, D = f.D, H = f.H;
 
   // (1) dHl_t = dY_t @ wout_t^T      (dY_t: the dispatched rows of dY)
@@ -535,21 +537,22 @@ dg_status dg_a2a_ffn_bwd(const dg_ffn_shape* shape, const void* inputs, const vo
   if (e != cudaSuccess) return cuda_fail(e, "LayerNorm-gate backward (row sums) launch");
   {
     TraceScope trace("ffn_bwd_ln_apply", s, 0.0,
-                     rows * (2.0 * 2 * H + 2.0 * H + 32.0 + 2.0 * 2 * H) + static_cast<double>(T) * 2 * H * 2 +
-                         static_cast<double>(T) * 4 * H * 4);
-    e = launch_ln_gate_bwd_apply(Z, stats, rowsum, dHl, nx_w, nx_b, ng_w, ng_b, dZ, d_b1, norm_part,
-                                 static_cast<int>(T), static_cast<int>(M), static_cast<int>(f.L), static_cast<int>(H),
-                                 dev, s);
+                     rows * (2.0 * 2 * H + 2.0 * H + 32.0 + 2.0 * 2 * H) +
+                         static_cast<double>(T) * bl.nsplit * 6 * H * 4);
+    e = launch_ln_gate_bwd_apply(Z, stats, rowsum, dHl, nx_w, nx_b, ng_w, ng_b, dZ, part, static_cast<int>(T),
+                                 static_cast<int>(M), static_cast<int>(f.L), static_cast<int>(H), bl.nsplit, dev, s);
   }
   if (e != cudaSuccess) return cuda_fail(e, "LayerNorm-gate backward (apply) launch");
 
-  // (5) d(norm_x), d(norm_gate): each rank's slices summed in order
+  // (5) db1, d(norm_x), d(norm_gate): partial sums added in a fixed order
   {
-    TraceScope trace("ffn_bwd_norm_reduce", s, 0.0, static_cast<double>(T) * 4 * H * 4 + static_cast<double>(f.P) * 4 * H * 2);
-    e = launch_norm_reduce(norm_part, d_nx_w, d_nx_b, d_ng_w, d_ng_b, static_cast<int>(f.P), static_cast<int>(f.L),
-                           static_cast<int>(H), dev, s);
+    TraceScope trace("ffn_bwd_grad_reduce", s, 0.0,
+                     static_cast<double>(T) * bl.nsplit * 6 * H * 4 + static_cast<double>(T) * 2 * H * 2 +
+                         static_cast<double>(f.P) * 4 * H * 2);
+    e = launch_grad_reduce(part, d_b1, d_nx_w, d_nx_b, d_ng_w, d_ng_b, static_cast<int>(f.P), static_cast<int>(f.L),
+                           static_cast<int>(H), bl.nsplit, dev, s);
   }
-  if (e != cudaSuccess) return cuda_fail(e, "norm-gradient reduction launch");
+  if (e != cudaSuccess) return cuda_fail(e, "gradient reduction launch");
 
   // (6) dX_t = dZ_t @ w1_t^T, stored at the rows dispatch read from (inverse permutation)
   CUtensorMap mdz_k, mw1_k, mdx;

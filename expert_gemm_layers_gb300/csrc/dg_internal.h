@@ -99,16 +99,19 @@ cudaError_t launch_ln_gate_bwd_rowsum(const void* Z, const void* stats, const vo
                                       const void* nx_b, const void* ng_w, const void* ng_b, void* rowsum, int T, int M,
                                       int L, int H, const DeviceInfo& dev, cudaStream_t s);
 
-// Pass 2: dZ [rows, 2H], db1 [T, 2H] (bf16) and per-token-position norm column
-// sums norm_part [T, 4, H] (fp32: da*x_u, da, ds*x_g, ds).
+// Pass 2: dZ [rows, 2H] and per-(t, row range) column partial sums
+// part [T, nsplit, 6, H] fp32 (dU, dG, da*x_u, da, ds*x_g, ds).
 cudaError_t launch_ln_gate_bwd_apply(const void* Z, const void* stats, const void* rowsum, const void* dHl,
                                      const void* nx_w, const void* nx_b, const void* ng_w, const void* ng_b, void* dZ,
-                                     void* d_b1, float* norm_part, int T, int M, int L, int H, const DeviceInfo& dev,
+                                     float* part, int T, int M, int L, int H, int nsplit, const DeviceInfo& dev,
                                      cudaStream_t s);
 
-// d_nx_w, d_nx_b, d_ng_w, d_ng_b [P, H] = sums over each rank's L slices of norm_part.
-cudaError_t launch_norm_reduce(const float* norm_part, void* d_nx_w, void* d_nx_b, void* d_ng_w, void* d_ng_b, int P,
-                               int L, int H, const DeviceInfo& dev, cudaStream_t s);
+// Row ranges per token position used by pass 2.
+int ffn_bwd_row_splits(int T, int M);
+
+// db1 [T, 2H] and d_nx_w, d_nx_b, d_ng_w, d_ng_b [P, H] from the partials, in a fixed order.
+cudaError_t launch_grad_reduce(const float* part, void* d_b1, void* d_nx_w, void* d_nx_b, void* d_ng_w, void* d_ng_b,
+                               int P, int L, int H, int nsplit, const DeviceInfo& dev, cudaStream_t s);
 
 // out[g, c] = sum_n src[g*g_stride + n*row_stride + c] (bf16 in, fp32 sum, bf16 out [G, ncols]).
 cudaError_t launch_column_sum(const void* src, void* out, int G, int rows, int ncols, int64_t g_stride,

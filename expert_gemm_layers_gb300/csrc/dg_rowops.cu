@@ -39,32 +39,6 @@ __device__ __forceinline__ void load8(const __nv_bfloat16* p, float (&f)[8]) {
   }
 }
 
-__device__ __forceinline__ void load8_stream(const __nv_bfloat16* p, float (&f)[8]) {
-  const uint4 v = __ldcs(reinterpret_cast<const uint4*>(p));
-  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    const float2 t = unpack_bf16x2(w[e]);
-    f[2 * e] = t.x;
-    f[2 * e + 1] = t.y;
-  }
-}
-
-__device__ __forceinline__ void load4(const __nv_bfloat16* p, float (&f)[4]) {
-  const uint2 v = __ldg(reinterpret_cast<const uint2*>(p));
-  const float2 a = unpack_bf16x2(v.x), b = unpack_bf16x2(v.y);
-  f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y;
-}
-
-
-__device__ __forceinline__ void store8(__nv_bfloat16* p, const float (&f)[8]) {
-  uint4 v;
-  v.x = pack_bf16x2(f[0], f[1]);
-  v.y = pack_bf16x2(f[2], f[3]);
-  v.z = pack_bf16x2(f[4], f[5]);
-  v.w = pack_bf16x2(f[6], f[7]);
-  *reinterpret_cast<uint4*>(p) = v;
-}
 
 __device__ __forceinline__ void store8_stream(__nv_bfloat16* p, const float (&f)[8]) {
   uint4 v;
@@ -75,7 +49,22 @@ __device__ __forceinline__ void store8_stream(__nv_bfloat16* p, const float (&f)
   __stcs(reinterpret_cast<uint4*>(p), v);
 }
 
-__device__ __forceinline__ float sigmoid_f(float x) { return 1.0f / (1.0f + __expf(-x)); }
+// sigmoid(x) = (1 + tanh(x/2)) / 2, with the hardware tanh approximation
+// (tanh.approx.f32, relative error about 2^-11): one MUFU operation instead of
+// an exponential and a division.
+__device__ __forceinline__ float tanh_fast(float x) {
+  float y;
+  asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ float sigmoid_fast(float x) { return fmaf(0.5f, tanh_fast(0.5f * x), 0.5f); }
+
+// silu(x) = x * sigmoid(x) = h + h * tanh(h) with h = x/2.
+__device__ __forceinline__ float silu_fast(float x) {
+  const float h = 0.5f * x;
+  return fmaf(h, tanh_fast(h), h);
+}
 
 // Block-uniform read of the error word (a divergent early return ahead of a
 // barrier would be undefined).
@@ -112,10 +101,37 @@ __device__ __forceinline__ void block_sum(float (&v)[N], float (*sm)[kMaxRowWarp
 
 // ------------------------------------------------------------------ forward
 //
-// One 256-thread CTA per row (grid-stride), several CTAs per SM.  Thread i
-// keeps 8-column vectors i, i + 256, ... of U and G as packed bf16 in
-// registers: mean, then the centred second moment (two passes, no
-// cancellation), then the affine and the gate.
+// One CTA per row (grid-stride).  Thread i keeps 8-column vectors
+// i, i + blockDim, ... of U and G as packed bf16 in registers, and loads the
+// CTA's next row while it finishes the current one.  The row statistics use
+// the shifted-data single pass (Chan, Golub & LeVeque, "Algorithms for
+// computing the sample variance"): with K the row's first element,
+// mean = K + S1/H and var = S2/H - (S1/H)^2 where S1 = sum(x-K),
+// S2 = sum((x-K)^2); K is a sample of the row, so the subtraction does not
+// cancel catastrophically, and a constant row gives exactly var = 0.
+
+template <int VPT>
+struct RowFrag {
+  uint4 u[VPT], g[VPT];
+  float ku, kg;
+};
+
+template <int VPT>
+__device__ __forceinline__ void load_zrow(RowFrag<VPT>& f, const __nv_bfloat16* zu, int H, int nvec) {
+  const __nv_bfloat16* zg = zu + H;
+#pragma unroll
+  for (int j = 0; j < VPT; ++j) {
+    const int v = threadIdx.x + blockDim.x * j;
+    if (v < nvec) {
+      f.u[j] = __ldcs(reinterpret_cast<const uint4*>(zu + 8 * v));
+      f.g[j] = __ldcs(reinterpret_cast<const uint4*>(zg + 8 * v));
+    } else {
+      f.u[j] = f.g[j] = make_uint4(0u, 0u, 0u, 0u);
+    }
+  }
+  f.ku = __bfloat162float(zu[0]);
+  f.kg = __bfloat162float(zg[0]);
+}
 
 template <int VPT>
 __global__ void __launch_bounds__(kRowThreads, 2) ln_gate_fwd_kernel(
@@ -126,60 +142,47 @@ __global__ void __launch_bounds__(kRowThreads, 2) ln_gate_fwd_kernel(
   if (block_aborted(err)) return;
   const int nvec = H >> 3;
   const float inv_h = 1.0f / static_cast<float>(H);
-  for (int64_t row = blockIdx.x; row < rows; row += gridDim.x) {
+  const int64_t zstride = 2 * static_cast<int64_t>(H);
+  RowFrag<VPT> cur, nxt;
+  int64_t row = blockIdx.x;
+  if (row < rows) load_zrow(cur, Z + row * zstride, H, nvec);
+  int slot = 0;
+  for (; row < rows; row += gridDim.x) {
+    const int64_t next = row + gridDim.x;
+    if (next < rows) load_zrow(nxt, Z + next * zstride, H, nvec);
     const int r = static_cast<int>(row / M) / L;
-    const __nv_bfloat16* zu = Z + row * (2 * static_cast<int64_t>(H));
-    const __nv_bfloat16* zg = zu + H;
-    uint4 pu[VPT], pg[VPT];
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int j = 0; j < VPT; ++j) {
-      const int v = threadIdx.x + kRowThreads * j;
-      if (v < nvec) {
-        pu[j] = __ldcs(reinterpret_cast<const uint4*>(zu + 8 * v));
-        pg[j] = __ldcs(reinterpret_cast<const uint4*>(zg + 8 * v));
-      } else {
-        pu[j] = pg[j] = make_uint4(0u, 0u, 0u, 0u);
-      }
-    }
-    float s[2] = {0.0f, 0.0f};
-#pragma unroll
-    for (int j = 0; j < VPT; ++j) {
-      float u[8], g[8];
-      unpack8(pu[j], u);
-      unpack8(pg[j], g);
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        s[0] += u[e];
-        s[1] += g[e];
-      }
-    }
-    block_sum<2>(s, sm, 0);
-    const float mu_u = s[0] * inv_h, mu_g = s[1] * inv_h;
-    float q[2] = {0.0f, 0.0f};
-#pragma unroll
-    for (int j = 0; j < VPT; ++j) {
-      if (threadIdx.x + kRowThreads * j < nvec) {
+      if (threadIdx.x + blockDim.x * j < nvec) {
         float u[8], g[8];
-        unpack8(pu[j], u);
-        unpack8(pg[j], g);
+        unpack8(cur.u[j], u);
+        unpack8(cur.g[j], g);
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
-          const float du = u[e] - mu_u, dg = g[e] - mu_g;
-          q[0] += du * du;
-          q[1] += dg * dg;
+          const float du = u[e] - cur.ku, dg = g[e] - cur.kg;
+          acc[0] += du;
+          acc[1] = fmaf(du, du, acc[1]);
+          acc[2] += dg;
+          acc[3] = fmaf(dg, dg, acc[3]);
         }
       }
     }
-    block_sum<2>(q, sm, 1);
-    const float rs_u = rsqrtf(q[0] * inv_h + eps), rs_g = rsqrtf(q[1] * inv_h + eps);
+    block_sum<4>(acc, sm, slot);
+    slot ^= 1;
+    const float m1u = acc[0] * inv_h, m1g = acc[2] * inv_h;
+    const float mu_u = cur.ku + m1u, mu_g = cur.kg + m1g;
+    const float rs_u = rsqrtf(fmaxf(acc[1] * inv_h - m1u * m1u, 0.0f) + eps);
+    const float rs_g = rsqrtf(fmaxf(acc[3] * inv_h - m1g * m1g, 0.0f) + eps);
+    const float cu = -mu_u * rs_u, cgg = -mu_g * rs_g;
     __nv_bfloat16* hrow = Hl + row * static_cast<int64_t>(H);
 #pragma unroll
     for (int j = 0; j < VPT; ++j) {
-      const int v = threadIdx.x + kRowThreads * j;
+      const int v = threadIdx.x + blockDim.x * j;
       if (v < nvec) {
         float u[8], g[8], wx[8], cx[8], wg[8], cg[8], h[8];
-        unpack8(pu[j], u);
-        unpack8(pg[j], g);
+        unpack8(cur.u[j], u);
+        unpack8(cur.g[j], g);
         const int64_t po = static_cast<int64_t>(r) * H + 8 * v;
         load8(gx + po, wx);
         load8(bx + po, cx);
@@ -187,33 +190,56 @@ __global__ void __launch_bounds__(kRowThreads, 2) ln_gate_fwd_kernel(
         load8(bg + po, cg);
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
-          const float a = (u[e] - mu_u) * rs_u * wx[e] + cx[e];
-          const float sg = (g[e] - mu_g) * rs_g * wg[e] + cg[e];
-          h[e] = a * (sg * sigmoid_f(sg));
+          const float a = fmaf(fmaf(u[e], rs_u, cu), wx[e], cx[e]);
+          const float sg = fmaf(fmaf(g[e], rs_g, cgg), wg[e], cg[e]);
+          h[e] = a * silu_fast(sg);
         }
         store8_stream(hrow + 8 * v, h);
       }
     }
     if (threadIdx.x == 0) stats[row] = make_float4(mu_u, rs_u, mu_g, rs_g);
+    cur = nxt;
   }
 }
 
 // ------------------------------------------------------------------ backward
 //
 // With x_u = (U - mu_u) * rstd_u, a = x_u*gx + bx, x_g likewise, s = x_g*gg + bg,
-// q = silu(s), Hl = a*q:  da = dHl*q, ds = dHl*a*sigmoid(s)*(1 + s*(1 - sigmoid(s))),
-// dx_u = da*gx, dU = rstd_u * (dx_u - mean(dx_u) - x_u*mean(dx_u*x_u)), and the
-// same for G with ds and gg.
+// q = silu(s), Hl = a*q:  da = dHl*q, ds = dHl*a*silu'(s) with
+// silu'(s) = sig(s) + s*sig(s)*(1 - sig(s)), dx_u = da*gx,
+// dU = rstd_u * (dx_u - mean(dx_u) - x_u*mean(dx_u*x_u)), and the same for G.
 //
 // Pass 1 (row sums): one CTA per row computes sum(dx_u), sum(dx_u*x_u),
-// sum(dx_g), sum(dx_g*x_g) -> rowsum[row].
-// Pass 2 (apply): a CTA owns 8*128 columns of one token position t and walks
-// all M rows of t: it writes dZ and keeps the column sums of dU, dG (db1),
-// da*x_u, da (norm_x grads), ds*x_g, ds (norm_gate grads) in registers, so
-// every column sum is complete in one CTA (fixed order, deterministic).
+// sum(dx_g), sum(dx_g*x_g) -> rowsum[row], loading the next row early.
+// Pass 2 (apply): a CTA owns a column block of one token position t and a
+// range of its rows: it writes dZ and sums, per column, dU, dG (db1),
+// da*x_u, da (norm_x grads), ds*x_g, ds (norm_gate grads) in registers; the
+// per-(t, row range) partial sums are added in a fixed order afterwards.
 
 template <int VPT>
-__global__ void __launch_bounds__(kRowThreads, 2) ln_gate_bwd_rowsum_kernel(
+struct GradFrag {
+  uint4 u[VPT], g[VPT], h[VPT];
+  float4 st;
+};
+
+template <int VPT>
+__device__ __forceinline__ void load_grow(GradFrag<VPT>& f, const __nv_bfloat16* zu, const __nv_bfloat16* dh,
+                                          const float4* st, int H, int nvec) {
+  const __nv_bfloat16* zg = zu + H;
+#pragma unroll
+  for (int j = 0; j < VPT; ++j) {
+    const int v = threadIdx.x + blockDim.x * j;
+    if (v < nvec) {
+      f.u[j] = __ldcs(reinterpret_cast<const uint4*>(zu + 8 * v));
+      f.g[j] = __ldcs(reinterpret_cast<const uint4*>(zg + 8 * v));
+      f.h[j] = __ldcs(reinterpret_cast<const uint4*>(dh + 8 * v));
+    }
+  }
+  f.st = *st;
+}
+
+template <int VPT>
+__global__ void __launch_bounds__(512, 1) ln_gate_bwd_rowsum_kernel(
     const __nv_bfloat16* __restrict__ Z, const float4* __restrict__ stats, const __nv_bfloat16* __restrict__ dHl,
     const __nv_bfloat16* __restrict__ gx, const __nv_bfloat16* __restrict__ bx, const __nv_bfloat16* __restrict__ gg,
     const __nv_bfloat16* __restrict__ bg, float4* __restrict__ rowsum, int64_t rows, int M, int L, int H,
@@ -221,32 +247,25 @@ __global__ void __launch_bounds__(kRowThreads, 2) ln_gate_bwd_rowsum_kernel(
   __shared__ float sm[2][kMaxRowWarps][4];
   if (block_aborted(err)) return;
   const int nvec = H >> 3;
+  const int64_t zstride = 2 * static_cast<int64_t>(H);
+  GradFrag<VPT> cur, nxt;
+  int64_t row = blockIdx.x;
+  if (row < rows) load_grow(cur, Z + row * zstride, dHl + row * H, stats + row, H, nvec);
   int slot = 0;
-  for (int64_t row = blockIdx.x; row < rows; row += gridDim.x) {
+  for (; row < rows; row += gridDim.x) {
+    const int64_t next = row + gridDim.x;
+    if (next < rows) load_grow(nxt, Z + next * zstride, dHl + next * H, stats + next, H, nvec);
     const int r = static_cast<int>(row / M) / L;
-    const float4 st = stats[row];
-    const __nv_bfloat16* zu = Z + row * (2 * static_cast<int64_t>(H));
-    const __nv_bfloat16* zg = zu + H;
-    const __nv_bfloat16* dh = dHl + row * static_cast<int64_t>(H);
-    uint4 pu[VPT], pg[VPT], ph[VPT];
-#pragma unroll
-    for (int j = 0; j < VPT; ++j) {
-      const int v = threadIdx.x + kRowThreads * j;
-      if (v < nvec) {
-        pu[j] = __ldcs(reinterpret_cast<const uint4*>(zu + 8 * v));
-        pg[j] = __ldcs(reinterpret_cast<const uint4*>(zg + 8 * v));
-        ph[j] = __ldcs(reinterpret_cast<const uint4*>(dh + 8 * v));
-      }
-    }
+    const float4 st = cur.st;
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int j = 0; j < VPT; ++j) {
-      const int v = threadIdx.x + kRowThreads * j;
+      const int v = threadIdx.x + blockDim.x * j;
       if (v < nvec) {
         float u[8], g[8], hv[8], wx[8], cx[8], wg[8], cg[8];
-        unpack8(pu[j], u);
-        unpack8(pg[j], g);
-        unpack8(ph[j], hv);
+        unpack8(cur.u[j], u);
+        unpack8(cur.g[j], g);
+        unpack8(cur.h[j], hv);
         const int64_t po = static_cast<int64_t>(r) * H + 8 * v;
         load8(gx + po, wx);
         load8(bx + po, cx);
@@ -255,123 +274,150 @@ __global__ void __launch_bounds__(kRowThreads, 2) ln_gate_bwd_rowsum_kernel(
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
           const float xu = (u[e] - st.x) * st.y, xg = (g[e] - st.z) * st.w;
-          const float a = xu * wx[e] + cx[e], sv = xg * wg[e] + cg[e];
-          const float sgm = sigmoid_f(sv);
-          const float dxu = hv[e] * (sv * sgm) * wx[e];
-          const float dxg = hv[e] * a * (sgm * (1.0f + sv * (1.0f - sgm))) * wg[e];
+          const float a = fmaf(xu, wx[e], cx[e]), sv = fmaf(xg, wg[e], cg[e]);
+          const float sg = sigmoid_fast(sv);
+          const float dxu = hv[e] * (sv * sg) * wx[e];
+          const float dxg = hv[e] * a * fmaf(sv * sg, 1.0f - sg, sg) * wg[e];
           acc[0] += dxu;
-          acc[1] += dxu * xu;
+          acc[1] = fmaf(dxu, xu, acc[1]);
           acc[2] += dxg;
-          acc[3] += dxg * xg;
+          acc[3] = fmaf(dxg, xg, acc[3]);
         }
       }
     }
     block_sum<4>(acc, sm, slot);
     slot ^= 1;
     if (threadIdx.x == 0) rowsum[row] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    cur = nxt;
   }
 }
 
-constexpr int kApplyThreads = 128;
-constexpr int kApplyCols = 8 * kApplyThreads;
+constexpr int kApplyVec = 4;   // columns per thread
+constexpr int kApplyRows = 4;  // rows in flight per thread
 
-__global__ void __launch_bounds__(kApplyThreads) ln_gate_bwd_apply_kernel(
+__device__ __forceinline__ void unpack4(const uint2 v, float (&f)[4]) {
+  const float2 a = unpack_bf16x2(v.x), b = unpack_bf16x2(v.y);
+  f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y;
+}
+
+__device__ __forceinline__ uint2 pack4(const float (&f)[4]) {
+  return make_uint2(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]));
+}
+
+// grid: (column blocks, T, row splits); block: cols_per_block / 4 threads.
+__global__ void __launch_bounds__(256) ln_gate_bwd_apply_kernel(
     const __nv_bfloat16* __restrict__ Z, const float4* __restrict__ stats, const float4* __restrict__ rowsum,
     const __nv_bfloat16* __restrict__ dHl, const __nv_bfloat16* __restrict__ gx, const __nv_bfloat16* __restrict__ bx,
     const __nv_bfloat16* __restrict__ gg, const __nv_bfloat16* __restrict__ bg, __nv_bfloat16* __restrict__ dZ,
-    __nv_bfloat16* __restrict__ d_b1, float* __restrict__ norm_part, int M, int L, int H, const uint32_t* err) {
+    float* __restrict__ part, int M, int L, int H, int cols_per_block, const uint32_t* err) {
   if (ld_volatile_u32(err) != 0u) return;
-  const int t = blockIdx.y;
+  const int t = blockIdx.y, rs = blockIdx.z, nsplit = gridDim.z;
   const int r = t / L;
-  const int c0 = blockIdx.x * kApplyCols + 8 * threadIdx.x;
-  if (c0 >= H) return;
+  const int c0 = blockIdx.x * cols_per_block + kApplyVec * threadIdx.x;
+  if (kApplyVec * threadIdx.x >= cols_per_block || c0 >= H) return;
   const float inv_h = 1.0f / static_cast<float>(H);
-  float wx[8], cx[8], wg[8], cg[8];
+  float wx[4], cx[4], wg[4], cg[4];
   {
     const int64_t po = static_cast<int64_t>(r) * H + c0;
-    load8(gx + po, wx);
-    load8(bx + po, cx);
-    load8(gg + po, wg);
-    load8(bg + po, cg);
+    unpack4(__ldg(reinterpret_cast<const uint2*>(gx + po)), wx);
+    unpack4(__ldg(reinterpret_cast<const uint2*>(bx + po)), cx);
+    unpack4(__ldg(reinterpret_cast<const uint2*>(gg + po)), wg);
+    unpack4(__ldg(reinterpret_cast<const uint2*>(bg + po)), cg);
   }
-  float s_du[8], s_dg[8], s_gx[8], s_bx[8], s_gg[8], s_bg[8];
+  float s_du[4], s_dg[4], s_gx[4], s_bx[4], s_gg[4], s_bg[4];
 #pragma unroll
-  for (int e = 0; e < 8; ++e) s_du[e] = s_dg[e] = s_gx[e] = s_bx[e] = s_gg[e] = s_bg[e] = 0.0f;
+  for (int e = 0; e < 4; ++e) s_du[e] = s_dg[e] = s_gx[e] = s_bx[e] = s_gg[e] = s_bg[e] = 0.0f;
+  const int rows_per = (M + nsplit - 1) / nsplit;
+  const int n_begin = rs * rows_per, n_end = min(M, n_begin + rows_per);
   const int64_t row0 = static_cast<int64_t>(t) * M;
   const int64_t zstride = 2 * static_cast<int64_t>(H);
-  constexpr int U = 2;  // rows in flight per thread
-  for (int n = 0; n < M; n += U) {
-    uint4 pu[U], pg[U], ph[U];
-    float4 st[U], rs[U];
+  for (int n = n_begin; n < n_end; n += kApplyRows) {
+    uint2 pu[kApplyRows], pg[kApplyRows], ph[kApplyRows];
+    float4 st[kApplyRows], rsm[kApplyRows];
 #pragma unroll
-    for (int i = 0; i < U; ++i) {
-      if (n + i < M) {
+    for (int i = 0; i < kApplyRows; ++i) {
+      if (n + i < n_end) {
         const int64_t row = row0 + n + i;
-        pu[i] = __ldcs(reinterpret_cast<const uint4*>(Z + row * zstride + c0));
-        pg[i] = __ldcs(reinterpret_cast<const uint4*>(Z + row * zstride + H + c0));
-        ph[i] = __ldcs(reinterpret_cast<const uint4*>(dHl + row * H + c0));
+        pu[i] = __ldcs(reinterpret_cast<const uint2*>(Z + row * zstride + c0));
+        pg[i] = __ldcs(reinterpret_cast<const uint2*>(Z + row * zstride + H + c0));
+        ph[i] = __ldcs(reinterpret_cast<const uint2*>(dHl + row * H + c0));
         st[i] = stats[row];
-        rs[i] = rowsum[row];
+        rsm[i] = rowsum[row];
       }
     }
 #pragma unroll
-    for (int i = 0; i < U; ++i) {
-      if (n + i < M) {
+    for (int i = 0; i < kApplyRows; ++i) {
+      if (n + i < n_end) {
         const int64_t row = row0 + n + i;
-        float u[8], g[8], hv[8], du[8], dg[8];
-        unpack8(pu[i], u);
-        unpack8(pg[i], g);
-        unpack8(ph[i], hv);
-        const float m1u = rs[i].x * inv_h, m2u = rs[i].y * inv_h;
-        const float m1g = rs[i].z * inv_h, m2g = rs[i].w * inv_h;
+        float u[4], g[4], hv[4], du[4], dg[4];
+        unpack4(pu[i], u);
+        unpack4(pg[i], g);
+        unpack4(ph[i], hv);
+        const float m1u = rsm[i].x * inv_h, m2u = rsm[i].y * inv_h;
+        const float m1g = rsm[i].z * inv_h, m2g = rsm[i].w * inv_h;
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
+        for (int e = 0; e < 4; ++e) {
           const float xu = (u[e] - st[i].x) * st[i].y, xg = (g[e] - st[i].z) * st[i].w;
-          const float a = xu * wx[e] + cx[e], sv = xg * wg[e] + cg[e];
-          const float sgm = sigmoid_f(sv);
-          const float da = hv[e] * (sv * sgm);
-          const float ds = hv[e] * a * (sgm * (1.0f + sv * (1.0f - sgm)));
-          du[e] = st[i].y * (da * wx[e] - m1u - xu * m2u);
-          dg[e] = st[i].w * (ds * wg[e] - m1g - xg * m2g);
+          const float a = fmaf(xu, wx[e], cx[e]), sv = fmaf(xg, wg[e], cg[e]);
+          const float sg = sigmoid_fast(sv);
+          const float da = hv[e] * (sv * sg);
+          const float ds = hv[e] * a * fmaf(sv * sg, 1.0f - sg, sg);
+          du[e] = st[i].y * (fmaf(da, wx[e], -m1u) - xu * m2u);
+          dg[e] = st[i].w * (fmaf(ds, wg[e], -m1g) - xg * m2g);
           s_du[e] += du[e];
           s_dg[e] += dg[e];
-          s_gx[e] += da * xu;
+          s_gx[e] = fmaf(da, xu, s_gx[e]);
           s_bx[e] += da;
-          s_gg[e] += ds * xg;
+          s_gg[e] = fmaf(ds, xg, s_gg[e]);
           s_bg[e] += ds;
         }
-        store8_stream(dZ + row * zstride + c0, du);
-        store8_stream(dZ + row * zstride + H + c0, dg);
+        __stcs(reinterpret_cast<uint2*>(dZ + row * zstride + c0), pack4(du));
+        __stcs(reinterpret_cast<uint2*>(dZ + row * zstride + H + c0), pack4(dg));
       }
     }
   }
-  store8(d_b1 + static_cast<int64_t>(t) * 2 * H + c0, s_du);
-  store8(d_b1 + static_cast<int64_t>(t) * 2 * H + H + c0, s_dg);
-  float* np = norm_part + static_cast<int64_t>(t) * 4 * H + c0;
-#pragma unroll
-  for (int e = 0; e < 8; ++e) {
-    np[e] = s_gx[e];
-    np[H + e] = s_bx[e];
-    np[2 * H + e] = s_gg[e];
-    np[3 * H + e] = s_bg[e];
-  }
+  // part[t][rs][q][c], q: dU, dG, da*x_u, da, ds*x_g, ds
+  float* pp = part + (static_cast<int64_t>(t) * nsplit + rs) * 6 * H + c0;
+  *reinterpret_cast<float4*>(pp + 0 * static_cast<int64_t>(H)) = make_float4(s_du[0], s_du[1], s_du[2], s_du[3]);
+  *reinterpret_cast<float4*>(pp + 1 * static_cast<int64_t>(H)) = make_float4(s_dg[0], s_dg[1], s_dg[2], s_dg[3]);
+  *reinterpret_cast<float4*>(pp + 2 * static_cast<int64_t>(H)) = make_float4(s_gx[0], s_gx[1], s_gx[2], s_gx[3]);
+  *reinterpret_cast<float4*>(pp + 3 * static_cast<int64_t>(H)) = make_float4(s_bx[0], s_bx[1], s_bx[2], s_bx[3]);
+  *reinterpret_cast<float4*>(pp + 4 * static_cast<int64_t>(H)) = make_float4(s_gg[0], s_gg[1], s_gg[2], s_gg[3]);
+  *reinterpret_cast<float4*>(pp + 5 * static_cast<int64_t>(H)) = make_float4(s_bg[0], s_bg[1], s_bg[2], s_bg[3]);
 }
 
-// Norm gradients of rank r: sum of its L slices' column sums, in slice order.
-__global__ void norm_reduce_kernel(const float* __restrict__ norm_part, __nv_bfloat16* __restrict__ d_nx_w,
-                                   __nv_bfloat16* __restrict__ d_nx_b, __nv_bfloat16* __restrict__ d_ng_w,
-                                   __nv_bfloat16* __restrict__ d_ng_b, int P, int L, int H, const uint32_t* err) {
+// db1 [T, 2H] and the norm gradients [P, H] from the partials, summed in a
+// fixed order (row splits, then the rank's slices): reruns are bit-identical.
+__global__ void grad_reduce_kernel(const float* __restrict__ part, __nv_bfloat16* __restrict__ d_b1,
+                                   __nv_bfloat16* __restrict__ d_nx_w, __nv_bfloat16* __restrict__ d_nx_b,
+                                   __nv_bfloat16* __restrict__ d_ng_w, __nv_bfloat16* __restrict__ d_ng_b, int P,
+                                   int L, int H, int nsplit, const uint32_t* err) {
   if (ld_volatile_u32(err) != 0u) return;
-  const int64_t n = static_cast<int64_t>(P) * 4 * H;
-  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
+  const int T = P * L;
+  const int64_t n_b1 = static_cast<int64_t>(T) * 2 * H;
+  const int64_t n_norm = static_cast<int64_t>(P) * 4 * H;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n_b1 + n_norm;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const int r = static_cast<int>(i / (4 * H));
-    const int q = static_cast<int>((i / H) % 4);  // 0: nx_w, 1: nx_b, 2: ng_w, 3: ng_b
-    const int c = static_cast<int>(i % H);
-    float s = 0.0f;
-    for (int l = 0; l < L; ++l) s += norm_part[(static_cast<int64_t>(r * L + l) * 4 + q) * H + c];
-    __nv_bfloat16* out = q == 0 ? d_nx_w : q == 1 ? d_nx_b : q == 2 ? d_ng_w : d_ng_b;
-    out[static_cast<int64_t>(r) * H + c] = __float2bfloat16_rn(s);
+    if (i < n_b1) {
+      const int t = static_cast<int>(i / (2 * H));
+      const int c2 = static_cast<int>(i - static_cast<int64_t>(t) * 2 * H);
+      const int q = c2 >= H ? 1 : 0;
+      const int c = c2 - q * H;
+      float s = 0.0f;
+      for (int k = 0; k < nsplit; ++k) s += part[((static_cast<int64_t>(t) * nsplit + k) * 6 + q) * H + c];
+      d_b1[i] = __float2bfloat16_rn(s);
+    } else {
+      const int64_t j = i - n_b1;
+      const int r = static_cast<int>(j / (4 * H));
+      const int q = static_cast<int>((j / H) % 4);  // 0: nx_w, 1: nx_b, 2: ng_w, 3: ng_b
+      const int c = static_cast<int>(j % H);
+      float s = 0.0f;
+      for (int l = 0; l < L; ++l)
+        for (int k = 0; k < nsplit; ++k)
+          s += part[((static_cast<int64_t>(r * L + l) * nsplit + k) * 6 + 2 + q) * H + c];
+      __nv_bfloat16* out = q == 0 ? d_nx_w : q == 1 ? d_nx_b : q == 2 ? d_ng_w : d_ng_b;
+      out[static_cast<int64_t>(r) * H + c] = __float2bfloat16_rn(s);
+    }
   }
 }
 
@@ -482,44 +528,60 @@ cudaError_t launch_ln_gate_bwd_rowsum(const void* Z, const void* stats, const vo
                                       const void* nx_b, const void* ng_w, const void* ng_b, void* rowsum, int T, int M,
                                       int L, int H, const DeviceInfo& dev, cudaStream_t s) {
   const int64_t rows = static_cast<int64_t>(T) * M;
-  const int vpt = (H / 8 + kRowThreads - 1) / kRowThreads;
+  const int nvec = H / 8;
+  // VPT vectors per thread, at most 512 threads
+  const int vpt = nvec <= 512 ? 1 : nvec <= 1024 ? 2 : nvec <= 2048 ? 4 : 0;
+  if (vpt == 0) return cudaErrorInvalidValue;
+  int threads = (nvec + vpt - 1) / vpt;
+  threads = ((threads + 31) / 32) * 32;
   auto run = [&](auto kern) {
-    const int grid = grid_for(dev, reinterpret_cast<const void*>(kern), kRowThreads, 0, rows);
-    kern<<<grid, kRowThreads, 0, s>>>(static_cast<const __nv_bfloat16*>(Z), static_cast<const float4*>(stats),
-                                      static_cast<const __nv_bfloat16*>(dHl), static_cast<const __nv_bfloat16*>(nx_w),
-                                      static_cast<const __nv_bfloat16*>(nx_b), static_cast<const __nv_bfloat16*>(ng_w),
-                                      static_cast<const __nv_bfloat16*>(ng_b), static_cast<float4*>(rowsum), rows, M,
-                                      L, H, dev.err);
+    const int grid = grid_for(dev, reinterpret_cast<const void*>(kern), threads, 0, rows);
+    kern<<<grid, threads, 0, s>>>(static_cast<const __nv_bfloat16*>(Z), static_cast<const float4*>(stats),
+                                  static_cast<const __nv_bfloat16*>(dHl), static_cast<const __nv_bfloat16*>(nx_w),
+                                  static_cast<const __nv_bfloat16*>(nx_b), static_cast<const __nv_bfloat16*>(ng_w),
+                                  static_cast<const __nv_bfloat16*>(ng_b), static_cast<float4*>(rowsum), rows, M, L,
+                                  H, dev.err);
     return cudaGetLastError();
   };
-  if (vpt <= 1) return run(ln_gate_bwd_rowsum_kernel<1>);
-  if (vpt <= 2) return run(ln_gate_bwd_rowsum_kernel<2>);
-  if (vpt <= 4) return run(ln_gate_bwd_rowsum_kernel<4>);
-  return cudaErrorInvalidValue;
+  if (vpt == 1) return run(ln_gate_bwd_rowsum_kernel<1>);
+  if (vpt == 2) return run(ln_gate_bwd_rowsum_kernel<2>);
+  return run(ln_gate_bwd_rowsum_kernel<4>);
+}
+
+int ffn_bwd_row_splits(int T, int M) {
+  // enough (t, column block, row range) items to fill the GPU several times over
+  int splits = (2048 + T - 1) / T;
+  const int cap = (M + 63) / 64;
+  if (splits > cap) splits = cap;
+  return splits < 1 ? 1 : splits;
 }
 
 cudaError_t launch_ln_gate_bwd_apply(const void* Z, const void* stats, const void* rowsum, const void* dHl,
                                      const void* nx_w, const void* nx_b, const void* ng_w, const void* ng_b, void* dZ,
-                                     void* d_b1, float* norm_part, int T, int M, int L, int H, const DeviceInfo& dev,
+                                     float* part, int T, int M, int L, int H, int nsplit, const DeviceInfo& dev,
                                      cudaStream_t s) {
-  dim3 grid((H + kApplyCols - 1) / kApplyCols, T);
-  ln_gate_bwd_apply_kernel<<<grid, kApplyThreads, 0, s>>>(
+  // balanced column blocks of at most 1024 columns (256 threads x 4 columns)
+  const int nblk = (H + 1023) / 1024;
+  int cols = (H + nblk - 1) / nblk;
+  cols = ((cols + 4 * 32 - 1) / (4 * 32)) * (4 * 32);
+  const int threads = cols / kApplyVec;
+  dim3 grid(nblk, T, nsplit);
+  ln_gate_bwd_apply_kernel<<<grid, threads, 0, s>>>(
       static_cast<const __nv_bfloat16*>(Z), static_cast<const float4*>(stats), static_cast<const float4*>(rowsum),
       static_cast<const __nv_bfloat16*>(dHl), static_cast<const __nv_bfloat16*>(nx_w),
       static_cast<const __nv_bfloat16*>(nx_b), static_cast<const __nv_bfloat16*>(ng_w),
-      static_cast<const __nv_bfloat16*>(ng_b), static_cast<__nv_bfloat16*>(dZ), static_cast<__nv_bfloat16*>(d_b1),
-      norm_part, M, L, H, dev.err);
+      static_cast<const __nv_bfloat16*>(ng_b), static_cast<__nv_bfloat16*>(dZ), part, M, L, H, cols, dev.err);
   return cudaGetLastError();
 }
 
-cudaError_t launch_norm_reduce(const float* norm_part, void* d_nx_w, void* d_nx_b, void* d_ng_w, void* d_ng_b, int P,
-                               int L, int H, const DeviceInfo& dev, cudaStream_t s) {
-  const int64_t n = static_cast<int64_t>(P) * 4 * H;
+cudaError_t launch_grad_reduce(const float* part, void* d_b1, void* d_nx_w, void* d_nx_b, void* d_ng_w, void* d_ng_b,
+                               int P, int L, int H, int nsplit, const DeviceInfo& dev, cudaStream_t s) {
+  const int64_t n = static_cast<int64_t>(P) * L * 2 * H + static_cast<int64_t>(P) * 4 * H;
   int64_t blocks = (n + 255) / 256;
   if (blocks > 8 * dev.num_sms) blocks = 8 * dev.num_sms;
-  norm_reduce_kernel<<<static_cast<int>(blocks), 256, 0, s>>>(
-      norm_part, static_cast<__nv_bfloat16*>(d_nx_w), static_cast<__nv_bfloat16*>(d_nx_b),
-      static_cast<__nv_bfloat16*>(d_ng_w), static_cast<__nv_bfloat16*>(d_ng_b), P, L, H, dev.err);
+  grad_reduce_kernel<<<static_cast<int>(blocks), 256, 0, s>>>(
+      part, static_cast<__nv_bfloat16*>(d_b1), static_cast<__nv_bfloat16*>(d_nx_w), static_cast<__nv_bfloat16*>(d_nx_b),
+      static_cast<__nv_bfloat16*>(d_ng_w), static_cast<__nv_bfloat16*>(d_ng_b), P, L, H, nsplit, dev.err);
   return cudaGetLastError();
 }
 
