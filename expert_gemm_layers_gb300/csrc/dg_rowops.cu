@@ -16,20 +16,8 @@ namespace dg {
 namespace {
 
 constexpr int kMaxRowWarps = 16;  // row kernels use up to 512 threads
-constexpr int kRowThreads = 256;  // threads of the per-row kernels
 
 __device__ __forceinline__ void unpack8(const uint4 v, float (&f)[8]) {
-  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    const float2 t = unpack_bf16x2(w[e]);
-    f[2 * e] = t.x;
-    f[2 * e + 1] = t.y;
-  }
-}
-
-__device__ __forceinline__ void load8(const __nv_bfloat16* p, float (&f)[8]) {
-  const uint4 v = __ldg(reinterpret_cast<const uint4*>(p));
   const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
   for (int e = 0; e < 4; ++e) {
@@ -99,68 +87,107 @@ __device__ __forceinline__ void block_sum(float (&v)[N], float (*sm)[kMaxRowWarp
   }
 }
 
+// Per-thread asynchronous copies into shared memory (cp.async): a thread
+// copies exactly the bytes it will read back itself, so a multi-stage ring
+// needs no barrier for the copies, only cp.async.wait_group.
+__device__ __forceinline__ void cp_async16(void* dst, const void* src, bool valid) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src),
+               "r"(valid ? 16 : 0)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// bf16x2-packed affine parameters of one 8-column vector (held for all rows).
+struct Affine8 {
+  uint4 wx, cx, wg, cg;
+};
+
+__device__ __forceinline__ Affine8 load_affine8(const __nv_bfloat16* gx, const __nv_bfloat16* bx,
+                                                const __nv_bfloat16* gg, const __nv_bfloat16* bg, int64_t off) {
+  Affine8 a;
+  a.wx = __ldg(reinterpret_cast<const uint4*>(gx + off));
+  a.cx = __ldg(reinterpret_cast<const uint4*>(bx + off));
+  a.wg = __ldg(reinterpret_cast<const uint4*>(gg + off));
+  a.cg = __ldg(reinterpret_cast<const uint4*>(bg + off));
+  return a;
+}
+
 // ------------------------------------------------------------------ forward
 //
-// One CTA per row (grid-stride).  Thread i keeps 8-column vectors
-// i, i + blockDim, ... of U and G as packed bf16 in registers, and loads the
-// CTA's next row while it finishes the current one.  The row statistics use
-// the shifted-data single pass (Chan, Golub & LeVeque, "Algorithms for
-// computing the sample variance"): with K the row's first element,
-// mean = K + S1/H and var = S2/H - (S1/H)^2 where S1 = sum(x-K),
+// A CTA walks rows (grid-stride) of ONE rank's token positions, so each
+// thread keeps the affine parameters of its columns in registers.  Rows are
+// staged through a kStages-deep shared-memory ring by per-thread cp.async.
+// Thread i owns 8-column vectors i, i + blockDim, ... of U and G.  The row
+// statistics use the shifted-data single pass (Chan, Golub & LeVeque,
+// "Algorithms for computing the sample variance"): with K the row's first
+// element, mean = K + S1/H and var = S2/H - (S1/H)^2 where S1 = sum(x-K),
 // S2 = sum((x-K)^2); K is a sample of the row, so the subtraction does not
 // cancel catastrophically, and a constant row gives exactly var = 0.
 
-template <int VPT>
-struct RowFrag {
-  uint4 u[VPT], g[VPT];
-  float ku, kg;
-};
+constexpr int kFwdStages = 3;
 
-template <int VPT>
-__device__ __forceinline__ void load_zrow(RowFrag<VPT>& f, const __nv_bfloat16* zu, int H, int nvec) {
-  const __nv_bfloat16* zg = zu + H;
-#pragma unroll
-  for (int j = 0; j < VPT; ++j) {
-    const int v = threadIdx.x + blockDim.x * j;
-    if (v < nvec) {
-      f.u[j] = __ldcs(reinterpret_cast<const uint4*>(zu + 8 * v));
-      f.g[j] = __ldcs(reinterpret_cast<const uint4*>(zg + 8 * v));
-    } else {
-      f.u[j] = f.g[j] = make_uint4(0u, 0u, 0u, 0u);
-    }
-  }
-  f.ku = __bfloat162float(zu[0]);
-  f.kg = __bfloat162float(zg[0]);
-}
-
-template <int VPT>
-__global__ void __launch_bounds__(kRowThreads, 2) ln_gate_fwd_kernel(
+template <int NT, int VPT>
+__global__ void __launch_bounds__(NT, 512 / NT) ln_gate_fwd_kernel(
     const __nv_bfloat16* __restrict__ Z, const __nv_bfloat16* __restrict__ gx, const __nv_bfloat16* __restrict__ bx,
     const __nv_bfloat16* __restrict__ gg, const __nv_bfloat16* __restrict__ bg, __nv_bfloat16* __restrict__ Hl,
-    float4* __restrict__ stats, int64_t rows, int M, int L, int H, float eps, const uint32_t* err) {
+    float4* __restrict__ stats, int M, int L, int H, int ctas_per_rank, float eps, const uint32_t* err) {
+  extern __shared__ uint4 ring[];  // [kFwdStages][VPT][2][NT]
   __shared__ float sm[2][kMaxRowWarps][4];
   if (block_aborted(err)) return;
   const int nvec = H >> 3;
   const float inv_h = 1.0f / static_cast<float>(H);
   const int64_t zstride = 2 * static_cast<int64_t>(H);
-  RowFrag<VPT> cur, nxt;
-  int64_t row = blockIdx.x;
-  if (row < rows) load_zrow(cur, Z + row * zstride, H, nvec);
+  const int r = blockIdx.x / ctas_per_rank;
+  const int64_t rank_rows = static_cast<int64_t>(L) * M;
+  const int64_t first = static_cast<int64_t>(r) * rank_rows;
+  const int64_t stride = ctas_per_rank;
+  const int64_t n_mine = (rank_rows - (blockIdx.x % ctas_per_rank) + stride - 1) / stride;
+  const int64_t row0 = first + (blockIdx.x % ctas_per_rank);
+
+  Affine8 aff[VPT];
+#pragma unroll
+  for (int j = 0; j < VPT; ++j) {
+    const int v = threadIdx.x + NT * j;
+    aff[j] = load_affine8(gx, bx, gg, bg, static_cast<int64_t>(r) * H + 8 * (v < nvec ? v : 0));
+  }
+  auto issue = [&](int64_t i) {
+    if (i < n_mine) {
+      const __nv_bfloat16* zu = Z + (row0 + i * stride) * zstride;
+      uint4* st = ring + (i % kFwdStages) * (VPT * 2 * NT);
+#pragma unroll
+      for (int j = 0; j < VPT; ++j) {
+        const int v = threadIdx.x + NT * j;
+        const bool ok = v < nvec;
+        cp_async16(st + (2 * j) * NT + threadIdx.x, zu + 8 * (ok ? v : 0), ok);
+        cp_async16(st + (2 * j + 1) * NT + threadIdx.x, zu + H + 8 * (ok ? v : 0), ok);
+      }
+    }
+    cp_async_commit();
+  };
+#pragma unroll
+  for (int i = 0; i < kFwdStages - 1; ++i) issue(i);
   int slot = 0;
-  for (; row < rows; row += gridDim.x) {
-    const int64_t next = row + gridDim.x;
-    if (next < rows) load_zrow(nxt, Z + next * zstride, H, nvec);
-    const int r = static_cast<int>(row / M) / L;
+  for (int64_t i = 0; i < n_mine; ++i) {
+    issue(i + kFwdStages - 1);
+    cp_async_wait<kFwdStages - 1>();
+    const int64_t row = row0 + i * stride;
+    const uint4* st = ring + (i % kFwdStages) * (VPT * 2 * NT);
+    const float ku = __bfloat162float(Z[row * zstride]);
+    const float kg = __bfloat162float(Z[row * zstride + H]);
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int j = 0; j < VPT; ++j) {
-      if (threadIdx.x + blockDim.x * j < nvec) {
-        float u[8], g[8];
-        unpack8(cur.u[j], u);
-        unpack8(cur.g[j], g);
+      float u[8], g[8];
+      unpack8(st[(2 * j) * NT + threadIdx.x], u);
+      unpack8(st[(2 * j + 1) * NT + threadIdx.x], g);
+      if (threadIdx.x + NT * j < nvec) {
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
-          const float du = u[e] - cur.ku, dg = g[e] - cur.kg;
+          const float du = u[e] - ku, dg = g[e] - kg;
           acc[0] += du;
           acc[1] = fmaf(du, du, acc[1]);
           acc[2] += dg;
@@ -171,23 +198,22 @@ __global__ void __launch_bounds__(kRowThreads, 2) ln_gate_fwd_kernel(
     block_sum<4>(acc, sm, slot);
     slot ^= 1;
     const float m1u = acc[0] * inv_h, m1g = acc[2] * inv_h;
-    const float mu_u = cur.ku + m1u, mu_g = cur.kg + m1g;
+    const float mu_u = ku + m1u, mu_g = kg + m1g;
     const float rs_u = rsqrtf(fmaxf(acc[1] * inv_h - m1u * m1u, 0.0f) + eps);
     const float rs_g = rsqrtf(fmaxf(acc[3] * inv_h - m1g * m1g, 0.0f) + eps);
     const float cu = -mu_u * rs_u, cgg = -mu_g * rs_g;
     __nv_bfloat16* hrow = Hl + row * static_cast<int64_t>(H);
 #pragma unroll
     for (int j = 0; j < VPT; ++j) {
-      const int v = threadIdx.x + blockDim.x * j;
+      const int v = threadIdx.x + NT * j;
       if (v < nvec) {
         float u[8], g[8], wx[8], cx[8], wg[8], cg[8], h[8];
-        unpack8(cur.u[j], u);
-        unpack8(cur.g[j], g);
-        const int64_t po = static_cast<int64_t>(r) * H + 8 * v;
-        load8(gx + po, wx);
-        load8(bx + po, cx);
-        load8(gg + po, wg);
-        load8(bg + po, cg);
+        unpack8(st[(2 * j) * NT + threadIdx.x], u);
+        unpack8(st[(2 * j + 1) * NT + threadIdx.x], g);
+        unpack8(aff[j].wx, wx);
+        unpack8(aff[j].cx, cx);
+        unpack8(aff[j].wg, wg);
+        unpack8(aff[j].cg, cg);
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
           const float a = fmaf(fmaf(u[e], rs_u, cu), wx[e], cx[e]);
@@ -198,8 +224,8 @@ __global__ void __launch_bounds__(kRowThreads, 2) ln_gate_fwd_kernel(
       }
     }
     if (threadIdx.x == 0) stats[row] = make_float4(mu_u, rs_u, mu_g, rs_g);
-    cur = nxt;
   }
+  cp_async_wait<0>();
 }
 
 // ------------------------------------------------------------------ backward
@@ -210,70 +236,79 @@ __global__ void __launch_bounds__(kRowThreads, 2) ln_gate_fwd_kernel(
 // dU = rstd_u * (dx_u - mean(dx_u) - x_u*mean(dx_u*x_u)), and the same for G.
 //
 // Pass 1 (row sums): one CTA per row computes sum(dx_u), sum(dx_u*x_u),
-// sum(dx_g), sum(dx_g*x_g) -> rowsum[row], loading the next row early.
+// sum(dx_g), sum(dx_g*x_g) -> rowsum[row]; rows staged like the forward.
 // Pass 2 (apply): a CTA owns a column block of one token position t and a
 // range of its rows: it writes dZ and sums, per column, dU, dG (db1),
 // da*x_u, da (norm_x grads), ds*x_g, ds (norm_gate grads) in registers; the
 // per-(t, row range) partial sums are added in a fixed order afterwards.
 
-template <int VPT>
-struct GradFrag {
-  uint4 u[VPT], g[VPT], h[VPT];
-  float4 st;
-};
+constexpr int kBwdStages = 3;
 
-template <int VPT>
-__device__ __forceinline__ void load_grow(GradFrag<VPT>& f, const __nv_bfloat16* zu, const __nv_bfloat16* dh,
-                                          const float4* st, int H, int nvec) {
-  const __nv_bfloat16* zg = zu + H;
-#pragma unroll
-  for (int j = 0; j < VPT; ++j) {
-    const int v = threadIdx.x + blockDim.x * j;
-    if (v < nvec) {
-      f.u[j] = __ldcs(reinterpret_cast<const uint4*>(zu + 8 * v));
-      f.g[j] = __ldcs(reinterpret_cast<const uint4*>(zg + 8 * v));
-      f.h[j] = __ldcs(reinterpret_cast<const uint4*>(dh + 8 * v));
-    }
-  }
-  f.st = *st;
-}
-
-template <int VPT>
-__global__ void __launch_bounds__(512, 1) ln_gate_bwd_rowsum_kernel(
+template <int NT, int VPT>
+__global__ void __launch_bounds__(NT, 512 / NT) ln_gate_bwd_rowsum_kernel(
     const __nv_bfloat16* __restrict__ Z, const float4* __restrict__ stats, const __nv_bfloat16* __restrict__ dHl,
     const __nv_bfloat16* __restrict__ gx, const __nv_bfloat16* __restrict__ bx, const __nv_bfloat16* __restrict__ gg,
-    const __nv_bfloat16* __restrict__ bg, float4* __restrict__ rowsum, int64_t rows, int M, int L, int H,
+    const __nv_bfloat16* __restrict__ bg, float4* __restrict__ rowsum, int M, int L, int H, int ctas_per_rank,
     const uint32_t* err) {
+  extern __shared__ uint4 ring[];  // [kBwdStages][VPT][3][NT]
   __shared__ float sm[2][kMaxRowWarps][4];
   if (block_aborted(err)) return;
   const int nvec = H >> 3;
   const int64_t zstride = 2 * static_cast<int64_t>(H);
-  GradFrag<VPT> cur, nxt;
-  int64_t row = blockIdx.x;
-  if (row < rows) load_grow(cur, Z + row * zstride, dHl + row * H, stats + row, H, nvec);
+  const int r = blockIdx.x / ctas_per_rank;
+  const int64_t rank_rows = static_cast<int64_t>(L) * M;
+  const int64_t stride = ctas_per_rank;
+  const int64_t n_mine = (rank_rows - (blockIdx.x % ctas_per_rank) + stride - 1) / stride;
+  const int64_t row0 = static_cast<int64_t>(r) * rank_rows + (blockIdx.x % ctas_per_rank);
+
+  Affine8 aff[VPT];
+#pragma unroll
+  for (int j = 0; j < VPT; ++j) {
+    const int v = threadIdx.x + NT * j;
+    aff[j] = load_affine8(gx, bx, gg, bg, static_cast<int64_t>(r) * H + 8 * (v < nvec ? v : 0));
+  }
+  auto issue = [&](int64_t i) {
+    if (i < n_mine) {
+      const int64_t row = row0 + i * stride;
+      const __nv_bfloat16* zu = Z + row * zstride;
+      const __nv_bfloat16* dh = dHl + row * H;
+      uint4* st = ring + (i % kBwdStages) * (VPT * 3 * NT);
+#pragma unroll
+      for (int j = 0; j < VPT; ++j) {
+        const int v = threadIdx.x + NT * j;
+        const bool ok = v < nvec;
+        const int vv = ok ? v : 0;
+        cp_async16(st + (3 * j) * NT + threadIdx.x, zu + 8 * vv, ok);
+        cp_async16(st + (3 * j + 1) * NT + threadIdx.x, zu + H + 8 * vv, ok);
+        cp_async16(st + (3 * j + 2) * NT + threadIdx.x, dh + 8 * vv, ok);
+      }
+    }
+    cp_async_commit();
+  };
+#pragma unroll
+  for (int i = 0; i < kBwdStages - 1; ++i) issue(i);
   int slot = 0;
-  for (; row < rows; row += gridDim.x) {
-    const int64_t next = row + gridDim.x;
-    if (next < rows) load_grow(nxt, Z + next * zstride, dHl + next * H, stats + next, H, nvec);
-    const int r = static_cast<int>(row / M) / L;
-    const float4 st = cur.st;
+  for (int64_t i = 0; i < n_mine; ++i) {
+    issue(i + kBwdStages - 1);
+    const int64_t row = row0 + i * stride;
+    const float4 sr = stats[row];
+    cp_async_wait<kBwdStages - 1>();
+    const uint4* st = ring + (i % kBwdStages) * (VPT * 3 * NT);
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int j = 0; j < VPT; ++j) {
-      const int v = threadIdx.x + blockDim.x * j;
-      if (v < nvec) {
+      if (threadIdx.x + NT * j < nvec) {
         float u[8], g[8], hv[8], wx[8], cx[8], wg[8], cg[8];
-        unpack8(cur.u[j], u);
-        unpack8(cur.g[j], g);
-        unpack8(cur.h[j], hv);
-        const int64_t po = static_cast<int64_t>(r) * H + 8 * v;
-        load8(gx + po, wx);
-        load8(bx + po, cx);
-        load8(gg + po, wg);
-        load8(bg + po, cg);
+        unpack8(st[(3 * j) * NT + threadIdx.x], u);
+        unpack8(st[(3 * j + 1) * NT + threadIdx.x], g);
+        unpack8(st[(3 * j + 2) * NT + threadIdx.x], hv);
+        unpack8(aff[j].wx, wx);
+        unpack8(aff[j].cx, cx);
+        unpack8(aff[j].wg, wg);
+        unpack8(aff[j].cg, cg);
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
-          const float xu = (u[e] - st.x) * st.y, xg = (g[e] - st.z) * st.w;
+          const float xu = (u[e] - sr.x) * sr.y, xg = (g[e] - sr.z) * sr.w;
           const float a = fmaf(xu, wx[e], cx[e]), sv = fmaf(xg, wg[e], cg[e]);
           const float sg = sigmoid_fast(sv);
           const float dxu = hv[e] * (sv * sg) * wx[e];
@@ -288,102 +323,104 @@ __global__ void __launch_bounds__(512, 1) ln_gate_bwd_rowsum_kernel(
     block_sum<4>(acc, sm, slot);
     slot ^= 1;
     if (threadIdx.x == 0) rowsum[row] = make_float4(acc[0], acc[1], acc[2], acc[3]);
-    cur = nxt;
   }
+  cp_async_wait<0>();
 }
 
-constexpr int kApplyVec = 4;   // columns per thread
-constexpr int kApplyRows = 4;  // rows in flight per thread
+constexpr int kApplyThreads = 128;  // 8 columns per thread
+constexpr int kApplyStages = 6;
 
-__device__ __forceinline__ void unpack4(const uint2 v, float (&f)[4]) {
-  const float2 a = unpack_bf16x2(v.x), b = unpack_bf16x2(v.y);
-  f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y;
-}
-
-__device__ __forceinline__ uint2 pack4(const float (&f)[4]) {
-  return make_uint2(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]));
-}
-
-// grid: (column blocks, T, row splits); block: cols_per_block / 4 threads.
-__global__ void __launch_bounds__(256) ln_gate_bwd_apply_kernel(
+// grid: (column blocks of 8*kApplyThreads, T, row splits).
+__global__ void __launch_bounds__(kApplyThreads) ln_gate_bwd_apply_kernel(
     const __nv_bfloat16* __restrict__ Z, const float4* __restrict__ stats, const float4* __restrict__ rowsum,
     const __nv_bfloat16* __restrict__ dHl, const __nv_bfloat16* __restrict__ gx, const __nv_bfloat16* __restrict__ bx,
     const __nv_bfloat16* __restrict__ gg, const __nv_bfloat16* __restrict__ bg, __nv_bfloat16* __restrict__ dZ,
-    float* __restrict__ part, int M, int L, int H, int cols_per_block, const uint32_t* err) {
+    float* __restrict__ part, int M, int L, int H, const uint32_t* err) {
+  // per stage and thread: u, g, dh (16 B each), stats, rowsum (16 B each)
+  extern __shared__ uint4 ring_raw[];
+  auto ring = reinterpret_cast<uint4(*)[5][kApplyThreads]>(ring_raw);
   if (ld_volatile_u32(err) != 0u) return;
-  const int t = blockIdx.y, rs = blockIdx.z, nsplit = gridDim.z;
+  const int t = blockIdx.y, rsp = blockIdx.z, nsplit = gridDim.z;
   const int r = t / L;
-  const int c0 = blockIdx.x * cols_per_block + kApplyVec * threadIdx.x;
-  if (kApplyVec * threadIdx.x >= cols_per_block || c0 >= H) return;
+  const int c0 = blockIdx.x * (8 * kApplyThreads) + 8 * threadIdx.x;
+  const bool active = c0 < H;
+  const int cc = active ? c0 : 0;
   const float inv_h = 1.0f / static_cast<float>(H);
-  float wx[4], cx[4], wg[4], cg[4];
+  float wx[8], cx[8], wg[8], cg[8];
   {
-    const int64_t po = static_cast<int64_t>(r) * H + c0;
-    unpack4(__ldg(reinterpret_cast<const uint2*>(gx + po)), wx);
-    unpack4(__ldg(reinterpret_cast<const uint2*>(bx + po)), cx);
-    unpack4(__ldg(reinterpret_cast<const uint2*>(gg + po)), wg);
-    unpack4(__ldg(reinterpret_cast<const uint2*>(bg + po)), cg);
+    const Affine8 a = load_affine8(gx, bx, gg, bg, static_cast<int64_t>(r) * H + cc);
+    unpack8(a.wx, wx);
+    unpack8(a.cx, cx);
+    unpack8(a.wg, wg);
+    unpack8(a.cg, cg);
   }
-  float s_du[4], s_dg[4], s_gx[4], s_bx[4], s_gg[4], s_bg[4];
+  float s_du[8], s_dg[8], s_gx[8], s_bx[8], s_gg[8], s_bg[8];
 #pragma unroll
-  for (int e = 0; e < 4; ++e) s_du[e] = s_dg[e] = s_gx[e] = s_bx[e] = s_gg[e] = s_bg[e] = 0.0f;
+  for (int e = 0; e < 8; ++e) s_du[e] = s_dg[e] = s_gx[e] = s_bx[e] = s_gg[e] = s_bg[e] = 0.0f;
   const int rows_per = (M + nsplit - 1) / nsplit;
-  const int n_begin = rs * rows_per, n_end = min(M, n_begin + rows_per);
-  const int64_t row0 = static_cast<int64_t>(t) * M;
+  const int n_begin = min(M, rsp * rows_per), n_end = min(M, n_begin + rows_per);
+  const int n_rows = n_end - n_begin;
+  const int64_t rowbase = static_cast<int64_t>(t) * M + n_begin;
   const int64_t zstride = 2 * static_cast<int64_t>(H);
-  for (int n = n_begin; n < n_end; n += kApplyRows) {
-    uint2 pu[kApplyRows], pg[kApplyRows], ph[kApplyRows];
-    float4 st[kApplyRows], rsm[kApplyRows];
-#pragma unroll
-    for (int i = 0; i < kApplyRows; ++i) {
-      if (n + i < n_end) {
-        const int64_t row = row0 + n + i;
-        pu[i] = __ldcs(reinterpret_cast<const uint2*>(Z + row * zstride + c0));
-        pg[i] = __ldcs(reinterpret_cast<const uint2*>(Z + row * zstride + H + c0));
-        ph[i] = __ldcs(reinterpret_cast<const uint2*>(dHl + row * H + c0));
-        st[i] = stats[row];
-        rsm[i] = rowsum[row];
-      }
+  auto issue = [&](int i) {
+    if (i < n_rows) {
+      const int64_t row = rowbase + i;
+      const int s = i % kApplyStages;
+      cp_async16(&ring[s][0][threadIdx.x], Z + row * zstride + cc, active);
+      cp_async16(&ring[s][1][threadIdx.x], Z + row * zstride + H + cc, active);
+      cp_async16(&ring[s][2][threadIdx.x], dHl + row * H + cc, active);
+      cp_async16(&ring[s][3][threadIdx.x], stats + row, true);
+      cp_async16(&ring[s][4][threadIdx.x], rowsum + row, true);
     }
+    cp_async_commit();
+  };
 #pragma unroll
-    for (int i = 0; i < kApplyRows; ++i) {
-      if (n + i < n_end) {
-        const int64_t row = row0 + n + i;
-        float u[4], g[4], hv[4], du[4], dg[4];
-        unpack4(pu[i], u);
-        unpack4(pg[i], g);
-        unpack4(ph[i], hv);
-        const float m1u = rsm[i].x * inv_h, m2u = rsm[i].y * inv_h;
-        const float m1g = rsm[i].z * inv_h, m2g = rsm[i].w * inv_h;
+  for (int i = 0; i < kApplyStages - 1; ++i) issue(i);
+  for (int i = 0; i < n_rows; ++i) {
+    issue(i + kApplyStages - 1);
+    cp_async_wait<kApplyStages - 1>();
+    const int s = i % kApplyStages;
+    if (!active) continue;
+    const int64_t row = rowbase + i;
+    float u[8], g[8], hv[8], du[8], dg[8];
+    unpack8(ring[s][0][threadIdx.x], u);
+    unpack8(ring[s][1][threadIdx.x], g);
+    unpack8(ring[s][2][threadIdx.x], hv);
+    const uint4 stv = ring[s][3][threadIdx.x], rsv = ring[s][4][threadIdx.x];
+    const float4 st = make_float4(__uint_as_float(stv.x), __uint_as_float(stv.y), __uint_as_float(stv.z),
+                                  __uint_as_float(stv.w));
+    const float m1u = __uint_as_float(rsv.x) * inv_h, m2u = __uint_as_float(rsv.y) * inv_h;
+    const float m1g = __uint_as_float(rsv.z) * inv_h, m2g = __uint_as_float(rsv.w) * inv_h;
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float xu = (u[e] - st[i].x) * st[i].y, xg = (g[e] - st[i].z) * st[i].w;
-          const float a = fmaf(xu, wx[e], cx[e]), sv = fmaf(xg, wg[e], cg[e]);
-          const float sg = sigmoid_fast(sv);
-          const float da = hv[e] * (sv * sg);
-          const float ds = hv[e] * a * fmaf(sv * sg, 1.0f - sg, sg);
-          du[e] = st[i].y * (fmaf(da, wx[e], -m1u) - xu * m2u);
-          dg[e] = st[i].w * (fmaf(ds, wg[e], -m1g) - xg * m2g);
-          s_du[e] += du[e];
-          s_dg[e] += dg[e];
-          s_gx[e] = fmaf(da, xu, s_gx[e]);
-          s_bx[e] += da;
-          s_gg[e] = fmaf(ds, xg, s_gg[e]);
-          s_bg[e] += ds;
-        }
-        __stcs(reinterpret_cast<uint2*>(dZ + row * zstride + c0), pack4(du));
-        __stcs(reinterpret_cast<uint2*>(dZ + row * zstride + H + c0), pack4(dg));
-      }
+    for (int e = 0; e < 8; ++e) {
+      const float xu = (u[e] - st.x) * st.y, xg = (g[e] - st.z) * st.w;
+      const float a = fmaf(xu, wx[e], cx[e]), sv = fmaf(xg, wg[e], cg[e]);
+      const float sg = sigmoid_fast(sv);
+      const float da = hv[e] * (sv * sg);
+      const float ds = hv[e] * a * fmaf(sv * sg, 1.0f - sg, sg);
+      du[e] = st.y * (fmaf(da, wx[e], -m1u) - xu * m2u);
+      dg[e] = st.w * (fmaf(ds, wg[e], -m1g) - xg * m2g);
+      s_du[e] += du[e];
+      s_dg[e] += dg[e];
+      s_gx[e] = fmaf(da, xu, s_gx[e]);
+      s_bx[e] += da;
+      s_gg[e] = fmaf(ds, xg, s_gg[e]);
+      s_bg[e] += ds;
     }
+    store8_stream(dZ + row * zstride + c0, du);
+    store8_stream(dZ + row * zstride + H + c0, dg);
   }
-  // part[t][rs][q][c], q: dU, dG, da*x_u, da, ds*x_g, ds
-  float* pp = part + (static_cast<int64_t>(t) * nsplit + rs) * 6 * H + c0;
-  *reinterpret_cast<float4*>(pp + 0 * static_cast<int64_t>(H)) = make_float4(s_du[0], s_du[1], s_du[2], s_du[3]);
-  *reinterpret_cast<float4*>(pp + 1 * static_cast<int64_t>(H)) = make_float4(s_dg[0], s_dg[1], s_dg[2], s_dg[3]);
-  *reinterpret_cast<float4*>(pp + 2 * static_cast<int64_t>(H)) = make_float4(s_gx[0], s_gx[1], s_gx[2], s_gx[3]);
-  *reinterpret_cast<float4*>(pp + 3 * static_cast<int64_t>(H)) = make_float4(s_bx[0], s_bx[1], s_bx[2], s_bx[3]);
-  *reinterpret_cast<float4*>(pp + 4 * static_cast<int64_t>(H)) = make_float4(s_gg[0], s_gg[1], s_gg[2], s_gg[3]);
-  *reinterpret_cast<float4*>(pp + 5 * static_cast<int64_t>(H)) = make_float4(s_bg[0], s_bg[1], s_bg[2], s_bg[3]);
+  cp_async_wait<0>();
+  if (!active) return;
+  // part[t][split][q][c], q: dU, dG, da*x_u, da, ds*x_g, ds
+  float* pp = part + (static_cast<int64_t>(t) * nsplit + rsp) * 6 * H + c0;
+  const float* src[6] = {s_du, s_dg, s_gx, s_bx, s_gg, s_bg};
+#pragma unroll
+  for (int q = 0; q < 6; ++q) {
+    float4* d4 = reinterpret_cast<float4*>(pp + q * static_cast<int64_t>(H));
+    d4[0] = make_float4(src[q][0], src[q][1], src[q][2], src[q][3]);
+    d4[1] = make_float4(src[q][4], src[q][5], src[q][6], src[q][7]);
+  }
 }
 
 // db1 [T, 2H] and the norm gradients [P, H] from the partials, summed in a
@@ -495,62 +532,76 @@ __global__ void debug_wait_kernel(uint32_t* err, uint64_t limit_ns) {
   if (threadIdx.x == 0) mbar_wait(&bar, 0u, err, 0x7fu, limit_ns);
 }
 
-int grid_for(const DeviceInfo& dev, const void* kernel, int threads, size_t smem, int64_t work_items) {
+}  // namespace
+
+// CTAs per rank so that the row kernels fill every SM (each CTA stays on one rank).
+static int ctas_per_rank(const DeviceInfo& dev, const void* kernel, int threads, size_t smem, int P,
+                         int64_t rank_rows) {
   int per_sm = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, smem) != cudaSuccess || per_sm < 1)
     per_sm = 1;
-  int64_t g = static_cast<int64_t>(per_sm) * dev.num_sms;
-  if (work_items < g) g = work_items;
-  return static_cast<int>(g < 1 ? 1 : g);
+  int64_t c = (static_cast<int64_t>(per_sm) * dev.num_sms + P - 1) / P;
+  if (c > rank_rows) c = rank_rows;
+  return static_cast<int>(c < 1 ? 1 : c);
 }
 
-}  // namespace
+// Block shape of the per-row kernels: NT threads x VPT 8-column vectors >= H.
+static bool row_shape(int H, int* nt, int* vpt) {
+  const int nvec = H / 8;
+  if (nvec <= 256) { *nt = 256; *vpt = 1; return true; }
+  if (nvec <= 512) { *nt = 256; *vpt = 2; return true; }
+  if (nvec <= 1024) { *nt = 512; *vpt = 2; return true; }
+  return false;
+}
 
 cudaError_t launch_ln_gate_fwd(const void* Z, const void* nx_w, const void* nx_b, const void* ng_w,
                                const void* ng_b, void* Hl, void* stats, int64_t rows, int M, int L, int H,
                                float eps, const DeviceInfo& dev, cudaStream_t s) {
-  const int vpt = (H / 8 + kRowThreads - 1) / kRowThreads;
+  int nt = 0, vpt = 0;
+  if (!row_shape(H, &nt, &vpt)) return cudaErrorInvalidValue;
+  const int P = static_cast<int>(rows / (static_cast<int64_t>(L) * M));
   auto run = [&](auto kern) {
-    const int grid = grid_for(dev, reinterpret_cast<const void*>(kern), kRowThreads, 0, rows);
-    kern<<<grid, kRowThreads, 0, s>>>(static_cast<const __nv_bfloat16*>(Z), static_cast<const __nv_bfloat16*>(nx_w),
-                                      static_cast<const __nv_bfloat16*>(nx_b), static_cast<const __nv_bfloat16*>(ng_w),
-                                      static_cast<const __nv_bfloat16*>(ng_b), static_cast<__nv_bfloat16*>(Hl),
-                                      static_cast<float4*>(stats), rows, M, L, H, eps, dev.err);
+    const size_t smem = static_cast<size_t>(kFwdStages) * vpt * 2 * nt * 16;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    const int cpr = ctas_per_rank(dev, reinterpret_cast<const void*>(kern), nt, smem, P, static_cast<int64_t>(L) * M);
+    kern<<<P * cpr, nt, smem, s>>>(static_cast<const __nv_bfloat16*>(Z), static_cast<const __nv_bfloat16*>(nx_w),
+                                   static_cast<const __nv_bfloat16*>(nx_b), static_cast<const __nv_bfloat16*>(ng_w),
+                                   static_cast<const __nv_bfloat16*>(ng_b), static_cast<__nv_bfloat16*>(Hl),
+                                   static_cast<float4*>(stats), M, L, H, cpr, eps, dev.err);
     return cudaGetLastError();
   };
-  if (vpt <= 1) return run(ln_gate_fwd_kernel<1>);
-  if (vpt <= 2) return run(ln_gate_fwd_kernel<2>);
-  if (vpt <= 4) return run(ln_gate_fwd_kernel<4>);
-  return cudaErrorInvalidValue;
+  if (nt == 256 && vpt == 1) return run(ln_gate_fwd_kernel<256, 1>);
+  if (nt == 256) return run(ln_gate_fwd_kernel<256, 2>);
+  return run(ln_gate_fwd_kernel<512, 2>);
 }
 
 cudaError_t launch_ln_gate_bwd_rowsum(const void* Z, const void* stats, const void* dHl, const void* nx_w,
                                       const void* nx_b, const void* ng_w, const void* ng_b, void* rowsum, int T, int M,
                                       int L, int H, const DeviceInfo& dev, cudaStream_t s) {
-  const int64_t rows = static_cast<int64_t>(T) * M;
-  const int nvec = H / 8;
-  // VPT vectors per thread, at most 512 threads
-  const int vpt = nvec <= 512 ? 1 : nvec <= 1024 ? 2 : nvec <= 2048 ? 4 : 0;
-  if (vpt == 0) return cudaErrorInvalidValue;
-  int threads = (nvec + vpt - 1) / vpt;
-  threads = ((threads + 31) / 32) * 32;
+  int nt = 0, vpt = 0;
+  if (!row_shape(H, &nt, &vpt)) return cudaErrorInvalidValue;
+  const int P = T / L;
   auto run = [&](auto kern) {
-    const int grid = grid_for(dev, reinterpret_cast<const void*>(kern), threads, 0, rows);
-    kern<<<grid, threads, 0, s>>>(static_cast<const __nv_bfloat16*>(Z), static_cast<const float4*>(stats),
-                                  static_cast<const __nv_bfloat16*>(dHl), static_cast<const __nv_bfloat16*>(nx_w),
-                                  static_cast<const __nv_bfloat16*>(nx_b), static_cast<const __nv_bfloat16*>(ng_w),
-                                  static_cast<const __nv_bfloat16*>(ng_b), static_cast<float4*>(rowsum), rows, M, L,
-                                  H, dev.err);
+    const size_t smem = static_cast<size_t>(kBwdStages) * vpt * 3 * nt * 16;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    const int cpr = ctas_per_rank(dev, reinterpret_cast<const void*>(kern), nt, smem, P, static_cast<int64_t>(L) * M);
+    kern<<<P * cpr, nt, smem, s>>>(static_cast<const __nv_bfloat16*>(Z), static_cast<const float4*>(stats),
+                                   static_cast<const __nv_bfloat16*>(dHl), static_cast<const __nv_bfloat16*>(nx_w),
+                                   static_cast<const __nv_bfloat16*>(nx_b), static_cast<const __nv_bfloat16*>(ng_w),
+                                   static_cast<const __nv_bfloat16*>(ng_b), static_cast<float4*>(rowsum), M, L, H, cpr,
+                                   dev.err);
     return cudaGetLastError();
   };
-  if (vpt == 1) return run(ln_gate_bwd_rowsum_kernel<1>);
-  if (vpt == 2) return run(ln_gate_bwd_rowsum_kernel<2>);
-  return run(ln_gate_bwd_rowsum_kernel<4>);
+  if (nt == 256 && vpt == 1) return run(ln_gate_bwd_rowsum_kernel<256, 1>);
+  if (nt == 256) return run(ln_gate_bwd_rowsum_kernel<256, 2>);
+  return run(ln_gate_bwd_rowsum_kernel<512, 2>);
 }
 
 int ffn_bwd_row_splits(int T, int M) {
   // enough (t, column block, row range) items to fill the GPU several times over
-  int splits = (2048 + T - 1) / T;
+  int splits = (4096 + T - 1) / T;
   const int cap = (M + 63) / 64;
   if (splits > cap) splits = cap;
   return splits < 1 ? 1 : splits;
@@ -560,17 +611,15 @@ cudaError_t launch_ln_gate_bwd_apply(const void* Z, const void* stats, const voi
                                      const void* nx_w, const void* nx_b, const void* ng_w, const void* ng_b, void* dZ,
                                      float* part, int T, int M, int L, int H, int nsplit, const DeviceInfo& dev,
                                      cudaStream_t s) {
-  // balanced column blocks of at most 1024 columns (256 threads x 4 columns)
-  const int nblk = (H + 1023) / 1024;
-  int cols = (H + nblk - 1) / nblk;
-  cols = ((cols + 4 * 32 - 1) / (4 * 32)) * (4 * 32);
-  const int threads = cols / kApplyVec;
-  dim3 grid(nblk, T, nsplit);
-  ln_gate_bwd_apply_kernel<<<grid, threads, 0, s>>>(
+  dim3 grid((H + 8 * kApplyThreads - 1) / (8 * kApplyThreads), T, nsplit);
+  const int smem = kApplyStages * 5 * kApplyThreads * 16;
+  cudaError_t e = cudaFuncSetAttribute(ln_gate_bwd_apply_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  ln_gate_bwd_apply_kernel<<<grid, kApplyThreads, smem, s>>>(
       static_cast<const __nv_bfloat16*>(Z), static_cast<const float4*>(stats), static_cast<const float4*>(rowsum),
       static_cast<const __nv_bfloat16*>(dHl), static_cast<const __nv_bfloat16*>(nx_w),
       static_cast<const __nv_bfloat16*>(nx_b), static_cast<const __nv_bfloat16*>(ng_w),
-      static_cast<const __nv_bfloat16*>(ng_b), static_cast<__nv_bfloat16*>(dZ), part, M, L, H, cols, dev.err);
+      static_cast<const __nv_bfloat16*>(ng_b), static_cast<__nv_bfloat16*>(dZ), part, M, L, H, dev.err);
   return cudaGetLastError();
 }
 
