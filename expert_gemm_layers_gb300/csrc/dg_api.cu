@@ -187,6 +187,7 @@ dg_status run_gemm(GemmVariant v, const CUtensorMap& a, const CUtensorMap& b, co
     case GV_BF16_KM_BIAS: e = launch_gemm_bf16_km_bias(a, b, d, c, p, grid, s); break;
     case GV_BF16_MM_STORE: e = launch_gemm_bf16_mm_store(a, b, d, c, p, grid, s); break;
     case GV_BF16_KK_SWIGLU: e = launch_gemm_bf16_kk_swiglu(a, b, d, c, p, grid, s); break;
+    case GV_BF16_KM_LNSTATS: e = launch_gemm_bf16_km_lnstats(a, b, d, c, p, grid, s); break;
     default: return fail(DG_ERR_UNSUPPORTED, "unknown GEMM variant");
   }
   if (e != cudaSuccess) return cuda_fail(e, "GEMM launch");
@@ -220,17 +221,21 @@ dg_status check_ffn_shape(const dg_ffn_shape* sh, FfnDims* o) {
   return DG_OK;
 }
 
-// Carving of the forward's `saved` buffer: Z [T,M,2H] bf16, Hl [T,M,H] bf16, stats [T,M] float4.
+// Carving of the forward's `saved` buffer: Z [T,M,2H] bf16, Hl [T,M,H] bf16,
+// stats [T,M] float4, and the per-tile LayerNorm partials [T,tiles_n,M] float4.
 struct SavedLayout {
-  size_t z, hl, stats, total;
+  size_t z, hl, stats, part, total;
+  int tiles_n;
 };
 SavedLayout saved_layout(const FfnDims& f) {
   SavedLayout l;
   const size_t rows = static_cast<size_t>(f.T) * f.M;
+  l.tiles_n = static_cast<int>((2 * f.H + gemm_tile_n(GV_BF16_KM_LNSTATS) - 1) / gemm_tile_n(GV_BF16_KM_LNSTATS));
   l.z = 0;
   l.hl = round_up(l.z + rows * 2 * f.H * 2, 256);
   l.stats = round_up(l.hl + rows * f.H * 2, 256);
-  l.total = round_up(l.stats + rows * 16, 256);
+  l.part = round_up(l.stats + rows * 16, 256);
+  l.total = round_up(l.part + rows * l.tiles_n * 16, 256);
   return l;
 }
 
@@ -392,9 +397,11 @@ dg_status dg_a2a_ffn_fwd(const dg_ffn_shape* shape, const void* inputs, const vo
   void* Z = sv + sl.z;
   void* Hl = sv + sl.hl;
   void* stats = sv + sl.stats;
+  void* part = sv + sl.part;
   const uint64_t T = f.T, M = f.M, D = f.D, H = f.H;
 
   // GEMM1: Z_t = Xlocal_t @ w1_t + b1_t.  Xlocal_t row n is inputs row n*T + t (dispatch).
+  // The epilogue also writes each row's per-tile mean and M2 of its U and G columns.
   CUtensorMap mx, mw1, mz;
   if ((st = make_map_3d(&mx, true, inputs, D, T, M, D * 2, T * D * 2, 64, 1, 128, "inputs")) != DG_OK) return st;
   if ((st = make_map_3d(&mw1, true, w1, 2 * H, D, T, 2 * H * 2, D * 2 * H * 2, 64, 64, 1, "w1")) != DG_OK) return st;
@@ -409,17 +416,26 @@ dg_status dg_a2a_ffn_fwd(const dg_ffn_shape* shape, const void* inputs, const vo
   p1.d_g = G_OUTER;
   p1.bias = static_cast<const __nv_bfloat16*>(b1);
   p1.bias_g_stride = static_cast<int64_t>(2 * H);
+  p1.ln_part = static_cast<float4*>(part);
+  p1.ln_H = static_cast<int32_t>(H);
   const double rows = static_cast<double>(T) * M;
-  if ((st = run_gemm(GV_BF16_KM_BIAS, mx, mw1, mz, mz, p1, dev, s, "ffn_gemm1",
-                     2.0 * (rows * D + static_cast<double>(T) * D * 2 * H + rows * 2 * H))) != DG_OK)
+  if ((st = run_gemm(GV_BF16_KM_LNSTATS, mx, mw1, mz, mz, p1, dev, s, "ffn_gemm1",
+                     2.0 * (rows * D + static_cast<double>(T) * D * 2 * H + rows * 2 * H) +
+                         rows * sl.tiles_n * 16.0)) != DG_OK)
     return st;
 
-  // LayerNorm of both halves, gate: Hl = LN_x(U) * silu(LN_g(G)).
+  // Per-row statistics, then LayerNorm of both halves and the gate: Hl = LN_x(U) * silu(LN_g(G)).
   cudaError_t e;
   {
+    TraceScope trace("ffn_ln_stats", s, 0.0, rows * sl.tiles_n * 16.0 + rows * 16.0);
+    e = launch_ln_stats_finalize(static_cast<const float4*>(part), stats, static_cast<int>(T), static_cast<int>(M),
+                                 static_cast<int>(H), gemm_tile_n(GV_BF16_KM_LNSTATS), sl.tiles_n, shape->eps, dev, s);
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "LayerNorm statistics launch");
+  {
     TraceScope trace("ffn_ln_gate_fwd", s, 0.0, rows * (2.0 * 2 * H + 2.0 * H + 16.0));
-    e = launch_ln_gate_fwd(Z, nx_w, nx_b, ng_w, ng_b, Hl, stats, static_cast<int64_t>(T * M),
-                                     static_cast<int>(M), static_cast<int>(f.L), static_cast<int>(H), shape->eps, dev, s);
+    e = launch_ln_gate_fwd(Z, stats, nx_w, nx_b, ng_w, ng_b, Hl, static_cast<int>(f.P), static_cast<int>(M),
+                           static_cast<int>(f.L), static_cast<int>(H), dev, s);
   }
   if (e != cudaSuccess) return cuda_fail(e, "LayerNorm-gate launch");
 

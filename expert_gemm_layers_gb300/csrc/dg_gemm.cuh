@@ -30,7 +30,7 @@
 namespace dg {
 
 enum GMode : int32_t { G_OUTER = 0, G_MID = 1, G_NONE = 2 };
-enum Epi : int32_t { EPI_STORE = 0, EPI_BIAS = 1, EPI_FP8 = 2, EPI_SWIGLU = 3 };
+enum Epi : int32_t { EPI_STORE = 0, EPI_BIAS = 1, EPI_FP8 = 2, EPI_SWIGLU = 3, EPI_BIAS_LNSTATS = 4 };
 
 // Wait-site codes recorded with a timeout.
 enum WaitSite : uint32_t {
@@ -45,8 +45,43 @@ struct GemmParams {
   int64_t bias_g_stride;
   float alpha, beta;         // EPI_FP8
   int32_t has_c;             // EPI_FP8: read C
+  float4* ln_part;           // EPI_BIAS_LNSTATS: [G][tiles_n][M] (mean_u, M2_u, mean_g, M2_g) per tile
+  int32_t ln_H;              // EPI_BIAS_LNSTATS: columns [0, ln_H) are U, [ln_H, N) are G
   uint32_t* err;             // device error word
 };
+
+// Running (count, mean, M2) of a set of values; merge() is the pairwise
+// combination of Chan, Golub & LeVeque ("Updating formulae and a pairwise
+// algorithm for computing sample variances").
+struct MeanM2 {
+  float n, mean, m2;
+  __device__ __forceinline__ void merge(float nb, float mean_b, float m2_b) {
+    if (nb <= 0.0f) return;
+    const float nn = n + nb;
+    const float d = mean_b - mean;
+    const float f = nb / nn;
+    mean = fmaf(d, f, mean);
+    m2 = m2 + m2_b + d * d * n * f;
+    n = nn;
+  }
+};
+
+// Two-pass (mean, M2) of v[lo, hi) -- values held in registers.
+template <int K>
+static __device__ __forceinline__ void chunk_mean_m2(const float (&v)[K], int lo, int hi, float& mean, float& m2) {
+  float s = 0.0f;
+#pragma unroll
+  for (int i = 0; i < K; ++i) s += (i >= lo && i < hi) ? v[i] : 0.0f;
+  const float n = static_cast<float>(hi - lo);
+  mean = s / n;
+  float q = 0.0f;
+#pragma unroll
+  for (int i = 0; i < K; ++i) {
+    const float d = v[i] - mean;
+    q = (i >= lo && i < hi) ? fmaf(d, d, q) : q;
+  }
+  m2 = q;
+}
 
 template <bool kFp8, bool kAMN, bool kBMN, int kEpi>
 struct GemmCfg {
@@ -314,6 +349,7 @@ __global__ void __launch_bounds__(GemmCfg<kFp8, kAMN, kBMN, kEpi>::NUM_THREADS, 
       tphase ^= 1u << acc;
       tc_fence_after_sync();
 
+      MeanM2 st_u{0.0f, 0.0f, 0.0f}, st_g{0.0f, 0.0f, 0.0f};
       for (int j = 0; j < nchunks; ++j) {
         const int buf = static_cast<int>((chunk_ctr + j) & 1u);
         if (use_c && j + 1 < nchunks) issue_c(j + 1, buf ^ 1);
@@ -373,7 +409,7 @@ __global__ void __launch_bounds__(GemmCfg<kFp8, kAMN, kBMN, kEpi>::NUM_THREADS, 
 #pragma unroll
             for (int i = 0; i < 64; ++i) v[i] *= p.alpha;
           }
-          if (kEpi == EPI_BIAS) {
+          if (kEpi == EPI_BIAS || kEpi == EPI_BIAS_LNSTATS) {
             const __nv_bfloat16* bp = p.bias + static_cast<int64_t>(g) * p.bias_g_stride + n0 + 64 * j;
 #pragma unroll
             for (int q = 0; q < 8; ++q) {
@@ -393,6 +429,35 @@ __global__ void __launch_bounds__(GemmCfg<kFp8, kAMN, kBMN, kEpi>::NUM_THREADS, 
           if (lane == 0) bulk_wait_group_read<1>();
           __syncwarp();
         }
+        if (kEpi == EPI_BIAS_LNSTATS) {
+          // statistics of this row's valid columns of the chunk, split at ln_H
+          const int c0 = n0 + 64 * j;
+          const int cend = min(c0 + 64, p.N);
+          const int nvalid = cend - c0;
+          const int usplit = min(max(p.ln_H - c0, 0), nvalid);  // columns [0, usplit) are U
+          float mean, m2;
+          if (nvalid == 64 && (usplit == 0 || usplit == 64)) {
+            float sum = 0.0f, q = 0.0f;
+#pragma unroll
+            for (int i = 0; i < 64; ++i) sum += v[i];
+            mean = sum * (1.0f / 64.0f);
+#pragma unroll
+            for (int i = 0; i < 64; ++i) {
+              const float d = v[i] - mean;
+              q = fmaf(d, d, q);
+            }
+            (usplit == 64 ? st_u : st_g).merge(64.0f, mean, q);
+          } else {
+            if (usplit > 0) {
+              chunk_mean_m2<64>(v, 0, usplit, mean, m2);
+              st_u.merge(static_cast<float>(usplit), mean, m2);
+            }
+            if (nvalid > usplit) {
+              chunk_mean_m2<64>(v, usplit, nvalid, mean, m2);
+              st_g.merge(static_cast<float>(nvalid - usplit), mean, m2);
+            }
+          }
+        }
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
           uint4 o;
@@ -410,6 +475,10 @@ __global__ void __launch_bounds__(GemmCfg<kFp8, kAMN, kBMN, kEpi>::NUM_THREADS, 
         }
       }
       if (!ok) break;
+      if (kEpi == EPI_BIAS_LNSTATS && nchunks > 0 && row0 + lane < p.M) {
+        p.ln_part[(static_cast<int64_t>(g) * p.tiles_n + rem / p.tiles_m) * p.M + row0 + lane] =
+            make_float4(st_u.mean, st_u.m2, st_g.mean, st_g.m2);
+      }
       chunk_ctr += static_cast<uint32_t>(nchunks);
       tc_fence_before_sync();
       __syncwarp();

@@ -1,0 +1,11 @@
+// Instantiation unit of the tcgen05 GEMM: bf16 A K-major, B MN-major, per-problem bias and per-tile LayerNorm statistics of each row.
+#include "dg_internal.h"
+
+namespace dg {
+
+cudaError_t launch_gemm_bf16_km_lnstats(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& d,
+                                        const CUtensorMap& c, const GemmParams& p, int grid, cudaStream_t s) {
+  return launch_gemm_t<false, false, true, EPI_BIAS_LNSTATS>(a, b, d, c, p, grid, s);
+}
+
+}  // namespace dg

@@ -33,7 +33,8 @@ enum GemmVariant : int {
   GV_BF16_KK_STORE = 1, // bf16, A and B K-major, plain store
   GV_BF16_KM_BIAS = 2,  // bf16, A K-major, B MN-major, bias epilogue
   GV_BF16_MM_STORE = 3, // bf16, A and B MN-major, plain store
-  GV_BF16_KK_SWIGLU = 4 // bf16, A and B K-major, paired silu(a)*b epilogue
+  GV_BF16_KK_SWIGLU = 4, // bf16, A and B K-major, paired silu(a)*b epilogue
+  GV_BF16_KM_LNSTATS = 5 // bf16, A K-major, B MN-major, bias + per-tile LayerNorm statistics
 };
 
 // Tiles along N of one problem for this variant (output columns per tile).
@@ -73,6 +74,8 @@ cudaError_t launch_gemm_bf16_mm_store(const CUtensorMap&, const CUtensorMap&, co
                                       const CUtensorMap&, const GemmParams&, int grid, cudaStream_t);
 cudaError_t launch_gemm_bf16_kk_swiglu(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
                                        const CUtensorMap&, const GemmParams&, int grid, cudaStream_t);
+cudaError_t launch_gemm_bf16_km_lnstats(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
+                                        const CUtensorMap&, const GemmParams&, int grid, cudaStream_t);
 
 // Host launcher body shared by the instantiation units.
 template <bool kFp8, bool kAMN, bool kBMN, int kEpi>
@@ -88,10 +91,15 @@ cudaError_t launch_gemm_t(const CUtensorMap& a, const CUtensorMap& b, const CUte
 
 // ---------------------------------------------------------------- row kernels (dg_rowops.cu)
 
-// LayerNorm-and-gate forward over rows of Z [rows, 2H]: Hl [rows, H], stats [rows] (mu_u, rstd_u, mu_g, rstd_g).
-cudaError_t launch_ln_gate_fwd(const void* Z, const void* nx_w, const void* nx_b, const void* ng_w,
-                               const void* ng_b, void* Hl, void* stats, int64_t rows, int M, int L, int H,
-                               float eps, const DeviceInfo& dev, cudaStream_t s);
+// Per-row LayerNorm statistics stats [T*M] (mean_u, rstd_u, mean_g, rstd_g) from the
+// per-tile (mean, M2) pairs part [T][tiles_n][M] the GEMM1 epilogue wrote.
+cudaError_t launch_ln_stats_finalize(const float4* part, void* stats, int T, int M, int H, int tile_n, int tiles_n,
+                                     float eps, const DeviceInfo& dev, cudaStream_t s);
+
+// Normalise and gate: Hl [rows, H] = LN_x(U) * silu(LN_g(G)) from Z [rows, 2H] and stats.
+cudaError_t launch_ln_gate_fwd(const void* Z, const void* stats, const void* nx_w, const void* nx_b, const void* ng_w,
+                               const void* ng_b, void* Hl, int P, int M, int L, int H, const DeviceInfo& dev,
+                               cudaStream_t s);
 
 // Backward of the gate and both LayerNorms, pass 1: per-row sums
 // rowsum[row] = (sum dx_u, sum dx_u*x_u, sum dx_g, sum dx_g*x_g).

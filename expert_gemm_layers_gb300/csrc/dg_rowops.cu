@@ -87,7 +87,7 @@ __device__ __forceinline__ void block_sum(float (&v)[N], float (*sm)[kMaxRowWarp
 #pragma unroll
   for (int i = 0; i < N; ++i) {
 #pragma unroll
-    for (int o = kMaxRowWarps / 2; o > 0; o >>= 1) w[i] += __shfl_xor_sync(0xffffffffu, w[i], o);
+    for (int o = 16; o > 0; o >>= 1) w[i] += __shfl_xor_sync(0xffffffffu, w[i], o);
     v[i] = w[i];
   }
 }
@@ -121,43 +121,82 @@ __device__ __forceinline__ Affine8 load_affine8(const __nv_bfloat16* gx, const _
   return a;
 }
 
+// Packed two-lane fp32 arithmetic (fma/mul .f32x2): one issue slot for two lanes.
+__device__ __forceinline__ unsigned long long f2u(float2 a) { return *reinterpret_cast<unsigned long long*>(&a); }
+__device__ __forceinline__ float2 u2f(unsigned long long a) { return *reinterpret_cast<float2*>(&a); }
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+  unsigned long long d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(f2u(a)), "l"(f2u(b)), "l"(f2u(c)));
+  return u2f(d);
+}
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
+  unsigned long long d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(f2u(a)), "l"(f2u(b)));
+  return u2f(d);
+}
+
 // ------------------------------------------------------------------ forward
 //
-// A CTA walks rows (grid-stride) of ONE rank's token positions, so each
-// thread keeps the affine parameters of its columns in registers.  Rows are
-// staged through a kStages-deep shared-memory ring by per-thread cp.async.
-// Thread i owns 8-column vectors i, i + blockDim, ... of U and G.  The row
-// statistics use the shifted-data single pass (Chan, Golub & LeVeque,
-// "Algorithms for computing the sample variance"): with K the row's first
-// element, mean = K + S1/H and var = S2/H - (S1/H)^2 where S1 = sum(x-K),
-// S2 = sum((x-K)^2); K is a sample of the row, so the subtraction does not
-// cancel catastrophically, and a constant row gives exactly var = 0.
+// The row statistics come from the GEMM that produced Z: its epilogue
+// writes, per row and per 256-column tile, the mean and centred second
+// moment of the tile's U and G columns; ln_stats_finalize merges the tiles
+// of a row (Chan's pairwise formula) into (mean_u, rstd_u, mean_g, rstd_g).
+// The normalise-and-gate pass is then a pure map: a CTA walks rows of ONE
+// rank (so each thread keeps the affines of its columns in fp32 registers),
+// staging rows through a shared-memory ring with per-thread cp.async.
 
-constexpr int kFwdStages = 3;
+__global__ void ln_stats_finalize_kernel(const float4* __restrict__ part, float4* __restrict__ stats, int T, int M,
+                                         int H, int tile_n, int tiles_n, float eps, const uint32_t* err) {
+  if (ld_volatile_u32(err) != 0u) return;
+  const int64_t rows = static_cast<int64_t>(T) * M;
+  const int N = 2 * H;
+  for (int64_t row = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; row < rows;
+       row += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int t = static_cast<int>(row / M), n = static_cast<int>(row - static_cast<int64_t>(t) * M);
+    MeanM2 su{0.0f, 0.0f, 0.0f}, sg{0.0f, 0.0f, 0.0f};
+    for (int nt = 0; nt < tiles_n; ++nt) {
+      const int c0 = nt * tile_n, cend = min(c0 + tile_n, N);
+      const int nu = min(max(H - c0, 0), cend - c0), ng = cend - c0 - nu;
+      const float4 q = part[(static_cast<int64_t>(t) * tiles_n + nt) * M + n];
+      su.merge(static_cast<float>(nu), q.x, q.y);
+      sg.merge(static_cast<float>(ng), q.z, q.w);
+    }
+    const float inv_h = 1.0f / static_cast<float>(H);
+    stats[row] = make_float4(su.mean, rsqrtf(su.m2 * inv_h + eps), sg.mean, rsqrtf(sg.m2 * inv_h + eps));
+  }
+}
+
+constexpr int kFwdStages = 4;
 
 template <int NT, int VPT>
 __global__ void __launch_bounds__(NT, 512 / NT) ln_gate_fwd_kernel(
-    const __nv_bfloat16* __restrict__ Z, const __nv_bfloat16* __restrict__ gx, const __nv_bfloat16* __restrict__ bx,
-    const __nv_bfloat16* __restrict__ gg, const __nv_bfloat16* __restrict__ bg, __nv_bfloat16* __restrict__ Hl,
-    float4* __restrict__ stats, int M, int L, int H, int ctas_per_rank, float eps, const uint32_t* err) {
+    const __nv_bfloat16* __restrict__ Z, const float4* __restrict__ stats, const __nv_bfloat16* __restrict__ gx,
+    const __nv_bfloat16* __restrict__ bx, const __nv_bfloat16* __restrict__ gg, const __nv_bfloat16* __restrict__ bg,
+    __nv_bfloat16* __restrict__ Hl, int M, int L, int H, int ctas_per_rank, const uint32_t* err) {
   extern __shared__ uint4 ring[];  // [kFwdStages][VPT][2][NT]
-  __shared__ float sm[2][kMaxRowWarps][4];
   if (block_aborted(err)) return;
   const int nvec = H >> 3;
-  const float inv_h = 1.0f / static_cast<float>(H);
   const int64_t zstride = 2 * static_cast<int64_t>(H);
   const int r = blockIdx.x / ctas_per_rank;
   const int64_t rank_rows = static_cast<int64_t>(L) * M;
-  const int64_t first = static_cast<int64_t>(r) * rank_rows;
   const int64_t stride = ctas_per_rank;
   const int64_t n_mine = (rank_rows - (blockIdx.x % ctas_per_rank) + stride - 1) / stride;
-  const int64_t row0 = first + (blockIdx.x % ctas_per_rank);
+  const int64_t row0 = static_cast<int64_t>(r) * rank_rows + (blockIdx.x % ctas_per_rank);
 
-  Affine8 aff[VPT];
+  float2 wx[VPT][4], cx[VPT][4], wg[VPT][4], cg[VPT][4];
 #pragma unroll
   for (int j = 0; j < VPT; ++j) {
     const int v = threadIdx.x + NT * j;
-    aff[j] = load_affine8(gx, bx, gg, bg, static_cast<int64_t>(r) * H + 8 * (v < nvec ? v : 0));
+    const Affine8 a = load_affine8(gx, bx, gg, bg, static_cast<int64_t>(r) * H + 8 * (v < nvec ? v : 0));
+    const uint32_t w0[4] = {a.wx.x, a.wx.y, a.wx.z, a.wx.w}, w1[4] = {a.cx.x, a.cx.y, a.cx.z, a.cx.w};
+    const uint32_t w2[4] = {a.wg.x, a.wg.y, a.wg.z, a.wg.w}, w3[4] = {a.cg.x, a.cg.y, a.cg.z, a.cg.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      wx[j][e] = unpack_bf16x2(w0[e]);
+      cx[j][e] = unpack_bf16x2(w1[e]);
+      wg[j][e] = unpack_bf16x2(w2[e]);
+      cg[j][e] = unpack_bf16x2(w3[e]);
+    }
   }
   auto issue = [&](int64_t i) {
     if (i < n_mine) {
@@ -175,69 +214,37 @@ __global__ void __launch_bounds__(NT, 512 / NT) ln_gate_fwd_kernel(
   };
 #pragma unroll
   for (int i = 0; i < kFwdStages - 1; ++i) issue(i);
-  // the shift of each row (its first U and G elements), loaded one row ahead
-  float ku_next = 0.0f, kg_next = 0.0f;
-  if (n_mine > 0) {
-    ku_next = __bfloat162float(Z[row0 * zstride]);
-    kg_next = __bfloat162float(Z[row0 * zstride + H]);
-  }
-  int slot = 0;
+  float4 st_next = n_mine > 0 ? stats[row0] : make_float4(0.f, 0.f, 0.f, 0.f);
+  const float2 half2 = make_float2(0.5f, 0.5f);
   for (int64_t i = 0; i < n_mine; ++i) {
     issue(i + kFwdStages - 1);
     const int64_t row = row0 + i * stride;
-    const float ku = ku_next, kg = kg_next;
-    if (i + 1 < n_mine) {
-      ku_next = __bfloat162float(Z[(row + stride) * zstride]);
-      kg_next = __bfloat162float(Z[(row + stride) * zstride + H]);
-    }
+    const float4 sr = st_next;
+    if (i + 1 < n_mine) st_next = stats[row + stride];
     cp_async_wait<kFwdStages - 1>();
     const uint4* st = ring + (i % kFwdStages) * (VPT * 2 * NT);
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-    for (int j = 0; j < VPT; ++j) {
-      float u[8], g[8];
-      unpack8(st[(2 * j) * NT + threadIdx.x], u);
-      unpack8(st[(2 * j + 1) * NT + threadIdx.x], g);
-      if (threadIdx.x + NT * j < nvec) {
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const float du = u[e] - ku, dg = g[e] - kg;
-          acc[0] += du;
-          acc[1] = fmaf(du, du, acc[1]);
-          acc[2] += dg;
-          acc[3] = fmaf(dg, dg, acc[3]);
-        }
-      }
-    }
-    block_sum<4>(acc, sm, slot);
-    slot ^= 1;
-    const float m1u = acc[0] * inv_h, m1g = acc[2] * inv_h;
-    const float mu_u = ku + m1u, mu_g = kg + m1g;
-    const float rs_u = rsqrtf(fmaxf(acc[1] * inv_h - m1u * m1u, 0.0f) + eps);
-    const float rs_g = rsqrtf(fmaxf(acc[3] * inv_h - m1g * m1g, 0.0f) + eps);
-    const float cu = -mu_u * rs_u, cgg = -mu_g * rs_g;
+    const float2 rsu = make_float2(sr.y, sr.y), cu = make_float2(-sr.x * sr.y, -sr.x * sr.y);
+    const float2 rsg = make_float2(sr.w, sr.w), cgs = make_float2(-sr.z * sr.w, -sr.z * sr.w);
     __nv_bfloat16* hrow = Hl + row * static_cast<int64_t>(H);
 #pragma unroll
     for (int j = 0; j < VPT; ++j) {
       const int v = threadIdx.x + NT * j;
       if (v < nvec) {
-        float u[8], g[8], wx[8], cx[8], wg[8], cg[8], h[8];
-        unpack8(st[(2 * j) * NT + threadIdx.x], u);
-        unpack8(st[(2 * j + 1) * NT + threadIdx.x], g);
-        unpack8(aff[j].wx, wx);
-        unpack8(aff[j].cx, cx);
-        unpack8(aff[j].wg, wg);
-        unpack8(aff[j].cg, cg);
+        const uint4 pu = st[(2 * j) * NT + threadIdx.x], pg = st[(2 * j + 1) * NT + threadIdx.x];
+        const uint32_t uw[4] = {pu.x, pu.y, pu.z, pu.w}, gw[4] = {pg.x, pg.y, pg.z, pg.w};
+        uint32_t ow[4];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const float a = fmaf(fmaf(u[e], rs_u, cu), wx[e], cx[e]);
-          const float sg = fmaf(fmaf(g[e], rs_g, cgg), wg[e], cg[e]);
-          h[e] = a * silu_fast(sg);
+        for (int e = 0; e < 4; ++e) {
+          const float2 a = fma2(fma2(unpack_bf16x2(uw[e]), rsu, cu), wx[j][e], cx[j][e]);
+          const float2 sv = fma2(fma2(unpack_bf16x2(gw[e]), rsg, cgs), wg[j][e], cg[j][e]);
+          const float2 h = mul2(sv, half2);
+          const float2 silu = fma2(h, make_float2(tanh_fast(h.x), tanh_fast(h.y)), h);
+          const float2 o = mul2(a, silu);
+          ow[e] = pack_bf16x2(o.x, o.y);
         }
-        store8_stream(hrow + 8 * v, h);
+        __stcs(reinterpret_cast<uint4*>(hrow + 8 * v), make_uint4(ow[0], ow[1], ow[2], ow[3]));
       }
     }
-    if (threadIdx.x == 0) stats[row] = make_float4(mu_u, rs_u, mu_g, rs_g);
   }
   cp_async_wait<0>();
 }
@@ -570,21 +577,30 @@ static bool row_shape(int H, int* nt, int* vpt) {
   return false;
 }
 
-cudaError_t launch_ln_gate_fwd(const void* Z, const void* nx_w, const void* nx_b, const void* ng_w,
-                               const void* ng_b, void* Hl, void* stats, int64_t rows, int M, int L, int H,
-                               float eps, const DeviceInfo& dev, cudaStream_t s) {
+cudaError_t launch_ln_stats_finalize(const float4* part, void* stats, int T, int M, int H, int tile_n, int tiles_n,
+                                     float eps, const DeviceInfo& dev, cudaStream_t s) {
+  const int64_t rows = static_cast<int64_t>(T) * M;
+  int64_t blocks = (rows + 255) / 256;
+  if (blocks > 16 * dev.num_sms) blocks = 16 * dev.num_sms;
+  ln_stats_finalize_kernel<<<static_cast<int>(blocks), 256, 0, s>>>(part, static_cast<float4*>(stats), T, M, H, tile_n,
+                                                                    tiles_n, eps, dev.err);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_ln_gate_fwd(const void* Z, const void* stats, const void* nx_w, const void* nx_b, const void* ng_w,
+                               const void* ng_b, void* Hl, int P, int M, int L, int H, const DeviceInfo& dev,
+                               cudaStream_t s) {
   int nt = 0, vpt = 0;
   if (!row_shape(H, &nt, &vpt)) return cudaErrorInvalidValue;
-  const int P = static_cast<int>(rows / (static_cast<int64_t>(L) * M));
   auto run = [&](auto kern) {
     const size_t smem = static_cast<size_t>(kFwdStages) * vpt * 2 * nt * 16;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     const int cpr = ctas_per_rank(dev, reinterpret_cast<const void*>(kern), nt, smem, P, static_cast<int64_t>(L) * M);
-    kern<<<P * cpr, nt, smem, s>>>(static_cast<const __nv_bfloat16*>(Z), static_cast<const __nv_bfloat16*>(nx_w),
-                                   static_cast<const __nv_bfloat16*>(nx_b), static_cast<const __nv_bfloat16*>(ng_w),
-                                   static_cast<const __nv_bfloat16*>(ng_b), static_cast<__nv_bfloat16*>(Hl),
-                                   static_cast<float4*>(stats), M, L, H, cpr, eps, dev.err);
+    kern<<<P * cpr, nt, smem, s>>>(static_cast<const __nv_bfloat16*>(Z), static_cast<const float4*>(stats),
+                                   static_cast<const __nv_bfloat16*>(nx_w), static_cast<const __nv_bfloat16*>(nx_b),
+                                   static_cast<const __nv_bfloat16*>(ng_w), static_cast<const __nv_bfloat16*>(ng_b),
+                                   static_cast<__nv_bfloat16*>(Hl), M, L, H, cpr, dev.err);
     return cudaGetLastError();
   };
   if (nt == 256 && vpt == 1) return run(ln_gate_fwd_kernel<256, 1>);
