@@ -134,6 +134,54 @@ __device__ __forceinline__ float2 mul2(float2 a, float2 b) {
   asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(f2u(a)), "l"(f2u(b)));
   return u2f(d);
 }
+__device__ __forceinline__ float2 add2(float2 a, float2 b) {
+  unsigned long long d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(f2u(a)), "l"(f2u(b)));
+  return u2f(d);
+}
+__device__ __forceinline__ float2 splat2(float x) { return make_float2(x, x); }
+
+// Affine parameters of one 8-column vector as four fp32 pairs each.
+struct AffineF {
+  float2 wx[4], cx[4], wg[4], cg[4];
+};
+
+__device__ __forceinline__ AffineF load_affine_f(const __nv_bfloat16* gx, const __nv_bfloat16* bx,
+                                                 const __nv_bfloat16* gg, const __nv_bfloat16* bg, int64_t off) {
+  const Affine8 a = load_affine8(gx, bx, gg, bg, off);
+  const uint32_t w0[4] = {a.wx.x, a.wx.y, a.wx.z, a.wx.w}, w1[4] = {a.cx.x, a.cx.y, a.cx.z, a.cx.w};
+  const uint32_t w2[4] = {a.wg.x, a.wg.y, a.wg.z, a.wg.w}, w3[4] = {a.cg.x, a.cg.y, a.cg.z, a.cg.w};
+  AffineF f;
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    f.wx[e] = unpack_bf16x2(w0[e]);
+    f.cx[e] = unpack_bf16x2(w1[e]);
+    f.wg[e] = unpack_bf16x2(w2[e]);
+    f.cg[e] = unpack_bf16x2(w3[e]);
+  }
+  return f;
+}
+
+// Forward quantities of the gate at one column pair, recomputed from Z:
+// x_u, x_g (normalised), a = LN_x(U), s = LN_g(G), q = silu(s), silu'(s).
+struct GatePair {
+  float2 xu, xg, a, q, dsil;
+};
+
+__device__ __forceinline__ GatePair gate_pair(float2 u, float2 g, float2 rsu, float2 cu, float2 rsg, float2 cg_,
+                                              float2 wx, float2 cx, float2 wg, float2 cgb) {
+  GatePair r;
+  r.xu = fma2(u, rsu, cu);
+  r.xg = fma2(g, rsg, cg_);
+  r.a = fma2(r.xu, wx, cx);
+  const float2 sv = fma2(r.xg, wg, cgb);
+  const float2 h = mul2(sv, splat2(0.5f));
+  const float2 sig = fma2(make_float2(tanh_fast(h.x), tanh_fast(h.y)), splat2(0.5f), splat2(0.5f));
+  r.q = mul2(sv, sig);
+  // silu'(s) = sig + s*sig*(1 - sig) = q*(1 - sig) + sig
+  r.dsil = fma2(r.q, fma2(sig, splat2(-1.0f), splat2(1.0f)), sig);
+  return r;
+}
 
 // ------------------------------------------------------------------ forward
 //
@@ -282,11 +330,11 @@ __global__ void __launch_bounds__(NT, 512 / NT) ln_gate_bwd_rowsum_kernel(
   const int64_t n_mine = (rank_rows - (blockIdx.x % ctas_per_rank) + stride - 1) / stride;
   const int64_t row0 = static_cast<int64_t>(r) * rank_rows + (blockIdx.x % ctas_per_rank);
 
-  Affine8 aff[VPT];
+  AffineF aff[VPT];
 #pragma unroll
   for (int j = 0; j < VPT; ++j) {
     const int v = threadIdx.x + NT * j;
-    aff[j] = load_affine8(gx, bx, gg, bg, static_cast<int64_t>(r) * H + 8 * (v < nvec ? v : 0));
+    aff[j] = load_affine_f(gx, bx, gg, bg, static_cast<int64_t>(r) * H + 8 * (v < nvec ? v : 0));
   }
   auto issue = [&](int64_t i) {
     if (i < n_mine) {
@@ -317,32 +365,30 @@ __global__ void __launch_bounds__(NT, 512 / NT) ln_gate_bwd_rowsum_kernel(
     if (i + 1 < n_mine) sr_next = stats[row + stride];
     cp_async_wait<kBwdStages - 1>();
     const uint4* st = ring + (i % kBwdStages) * (VPT * 3 * NT);
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    const float2 rsu = splat2(sr.y), cu = splat2(-sr.x * sr.y), rsg = splat2(sr.w), cgs = splat2(-sr.z * sr.w);
+    float2 s1u = splat2(0.f), s2u = splat2(0.f), s1g = splat2(0.f), s2g = splat2(0.f);
 #pragma unroll
     for (int j = 0; j < VPT; ++j) {
       if (threadIdx.x + NT * j < nvec) {
-        float u[8], g[8], hv[8], wx[8], cx[8], wg[8], cg[8];
-        unpack8(st[(3 * j) * NT + threadIdx.x], u);
-        unpack8(st[(3 * j + 1) * NT + threadIdx.x], g);
-        unpack8(st[(3 * j + 2) * NT + threadIdx.x], hv);
-        unpack8(aff[j].wx, wx);
-        unpack8(aff[j].cx, cx);
-        unpack8(aff[j].wg, wg);
-        unpack8(aff[j].cg, cg);
+        const uint4 pu = st[(3 * j) * NT + threadIdx.x], pg = st[(3 * j + 1) * NT + threadIdx.x];
+        const uint4 ph = st[(3 * j + 2) * NT + threadIdx.x];
+        const uint32_t uw[4] = {pu.x, pu.y, pu.z, pu.w}, gw[4] = {pg.x, pg.y, pg.z, pg.w};
+        const uint32_t hw[4] = {ph.x, ph.y, ph.z, ph.w};
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const float xu = (u[e] - sr.x) * sr.y, xg = (g[e] - sr.z) * sr.w;
-          const float a = fmaf(xu, wx[e], cx[e]), sv = fmaf(xg, wg[e], cg[e]);
-          const float sg = sigmoid_fast(sv);
-          const float dxu = hv[e] * (sv * sg) * wx[e];
-          const float dxg = hv[e] * a * fmaf(sv * sg, 1.0f - sg, sg) * wg[e];
-          acc[0] += dxu;
-          acc[1] = fmaf(dxu, xu, acc[1]);
-          acc[2] += dxg;
-          acc[3] = fmaf(dxg, xg, acc[3]);
+        for (int e = 0; e < 4; ++e) {
+          const GatePair gp = gate_pair(unpack_bf16x2(uw[e]), unpack_bf16x2(gw[e]), rsu, cu, rsg, cgs, aff[j].wx[e],
+                                        aff[j].cx[e], aff[j].wg[e], aff[j].cg[e]);
+          const float2 dh = unpack_bf16x2(hw[e]);
+          const float2 dxu = mul2(mul2(dh, gp.q), aff[j].wx[e]);
+          const float2 dxg = mul2(mul2(mul2(dh, gp.a), gp.dsil), aff[j].wg[e]);
+          s1u = add2(s1u, dxu);
+          s2u = fma2(dxu, gp.xu, s2u);
+          s1g = add2(s1g, dxg);
+          s2g = fma2(dxg, gp.xg, s2g);
         }
       }
     }
+    float acc[4] = {s1u.x + s1u.y, s2u.x + s2u.y, s1g.x + s1g.y, s2g.x + s2g.y};
     block_sum<4>(acc, sm, slot);
     slot ^= 1;
     if (threadIdx.x == 0) rowsum[row] = make_float4(acc[0], acc[1], acc[2], acc[3]);
@@ -369,17 +415,10 @@ __global__ void __launch_bounds__(kApplyThreads) ln_gate_bwd_apply_kernel(
   const bool active = c0 < H;
   const int cc = active ? c0 : 0;
   const float inv_h = 1.0f / static_cast<float>(H);
-  float wx[8], cx[8], wg[8], cg[8];
-  {
-    const Affine8 a = load_affine8(gx, bx, gg, bg, static_cast<int64_t>(r) * H + cc);
-    unpack8(a.wx, wx);
-    unpack8(a.cx, cx);
-    unpack8(a.wg, wg);
-    unpack8(a.cg, cg);
-  }
-  float s_du[8], s_dg[8], s_gx[8], s_bx[8], s_gg[8], s_bg[8];
+  const AffineF aff = load_affine_f(gx, bx, gg, bg, static_cast<int64_t>(r) * H + cc);
+  float2 s_du[4], s_dg[4], s_gx[4], s_bx[4], s_gg[4], s_bg[4];
 #pragma unroll
-  for (int e = 0; e < 8; ++e) s_du[e] = s_dg[e] = s_gx[e] = s_bx[e] = s_gg[e] = s_bg[e] = 0.0f;
+  for (int e = 0; e < 4; ++e) s_du[e] = s_dg[e] = s_gx[e] = s_bx[e] = s_gg[e] = s_bg[e] = splat2(0.0f);
   const int rows_per = (M + nsplit - 1) / nsplit;
   const int n_begin = min(M, rsp * rows_per), n_end = min(M, n_begin + rows_per);
   const int n_rows = n_end - n_begin;
@@ -405,44 +444,47 @@ __global__ void __launch_bounds__(kApplyThreads) ln_gate_bwd_apply_kernel(
     const int s = i % kApplyStages;
     if (!active) continue;
     const int64_t row = rowbase + i;
-    float u[8], g[8], hv[8], du[8], dg[8];
-    unpack8(ring[s][0][threadIdx.x], u);
-    unpack8(ring[s][1][threadIdx.x], g);
-    unpack8(ring[s][2][threadIdx.x], hv);
+    const uint4 pu = ring[s][0][threadIdx.x], pg = ring[s][1][threadIdx.x], ph = ring[s][2][threadIdx.x];
     const uint4 stv = ring[s][3][threadIdx.x], rsv = ring[s][4][threadIdx.x];
-    const float4 st = make_float4(__uint_as_float(stv.x), __uint_as_float(stv.y), __uint_as_float(stv.z),
-                                  __uint_as_float(stv.w));
-    const float m1u = __uint_as_float(rsv.x) * inv_h, m2u = __uint_as_float(rsv.y) * inv_h;
-    const float m1g = __uint_as_float(rsv.z) * inv_h, m2g = __uint_as_float(rsv.w) * inv_h;
+    const float mu_u = __uint_as_float(stv.x), rs_u = __uint_as_float(stv.y);
+    const float mu_g = __uint_as_float(stv.z), rs_g = __uint_as_float(stv.w);
+    const float2 rsu = splat2(rs_u), cu = splat2(-mu_u * rs_u), rsg = splat2(rs_g), cgs = splat2(-mu_g * rs_g);
+    const float2 m1u = splat2(-__uint_as_float(rsv.x) * inv_h), m2u = splat2(-__uint_as_float(rsv.y) * inv_h);
+    const float2 m1g = splat2(-__uint_as_float(rsv.z) * inv_h), m2g = splat2(-__uint_as_float(rsv.w) * inv_h);
+    const uint32_t uw[4] = {pu.x, pu.y, pu.z, pu.w}, gw[4] = {pg.x, pg.y, pg.z, pg.w}, hw[4] = {ph.x, ph.y, ph.z, ph.w};
+    uint32_t ou[4], og[4];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      const float xu = (u[e] - st.x) * st.y, xg = (g[e] - st.z) * st.w;
-      const float a = fmaf(xu, wx[e], cx[e]), sv = fmaf(xg, wg[e], cg[e]);
-      const float sg = sigmoid_fast(sv);
-      const float da = hv[e] * (sv * sg);
-      const float ds = hv[e] * a * fmaf(sv * sg, 1.0f - sg, sg);
-      du[e] = st.y * (fmaf(da, wx[e], -m1u) - xu * m2u);
-      dg[e] = st.w * (fmaf(ds, wg[e], -m1g) - xg * m2g);
-      s_du[e] += du[e];
-      s_dg[e] += dg[e];
-      s_gx[e] = fmaf(da, xu, s_gx[e]);
-      s_bx[e] += da;
-      s_gg[e] = fmaf(ds, xg, s_gg[e]);
-      s_bg[e] += ds;
+    for (int e = 0; e < 4; ++e) {
+      const GatePair gp = gate_pair(unpack_bf16x2(uw[e]), unpack_bf16x2(gw[e]), rsu, cu, rsg, cgs, aff.wx[e], aff.cx[e],
+                                    aff.wg[e], aff.cg[e]);
+      const float2 dh = unpack_bf16x2(hw[e]);
+      const float2 da = mul2(dh, gp.q);
+      const float2 ds = mul2(mul2(dh, gp.a), gp.dsil);
+      // dU = rstd_u * (da*gx - mean(dx_u) - x_u*mean(dx_u*x_u)); same for dG
+      const float2 du = mul2(rsu, fma2(gp.xu, m2u, fma2(da, aff.wx[e], m1u)));
+      const float2 dg = mul2(rsg, fma2(gp.xg, m2g, fma2(ds, aff.wg[e], m1g)));
+      s_du[e] = add2(s_du[e], du);
+      s_dg[e] = add2(s_dg[e], dg);
+      s_gx[e] = fma2(da, gp.xu, s_gx[e]);
+      s_bx[e] = add2(s_bx[e], da);
+      s_gg[e] = fma2(ds, gp.xg, s_gg[e]);
+      s_bg[e] = add2(s_bg[e], ds);
+      ou[e] = pack_bf16x2(du.x, du.y);
+      og[e] = pack_bf16x2(dg.x, dg.y);
     }
-    store8_stream(dZ + row * zstride + c0, du);
-    store8_stream(dZ + row * zstride + H + c0, dg);
+    __stcs(reinterpret_cast<uint4*>(dZ + row * zstride + c0), make_uint4(ou[0], ou[1], ou[2], ou[3]));
+    __stcs(reinterpret_cast<uint4*>(dZ + row * zstride + H + c0), make_uint4(og[0], og[1], og[2], og[3]));
   }
   cp_async_wait<0>();
   if (!active) return;
   // part[t][split][q][c], q: dU, dG, da*x_u, da, ds*x_g, ds
   float* pp = part + (static_cast<int64_t>(t) * nsplit + rsp) * 6 * H + c0;
-  const float* src[6] = {s_du, s_dg, s_gx, s_bx, s_gg, s_bg};
+  const float2* src[6] = {s_du, s_dg, s_gx, s_bx, s_gg, s_bg};
 #pragma unroll
   for (int q = 0; q < 6; ++q) {
     float4* d4 = reinterpret_cast<float4*>(pp + q * static_cast<int64_t>(H));
-    d4[0] = make_float4(src[q][0], src[q][1], src[q][2], src[q][3]);
-    d4[1] = make_float4(src[q][4], src[q][5], src[q][6], src[q][7]);
+    d4[0] = make_float4(src[q][0].x, src[q][0].y, src[q][1].x, src[q][1].y);
+    d4[1] = make_float4(src[q][2].x, src[q][2].y, src[q][3].x, src[q][3].y);
   }
 }
 
