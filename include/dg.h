@@ -178,6 +178,31 @@ dg_status dg_tp_swiglu(int64_t S, int64_t d, int64_t ffn, int32_t W, int32_t bsz
                        const void* x_shards, const void* w13, const void* w2,
                        void* y_shards, void* ws, size_t ws_bytes, void* stream);
 
+/*
+ * dg_tp_swiglu_noalloc: the same SwiGLU pair as dg_tp_swiglu, for callers
+ * that cannot allocate device memory -- for example code that runs under a
+ * framework which owns the device's memory pool and accounts for every
+ * allocation, or a latency-critical path where cudaMalloc/cudaFree (which can
+ * synchronise the device) are not allowed.  No source page has a counterpart
+ * of this call; it exists for such callers only.
+ *
+ * The h activations live in a 32 MiB array built into the library instead of
+ * a caller workspace, so the call takes no scratch argument and allocates
+ * nothing: S*bsz*ffn*2 bytes must not exceed 32 MiB (33554432), otherwise
+ * the call returns DG_ERR_UNSUPPORTED without enqueuing anything.  Every
+ * device that loads the library holds that array until the process exits.
+ * The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call
+ * before any stream capture.  All calls on a device share the one array, so
+ * calls whose executions overlap on the GPU (different streams, no ordering
+ * between them) race on it; calls ordered on one stream are safe.  Each call
+ * overwrites all of h before reading it, so nothing needs clearing between
+ * calls.  Tensors, layouts and requirements are those of dg_tp_swiglu.
+ */
+dg_status dg_tp_swiglu_noalloc(int64_t S, int64_t d, int64_t ffn, int32_t W, int32_t bsz,
+                               const void* x_shards, const void* w13, const void* w2,
+                               void* y_shards, void* stream);
+
 /* ------------------------------------------------------------------------
  * Diagnostics.
  * dg_debug_wait_timeout launches one small kernel that waits, with the
