@@ -164,7 +164,7 @@ dg_status make_map_3d(CUtensorMap* map, bool is_bf16, const void* base, uint64_t
   return DG_OK;
 }
 
-int gemm_tile_m() { return 128; }
+int gemm_tile_m() { return kUsePairs ? 256 : 128; }
 
 int gemm_tile_n(GemmVariant v) { return v == GV_BF16_KK_SWIGLU ? 128 : 256; }
 
@@ -177,7 +177,7 @@ dg_status run_gemm(GemmVariant v, const CUtensorMap& a, const CUtensorMap& b, co
   const int64_t tiles = static_cast<int64_t>(p.G) * p.tiles_m * p.tiles_n;
   if (tiles == 0) return DG_OK;
   if (tiles > 0x7fffffff) return fail(DG_ERR_UNSUPPORTED, "too many output tiles (%lld)", (long long)tiles);
-  const int grid = static_cast<int>(tiles < dev.num_sms ? tiles : dev.num_sms);
+  const int grid = dev.num_sms;
   const double n_mma = v == GV_BF16_KK_SWIGLU ? 2.0 * p.N : static_cast<double>(p.N);
   TraceScope trace(name, s, 2.0 * p.G * static_cast<double>(p.M) * n_mma * p.K, bytes);
   cudaError_t e;
@@ -338,7 +338,7 @@ dg_status dg_gemm_fp8(int64_t M, int64_t N, int64_t K, const void* A, const void
   const void* b_ptr = K > 0 ? B : D;
   const uint64_t am = K > 0 ? static_cast<uint64_t>(M) : 1u, bn = K > 0 ? static_cast<uint64_t>(N) : 1u;
   if ((st = make_map_3d(&ma, false, a_ptr, kd, am, 1, kd, kd * am, 128, 128, 1, "A")) != DG_OK) return st;
-  if ((st = make_map_3d(&mb, false, b_ptr, kd, bn, 1, kd, kd * bn, 128, 256, 1, "B")) != DG_OK) return st;
+  if ((st = make_map_3d(&mb, false, b_ptr, kd, bn, 1, kd, kd * bn, 128, kKMajorBRows, 1, "B")) != DG_OK) return st;
   if ((st = make_map_3d(&md, true, D, N, M, 1, N * 2, N * 2 * M, 64, 32, 1, "D")) != DG_OK) return st;
   if (has_c) {
     if ((st = make_map_3d(&mc, true, C, N, M, 1, N * 2, N * 2 * M, 64, 32, 1, "C")) != DG_OK) return st;
@@ -503,7 +503,7 @@ dg_status dg_a2a_ffn_bwd(const dg_ffn_shape* shape, const void* inputs, const vo
   // (1) dHl_t = dY_t @ wout_t^T      (dY_t: the dispatched rows of dY)
   CUtensorMap mdy_k, mwo_k, mdh;
   if ((st = make_map_3d(&mdy_k, true, dY, D, T, M, D * 2, T * D * 2, 64, 1, 128, "dY")) != DG_OK) return st;
-  if ((st = make_map_3d(&mwo_k, true, wout, D, H, T, D * 2, H * D * 2, 64, 256, 1, "wout")) != DG_OK) return st;
+  if ((st = make_map_3d(&mwo_k, true, wout, D, H, T, D * 2, H * D * 2, 64, kKMajorBRows, 1, "wout")) != DG_OK) return st;
   if ((st = make_map_3d(&mdh, true, dHl, H, M, T, H * 2, M * H * 2, 64, 32, 1, "dHl")) != DG_OK) return st;
   GemmParams p{};
   p.G = static_cast<int32_t>(T);
@@ -573,7 +573,7 @@ dg_status dg_a2a_ffn_bwd(const dg_ffn_shape* shape, const void* inputs, const vo
   // (6) dX_t = dZ_t @ w1_t^T, stored at the rows dispatch read from (inverse permutation)
   CUtensorMap mdz_k, mw1_k, mdx;
   if ((st = make_map_3d(&mdz_k, true, dZ, 2 * H, M, T, 2 * H * 2, M * 2 * H * 2, 64, 128, 1, "dZ")) != DG_OK) return st;
-  if ((st = make_map_3d(&mw1_k, true, w1, 2 * H, D, T, 2 * H * 2, D * 2 * H * 2, 64, 256, 1, "w1 (K-major)")) != DG_OK)
+  if ((st = make_map_3d(&mw1_k, true, w1, 2 * H, D, T, 2 * H * 2, D * 2 * H * 2, 64, kKMajorBRows, 1, "w1 (K-major)")) != DG_OK)
     return st;
   if ((st = make_map_3d(&mdx, true, d_inputs, D, T, M, D * 2, T * D * 2, 64, 1, 32, "d_inputs")) != DG_OK) return st;
   p = GemmParams{};
@@ -693,7 +693,7 @@ dg_status dg_tp_swiglu(int64_t S, int64_t d, int64_t ffn, int32_t W, int32_t bsz
   // GEMM2: y = sum_s h_s @ w2_s^T = h @ w2^T; the shard sum is the K loop.
   CUtensorMap mh_k, mw2, my;
   if ((st = make_map_3d(&mh_k, true, ws, FF, R, 1, FF * 2, R * FF * 2, 64, 128, 1, "h (A)")) != DG_OK) return st;
-  if ((st = make_map_3d(&mw2, true, w2, FF, Dm, 1, FF * 2, Dm * FF * 2, 64, 256, 1, "w2")) != DG_OK) return st;
+  if ((st = make_map_3d(&mw2, true, w2, FF, Dm, 1, FF * 2, Dm * FF * 2, 64, kKMajorBRows, 1, "w2")) != DG_OK) return st;
   if ((st = make_map_3d(&my, true, y_shards, Dm, R, 1, Dm * 2, R * Dm * 2, 64, 32, 1, "y_shards")) != DG_OK) return st;
   p = GemmParams{};
   p.G = 1;

@@ -83,28 +83,32 @@ static __device__ __forceinline__ void chunk_mean_m2(const float (&v)[K], int lo
   m2 = q;
 }
 
-template <bool kFp8, bool kAMN, bool kBMN, int kEpi>
+template <bool kFp8, bool kAMN, bool kBMN, int kEpi, bool kPair>
 struct GemmCfg {
-  static constexpr int BM = 128;                      // UMMA M (one TMEM lane per row)
+  static constexpr int CTAS = kPair ? 2 : 1;          // CTAs sharing one UMMA (cta_group)
+  static constexpr int BM = 128;                      // rows per CTA (one TMEM lane per row)
+  static constexpr int UMMA_M = BM * CTAS;            // rows per MMA tile
   static constexpr int BN = 256;                      // UMMA N = accumulator columns
   static constexpr int BN_OUT = (kEpi == EPI_SWIGLU) ? BN / 2 : BN;
+  static constexpr int B_ROWS = BN / CTAS;            // B rows each CTA stages per K-block
   static constexpr int ROW_BYTES = 128;               // K-block = one 128-byte swizzle row
   static constexpr int BK = kFp8 ? 128 : 64;          // K elements per stage
   static constexpr int K_STEPS = 4;                   // UMMA K = 32 bytes: 16 bf16 / 32 e4m3
-  static constexpr int STAGES = 4;
+  static constexpr int STAGES = kPair ? 6 : 4;
   static constexpr int A_BYTES = BM * ROW_BYTES;      // 16 KB
-  static constexpr int B_BYTES = BN * ROW_BYTES;      // 32 KB
+  static constexpr int B_BYTES = B_ROWS * ROW_BYTES;  // 16 KB (pair) or 32 KB
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int MN_BOX_BYTES = 64 * 64 * 2;    // MN-major box: 64 k-rows x 64 bf16
   static constexpr int EPI_WARPS = 4;
   static constexpr int EPI_BUF_BYTES = 32 * 128;      // 32 rows x 64 bf16
   static constexpr int EPI_BYTES = EPI_WARPS * 2 * EPI_BUF_BYTES;
   static constexpr int NUM_THREADS = 64 + EPI_WARPS * 32;
-  static constexpr uint32_t TMEM_COLS = 2 * BN;
+  static constexpr int NACC = kPair ? 1 : 2;          // TMEM accumulators
+  static constexpr uint32_t TMEM_COLS = NACC * BN;
   static constexpr int NUM_BARS = 2 * STAGES + 4 + 2 * EPI_WARPS + 1;
   static constexpr int BAR_BYTES = 256;
   static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + EPI_BYTES + BAR_BYTES;
-  static constexpr uint32_t IDESC = umma_idesc(kFp8 ? 0u : 1u, kAMN, kBMN, BN, BM);
+  static constexpr uint32_t IDESC = umma_idesc(kFp8 ? 0u : 1u, kAMN, kBMN, BN, UMMA_M);
   static_assert(NUM_BARS * 8 + 4 <= BAR_BYTES, "barrier area");
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
   static_assert(!(kFp8 && (kAMN || kBMN)), "e4m3 operands are K-major here");
@@ -134,12 +138,12 @@ static __device__ __forceinline__ void tma_store_op(const CUtensorMap* map, cons
 
 static __device__ __forceinline__ float silu_f(float x) { return x / (1.0f + __expf(-x)); }
 
-template <bool kFp8, bool kAMN, bool kBMN, int kEpi>
-__global__ void __launch_bounds__(GemmCfg<kFp8, kAMN, kBMN, kEpi>::NUM_THREADS, 1)
+template <bool kFp8, bool kAMN, bool kBMN, int kEpi, bool kPair>
+__global__ void __launch_bounds__(GemmCfg<kFp8, kAMN, kBMN, kEpi, kPair>::NUM_THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmD, const __grid_constant__ CUtensorMap tmC,
                    const GemmParams p) {
-  using Cfg = GemmCfg<kFp8, kAMN, kBMN, kEpi>;
+  using Cfg = GemmCfg<kFp8, kAMN, kBMN, kEpi, kPair>;
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint32_t s_abort;
 
@@ -159,9 +163,23 @@ __global__ void __launch_bounds__(GemmCfg<kFp8, kAMN, kBMN, kEpi>::NUM_THREADS, 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  // A sticky device error from an earlier failure: do nothing.
-  if (threadIdx.x == 0) s_abort = ld_volatile_u32(p.err);
-  __syncthreads();
+  const uint32_t rank = kPair ? cluster_ctarank() : 0u;  // position in the CTA pair
+  const bool leader = rank == 0u;
+
+  // A sticky device error from an earlier failure: do nothing.  In a CTA pair
+  // the leader decides for both, so the pair's control flow stays uniform.
+  if (kPair) {
+    cluster_sync_all();  // both CTAs are running before any access to the peer's shared memory
+    if (threadIdx.x == 0 && leader) {
+      const uint32_t v = ld_volatile_u32(p.err);
+      st_cluster_u32(mapa_shared(smem_u32(&s_abort), 0), v);
+      st_cluster_u32(mapa_shared(smem_u32(&s_abort), 1), v);
+    }
+    cluster_sync_all();
+  } else {
+    if (threadIdx.x == 0) s_abort = ld_volatile_u32(p.err);
+    __syncthreads();
+  }
   if (s_abort != 0u) return;
 
   if (warp == 0 && lane == 0) {
@@ -171,7 +189,7 @@ __global__ void __launch_bounds__(GemmCfg<kFp8, kAMN, kBMN, kEpi>::NUM_THREADS, 
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull[a], 1);
-      mbar_init(&tempty[a], Cfg::EPI_WARPS);
+      mbar_init(&tempty[a], Cfg::EPI_WARPS * Cfg::CTAS);
     }
     for (int i = 0; i < 2 * Cfg::EPI_WARPS; ++i) mbar_init(&cbar[i], 1);
     mbar_init(drain, 1);
@@ -182,17 +200,27 @@ __global__ void __launch_bounds__(GemmCfg<kFp8, kAMN, kBMN, kEpi>::NUM_THREADS, 
     if (kEpi == EPI_FP8 && p.has_c) tma_prefetch_desc(&tmC);
   }
   if (warp == 1) {
-    tmem_alloc(tmem_holder, Cfg::TMEM_COLS);
-    tmem_relinquish();
+    if (kPair) {
+      tmem_alloc_pair(tmem_holder, Cfg::TMEM_COLS);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(tmem_holder, Cfg::TMEM_COLS);
+      tmem_relinquish();
+    }
   }
   tc_fence_before_sync();
-  __syncthreads();
+  if (kPair)
+    cluster_sync_all();
+  else
+    __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem_base = *tmem_holder;
 
   const int tiles_per_group = p.tiles_m * p.tiles_n;
   const int total_tiles = p.G * tiles_per_group;
   const int num_kb = (p.K + Cfg::BK - 1) / Cfg::BK;
+  const int unit = static_cast<int>(blockIdx.x) / Cfg::CTAS;  // this CTA's (pair's) slot in the schedule
+  const int num_units = static_cast<int>(gridDim.x) / Cfg::CTAS;
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -201,37 +229,56 @@ __global__ void __launch_bounds__(GemmCfg<kFp8, kAMN, kBMN, kEpi>::NUM_THREADS, 
       uint32_t phase = 0;
       uint32_t armed = 0, armed_parity = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x) {
+      for (int tile = unit; tile < total_tiles && ok; tile += num_units) {
         const int g = tile / tiles_per_group;
         const int rem = tile - g * tiles_per_group;
-        const int m0 = (rem % p.tiles_m) * Cfg::BM;
+        const int m0 = (rem % p.tiles_m) * Cfg::UMMA_M + static_cast<int>(rank) * Cfg::BM;
         const int n0 = (rem / p.tiles_m) * Cfg::BN_OUT;
         for (int kb = 0; kb < num_kb; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1u, p.err, SITE_EMPTY)) {
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(&full[stage], Cfg::STAGE_BYTES);
+          // The pair's loads all complete on the leader's full barrier.
+          if (leader) mbar_arrive_expect_tx(&full[stage], Cfg::STAGE_BYTES * Cfg::CTAS);
+          const uint32_t bar_c = kPair ? mapa_shared(smem_u32(&full[stage]), 0) : smem_u32(&full[stage]);
           uint8_t* sa = stage_base + stage * Cfg::STAGE_BYTES;
           uint8_t* sb = sa + Cfg::A_BYTES;
           const int k0 = kb * Cfg::BK;
+          auto load = [&](void* dst, const CUtensorMap* map, int32_t x, int32_t y, int32_t g3, int32_t mode) {
+            int32_t c1 = y, c2 = g3;
+            if (mode == G_MID) {
+              c1 = g3;
+              c2 = y;
+            } else if (mode == G_NONE) {
+              c2 = 0;
+            }
+            if (kPair)
+              tma_load_3d_pair(dst, map, bar_c, x, c1, c2);
+            else
+              tma_load_3d(dst, map, &full[stage], x, c1, c2);
+          };
           if (!kAMN) {
-            tma_load_op(sa, &tmA, &full[stage], k0, m0, g, p.a_g);
+            load(sa, &tmA, k0, m0, g, p.a_g);
           } else {
 #pragma unroll
-            for (int i = 0; i < Cfg::BM / 64; ++i)
-              tma_load_op(sa + i * Cfg::MN_BOX_BYTES, &tmA, &full[stage], m0 + 64 * i, k0, g, p.a_g);
+            for (int i = 0; i < Cfg::BM / 64; ++i) load(sa + i * Cfg::MN_BOX_BYTES, &tmA, m0 + 64 * i, k0, g, p.a_g);
           }
           if (kEpi == EPI_SWIGLU) {
-            // rows [c0, c0+BN/2) of w1_g, then the same rows of w3_g
-            tma_load_3d(sb, &tmB, &full[stage], k0, n0, 2 * g);
-            tma_load_3d(sb + (Cfg::BN / 2) * Cfg::ROW_BYTES, &tmB, &full[stage], k0, n0, 2 * g + 1);
+            // rows [c0, c0+BN/2) of w1_g, then the same rows of w3_g (one plane per CTA of a pair)
+            if (kPair) {
+              load(sb, &tmB, k0, n0, 2 * g + static_cast<int>(rank), G_OUTER);
+            } else {
+              load(sb, &tmB, k0, n0, 2 * g, G_OUTER);
+              load(sb + (Cfg::BN / 2) * Cfg::ROW_BYTES, &tmB, k0, n0, 2 * g + 1, G_OUTER);
+            }
           } else if (!kBMN) {
-            tma_load_op(sb, &tmB, &full[stage], k0, n0, g, p.b_g);
+            load(sb, &tmB, k0, n0 + static_cast<int>(rank) * Cfg::B_ROWS, g, p.b_g);
           } else {
 #pragma unroll
-            for (int i = 0; i < Cfg::BN / 64; ++i)
-              tma_load_op(sb + i * Cfg::MN_BOX_BYTES, &tmB, &full[stage], n0 + 64 * i, k0, g, p.b_g);
+            for (int i = 0; i < Cfg::B_ROWS / 64; ++i)
+              load(sb + i * Cfg::MN_BOX_BYTES, &tmB, n0 + static_cast<int>(rank) * Cfg::B_ROWS + 64 * i, k0, g,
+                   p.b_g);
           }
           armed |= 1u << stage;
           armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
@@ -241,9 +288,10 @@ __global__ void __launch_bounds__(GemmCfg<kFp8, kAMN, kBMN, kEpi>::NUM_THREADS, 
           }
         }
       }
-      // Every load this thread issued must land before the CTA exits.
+      // Every load issued must land before the CTA exits (the leader's full
+      // barriers count the loads of both CTAs of a pair).
       for (int s = 0; s < Cfg::STAGES; ++s)
-        if (armed & (1u << s)) {
+        if (leader && (armed & (1u << s))) {
           if (!mbar_try_wait(&full[s], (armed_parity >> s) & 1u)) {
             uint32_t dummy = 0;
             mbar_wait_slow(&full[s], (armed_parity >> s) & 1u, &dummy, SITE_DRAIN, kWaitLimitNs);
@@ -251,14 +299,14 @@ __global__ void __launch_bounds__(GemmCfg<kFp8, kAMN, kBMN, kEpi>::NUM_THREADS, 
         }
     }
   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // ------------------------------------------------------------ MMA issuer (pair leader)
+    if (lane == 0 && leader) {
       int stage = 0;
       uint32_t phase = 0, tphase = 0;
       bool ok = true;
       int local = 0;
-      for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x, ++local) {
-        const int acc = local & 1;
+      for (int tile = unit; tile < total_tiles && ok; tile += num_units, ++local) {
+        const int acc = local & (Cfg::NACC - 1);
         if (!mbar_wait(&tempty[acc], ((tphase >> acc) & 1u) ^ 1u, p.err, SITE_TEMPTY)) {
           ok = false;
           break;
@@ -284,22 +332,38 @@ __global__ void __launch_bounds__(GemmCfg<kFp8, kAMN, kBMN, kEpi>::NUM_THREADS, 
             const uint64_t bd = kBMN ? smem_desc_sw128(sb + j * 2048, Cfg::MN_BOX_BYTES, 1024)
                                      : smem_desc_sw128(sb + j * 32, 16, 1024);
             const uint32_t accum = (kb > 0 || j > 0) ? 1u : 0u;
-            if (kFp8)
-              umma_f8(d_tmem, ad, bd, Cfg::IDESC, accum);
-            else
-              umma_bf16(d_tmem, ad, bd, Cfg::IDESC, accum);
+            if (kPair) {
+              if (kFp8)
+                umma_f8_pair(d_tmem, ad, bd, Cfg::IDESC, accum);
+              else
+                umma_bf16_pair(d_tmem, ad, bd, Cfg::IDESC, accum);
+            } else {
+              if (kFp8)
+                umma_f8(d_tmem, ad, bd, Cfg::IDESC, accum);
+              else
+                umma_bf16(d_tmem, ad, bd, Cfg::IDESC, accum);
+            }
           }
-          tc_commit(&empty[stage]);
+          if (kPair)
+            tc_commit_pair_mc(&empty[stage], 0x3);
+          else
+            tc_commit(&empty[stage]);
           if (++stage == Cfg::STAGES) {
             stage = 0;
             phase ^= 1u;
           }
         }
         if (!ok) break;
-        tc_commit(&tfull[acc]);
+        if (kPair)
+          tc_commit_pair_mc(&tfull[acc], 0x3);
+        else
+          tc_commit(&tfull[acc]);
       }
       // Every MMA this thread issued must complete before TMEM is released.
-      tc_commit(drain);
+      if (kPair)
+        tc_commit_pair_mc(drain, 0x1);
+      else
+        tc_commit(drain);
       if (!mbar_try_wait(drain, 0)) {
         uint32_t dummy = 0;
         mbar_wait_slow(drain, 0, &dummy, SITE_DRAIN, kWaitLimitNs);
@@ -318,12 +382,12 @@ __global__ void __launch_bounds__(GemmCfg<kFp8, kAMN, kBMN, kEpi>::NUM_THREADS, 
     bool ok = true;
     const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(32 * lg) << 16);
     int local = 0;
-    for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x, ++local) {
+    for (int tile = unit; tile < total_tiles && ok; tile += num_units, ++local) {
       const int g = tile / tiles_per_group;
       const int rem = tile - g * tiles_per_group;
-      const int m0 = (rem % p.tiles_m) * Cfg::BM;
+      const int m0 = (rem % p.tiles_m) * Cfg::UMMA_M + static_cast<int>(rank) * Cfg::BM;
       const int n0 = (rem / p.tiles_m) * Cfg::BN_OUT;
-      const int acc = local & 1;
+      const int acc = local & (Cfg::NACC - 1);
       const int row0 = m0 + 32 * lg;
       int nchunks = (p.N - n0 + 63) / 64;
       if (nchunks > Cfg::BN_OUT / 64) nchunks = Cfg::BN_OUT / 64;
@@ -482,7 +546,12 @@ __global__ void __launch_bounds__(GemmCfg<kFp8, kAMN, kBMN, kEpi>::NUM_THREADS, 
       chunk_ctr += static_cast<uint32_t>(nchunks);
       tc_fence_before_sync();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&tempty[acc]);
+      if (lane == 0) {
+        if (kPair)
+          mbar_arrive_cluster(mapa_shared(smem_u32(&tempty[acc]), 0));
+        else
+          mbar_arrive(&tempty[acc]);
+      }
     }
     // Outstanding copies of this warp must finish before the CTA exits.
     if (lane == 0) bulk_wait_group<0>();
@@ -494,10 +563,16 @@ __global__ void __launch_bounds__(GemmCfg<kFp8, kAMN, kBMN, kEpi>::NUM_THREADS, 
   }
 
   tc_fence_before_sync();
-  __syncthreads();
+  if (kPair)
+    cluster_sync_all();
+  else
+    __syncthreads();
   if (warp == 1) {
     tc_fence_after_sync();
-    tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
+    if (kPair)
+      tmem_dealloc_pair(tmem_base, Cfg::TMEM_COLS);
+    else
+      tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
   }
 }
 

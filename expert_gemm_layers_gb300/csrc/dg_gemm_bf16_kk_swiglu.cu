@@ -4,8 +4,8 @@
 namespace dg {
 
 cudaError_t launch_gemm_bf16_kk_swiglu(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& d,
-                                       const CUtensorMap& c, const GemmParams& p, int grid, cudaStream_t s) {
-  return launch_gemm_t<false, false, false, EPI_SWIGLU>(a, b, d, c, p, grid, s);
+                                       const CUtensorMap& c, const GemmParams& p, int num_sms, cudaStream_t s) {
+  return launch_gemm_t<false, false, false, EPI_SWIGLU>(a, b, d, c, p, num_sms, s);
 }
 
 }  // namespace dg

@@ -65,28 +65,56 @@ class TraceScope {
 
 // Launchers, one per translation unit.
 cudaError_t launch_gemm_fp8_kk(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
-                               const GemmParams&, int grid, cudaStream_t);
+                               const GemmParams&, int num_sms, cudaStream_t);
 cudaError_t launch_gemm_bf16_kk_store(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
-                                      const CUtensorMap&, const GemmParams&, int grid, cudaStream_t);
+                                      const CUtensorMap&, const GemmParams&, int num_sms, cudaStream_t);
 cudaError_t launch_gemm_bf16_km_bias(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
-                                     const CUtensorMap&, const GemmParams&, int grid, cudaStream_t);
+                                     const CUtensorMap&, const GemmParams&, int num_sms, cudaStream_t);
 cudaError_t launch_gemm_bf16_mm_store(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
-                                      const CUtensorMap&, const GemmParams&, int grid, cudaStream_t);
+                                      const CUtensorMap&, const GemmParams&, int num_sms, cudaStream_t);
 cudaError_t launch_gemm_bf16_kk_swiglu(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
-                                       const CUtensorMap&, const GemmParams&, int grid, cudaStream_t);
+                                       const CUtensorMap&, const GemmParams&, int num_sms, cudaStream_t);
 cudaError_t launch_gemm_bf16_km_lnstats(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
-                                        const CUtensorMap&, const GemmParams&, int grid, cudaStream_t);
+                                        const CUtensorMap&, const GemmParams&, int num_sms, cudaStream_t);
 
-// Host launcher body shared by the instantiation units.
+// The GEMMs run as CTA pairs (cta_group::2, 256-row tiles, clusters of 2).
+constexpr bool kUsePairs = true;
+
+// Rows of a K-major B tile each CTA loads (the TMA box height of such B maps).
+constexpr int kKMajorBRows = kUsePairs ? 128 : 256;
+
+// Host launcher body shared by the instantiation units: one persistent launch,
+// one CTA (or CTA pair) per SM (pair of SMs) up to the number of tiles.
 template <bool kFp8, bool kAMN, bool kBMN, int kEpi>
 cudaError_t launch_gemm_t(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& d, const CUtensorMap& c,
-                          const GemmParams& p, int grid, cudaStream_t s) {
-  using Cfg = GemmCfg<kFp8, kAMN, kBMN, kEpi>;
-  auto kern = gemm_tc_kernel<kFp8, kAMN, kBMN, kEpi>;
+                          const GemmParams& p, int num_sms, cudaStream_t s) {
+  using Cfg = GemmCfg<kFp8, kAMN, kBMN, kEpi, kUsePairs>;
+  auto kern = gemm_tc_kernel<kFp8, kAMN, kBMN, kEpi, kUsePairs>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  kern<<<grid, Cfg::NUM_THREADS, Cfg::SMEM_BYTES, s>>>(a, b, d, c, p);
-  return cudaGetLastError();
+  const int64_t tiles = static_cast<int64_t>(p.G) * p.tiles_m * p.tiles_n;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  cfg.blockDim = dim3(Cfg::NUM_THREADS);
+  cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
+  cfg.stream = s;
+  int units = num_sms;
+  if (kUsePairs) {
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cfg.gridDim = dim3(2);
+    int clusters = 0;
+    e = cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg);
+    if (e != cudaSuccess) return e;
+    units = clusters > 0 ? clusters : 1;
+  }
+  if (tiles < units) units = static_cast<int>(tiles);
+  cfg.gridDim = dim3(units * Cfg::CTAS);
+  return cudaLaunchKernelEx(&cfg, kern, a, b, d, c, p);
 }
 
 // ---------------------------------------------------------------- row kernels (dg_rowops.cu)

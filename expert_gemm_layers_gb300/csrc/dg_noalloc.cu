@@ -47,9 +47,8 @@ dg_status launch_untraced(GemmVariant v, const CUtensorMap& a, const CUtensorMap
   p.err = dev.err;
   const int64_t tiles = static_cast<int64_t>(p.G) * p.tiles_m * p.tiles_n;
   if (tiles == 0) return DG_OK;
-  const int grid = static_cast<int>(tiles < dev.num_sms ? tiles : dev.num_sms);
-  cudaError_t e = v == GV_BF16_KK_SWIGLU ? launch_gemm_bf16_kk_swiglu(a, b, d, d, p, grid, s)
-                                         : launch_gemm_bf16_kk_store(a, b, d, d, p, grid, s);
+  cudaError_t e = v == GV_BF16_KK_SWIGLU ? launch_gemm_bf16_kk_swiglu(a, b, d, d, p, dev.num_sms, s)
+                                         : launch_gemm_bf16_kk_store(a, b, d, d, p, dev.num_sms, s);
   if (e != cudaSuccess) return fail(DG_ERR_CUDA, "tp_swiglu_noalloc: GEMM launch: %s", cudaGetErrorString(e));
   return DG_OK;
 }
@@ -109,7 +108,7 @@ extern "C" dg_status dg_tp_swiglu_noalloc(int64_t S, int64_t d, int64_t ffn, int
   // GEMM2: y = h @ w2^T, the shard sum being the K loop.
   CUtensorMap mh_k, mw2, my;
   if ((st = make_map_3d(&mh_k, true, h, FF, R, 1, FF * 2, R * FF * 2, 64, 128, 1, "h (A)")) != DG_OK) return st;
-  if ((st = make_map_3d(&mw2, true, w2, FF, Dm, 1, FF * 2, Dm * FF * 2, 64, 256, 1, "w2")) != DG_OK) return st;
+  if ((st = make_map_3d(&mw2, true, w2, FF, Dm, 1, FF * 2, Dm * FF * 2, 64, kKMajorBRows, 1, "w2")) != DG_OK) return st;
   if ((st = make_map_3d(&my, true, y_shards, Dm, R, 1, Dm * 2, R * Dm * 2, 64, 32, 1, "y_shards")) != DG_OK) return st;
   p = GemmParams{};
   p.G = 1;
