@@ -103,7 +103,7 @@ struct GemmCfg {
   static constexpr int EPI_BUF_BYTES = 32 * 128;      // 32 rows x 64 bf16
   static constexpr int EPI_BYTES = EPI_WARPS * 2 * EPI_BUF_BYTES;
   static constexpr int NUM_THREADS = 64 + EPI_WARPS * 32;
-  static constexpr int NACC = kPair ? 1 : 2;          // TMEM accumulators
+  static constexpr int NACC = 2;                      // TMEM accumulators (double buffered)
   static constexpr uint32_t TMEM_COLS = NACC * BN;
   static constexpr int NUM_BARS = 2 * STAGES + 4 + 2 * EPI_WARPS + 1;
   static constexpr int BAR_BYTES = 256;
