@@ -40,9 +40,32 @@ MEASURED_PEAKS = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK_PEAKS = dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0)
 
 # Per-launch DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) from
-# one ncu capture of each kernel, with the source file hash it was taken at;
-# a kernel whose source changed since reports null.
-TRAFFIC = {}
+# one ncu capture of the kernel, scaled to the benchmark's launch, with the
+# sha256 of its sources at capture time; a kernel whose sources changed since
+# reports null.  Capture summary: profiles/gemm_tc_kernel_ffn_T8_and_fp8_4096.md.
+TRAFFIC = {
+    "ffn_bwd_dw1": {
+        "bytes_per_launch": 8 * (1.133279e9 + 0.299984e9),   # captured at T=8; the benchmark has T=64
+        "sources": ["expert_gemm_layers_gb300/csrc/dg_gemm.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh",
+                    "expert_gemm_layers_gb300/csrc/dg_gemm_bf16_mm_store.cu"],
+        "sha256": "feaf07905b5222e4e4b69f62c7673263a7bd31922ed82ea266eb033bd50374a9",
+    },
+}
+
+
+def traffic_for(kernel: str):
+    import hashlib
+    t = TRAFFIC.get(kernel)
+    if not t:
+        return None
+    h = hashlib.sha256()
+    for f in t["sources"]:
+        try:
+            with open(os.path.join(ROOT, f), "rb") as fh:
+                h.update(fh.read())
+        except OSError:
+            return None
+    return t["bytes_per_launch"] if h.hexdigest() == t["sha256"] else None
 
 
 def gemm_flops():
@@ -379,7 +402,7 @@ def run_dg(args, rank, world):
                 "frac": round(achieved / peak, 4)}
     roof["kernel"] = top["name"]
     roof["peak_source"] = peaks["source"] + (" sustained bf16" if top["flops"] > 0 else " HBM copy")
-    roof["traffic"] = TRAFFIC.get(top["name"], {}).get("bytes_per_launch")
+    roof["traffic"] = traffic_for(top["name"])
     total_ms = sum(e["total_ms"] for e in trace)
     kernel_table = {e["name"]: {"launches": e["launches"], "ms_per_launch": round(e["total_ms"] / e["launches"], 4),
                                 "share": round(e["total_ms"] / total_ms, 4)} for e in trace}
