@@ -9,6 +9,7 @@
 // (what the page's bmm path normalises), two passes over registers.
 #include <cuda_bf16.h>
 
+#include "dg_gate.cuh"
 #include "dg_internal.h"
 
 namespace dg {
@@ -35,23 +36,6 @@ __device__ __forceinline__ void store8_stream(__nv_bfloat16* p, const float (&f)
   v.z = pack_bf16x2(f[4], f[5]);
   v.w = pack_bf16x2(f[6], f[7]);
   __stcs(reinterpret_cast<uint4*>(p), v);
-}
-
-// sigmoid(x) = (1 + tanh(x/2)) / 2, with the hardware tanh approximation
-// (tanh.approx.f32, relative error about 2^-11): one MUFU operation instead of
-// an exponential and a division.
-__device__ __forceinline__ float tanh_fast(float x) {
-  float y;
-  asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-
-__device__ __forceinline__ float sigmoid_fast(float x) { return fmaf(0.5f, tanh_fast(0.5f * x), 0.5f); }
-
-// silu(x) = x * sigmoid(x) = h + h * tanh(h) with h = x/2.
-__device__ __forceinline__ float silu_fast(float x) {
-  const float h = 0.5f * x;
-  return fmaf(h, tanh_fast(h), h);
 }
 
 // Block-uniform read of the error word (a divergent early return ahead of a
@@ -104,83 +88,6 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 template <int N>
 __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-
-// bf16x2-packed affine parameters of one 8-column vector (held for all rows).
-struct Affine8 {
-  uint4 wx, cx, wg, cg;
-};
-
-__device__ __forceinline__ Affine8 load_affine8(const __nv_bfloat16* gx, const __nv_bfloat16* bx,
-                                                const __nv_bfloat16* gg, const __nv_bfloat16* bg, int64_t off) {
-  Affine8 a;
-  a.wx = __ldg(reinterpret_cast<const uint4*>(gx + off));
-  a.cx = __ldg(reinterpret_cast<const uint4*>(bx + off));
-  a.wg = __ldg(reinterpret_cast<const uint4*>(gg + off));
-  a.cg = __ldg(reinterpret_cast<const uint4*>(bg + off));
-  return a;
-}
-
-// Packed two-lane fp32 arithmetic (fma/mul .f32x2): one issue slot for two lanes.
-__device__ __forceinline__ unsigned long long f2u(float2 a) { return *reinterpret_cast<unsigned long long*>(&a); }
-__device__ __forceinline__ float2 u2f(unsigned long long a) { return *reinterpret_cast<float2*>(&a); }
-__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
-  unsigned long long d;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(f2u(a)), "l"(f2u(b)), "l"(f2u(c)));
-  return u2f(d);
-}
-__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
-  unsigned long long d;
-  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(f2u(a)), "l"(f2u(b)));
-  return u2f(d);
-}
-__device__ __forceinline__ float2 add2(float2 a, float2 b) {
-  unsigned long long d;
-  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(f2u(a)), "l"(f2u(b)));
-  return u2f(d);
-}
-__device__ __forceinline__ float2 splat2(float x) { return make_float2(x, x); }
-
-// Affine parameters of one 8-column vector as four fp32 pairs each.
-struct AffineF {
-  float2 wx[4], cx[4], wg[4], cg[4];
-};
-
-__device__ __forceinline__ AffineF load_affine_f(const __nv_bfloat16* gx, const __nv_bfloat16* bx,
-                                                 const __nv_bfloat16* gg, const __nv_bfloat16* bg, int64_t off) {
-  const Affine8 a = load_affine8(gx, bx, gg, bg, off);
-  const uint32_t w0[4] = {a.wx.x, a.wx.y, a.wx.z, a.wx.w}, w1[4] = {a.cx.x, a.cx.y, a.cx.z, a.cx.w};
-  const uint32_t w2[4] = {a.wg.x, a.wg.y, a.wg.z, a.wg.w}, w3[4] = {a.cg.x, a.cg.y, a.cg.z, a.cg.w};
-  AffineF f;
-#pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    f.wx[e] = unpack_bf16x2(w0[e]);
-    f.cx[e] = unpack_bf16x2(w1[e]);
-    f.wg[e] = unpack_bf16x2(w2[e]);
-    f.cg[e] = unpack_bf16x2(w3[e]);
-  }
-  return f;
-}
-
-// Forward quantities of the gate at one column pair, recomputed from Z:
-// x_u, x_g (normalised), a = LN_x(U), s = LN_g(G), q = silu(s), silu'(s).
-struct GatePair {
-  float2 xu, xg, a, q, dsil;
-};
-
-__device__ __forceinline__ GatePair gate_pair(float2 u, float2 g, float2 rsu, float2 cu, float2 rsg, float2 cg_,
-                                              float2 wx, float2 cx, float2 wg, float2 cgb) {
-  GatePair r;
-  r.xu = fma2(u, rsu, cu);
-  r.xg = fma2(g, rsg, cg_);
-  r.a = fma2(r.xu, wx, cx);
-  const float2 sv = fma2(r.xg, wg, cgb);
-  const float2 h = mul2(sv, splat2(0.5f));
-  const float2 sig = fma2(make_float2(tanh_fast(h.x), tanh_fast(h.y)), splat2(0.5f), splat2(0.5f));
-  r.q = mul2(sv, sig);
-  // silu'(s) = sig + s*sig*(1 - sig) = q*(1 - sig) + sig
-  r.dsil = fma2(r.q, fma2(sig, splat2(-1.0f), splat2(1.0f)), sig);
-  return r;
 }
 
 // ------------------------------------------------------------------ forward
@@ -304,96 +211,31 @@ __global__ void __launch_bounds__(NT, 512 / NT) ln_gate_fwd_kernel(
 // silu'(s) = sig(s) + s*sig(s)*(1 - sig(s)), dx_u = da*gx,
 // dU = rstd_u * (dx_u - mean(dx_u) - x_u*mean(dx_u*x_u)), and the same for G.
 //
-// Pass 1 (row sums): one CTA per row computes sum(dx_u), sum(dx_u*x_u),
-// sum(dx_g), sum(dx_g*x_g) -> rowsum[row]; rows staged like the forward.
+// Pass 1 (row sums) runs in the epilogue of the GEMM that produces dHl: per
+// 256-column tile it sums dx_u, dx_u*x_u, dx_g, dx_g*x_g of each row;
+// rowsum_finalize adds the tiles in order.
 // Pass 2 (apply): a CTA owns a column block of one token position t and a
 // range of its rows: it writes dZ and sums, per column, dU, dG (db1),
 // da*x_u, da (norm_x grads), ds*x_g, ds (norm_gate grads) in registers; the
 // per-(t, row range) partial sums are added in a fixed order afterwards.
 
-constexpr int kBwdStages = 3;
-
-template <int NT, int VPT>
-__global__ void __launch_bounds__(NT, 512 / NT) ln_gate_bwd_rowsum_kernel(
-    const __nv_bfloat16* __restrict__ Z, const float4* __restrict__ stats, const __nv_bfloat16* __restrict__ dHl,
-    const __nv_bfloat16* __restrict__ gx, const __nv_bfloat16* __restrict__ bx, const __nv_bfloat16* __restrict__ gg,
-    const __nv_bfloat16* __restrict__ bg, float4* __restrict__ rowsum, int M, int L, int H, int ctas_per_rank,
-    const uint32_t* err) {
-  extern __shared__ uint4 ring[];  // [kBwdStages][VPT][3][NT]
-  __shared__ float sm[2][kMaxRowWarps][4];
-  if (block_aborted(err)) return;
-  const int nvec = H >> 3;
-  const int64_t zstride = 2 * static_cast<int64_t>(H);
-  const int r = blockIdx.x / ctas_per_rank;
-  const int64_t rank_rows = static_cast<int64_t>(L) * M;
-  const int64_t stride = ctas_per_rank;
-  const int64_t n_mine = (rank_rows - (blockIdx.x % ctas_per_rank) + stride - 1) / stride;
-  const int64_t row0 = static_cast<int64_t>(r) * rank_rows + (blockIdx.x % ctas_per_rank);
-
-  AffineF aff[VPT];
-#pragma unroll
-  for (int j = 0; j < VPT; ++j) {
-    const int v = threadIdx.x + NT * j;
-    aff[j] = load_affine_f(gx, bx, gg, bg, static_cast<int64_t>(r) * H + 8 * (v < nvec ? v : 0));
-  }
-  auto issue = [&](int64_t i) {
-    if (i < n_mine) {
-      const int64_t row = row0 + i * stride;
-      const __nv_bfloat16* zu = Z + row * zstride;
-      const __nv_bfloat16* dh = dHl + row * H;
-      uint4* st = ring + (i % kBwdStages) * (VPT * 3 * NT);
-#pragma unroll
-      for (int j = 0; j < VPT; ++j) {
-        const int v = threadIdx.x + NT * j;
-        const bool ok = v < nvec;
-        const int vv = ok ? v : 0;
-        cp_async16(st + (3 * j) * NT + threadIdx.x, zu + 8 * vv, ok);
-        cp_async16(st + (3 * j + 1) * NT + threadIdx.x, zu + H + 8 * vv, ok);
-        cp_async16(st + (3 * j + 2) * NT + threadIdx.x, dh + 8 * vv, ok);
-      }
+__global__ void rowsum_finalize_kernel(const float4* __restrict__ part, float4* __restrict__ rowsum, int T, int M,
+                                       int tiles_n, const uint32_t* err) {
+  if (ld_volatile_u32(err) != 0u) return;
+  const int64_t rows = static_cast<int64_t>(T) * M;
+  for (int64_t row = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; row < rows;
+       row += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int t = static_cast<int>(row / M), n = static_cast<int>(row - static_cast<int64_t>(t) * M);
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int nt = 0; nt < tiles_n; ++nt) {
+      const float4 q = part[(static_cast<int64_t>(t) * tiles_n + nt) * M + n];
+      acc.x += q.x;
+      acc.y += q.y;
+      acc.z += q.z;
+      acc.w += q.w;
     }
-    cp_async_commit();
-  };
-#pragma unroll
-  for (int i = 0; i < kBwdStages - 1; ++i) issue(i);
-  float4 sr_next = n_mine > 0 ? stats[row0] : make_float4(0.f, 0.f, 0.f, 0.f);
-  int slot = 0;
-  for (int64_t i = 0; i < n_mine; ++i) {
-    issue(i + kBwdStages - 1);
-    const int64_t row = row0 + i * stride;
-    const float4 sr = sr_next;
-    if (i + 1 < n_mine) sr_next = stats[row + stride];
-    cp_async_wait<kBwdStages - 1>();
-    const uint4* st = ring + (i % kBwdStages) * (VPT * 3 * NT);
-    const float2 rsu = splat2(sr.y), cu = splat2(-sr.x * sr.y), rsg = splat2(sr.w), cgs = splat2(-sr.z * sr.w);
-    float2 s1u = splat2(0.f), s2u = splat2(0.f), s1g = splat2(0.f), s2g = splat2(0.f);
-#pragma unroll
-    for (int j = 0; j < VPT; ++j) {
-      if (threadIdx.x + NT * j < nvec) {
-        const uint4 pu = st[(3 * j) * NT + threadIdx.x], pg = st[(3 * j + 1) * NT + threadIdx.x];
-        const uint4 ph = st[(3 * j + 2) * NT + threadIdx.x];
-        const uint32_t uw[4] = {pu.x, pu.y, pu.z, pu.w}, gw[4] = {pg.x, pg.y, pg.z, pg.w};
-        const uint32_t hw[4] = {ph.x, ph.y, ph.z, ph.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const GatePair gp = gate_pair(unpack_bf16x2(uw[e]), unpack_bf16x2(gw[e]), rsu, cu, rsg, cgs, aff[j].wx[e],
-                                        aff[j].cx[e], aff[j].wg[e], aff[j].cg[e]);
-          const float2 dh = unpack_bf16x2(hw[e]);
-          const float2 dxu = mul2(mul2(dh, gp.q), aff[j].wx[e]);
-          const float2 dxg = mul2(mul2(mul2(dh, gp.a), gp.dsil), aff[j].wg[e]);
-          s1u = add2(s1u, dxu);
-          s2u = fma2(dxu, gp.xu, s2u);
-          s1g = add2(s1g, dxg);
-          s2g = fma2(dxg, gp.xg, s2g);
-        }
-      }
-    }
-    float acc[4] = {s1u.x + s1u.y, s2u.x + s2u.y, s1g.x + s1g.y, s2g.x + s2g.y};
-    block_sum<4>(acc, sm, slot);
-    slot ^= 1;
-    if (threadIdx.x == 0) rowsum[row] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    rowsum[row] = acc;
   }
-  cp_async_wait<0>();
 }
 
 constexpr int kApplyThreads = 128;  // 8 columns per thread
@@ -650,27 +492,14 @@ cudaError_t launch_ln_gate_fwd(const void* Z, const void* stats, const void* nx_
   return run(ln_gate_fwd_kernel<512, 2>);
 }
 
-cudaError_t launch_ln_gate_bwd_rowsum(const void* Z, const void* stats, const void* dHl, const void* nx_w,
-                                      const void* nx_b, const void* ng_w, const void* ng_b, void* rowsum, int T, int M,
-                                      int L, int H, const DeviceInfo& dev, cudaStream_t s) {
-  int nt = 0, vpt = 0;
-  if (!row_shape(H, &nt, &vpt)) return cudaErrorInvalidValue;
-  const int P = T / L;
-  auto run = [&](auto kern) {
-    const size_t smem = static_cast<size_t>(kBwdStages) * vpt * 3 * nt * 16;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
-    const int cpr = ctas_per_rank(dev, reinterpret_cast<const void*>(kern), nt, smem, P, static_cast<int64_t>(L) * M);
-    kern<<<P * cpr, nt, smem, s>>>(static_cast<const __nv_bfloat16*>(Z), static_cast<const float4*>(stats),
-                                   static_cast<const __nv_bfloat16*>(dHl), static_cast<const __nv_bfloat16*>(nx_w),
-                                   static_cast<const __nv_bfloat16*>(nx_b), static_cast<const __nv_bfloat16*>(ng_w),
-                                   static_cast<const __nv_bfloat16*>(ng_b), static_cast<float4*>(rowsum), M, L, H, cpr,
-                                   dev.err);
-    return cudaGetLastError();
-  };
-  if (nt == 256 && vpt == 1) return run(ln_gate_bwd_rowsum_kernel<256, 1>);
-  if (nt == 256) return run(ln_gate_bwd_rowsum_kernel<256, 2>);
-  return run(ln_gate_bwd_rowsum_kernel<512, 2>);
+cudaError_t launch_rowsum_finalize(const float4* part, void* rowsum, int T, int M, int tiles_n, const DeviceInfo& dev,
+                                   cudaStream_t s) {
+  const int64_t rows = static_cast<int64_t>(T) * M;
+  int64_t blocks = (rows + 255) / 256;
+  if (blocks > 16 * dev.num_sms) blocks = 16 * dev.num_sms;
+  rowsum_finalize_kernel<<<static_cast<int>(blocks), 256, 0, s>>>(part, static_cast<float4*>(rowsum), T, M, tiles_n,
+                                                                  dev.err);
+  return cudaGetLastError();
 }
 
 int ffn_bwd_row_splits(int T, int M) {
