@@ -422,6 +422,7 @@ dg_status dg_a2a_ffn_fwd(const dg_ffn_shape* shape, const void* inputs, const vo
   p1.bias_g_stride = static_cast<int64_t>(2 * H);
   p1.ln_part = static_cast<float4*>(part);
   p1.ln_H = static_cast<int32_t>(H);
+  p1.n_fastest = 1;  // Z is written in whole rows
   const double rows = static_cast<double>(T) * M;
   if ((st = run_gemm(GV_BF16_KM_LNSTATS, mx, mw1, mz, mz, p1, dev, s, "ffn_gemm1",
                      2.0 * (rows * D + static_cast<double>(T) * D * 2 * H + rows * 2 * H) +
@@ -458,6 +459,7 @@ dg_status dg_a2a_ffn_fwd(const dg_ffn_shape* shape, const void* inputs, const vo
   p2.d_g = G_MID;
   p2.bias = static_cast<const __nv_bfloat16*>(bout);
   p2.bias_g_stride = static_cast<int64_t>(D);
+  p2.n_fastest = 1;
   return run_gemm(GV_BF16_KM_BIAS, mh, mwo, mo, mo, p2, dev, s, "ffn_gemm2",
                   2.0 * (rows * H + static_cast<double>(T) * H * D + rows * D));
 }
@@ -530,6 +532,7 @@ dg_status dg_a2a_ffn_bwd(const dg_ffn_shape* shape, const void* inputs, const vo
   p.ln_gg = static_cast<const __nv_bfloat16*>(ng_w);
   p.ln_bg = static_cast<const __nv_bfloat16*>(ng_b);
   p.rs_part = reinterpret_cast<float4*>(rspart);
+  p.n_fastest = 1;  // the tiles of a row block run together: Z is read in whole rows
   const double rows = static_cast<double>(T) * M;
   if ((st = run_gemm(GV_BF16_KK_DHL, mdy_k, mwo_k, mdh, mz_chunk, p, dev, s, "ffn_bwd_dhl",
                      2.0 * (rows * D + static_cast<double>(T) * H * D + rows * H) + rows * 2.0 * 2 * H +
@@ -603,6 +606,7 @@ dg_status dg_a2a_ffn_bwd(const dg_ffn_shape* shape, const void* inputs, const vo
   p.a_g = G_OUTER;
   p.b_g = G_OUTER;
   p.d_g = G_MID;
+  p.n_fastest = 1;  // the column tiles of a dZ row block share its reads in L2
   if ((st = run_gemm(GV_BF16_KK_STORE, mdz_k, mw1_k, mdx, mdx, p, dev, s, "ffn_bwd_dx",
                      2.0 * (rows * 2 * H + static_cast<double>(T) * D * 2 * H + rows * D))) != DG_OK)
     return st;

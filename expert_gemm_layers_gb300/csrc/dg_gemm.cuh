@@ -48,6 +48,7 @@ enum WaitSite : uint32_t {
 struct GemmParams {
   int32_t G, M, N, K;        // problems; rows, output columns, contraction of each problem
   int32_t tiles_m, tiles_n;  // tiles per problem
+  int32_t n_fastest;         // tile order within a problem: 0 = row tiles fastest, 1 = column tiles fastest
   int32_t a_g, b_g, d_g;     // GMode of the group coordinate of A, B and D (C follows D)
   const __nv_bfloat16* bias; // EPI_BIAS: bias[g * bias_g_stride + n]
   int64_t bias_g_stride;
@@ -155,6 +156,17 @@ static __device__ __forceinline__ void tma_store_op(const CUtensorMap* map, cons
 
 static __device__ __forceinline__ float silu_f(float x) { return x / (1.0f + __expf(-x)); }
 
+// (row tile, column tile) of the rem-th tile of a problem in the launch's order.
+static __device__ __forceinline__ void tile_coords(const GemmParams& p, int rem, int& mt, int& nt) {
+  if (p.n_fastest) {
+    mt = rem / p.tiles_n;
+    nt = rem - mt * p.tiles_n;
+  } else {
+    nt = rem / p.tiles_m;
+    mt = rem - nt * p.tiles_m;
+  }
+}
+
 template <bool kFp8, bool kAMN, bool kBMN, int kEpi, bool kPair>
 __global__ void __launch_bounds__(GemmCfg<kFp8, kAMN, kBMN, kEpi, kPair>::NUM_THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -250,8 +262,10 @@ __global__ void __launch_bounds__(GemmCfg<kFp8, kAMN, kBMN, kEpi, kPair>::NUM_TH
       for (int tile = unit; tile < total_tiles && ok; tile += num_units) {
         const int g = tile / tiles_per_group;
         const int rem = tile - g * tiles_per_group;
-        const int m0 = (rem % p.tiles_m) * Cfg::UMMA_M + static_cast<int>(rank) * Cfg::BM;
-        const int n0 = (rem / p.tiles_m) * Cfg::BN_OUT;
+        int mt, nt;
+        tile_coords(p, rem, mt, nt);
+        const int m0 = mt * Cfg::UMMA_M + static_cast<int>(rank) * Cfg::BM;
+        const int n0 = nt * Cfg::BN_OUT;
         for (int kb = 0; kb < num_kb; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1u, p.err, SITE_EMPTY)) {
             ok = false;
@@ -404,8 +418,10 @@ __global__ void __launch_bounds__(GemmCfg<kFp8, kAMN, kBMN, kEpi, kPair>::NUM_TH
     for (int tile = unit; tile < total_tiles && ok; tile += num_units, ++local) {
       const int g = tile / tiles_per_group;
       const int rem = tile - g * tiles_per_group;
-      const int m0 = (rem % p.tiles_m) * Cfg::UMMA_M + static_cast<int>(rank) * Cfg::BM;
-      const int n0 = (rem / p.tiles_m) * Cfg::BN_OUT;
+      int mt, nt;
+      tile_coords(p, rem, mt, nt);
+      const int m0 = mt * Cfg::UMMA_M + static_cast<int>(rank) * Cfg::BM;
+      const int n0 = nt * Cfg::BN_OUT;
       const int acc = local & (Cfg::NACC - 1);
       const int row0 = m0 + 32 * lg;
       int nchunks = (p.N - n0 + 63) / 64;
@@ -611,11 +627,11 @@ __global__ void __launch_bounds__(GemmCfg<kFp8, kAMN, kBMN, kEpi, kPair>::NUM_TH
       }
       if (!ok) break;
       if (kEpi == EPI_BIAS_LNSTATS && nchunks > 0 && row0 + lane < p.M) {
-        p.ln_part[(static_cast<int64_t>(g) * p.tiles_n + rem / p.tiles_m) * p.M + row0 + lane] =
+        p.ln_part[(static_cast<int64_t>(g) * p.tiles_n + nt) * p.M + row0 + lane] =
             make_float4(st_u.mean, st_u.m2, st_g.mean, st_g.m2);
       }
       if (kZ && nchunks > 0 && row0 + lane < p.M) {
-        p.rs_part[(static_cast<int64_t>(g) * p.tiles_n + rem / p.tiles_m) * p.M + row0 + lane] =
+        p.rs_part[(static_cast<int64_t>(g) * p.tiles_n + nt) * p.M + row0 + lane] =
             make_float4(s1u.x + s1u.y, s2u.x + s2u.y, s1g.x + s1g.y, s2g.x + s2g.y);
       }
       chunk_ctr += static_cast<uint32_t>(nchunks);
