@@ -188,7 +188,6 @@ dg_status run_gemm(GemmVariant v, const CUtensorMap& a, const CUtensorMap& b, co
     case GV_BF16_MM_STORE: e = launch_gemm_bf16_mm_store(a, b, d, c, p, grid, s); break;
     case GV_BF16_KK_SWIGLU: e = launch_gemm_bf16_kk_swiglu(a, b, d, c, p, grid, s); break;
     case GV_BF16_KM_LNSTATS: e = launch_gemm_bf16_km_lnstats(a, b, d, c, p, grid, s); break;
-    case GV_BF16_KK_DHL: e = launch_gemm_bf16_kk_dhl(a, b, d, c, p, grid, s); break;
     default: return fail(DG_ERR_UNSUPPORTED, "unknown GEMM variant");
   }
   if (e != cudaSuccess) return cuda_fail(e, "GEMM launch");
@@ -241,11 +240,10 @@ SavedLayout saved_layout(const FfnDims& f) {
 }
 
 // Carving of the backward's workspace: dHl [T,M,H] bf16, dZ [T,M,2H] bf16,
-// rowsum [T,M] float4, column partials [T,nsplit,6,H] fp32, and the dHl
-// GEMM's per-tile row-term partials [T,tiles_n,M] float4.
+// rowsum [T,M] float4, column partials [T,nsplit,6,H] fp32.
 struct BwdLayout {
-  size_t dhl, dz, rowsum, part, rspart, total;
-  int nsplit, tiles_n;
+  size_t dhl, dz, rowsum, part, total;
+  int nsplit;
 };
 BwdLayout bwd_layout(const FfnDims& f) {
   BwdLayout l;
@@ -255,9 +253,7 @@ BwdLayout bwd_layout(const FfnDims& f) {
   l.dz = round_up(rows * f.H * 2, 256);
   l.rowsum = round_up(l.dz + rows * 2 * f.H * 2, 256);
   l.part = round_up(l.rowsum + rows * 16, 256);
-  l.tiles_n = static_cast<int>((f.H + gemm_tile_n(GV_BF16_KK_DHL) - 1) / gemm_tile_n(GV_BF16_KK_DHL));
-  l.rspart = round_up(l.part + static_cast<size_t>(f.T) * l.nsplit * 6 * f.H * 4, 256);
-  l.total = round_up(l.rspart + rows * l.tiles_n * 16, 256);
+  l.total = round_up(l.part + static_cast<size_t>(f.T) * l.nsplit * 6 * f.H * 4, 256);
   return l;
 }
 
@@ -422,7 +418,6 @@ dg_status dg_a2a_ffn_fwd(const dg_ffn_shape* shape, const void* inputs, const vo
   p1.bias_g_stride = static_cast<int64_t>(2 * H);
   p1.ln_part = static_cast<float4*>(part);
   p1.ln_H = static_cast<int32_t>(H);
-  p1.n_fastest = 1;  // Z is written in whole rows
   const double rows = static_cast<double>(T) * M;
   if ((st = run_gemm(GV_BF16_KM_LNSTATS, mx, mw1, mz, mz, p1, dev, s, "ffn_gemm1",
                      2.0 * (rows * D + static_cast<double>(T) * D * 2 * H + rows * 2 * H) +
@@ -459,7 +454,6 @@ dg_status dg_a2a_ffn_fwd(const dg_ffn_shape* shape, const void* inputs, const vo
   p2.d_g = G_MID;
   p2.bias = static_cast<const __nv_bfloat16*>(bout);
   p2.bias_g_stride = static_cast<int64_t>(D);
-  p2.n_fastest = 1;
   return run_gemm(GV_BF16_KM_BIAS, mh, mwo, mo, mo, p2, dev, s, "ffn_gemm2",
                   2.0 * (rows * H + static_cast<double>(T) * H * D + rows * D));
 }
@@ -504,18 +498,13 @@ dg_status dg_a2a_ffn_bwd(const dg_ffn_shape* shape, const void* inputs, const vo
   void* dZ = w + bl.dz;
   void* rowsum = w + bl.rowsum;
   float* part = reinterpret_cast<float*>(w + bl.part);
-  void* rspart = w + bl.rspart;
   const uint64_t T = f.T, M = f.M, D = f.D, H = f.H;
 
-  // (1) dHl_t = dY_t @ wout_t^T (dY_t: the dispatched rows of dY).  The epilogue
-  //     also forms, per 256-column tile, each row's sums of the LayerNorm
-  //     backward's terms, reading the matching columns of Z.
-  CUtensorMap mdy_k, mwo_k, mdh, mz_chunk;
+  // (1) dHl_t = dY_t @ wout_t^T      (dY_t: the dispatched rows of dY)
+  CUtensorMap mdy_k, mwo_k, mdh;
   if ((st = make_map_3d(&mdy_k, true, dY, D, T, M, D * 2, T * D * 2, 64, 1, 128, "dY")) != DG_OK) return st;
   if ((st = make_map_3d(&mwo_k, true, wout, D, H, T, D * 2, H * D * 2, 64, kKMajorBRows, 1, "wout")) != DG_OK) return st;
   if ((st = make_map_3d(&mdh, true, dHl, H, M, T, H * 2, M * H * 2, 64, 32, 1, "dHl")) != DG_OK) return st;
-  if ((st = make_map_3d(&mz_chunk, true, Z, 2 * H, M, T, 2 * H * 2, M * 2 * H * 2, 64, 32, 1, "Z (chunks)")) != DG_OK)
-    return st;
   GemmParams p{};
   p.G = static_cast<int32_t>(T);
   p.M = static_cast<int32_t>(M);
@@ -524,19 +513,9 @@ dg_status dg_a2a_ffn_bwd(const dg_ffn_shape* shape, const void* inputs, const vo
   p.a_g = G_MID;
   p.b_g = G_OUTER;
   p.d_g = G_OUTER;
-  p.ln_H = static_cast<int32_t>(H);
-  p.ln_L = static_cast<int32_t>(f.L);
-  p.ln_stats = static_cast<const float4*>(stats);
-  p.ln_gx = static_cast<const __nv_bfloat16*>(nx_w);
-  p.ln_bx = static_cast<const __nv_bfloat16*>(nx_b);
-  p.ln_gg = static_cast<const __nv_bfloat16*>(ng_w);
-  p.ln_bg = static_cast<const __nv_bfloat16*>(ng_b);
-  p.rs_part = reinterpret_cast<float4*>(rspart);
-  p.n_fastest = 1;  // the tiles of a row block run together: Z is read in whole rows
   const double rows = static_cast<double>(T) * M;
-  if ((st = run_gemm(GV_BF16_KK_DHL, mdy_k, mwo_k, mdh, mz_chunk, p, dev, s, "ffn_bwd_dhl",
-                     2.0 * (rows * D + static_cast<double>(T) * H * D + rows * H) + rows * 2.0 * 2 * H +
-                         rows * bl.tiles_n * 16.0)) != DG_OK)
+  if ((st = run_gemm(GV_BF16_KK_STORE, mdy_k, mwo_k, mdh, mdh, p, dev, s, "ffn_bwd_dhl",
+                     2.0 * (rows * D + static_cast<double>(T) * H * D + rows * H))) != DG_OK)
     return st;
 
   // (2) dwout_t = Hl_t^T @ dY_t     [H, D], contraction over the M rows
@@ -565,14 +544,13 @@ dg_status dg_a2a_ffn_bwd(const dg_ffn_shape* shape, const void* inputs, const vo
   }
   if (e != cudaSuccess) return cuda_fail(e, "column-sum launch");
 
-  // (4) gate + LayerNorm backward: the row sums (from the dHl GEMM's partials),
-  //     then dZ with db1 and the norm column sums
+  // (4) gate + LayerNorm backward: per-row sums, then dZ with db1 and the norm column sums
   {
-    TraceScope trace("ffn_bwd_rowsum_finalize", s, 0.0, rows * bl.tiles_n * 16.0 + rows * 16.0);
-    e = launch_rowsum_finalize(reinterpret_cast<const float4*>(rspart), rowsum, static_cast<int>(T),
-                               static_cast<int>(M), bl.tiles_n, dev, s);
+    TraceScope trace("ffn_bwd_ln_rowsum", s, 0.0, rows * (2.0 * 2 * H + 2.0 * H + 32.0));
+    e = launch_ln_gate_bwd_rowsum(Z, stats, dHl, nx_w, nx_b, ng_w, ng_b, rowsum, static_cast<int>(T),
+                                  static_cast<int>(M), static_cast<int>(f.L), static_cast<int>(H), dev, s);
   }
-  if (e != cudaSuccess) return cuda_fail(e, "row-sum finalize launch");
+  if (e != cudaSuccess) return cuda_fail(e, "LayerNorm-gate backward (row sums) launch");
   {
     TraceScope trace("ffn_bwd_ln_apply", s, 0.0,
                      rows * (2.0 * 2 * H + 2.0 * H + 32.0 + 2.0 * 2 * H) +
@@ -606,7 +584,6 @@ dg_status dg_a2a_ffn_bwd(const dg_ffn_shape* shape, const void* inputs, const vo
   p.a_g = G_OUTER;
   p.b_g = G_OUTER;
   p.d_g = G_MID;
-  p.n_fastest = 1;  // the column tiles of a dZ row block share its reads in L2
   if ((st = run_gemm(GV_BF16_KK_STORE, mdz_k, mw1_k, mdx, mdx, p, dev, s, "ffn_bwd_dx",
                      2.0 * (rows * 2 * H + static_cast<double>(T) * D * 2 * H + rows * D))) != DG_OK)
     return st;

@@ -36,8 +36,7 @@ enum Epi : int32_t {
   EPI_BIAS = 1,          // D = acc + bias
   EPI_FP8 = 2,           // D = alpha*acc + beta*C
   EPI_SWIGLU = 3,        // D = silu(acc[:, :BN/2]) * acc[:, BN/2:]
-  EPI_BIAS_LNSTATS = 4,  // D = acc + bias, and per-tile (mean, M2) of each row's U and G columns
-  EPI_DHL_ROWSUM = 5     // D = acc (= dHl), and per-tile sums of the LayerNorm backward's row terms
+  EPI_BIAS_LNSTATS = 4   // D = acc + bias, and per-tile (mean, M2) of each row's U and G columns
 };
 
 // Wait-site codes recorded with a timeout.
@@ -55,14 +54,7 @@ struct GemmParams {
   float alpha, beta;         // EPI_FP8
   int32_t has_c;             // EPI_FP8: read C
   float4* ln_part;           // EPI_BIAS_LNSTATS: [G][tiles_n][M] (mean_u, M2_u, mean_g, M2_g) per tile
-  int32_t ln_H;              // EPI_BIAS_LNSTATS: columns [0, ln_H) are U, [ln_H, N) are G; EPI_DHL_ROWSUM: H
-  const float4* ln_stats;    // EPI_DHL_ROWSUM: per row (mean_u, rstd_u, mean_g, rstd_g), [G*M]
-  const __nv_bfloat16* ln_gx;  // EPI_DHL_ROWSUM: LayerNorm affines [P, H]
-  const __nv_bfloat16* ln_bx;
-  const __nv_bfloat16* ln_gg;
-  const __nv_bfloat16* ln_bg;
-  int32_t ln_L;              // EPI_DHL_ROWSUM: problems per rank (the rank of problem g is g / ln_L)
-  float4* rs_part;           // EPI_DHL_ROWSUM: [G][tiles_n][M] sums of (dx_u, dx_u*x_u, dx_g, dx_g*x_g)
+  int32_t ln_H;              // EPI_BIAS_LNSTATS: columns [0, ln_H) are U, [ln_H, N) are G
   uint32_t* err;             // device error word
 };
 
@@ -110,7 +102,7 @@ struct GemmCfg {
   static constexpr int ROW_BYTES = 128;               // K-block = one 128-byte swizzle row
   static constexpr int BK = kFp8 ? 128 : 64;          // K elements per stage
   static constexpr int K_STEPS = 4;                   // UMMA K = 32 bytes: 16 bf16 / 32 e4m3
-  static constexpr int STAGES = (kEpi == EPI_DHL_ROWSUM || !kPair) ? 4 : 6;
+  static constexpr int STAGES = kPair ? 6 : 4;
   static constexpr int A_BYTES = BM * ROW_BYTES;      // 16 KB
   static constexpr int B_BYTES = B_ROWS * ROW_BYTES;  // 16 KB (pair) or 32 KB
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
@@ -118,14 +110,12 @@ struct GemmCfg {
   static constexpr int EPI_WARPS = 4;
   static constexpr int EPI_BUF_BYTES = 32 * 128;      // 32 rows x 64 bf16
   static constexpr int EPI_BYTES = EPI_WARPS * 2 * EPI_BUF_BYTES;
-  static constexpr int ZBUF_BYTES = 2 * EPI_BUF_BYTES;  // EPI_DHL_ROWSUM: a 32x64 chunk of U and of G
-  static constexpr int ZBYTES = (kEpi == EPI_DHL_ROWSUM) ? EPI_WARPS * 2 * ZBUF_BYTES : 0;
   static constexpr int NUM_THREADS = 64 + EPI_WARPS * 32;
   static constexpr int NACC = 2;                      // TMEM accumulators (double buffered)
   static constexpr uint32_t TMEM_COLS = NACC * BN;
   static constexpr int NUM_BARS = 2 * STAGES + 4 + 2 * EPI_WARPS + 1;
   static constexpr int BAR_BYTES = 256;
-  static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + EPI_BYTES + ZBYTES + BAR_BYTES;
+  static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + EPI_BYTES + BAR_BYTES;
   static constexpr uint32_t IDESC = umma_idesc(kFp8 ? 0u : 1u, kAMN, kBMN, BN, UMMA_M);
   static_assert(NUM_BARS * 8 + 4 <= BAR_BYTES, "barrier area");
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
@@ -180,8 +170,7 @@ __global__ void __launch_bounds__(GemmCfg<kFp8, kAMN, kBMN, kEpi, kPair>::NUM_TH
   uint8_t* smem = smem_raw + pad;
   uint8_t* stage_base = smem;
   uint8_t* epi_base = smem + Cfg::STAGES * Cfg::STAGE_BYTES;
-  uint8_t* zbuf_base = epi_base + Cfg::EPI_BYTES;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(zbuf_base + Cfg::ZBYTES);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(epi_base + Cfg::EPI_BYTES);
   uint64_t* full = bars;
   uint64_t* empty = bars + Cfg::STAGES;
   uint64_t* tfull = bars + 2 * Cfg::STAGES;
@@ -406,10 +395,8 @@ __global__ void __launch_bounds__(GemmCfg<kFp8, kAMN, kBMN, kEpi, kPair>::NUM_TH
     const int ew = warp - 2;  // staging-buffer owner index
     const int lg = warp & 3;  // TMEM lane quarter this warp may access
     uint8_t* stg = epi_base + ew * 2 * Cfg::EPI_BUF_BYTES;
-    uint8_t* zst = zbuf_base + ew * 2 * Cfg::ZBUF_BYTES;
     uint64_t* my_cbar = cbar + 2 * ew;
     const bool use_c = (kEpi == EPI_FP8) && (p.has_c != 0);
-    constexpr bool kZ = kEpi == EPI_DHL_ROWSUM;  // loads U/G chunks of Z next to each chunk
     uint32_t tphase = 0, cphase = 0, chunk_ctr = 0;
     uint32_t pending = 0, pending_parity = 0;  // async loads in flight, per staging buffer
     bool ok = true;
@@ -428,31 +415,18 @@ __global__ void __launch_bounds__(GemmCfg<kFp8, kAMN, kBMN, kEpi, kPair>::NUM_TH
       if (nchunks > Cfg::BN_OUT / 64) nchunks = Cfg::BN_OUT / 64;
       if (row0 >= p.M) nchunks = 0;
 
-      // C (FP8) or the U/G chunks of Z (DHL_ROWSUM) for chunk j into staging buffer buf
+      // C (FP8 epilogue) of chunk j into staging buffer buf
       auto issue_load = [&](int j, int buf) {
         if (lane == 0) {
-          if (kZ) {
-            mbar_arrive_expect_tx(&my_cbar[buf], Cfg::ZBUF_BYTES);
-            uint8_t* zb = zst + buf * Cfg::ZBUF_BYTES;
-            tma_load_op(zb, &tmC, &my_cbar[buf], n0 + 64 * j, row0, g, G_OUTER);
-            tma_load_op(zb + Cfg::EPI_BUF_BYTES, &tmC, &my_cbar[buf], p.ln_H + n0 + 64 * j, row0, g, G_OUTER);
-          } else {
-            bulk_wait_group_read<0>();
-            mbar_arrive_expect_tx(&my_cbar[buf], Cfg::EPI_BUF_BYTES);
-            tma_load_op(stg + buf * Cfg::EPI_BUF_BYTES, &tmC, &my_cbar[buf], n0 + 64 * j, row0, g, p.d_g);
-          }
+          bulk_wait_group_read<0>();
+          mbar_arrive_expect_tx(&my_cbar[buf], Cfg::EPI_BUF_BYTES);
+          tma_load_op(stg + buf * Cfg::EPI_BUF_BYTES, &tmC, &my_cbar[buf], n0 + 64 * j, row0, g, p.d_g);
         }
         pending |= 1u << buf;
         pending_parity = (pending_parity & ~(1u << buf)) | (((cphase >> buf) & 1u) << buf);
         __syncwarp();
       };
-      const bool use_load = use_c || kZ;
-      if (use_load && nchunks > 0) issue_load(0, static_cast<int>(chunk_ctr & 1u));
-
-      // DHL_ROWSUM: this thread's row statistics and running row sums
-      float4 rstat = make_float4(0.f, 0.f, 0.f, 0.f);
-      float2 s1u = splat2(0.f), s2u = splat2(0.f), s1g = splat2(0.f), s2g = splat2(0.f);
-      if (kZ && row0 + lane < p.M) rstat = p.ln_stats[static_cast<int64_t>(g) * p.M + row0 + lane];
+      if (use_c && nchunks > 0) issue_load(0, static_cast<int>(chunk_ctr & 1u));
 
       if (!mbar_wait(&tfull[acc], (tphase >> acc) & 1u, p.err, SITE_TFULL)) {
         ok = false;
@@ -464,7 +438,7 @@ __global__ void __launch_bounds__(GemmCfg<kFp8, kAMN, kBMN, kEpi, kPair>::NUM_TH
       MeanM2 st_u{0.0f, 0.0f, 0.0f}, st_g{0.0f, 0.0f, 0.0f};
       for (int j = 0; j < nchunks; ++j) {
         const int buf = static_cast<int>((chunk_ctr + j) & 1u);
-        if (use_load && j + 1 < nchunks) issue_load(j + 1, buf ^ 1);
+        if (use_c && j + 1 < nchunks) issue_load(j + 1, buf ^ 1);
 
         float v[64];
         if (kEpi == EPI_SWIGLU) {
@@ -584,55 +558,11 @@ __global__ void __launch_bounds__(GemmCfg<kFp8, kAMN, kBMN, kEpi, kPair>::NUM_TH
           tma_store_op(&tmD, sbuf, n0 + 64 * j, row0, g, p.d_g);
           bulk_commit_group();
         }
-        if (kZ) {
-          // Row terms of the LayerNorm backward over this chunk's columns, from the
-          // stored (bf16) dHl, the U/G chunk of Z and the row statistics:
-          // dx_u = dHl*q*gx, dx_g = dHl*a*silu'(s)*gg (see the backward row kernels).
-          if (!mbar_wait(&my_cbar[buf], (cphase >> buf) & 1u, p.err, SITE_CLOAD)) {
-            ok = false;
-            break;
-          }
-          cphase ^= 1u << buf;
-          pending &= ~(1u << buf);
-          const uint8_t* zb = zst + buf * Cfg::ZBUF_BYTES;
-          const int r = g / p.ln_L;
-          const float2 rsu = splat2(rstat.y), cu = splat2(-rstat.x * rstat.y);
-          const float2 rsg = splat2(rstat.w), cgs = splat2(-rstat.z * rstat.w);
-#pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            const int col = n0 + 64 * j + 8 * q;
-            if (col < p.ln_H) {
-              const AffineF af =
-                  load_affine_f(p.ln_gx, p.ln_bx, p.ln_gg, p.ln_bg, static_cast<int64_t>(r) * p.ln_H + col);
-              const uint4 uu = *reinterpret_cast<const uint4*>(zb + lane * 128 + ((q ^ (lane & 7)) << 4));
-              const uint4 gg = *reinterpret_cast<const uint4*>(zb + Cfg::EPI_BUF_BYTES + lane * 128 +
-                                                               ((q ^ (lane & 7)) << 4));
-              const uint32_t uw[4] = {uu.x, uu.y, uu.z, uu.w}, gw[4] = {gg.x, gg.y, gg.z, gg.w};
-#pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const GatePair gp = gate_pair(unpack_bf16x2(uw[e]), unpack_bf16x2(gw[e]), rsu, cu, rsg, cgs,
-                                              af.wx[e], af.cx[e], af.wg[e], af.cg[e]);
-                const float2 dh = unpack_bf16x2(packed[4 * q + e]);
-                const float2 dxu = mul2(mul2(dh, gp.q), af.wx[e]);
-                const float2 dxg = mul2(mul2(mul2(dh, gp.a), gp.dsil), af.wg[e]);
-                s1u = add2(s1u, dxu);
-                s2u = fma2(dxu, gp.xu, s2u);
-                s1g = add2(s1g, dxg);
-                s2g = fma2(dxg, gp.xg, s2g);
-              }
-            }
-          }
-          __syncwarp();  // every lane has read this Z buffer before it is refilled
-        }
       }
       if (!ok) break;
       if (kEpi == EPI_BIAS_LNSTATS && nchunks > 0 && row0 + lane < p.M) {
         p.ln_part[(static_cast<int64_t>(g) * p.tiles_n + nt) * p.M + row0 + lane] =
             make_float4(st_u.mean, st_u.m2, st_g.mean, st_g.m2);
-      }
-      if (kZ && nchunks > 0 && row0 + lane < p.M) {
-        p.rs_part[(static_cast<int64_t>(g) * p.tiles_n + nt) * p.M + row0 + lane] =
-            make_float4(s1u.x + s1u.y, s2u.x + s2u.y, s1g.x + s1g.y, s2g.x + s2g.y);
       }
       chunk_ctr += static_cast<uint32_t>(nchunks);
       tc_fence_before_sync();

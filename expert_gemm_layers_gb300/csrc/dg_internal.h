@@ -34,8 +34,7 @@ enum GemmVariant : int {
   GV_BF16_KM_BIAS = 2,  // bf16, A K-major, B MN-major, bias epilogue
   GV_BF16_MM_STORE = 3, // bf16, A and B MN-major, plain store
   GV_BF16_KK_SWIGLU = 4, // bf16, A and B K-major, paired silu(a)*b epilogue
-  GV_BF16_KM_LNSTATS = 5, // bf16, A K-major, B MN-major, bias + per-tile LayerNorm statistics
-  GV_BF16_KK_DHL = 6      // bf16, A and B K-major, dHl store + per-tile LayerNorm-backward row terms
+  GV_BF16_KM_LNSTATS = 5 // bf16, A K-major, B MN-major, bias + per-tile LayerNorm statistics
 };
 
 // Tiles along N of one problem for this variant (output columns per tile).
@@ -77,8 +76,6 @@ cudaError_t launch_gemm_bf16_kk_swiglu(const CUtensorMap&, const CUtensorMap&, c
                                        const CUtensorMap&, const GemmParams&, int num_sms, cudaStream_t);
 cudaError_t launch_gemm_bf16_km_lnstats(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
                                         const CUtensorMap&, const GemmParams&, int num_sms, cudaStream_t);
-cudaError_t launch_gemm_bf16_kk_dhl(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
-                                    const CUtensorMap&, const GemmParams&, int num_sms, cudaStream_t);
 
 // The GEMMs run as CTA pairs (cta_group::2, 256-row tiles, clusters of 2).
 constexpr bool kUsePairs = true;
@@ -132,10 +129,11 @@ cudaError_t launch_ln_gate_fwd(const void* Z, const void* stats, const void* nx_
                                const void* ng_b, void* Hl, int P, int M, int L, int H, const DeviceInfo& dev,
                                cudaStream_t s);
 
-// Row sums from the per-tile partials part [T][tiles_n][M] that the dHl
-// GEMM's epilogue wrote: rowsum[t*M + n] = sum over tiles, in tile order.
-cudaError_t launch_rowsum_finalize(const float4* part, void* rowsum, int T, int M, int tiles_n, const DeviceInfo& dev,
-                                   cudaStream_t s);
+// Backward of the gate and both LayerNorms, pass 1: per-row sums
+// rowsum[row] = (sum dx_u, sum dx_u*x_u, sum dx_g, sum dx_g*x_g), one warp per row.
+cudaError_t launch_ln_gate_bwd_rowsum(const void* Z, const void* stats, const void* dHl, const void* nx_w,
+                                      const void* nx_b, const void* ng_w, const void* ng_b, void* rowsum, int T, int M,
+                                      int L, int H, const DeviceInfo& dev, cudaStream_t s);
 
 // Pass 2: dZ [rows, 2H] and per-(t, row range) column partial sums
 // part [T, nsplit, 6, H] fp32 (dU, dG, da*x_u, da, ds*x_g, ds).

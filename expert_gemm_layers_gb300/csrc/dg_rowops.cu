@@ -211,30 +211,64 @@ __global__ void __launch_bounds__(NT, 512 / NT) ln_gate_fwd_kernel(
 // silu'(s) = sig(s) + s*sig(s)*(1 - sig(s)), dx_u = da*gx,
 // dU = rstd_u * (dx_u - mean(dx_u) - x_u*mean(dx_u*x_u)), and the same for G.
 //
-// Pass 1 (row sums) runs in the epilogue of the GEMM that produces dHl: per
-// 256-column tile it sums dx_u, dx_u*x_u, dx_g, dx_g*x_g of each row;
-// rowsum_finalize adds the tiles in order.
+// Pass 1 (row sums): one warp per row sums dx_u, dx_u*x_u, dx_g, dx_g*x_g.
 // Pass 2 (apply): a CTA owns a column block of one token position t and a
 // range of its rows: it writes dZ and sums, per column, dU, dG (db1),
 // da*x_u, da (norm_x grads), ds*x_g, ds (norm_gate grads) in registers; the
 // per-(t, row range) partial sums are added in a fixed order afterwards.
 
-__global__ void rowsum_finalize_kernel(const float4* __restrict__ part, float4* __restrict__ rowsum, int T, int M,
-                                       int tiles_n, const uint32_t* err) {
+// Pass 1: one warp per row, no block barrier.  The warp walks the row in
+// 256-column steps (8 columns per lane), two steps in flight, and reduces
+// the four sums with shuffles.  The affines come through L1 (a CTA's warps
+// work on consecutive rows, hence mostly on one rank).
+constexpr int kRowsumThreads = 256;
+
+__global__ void __launch_bounds__(kRowsumThreads, 2) ln_gate_bwd_rowsum_kernel(
+    const __nv_bfloat16* __restrict__ Z, const float4* __restrict__ stats, const __nv_bfloat16* __restrict__ dHl,
+    const __nv_bfloat16* __restrict__ gx, const __nv_bfloat16* __restrict__ bx, const __nv_bfloat16* __restrict__ gg,
+    const __nv_bfloat16* __restrict__ bg, float4* __restrict__ rowsum, int64_t rows, int M, int L, int H,
+    const uint32_t* err) {
   if (ld_volatile_u32(err) != 0u) return;
-  const int64_t rows = static_cast<int64_t>(T) * M;
-  for (int64_t row = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; row < rows;
-       row += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const int t = static_cast<int>(row / M), n = static_cast<int>(row - static_cast<int64_t>(t) * M);
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int nt = 0; nt < tiles_n; ++nt) {
-      const float4 q = part[(static_cast<int64_t>(t) * tiles_n + nt) * M + n];
-      acc.x += q.x;
-      acc.y += q.y;
-      acc.z += q.z;
-      acc.w += q.w;
+  const int lane = threadIdx.x & 31;
+  const int64_t warps = static_cast<int64_t>(gridDim.x) * (kRowsumThreads / 32);
+  const int64_t zstride = 2 * static_cast<int64_t>(H);
+  for (int64_t row = static_cast<int64_t>(blockIdx.x) * (kRowsumThreads / 32) + (threadIdx.x >> 5); row < rows;
+       row += warps) {
+    const int r = static_cast<int>(row / M) / L;
+    const float4 sr = stats[row];
+    const float2 rsu = splat2(sr.y), cu = splat2(-sr.x * sr.y), rsg = splat2(sr.w), cgs = splat2(-sr.z * sr.w);
+    const __nv_bfloat16* zu = Z + row * zstride;
+    const __nv_bfloat16* dh = dHl + row * static_cast<int64_t>(H);
+    const int64_t pr = static_cast<int64_t>(r) * H;
+    float2 s1u = splat2(0.f), s2u = splat2(0.f), s1g = splat2(0.f), s2g = splat2(0.f);
+#pragma unroll 2
+    for (int c = 8 * lane; c < H; c += 256) {
+      const uint4 pu = __ldcs(reinterpret_cast<const uint4*>(zu + c));
+      const uint4 pg = __ldcs(reinterpret_cast<const uint4*>(zu + H + c));
+      const uint4 ph = __ldcs(reinterpret_cast<const uint4*>(dh + c));
+      const AffineF af = load_affine_f(gx, bx, gg, bg, pr + c);
+      const uint32_t uw[4] = {pu.x, pu.y, pu.z, pu.w}, gw[4] = {pg.x, pg.y, pg.z, pg.w};
+      const uint32_t hw[4] = {ph.x, ph.y, ph.z, ph.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const GatePair gp = gate_pair(unpack_bf16x2(uw[e]), unpack_bf16x2(gw[e]), rsu, cu, rsg, cgs, af.wx[e],
+                                      af.cx[e], af.wg[e], af.cg[e]);
+        const float2 d = unpack_bf16x2(hw[e]);
+        const float2 dxu = mul2(mul2(d, gp.q), af.wx[e]);
+        const float2 dxg = mul2(mul2(mul2(d, gp.a), gp.dsil), af.wg[e]);
+        s1u = add2(s1u, dxu);
+        s2u = fma2(dxu, gp.xu, s2u);
+        s1g = add2(s1g, dxg);
+        s2g = fma2(dxg, gp.xg, s2g);
+      }
     }
-    rowsum[row] = acc;
+    float acc[4] = {s1u.x + s1u.y, s2u.x + s2u.y, s1g.x + s1g.y, s2g.x + s2g.y};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) acc[i] += __shfl_xor_sync(0xffffffffu, acc[i], o);
+    }
+    if (lane == 0) rowsum[row] = make_float4(acc[0], acc[1], acc[2], acc[3]);
   }
 }
 
@@ -492,13 +526,23 @@ cudaError_t launch_ln_gate_fwd(const void* Z, const void* stats, const void* nx_
   return run(ln_gate_fwd_kernel<512, 2>);
 }
 
-cudaError_t launch_rowsum_finalize(const float4* part, void* rowsum, int T, int M, int tiles_n, const DeviceInfo& dev,
-                                   cudaStream_t s) {
+cudaError_t launch_ln_gate_bwd_rowsum(const void* Z, const void* stats, const void* dHl, const void* nx_w,
+                                      const void* nx_b, const void* ng_w, const void* ng_b, void* rowsum, int T, int M,
+                                      int L, int H, const DeviceInfo& dev, cudaStream_t s) {
   const int64_t rows = static_cast<int64_t>(T) * M;
-  int64_t blocks = (rows + 255) / 256;
-  if (blocks > 16 * dev.num_sms) blocks = 16 * dev.num_sms;
-  rowsum_finalize_kernel<<<static_cast<int>(blocks), 256, 0, s>>>(part, static_cast<float4*>(rowsum), T, M, tiles_n,
-                                                                  dev.err);
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, ln_gate_bwd_rowsum_kernel, kRowsumThreads, 0) !=
+          cudaSuccess ||
+      per_sm < 1)
+    per_sm = 1;
+  int64_t blocks = static_cast<int64_t>(per_sm) * dev.num_sms;
+  const int64_t need = (rows + kRowsumThreads / 32 - 1) / (kRowsumThreads / 32);
+  if (blocks > need) blocks = need;
+  ln_gate_bwd_rowsum_kernel<<<static_cast<int>(blocks), kRowsumThreads, 0, s>>>(
+      static_cast<const __nv_bfloat16*>(Z), static_cast<const float4*>(stats), static_cast<const __nv_bfloat16*>(dHl),
+      static_cast<const __nv_bfloat16*>(nx_w), static_cast<const __nv_bfloat16*>(nx_b),
+      static_cast<const __nv_bfloat16*>(ng_w), static_cast<const __nv_bfloat16*>(ng_b), static_cast<float4*>(rowsum),
+      rows, M, L, H, dev.err);
   return cudaGetLastError();
 }
 
