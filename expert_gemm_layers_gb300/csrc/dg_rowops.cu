@@ -38,6 +38,12 @@ __device__ __forceinline__ void store8_stream(__nv_bfloat16* p, const float (&f)
   __stcs(reinterpret_cast<uint4*>(p), v);
 }
 
+// Warp-uniform read of the error word (these kernels use full-warp barriers
+// and shuffles, so a warp must not split on it).
+__device__ __forceinline__ bool warp_aborted(const uint32_t* err) {
+  return __shfl_sync(0xffffffffu, ld_volatile_u32(err), 0) != 0u;
+}
+
 // Block-uniform read of the error word (a divergent early return ahead of a
 // barrier would be undefined).
 __device__ __forceinline__ bool block_aborted(const uint32_t* err) {
@@ -217,35 +223,73 @@ __global__ void __launch_bounds__(NT, 512 / NT) ln_gate_fwd_kernel(
 // da*x_u, da (norm_x grads), ds*x_g, ds (norm_gate grads) in registers; the
 // per-(t, row range) partial sums are added in a fixed order afterwards.
 
-// Pass 1: one warp per row, no block barrier.  The warp walks the row in
-// 256-column steps (8 columns per lane), two steps in flight, and reduces
-// the four sums with shuffles.  The affines come through L1 (a CTA's warps
-// work on consecutive rows, hence mostly on one rank).
+// Pass 1: one warp per row, no block barrier.  A warp's rows are cut into
+// 256-column chunks (8 columns per lane) that stream through a per-warp
+// shared-memory ring filled by per-lane cp.async; the ring runs on across
+// row boundaries, so several KB per warp stay in flight.  The four sums are
+// reduced with shuffles at the end of each row.  The affines come through L1
+// (a CTA's warps work on consecutive rows, hence mostly on one rank).
 constexpr int kRowsumThreads = 256;
+constexpr int kRowsumWarps = kRowsumThreads / 32;
+constexpr int kRowsumStages = 6;
 
-__global__ void __launch_bounds__(kRowsumThreads, 2) ln_gate_bwd_rowsum_kernel(
+__global__ void __launch_bounds__(kRowsumThreads, 3) ln_gate_bwd_rowsum_kernel(
     const __nv_bfloat16* __restrict__ Z, const float4* __restrict__ stats, const __nv_bfloat16* __restrict__ dHl,
     const __nv_bfloat16* __restrict__ gx, const __nv_bfloat16* __restrict__ bx, const __nv_bfloat16* __restrict__ gg,
     const __nv_bfloat16* __restrict__ bg, float4* __restrict__ rowsum, int64_t rows, int M, int L, int H,
     const uint32_t* err) {
-  if (ld_volatile_u32(err) != 0u) return;
-  const int lane = threadIdx.x & 31;
-  const int64_t warps = static_cast<int64_t>(gridDim.x) * (kRowsumThreads / 32);
+  extern __shared__ uint4 rs_ring[];  // [kRowsumWarps][kRowsumStages][3][32]
+  if (warp_aborted(err)) return;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint4* ring = rs_ring + warp * (kRowsumStages * 3 * 32);
+  const int64_t warps = static_cast<int64_t>(gridDim.x) * kRowsumWarps;
+  const int64_t first = static_cast<int64_t>(blockIdx.x) * kRowsumWarps + warp;
   const int64_t zstride = 2 * static_cast<int64_t>(H);
-  for (int64_t row = static_cast<int64_t>(blockIdx.x) * (kRowsumThreads / 32) + (threadIdx.x >> 5); row < rows;
-       row += warps) {
-    const int r = static_cast<int>(row / M) / L;
-    const float4 sr = stats[row];
-    const float2 rsu = splat2(sr.y), cu = splat2(-sr.x * sr.y), rsg = splat2(sr.w), cgs = splat2(-sr.z * sr.w);
-    const __nv_bfloat16* zu = Z + row * zstride;
-    const __nv_bfloat16* dh = dHl + row * static_cast<int64_t>(H);
-    const int64_t pr = static_cast<int64_t>(r) * H;
-    float2 s1u = splat2(0.f), s2u = splat2(0.f), s1g = splat2(0.f), s2g = splat2(0.f);
-#pragma unroll 2
-    for (int c = 8 * lane; c < H; c += 256) {
-      const uint4 pu = __ldcs(reinterpret_cast<const uint4*>(zu + c));
-      const uint4 pg = __ldcs(reinterpret_cast<const uint4*>(zu + H + c));
-      const uint4 ph = __ldcs(reinterpret_cast<const uint4*>(dh + c));
+  const int nch = (H + 255) / 256;
+  const int64_t my_rows = first < rows ? (rows - first + warps - 1) / warps : 0;
+  const int64_t items = my_rows * nch;  // (row, chunk) pairs of this warp, row-major
+
+  auto issue = [&](int64_t i) {
+    if (i < items) {
+      const int64_t k = i / nch;
+      const int c = static_cast<int>(i - k * nch) * 256 + 8 * lane;
+      const int64_t row = first + k * warps;
+      const bool ok = c < H;
+      const int cc = ok ? c : 0;
+      uint4* st = ring + (i % kRowsumStages) * (3 * 32);
+      cp_async16(st + lane, Z + row * zstride + cc, ok);
+      cp_async16(st + 32 + lane, Z + row * zstride + H + cc, ok);
+      cp_async16(st + 64 + lane, dHl + row * static_cast<int64_t>(H) + cc, ok);
+    }
+    cp_async_commit();
+  };
+#pragma unroll
+  for (int i = 0; i < kRowsumStages - 1; ++i) issue(i);
+
+  float4 sr_next = my_rows > 0 ? stats[first] : make_float4(0.f, 0.f, 0.f, 0.f);
+  float4 sr = sr_next;
+  float2 s1u = splat2(0.f), s2u = splat2(0.f), s1g = splat2(0.f), s2g = splat2(0.f);
+  float2 rsu = splat2(0.f), cu = rsu, rsg = rsu, cgs = rsu;
+  int64_t pr = 0;
+  for (int64_t i = 0; i < items; ++i) {
+    issue(i + kRowsumStages - 1);
+    const int64_t k = i / nch;
+    const int ch = static_cast<int>(i - k * nch);
+    const int64_t row = first + k * warps;
+    if (ch == 0) {
+      sr = sr_next;
+      if (k + 1 < my_rows) sr_next = stats[row + warps];
+      rsu = splat2(sr.y);
+      cu = splat2(-sr.x * sr.y);
+      rsg = splat2(sr.w);
+      cgs = splat2(-sr.z * sr.w);
+      pr = static_cast<int64_t>(static_cast<int>(row / M) / L) * H;
+    }
+    cp_async_wait<kRowsumStages - 1>();
+    const int c = ch * 256 + 8 * lane;
+    if (c < H) {
+      const uint4* st = ring + (i % kRowsumStages) * (3 * 32);
+      const uint4 pu = st[lane], pg = st[32 + lane], ph = st[64 + lane];
       const AffineF af = load_affine_f(gx, bx, gg, bg, pr + c);
       const uint32_t uw[4] = {pu.x, pu.y, pu.z, pu.w}, gw[4] = {pg.x, pg.y, pg.z, pg.w};
       const uint32_t hw[4] = {ph.x, ph.y, ph.z, ph.w};
@@ -262,14 +306,18 @@ __global__ void __launch_bounds__(kRowsumThreads, 2) ln_gate_bwd_rowsum_kernel(
         s2g = fma2(dxg, gp.xg, s2g);
       }
     }
-    float acc[4] = {s1u.x + s1u.y, s2u.x + s2u.y, s1g.x + s1g.y, s2g.x + s2g.y};
+    if (ch == nch - 1) {
+      float acc[4] = {s1u.x + s1u.y, s2u.x + s2u.y, s1g.x + s1g.y, s2g.x + s2g.y};
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
+      for (int q = 0; q < 4; ++q) {
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) acc[i] += __shfl_xor_sync(0xffffffffu, acc[i], o);
+        for (int o = 16; o > 0; o >>= 1) acc[q] += __shfl_xor_sync(0xffffffffu, acc[q], o);
+      }
+      if (lane == 0) rowsum[row] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+      s1u = s2u = s1g = s2g = splat2(0.f);
     }
-    if (lane == 0) rowsum[row] = make_float4(acc[0], acc[1], acc[2], acc[3]);
   }
+  cp_async_wait<0>();
 }
 
 constexpr int kApplyThreads = 128;  // 8 columns per thread
@@ -281,10 +329,13 @@ __global__ void __launch_bounds__(kApplyThreads) ln_gate_bwd_apply_kernel(
     const __nv_bfloat16* __restrict__ dHl, const __nv_bfloat16* __restrict__ gx, const __nv_bfloat16* __restrict__ bx,
     const __nv_bfloat16* __restrict__ gg, const __nv_bfloat16* __restrict__ bg, __nv_bfloat16* __restrict__ dZ,
     float* __restrict__ part, int M, int L, int H, const uint32_t* err) {
-  // per stage and thread: u, g, dh (16 B each), stats, rowsum (16 B each)
+  // per stage: u, g, dh of each thread (16 B each), then the row's statistics
+  // and row sums once per warp (copied by lanes 0 and 1)
   extern __shared__ uint4 ring_raw[];
-  auto ring = reinterpret_cast<uint4(*)[5][kApplyThreads]>(ring_raw);
-  if (ld_volatile_u32(err) != 0u) return;
+  auto ring = reinterpret_cast<uint4(*)[3][kApplyThreads]>(ring_raw);
+  auto slot = reinterpret_cast<uint4(*)[kApplyThreads / 32][2]>(ring_raw + kApplyStages * 3 * kApplyThreads);
+  if (warp_aborted(err)) return;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int t = blockIdx.y, rsp = blockIdx.z, nsplit = gridDim.z;
   const int r = t / L;
   const int c0 = blockIdx.x * (8 * kApplyThreads) + 8 * threadIdx.x;
@@ -307,8 +358,8 @@ __global__ void __launch_bounds__(kApplyThreads) ln_gate_bwd_apply_kernel(
       cp_async16(&ring[s][0][threadIdx.x], Z + row * zstride + cc, active);
       cp_async16(&ring[s][1][threadIdx.x], Z + row * zstride + H + cc, active);
       cp_async16(&ring[s][2][threadIdx.x], dHl + row * H + cc, active);
-      cp_async16(&ring[s][3][threadIdx.x], stats + row, true);
-      cp_async16(&ring[s][4][threadIdx.x], rowsum + row, true);
+      if (lane == 0) cp_async16(&slot[s][warp][0], stats + row, true);
+      if (lane == 1) cp_async16(&slot[s][warp][1], rowsum + row, true);
     }
     cp_async_commit();
   };
@@ -317,11 +368,12 @@ __global__ void __launch_bounds__(kApplyThreads) ln_gate_bwd_apply_kernel(
   for (int i = 0; i < n_rows; ++i) {
     issue(i + kApplyStages - 1);
     cp_async_wait<kApplyStages - 1>();
+    __syncwarp();  // lanes 0 and 1 copied this row's scalars for the whole warp
     const int s = i % kApplyStages;
     if (!active) continue;
     const int64_t row = rowbase + i;
     const uint4 pu = ring[s][0][threadIdx.x], pg = ring[s][1][threadIdx.x], ph = ring[s][2][threadIdx.x];
-    const uint4 stv = ring[s][3][threadIdx.x], rsv = ring[s][4][threadIdx.x];
+    const uint4 stv = slot[s][warp][0], rsv = slot[s][warp][1];
     const float mu_u = __uint_as_float(stv.x), rs_u = __uint_as_float(stv.y);
     const float mu_g = __uint_as_float(stv.z), rs_g = __uint_as_float(stv.w);
     const float2 rsu = splat2(rs_u), cu = splat2(-mu_u * rs_u), rsg = splat2(rs_g), cgs = splat2(-mu_g * rs_g);
@@ -530,15 +582,18 @@ cudaError_t launch_ln_gate_bwd_rowsum(const void* Z, const void* stats, const vo
                                       const void* nx_b, const void* ng_w, const void* ng_b, void* rowsum, int T, int M,
                                       int L, int H, const DeviceInfo& dev, cudaStream_t s) {
   const int64_t rows = static_cast<int64_t>(T) * M;
+  const int smem = kRowsumWarps * kRowsumStages * 3 * 32 * 16;
+  cudaError_t e = cudaFuncSetAttribute(ln_gate_bwd_rowsum_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
   int per_sm = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, ln_gate_bwd_rowsum_kernel, kRowsumThreads, 0) !=
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, ln_gate_bwd_rowsum_kernel, kRowsumThreads, smem) !=
           cudaSuccess ||
       per_sm < 1)
     per_sm = 1;
   int64_t blocks = static_cast<int64_t>(per_sm) * dev.num_sms;
-  const int64_t need = (rows + kRowsumThreads / 32 - 1) / (kRowsumThreads / 32);
+  const int64_t need = (rows + kRowsumWarps - 1) / kRowsumWarps;
   if (blocks > need) blocks = need;
-  ln_gate_bwd_rowsum_kernel<<<static_cast<int>(blocks), kRowsumThreads, 0, s>>>(
+  ln_gate_bwd_rowsum_kernel<<<static_cast<int>(blocks), kRowsumThreads, smem, s>>>(
       static_cast<const __nv_bfloat16*>(Z), static_cast<const float4*>(stats), static_cast<const __nv_bfloat16*>(dHl),
       static_cast<const __nv_bfloat16*>(nx_w), static_cast<const __nv_bfloat16*>(nx_b),
       static_cast<const __nv_bfloat16*>(ng_w), static_cast<const __nv_bfloat16*>(ng_b), static_cast<float4*>(rowsum),
@@ -559,7 +614,7 @@ cudaError_t launch_ln_gate_bwd_apply(const void* Z, const void* stats, const voi
                                      float* part, int T, int M, int L, int H, int nsplit, const DeviceInfo& dev,
                                      cudaStream_t s) {
   dim3 grid((H + 8 * kApplyThreads - 1) / (8 * kApplyThreads), T, nsplit);
-  const int smem = kApplyStages * 5 * kApplyThreads * 16;
+  const int smem = kApplyStages * (3 * kApplyThreads + 2 * (kApplyThreads / 32)) * 16;
   cudaError_t e = cudaFuncSetAttribute(ln_gate_bwd_apply_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   ln_gate_bwd_apply_kernel<<<grid, kApplyThreads, smem, s>>>(
