@@ -249,36 +249,43 @@ __global__ void __launch_bounds__(kRowsumThreads, 3) ln_gate_bwd_rowsum_kernel(
   const int64_t my_rows = first < rows ? (rows - first + warps - 1) / warps : 0;
   const int64_t items = my_rows * nch;  // (row, chunk) pairs of this warp, row-major
 
-  auto issue = [&](int64_t i) {
-    if (i < items) {
-      const int64_t k = i / nch;
-      const int c = static_cast<int>(i - k * nch) * 256 + 8 * lane;
-      const int64_t row = first + k * warps;
+  // issue cursor: the (row, chunk) of the next item to copy, advanced one item at a time
+  int64_t iss_row = first;
+  int iss_ch = 0, iss_stage = 0;
+  int64_t issued = 0;
+  auto issue = [&]() {
+    if (issued < items) {
+      const int c = iss_ch * 256 + 8 * lane;
       const bool ok = c < H;
       const int cc = ok ? c : 0;
-      uint4* st = ring + (i % kRowsumStages) * (3 * 32);
-      cp_async16(st + lane, Z + row * zstride + cc, ok);
-      cp_async16(st + 32 + lane, Z + row * zstride + H + cc, ok);
-      cp_async16(st + 64 + lane, dHl + row * static_cast<int64_t>(H) + cc, ok);
+      uint4* st = ring + iss_stage * (3 * 32);
+      cp_async16(st + lane, Z + iss_row * zstride + cc, ok);
+      cp_async16(st + 32 + lane, Z + iss_row * zstride + H + cc, ok);
+      cp_async16(st + 64 + lane, dHl + iss_row * static_cast<int64_t>(H) + cc, ok);
+      if (++iss_ch == nch) {
+        iss_ch = 0;
+        iss_row += warps;
+      }
+      if (++iss_stage == kRowsumStages) iss_stage = 0;
+      ++issued;
     }
     cp_async_commit();
   };
 #pragma unroll
-  for (int i = 0; i < kRowsumStages - 1; ++i) issue(i);
+  for (int i = 0; i < kRowsumStages - 1; ++i) issue();
 
   float4 sr_next = my_rows > 0 ? stats[first] : make_float4(0.f, 0.f, 0.f, 0.f);
   float4 sr = sr_next;
   float2 s1u = splat2(0.f), s2u = splat2(0.f), s1g = splat2(0.f), s2g = splat2(0.f);
   float2 rsu = splat2(0.f), cu = rsu, rsg = rsu, cgs = rsu;
   int64_t pr = 0;
+  int64_t row = first;
+  int ch = 0, stage = 0;
   for (int64_t i = 0; i < items; ++i) {
-    issue(i + kRowsumStages - 1);
-    const int64_t k = i / nch;
-    const int ch = static_cast<int>(i - k * nch);
-    const int64_t row = first + k * warps;
+    issue();
     if (ch == 0) {
       sr = sr_next;
-      if (k + 1 < my_rows) sr_next = stats[row + warps];
+      if (row + warps < rows) sr_next = stats[row + warps];
       rsu = splat2(sr.y);
       cu = splat2(-sr.x * sr.y);
       rsg = splat2(sr.w);
@@ -288,7 +295,7 @@ __global__ void __launch_bounds__(kRowsumThreads, 3) ln_gate_bwd_rowsum_kernel(
     cp_async_wait<kRowsumStages - 1>();
     const int c = ch * 256 + 8 * lane;
     if (c < H) {
-      const uint4* st = ring + (i % kRowsumStages) * (3 * 32);
+      const uint4* st = ring + stage * (3 * 32);
       const uint4 pu = st[lane], pg = st[32 + lane], ph = st[64 + lane];
       const AffineF af = load_affine_f(gx, bx, gg, bg, pr + c);
       const uint32_t uw[4] = {pu.x, pu.y, pu.z, pu.w}, gw[4] = {pg.x, pg.y, pg.z, pg.w};
@@ -316,6 +323,11 @@ __global__ void __launch_bounds__(kRowsumThreads, 3) ln_gate_bwd_rowsum_kernel(
       if (lane == 0) rowsum[row] = make_float4(acc[0], acc[1], acc[2], acc[3]);
       s1u = s2u = s1g = s2g = splat2(0.f);
     }
+    if (++ch == nch) {
+      ch = 0;
+      row += warps;
+    }
+    if (++stage == kRowsumStages) stage = 0;
   }
   cp_async_wait<0>();
 }
