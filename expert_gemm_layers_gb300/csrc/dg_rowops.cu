@@ -223,80 +223,35 @@ __global__ void __launch_bounds__(NT, 512 / NT) ln_gate_fwd_kernel(
 // da*x_u, da (norm_x grads), ds*x_g, ds (norm_gate grads) in registers; the
 // per-(t, row range) partial sums are added in a fixed order afterwards.
 
-// Pass 1: one warp per row, no block barrier.  A warp's rows are cut into
-// 256-column chunks (8 columns per lane) that stream through a per-warp
-// shared-memory ring filled by per-lane cp.async; the ring runs on across
-// row boundaries, so several KB per warp stay in flight.  The four sums are
-// reduced with shuffles at the end of each row.  The affines come through L1
-// (a CTA's warps work on consecutive rows, hence mostly on one rank).
+// Pass 1: one warp per row, no block barrier.  The warp walks the row in
+// 256-column steps (8 columns per lane), two steps in flight, and reduces
+// the four sums with shuffles.  The affines come through L1 (a CTA's warps
+// work on consecutive rows, hence mostly on one rank).
 constexpr int kRowsumThreads = 256;
-constexpr int kRowsumWarps = kRowsumThreads / 32;
-constexpr int kRowsumStages = 6;
 
-__global__ void __launch_bounds__(kRowsumThreads, 3) ln_gate_bwd_rowsum_kernel(
+__global__ void __launch_bounds__(kRowsumThreads, 2) ln_gate_bwd_rowsum_kernel(
     const __nv_bfloat16* __restrict__ Z, const float4* __restrict__ stats, const __nv_bfloat16* __restrict__ dHl,
     const __nv_bfloat16* __restrict__ gx, const __nv_bfloat16* __restrict__ bx, const __nv_bfloat16* __restrict__ gg,
     const __nv_bfloat16* __restrict__ bg, float4* __restrict__ rowsum, int64_t rows, int M, int L, int H,
     const uint32_t* err) {
-  extern __shared__ uint4 rs_ring[];  // [kRowsumWarps][kRowsumStages][3][32]
   if (warp_aborted(err)) return;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  uint4* ring = rs_ring + warp * (kRowsumStages * 3 * 32);
-  const int64_t warps = static_cast<int64_t>(gridDim.x) * kRowsumWarps;
-  const int64_t first = static_cast<int64_t>(blockIdx.x) * kRowsumWarps + warp;
+  const int lane = threadIdx.x & 31;
+  const int64_t warps = static_cast<int64_t>(gridDim.x) * (kRowsumThreads / 32);
   const int64_t zstride = 2 * static_cast<int64_t>(H);
-  const int nch = (H + 255) / 256;
-  const int64_t my_rows = first < rows ? (rows - first + warps - 1) / warps : 0;
-  const int64_t items = my_rows * nch;  // (row, chunk) pairs of this warp, row-major
-
-  // issue cursor: the (row, chunk) of the next item to copy, advanced one item at a time
-  int64_t iss_row = first;
-  int iss_ch = 0, iss_stage = 0;
-  int64_t issued = 0;
-  auto issue = [&]() {
-    if (issued < items) {
-      const int c = iss_ch * 256 + 8 * lane;
-      const bool ok = c < H;
-      const int cc = ok ? c : 0;
-      uint4* st = ring + iss_stage * (3 * 32);
-      cp_async16(st + lane, Z + iss_row * zstride + cc, ok);
-      cp_async16(st + 32 + lane, Z + iss_row * zstride + H + cc, ok);
-      cp_async16(st + 64 + lane, dHl + iss_row * static_cast<int64_t>(H) + cc, ok);
-      if (++iss_ch == nch) {
-        iss_ch = 0;
-        iss_row += warps;
-      }
-      if (++iss_stage == kRowsumStages) iss_stage = 0;
-      ++issued;
-    }
-    cp_async_commit();
-  };
-#pragma unroll
-  for (int i = 0; i < kRowsumStages - 1; ++i) issue();
-
-  float4 sr_next = my_rows > 0 ? stats[first] : make_float4(0.f, 0.f, 0.f, 0.f);
-  float4 sr = sr_next;
-  float2 s1u = splat2(0.f), s2u = splat2(0.f), s1g = splat2(0.f), s2g = splat2(0.f);
-  float2 rsu = splat2(0.f), cu = rsu, rsg = rsu, cgs = rsu;
-  int64_t pr = 0;
-  int64_t row = first;
-  int ch = 0, stage = 0;
-  for (int64_t i = 0; i < items; ++i) {
-    issue();
-    if (ch == 0) {
-      sr = sr_next;
-      if (row + warps < rows) sr_next = stats[row + warps];
-      rsu = splat2(sr.y);
-      cu = splat2(-sr.x * sr.y);
-      rsg = splat2(sr.w);
-      cgs = splat2(-sr.z * sr.w);
-      pr = static_cast<int64_t>(static_cast<int>(row / M) / L) * H;
-    }
-    cp_async_wait<kRowsumStages - 1>();
-    const int c = ch * 256 + 8 * lane;
-    if (c < H) {
-      const uint4* st = ring + stage * (3 * 32);
-      const uint4 pu = st[lane], pg = st[32 + lane], ph = st[64 + lane];
+  for (int64_t row = static_cast<int64_t>(blockIdx.x) * (kRowsumThreads / 32) + (threadIdx.x >> 5); row < rows;
+       row += warps) {
+    const int r = static_cast<int>(row / M) / L;
+    const float4 sr = stats[row];
+    const float2 rsu = splat2(sr.y), cu = splat2(-sr.x * sr.y), rsg = splat2(sr.w), cgs = splat2(-sr.z * sr.w);
+    const __nv_bfloat16* zu = Z + row * zstride;
+    const __nv_bfloat16* dh = dHl + row * static_cast<int64_t>(H);
+    const int64_t pr = static_cast<int64_t>(r) * H;
+    float2 s1u = splat2(0.f), s2u = splat2(0.f), s1g = splat2(0.f), s2g = splat2(0.f);
+#pragma unroll 2
+    for (int c = 8 * lane; c < H; c += 256) {
+      const uint4 pu = __ldcs(reinterpret_cast<const uint4*>(zu + c));
+      const uint4 pg = __ldcs(reinterpret_cast<const uint4*>(zu + H + c));
+      const uint4 ph = __ldcs(reinterpret_cast<const uint4*>(dh + c));
       const AffineF af = load_affine_f(gx, bx, gg, bg, pr + c);
       const uint32_t uw[4] = {pu.x, pu.y, pu.z, pu.w}, gw[4] = {pg.x, pg.y, pg.z, pg.w};
       const uint32_t hw[4] = {ph.x, ph.y, ph.z, ph.w};
@@ -313,23 +268,14 @@ __global__ void __launch_bounds__(kRowsumThreads, 3) ln_gate_bwd_rowsum_kernel(
         s2g = fma2(dxg, gp.xg, s2g);
       }
     }
-    if (ch == nch - 1) {
-      float acc[4] = {s1u.x + s1u.y, s2u.x + s2u.y, s1g.x + s1g.y, s2g.x + s2g.y};
+    float acc[4] = {s1u.x + s1u.y, s2u.x + s2u.y, s1g.x + s1g.y, s2g.x + s2g.y};
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
+    for (int i = 0; i < 4; ++i) {
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) acc[q] += __shfl_xor_sync(0xffffffffu, acc[q], o);
-      }
-      if (lane == 0) rowsum[row] = make_float4(acc[0], acc[1], acc[2], acc[3]);
-      s1u = s2u = s1g = s2g = splat2(0.f);
+      for (int o = 16; o > 0; o >>= 1) acc[i] += __shfl_xor_sync(0xffffffffu, acc[i], o);
     }
-    if (++ch == nch) {
-      ch = 0;
-      row += warps;
-    }
-    if (++stage == kRowsumStages) stage = 0;
+    if (lane == 0) rowsum[row] = make_float4(acc[0], acc[1], acc[2], acc[3]);
   }
-  cp_async_wait<0>();
 }
 
 constexpr int kApplyThreads = 128;  // 8 columns per thread
@@ -594,18 +540,15 @@ cudaError_t launch_ln_gate_bwd_rowsum(const void* Z, const void* stats, const vo
                                       const void* nx_b, const void* ng_w, const void* ng_b, void* rowsum, int T, int M,
                                       int L, int H, const DeviceInfo& dev, cudaStream_t s) {
   const int64_t rows = static_cast<int64_t>(T) * M;
-  const int smem = kRowsumWarps * kRowsumStages * 3 * 32 * 16;
-  cudaError_t e = cudaFuncSetAttribute(ln_gate_bwd_rowsum_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (e != cudaSuccess) return e;
   int per_sm = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, ln_gate_bwd_rowsum_kernel, kRowsumThreads, smem) !=
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, ln_gate_bwd_rowsum_kernel, kRowsumThreads, 0) !=
           cudaSuccess ||
       per_sm < 1)
     per_sm = 1;
   int64_t blocks = static_cast<int64_t>(per_sm) * dev.num_sms;
-  const int64_t need = (rows + kRowsumWarps - 1) / kRowsumWarps;
+  const int64_t need = (rows + kRowsumThreads / 32 - 1) / (kRowsumThreads / 32);
   if (blocks > need) blocks = need;
-  ln_gate_bwd_rowsum_kernel<<<static_cast<int>(blocks), kRowsumThreads, smem, s>>>(
+  ln_gate_bwd_rowsum_kernel<<<static_cast<int>(blocks), kRowsumThreads, 0, s>>>(
       static_cast<const __nv_bfloat16*>(Z), static_cast<const float4*>(stats), static_cast<const __nv_bfloat16*>(dHl),
       static_cast<const __nv_bfloat16*>(nx_w), static_cast<const __nv_bfloat16*>(nx_b),
       static_cast<const __nv_bfloat16*>(ng_w), static_cast<const __nv_bfloat16*>(ng_b), static_cast<float4*>(rowsum),
