@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "../../include/dg.h"
 #include "dg_gemm.cuh"
 
@@ -90,15 +92,18 @@ cudaError_t launch_gemm_t(const CUtensorMap& a, const CUtensorMap& b, const CUte
                           const GemmParams& p, int num_sms, cudaStream_t s) {
   using Cfg = GemmCfg<kFp8, kAMN, kBMN, kEpi, kUsePairs>;
   auto kern = gemm_tc_kernel<kFp8, kAMN, kBMN, kEpi, kUsePairs>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
+  // Per device, once: the shared-memory attribute and the number of co-resident
+  // CTA pairs (host-side work kept off the launch path).
+  static std::atomic<int> units_cache[64];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  const int64_t tiles = static_cast<int64_t>(p.G) * p.tiles_m * p.tiles_n;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   cfg.blockDim = dim3(Cfg::NUM_THREADS);
   cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
   cfg.stream = s;
-  int units = num_sms;
   if (kUsePairs) {
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
@@ -106,12 +111,22 @@ cudaError_t launch_gemm_t(const CUtensorMap& a, const CUtensorMap& b, const CUte
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cfg.gridDim = dim3(2);
-    int clusters = 0;
-    e = cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg);
-    if (e != cudaSuccess) return e;
-    units = clusters > 0 ? clusters : 1;
   }
+  int units = units_cache[dev].load(std::memory_order_relaxed);
+  if (units == 0) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    units = num_sms;
+    if (kUsePairs) {
+      cfg.gridDim = dim3(2);
+      int clusters = 0;
+      e = cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg);
+      if (e != cudaSuccess) return e;
+      units = clusters > 0 ? clusters : 1;
+    }
+    units_cache[dev].store(units, std::memory_order_relaxed);
+  }
+  const int64_t tiles = static_cast<int64_t>(p.G) * p.tiles_m * p.tiles_n;
   if (tiles < units) units = static_cast<int>(tiles);
   cfg.gridDim = dim3(units * Cfg::CTAS);
   return cudaLaunchKernelEx(&cfg, kern, a, b, d, c, p);

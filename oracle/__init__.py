@@ -47,7 +47,8 @@ __all__ = [
     "layer_norm", "silu", "FFNShape", "ffn_forward", "ffn_forward_rows",
     "ffn_problem_backward", "ffn_backward", "ffn_backward_dx_rows",
     "ffn_backward_problem", "ffn_backward_norm_rank",
-    "tp_swiglu", "tp_swiglu_rows",
+    "tp_swiglu", "tp_swiglu_rows", "tp_swiglu_backward", "tp_swiglu_backward_rows",
+    "tp_swiglu_backward_weight_cols",
 ]
 
 
@@ -503,3 +504,95 @@ def tp_swiglu_rows(x_shards_bits, w13_bits, w2_bits, W: int, rows) -> np.ndarray
     d = xs.shape[-1]
     X = bf16_to_f64(xs.reshape(-1, d)[np.asarray(rows, dtype=np.int64)])
     return _swiglu_shards(X, bf16_to_f64(w13_bits), bf16_to_f64(w2_bits), W)
+
+
+def _swiglu_shard_backward(X, dY, w13s, w2s):
+    """Gradients of one shard's pair, Y_s = (silu(X w1_s^T) * (X w3_s^T)) w2_s^T.
+
+    The row-parallel sum passes dY unchanged to every shard's partial.  With
+    a = X w1^T, b = X w3^T, sig = sigmoid(a), h = a*sig*b:
+      dh = dY w2_s;  dw2_s = dY^T h;
+      da = dh * b * (sig + a*sig*(1 - sig));  db = dh * a * sig;
+      dw1_s = da^T X;  dw3_s = db^T X;  dX_s = [da | db] [w1_s ; w3_s]
+    (one concatenated product for both column-parallel projections).
+    """
+    F = w13s.shape[0] // 2
+    w1, w3 = w13s[:F], w13s[F:]
+    a = X @ w1.T
+    b = X @ w3.T
+    sig = 1.0 / (1.0 + np.exp(-a))
+    h = a * sig * b
+    dh = dY @ w2s
+    da = dh * b * (sig + a * sig * (1.0 - sig))
+    db = dh * a * sig
+    dab = np.concatenate([da, db], axis=1)
+    return dict(dX=dab @ w13s, dw13=dab.T @ X, dw2=dY.T @ h)
+
+
+def tp_swiglu_backward(x_shards, w13, w2, dy_shards, W: int, decoded: bool = False) -> dict:
+    """Gradients of tp_swiglu w.r.t. x_shards, w13 and w2 (float64).
+
+    Rows are gathered exactly as in the forward (rank, seq_local, batch);
+    each shard's gradients follow _swiglu_shard_backward; dX sums the
+    shards' contributions (the transpose of the all-gather is a
+    reduce-scatter), then is scattered back to [W, bsz, S/W, d].
+    """
+    xs = np.asarray(x_shards)
+    Wn, b_, sl, d = xs.shape
+    f = (lambda a: np.asarray(a, dtype=np.float64)) if decoded else bf16_to_f64
+    X = f(xs).transpose(0, 2, 1, 3).reshape(Wn * sl * b_, d)
+    dY = f(np.asarray(dy_shards)).transpose(0, 2, 1, 3).reshape(Wn * sl * b_, d)
+    w13f, w2f = f(w13), f(w2)
+    F = w13f.shape[1] // 2
+    dX = np.zeros_like(X)
+    dw13 = np.empty_like(w13f)
+    dw2 = np.empty_like(w2f)
+    for s in range(W):
+        o = _swiglu_shard_backward(X, dY, w13f[s], w2f[:, s * F:(s + 1) * F])
+        dX += o["dX"]
+        dw13[s] = o["dw13"]
+        dw2[:, s * F:(s + 1) * F] = o["dw2"]
+    dx = dX.reshape(Wn, sl, b_, d).transpose(0, 2, 1, 3)
+    return dict(dx=dx, dw13=dw13, dw2=dw2)
+
+
+def tp_swiglu_backward_rows(x_shards_bits, w13_bits, w2_bits, dy_shards_bits, W: int, rows) -> np.ndarray:
+    """Selected rows (flat, memory order of x_shards) of dx: row-local like the forward."""
+    xs = np.asarray(x_shards_bits)
+    d = xs.shape[-1]
+    r = np.asarray(rows, dtype=np.int64)
+    X = bf16_to_f64(xs.reshape(-1, d)[r])
+    dY = bf16_to_f64(np.asarray(dy_shards_bits).reshape(-1, d)[r])
+    w13f, w2f = bf16_to_f64(w13_bits), bf16_to_f64(w2_bits)
+    F = w13f.shape[1] // 2
+    dX = np.zeros_like(X)
+    for s in range(W):
+        dX += _swiglu_shard_backward(X, dY, w13f[s], w2f[:, s * F:(s + 1) * F])["dX"]
+    return dX
+
+
+def tp_swiglu_backward_weight_cols(x_shards_bits, w13_bits, w2_bits, dy_shards_bits, W: int, cols) -> dict:
+    """dw2[:, j] and the rows j of w1_s / w3_s gradients for selected ffn columns j.
+
+    Column j = s*F + c of the ffn axis belongs to shard s; its weight
+    gradients need a[:, c], b[:, c] over all rows only, so a column subset is
+    exact.  Returns dw2 [d, len(cols)], dw1 [len(cols), d], dw3 [len(cols), d].
+    """
+    xs = np.asarray(x_shards_bits)
+    d = xs.shape[-1]
+    X = bf16_to_f64(xs.reshape(-1, d))
+    dY = bf16_to_f64(np.asarray(dy_shards_bits).reshape(-1, d))
+    w13f, w2f = bf16_to_f64(w13_bits), bf16_to_f64(w2_bits)
+    F = w13f.shape[1] // 2
+    cols = np.asarray(cols, dtype=np.int64)
+    s_idx, c_idx = np.divmod(cols, F)
+    w1 = w13f[s_idx, c_idx]          # [n, d]
+    w3 = w13f[s_idx, F + c_idx]
+    a = X @ w1.T
+    b = X @ w3.T
+    sig = 1.0 / (1.0 + np.exp(-a))
+    h = a * sig * b
+    dh = dY @ w2f[:, cols]
+    da = dh * b * (sig + a * sig * (1.0 - sig))
+    db = dh * a * sig
+    return dict(dw2=dY.T @ h, dw1=da.T @ X, dw3=db.T @ X)

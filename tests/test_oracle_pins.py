@@ -429,3 +429,73 @@ def test_oracle_is_not_imported_by_the_product_package():
             if fn.endswith((".py", ".cu", ".cuh", ".cpp", ".h")):
                 src = open(os.path.join(root, fn)).read()
                 assert "import oracle" not in src and "from oracle" not in src, fn
+
+
+# --------------------------------------------------------------------------
+# TP SwiGLU backward
+# --------------------------------------------------------------------------
+
+def _tp_tiny(seed, W=2, bsz=1, sl=2, d=3, F=2):
+    rng = np.random.default_rng(seed)
+    x = rng.standard_normal((W, bsz, sl, d))
+    w13 = rng.standard_normal((W, 2 * F, d)) / 2
+    w2 = rng.standard_normal((d, W * F)) / 2
+    dy = rng.standard_normal((W, bsz, sl, d))
+    return x, w13, w2, dy
+
+
+def test_tp_swiglu_backward_finite_differences():
+    x, w13, w2, dy = _tp_tiny(3, bsz=2)
+    g = O.tp_swiglu_backward(x, w13, w2, dy, W=2, decoded=True)
+
+    def loss():
+        return float((O.tp_swiglu(x, w13, w2, W=2, decoded=True) * dy).sum())
+    h = 1e-6
+    for arr, ga in ((x, g["dx"]), (w13, g["dw13"]), (w2, g["dw2"])):
+        flat, gf = arr.reshape(-1), ga.reshape(-1)
+        for i in range(flat.size):
+            old = flat[i]
+            flat[i] = old + h
+            lp = loss()
+            flat[i] = old - h
+            lm = loss()
+            flat[i] = old
+            num = (lp - lm) / (2 * h)
+            assert abs(num - gf[i]) <= 1e-6 * max(1.0, abs(num)), (i, num, gf[i])
+
+
+def test_tp_swiglu_backward_matches_torch_autograd_and_subsets():
+    W, Fs, d, S = 4, 6, 8, 16
+    rng = np.random.default_rng(12)
+    x = torch.from_numpy(rng.standard_normal((W, 1, S // W, d))).requires_grad_(True)
+    w1 = torch.from_numpy(rng.standard_normal((W * Fs, d)) / 3).requires_grad_(True)
+    w3 = torch.from_numpy(rng.standard_normal((W * Fs, d)) / 3).requires_grad_(True)
+    w2 = torch.from_numpy(rng.standard_normal((d, W * Fs)) / 3).requires_grad_(True)
+    dy = torch.from_numpy(rng.standard_normal((W, 1, S // W, d)))
+    # textbook unsharded SwiGLU with torch library ops
+    X = x.reshape(S, d)
+    y = (F.silu(X @ w1.T) * (X @ w3.T)) @ w2.T
+    y.reshape(W, 1, S // W, d).backward(dy)
+    w13 = torch.stack([torch.cat([w1[s * Fs:(s + 1) * Fs], w3[s * Fs:(s + 1) * Fs]]) for s in range(W)])
+    g = O.tp_swiglu_backward(x.detach().numpy(), w13.detach().numpy(), w2.detach().numpy(), dy.numpy(), W=W,
+                             decoded=True)
+    assert np.allclose(g["dx"], x.grad.numpy(), rtol=1e-10, atol=1e-10)
+    assert np.allclose(g["dw2"], w2.grad.numpy(), rtol=1e-10, atol=1e-10)
+    dw1 = np.concatenate([g["dw13"][s, :Fs] for s in range(W)])
+    dw3 = np.concatenate([g["dw13"][s, Fs:] for s in range(W)])
+    assert np.allclose(dw1, w1.grad.numpy(), rtol=1e-10, atol=1e-10)
+    assert np.allclose(dw3, w3.grad.numpy(), rtol=1e-10, atol=1e-10)
+    # bit-pattern subsets agree with the full result
+    xb, w13b, w2b, dyb = (synth.bits(torch.from_numpy(a.astype(np.float32)).to(torch.bfloat16))
+                          for a in (x.detach().numpy(), w13.detach().numpy(), w2.detach().numpy(), dy.numpy()))
+    full = O.tp_swiglu_backward(xb, w13b, w2b, dyb, W=W)
+    rows = [0, 5, S - 1]
+    assert np.allclose(O.tp_swiglu_backward_rows(xb, w13b, w2b, dyb, W, rows), full["dx"].reshape(-1, d)[rows],
+                       rtol=1e-12, atol=1e-12)
+    cols = [0, 7, W * Fs - 1]
+    wc = O.tp_swiglu_backward_weight_cols(xb, w13b, w2b, dyb, W, cols)
+    assert np.allclose(wc["dw2"], full["dw2"][:, cols], rtol=1e-12, atol=1e-12)
+    for j, c in enumerate(cols):
+        s_, cc = divmod(c, Fs)
+        assert np.allclose(wc["dw1"][j], full["dw13"][s_, cc], rtol=1e-12, atol=1e-12)
+        assert np.allclose(wc["dw3"][j], full["dw13"][s_, Fs + cc], rtol=1e-12, atol=1e-12)
