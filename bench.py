@@ -185,6 +185,12 @@ class Workload:
         self.y = torch.empty_like(self.xs)
         self.tp_ws = torch.empty(lib.dg_tp_swiglu_workspace_bytes(TP["S"], TP["d"], TP["ffn"], TP["W"], 1),
                                  dtype=torch.uint8, device=dev)
+        # the TP SwiGLU backward, timed on its own after the step
+        self.tp_dy = synth.tp_swiglu_inputs(TP["S"], TP["d"], TP["ffn"], TP["W"], seed=TP["seed"] + 1,
+                                            device=dev)[0]
+        self.tp_bws = torch.empty(lib.dg_tp_swiglu_bwd_workspace_bytes(TP["S"], TP["d"], TP["ffn"], TP["W"], 1),
+                                  dtype=torch.uint8, device=dev)
+        self.tp_grads = dict(x=torch.empty_like(self.xs), w13=torch.empty_like(self.w13), w2=torch.empty_like(self.w2))
 
     def inputs(self):
         return [self.A, self.B, self.C, self.x, *self.params.values(), self.dY, self.xs, self.w13, self.w2]
@@ -204,6 +210,10 @@ class Workload:
         if marks is not None:
             marks[2].record()
         dg.tp_swiglu(self.xs, self.w13, self.w2, workspace=self.tp_ws, out=self.y)
+
+    def tp_backward(self):
+        self.dg.tp_swiglu_backward(self.xs, self.w13, self.w2, self.tp_dy, workspace=self.tp_bws,
+                                   grads=self.tp_grads)
 
 
 # ---------------------------------------------------------------- oracle sample
@@ -408,6 +418,9 @@ def run_dg(args, rank, world):
                                 "share": round(e["total_ms"] / total_ms, 4)} for e in trace}
     launches = int(sum(e["launches"] for e in trace))
 
+    # outside the step: the TP SwiGLU backward (recompute [a|b], dh, gate backward, dw2, dX, dw13)
+    extra = run_tp_backward(w, args, dev, peaks)
+
     # end to end: inputs from pinned host memory in, results back to pinned host memory
     e2e = run_e2e(w, args, dev, step_flops, world)
 
@@ -418,7 +431,7 @@ def run_dg(args, rank, world):
         "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16+e4m3 (fp32 accumulate)", "data": "synthetic",
         "config": workload_config(), "parts": parts, "roofline": roof, "kernels": kernel_table,
-        "gpu_launches": launches, "e2e": e2e, "clocks": clk,
+        "gpu_launches": launches, "e2e": e2e, "clocks": clk, "outside_step": extra,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         sample = OracleSample(host_bits(w))
@@ -428,6 +441,37 @@ def run_dg(args, rank, world):
                                 "seconds": round(sec, 2)}
     if rank == 0:
         print(json.dumps(line), flush=True)
+
+
+def run_tp_backward(w, args, dev, peaks):
+    """The TP SwiGLU backward at the forward's shape, timed alone (not part of the step)."""
+    import torch
+    dg = w.dg
+    for _ in range(max(args.warmup, 2)):
+        w.tp_backward()
+    iters = 5
+    stream = torch.cuda.current_stream(dev)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    torch.cuda.synchronize(dev)
+    dg.trace_begin()
+    ev[0].record(stream)
+    for _ in range(iters):
+        w.tp_backward()
+    ev[1].record(stream)
+    torch.cuda.synchronize(dev)
+    trace = dg.trace_end()
+    st, code = dg.device_status(dev)
+    if st != 0:
+        raise RuntimeError(f"device error word after the TP backward: {code:#x}")
+    ms = ev[0].elapsed_time(ev[1]) / iters
+    R, d, ffn = TP["S"], TP["d"], TP["ffn"]
+    flops = 16.0 * R * d * ffn  # [a|b] 4, dh 2, dw2 2, dX 4, dw13 4 (x R*d*ffn)
+    tf = flops / (ms * 1e-3) / 1e12
+    return {"tp_swiglu_bwd": {
+        "ms": round(ms, 4), "tflops": round(tf, 2), "peak_tflops": peaks["bf16_tflops"],
+        "frac_of_peak": round(tf / peaks["bf16_tflops"], 4), "iters": iters,
+        "kernels": {e["name"]: {"launches": e["launches"], "ms_per_launch": round(e["total_ms"] / e["launches"], 4)}
+                    for e in trace}}}
 
 
 def run_e2e(w, args, dev, step_flops, world):

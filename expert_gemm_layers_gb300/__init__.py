@@ -7,16 +7,17 @@ TMA/mbarrier pipelines):
 * gemm_fp8      D = alpha * (A @ B^T) + beta * C, e4m3 inputs, bf16 output
 * a2a_ffn       the all-to-all expert-parallel FFN layer (forward, backward,
                 autograd), P logical ranks in one GPU's memory
-* tp_swiglu     the SwiGLU column/row-parallel pair over W shards
+* tp_swiglu     the SwiGLU column/row-parallel pair over W shards (forward,
+                backward, autograd)
 
 The library is loaded lazily on first use and fails loudly if it is missing.
 """
-from .ops import (A2AFFN, FFN_PARAM_NAMES, a2a_combine, a2a_dispatch, a2a_ffn, a2a_ffn_backward,
+from .ops import (A2AFFN, FFN_PARAM_NAMES, TPSwiGLU, a2a_combine, a2a_dispatch, a2a_ffn, a2a_ffn_backward,
                   a2a_ffn_forward, debug_wait_timeout, device_status, ffn_shape, gemm_fp8, tp_swiglu,
-                  trace_begin, trace_end)
+                  tp_swiglu_backward, tp_swiglu_layer, trace_begin, trace_end)
 
 __all__ = [
     "A2AFFN", "FFN_PARAM_NAMES", "a2a_combine", "a2a_dispatch", "a2a_ffn", "a2a_ffn_backward",
     "a2a_ffn_forward", "debug_wait_timeout", "device_status", "ffn_shape", "gemm_fp8", "tp_swiglu",
-    "trace_begin", "trace_end",
+    "tp_swiglu_backward", "TPSwiGLU", "tp_swiglu_layer", "trace_begin", "trace_end",
 ]

@@ -52,6 +52,9 @@ SIGNATURES = {
     "dg_a2a_combine": (ctypes.c_int, [_i32, _i32, _i32, _i32, _vp, _vp, _vp]),
     "dg_tp_swiglu_workspace_bytes": (_sz, [_i64, _i64, _i64, _i32, _i32]),
     "dg_tp_swiglu": (ctypes.c_int, [_i64, _i64, _i64, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
+    "dg_tp_swiglu_bwd_workspace_bytes": (_sz, [_i64, _i64, _i64, _i32, _i32]),
+    "dg_tp_swiglu_bwd": (ctypes.c_int, [_i64, _i64, _i64, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz,
+                                        _vp]),
     "dg_tp_swiglu_noalloc": (ctypes.c_int, [_i64, _i64, _i64, _i32, _i32, _vp, _vp, _vp, _vp, _vp]),
     "dg_trace_begin": (ctypes.c_int, []),
     "dg_trace_end": (ctypes.c_int32, [ctypes.POINTER(TraceEntry), ctypes.c_int32]),

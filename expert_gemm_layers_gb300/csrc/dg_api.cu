@@ -188,6 +188,7 @@ dg_status run_gemm(GemmVariant v, const CUtensorMap& a, const CUtensorMap& b, co
     case GV_BF16_MM_STORE: e = launch_gemm_bf16_mm_store(a, b, d, c, p, grid, s); break;
     case GV_BF16_KK_SWIGLU: e = launch_gemm_bf16_kk_swiglu(a, b, d, c, p, grid, s); break;
     case GV_BF16_KM_LNSTATS: e = launch_gemm_bf16_km_lnstats(a, b, d, c, p, grid, s); break;
+    case GV_BF16_KM_STORE: e = launch_gemm_bf16_km_store(a, b, d, c, p, grid, s); break;
     default: return fail(DG_ERR_UNSUPPORTED, "unknown GEMM variant");
   }
   if (e != cudaSuccess) return cuda_fail(e, "GEMM launch");
@@ -705,6 +706,141 @@ dg_status dg_tp_swiglu(int64_t S, int64_t d, int64_t ffn, int32_t W, int32_t bsz
   p.d_g = G_OUTER;
   return run_gemm(GV_BF16_KK_STORE, mh_k, mw2, my, my, p, dev, s, "tp_gemm2",
                   2.0 * (static_cast<double>(R) * FF + static_cast<double>(Dm) * FF + static_cast<double>(R) * Dm));
+}
+
+size_t dg_tp_swiglu_bwd_workspace_bytes(int64_t S, int64_t d, int64_t ffn, int32_t W, int32_t bsz) {
+  if (S < 1 || d < 1 || ffn < 1 || W < 1 || bsz < 1 || S % W || ffn % W) return 0;
+  // [a|b] (later [da|db]) is [rows, 2*ffn]; dh (later h) is [rows, ffn].
+  return 3 * round_up(static_cast<size_t>(S) * bsz * ffn * 2, 256);
+}
+
+dg_status dg_tp_swiglu_bwd(int64_t S, int64_t d, int64_t ffn, int32_t W, int32_t bsz, const void* x_shards,
+                           const void* w13, const void* w2, const void* dy_shards, void* dx_shards, void* d_w13,
+                           void* d_w2, void* ws, size_t ws_bytes, void* stream) {
+  if (S < 1 || d < 1 || ffn < 1 || W < 1 || bsz < 1)
+    return fail(DG_ERR_INVALID_ARGUMENT, "tp_swiglu_bwd: S, d, ffn, W, bsz must be >= 1");
+  if (S % W || ffn % W) return fail(DG_ERR_INVALID_ARGUMENT, "tp_swiglu_bwd: S and ffn must be divisible by W");
+  const int64_t F = ffn / W;
+  if (d % 8 || F % 8) return fail(DG_ERR_INVALID_ARGUMENT, "tp_swiglu_bwd: d and ffn/W must be multiples of 8");
+  const int64_t rows = S * bsz;
+  if (rows > 0x7fffffff || 2 * ffn > 0x7fffffff || d > 0x7fffffff)
+    return fail(DG_ERR_UNSUPPORTED, "tp_swiglu_bwd: sizes beyond 2^31-1");
+  const void* ptrs[] = {x_shards, w13, w2, dy_shards, dx_shards, d_w13, d_w2, ws};
+  const char* names[] = {"x_shards", "w13", "w2", "dy_shards", "dx_shards", "d_w13", "d_w2", "ws"};
+  if (const char* n = ptr_name_null(ptrs, names, 8))
+    return fail(DG_ERR_INVALID_ARGUMENT, "tp_swiglu_bwd: %s is NULL", n);
+  if (const char* n = ptr_name_unaligned(ptrs, names, 8))
+    return fail(DG_ERR_INVALID_ARGUMENT, "tp_swiglu_bwd: %s is not 16-byte aligned", n);
+  const size_t need = dg_tp_swiglu_bwd_workspace_bytes(S, d, ffn, W, bsz);
+  if (ws_bytes < need)
+    return fail(DG_ERR_WORKSPACE, "tp_swiglu_bwd: workspace has %zu bytes, needs %zu", ws_bytes, need);
+  const size_t act = static_cast<size_t>(rows) * d * 2;
+  const size_t wbytes = static_cast<size_t>(2) * ffn * d * 2, w2bytes = static_cast<size_t>(ffn) * d * 2;
+  // Every written region (dx, d_w13, d_w2, ws) must be disjoint from every
+  // other region, read or written.
+  const void* wr[] = {dx_shards, d_w13, d_w2, ws};
+  const size_t wr_n[] = {act, wbytes, w2bytes, need};
+  const void* all[] = {x_shards, w13, w2, dy_shards, dx_shards, d_w13, d_w2, ws};
+  const size_t all_n[] = {act, wbytes, w2bytes, act, act, wbytes, w2bytes, need};
+  for (int i = 0; i < 4; ++i)
+    for (int j = 0; j < 8; ++j)
+      if (j != 4 + i && overlaps(wr[i], wr_n[i], all[j], all_n[j]))
+        return fail(DG_ERR_INVALID_ARGUMENT, "tp_swiglu_bwd: %s overlaps %s", names[4 + i], names[j]);
+  DeviceInfo dev;
+  dg_status st = device_info(&dev);
+  if (st != DG_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const uint64_t R = rows, Dm = d, FF = ffn, F2 = 2 * ffn;
+  const size_t ab_bytes = round_up(static_cast<size_t>(rows) * ffn * 2, 256) * 2;
+  void* ab = ws;                                             // [R, W, 2F]: (a_s | b_s), then (da_s | db_s)
+  void* dh = static_cast<unsigned char*>(ws) + ab_bytes;     // [R, ffn]: dh, then h
+  const double r = static_cast<double>(R), dd = static_cast<double>(Dm), ff = static_cast<double>(FF);
+
+  // 1. Recompute the gate inputs of all shards at once: [a | b] = X [w1_s ; w3_s]^T,
+  //    w13 read as one [2*ffn, d] matrix whose rows are ordered (shard, w1|w3, c).
+  CUtensorMap mx_k, mw13_k, mab;
+  if ((st = make_map_3d(&mx_k, true, x_shards, Dm, R, 1, Dm * 2, R * Dm * 2, 64, 128, 1, "x_shards")) != DG_OK) return st;
+  if ((st = make_map_3d(&mw13_k, true, w13, Dm, F2, 1, Dm * 2, F2 * Dm * 2, 64, kKMajorBRows, 1, "w13")) != DG_OK)
+    return st;
+  if ((st = make_map_3d(&mab, true, ab, F2, R, 1, F2 * 2, R * F2 * 2, 64, 32, 1, "[a|b]")) != DG_OK) return st;
+  GemmParams p{};
+  p.G = 1;
+  p.M = static_cast<int32_t>(R);
+  p.N = static_cast<int32_t>(F2);
+  p.K = static_cast<int32_t>(d);
+  p.a_g = p.b_g = p.d_g = G_OUTER;
+  if ((st = run_gemm(GV_BF16_KK_STORE, mx_k, mw13_k, mab, mab, p, dev, s, "tp_bwd_ab",
+                     2.0 * (r * dd + 2.0 * ff * dd + 2.0 * r * ff))) != DG_OK)
+    return st;
+
+  // 2. dh = dY w2 (w2 [d, ffn] read N-major: the gradient of y = h w2^T w.r.t. h).
+  CUtensorMap mdy_k, mw2_n, mdh;
+  if ((st = make_map_3d(&mdy_k, true, dy_shards, Dm, R, 1, Dm * 2, R * Dm * 2, 64, 128, 1, "dy_shards")) != DG_OK)
+    return st;
+  if ((st = make_map_3d(&mw2_n, true, w2, FF, Dm, 1, FF * 2, Dm * FF * 2, 64, 64, 1, "w2 (N-major)")) != DG_OK) return st;
+  if ((st = make_map_3d(&mdh, true, dh, FF, R, 1, FF * 2, R * FF * 2, 64, 32, 1, "dh")) != DG_OK) return st;
+  p = GemmParams{};
+  p.G = 1;
+  p.M = static_cast<int32_t>(R);
+  p.N = static_cast<int32_t>(ffn);
+  p.K = static_cast<int32_t>(d);
+  p.a_g = p.b_g = p.d_g = G_OUTER;
+  if ((st = run_gemm(GV_BF16_KM_STORE, mdy_k, mw2_n, mdh, mdh, p, dev, s, "tp_bwd_dh",
+                     2.0 * (r * dd + ff * dd + r * ff))) != DG_OK)
+    return st;
+
+  // 3. Gate backward, in place: [a|b] -> [da|db], dh -> h.
+  {
+    TraceScope trace("tp_bwd_gate", s, 0.0, 12.0 * r * ff);
+    cudaError_t e = launch_swiglu_gate_bwd(ab, dh, rows, W, static_cast<int>(F), dev, s);
+    if (e != cudaSuccess) return cuda_fail(e, "tp_bwd_gate launch");
+  }
+
+  // 4. d_w2 = dY^T h: [d, ffn], contraction over the gathered rows.
+  CUtensorMap mdy_t, mh_n, mdw2;
+  if ((st = make_map_3d(&mdy_t, true, dy_shards, Dm, R, 1, Dm * 2, R * Dm * 2, 64, 64, 1, "dy^T")) != DG_OK) return st;
+  if ((st = make_map_3d(&mh_n, true, dh, FF, R, 1, FF * 2, R * FF * 2, 64, 64, 1, "h (N-major)")) != DG_OK) return st;
+  if ((st = make_map_3d(&mdw2, true, d_w2, FF, Dm, 1, FF * 2, Dm * FF * 2, 64, 32, 1, "d_w2")) != DG_OK) return st;
+  p = GemmParams{};
+  p.G = 1;
+  p.M = static_cast<int32_t>(d);
+  p.N = static_cast<int32_t>(ffn);
+  p.K = static_cast<int32_t>(R);
+  p.a_g = p.b_g = p.d_g = G_OUTER;
+  if ((st = run_gemm(GV_BF16_MM_STORE, mdy_t, mh_n, mdw2, mdw2, p, dev, s, "tp_bwd_dw2",
+                     2.0 * (r * dd + r * ff + dd * ff))) != DG_OK)
+    return st;
+
+  // 5. dX = [da|db] [w1_s ; w3_s] over all shards at once: one product with
+  //    K = 2*ffn, so the shard sum (the row-parallel reduction) is the K loop.
+  CUtensorMap mdab_k, mw13_n, mdx;
+  if ((st = make_map_3d(&mdab_k, true, ab, F2, R, 1, F2 * 2, R * F2 * 2, 64, 128, 1, "[da|db]")) != DG_OK) return st;
+  if ((st = make_map_3d(&mw13_n, true, w13, Dm, F2, 1, Dm * 2, F2 * Dm * 2, 64, 64, 1, "w13 (N-major)")) != DG_OK)
+    return st;
+  if ((st = make_map_3d(&mdx, true, dx_shards, Dm, R, 1, Dm * 2, R * Dm * 2, 64, 32, 1, "dx_shards")) != DG_OK) return st;
+  p = GemmParams{};
+  p.G = 1;
+  p.M = static_cast<int32_t>(R);
+  p.N = static_cast<int32_t>(d);
+  p.K = static_cast<int32_t>(F2);
+  p.a_g = p.b_g = p.d_g = G_OUTER;
+  if ((st = run_gemm(GV_BF16_KM_STORE, mdab_k, mw13_n, mdx, mdx, p, dev, s, "tp_bwd_dx",
+                     2.0 * (2.0 * r * ff + 2.0 * ff * dd + r * dd))) != DG_OK)
+    return st;
+
+  // 6. d_w13 = [da|db]^T X: [2*ffn, d] in w13's own row order.
+  CUtensorMap mdab_t, mx_n, mdw13;
+  if ((st = make_map_3d(&mdab_t, true, ab, F2, R, 1, F2 * 2, R * F2 * 2, 64, 64, 1, "[da|db]^T")) != DG_OK) return st;
+  if ((st = make_map_3d(&mx_n, true, x_shards, Dm, R, 1, Dm * 2, R * Dm * 2, 64, 64, 1, "x (N-major)")) != DG_OK) return st;
+  if ((st = make_map_3d(&mdw13, true, d_w13, Dm, F2, 1, Dm * 2, F2 * Dm * 2, 64, 32, 1, "d_w13")) != DG_OK) return st;
+  p = GemmParams{};
+  p.G = 1;
+  p.M = static_cast<int32_t>(F2);
+  p.N = static_cast<int32_t>(d);
+  p.K = static_cast<int32_t>(R);
+  p.a_g = p.b_g = p.d_g = G_OUTER;
+  return run_gemm(GV_BF16_MM_STORE, mdab_t, mx_n, mdw13, mdw13, p, dev, s, "tp_bwd_dw13",
+                  2.0 * (2.0 * r * ff + r * dd + 2.0 * ff * dd));
 }
 
 dg_status dg_trace_begin(void) {

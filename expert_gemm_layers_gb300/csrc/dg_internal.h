@@ -36,7 +36,8 @@ enum GemmVariant : int {
   GV_BF16_KM_BIAS = 2,  // bf16, A K-major, B MN-major, bias epilogue
   GV_BF16_MM_STORE = 3, // bf16, A and B MN-major, plain store
   GV_BF16_KK_SWIGLU = 4, // bf16, A and B K-major, paired silu(a)*b epilogue
-  GV_BF16_KM_LNSTATS = 5 // bf16, A K-major, B MN-major, bias + per-tile LayerNorm statistics
+  GV_BF16_KM_LNSTATS = 5, // bf16, A K-major, B MN-major, bias + per-tile LayerNorm statistics
+  GV_BF16_KM_STORE = 6    // bf16, A K-major, B MN-major, plain store
 };
 
 // Tiles along N of one problem for this variant (output columns per tile).
@@ -78,6 +79,8 @@ cudaError_t launch_gemm_bf16_kk_swiglu(const CUtensorMap&, const CUtensorMap&, c
                                        const CUtensorMap&, const GemmParams&, int num_sms, cudaStream_t);
 cudaError_t launch_gemm_bf16_km_lnstats(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
                                         const CUtensorMap&, const GemmParams&, int num_sms, cudaStream_t);
+cudaError_t launch_gemm_bf16_km_store(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
+                                      const CUtensorMap&, const GemmParams&, int num_sms, cudaStream_t);
 
 // The GEMMs run as CTA pairs (cta_group::2, 256-row tiles, clusters of 2).
 constexpr bool kUsePairs = true;
@@ -167,6 +170,11 @@ cudaError_t launch_grad_reduce(const float* part, void* d_b1, void* d_nx_w, void
 // out[g, c] = sum_n src[g*g_stride + n*row_stride + c] (bf16 in, fp32 sum, bf16 out [G, ncols]).
 cudaError_t launch_column_sum(const void* src, void* out, int G, int rows, int ncols, int64_t g_stride,
                               int64_t row_stride, const DeviceInfo& dev, cudaStream_t s);
+
+// Backward of the SwiGLU gate, in place: ab [rows, W, 2F] holds (a_s | b_s)
+// and becomes (da_s | db_s); dh [rows, W*F] becomes h = silu(a)*b.
+cudaError_t launch_swiglu_gate_bwd(void* ab, void* dh_h, int64_t rows, int W, int F, const DeviceInfo& dev,
+                                   cudaStream_t s);
 
 // Row permutations of the exchange (16-byte vector copies).
 cudaError_t launch_dispatch(const void* in, void* out, int P, int B, int T, int D, const DeviceInfo& dev,

@@ -438,6 +438,48 @@ __global__ void column_sum_kernel(const __nv_bfloat16* __restrict__ src, __nv_bf
   *reinterpret_cast<uint32_t*>(out + static_cast<int64_t>(g) * ncols + c) = pack_bf16x2(s0, s1);
 }
 
+// Backward of the SwiGLU gate h = silu(a) * b for the column-parallel pair:
+// with sig = sigmoid(a),  da = dh * b * (sig + a*sig*(1 - sig)),  db = dh * a * sig,
+// and h itself (needed for w2's gradient).  In place: (a, b) -> (da, db),
+// dh -> h; 8 columns per thread.
+__global__ void swiglu_gate_bwd_kernel(__nv_bfloat16* __restrict__ ab, __nv_bfloat16* __restrict__ dh_h, int64_t rows,
+                                       int W, int F, const uint32_t* err) {
+  if (ld_volatile_u32(err) != 0u) return;
+  const int fv = F / 8;
+  const int64_t total = rows * W * fv;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t n = i / (static_cast<int64_t>(W) * fv);
+    const int rem = static_cast<int>(i - n * W * fv);
+    const int sh = rem / fv, c = 8 * (rem - sh * fv);
+    __nv_bfloat16* pa = ab + (n * W + sh) * 2 * static_cast<int64_t>(F) + c;
+    __nv_bfloat16* pb = pa + F;
+    __nv_bfloat16* ph = dh_h + (n * W + sh) * static_cast<int64_t>(F) + c;
+    const uint4 va = *reinterpret_cast<const uint4*>(pa), vb = *reinterpret_cast<const uint4*>(pb);
+    const uint4 vh = *reinterpret_cast<const uint4*>(ph);
+    const uint32_t aw[4] = {va.x, va.y, va.z, va.w}, bw[4] = {vb.x, vb.y, vb.z, vb.w};
+    const uint32_t hw[4] = {vh.x, vh.y, vh.z, vh.w};
+    uint32_t oa[4], ob[4], oh[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 a = unpack_bf16x2(aw[e]), b = unpack_bf16x2(bw[e]), d = unpack_bf16x2(hw[e]);
+      const float2 half_a = mul2(a, splat2(0.5f));
+      const float2 sig = fma2(make_float2(tanh_fast(half_a.x), tanh_fast(half_a.y)), splat2(0.5f), splat2(0.5f));
+      const float2 as = mul2(a, sig);                                         // silu(a)
+      const float2 dsil = fma2(as, fma2(sig, splat2(-1.0f), splat2(1.0f)), sig);  // silu'(a)
+      const float2 da = mul2(mul2(d, b), dsil);
+      const float2 db = mul2(d, as);
+      const float2 h = mul2(as, b);
+      oa[e] = pack_bf16x2(da.x, da.y);
+      ob[e] = pack_bf16x2(db.x, db.y);
+      oh[e] = pack_bf16x2(h.x, h.y);
+    }
+    *reinterpret_cast<uint4*>(pa) = make_uint4(oa[0], oa[1], oa[2], oa[3]);
+    *reinterpret_cast<uint4*>(pb) = make_uint4(ob[0], ob[1], ob[2], ob[3]);
+    *reinterpret_cast<uint4*>(ph) = make_uint4(oh[0], oh[1], oh[2], oh[3]);
+  }
+}
+
 // Exchange permutations, 16 bytes per thread.
 __global__ void dispatch_kernel(const uint4* __restrict__ in, uint4* __restrict__ out, int P, int B, int T,
                                 int vec_per_row, const uint32_t* err) {
@@ -597,6 +639,16 @@ cudaError_t launch_column_sum(const void* src, void* out, int G, int rows, int n
   dim3 grid((ncols / 2 + threads - 1) / threads, G);
   column_sum_kernel<<<grid, threads, 0, s>>>(static_cast<const __nv_bfloat16*>(src), static_cast<__nv_bfloat16*>(out),
                                             rows, ncols, g_stride, row_stride, dev.err);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_swiglu_gate_bwd(void* ab, void* dh_h, int64_t rows, int W, int F, const DeviceInfo& dev,
+                                   cudaStream_t s) {
+  const int64_t total = rows * W * (F / 8);
+  int64_t blocks = (total + 255) / 256;
+  if (blocks > 16 * dev.num_sms) blocks = 16 * dev.num_sms;
+  swiglu_gate_bwd_kernel<<<static_cast<int>(blocks), 256, 0, s>>>(static_cast<__nv_bfloat16*>(ab),
+                                                                  static_cast<__nv_bfloat16*>(dh_h), rows, W, F, dev.err);
   return cudaGetLastError();
 }
 

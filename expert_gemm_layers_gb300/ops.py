@@ -14,7 +14,8 @@ from ._lib import FFNShape, TraceEntry, check, load
 
 __all__ = [
     "gemm_fp8", "ffn_shape", "a2a_ffn_forward", "a2a_ffn_backward", "A2AFFN", "a2a_ffn",
-    "a2a_dispatch", "a2a_combine", "tp_swiglu", "device_status", "debug_wait_timeout",
+    "a2a_dispatch", "a2a_combine", "tp_swiglu", "tp_swiglu_backward", "TPSwiGLU", "tp_swiglu_layer",
+    "device_status", "debug_wait_timeout",
     "FFN_PARAM_NAMES", "trace_begin", "trace_end",
 ]
 
@@ -211,6 +212,53 @@ def tp_swiglu(x_shards: torch.Tensor, w13: torch.Tensor, w2: torch.Tensor,
         check(lib.dg_tp_swiglu(S, d, ffn, W, bsz, _ptr(x_shards), _ptr(w13), _ptr(w2), _ptr(out),
                                _ptr(workspace), workspace.numel(), ctypes.c_void_p(_stream(dev))))
     return out
+
+
+def tp_swiglu_backward(x_shards: torch.Tensor, w13: torch.Tensor, w2: torch.Tensor, dy_shards: torch.Tensor,
+                       workspace: torch.Tensor | None = None, grads: dict | None = None) -> dict:
+    """Gradients of tp_swiglu given dy_shards (layout of y_shards): dict with
+    "x" (like x_shards), "w13" [W, 2F, d] and "w2" [d, W*F]."""
+    lib = load()
+    squeeze = x_shards.dim() == 3
+    xs = x_shards.unsqueeze(1) if squeeze else x_shards
+    W, bsz, sl, d = xs.shape
+    ffn = w2.shape[1]
+    dev = x_shards.device
+    _need(x_shards, "x_shards", torch.bfloat16)
+    _need(w13, "w13", torch.bfloat16, (W, 2 * (ffn // W), d), dev)
+    _need(w2, "w2", torch.bfloat16, (d, ffn), dev)
+    _need(dy_shards, "dy_shards", torch.bfloat16, tuple(x_shards.shape), dev)
+    S = W * sl
+    wsb = lib.dg_tp_swiglu_bwd_workspace_bytes(S, d, ffn, W, bsz)
+    if workspace is None:
+        workspace = torch.empty(max(wsb, 1), dtype=torch.uint8, device=dev)
+    if grads is None:
+        grads = dict(x=torch.empty_like(x_shards), w13=torch.empty_like(w13), w2=torch.empty_like(w2))
+    with torch.cuda.device(dev):
+        check(lib.dg_tp_swiglu_bwd(S, d, ffn, W, bsz, _ptr(x_shards), _ptr(w13), _ptr(w2), _ptr(dy_shards),
+                                   _ptr(grads["x"]), _ptr(grads["w13"]), _ptr(grads["w2"]), _ptr(workspace),
+                                   workspace.numel(), ctypes.c_void_p(_stream(dev))))
+    return grads
+
+
+class TPSwiGLU(torch.autograd.Function):
+    """Autograd wrapper of the SwiGLU pair; the backward recomputes [a|b] from x."""
+
+    @staticmethod
+    def forward(ctx, x_shards, w13, w2):
+        ctx.save_for_backward(x_shards, w13, w2)
+        return tp_swiglu(x_shards, w13, w2)
+
+    @staticmethod
+    def backward(ctx, dy):
+        x_shards, w13, w2 = ctx.saved_tensors
+        g = tp_swiglu_backward(x_shards, w13, w2, dy.contiguous())
+        return g["x"], g["w13"], g["w2"]
+
+
+def tp_swiglu_layer(x_shards, w13, w2):
+    """Differentiable SwiGLU pair (see TPSwiGLU)."""
+    return TPSwiGLU.apply(x_shards, w13, w2)
 
 
 # ------------------------------------------------------------------ diagnostics

@@ -179,6 +179,37 @@ dg_status dg_tp_swiglu(int64_t S, int64_t d, int64_t ffn, int32_t W, int32_t bsz
                        void* y_shards, void* ws, size_t ws_bytes, void* stream);
 
 /*
+ * dg_tp_swiglu_bwd: gradients of the SwiGLU pair above with respect to the
+ * gathered input and both weights, given dY = dL/dy.
+ *
+ * Source: "Add dist GEMM attention and FFN backend" (torchtitan PR #4044),
+ * section "Structure": the backward of the column-parallel pair is one
+ * product over the concatenated [w1_s ; w3_s] rows of every shard, so its
+ * input gradient (the row-parallel reduction across shards) is a single K
+ * loop.  With a = X w1_s^T, b = X w3_s^T, h = silu(a) * b and
+ * sig = sigmoid(a):
+ *   dh_s   = dY w2_s                 da = dh * b * (sig + a*sig*(1-sig))
+ *   d_w2_s = dY^T h_s                db = dh * a * sig
+ *   d_w13_s = [da | db]^T X          dX = sum_s [da | db] [w1_s ; w3_s]
+ * a and b are recomputed from X (nothing from the forward is kept).
+ *
+ *   x_shards, w13, w2   as for dg_tp_swiglu (inputs)
+ *   dy_shards [W, bsz, S/W, d]   dL/dy, same layout as y_shards (input)
+ *   dx_shards [W, bsz, S/W, d]   dL/dx (output, overwritten)
+ *   d_w13     [W, 2*ffn/W, d]    dL/dw13 in w13's layout (output, overwritten)
+ *   d_w2      [d, ffn]           dL/dw2 (output, overwritten)
+ * Scratch: [a|b] [rows, 2*ffn] and dh [rows, ffn] bf16 in `ws`
+ * (dg_tp_swiglu_bwd_workspace_bytes); no written buffer may overlap any other.
+ * Requirements and errors are those of dg_tp_swiglu.
+ */
+size_t dg_tp_swiglu_bwd_workspace_bytes(int64_t S, int64_t d, int64_t ffn, int32_t W, int32_t bsz);
+
+dg_status dg_tp_swiglu_bwd(int64_t S, int64_t d, int64_t ffn, int32_t W, int32_t bsz,
+                           const void* x_shards, const void* w13, const void* w2,
+                           const void* dy_shards, void* dx_shards, void* d_w13, void* d_w2,
+                           void* ws, size_t ws_bytes, void* stream);
+
+/*
  * dg_tp_swiglu_noalloc: the same SwiGLU pair as dg_tp_swiglu, for callers
  * that cannot allocate device memory -- for example code that runs under a
  * framework which owns the device's memory pool and accounts for every

@@ -55,3 +55,64 @@ def test_full_size_row_subset():
     ref = O.tp_swiglu_rows(synth.bits(x), synth.bits(w13), synth.bits(w2), W, rows)
     got = y.reshape(-1, d)[torch.from_numpy(rows).to(DEV)]
     assert_close(got, ref, TOL_BF16, "tp_swiglu full size (64 rows)")
+
+
+# ------------------------------------------------------------------ backward
+
+def _grads_vs_oracle(x, w13, w2, dy, W, what):
+    from expert_gemm_layers_gb300 import tp_swiglu_backward
+    g = tp_swiglu_backward(x.to(DEV), w13.to(DEV), w2.to(DEV), dy.to(DEV))
+    torch.cuda.synchronize()
+    ref = O.tp_swiglu_backward(synth.bits(x), synth.bits(w13), synth.bits(w2), synth.bits(dy), W=W)
+    assert_close(g["x"], ref["dx"], TOL_BF16, f"{what} dx")
+    assert_close(g["w13"], ref["dw13"], TOL_BF16, f"{what} dw13")
+    assert_close(g["w2"], ref["dw2"], TOL_BF16, f"{what} dw2")
+
+
+@pytest.mark.parametrize("S,d,ffn,W,bsz", [
+    (256, 128, 512, 2, 1),
+    (8 * 40, 136, 8 * 72, 8, 1),  # ragged rows (K of the weight GEMMs), d and F off the tile grid
+    (512, 256, 1024, 4, 2),
+    (128, 64, 128, 1, 1),
+    (8, 8, 16, 2, 1),             # far below one tile in every dimension
+])
+def test_backward_small_full(S, d, ffn, W, bsz):
+    x, w13, w2 = synth.tp_swiglu_inputs(S, d, ffn, W, bsz=bsz, seed=S + d + 1)
+    dy = synth.tp_swiglu_inputs(S, d, ffn, W, bsz=bsz, seed=S + d + 2)[0]
+    _grads_vs_oracle(x, w13, w2, dy, W, f"tp_swiglu_bwd {S,d,ffn,W,bsz}")
+
+
+def test_backward_autograd_matches_direct_call():
+    from expert_gemm_layers_gb300 import tp_swiglu_backward, tp_swiglu_layer
+    S, d, ffn, W = 256, 128, 512, 4
+    x, w13, w2 = synth.tp_swiglu_inputs(S, d, ffn, W, seed=11, device=DEV)
+    dy = synth.tp_swiglu_inputs(S, d, ffn, W, seed=12, device=DEV)[0]
+    xr, w13r, w2r = (t.clone().requires_grad_(True) for t in (x, w13, w2))
+    y = tp_swiglu_layer(xr, w13r, w2r)
+    assert torch.equal(y.detach(), tp_swiglu(x, w13, w2))
+    y.backward(dy)
+    g = tp_swiglu_backward(x, w13, w2, dy)
+    assert torch.equal(xr.grad, g["x"]) and torch.equal(w13r.grad, g["w13"]) and torch.equal(w2r.grad, g["w2"])
+
+
+def test_backward_full_size_subsets():
+    # Llama-3-8B FFN shape over W=8 shards: 64 rows of dx and 16 ffn columns of every weight gradient
+    S, d, ffn, W = 8192, 4096, 14336, 8
+    F = ffn // W
+    from expert_gemm_layers_gb300 import tp_swiglu_backward
+    x, w13, w2 = synth.tp_swiglu_inputs(S, d, ffn, W, seed=7, device=DEV)
+    dy = synth.tp_swiglu_inputs(S, d, ffn, W, seed=8, device=DEV)[0]
+    g = tp_swiglu_backward(x, w13, w2, dy)
+    torch.cuda.synchronize()
+    xb, w13b, w2b, dyb = synth.bits(x), synth.bits(w13), synth.bits(w2), synth.bits(dy)
+    rng = np.random.default_rng(8)
+    rows = rng.choice(S, size=64, replace=False)
+    ref = O.tp_swiglu_backward_rows(xb, w13b, w2b, dyb, W, rows)
+    assert_close(g["x"].reshape(-1, d)[torch.from_numpy(rows).to(DEV)], ref, TOL_BF16, "dx (64 rows)")
+    cols = np.sort(np.concatenate([rng.choice(ffn, size=14, replace=False), [0, ffn - 1]]))
+    ref = O.tp_swiglu_backward_weight_cols(xb, w13b, w2b, dyb, W, cols)
+    c = torch.from_numpy(cols).to(DEV)
+    s_idx, c_idx = torch.from_numpy(cols // F).to(DEV), torch.from_numpy(cols % F).to(DEV)
+    assert_close(g["w2"][:, c], ref["dw2"], TOL_BF16, "dw2 (16 columns)")
+    assert_close(g["w13"][s_idx, c_idx], ref["dw1"], TOL_BF16, "dw1 (16 rows)")
+    assert_close(g["w13"][s_idx, F + c_idx], ref["dw3"], TOL_BF16, "dw3 (16 rows)")
