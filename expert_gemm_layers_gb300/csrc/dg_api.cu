@@ -166,7 +166,7 @@ dg_status make_map_3d(CUtensorMap* map, bool is_bf16, const void* base, uint64_t
 
 int gemm_tile_m() { return kUsePairs ? 256 : 128; }
 
-int gemm_tile_n(GemmVariant v) { return v == GV_BF16_KK_SWIGLU ? 128 : 256; }
+int gemm_tile_n(GemmVariant v) { return v == GV_BF16_KK_SWIGLU ? 128 : v == GV_FP8_KK_N224 ? 224 : 256; }
 
 dg_status run_gemm(GemmVariant v, const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& d,
                    const CUtensorMap& c, GemmParams p, const DeviceInfo& dev, cudaStream_t s, const char* name,
@@ -189,6 +189,7 @@ dg_status run_gemm(GemmVariant v, const CUtensorMap& a, const CUtensorMap& b, co
     case GV_BF16_KK_SWIGLU: e = launch_gemm_bf16_kk_swiglu(a, b, d, c, p, grid, s); break;
     case GV_BF16_KM_LNSTATS: e = launch_gemm_bf16_km_lnstats(a, b, d, c, p, grid, s); break;
     case GV_BF16_KM_STORE: e = launch_gemm_bf16_km_store(a, b, d, c, p, grid, s); break;
+    case GV_FP8_KK_N224: e = launch_gemm_fp8_kk_n224(a, b, d, c, p, grid, s); break;
     default: return fail(DG_ERR_UNSUPPORTED, "unknown GEMM variant");
   }
   if (e != cudaSuccess) return cuda_fail(e, "GEMM launch");
@@ -332,6 +333,19 @@ dg_status dg_gemm_fp8(int64_t M, int64_t N, int64_t K, const void* A, const void
   DeviceInfo dev;
   dg_status st = device_info(&dev);
   if (st != DG_OK) return st;
+  // Tile width: 224 columns where that needs fewer (wave x width) column
+  // steps than 256 across the co-resident CTA pairs (e.g. 4096 x 4096:
+  // 304 tiles = 4 full waves of 76 pairs instead of 256 tiles = 3.4 waves).
+  int units = 0;
+  cudaError_t ce = gemm_fp8_units(dev.num_sms, &units);
+  if (ce != cudaSuccess) return cuda_fail(ce, "gemm_fp8: occupancy query");
+  const int64_t tiles_m = (M + gemm_tile_m() - 1) / gemm_tile_m();
+  auto wave_cost = [&](int64_t bn) {
+    const int64_t tiles = tiles_m * ((N + bn - 1) / bn);
+    return ((tiles + units - 1) / units) * bn;
+  };
+  const GemmVariant v = wave_cost(224) < wave_cost(256) ? GV_FP8_KK_N224 : GV_FP8_KK;
+  const uint32_t b_rows = static_cast<uint32_t>(gemm_tile_n(v) / (kUsePairs ? 2 : 1));
   CUtensorMap ma, mb, md, mc;
   // K == 0: the maps still need a valid (non-empty) tensor; the kernel loads nothing.
   const uint64_t kd = K > 0 ? static_cast<uint64_t>(K) : 16u;
@@ -339,7 +353,7 @@ dg_status dg_gemm_fp8(int64_t M, int64_t N, int64_t K, const void* A, const void
   const void* b_ptr = K > 0 ? B : D;
   const uint64_t am = K > 0 ? static_cast<uint64_t>(M) : 1u, bn = K > 0 ? static_cast<uint64_t>(N) : 1u;
   if ((st = make_map_3d(&ma, false, a_ptr, kd, am, 1, kd, kd * am, 128, 128, 1, "A")) != DG_OK) return st;
-  if ((st = make_map_3d(&mb, false, b_ptr, kd, bn, 1, kd, kd * bn, 128, kKMajorBRows, 1, "B")) != DG_OK) return st;
+  if ((st = make_map_3d(&mb, false, b_ptr, kd, bn, 1, kd, kd * bn, 128, b_rows, 1, "B")) != DG_OK) return st;
   if ((st = make_map_3d(&md, true, D, N, M, 1, N * 2, N * 2 * M, 64, 32, 1, "D")) != DG_OK) return st;
   if (has_c) {
     if ((st = make_map_3d(&mc, true, C, N, M, 1, N * 2, N * 2 * M, 64, 32, 1, "C")) != DG_OK) return st;
@@ -355,8 +369,11 @@ dg_status dg_gemm_fp8(int64_t M, int64_t N, int64_t K, const void* A, const void
   p.alpha = alpha;
   p.beta = beta;
   p.has_c = has_c ? 1 : 0;
+  p.c_ptr = static_cast<const __nv_bfloat16*>(has_c ? C : D);
+  p.d_ptr = static_cast<__nv_bfloat16*>(D);
   const double bytes = static_cast<double>(M) * K + static_cast<double>(N) * K + (has_c ? 2.0 : 1.0) * 2.0 * M * N;
-  return run_gemm(GV_FP8_KK, ma, mb, md, mc, p, dev, static_cast<cudaStream_t>(stream), "gemm_fp8", bytes);
+  return run_gemm(v, ma, mb, md, mc, p, dev, static_cast<cudaStream_t>(stream),
+                  v == GV_FP8_KK_N224 ? "gemm_fp8_n224" : "gemm_fp8", bytes);
 }
 
 // ------------------------------------------------------------------ A2A FFN

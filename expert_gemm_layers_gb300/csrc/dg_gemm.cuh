@@ -56,6 +56,8 @@ struct GemmParams {
   float4* ln_part;           // EPI_BIAS_LNSTATS: [G][tiles_n][M] (mean_u, M2_u, mean_g, M2_g) per tile
   int32_t ln_H;              // EPI_BIAS_LNSTATS: columns [0, ln_H) are U, [ln_H, N) are G
   uint32_t* err;             // device error word
+  const __nv_bfloat16* c_ptr; // narrow tiles: C and D as row-major [G][M][N] for the last 32-column chunk
+  __nv_bfloat16* d_ptr;
 };
 
 // Running (count, mean, M2) of a set of values; merge() is the pairwise
@@ -91,12 +93,13 @@ static __device__ __forceinline__ void chunk_mean_m2(const float (&v)[K], int lo
   m2 = q;
 }
 
-template <bool kFp8, bool kAMN, bool kBMN, int kEpi, bool kPair>
+template <bool kFp8, bool kAMN, bool kBMN, int kEpi, bool kPair, int kBN = 256>
 struct GemmCfg {
   static constexpr int CTAS = kPair ? 2 : 1;          // CTAs sharing one UMMA (cta_group)
   static constexpr int BM = 128;                      // rows per CTA (one TMEM lane per row)
   static constexpr int UMMA_M = BM * CTAS;            // rows per MMA tile
-  static constexpr int BN = 256;                      // UMMA N = accumulator columns
+  static constexpr int BN = kBN;                      // UMMA N = accumulator columns
+  static constexpr int ACC_STRIDE = 256;              // TMEM columns between the two accumulators
   static constexpr int BN_OUT = (kEpi == EPI_SWIGLU) ? BN / 2 : BN;
   static constexpr int B_ROWS = BN / CTAS;            // B rows each CTA stages per K-block
   static constexpr int ROW_BYTES = 128;               // K-block = one 128-byte swizzle row
@@ -112,7 +115,8 @@ struct GemmCfg {
   static constexpr int EPI_BYTES = EPI_WARPS * 2 * EPI_BUF_BYTES;
   static constexpr int NUM_THREADS = 64 + EPI_WARPS * 32;
   static constexpr int NACC = 2;                      // TMEM accumulators (double buffered)
-  static constexpr uint32_t TMEM_COLS = NACC * BN;
+  static constexpr uint32_t TMEM_COLS = NACC * ACC_STRIDE;
+  static constexpr bool HALF_CHUNK = (BN_OUT % 64) == 32;  // a last 32-column chunk per tile
   static constexpr int NUM_BARS = 2 * STAGES + 4 + 2 * EPI_WARPS + 1;
   static constexpr int BAR_BYTES = 256;
   static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + EPI_BYTES + BAR_BYTES;
@@ -120,6 +124,8 @@ struct GemmCfg {
   static_assert(NUM_BARS * 8 + 4 <= BAR_BYTES, "barrier area");
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
   static_assert(!(kFp8 && (kAMN || kBMN)), "e4m3 operands are K-major here");
+  static_assert(kBN <= ACC_STRIDE && kBN % 32 == 0 && (kBN / CTAS) % 8 == 0, "tile width");
+  static_assert(kBN == 256 || kEpi == EPI_FP8, "narrow tiles: the alpha/beta/C epilogue only");
 };
 
 static __device__ __forceinline__ void tma_load_op(void* dst, const CUtensorMap* map, uint64_t* bar, int32_t x,
@@ -157,12 +163,12 @@ static __device__ __forceinline__ void tile_coords(const GemmParams& p, int rem,
   }
 }
 
-template <bool kFp8, bool kAMN, bool kBMN, int kEpi, bool kPair>
-__global__ void __launch_bounds__(GemmCfg<kFp8, kAMN, kBMN, kEpi, kPair>::NUM_THREADS, 1)
+template <bool kFp8, bool kAMN, bool kBMN, int kEpi, bool kPair, int kBN>
+__global__ void __launch_bounds__(GemmCfg<kFp8, kAMN, kBMN, kEpi, kPair, kBN>::NUM_THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmD, const __grid_constant__ CUtensorMap tmC,
                    const GemmParams p) {
-  using Cfg = GemmCfg<kFp8, kAMN, kBMN, kEpi, kPair>;
+  using Cfg = GemmCfg<kFp8, kAMN, kBMN, kEpi, kPair, kBN>;
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint32_t s_abort;
 
@@ -334,7 +340,7 @@ __global__ void __launch_bounds__(GemmCfg<kFp8, kAMN, kBMN, kEpi, kPair>::NUM_TH
         }
         tphase ^= 1u << acc;
         tc_fence_after_sync();
-        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * Cfg::BN);
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * Cfg::ACC_STRIDE);
         for (int kb = 0; kb < num_kb; ++kb) {
           if (!mbar_wait(&full[stage], phase, p.err, SITE_FULL)) {
             ok = false;
@@ -445,7 +451,7 @@ __global__ void __launch_bounds__(GemmCfg<kFp8, kAMN, kBMN, kEpi, kPair>::NUM_TH
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
             uint32_t ra[32], rb[32];
-            const uint32_t col = static_cast<uint32_t>(acc * Cfg::BN + 64 * j + 32 * h);
+            const uint32_t col = static_cast<uint32_t>(acc * Cfg::ACC_STRIDE + 64 * j + 32 * h);
             tmem_ld_32x32b_x32(lane_addr + col, ra);
             tmem_ld_32x32b_x32(lane_addr + col + Cfg::BN / 2, rb);
             tmem_ld_wait();
@@ -455,7 +461,7 @@ __global__ void __launch_bounds__(GemmCfg<kFp8, kAMN, kBMN, kEpi, kPair>::NUM_TH
           }
         } else {
           uint32_t r0[32], r1[32];
-          const uint32_t col = static_cast<uint32_t>(acc * Cfg::BN + 64 * j);
+          const uint32_t col = static_cast<uint32_t>(acc * Cfg::ACC_STRIDE + 64 * j);
           tmem_ld_32x32b_x32(lane_addr + col, r0);
           tmem_ld_32x32b_x32(lane_addr + col + 32, r1);
           tmem_ld_wait();
@@ -560,6 +566,42 @@ __global__ void __launch_bounds__(GemmCfg<kFp8, kAMN, kBMN, kEpi, kPair>::NUM_TH
         }
       }
       if (!ok) break;
+      if (Cfg::HALF_CHUNK) {
+        // Columns [BN_OUT - 32, BN_OUT) of the tile: one 32-column TMEM load,
+        // then plain 16-byte global loads/stores per row (a 64-wide TMA box
+        // would reach into the next tile's columns).
+        const int c0 = n0 + Cfg::BN_OUT - 32;
+        if (row0 < p.M && c0 < p.N) {
+          uint32_t r0[32];
+          tmem_ld_32x32b_x32(lane_addr + static_cast<uint32_t>(acc * Cfg::ACC_STRIDE + Cfg::BN_OUT - 32), r0);
+          tmem_ld_wait();
+          const int row = row0 + lane;
+          if (row < p.M) {
+            const int64_t off = (static_cast<int64_t>(g) * p.M + row) * p.N + c0;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              if (c0 + 8 * q < p.N) {
+                float v[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) v[i] = num_kb == 0 ? 0.0f : p.alpha * __uint_as_float(r0[8 * q + i]);
+                if (use_c) {
+                  const uint4 cv = __ldg(reinterpret_cast<const uint4*>(p.c_ptr + off + 8 * q));
+                  const uint32_t cw[4] = {cv.x, cv.y, cv.z, cv.w};
+#pragma unroll
+                  for (int e = 0; e < 4; ++e) {
+                    const float2 c2 = unpack_bf16x2(cw[e]);
+                    v[2 * e] = fmaf(p.beta, c2.x, v[2 * e]);
+                    v[2 * e + 1] = fmaf(p.beta, c2.y, v[2 * e + 1]);
+                  }
+                }
+                *reinterpret_cast<uint4*>(p.d_ptr + off + 8 * q) =
+                    make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]), pack_bf16x2(v[4], v[5]),
+                               pack_bf16x2(v[6], v[7]));
+              }
+            }
+          }
+        }
+      }
       if (kEpi == EPI_BIAS_LNSTATS && nchunks > 0 && row0 + lane < p.M) {
         p.ln_part[(static_cast<int64_t>(g) * p.tiles_n + nt) * p.M + row0 + lane] =
             make_float4(st_u.mean, st_u.m2, st_g.mean, st_g.m2);

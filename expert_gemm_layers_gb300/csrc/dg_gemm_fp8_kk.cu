@@ -8,4 +8,8 @@ cudaError_t launch_gemm_fp8_kk(const CUtensorMap& a, const CUtensorMap& b, const
   return launch_gemm_t<true, false, false, EPI_FP8>(a, b, d, c, p, num_sms, s);
 }
 
+cudaError_t gemm_fp8_units(int num_sms, int* units) {
+  return gemm_units_t<true, false, false, EPI_FP8>(num_sms, units);
+}
+
 }  // namespace dg

@@ -1,0 +1,12 @@
+// Instantiation unit of the tcgen05 GEMM: e4m3 A and B K-major, D = alpha*acc + beta*C,
+// 224-column tiles (UMMA N = 224).
+#include "dg_internal.h"
+
+namespace dg {
+
+cudaError_t launch_gemm_fp8_kk_n224(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& d,
+                                    const CUtensorMap& c, const GemmParams& p, int num_sms, cudaStream_t s) {
+  return launch_gemm_t<true, false, false, EPI_FP8, 224>(a, b, d, c, p, num_sms, s);
+}
+
+}  // namespace dg

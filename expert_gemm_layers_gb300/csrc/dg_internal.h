@@ -37,7 +37,8 @@ enum GemmVariant : int {
   GV_BF16_MM_STORE = 3, // bf16, A and B MN-major, plain store
   GV_BF16_KK_SWIGLU = 4, // bf16, A and B K-major, paired silu(a)*b epilogue
   GV_BF16_KM_LNSTATS = 5, // bf16, A K-major, B MN-major, bias + per-tile LayerNorm statistics
-  GV_BF16_KM_STORE = 6    // bf16, A K-major, B MN-major, plain store
+  GV_BF16_KM_STORE = 6,   // bf16, A K-major, B MN-major, plain store
+  GV_FP8_KK_N224 = 7      // GV_FP8_KK with 224-column tiles
 };
 
 // Tiles along N of one problem for this variant (output columns per tile).
@@ -81,6 +82,10 @@ cudaError_t launch_gemm_bf16_km_lnstats(const CUtensorMap&, const CUtensorMap&, 
                                         const CUtensorMap&, const GemmParams&, int num_sms, cudaStream_t);
 cudaError_t launch_gemm_bf16_km_store(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
                                       const CUtensorMap&, const GemmParams&, int num_sms, cudaStream_t);
+cudaError_t launch_gemm_fp8_kk_n224(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
+                                    const GemmParams&, int num_sms, cudaStream_t);
+// Co-resident CTA pairs (or CTAs) of the e4m3 GEMM on the current device.
+cudaError_t gemm_fp8_units(int num_sms, int* units);
 
 // The GEMMs run as CTA pairs (cta_group::2, 256-row tiles, clusters of 2).
 constexpr bool kUsePairs = true;
@@ -88,20 +93,55 @@ constexpr bool kUsePairs = true;
 // Rows of a K-major B tile each CTA loads (the TMA box height of such B maps).
 constexpr int kKMajorBRows = kUsePairs ? 128 : 256;
 
-// Host launcher body shared by the instantiation units: one persistent launch,
-// one CTA (or CTA pair) per SM (pair of SMs) up to the number of tiles.
-template <bool kFp8, bool kAMN, bool kBMN, int kEpi>
-cudaError_t launch_gemm_t(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& d, const CUtensorMap& c,
-                          const GemmParams& p, int num_sms, cudaStream_t s) {
-  using Cfg = GemmCfg<kFp8, kAMN, kBMN, kEpi, kUsePairs>;
-  auto kern = gemm_tc_kernel<kFp8, kAMN, kBMN, kEpi, kUsePairs>;
-  // Per device, once: the shared-memory attribute and the number of co-resident
-  // CTA pairs (host-side work kept off the launch path).
+// Per device, once: the kernel's shared-memory attribute and the number of
+// co-resident CTA pairs (CTAs) -- host-side work kept off the launch path.
+template <bool kFp8, bool kAMN, bool kBMN, int kEpi, int kBN = 256>
+cudaError_t gemm_units_t(int num_sms, int* out) {
+  using Cfg = GemmCfg<kFp8, kAMN, kBMN, kEpi, kUsePairs, kBN>;
+  auto kern = gemm_tc_kernel<kFp8, kAMN, kBMN, kEpi, kUsePairs, kBN>;
   static std::atomic<int> units_cache[64];
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  int units = units_cache[dev].load(std::memory_order_relaxed);
+  if (units == 0) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    units = num_sms;
+    if (kUsePairs) {
+      cudaLaunchConfig_t cfg = {};
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = 2;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      cfg.blockDim = dim3(Cfg::NUM_THREADS);
+      cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
+      cfg.gridDim = dim3(2);
+      int clusters = 0;
+      e = cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg);
+      if (e != cudaSuccess) return e;
+      units = clusters > 0 ? clusters : 1;
+    }
+    units_cache[dev].store(units, std::memory_order_relaxed);
+  }
+  *out = units;
+  return cudaSuccess;
+}
+
+// Host launcher body shared by the instantiation units: one persistent launch,
+// one CTA (or CTA pair) per SM (pair of SMs) up to the number of tiles.
+template <bool kFp8, bool kAMN, bool kBMN, int kEpi, int kBN = 256>
+cudaError_t launch_gemm_t(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& d, const CUtensorMap& c,
+                          const GemmParams& p, int num_sms, cudaStream_t s) {
+  using Cfg = GemmCfg<kFp8, kAMN, kBMN, kEpi, kUsePairs, kBN>;
+  auto kern = gemm_tc_kernel<kFp8, kAMN, kBMN, kEpi, kUsePairs, kBN>;
+  int units = 0;
+  cudaError_t e = gemm_units_t<kFp8, kAMN, kBMN, kEpi, kBN>(num_sms, &units);
+  if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   cfg.blockDim = dim3(Cfg::NUM_THREADS);
@@ -114,20 +154,6 @@ cudaError_t launch_gemm_t(const CUtensorMap& a, const CUtensorMap& b, const CUte
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-  }
-  int units = units_cache[dev].load(std::memory_order_relaxed);
-  if (units == 0) {
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    units = num_sms;
-    if (kUsePairs) {
-      cfg.gridDim = dim3(2);
-      int clusters = 0;
-      e = cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg);
-      if (e != cudaSuccess) return e;
-      units = clusters > 0 ? clusters : 1;
-    }
-    units_cache[dev].store(units, std::memory_order_relaxed);
   }
   const int64_t tiles = static_cast<int64_t>(p.G) * p.tiles_m * p.tiles_n;
   if (tiles < units) units = static_cast<int>(tiles);

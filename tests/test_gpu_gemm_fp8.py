@@ -13,6 +13,7 @@ from expert_gemm_layers_gb300 import gemm_fp8, synth
 from _compare import TOL_FP8, assert_close, err_max, to_f64
 
 pytestmark = pytest.mark.gpu
+DEV = torch.device("cuda")
 
 
 def _run(A, B, C, alpha, beta):
@@ -97,3 +98,20 @@ def test_deterministic_reruns():
     A, B, C = synth.fp8_gemm_inputs(384, 512, 512, seed=11)
     d1, d2 = _run(A, B, C, 0.5, 1.0), _run(A, B, C, 0.5, 1.0)
     assert torch.equal(d1, d2)
+
+
+def test_tile_widths_both_run():
+    # Small problems take 224-column tiles; at 19456 x 4864 (76 x 19 tiles of
+    # 256 columns) the 256-column tiles need fewer column steps per CTA pair.
+    from expert_gemm_layers_gb300 import trace_begin, trace_end
+    names = []
+    for M, N, K in [(512, 1024, 256), (19456, 4864, 128)]:
+        A, B, C = synth.fp8_gemm_inputs(M, N, K, seed=M + K, device=DEV)
+        trace_begin()
+        D = gemm_fp8(A, B, C, 0.5, 1.0)
+        torch.cuda.synchronize()
+        names += [e["name"] for e in trace_end()]
+        rows = np.random.default_rng(M).choice(M, size=48, replace=False)
+        ref = O.gemm_fp8(synth.bits(A), synth.bits(B), synth.bits(C), 0.5, 1.0, rows=rows)
+        assert_close(D[torch.from_numpy(rows).to(DEV)], ref, TOL_FP8, f"gemm_fp8 {M}x{N}x{K}")
+    assert names == ["gemm_fp8_n224", "gemm_fp8"], names
