@@ -57,6 +57,7 @@ SIGNATURES = {
                                         _vp]),
     "dg_tp_swiglu_noalloc": (ctypes.c_int, [_i64, _i64, _i64, _i32, _i32, _vp, _vp, _vp, _vp, _vp]),
     "dg_trace_begin": (ctypes.c_int, []),
+    "dg_trace_begin_only": (ctypes.c_int, [ctypes.c_char_p]),
     "dg_trace_end": (ctypes.c_int32, [ctypes.POINTER(TraceEntry), ctypes.c_int32]),
 }
 

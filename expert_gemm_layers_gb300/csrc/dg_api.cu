@@ -6,6 +6,7 @@
 #include <stdio.h>
 
 #include <mutex>
+#include <string>
 #include <string.h>
 #include <vector>
 
@@ -79,6 +80,7 @@ struct TraceRecord {
 };
 std::mutex g_trace_mu;
 bool g_tracing = false;
+std::string g_trace_only;  // record only launches of this name (empty: all)
 std::vector<TraceRecord> g_trace;
 }  // namespace
 
@@ -87,6 +89,7 @@ TraceScope::TraceScope(const char* name, cudaStream_t s, double flops, double by
   {
     std::lock_guard<std::mutex> g(g_trace_mu);
     if (!g_tracing) return;
+    if (!g_trace_only.empty() && g_trace_only != name) return;
   }
   if (cudaEventCreate(&e0_) != cudaSuccess) return;
   if (cudaEventCreate(&e1_) != cudaSuccess) {
@@ -860,8 +863,11 @@ dg_status dg_tp_swiglu_bwd(int64_t S, int64_t d, int64_t ffn, int32_t W, int32_t
                   2.0 * (2.0 * r * ff + r * dd + 2.0 * ff * dd));
 }
 
-dg_status dg_trace_begin(void) {
+dg_status dg_trace_begin(void) { return dg_trace_begin_only(nullptr); }
+
+dg_status dg_trace_begin_only(const char* name) {
   std::lock_guard<std::mutex> g(g_trace_mu);
+  g_trace_only = name ? name : "";
   g_tracing = true;
   return DG_OK;
 }

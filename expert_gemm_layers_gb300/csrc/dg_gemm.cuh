@@ -191,22 +191,8 @@ __global__ void __launch_bounds__(GemmCfg<kFp8, kAMN, kBMN, kEpi, kPair, kBN>::N
   const uint32_t rank = kPair ? cluster_ctarank() : 0u;  // position in the CTA pair
   const bool leader = rank == 0u;
 
-  // A sticky device error from an earlier failure: do nothing.  In a CTA pair
-  // the leader decides for both, so the pair's control flow stays uniform.
-  if (kPair) {
-    cluster_sync_all();  // both CTAs are running before any access to the peer's shared memory
-    if (threadIdx.x == 0 && leader) {
-      const uint32_t v = ld_volatile_u32(p.err);
-      st_cluster_u32(mapa_shared(smem_u32(&s_abort), 0), v);
-      st_cluster_u32(mapa_shared(smem_u32(&s_abort), 1), v);
-    }
-    cluster_sync_all();
-  } else {
-    if (threadIdx.x == 0) s_abort = ld_volatile_u32(p.err);
-    __syncthreads();
-  }
-  if (s_abort != 0u) return;
-
+  // Prologue: barriers and descriptor prefetch touch nothing a preceding
+  // kernel writes, so with programmatic launch they overlap its tail.
   if (warp == 0 && lane == 0) {
     for (int s = 0; s < Cfg::STAGES; ++s) {
       mbar_init(&full[s], 1);
@@ -224,6 +210,23 @@ __global__ void __launch_bounds__(GemmCfg<kFp8, kAMN, kBMN, kEpi, kPair, kBN>::N
     tma_prefetch_desc(&tmD);
     if (kEpi == EPI_FP8 && p.has_c) tma_prefetch_desc(&tmC);
   }
+  if (kPair) cluster_sync_all();  // both CTAs run before any access to the peer's shared memory
+  griddep_wait();                 // inputs and the error word may come from the preceding kernel
+
+  // A sticky device error from an earlier failure: do nothing.  In a CTA pair
+  // the leader decides for both, so the pair's control flow stays uniform
+  // (the value is published by the barrier after the TMEM allocation).
+  if (threadIdx.x == 0) {
+    const uint32_t v = ld_volatile_u32(p.err);
+    if (kPair) {
+      if (leader) {
+        st_cluster_u32(mapa_shared(smem_u32(&s_abort), 0), v);
+        st_cluster_u32(mapa_shared(smem_u32(&s_abort), 1), v);
+      }
+    } else {
+      s_abort = v;
+    }
+  }
   if (warp == 1) {
     if (kPair) {
       tmem_alloc_pair(tmem_holder, Cfg::TMEM_COLS);
@@ -240,6 +243,7 @@ __global__ void __launch_bounds__(GemmCfg<kFp8, kAMN, kBMN, kEpi, kPair, kBN>::N
     __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem_base = *tmem_holder;
+  const bool aborted = s_abort != 0u;
 
   const int tiles_per_group = p.tiles_m * p.tiles_n;
   const int total_tiles = p.G * tiles_per_group;
@@ -247,7 +251,9 @@ __global__ void __launch_bounds__(GemmCfg<kFp8, kAMN, kBMN, kEpi, kPair, kBN>::N
   const int unit = static_cast<int>(blockIdx.x) / Cfg::CTAS;  // this CTA's (pair's) slot in the schedule
   const int num_units = static_cast<int>(gridDim.x) / Cfg::CTAS;
 
-  if (warp == 0) {
+  if (aborted) {
+    // nothing to do: straight to the teardown (TMEM is freed there)
+  } else if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       int stage = 0;
@@ -630,6 +636,8 @@ __global__ void __launch_bounds__(GemmCfg<kFp8, kAMN, kBMN, kEpi, kPair, kBN>::N
     __syncwarp();
   }
 
+  // This CTA's work is issued: the next kernel may start launching.
+  griddep_launch_dependents();
   tc_fence_before_sync();
   if (kPair)
     cluster_sync_all();

@@ -255,6 +255,20 @@ static __device__ __forceinline__ uint32_t mapa_shared(uint32_t saddr, uint32_t 
   return r;
 }
 
+// Programmatic dependent launch.  griddep_wait blocks until the preceding
+// grid of the stream has completed and its memory operations are visible (it
+// returns at once for a launch without the programmatic-serialisation
+// attribute); every read of data a preceding kernel may have written comes
+// after it.  griddep_launch_dependents lets the next grid of the stream start
+// launching (its CTAs then run their own prologue up to their griddep_wait);
+// without it that happens as the CTAs exit.  It is issued late, near the end
+// of a CTA's work, so that waiting CTAs of the next grid do not sit beside
+// this one for long.
+static __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+static __device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // All threads of both CTAs of the cluster.
 static __device__ __forceinline__ void cluster_sync_all() {
   asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");

@@ -108,6 +108,7 @@ __device__ __forceinline__ void cp_async_wait() {
 
 __global__ void ln_stats_finalize_kernel(const float4* __restrict__ part, float4* __restrict__ stats, int T, int M,
                                          int H, int tile_n, int tiles_n, float eps, const uint32_t* err) {
+  griddep_wait();
   if (ld_volatile_u32(err) != 0u) return;
   const int64_t rows = static_cast<int64_t>(T) * M;
   const int N = 2 * H;
@@ -135,6 +136,7 @@ __global__ void __launch_bounds__(NT, 512 / NT) ln_gate_fwd_kernel(
     const __nv_bfloat16* __restrict__ bx, const __nv_bfloat16* __restrict__ gg, const __nv_bfloat16* __restrict__ bg,
     __nv_bfloat16* __restrict__ Hl, int M, int L, int H, int ctas_per_rank, const uint32_t* err) {
   extern __shared__ uint4 ring[];  // [kFwdStages][VPT][2][NT]
+  griddep_wait();
   if (block_aborted(err)) return;
   const int nvec = H >> 3;
   const int64_t zstride = 2 * static_cast<int64_t>(H);
@@ -234,6 +236,7 @@ __global__ void __launch_bounds__(kRowsumThreads, 2) ln_gate_bwd_rowsum_kernel(
     const __nv_bfloat16* __restrict__ gx, const __nv_bfloat16* __restrict__ bx, const __nv_bfloat16* __restrict__ gg,
     const __nv_bfloat16* __restrict__ bg, float4* __restrict__ rowsum, int64_t rows, int M, int L, int H,
     const uint32_t* err) {
+  griddep_wait();
   if (warp_aborted(err)) return;
   const int lane = threadIdx.x & 31;
   const int64_t warps = static_cast<int64_t>(gridDim.x) * (kRowsumThreads / 32);
@@ -292,6 +295,7 @@ __global__ void __launch_bounds__(kApplyThreads) ln_gate_bwd_apply_kernel(
   extern __shared__ uint4 ring_raw[];
   auto ring = reinterpret_cast<uint4(*)[3][kApplyThreads]>(ring_raw);
   auto slot = reinterpret_cast<uint4(*)[kApplyThreads / 32][2]>(ring_raw + kApplyStages * 3 * kApplyThreads);
+  griddep_wait();
   if (warp_aborted(err)) return;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int t = blockIdx.y, rsp = blockIdx.z, nsplit = gridDim.z;
@@ -380,6 +384,7 @@ __global__ void grad_reduce_kernel(const float* __restrict__ part, __nv_bfloat16
                                    __nv_bfloat16* __restrict__ d_nx_w, __nv_bfloat16* __restrict__ d_nx_b,
                                    __nv_bfloat16* __restrict__ d_ng_w, __nv_bfloat16* __restrict__ d_ng_b, int P,
                                    int L, int H, int nsplit, const uint32_t* err) {
+  griddep_wait();
   if (ld_volatile_u32(err) != 0u) return;
   const int T = P * L;
   const int64_t n_b1 = static_cast<int64_t>(T) * 2 * H;
@@ -412,6 +417,7 @@ __global__ void grad_reduce_kernel(const float* __restrict__ part, __nv_bfloat16
 // out[g, c] = sum over rows n of src[g*g_stride + n*row_stride + c]; two columns per thread.
 __global__ void column_sum_kernel(const __nv_bfloat16* __restrict__ src, __nv_bfloat16* __restrict__ out, int rows,
                                   int ncols, int64_t g_stride, int64_t row_stride, const uint32_t* err) {
+  griddep_wait();
   if (ld_volatile_u32(err) != 0u) return;
   const int g = blockIdx.y;
   const int c = 2 * (blockIdx.x * blockDim.x + threadIdx.x);
@@ -444,6 +450,7 @@ __global__ void column_sum_kernel(const __nv_bfloat16* __restrict__ src, __nv_bf
 // dh -> h; 8 columns per thread.
 __global__ void swiglu_gate_bwd_kernel(__nv_bfloat16* __restrict__ ab, __nv_bfloat16* __restrict__ dh_h, int64_t rows,
                                        int W, int F, const uint32_t* err) {
+  griddep_wait();
   if (ld_volatile_u32(err) != 0u) return;
   const int fv = F / 8;
   const int64_t total = rows * W * fv;
@@ -483,6 +490,7 @@ __global__ void swiglu_gate_bwd_kernel(__nv_bfloat16* __restrict__ ab, __nv_bflo
 // Exchange permutations, 16 bytes per thread.
 __global__ void dispatch_kernel(const uint4* __restrict__ in, uint4* __restrict__ out, int P, int B, int T,
                                 int vec_per_row, const uint32_t* err) {
+  griddep_wait();
   if (ld_volatile_u32(err) != 0u) return;
   const int L = T / P, PB = P * B;
   const int64_t total = static_cast<int64_t>(P) * PB * L * vec_per_row;
@@ -500,6 +508,7 @@ __global__ void dispatch_kernel(const uint4* __restrict__ in, uint4* __restrict_
 
 __global__ void combine_kernel(const uint4* __restrict__ in, uint4* __restrict__ out, int P, int B, int T,
                                int vec_per_row, const uint32_t* err) {
+  griddep_wait();
   if (ld_volatile_u32(err) != 0u) return;
   const int L = T / P, PB = P * B;
   const int64_t total = static_cast<int64_t>(PB) * T * vec_per_row;
@@ -517,6 +526,7 @@ __global__ void combine_kernel(const uint4* __restrict__ in, uint4* __restrict__
 // Waits, with the library's bounded wait, on a barrier nobody arrives at.
 __global__ void debug_wait_kernel(uint32_t* err, uint64_t limit_ns) {
   __shared__ uint64_t bar;
+  griddep_wait();
   if (threadIdx.x == 0) {
     mbar_init(&bar, 1);
     fence_mbar_init();
@@ -552,9 +562,8 @@ cudaError_t launch_ln_stats_finalize(const float4* part, void* stats, int T, int
   const int64_t rows = static_cast<int64_t>(T) * M;
   int64_t blocks = (rows + 255) / 256;
   if (blocks > 16 * dev.num_sms) blocks = 16 * dev.num_sms;
-  ln_stats_finalize_kernel<<<static_cast<int>(blocks), 256, 0, s>>>(part, static_cast<float4*>(stats), T, M, H, tile_n,
-                                                                    tiles_n, eps, dev.err);
-  return cudaGetLastError();
+  return launch_pdl(ln_stats_finalize_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, s, part,
+                    static_cast<float4*>(stats), T, M, H, tile_n, tiles_n, eps, dev.err);
 }
 
 cudaError_t launch_ln_gate_fwd(const void* Z, const void* stats, const void* nx_w, const void* nx_b, const void* ng_w,
@@ -567,11 +576,10 @@ cudaError_t launch_ln_gate_fwd(const void* Z, const void* stats, const void* nx_
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     const int cpr = ctas_per_rank(dev, reinterpret_cast<const void*>(kern), nt, smem, P, static_cast<int64_t>(L) * M);
-    kern<<<P * cpr, nt, smem, s>>>(static_cast<const __nv_bfloat16*>(Z), static_cast<const float4*>(stats),
-                                   static_cast<const __nv_bfloat16*>(nx_w), static_cast<const __nv_bfloat16*>(nx_b),
-                                   static_cast<const __nv_bfloat16*>(ng_w), static_cast<const __nv_bfloat16*>(ng_b),
-                                   static_cast<__nv_bfloat16*>(Hl), M, L, H, cpr, dev.err);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3(P * cpr), dim3(nt), smem, s, static_cast<const __nv_bfloat16*>(Z),
+                      static_cast<const float4*>(stats), static_cast<const __nv_bfloat16*>(nx_w),
+                      static_cast<const __nv_bfloat16*>(nx_b), static_cast<const __nv_bfloat16*>(ng_w),
+                      static_cast<const __nv_bfloat16*>(ng_b), static_cast<__nv_bfloat16*>(Hl), M, L, H, cpr, dev.err);
   };
   if (nt == 256 && vpt == 1) return run(ln_gate_fwd_kernel<256, 1>);
   if (nt == 256) return run(ln_gate_fwd_kernel<256, 2>);
@@ -590,12 +598,11 @@ cudaError_t launch_ln_gate_bwd_rowsum(const void* Z, const void* stats, const vo
   int64_t blocks = static_cast<int64_t>(per_sm) * dev.num_sms;
   const int64_t need = (rows + kRowsumThreads / 32 - 1) / (kRowsumThreads / 32);
   if (blocks > need) blocks = need;
-  ln_gate_bwd_rowsum_kernel<<<static_cast<int>(blocks), kRowsumThreads, 0, s>>>(
+  return launch_pdl(ln_gate_bwd_rowsum_kernel, dim3(static_cast<unsigned>(blocks)), dim3(kRowsumThreads), 0, s,
       static_cast<const __nv_bfloat16*>(Z), static_cast<const float4*>(stats), static_cast<const __nv_bfloat16*>(dHl),
       static_cast<const __nv_bfloat16*>(nx_w), static_cast<const __nv_bfloat16*>(nx_b),
       static_cast<const __nv_bfloat16*>(ng_w), static_cast<const __nv_bfloat16*>(ng_b), static_cast<float4*>(rowsum),
       rows, M, L, H, dev.err);
-  return cudaGetLastError();
 }
 
 int ffn_bwd_row_splits(int T, int M) {
@@ -614,12 +621,11 @@ cudaError_t launch_ln_gate_bwd_apply(const void* Z, const void* stats, const voi
   const int smem = kApplyStages * (3 * kApplyThreads + 2 * (kApplyThreads / 32)) * 16;
   cudaError_t e = cudaFuncSetAttribute(ln_gate_bwd_apply_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  ln_gate_bwd_apply_kernel<<<grid, kApplyThreads, smem, s>>>(
+  return launch_pdl(ln_gate_bwd_apply_kernel, grid, dim3(kApplyThreads), smem, s,
       static_cast<const __nv_bfloat16*>(Z), static_cast<const float4*>(stats), static_cast<const float4*>(rowsum),
       static_cast<const __nv_bfloat16*>(dHl), static_cast<const __nv_bfloat16*>(nx_w),
       static_cast<const __nv_bfloat16*>(nx_b), static_cast<const __nv_bfloat16*>(ng_w),
       static_cast<const __nv_bfloat16*>(ng_b), static_cast<__nv_bfloat16*>(dZ), part, M, L, H, dev.err);
-  return cudaGetLastError();
 }
 
 cudaError_t launch_grad_reduce(const float* part, void* d_b1, void* d_nx_w, void* d_nx_b, void* d_ng_w, void* d_ng_b,
@@ -627,19 +633,17 @@ cudaError_t launch_grad_reduce(const float* part, void* d_b1, void* d_nx_w, void
   const int64_t n = static_cast<int64_t>(P) * L * 2 * H + static_cast<int64_t>(P) * 4 * H;
   int64_t blocks = (n + 255) / 256;
   if (blocks > 8 * dev.num_sms) blocks = 8 * dev.num_sms;
-  grad_reduce_kernel<<<static_cast<int>(blocks), 256, 0, s>>>(
+  return launch_pdl(grad_reduce_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, s,
       part, static_cast<__nv_bfloat16*>(d_b1), static_cast<__nv_bfloat16*>(d_nx_w), static_cast<__nv_bfloat16*>(d_nx_b),
       static_cast<__nv_bfloat16*>(d_ng_w), static_cast<__nv_bfloat16*>(d_ng_b), P, L, H, nsplit, dev.err);
-  return cudaGetLastError();
 }
 
 cudaError_t launch_column_sum(const void* src, void* out, int G, int rows, int ncols, int64_t g_stride,
                               int64_t row_stride, const DeviceInfo& dev, cudaStream_t s) {
   const int threads = 128;
   dim3 grid((ncols / 2 + threads - 1) / threads, G);
-  column_sum_kernel<<<grid, threads, 0, s>>>(static_cast<const __nv_bfloat16*>(src), static_cast<__nv_bfloat16*>(out),
-                                            rows, ncols, g_stride, row_stride, dev.err);
-  return cudaGetLastError();
+  return launch_pdl(column_sum_kernel, grid, dim3(threads), 0, s, static_cast<const __nv_bfloat16*>(src),
+                    static_cast<__nv_bfloat16*>(out), rows, ncols, g_stride, row_stride, dev.err);
 }
 
 cudaError_t launch_swiglu_gate_bwd(void* ab, void* dh_h, int64_t rows, int W, int F, const DeviceInfo& dev,
@@ -647,9 +651,8 @@ cudaError_t launch_swiglu_gate_bwd(void* ab, void* dh_h, int64_t rows, int W, in
   const int64_t total = rows * W * (F / 8);
   int64_t blocks = (total + 255) / 256;
   if (blocks > 16 * dev.num_sms) blocks = 16 * dev.num_sms;
-  swiglu_gate_bwd_kernel<<<static_cast<int>(blocks), 256, 0, s>>>(static_cast<__nv_bfloat16*>(ab),
-                                                                  static_cast<__nv_bfloat16*>(dh_h), rows, W, F, dev.err);
-  return cudaGetLastError();
+  return launch_pdl(swiglu_gate_bwd_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, s,
+                    static_cast<__nv_bfloat16*>(ab), static_cast<__nv_bfloat16*>(dh_h), rows, W, F, dev.err);
 }
 
 cudaError_t launch_dispatch(const void* in, void* out, int P, int B, int T, int D, const DeviceInfo& dev,
@@ -657,9 +660,8 @@ cudaError_t launch_dispatch(const void* in, void* out, int P, int B, int T, int 
   const int64_t total = static_cast<int64_t>(P) * B * T * (D / 8);
   int64_t blocks = (total + 255) / 256;
   if (blocks > 16 * dev.num_sms) blocks = 16 * dev.num_sms;
-  dispatch_kernel<<<static_cast<int>(blocks), 256, 0, s>>>(static_cast<const uint4*>(in), static_cast<uint4*>(out), P,
-                                                            B, T, D / 8, dev.err);
-  return cudaGetLastError();
+  return launch_pdl(dispatch_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, s,
+                    static_cast<const uint4*>(in), static_cast<uint4*>(out), P, B, T, D / 8, dev.err);
 }
 
 cudaError_t launch_combine(const void* in, void* out, int P, int B, int T, int D, const DeviceInfo& dev,
@@ -667,14 +669,12 @@ cudaError_t launch_combine(const void* in, void* out, int P, int B, int T, int D
   const int64_t total = static_cast<int64_t>(P) * B * T * (D / 8);
   int64_t blocks = (total + 255) / 256;
   if (blocks > 16 * dev.num_sms) blocks = 16 * dev.num_sms;
-  combine_kernel<<<static_cast<int>(blocks), 256, 0, s>>>(static_cast<const uint4*>(in), static_cast<uint4*>(out), P,
-                                                           B, T, D / 8, dev.err);
-  return cudaGetLastError();
+  return launch_pdl(combine_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, s,
+                    static_cast<const uint4*>(in), static_cast<uint4*>(out), P, B, T, D / 8, dev.err);
 }
 
 cudaError_t launch_debug_wait(uint32_t* err, uint64_t limit_ns, cudaStream_t s) {
-  debug_wait_kernel<<<1, 32, 0, s>>>(err, limit_ns);
-  return cudaGetLastError();
+  return launch_pdl(debug_wait_kernel, dim3(1), dim3(32), 0, s, err, limit_ns);
 }
 
 }  // namespace dg

@@ -280,9 +280,13 @@ def debug_wait_timeout(limit_us: int, device=None) -> None:
         check(lib.dg_debug_wait_timeout(int(limit_us), ctypes.c_void_p(_stream(dev))))
 
 
-def trace_begin() -> None:
-    """Start recording every libdg kernel launch with CUDA events."""
-    check(load().dg_trace_begin())
+def trace_begin(only: str | None = None) -> None:
+    """Start recording libdg kernel launches with CUDA events: all of them, or
+    only those named `only`."""
+    if only:
+        check(load().dg_trace_begin_only(only.encode()))
+    else:
+        check(load().dg_trace_begin())
 
 
 def trace_end() -> list[dict]:

@@ -266,6 +266,12 @@ typedef struct {
 dg_status dg_trace_begin(void);
 int32_t dg_trace_end(dg_trace_entry* out, int32_t max_entries);
 
+/* dg_trace_begin_only: as dg_trace_begin, but records only the launches named
+ * `name` (a NUL-terminated kernel name as reported by dg_trace_end; NULL or ""
+ * records every launch).  Launches not recorded get no events, so the
+ * kernels around them keep their programmatic-launch overlap. */
+dg_status dg_trace_begin_only(const char* name);
+
 #ifdef __cplusplus
 }
 #endif
