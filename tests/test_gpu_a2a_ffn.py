@@ -26,6 +26,8 @@ SMALL_SHAPES = [
     (2, 3, 4, 136, 3),      # ragged everything: H=408, 2H=816, D=136 (K not a multiple of 64)
     (4, 40, 16, 64, 2),     # M=160 rows: two row tiles, the second ragged
     (1, 5, 16, 128, 6),     # one rank (dispatch/combine are the identity)
+    (2, 2, 4, 680, 6),      # H=4080: the backward's row split over a CTA pair, last threads idle
+    (2, 2, 4, 1024, 8),     # H=8192, the largest supported width: three CTAs per row
 ]
 
 
