@@ -40,16 +40,21 @@ MEASURED_PEAKS = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK_PEAKS = dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0)
 
 # Per-launch DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) from
-# one ncu capture of the kernel, scaled to the benchmark's launch, with the
-# sha256 of its sources at capture time; a kernel whose sources changed since
-# reports null.  Capture summary: profiles/gemm_tc_kernel_ffn_T8_and_fp8_4096.md.
+# one ncu capture of each kernel of the FFN layer at T=8 token positions (an
+# eighth of the benchmark's problems; traffic grows in proportion, so it is
+# scaled by 8), with the sha256 of the kernel's sources at capture time; a
+# kernel whose sources changed since reports null.  Capture summary:
+# profiles/ffn_layer_kernels_traffic_T8.md.
 TRAFFIC = {
-    "ffn_bwd_dw1": {
-        "bytes_per_launch": 8 * (1.133279e9 + 0.299984e9),   # captured at T=8; the benchmark has T=64
-        "sources": ["expert_gemm_layers_gb300/csrc/dg_gemm.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh",
-                    "expert_gemm_layers_gb300/csrc/dg_gemm_bf16_mm_store.cu"],
-        "sha256": "feaf07905b5222e4e4b69f62c7673263a7bd31922ed82ea266eb033bd50374a9",
-    },
+    "ffn_gemm1": {"bytes_per_launch": 8 * 1.384868e+09, "sources": ["expert_gemm_layers_gb300/csrc/dg_gemm.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh", "expert_gemm_layers_gb300/csrc/dg_gemm_bf16_km_lnstats.cu"], "sha256": "b123a40f933bda2c0ab1c5011008851688923a307da03bd8ebded7ca0535a83f"},
+    "ffn_ln_gate_fwd": {"bytes_per_launch": 8 * 1.472826e+09, "sources": ["expert_gemm_layers_gb300/csrc/dg_rowops.cu", "expert_gemm_layers_gb300/csrc/dg_gate.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh"], "sha256": "898882bb8f87985a51ae9ba812b3d3f613cba2892fe48da6044ff2f77735bca5"},
+    "ffn_gemm2": {"bytes_per_launch": 8 * 1.170274e+09, "sources": ["expert_gemm_layers_gb300/csrc/dg_gemm.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh", "expert_gemm_layers_gb300/csrc/dg_gemm_bf16_km_bias.cu"], "sha256": "2d9a88fb5baeac441676751484ffebb16656647fbae4594fab1170dd0fa06cd6"},
+    "ffn_bwd_dhl": {"bytes_per_launch": 8 * 6.904627e+08, "sources": ["expert_gemm_layers_gb300/csrc/dg_gemm.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh", "expert_gemm_layers_gb300/csrc/dg_gemm_bf16_kk_store.cu"], "sha256": "dd10d6be8829e588a6c479b3fcca3d7188e9ba2ae99b70492cacaf08bc82e008"},
+    "ffn_bwd_dwout": {"bytes_per_launch": 8 * 1.121104e+09, "sources": ["expert_gemm_layers_gb300/csrc/dg_gemm.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh", "expert_gemm_layers_gb300/csrc/dg_gemm_bf16_mm_store.cu"], "sha256": "8f421cda73a0cccf49d2638dfbabcfa3cd33347bb10b0350baa017ea8c1fe572"},
+    "ffn_bwd_ln_rowsum": {"bytes_per_launch": 8 * 1.512092e+09, "sources": ["expert_gemm_layers_gb300/csrc/dg_rowops.cu", "expert_gemm_layers_gb300/csrc/dg_gate.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh"], "sha256": "898882bb8f87985a51ae9ba812b3d3f613cba2892fe48da6044ff2f77735bca5"},
+    "ffn_bwd_ln_apply": {"bytes_per_launch": 8 * 2.566492e+09, "sources": ["expert_gemm_layers_gb300/csrc/dg_rowops.cu", "expert_gemm_layers_gb300/csrc/dg_gate.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh"], "sha256": "898882bb8f87985a51ae9ba812b3d3f613cba2892fe48da6044ff2f77735bca5"},
+    "ffn_bwd_dx": {"bytes_per_launch": 8 * 2.750209e+09, "sources": ["expert_gemm_layers_gb300/csrc/dg_gemm.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh", "expert_gemm_layers_gb300/csrc/dg_gemm_bf16_kk_store.cu"], "sha256": "dd10d6be8829e588a6c479b3fcca3d7188e9ba2ae99b70492cacaf08bc82e008"},
+    "ffn_bwd_dw1": {"bytes_per_launch": 8 * 1.440493e+09, "sources": ["expert_gemm_layers_gb300/csrc/dg_gemm.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh", "expert_gemm_layers_gb300/csrc/dg_gemm_bf16_mm_store.cu"], "sha256": "8f421cda73a0cccf49d2638dfbabcfa3cd33347bb10b0350baa017ea8c1fe572"},
 }
 
 
@@ -423,6 +428,8 @@ def run_dg(args, rank, world):
     roof["kernel"] = top["name"]
     roof["peak_source"] = peaks["source"] + (" sustained bf16" if top["flops"] > 0 else " HBM copy")
     roof["traffic"] = traffic_for(top["name"])
+    if roof["traffic"] is not None:
+        roof["traffic_source"] = "ncu dram__bytes_read+write at T=8 token positions, x8 (profiles/ffn_layer_kernels_traffic_T8.md)"
     roof["launches_timed"] = top["launches"]
     total_ms = sum(e["total_ms"] for e in table)
     kernel_table = {e["name"]: {"launches_per_step": e["launches"] // 2,
