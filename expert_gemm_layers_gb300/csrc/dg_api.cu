@@ -221,7 +221,8 @@ dg_status check_ffn_shape(const dg_ffn_shape* sh, FfnDims* o) {
   o->H = o->D * o->k;
   o->L = o->T / o->P;
   o->M = o->P * o->B;
-  if (o->H > 8192) return fail(DG_ERR_UNSUPPORTED, "shape: H = D*k = %lld exceeds 8192", (long long)o->H);
+  if (o->H > kMaxFfnH)
+    return fail(DG_ERR_UNSUPPORTED, "shape: H = D*k = %lld exceeds %d", (long long)o->H, kMaxFfnH);
   if (o->M > (1 << 30)) return fail(DG_ERR_UNSUPPORTED, "shape: P*B too large");
   return DG_OK;
 }

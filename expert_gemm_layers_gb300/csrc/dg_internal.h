@@ -88,6 +88,10 @@ cudaError_t launch_gemm_fp8_kk_n224(const CUtensorMap&, const CUtensorMap&, cons
 // Co-resident CTA pairs (or CTAs) of the e4m3 GEMM on the current device.
 cudaError_t gemm_fp8_units(int num_sms, int* units);
 
+// Widest FFN hidden size H = D*k accepted (GEMM N = 2H stays far inside int32
+// tile arithmetic; the row kernels split wider rows into column blocks).
+constexpr int kMaxFfnH = 65536;
+
 // The GEMMs run as CTA pairs (cta_group::2, 256-row tiles, clusters of 2).
 constexpr bool kUsePairs = true;
 

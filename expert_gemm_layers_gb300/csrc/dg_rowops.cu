@@ -134,22 +134,27 @@ template <int NT, int VPT>
 __global__ void __launch_bounds__(NT, 512 / NT) ln_gate_fwd_kernel(
     const __nv_bfloat16* __restrict__ Z, const float4* __restrict__ stats, const __nv_bfloat16* __restrict__ gx,
     const __nv_bfloat16* __restrict__ bx, const __nv_bfloat16* __restrict__ gg, const __nv_bfloat16* __restrict__ bg,
-    __nv_bfloat16* __restrict__ Hl, int M, int L, int H, int ctas_per_rank, const uint32_t* err) {
+    __nv_bfloat16* __restrict__ Hl, int M, int L, int H, int ctas_per_rank, int col_blocks, const uint32_t* err) {
   extern __shared__ uint4 ring[];  // [kFwdStages][VPT][2][NT]
   griddep_wait();
   if (block_aborted(err)) return;
+  // CTA -> (rank, slot within the rank, column block); a column block is
+  // NT*VPT 8-column vectors of U (and the same columns of G)
+  const int cb = blockIdx.x % col_blocks;
+  const int cta = blockIdx.x / col_blocks;
   const int nvec = H >> 3;
+  const int vbase = cb * NT * VPT;
   const int64_t zstride = 2 * static_cast<int64_t>(H);
-  const int r = blockIdx.x / ctas_per_rank;
+  const int r = cta / ctas_per_rank;
   const int64_t rank_rows = static_cast<int64_t>(L) * M;
   const int64_t stride = ctas_per_rank;
-  const int64_t n_mine = (rank_rows - (blockIdx.x % ctas_per_rank) + stride - 1) / stride;
-  const int64_t row0 = static_cast<int64_t>(r) * rank_rows + (blockIdx.x % ctas_per_rank);
+  const int64_t n_mine = (rank_rows - (cta % ctas_per_rank) + stride - 1) / stride;
+  const int64_t row0 = static_cast<int64_t>(r) * rank_rows + (cta % ctas_per_rank);
 
   float2 wx[VPT][4], cx[VPT][4], wg[VPT][4], cg[VPT][4];
 #pragma unroll
   for (int j = 0; j < VPT; ++j) {
-    const int v = threadIdx.x + NT * j;
+    const int v = vbase + threadIdx.x + NT * j;
     const Affine8 a = load_affine8(gx, bx, gg, bg, static_cast<int64_t>(r) * H + 8 * (v < nvec ? v : 0));
     const uint32_t w0[4] = {a.wx.x, a.wx.y, a.wx.z, a.wx.w}, w1[4] = {a.cx.x, a.cx.y, a.cx.z, a.cx.w};
     const uint32_t w2[4] = {a.wg.x, a.wg.y, a.wg.z, a.wg.w}, w3[4] = {a.cg.x, a.cg.y, a.cg.z, a.cg.w};
@@ -167,7 +172,7 @@ __global__ void __launch_bounds__(NT, 512 / NT) ln_gate_fwd_kernel(
       uint4* st = ring + (i % kFwdStages) * (VPT * 2 * NT);
 #pragma unroll
       for (int j = 0; j < VPT; ++j) {
-        const int v = threadIdx.x + NT * j;
+        const int v = vbase + threadIdx.x + NT * j;
         const bool ok = v < nvec;
         cp_async16(st + (2 * j) * NT + threadIdx.x, zu + 8 * (ok ? v : 0), ok);
         cp_async16(st + (2 * j + 1) * NT + threadIdx.x, zu + H + 8 * (ok ? v : 0), ok);
@@ -191,7 +196,7 @@ __global__ void __launch_bounds__(NT, 512 / NT) ln_gate_fwd_kernel(
     __nv_bfloat16* hrow = Hl + row * static_cast<int64_t>(H);
 #pragma unroll
     for (int j = 0; j < VPT; ++j) {
-      const int v = threadIdx.x + NT * j;
+      const int v = vbase + threadIdx.x + NT * j;
       if (v < nvec) {
         const uint4 pu = st[(2 * j) * NT + threadIdx.x], pg = st[(2 * j + 1) * NT + threadIdx.x];
         const uint32_t uw[4] = {pu.x, pu.y, pu.z, pu.w}, gw[4] = {pg.x, pg.y, pg.z, pg.w};
@@ -548,13 +553,17 @@ static int ctas_per_rank(const DeviceInfo& dev, const void* kernel, int threads,
   return static_cast<int>(c < 1 ? 1 : c);
 }
 
-// Block shape of the per-row kernels: NT threads x VPT 8-column vectors >= H.
-static bool row_shape(int H, int* nt, int* vpt) {
+// Block shape of the normalise-and-gate pass: NT threads x VPT 8-column
+// vectors per CTA, and the number of CTAs (column blocks) one row is split
+// over when it is wider than 8192 columns.
+static void row_shape(int H, int* nt, int* vpt, int* col_blocks) {
   const int nvec = H / 8;
-  if (nvec <= 256) { *nt = 256; *vpt = 1; return true; }
-  if (nvec <= 512) { *nt = 256; *vpt = 2; return true; }
-  if (nvec <= 1024) { *nt = 512; *vpt = 2; return true; }
-  return false;
+  *col_blocks = 1;
+  if (nvec <= 256) { *nt = 256; *vpt = 1; return; }
+  if (nvec <= 512) { *nt = 256; *vpt = 2; return; }
+  *nt = 512;
+  *vpt = 2;
+  *col_blocks = (nvec + 1023) / 1024;
 }
 
 cudaError_t launch_ln_stats_finalize(const float4* part, void* stats, int T, int M, int H, int tile_n, int tiles_n,
@@ -569,17 +578,20 @@ cudaError_t launch_ln_stats_finalize(const float4* part, void* stats, int T, int
 cudaError_t launch_ln_gate_fwd(const void* Z, const void* stats, const void* nx_w, const void* nx_b, const void* ng_w,
                                const void* ng_b, void* Hl, int P, int M, int L, int H, const DeviceInfo& dev,
                                cudaStream_t s) {
-  int nt = 0, vpt = 0;
-  if (!row_shape(H, &nt, &vpt)) return cudaErrorInvalidValue;
+  int nt = 0, vpt = 0, cb = 1;
+  row_shape(H, &nt, &vpt, &cb);
   auto run = [&](auto kern) {
     const size_t smem = static_cast<size_t>(kFwdStages) * vpt * 2 * nt * 16;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    const int cpr = ctas_per_rank(dev, reinterpret_cast<const void*>(kern), nt, smem, P, static_cast<int64_t>(L) * M);
-    return launch_pdl(kern, dim3(P * cpr), dim3(nt), smem, s, static_cast<const __nv_bfloat16*>(Z),
+    // CTAs per rank and column block, so that the grid fills every SM
+    const int cpr =
+        ctas_per_rank(dev, reinterpret_cast<const void*>(kern), nt, smem, P * cb, static_cast<int64_t>(L) * M);
+    return launch_pdl(kern, dim3(P * cpr * cb), dim3(nt), smem, s, static_cast<const __nv_bfloat16*>(Z),
                       static_cast<const float4*>(stats), static_cast<const __nv_bfloat16*>(nx_w),
                       static_cast<const __nv_bfloat16*>(nx_b), static_cast<const __nv_bfloat16*>(ng_w),
-                      static_cast<const __nv_bfloat16*>(ng_b), static_cast<__nv_bfloat16*>(Hl), M, L, H, cpr, dev.err);
+                      static_cast<const __nv_bfloat16*>(ng_b), static_cast<__nv_bfloat16*>(Hl), M, L, H, cpr, cb,
+                      dev.err);
   };
   if (nt == 256 && vpt == 1) return run(ln_gate_fwd_kernel<256, 1>);
   if (nt == 256) return run(ln_gate_fwd_kernel<256, 2>);

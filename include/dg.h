@@ -101,7 +101,8 @@ dg_status dg_gemm_fp8(int64_t M, int64_t N, int64_t K,
  *   inputs, output, dY, d_inputs : [P, B, T, D]
  *   w1 [P, L, D, 2H]   b1 [P, L, 2H]   wout [P, L, H, D]   bout [P, L, D]
  *   nx_w, nx_b, ng_w, ng_b : [P, H]   (LayerNorm weight/bias for U and G)
- * Requirements: T % P == 0, D % 8 == 0, P*B >= 1.
+ * Requirements: T % P == 0, D % 8 == 0, P*B >= 1; H = D*k <= 65536 (larger H
+ * returns DG_ERR_UNSUPPORTED).
  *
  * `saved` (size dg_a2a_ffn_saved_bytes) is required: the forward writes Z,
  * Hl and the per-row LayerNorm statistics there, and the backward reads

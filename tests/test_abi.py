@@ -46,7 +46,7 @@ def _shape(P, B, T, D, k, eps=1e-5):
 def test_ffn_shape_validation_without_gpu(lib):
     from expert_gemm_layers_gb300._lib import STATUS_NAMES
     bad = [_shape(3, 1, 16, 128, 2), _shape(2, 1, 16, 100, 2), _shape(0, 1, 16, 128, 2),
-           _shape(2, 1, 16, 128, 2, eps=0.0), _shape(2, 1, 16, 4096, 4)]
+           _shape(2, 1, 16, 128, 2, eps=0.0), _shape(2, 1, 16, 8192, 9)]  # last: H = 73728 > 65536
     for sh in bad:
         st = lib.dg_a2a_ffn_fwd(ctypes.byref(sh), *([None] * 10), None, 0, None)
         assert STATUS_NAMES[st] in ("DG_ERR_INVALID_ARGUMENT", "DG_ERR_UNSUPPORTED"), (st, lib.dg_last_error())

@@ -31,6 +31,22 @@ SMALL_SHAPES = [
 ]
 
 
+# Held-out ranges of the project statement ("Public checks and instructor
+# coverage": 1<=B<=512, 16<=T<=64, 128<=D<=1280, D%T==0, T%P==0, k in {2,3,6})
+# with our own picks, plus the compute-scaled width (H doubled: k = 12 at
+# D = 1280, H = 15360, a row split over two CTAs in the forward gate pass).
+SWEEP_SHAPES = [
+    (2, 1, 16, 128, 2),     # smallest B, T and D
+    (4, 3, 32, 384, 3),
+    (8, 2, 64, 640, 6),
+    (2, 5, 48, 960, 2),
+    (4, 1, 16, 1280, 3),
+    (8, 7, 64, 1280, 2),
+    (2, 512, 16, 128, 6),   # largest B
+    (2, 2, 16, 1280, 12),   # compute scale 2: H = 15360
+]
+
+
 def _inputs(P, B, T, D, k, seed, device, affine="random"):
     t = synth.ffn_inputs(P, B, T, D, k, seed=seed, device=device, norm_affine=affine)
     return t["inputs"], {n: t[n] for n in FFN_PARAM_NAMES}
@@ -207,3 +223,23 @@ def test_backward_full_width_one_row_per_rank():
     ref = _grads_ref_full(O.FFNShape(P, B, T, D, k), xb, pb, synth.bits(dY))
     for name, r in ref.items():
         assert_close(grads[name].reshape(r.shape), r, TOL_BF16, f"grad {name} (B=1)")
+
+
+# ------------------------------------------------------------------ shape sweep
+
+@pytest.mark.parametrize("P,B,T,D,k", SWEEP_SHAPES)
+def test_shape_sweep_forward_backward(P, B, T, D, k):
+    assert D % T == 0 and T % P == 0
+    inputs, params = _inputs(P, B, T, D, k, seed=7101 + P + B + T + D + k, device="cpu")
+    dY = synth.ffn_grad_output(P, B, T, D, seed=7108 + P + B + T + D + k)
+    xd, pd = inputs.to(DEV), {n: v.to(DEV) for n, v in params.items()}
+    out, saved = a2a_ffn_forward(xd, pd)
+    grads = a2a_ffn_backward(xd, pd, saved, dY.to(DEV))
+    torch.cuda.synchronize()
+    xb, pb = _bits(inputs, params)
+    sh = O.FFNShape(P, B, T, D, k)
+    assert_close(out, O.ffn_forward(sh, xb, pb), TOL_BF16, f"forward {P,B,T,D,k}")
+    for name, r in _grads_ref_full(sh, xb, pb, synth.bits(dY)).items():
+        got = grads[name].reshape(r.shape)
+        assert_close(got, r, TOL_BF16, f"grad {name} {P,B,T,D,k}")
+        assert err_fro(got, r) <= TOL_BF16, name
