@@ -23,8 +23,9 @@ Sources (web pages, cited by title and section):
   dispatch / GEMM1 / LayerNorm-gate / GEMM2 / combine layer and its exchange
   example; "Cross-node tests and correctness" for the gradient check.
 * "Add dist GEMM attention and FFN backend" (torchtitan PR #4044), sections
-  "Structure" and "Row ordering": the SwiGLU column/row-parallel pair and the
-  (rank, batch, seq_local) order of gathered rows.
+  "Structure" and "Row ordering": the SwiGLU column/row-parallel pair, the
+  attention projections (column-parallel AllGatherLinear, row-parallel
+  LinearReduceScatter) and the (rank, batch, seq_local) order of gathered rows.
 
 Readings where the pages are silent are listed in the module docstrings of the
 functions concerned (U = first half of Z, biased variance, silu(x) = x*sigmoid(x),
@@ -596,3 +597,111 @@ def tp_swiglu_backward_weight_cols(x_shards_bits, w13_bits, w2_bits, dy_shards_b
     da = dh * b * (sig + a * sig * (1.0 - sig))
     db = dh * a * sig
     return dict(dw2=dY.T @ h, dw1=da.T @ X, dw3=db.T @ X)
+
+
+# --------------------------------------------------------------------------
+# Attention projections: the column-parallel AllGatherLinear (the fused QKV
+# projection) and the row-parallel LinearReduceScatter (the output projection
+# wo), "Add dist GEMM attention and FFN backend" (torchtitan PR #4044),
+# sections "Structure" and "Row ordering".  Both keep the stock parameter
+# layout: weight [out, in]; the column-parallel shard s is the row block
+# [s*out/W, (s+1)*out/W) of the weight (and of the bias), the row-parallel
+# shard s is the column block [s*in/W, (s+1)*in/W).
+# --------------------------------------------------------------------------
+
+def _gather_rows(x_shards):
+    """All-gather of sequence shards [W, bsz, S/W, f] -> rows (rank, seq_local, batch)."""
+    Wn, b_, sl, f = x_shards.shape
+    return x_shards.transpose(0, 2, 1, 3).reshape(Wn * sl * b_, f)
+
+
+def _scatter_rows(Y, Wn, b_):
+    """Inverse of _gather_rows: rows (rank, seq_local, batch) -> [W, bsz, S/W, f]."""
+    sl = Y.shape[0] // (Wn * b_)
+    return Y.reshape(Wn, sl, b_, -1).transpose(0, 2, 1, 3)
+
+
+def allgather_linear(x_shards, weight, bias, W: int, decoded: bool = False) -> np.ndarray:
+    """Column-parallel linear over W shards: every rank gathers all sequence
+    shards and multiplies by its own block of output features.
+
+    x_shards [W, bsz, S/W, in]; weight [out, in]; bias [out] or None.
+    Returns float64 [W, S*bsz, out/W]: rank s's output Y_s = X W_s^T + b_s,
+    rows in gathered order (rank, seq_local, batch).
+    """
+    f = (lambda a: np.asarray(a, dtype=np.float64)) if decoded else bf16_to_f64
+    X = _gather_rows(f(np.asarray(x_shards)))
+    Wt = f(np.asarray(weight))
+    bt = None if bias is None else f(np.asarray(bias))
+    F = Wt.shape[0] // W
+    out = []
+    for s in range(W):
+        Ys = X @ Wt[s * F:(s + 1) * F].T
+        if bt is not None:
+            Ys = Ys + bt[s * F:(s + 1) * F]
+        out.append(Ys)
+    return np.stack(out)
+
+
+def linear_reduce_scatter(a_ranks, weight, bias, W: int, bsz: int = 1, decoded: bool = False) -> np.ndarray:
+    """Row-parallel linear over W shards: each rank multiplies its block of
+    input features by its block of weight columns, the partial products are
+    summed (reduce) and the rows split back into sequence shards (scatter).
+
+    a_ranks [W, S*bsz, in/W] (rank s's input features for all gathered rows,
+    in gathered order); weight [out, in]; bias [out] or None, added once to the
+    sum.  Returns float64 y_shards [W, bsz, S/W, out].
+    """
+    f = (lambda a: np.asarray(a, dtype=np.float64)) if decoded else bf16_to_f64
+    A = f(np.asarray(a_ranks))
+    Wt = f(np.asarray(weight))
+    K = A.shape[2]
+    Y = np.zeros((A.shape[1], Wt.shape[0]))
+    for s in range(W):
+        Y += A[s] @ Wt[:, s * K:(s + 1) * K].T        # partial of shard s, then the sum
+    if bias is not None:
+        Y = Y + f(np.asarray(bias))
+    return _scatter_rows(Y, W, bsz)
+
+
+def allgather_linear_backward(x_shards, weight, dy_ranks, W: int, decoded: bool = False) -> dict:
+    """Gradients of allgather_linear given dY_s [W, S*bsz, out/W].
+
+    Per rank: dW_s = dY_s^T X, db_s = sum over rows of dY_s, and the rank's
+    share of dX, dY_s W_s; the shares are summed (the transpose of the
+    all-gather is a reduce-scatter) and scattered to [W, bsz, S/W, in].
+    Returns dx_shards, d_weight [out, in], d_bias [out].
+    """
+    f = (lambda a: np.asarray(a, dtype=np.float64)) if decoded else bf16_to_f64
+    xs = f(np.asarray(x_shards))
+    Wn, b_ = xs.shape[0], xs.shape[1]
+    X = _gather_rows(xs)
+    Wt = f(np.asarray(weight))
+    dY = f(np.asarray(dy_ranks))
+    F = Wt.shape[0] // W
+    dX = np.zeros_like(X)
+    dW = np.zeros_like(Wt)
+    db = np.zeros(Wt.shape[0])
+    for s in range(W):
+        dX += dY[s] @ Wt[s * F:(s + 1) * F]
+        dW[s * F:(s + 1) * F] = dY[s].T @ X
+        db[s * F:(s + 1) * F] = dY[s].sum(axis=0)
+    return dict(dx=_scatter_rows(dX, Wn, b_), d_weight=dW, d_bias=db)
+
+
+def linear_reduce_scatter_backward(a_ranks, weight, dy_shards, W: int, decoded: bool = False) -> dict:
+    """Gradients of linear_reduce_scatter given dy_shards [W, bsz, S/W, out].
+
+    dY is all-gathered back to rows in gathered order (the transpose of the
+    reduce-scatter); each rank gets dA_s = dY W_s (its block of weight
+    columns) and dW_s = dY^T A_s; d_bias = sum over rows of dY.
+    Returns da_ranks [W, S*bsz, in/W], d_weight [out, in], d_bias [out].
+    """
+    f = (lambda a: np.asarray(a, dtype=np.float64)) if decoded else bf16_to_f64
+    A = f(np.asarray(a_ranks))
+    Wt = f(np.asarray(weight))
+    dY = _gather_rows(f(np.asarray(dy_shards)))
+    K = A.shape[2]
+    dA = np.stack([dY @ Wt[:, s * K:(s + 1) * K] for s in range(W)])
+    dW = np.concatenate([dY.T @ A[s] for s in range(W)], axis=1)
+    return dict(da=dA, d_weight=dW, d_bias=dY.sum(axis=0))

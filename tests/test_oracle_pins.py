@@ -499,3 +499,115 @@ def test_tp_swiglu_backward_matches_torch_autograd_and_subsets():
         s_, cc = divmod(c, Fs)
         assert np.allclose(wc["dw1"][j], full["dw13"][s_, cc], rtol=1e-12, atol=1e-12)
         assert np.allclose(wc["dw3"][j], full["dw13"][s_, Fs + cc], rtol=1e-12, atol=1e-12)
+
+
+# ------------------------------------------------------------------ attention projections
+
+def test_allgather_linear_hand_computed():
+    # W = 2 ranks, bsz = 1, one token each, in = 2, out = 2 (one feature per rank)
+    x = np.array([[[[1.0, 2.0]]], [[[3.0, -1.0]]]])            # [W, bsz, S/W, in]
+    w = np.array([[1.0, 1.0], [2.0, -1.0]])                    # [out, in]
+    b = np.array([0.5, -0.5])
+    y = O.allgather_linear(x, w, b, W=2, decoded=True)         # [W, rows, out/W]
+    # gathered rows: (1, 2), (3, -1); rank 0 owns feature 0: x0+x1+0.5, rank 1 feature 1: 2x0-x1-0.5
+    assert np.array_equal(y[0, :, 0], [3.5, 2.5])
+    assert np.array_equal(y[1, :, 0], [-0.5, 6.5])
+
+
+def test_linear_reduce_scatter_hand_computed():
+    # rank 0 holds input feature 0, rank 1 feature 1, for both gathered rows
+    a = np.array([[[1.0], [3.0]], [[2.0], [-1.0]]])            # [W, rows, in/W]
+    w = np.array([[1.0, 1.0], [2.0, -1.0]])
+    b = np.array([0.5, -0.5])
+    y = O.linear_reduce_scatter(a, w, b, W=2, bsz=1, decoded=True)   # [W, bsz, S/W, out]
+    assert np.array_equal(y[0, 0, 0], [3.5, -0.5])
+    assert np.array_equal(y[1, 0, 0], [2.5, 6.5])
+
+
+@pytest.mark.parametrize("W,bsz", [(1, 1), (2, 3), (4, 2)])
+def test_attention_projections_match_unsharded_torch_linear(W, bsz):
+    rng = np.random.default_rng(W * 10 + bsz)
+    S, din, dout = 8, 16, 24
+    x = rng.standard_normal((W, bsz, S // W, din))
+    wq = rng.standard_normal((dout, din))
+    bq = rng.standard_normal(dout)
+    wo = rng.standard_normal((din, dout))
+    bo = rng.standard_normal(din)
+    # column-parallel: concatenating the ranks' feature blocks gives the unsharded linear
+    # of the gathered rows (rank, seq_local, batch)
+    X = torch.from_numpy(x).permute(0, 2, 1, 3).reshape(-1, din)
+    ref = F.linear(X, torch.from_numpy(wq), torch.from_numpy(bq)).numpy()
+    y = O.allgather_linear(x, wq, bq, W=W, decoded=True)
+    assert np.allclose(np.concatenate(list(y), axis=1), ref, rtol=1e-12, atol=1e-12)
+    # row-parallel on the column-parallel output: the unsharded composition, scattered back
+    z = O.linear_reduce_scatter(y, wo, bo, W=W, bsz=bsz, decoded=True)
+    ref2 = F.linear(torch.from_numpy(ref), torch.from_numpy(wo), torch.from_numpy(bo))
+    ref2 = ref2.reshape(W, S // W, bsz, din).permute(0, 2, 1, 3).numpy()
+    assert np.allclose(z, ref2, rtol=1e-11, atol=1e-11)
+
+
+def test_attention_projection_backward_finite_differences():
+    rng = np.random.default_rng(5)
+    W, bsz, sl, din, dout = 2, 2, 2, 3, 4
+    x = rng.standard_normal((W, bsz, sl, din))
+    w = rng.standard_normal((dout, din))
+    b = rng.standard_normal(dout)
+    dy = rng.standard_normal((W, W * sl * bsz, dout // W))
+    g = O.allgather_linear_backward(x, w, dy, W=W, decoded=True)
+
+    def loss_col():
+        return float((O.allgather_linear(x, w, b, W=W, decoded=True) * dy).sum())
+    a = rng.standard_normal((W, W * sl * bsz, 2))              # 2 input features per rank
+    wo = rng.standard_normal((dout, 2 * W))
+    bo = rng.standard_normal(dout)
+    dz = rng.standard_normal((W, bsz, sl, dout))
+    g2 = O.linear_reduce_scatter_backward(a, wo, dz, W=W, decoded=True)
+
+    def loss_row():
+        return float((O.linear_reduce_scatter(a, wo, bo, W=W, bsz=bsz, decoded=True) * dz).sum())
+    h = 1e-6
+    for loss, pairs in ((loss_col, ((x, g["dx"]), (w, g["d_weight"]), (b, g["d_bias"]))),
+                        (loss_row, ((a, g2["da"]), (wo, g2["d_weight"]), (bo, g2["d_bias"])))):
+        for arr, ga in pairs:
+            flat, gf = arr.reshape(-1), ga.reshape(-1)
+            for i in range(flat.size):
+                old = flat[i]
+                flat[i] = old + h
+                lp = loss()
+                flat[i] = old - h
+                lm = loss()
+                flat[i] = old
+                num = (lp - lm) / (2 * h)
+                assert abs(num - gf[i]) <= 1e-6 * max(1.0, abs(num)), (i, num, gf[i])
+
+
+def test_attention_projection_backward_matches_torch_autograd():
+    rng = np.random.default_rng(9)
+    W, bsz, S, din, dout = 4, 2, 8, 16, 12
+    x = torch.from_numpy(rng.standard_normal((W, bsz, S // W, din))).requires_grad_(True)
+    w = torch.from_numpy(rng.standard_normal((dout, din))).requires_grad_(True)
+    b = torch.from_numpy(rng.standard_normal(dout)).requires_grad_(True)
+    X = x.permute(0, 2, 1, 3).reshape(-1, din)
+    y = F.linear(X, w, b)
+    dy = torch.from_numpy(rng.standard_normal(y.shape))
+    y.backward(dy)
+    F_ = dout // W
+    dy_ranks = np.stack([dy.numpy()[:, s * F_:(s + 1) * F_] for s in range(W)])
+    g = O.allgather_linear_backward(x.detach().numpy(), w.detach().numpy(), dy_ranks, W=W, decoded=True)
+    assert np.allclose(g["dx"], x.grad.numpy(), rtol=1e-11, atol=1e-11)
+    assert np.allclose(g["d_weight"], w.grad.numpy(), rtol=1e-11, atol=1e-11)
+    assert np.allclose(g["d_bias"], b.grad.numpy(), rtol=1e-11, atol=1e-11)
+    # row-parallel: the input is the ranks' feature blocks of an unsharded activation
+    A = torch.from_numpy(rng.standard_normal((W * S // W * bsz, din))).requires_grad_(True)
+    wo = torch.from_numpy(rng.standard_normal((dout, din))).requires_grad_(True)
+    bo = torch.from_numpy(rng.standard_normal(dout)).requires_grad_(True)
+    z = F.linear(A, wo, bo)
+    dz = torch.from_numpy(rng.standard_normal(z.shape))
+    z.backward(dz)
+    K = din // W
+    a_ranks = np.stack([A.detach().numpy()[:, s * K:(s + 1) * K] for s in range(W)])
+    dz_shards = dz.numpy().reshape(W, S // W, bsz, dout).transpose(0, 2, 1, 3)
+    g2 = O.linear_reduce_scatter_backward(a_ranks, wo.detach().numpy(), dz_shards, W=W, decoded=True)
+    assert np.allclose(np.concatenate(list(g2["da"]), axis=1), A.grad.numpy(), rtol=1e-11, atol=1e-11)
+    assert np.allclose(g2["d_weight"], wo.grad.numpy(), rtol=1e-11, atol=1e-11)
+    assert np.allclose(g2["d_bias"], bo.grad.numpy(), rtol=1e-11, atol=1e-11)
