@@ -35,6 +35,7 @@ sys.path.insert(0, ROOT)
 FP8 = dict(M=4096, N=4096, K=4096, alpha=0.5, beta=1.0, seed=1)
 FFN = dict(P=8, B=512, T=64, D=1280, k=6, seed=42, dy_seed=43)
 TP = dict(S=8192, d=4096, ffn=14336, W=8, seed=7)
+ATTN = dict(qkv_out=4096 + 2 * 1024)  # fused QKV rows of Llama-3-8B: 32 query + 2 x 8 key/value heads of 128
 
 MEASURED_PEAKS = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK_PEAKS = dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0)
@@ -196,6 +197,17 @@ class Workload:
         self.tp_bws = torch.empty(lib.dg_tp_swiglu_bwd_workspace_bytes(TP["S"], TP["d"], TP["ffn"], TP["W"], 1),
                                   dtype=torch.uint8, device=dev)
         self.tp_grads = dict(x=torch.empty_like(self.xs), w13=torch.empty_like(self.w13), w2=torch.empty_like(self.w2))
+        # attention projections at the same Llama-3-8B shape (32 query / 8 key-value heads of 128), no bias
+        S, W, d = TP["S"], TP["W"], TP["d"]
+        gen = torch.Generator(device=dev).manual_seed(TP["seed"] + 2)
+        self.attn_x = torch.randn((W, 1, S // W, d), generator=gen, device=dev).to(bf)
+        self.wqkv = ((torch.rand((ATTN["qkv_out"], d), generator=gen, device=dev) - 0.5) * (2 / d ** 0.5)).to(bf)
+        self.attn_a = torch.randn((W, 1, S // W, d), generator=gen, device=dev).to(bf)
+        self.wo = ((torch.rand((d, d), generator=gen, device=dev) - 0.5) * (2 / d ** 0.5)).to(bf)
+        self.qkv = torch.empty((W, 1, S // W, ATTN["qkv_out"]), dtype=bf, device=dev)
+        self.attn_y = torch.empty((W, 1, S // W, d), dtype=bf, device=dev)
+        self.dqkv = torch.randn_like(self.qkv, dtype=torch.float32).to(bf)
+        self.dattn_y = torch.randn_like(self.attn_y, dtype=torch.float32).to(bf)
 
     def inputs(self):
         return [self.A, self.B, self.C, self.x, *self.params.values(), self.dY, self.xs, self.w13, self.w2]
@@ -215,6 +227,13 @@ class Workload:
         if marks is not None:
             marks[2].record()
         dg.tp_swiglu(self.xs, self.w13, self.w2, workspace=self.tp_ws, out=self.y)
+
+    def attn_proj(self):
+        dg = self.dg
+        dg.tp_linear(self.attn_x, self.wqkv, out=self.qkv)
+        dg.tp_linear(self.attn_a, self.wo, out=self.attn_y)
+        dg.tp_linear_backward(self.attn_a, self.wo, self.dattn_y)
+        dg.tp_linear_backward(self.attn_x, self.wqkv, self.dqkv)
 
     def tp_backward(self):
         self.dg.tp_swiglu_backward(self.xs, self.w13, self.w2, self.tp_dy, workspace=self.tp_bws,
@@ -441,6 +460,7 @@ def run_dg(args, rank, world):
     # the TP SwiGLU backward (recompute [a|b], dh, gate backward, dw2, dX, dw13)
     extra = run_fp8_alone(w, args, dev, peaks)
     extra.update(run_tp_backward(w, args, dev, peaks))
+    extra.update(run_attn_proj(w, args, dev, peaks))
 
     # end to end: inputs from pinned host memory in, results back to pinned host memory
     e2e = run_e2e(w, args, dev, step_flops, world)
@@ -529,6 +549,39 @@ def run_tp_backward(w, args, dev, peaks):
     return {"tp_swiglu_bwd": {
         "ms": round(ms, 4), "tflops": round(tf, 2), "peak_tflops": peaks["bf16_tflops"],
         "frac_of_peak": round(tf / peaks["bf16_tflops"], 4), "iters": iters,
+        "kernels": {e["name"]: {"launches": e["launches"], "ms_per_launch": round(e["total_ms"] / e["launches"], 4)}
+                    for e in trace}}}
+
+
+def run_attn_proj(w, args, dev, peaks):
+    """Attention projections at the Llama-3-8B shape over W=8 shards (outside the step):
+    fused QKV and wo forward, then both backward (dx and d_weight)."""
+    import torch
+    dg = w.dg
+    for _ in range(max(args.warmup, 2)):
+        w.attn_proj()
+    iters = 5
+    stream = torch.cuda.current_stream(dev)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    torch.cuda.synchronize(dev)
+    dg.trace_begin()
+    ev[0].record(stream)
+    for _ in range(iters):
+        w.attn_proj()
+    ev[1].record(stream)
+    torch.cuda.synchronize(dev)
+    trace = dg.trace_end()
+    st, code = dg.device_status(dev)
+    if st != 0:
+        raise RuntimeError(f"device error word after the attention projections: {code:#x}")
+    ms = ev[0].elapsed_time(ev[1]) / iters
+    S, d = TP["S"], TP["d"]
+    flops = 3 * 2.0 * S * d * (ATTN["qkv_out"] + d)  # forward, dx and d_weight of both projections
+    tf = flops / (ms * 1e-3) / 1e12
+    return {"attn_proj_fwd_bwd": {
+        "ms": round(ms, 4), "tflops": round(tf, 2), "peak_tflops": peaks["bf16_tflops"],
+        "frac_of_peak": round(tf / peaks["bf16_tflops"], 4), "iters": iters,
+        "shape": f"S={S}, d={d}, QKV out {ATTN['qkv_out']}, wo {d}x{d}, W={TP['W']}, no bias",
         "kernels": {e["name"]: {"launches": e["launches"], "ms_per_launch": round(e["total_ms"] / e["launches"], 4)}
                     for e in trace}}}
 

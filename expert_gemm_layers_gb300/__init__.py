@@ -9,15 +9,19 @@ TMA/mbarrier pipelines):
                 autograd), P logical ranks in one GPU's memory
 * tp_swiglu     the SwiGLU column/row-parallel pair over W shards (forward,
                 backward, autograd)
+* tp_linear     the attention projections (column-parallel QKV, row-parallel
+                wo) over W shards (forward, backward, autograd)
 
 The library is loaded lazily on first use and fails loudly if it is missing.
 """
 from .ops import (A2AFFN, FFN_PARAM_NAMES, TPSwiGLU, a2a_combine, a2a_dispatch, a2a_ffn, a2a_ffn_backward,
                   a2a_ffn_forward, debug_wait_timeout, device_status, ffn_shape, gemm_fp8, tp_swiglu,
-                  tp_swiglu_backward, tp_swiglu_layer, trace_begin, trace_end)
+                  tp_linear, tp_linear_backward, tp_linear_layer, TPLinear, tp_swiglu_backward, tp_swiglu_layer,
+                  trace_begin, trace_end)
 
 __all__ = [
     "A2AFFN", "FFN_PARAM_NAMES", "a2a_combine", "a2a_dispatch", "a2a_ffn", "a2a_ffn_backward",
     "a2a_ffn_forward", "debug_wait_timeout", "device_status", "ffn_shape", "gemm_fp8", "tp_swiglu",
-    "tp_swiglu_backward", "TPSwiGLU", "tp_swiglu_layer", "trace_begin", "trace_end",
+    "tp_swiglu_backward", "TPSwiGLU", "tp_swiglu_layer", "tp_linear", "tp_linear_backward", "TPLinear",
+    "tp_linear_layer", "trace_begin", "trace_end",
 ]

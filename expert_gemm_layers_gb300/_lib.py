@@ -55,6 +55,8 @@ SIGNATURES = {
     "dg_tp_swiglu_bwd_workspace_bytes": (_sz, [_i64, _i64, _i64, _i32, _i32]),
     "dg_tp_swiglu_bwd": (ctypes.c_int, [_i64, _i64, _i64, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz,
                                         _vp]),
+    "dg_tp_linear_fwd": (ctypes.c_int, [_i64, _i64, _i64, _vp, _vp, _vp, _vp, _vp]),
+    "dg_tp_linear_bwd": (ctypes.c_int, [_i64, _i64, _i64, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
     "dg_tp_swiglu_noalloc": (ctypes.c_int, [_i64, _i64, _i64, _i32, _i32, _vp, _vp, _vp, _vp, _vp]),
     "dg_trace_begin": (ctypes.c_int, []),
     "dg_trace_begin_only": (ctypes.c_int, [ctypes.c_char_p]),

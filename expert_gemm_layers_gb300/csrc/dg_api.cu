@@ -193,6 +193,7 @@ dg_status run_gemm(GemmVariant v, const CUtensorMap& a, const CUtensorMap& b, co
     case GV_BF16_KM_LNSTATS: e = launch_gemm_bf16_km_lnstats(a, b, d, c, p, grid, s); break;
     case GV_BF16_KM_STORE: e = launch_gemm_bf16_km_store(a, b, d, c, p, grid, s); break;
     case GV_FP8_KK_N224: e = launch_gemm_fp8_kk_n224(a, b, d, c, p, grid, s); break;
+    case GV_BF16_KK_BIAS: e = launch_gemm_bf16_kk_bias(a, b, d, c, p, grid, s); break;
     default: return fail(DG_ERR_UNSUPPORTED, "unknown GEMM variant");
   }
   if (e != cudaSuccess) return cuda_fail(e, "GEMM launch");
@@ -862,6 +863,129 @@ dg_status dg_tp_swiglu_bwd(int64_t S, int64_t d, int64_t ffn, int32_t W, int32_t
   p.a_g = p.b_g = p.d_g = G_OUTER;
   return run_gemm(GV_BF16_MM_STORE, mdab_t, mx_n, mdw13, mdw13, p, dev, s, "tp_bwd_dw13",
                   2.0 * (2.0 * r * ff + r * dd + 2.0 * ff * dd));
+}
+
+// ------------------------------------------------------------------ TP linear (attention projections)
+
+namespace {
+
+dg_status check_linear(int64_t rows, int64_t in_f, int64_t out_f, const char* what) {
+  if (rows < 1 || in_f < 1 || out_f < 1)
+    return fail(DG_ERR_INVALID_ARGUMENT, "%s: rows, in_features, out_features must be >= 1", what);
+  if (in_f % 8 || out_f % 8)
+    return fail(DG_ERR_INVALID_ARGUMENT, "%s: in_features and out_features must be multiples of 8", what);
+  if (rows > 0x7fffffff || in_f > 0x7fffffff || out_f > 0x7fffffff)
+    return fail(DG_ERR_UNSUPPORTED, "%s: sizes beyond 2^31-1", what);
+  return DG_OK;
+}
+
+}  // namespace
+
+dg_status dg_tp_linear_fwd(int64_t rows, int64_t in_f, int64_t out_f, const void* x, const void* weight,
+                           const void* bias, void* y, void* stream) {
+  dg_status st = check_linear(rows, in_f, out_f, "tp_linear_fwd");
+  if (st != DG_OK) return st;
+  const void* ptrs[] = {x, weight, y};
+  const char* names[] = {"x", "weight", "y"};
+  if (const char* n = ptr_name_null(ptrs, names, 3)) return fail(DG_ERR_INVALID_ARGUMENT, "tp_linear_fwd: %s is NULL", n);
+  if (const char* n = ptr_name_unaligned(ptrs, names, 3))
+    return fail(DG_ERR_INVALID_ARGUMENT, "tp_linear_fwd: %s is not 16-byte aligned", n);
+  if (bias && !aligned16(bias)) return fail(DG_ERR_INVALID_ARGUMENT, "tp_linear_fwd: bias is not 16-byte aligned");
+  const size_t xb = static_cast<size_t>(rows) * in_f * 2, wb = static_cast<size_t>(out_f) * in_f * 2;
+  const size_t yb = static_cast<size_t>(rows) * out_f * 2;
+  if (overlaps(y, yb, x, xb) || overlaps(y, yb, weight, wb) || (bias && overlaps(y, yb, bias, out_f * 2)))
+    return fail(DG_ERR_INVALID_ARGUMENT, "tp_linear_fwd: y overlaps an input");
+  DeviceInfo dev;
+  if ((st = device_info(&dev)) != DG_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const uint64_t R = rows, I = in_f, O = out_f;
+  // y = x weight^T (+ bias): one K/K GEMM; every rank's feature block (column
+  // parallel) or every rank's partial product (row parallel, summed in the K
+  // loop) is part of it.
+  CUtensorMap mx, mw, my;
+  if ((st = make_map_3d(&mx, true, x, I, R, 1, I * 2, R * I * 2, 64, 128, 1, "x")) != DG_OK) return st;
+  if ((st = make_map_3d(&mw, true, weight, I, O, 1, I * 2, O * I * 2, 64, kKMajorBRows, 1, "weight")) != DG_OK)
+    return st;
+  if ((st = make_map_3d(&my, true, y, O, R, 1, O * 2, R * O * 2, 64, 32, 1, "y")) != DG_OK) return st;
+  GemmParams p{};
+  p.G = 1;
+  p.M = static_cast<int32_t>(rows);
+  p.N = static_cast<int32_t>(out_f);
+  p.K = static_cast<int32_t>(in_f);
+  p.a_g = p.b_g = p.d_g = G_OUTER;
+  p.bias = static_cast<const __nv_bfloat16*>(bias);
+  p.bias_g_stride = 0;
+  const double bytes = static_cast<double>(xb) + wb + yb + (bias ? 2.0 * out_f : 0.0);
+  return run_gemm(bias ? GV_BF16_KK_BIAS : GV_BF16_KK_STORE, mx, mw, my, my, p, dev, s, "tp_linear_fwd", bytes);
+}
+
+dg_status dg_tp_linear_bwd(int64_t rows, int64_t in_f, int64_t out_f, const void* x, const void* weight,
+                           const void* dy, void* dx, void* d_weight, void* d_bias, void* stream) {
+  dg_status st = check_linear(rows, in_f, out_f, "tp_linear_bwd");
+  if (st != DG_OK) return st;
+  const void* ptrs[] = {x, weight, dy};
+  const char* names[] = {"x", "weight", "dy"};
+  if (const char* n = ptr_name_null(ptrs, names, 3)) return fail(DG_ERR_INVALID_ARGUMENT, "tp_linear_bwd: %s is NULL", n);
+  if (const char* n = ptr_name_unaligned(ptrs, names, 3))
+    return fail(DG_ERR_INVALID_ARGUMENT, "tp_linear_bwd: %s is not 16-byte aligned", n);
+  if ((dx && !aligned16(dx)) || (d_weight && !aligned16(d_weight)) || (d_bias && !aligned16(d_bias)))
+    return fail(DG_ERR_INVALID_ARGUMENT, "tp_linear_bwd: an output is not 16-byte aligned");
+  const size_t xb = static_cast<size_t>(rows) * in_f * 2, wb = static_cast<size_t>(out_f) * in_f * 2;
+  const size_t yb = static_cast<size_t>(rows) * out_f * 2, bb = static_cast<size_t>(out_f) * 2;
+  const void* outs[] = {dx, d_weight, d_bias};
+  const size_t outs_n[] = {xb, wb, bb};
+  const void* all[] = {x, weight, dy, dx, d_weight, d_bias};
+  const size_t all_n[] = {xb, wb, yb, xb, wb, bb};
+  for (int i = 0; i < 3; ++i)
+    for (int j = 0; j < 6; ++j)
+      if (outs[i] && all[j] && j != 3 + i && overlaps(outs[i], outs_n[i], all[j], all_n[j]))
+        return fail(DG_ERR_INVALID_ARGUMENT, "tp_linear_bwd: outputs and inputs overlap");
+  DeviceInfo dev;
+  if ((st = device_info(&dev)) != DG_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const uint64_t R = rows, I = in_f, O = out_f;
+  const double r = static_cast<double>(rows), fi = static_cast<double>(in_f), fo = static_cast<double>(out_f);
+  if (dx) {
+    // dx = dy weight: B = weight read N-major ([out, in], in contiguous)
+    CUtensorMap mdy, mw, mdx;
+    if ((st = make_map_3d(&mdy, true, dy, O, R, 1, O * 2, R * O * 2, 64, 128, 1, "dy")) != DG_OK) return st;
+    if ((st = make_map_3d(&mw, true, weight, I, O, 1, I * 2, O * I * 2, 64, 64, 1, "weight (N-major)")) != DG_OK)
+      return st;
+    if ((st = make_map_3d(&mdx, true, dx, I, R, 1, I * 2, R * I * 2, 64, 32, 1, "dx")) != DG_OK) return st;
+    GemmParams p{};
+    p.G = 1;
+    p.M = static_cast<int32_t>(rows);
+    p.N = static_cast<int32_t>(in_f);
+    p.K = static_cast<int32_t>(out_f);
+    p.a_g = p.b_g = p.d_g = G_OUTER;
+    if ((st = run_gemm(GV_BF16_KM_STORE, mdy, mw, mdx, mdx, p, dev, s, "tp_linear_bwd_dx",
+                       2.0 * (r * fo + fo * fi + r * fi))) != DG_OK)
+      return st;
+  }
+  if (d_weight) {
+    // d_weight = dy^T x: both operands MN-major, the contraction over rows
+    CUtensorMap mdy_t, mx_n, mdw;
+    if ((st = make_map_3d(&mdy_t, true, dy, O, R, 1, O * 2, R * O * 2, 64, 64, 1, "dy^T")) != DG_OK) return st;
+    if ((st = make_map_3d(&mx_n, true, x, I, R, 1, I * 2, R * I * 2, 64, 64, 1, "x (N-major)")) != DG_OK) return st;
+    if ((st = make_map_3d(&mdw, true, d_weight, I, O, 1, I * 2, O * I * 2, 64, 32, 1, "d_weight")) != DG_OK)
+      return st;
+    GemmParams p{};
+    p.G = 1;
+    p.M = static_cast<int32_t>(out_f);
+    p.N = static_cast<int32_t>(in_f);
+    p.K = static_cast<int32_t>(rows);
+    p.a_g = p.b_g = p.d_g = G_OUTER;
+    if ((st = run_gemm(GV_BF16_MM_STORE, mdy_t, mx_n, mdw, mdw, p, dev, s, "tp_linear_bwd_dw",
+                       2.0 * (r * fo + r * fi + fo * fi))) != DG_OK)
+      return st;
+  }
+  if (d_bias) {
+    TraceScope trace("tp_linear_bwd_db", s, 0.0, r * fo * 2.0 + fo * 2.0);
+    cudaError_t e = launch_column_sum(dy, d_bias, 1, static_cast<int>(rows), static_cast<int>(out_f), 0,
+                                      static_cast<int64_t>(out_f), dev, s);
+    if (e != cudaSuccess) return cuda_fail(e, "tp_linear_bwd: column-sum launch");
+  }
+  return DG_OK;
 }
 
 dg_status dg_trace_begin(void) { return dg_trace_begin_only(nullptr); }

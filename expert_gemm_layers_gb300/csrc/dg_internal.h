@@ -39,7 +39,8 @@ enum GemmVariant : int {
   GV_BF16_KK_SWIGLU = 4, // bf16, A and B K-major, paired silu(a)*b epilogue
   GV_BF16_KM_LNSTATS = 5, // bf16, A K-major, B MN-major, bias + per-tile LayerNorm statistics
   GV_BF16_KM_STORE = 6,   // bf16, A K-major, B MN-major, plain store
-  GV_FP8_KK_N224 = 7      // GV_FP8_KK with 224-column tiles
+  GV_FP8_KK_N224 = 7,     // GV_FP8_KK with 224-column tiles
+  GV_BF16_KK_BIAS = 8     // bf16, A and B K-major, bias epilogue
 };
 
 // Tiles along N of one problem for this variant (output columns per tile).
@@ -83,6 +84,8 @@ cudaError_t launch_gemm_bf16_km_lnstats(const CUtensorMap&, const CUtensorMap&, 
                                         const CUtensorMap&, const GemmParams&, int num_sms, cudaStream_t);
 cudaError_t launch_gemm_bf16_km_store(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
                                       const CUtensorMap&, const GemmParams&, int num_sms, cudaStream_t);
+cudaError_t launch_gemm_bf16_kk_bias(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
+                                     const CUtensorMap&, const GemmParams&, int num_sms, cudaStream_t);
 cudaError_t launch_gemm_fp8_kk_n224(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
                                     const GemmParams&, int num_sms, cudaStream_t);
 // Co-resident CTA pairs (or CTAs) of the e4m3 GEMM on the current device.

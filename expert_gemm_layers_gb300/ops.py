@@ -15,7 +15,7 @@ from ._lib import FFNShape, TraceEntry, check, load
 __all__ = [
     "gemm_fp8", "ffn_shape", "a2a_ffn_forward", "a2a_ffn_backward", "A2AFFN", "a2a_ffn",
     "a2a_dispatch", "a2a_combine", "tp_swiglu", "tp_swiglu_backward", "TPSwiGLU", "tp_swiglu_layer",
-    "device_status", "debug_wait_timeout",
+    "tp_linear", "tp_linear_backward", "TPLinear", "tp_linear_layer", "device_status", "debug_wait_timeout",
     "FFN_PARAM_NAMES", "trace_begin", "trace_end",
 ]
 
@@ -259,6 +259,78 @@ class TPSwiGLU(torch.autograd.Function):
 def tp_swiglu_layer(x_shards, w13, w2):
     """Differentiable SwiGLU pair (see TPSwiGLU)."""
     return TPSwiGLU.apply(x_shards, w13, w2)
+
+
+# ------------------------------------------------------------------ attention projections
+
+def tp_linear(x: torch.Tensor, weight: torch.Tensor, bias: torch.Tensor | None = None,
+              out: torch.Tensor | None = None) -> torch.Tensor:
+    """y = x @ weight^T (+ bias) over all tensor-parallel shards at once.
+
+    The column-parallel all-gather linear (fused QKV) and the row-parallel
+    linear reduce-scatter (wo) in the stock layout: x [..., in] (e.g. sequence
+    shards [W, bsz, S/W, in]), weight [out, in], bias [out]; rank s's block is
+    a column block of the output (column parallel) or of x and weight (row
+    parallel).  Returns [..., out] with the rows of x in place."""
+    lib = load()
+    in_f = x.shape[-1]
+    out_f = weight.shape[0]
+    dev = x.device
+    _need(x, "x", torch.bfloat16)
+    _need(weight, "weight", torch.bfloat16, (out_f, in_f), dev)
+    if bias is not None:
+        _need(bias, "bias", torch.bfloat16, (out_f,), dev)
+    rows = x.numel() // in_f
+    if out is None:
+        out = torch.empty((*x.shape[:-1], out_f), dtype=torch.bfloat16, device=dev)
+    with torch.cuda.device(dev):
+        check(lib.dg_tp_linear_fwd(rows, in_f, out_f, _ptr(x), _ptr(weight),
+                                   None if bias is None else _ptr(bias), _ptr(out), ctypes.c_void_p(_stream(dev))))
+    return out
+
+
+def tp_linear_backward(x: torch.Tensor, weight: torch.Tensor, dy: torch.Tensor, need_dx: bool = True,
+                       need_dw: bool = True, need_db: bool = False) -> dict:
+    """Gradients of tp_linear: "x" = dy weight, "weight" = dy^T x, "bias" = column sums of dy."""
+    lib = load()
+    in_f = x.shape[-1]
+    out_f = weight.shape[0]
+    dev = x.device
+    _need(x, "x", torch.bfloat16)
+    _need(weight, "weight", torch.bfloat16, (out_f, in_f), dev)
+    _need(dy, "dy", torch.bfloat16, (*x.shape[:-1], out_f), dev)
+    rows = x.numel() // in_f
+    g = {}
+    g["x"] = torch.empty_like(x) if need_dx else None
+    g["weight"] = torch.empty_like(weight) if need_dw else None
+    g["bias"] = torch.empty(out_f, dtype=torch.bfloat16, device=dev) if need_db else None
+    p = lambda t: None if t is None else _ptr(t)
+    with torch.cuda.device(dev):
+        check(lib.dg_tp_linear_bwd(rows, in_f, out_f, _ptr(x), _ptr(weight), _ptr(dy), p(g["x"]), p(g["weight"]),
+                                   p(g["bias"]), ctypes.c_void_p(_stream(dev))))
+    return g
+
+
+class TPLinear(torch.autograd.Function):
+    """Autograd wrapper of tp_linear (gradients for x, weight and bias)."""
+
+    @staticmethod
+    def forward(ctx, x, weight, bias):
+        ctx.save_for_backward(x, weight)
+        ctx.has_bias = bias is not None
+        return tp_linear(x, weight, bias)
+
+    @staticmethod
+    def backward(ctx, dy):
+        x, weight = ctx.saved_tensors
+        g = tp_linear_backward(x, weight, dy.contiguous(), need_dx=ctx.needs_input_grad[0],
+                               need_dw=ctx.needs_input_grad[1], need_db=ctx.has_bias and ctx.needs_input_grad[2])
+        return g["x"], g["weight"], g["bias"]
+
+
+def tp_linear_layer(x, weight, bias=None):
+    """Differentiable tp_linear (see TPLinear)."""
+    return TPLinear.apply(x, weight, bias)
 
 
 # ------------------------------------------------------------------ diagnostics

@@ -236,6 +236,42 @@ dg_status dg_tp_swiglu_noalloc(int64_t S, int64_t d, int64_t ffn, int32_t W, int
                                void* y_shards, void* stream);
 
 /* ------------------------------------------------------------------------
+ * Attention projections over W tensor-parallel shards: the column-parallel
+ * all-gather linear (fused QKV) and the row-parallel linear reduce-scatter
+ * (output projection wo).
+ *
+ * Source: "Add dist GEMM attention and FFN backend" (torchtitan PR #4044),
+ * sections "Structure" and "Row ordering".  Both keep the stock parameter
+ * layout weight [out_features, in_features] (+ bias [out_features]).
+ *   column parallel: rank s owns weight rows [s*out/W, (s+1)*out/W) and
+ *     multiplies the all-gathered rows by them; its output is the column block
+ *     s of y.
+ *   row parallel: rank s owns input columns [s*in/W, (s+1)*in/W) and the same
+ *     weight columns; the ranks' partial products are summed (reduce) and the
+ *     rows split back into sequence shards (scatter).
+ * On one GPU both are y = x weight^T (+ bias) over all shards at once: the
+ * rank blocks are column blocks of x, y and weight, the shard sum of the row
+ * parallel form is the K loop, and gathering/scattering rows is the identity
+ * on memory order because every output row depends on its own input row only.
+ *
+ *   x [rows, in_features], y [rows, out_features]   (row-major, bf16)
+ *   weight [out_features, in_features], bias [out_features] or NULL
+ * dg_tp_linear_bwd writes dx = dy weight [rows, in], d_weight = dy^T x
+ * [out, in] and d_bias = column sums of dy [out]; any of the three may be NULL
+ * (not computed).  Outputs are overwritten.
+ * Requirements: rows, in_features, out_features >= 1; in_features and
+ * out_features multiples of 8; 16-byte aligned tensors; outputs disjoint from
+ * each other and from the inputs.
+ * ------------------------------------------------------------------------ */
+dg_status dg_tp_linear_fwd(int64_t rows, int64_t in_features, int64_t out_features,
+                           const void* x, const void* weight, const void* bias,
+                           void* y, void* stream);
+
+dg_status dg_tp_linear_bwd(int64_t rows, int64_t in_features, int64_t out_features,
+                           const void* x, const void* weight, const void* dy,
+                           void* dx, void* d_weight, void* d_bias, void* stream);
+
+/* ------------------------------------------------------------------------
  * Diagnostics.
  * dg_debug_wait_timeout launches one small kernel that waits, with the
  * library's bounded wait, on a barrier nothing will ever arrive at; after
