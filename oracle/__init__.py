@@ -705,3 +705,80 @@ def linear_reduce_scatter_backward(a_ranks, weight, dy_shards, W: int, decoded: 
     dA = np.stack([dY @ Wt[:, s * K:(s + 1) * K] for s in range(W)])
     dW = np.concatenate([dY.T @ A[s] for s in range(W)], axis=1)
     return dict(da=dA, d_weight=dW, d_bias=dY.sum(axis=0))
+
+
+# --------------------------------------------------------------------------
+# FP8 GEMMs inside the A2A FFN (forward).  The project statement lists
+# optional FP8 paths for the layer ("Public checks and instructor coverage")
+# without a recipe; the reading taken here: GEMM1 and GEMM2 run on e4m3
+# operands with fp32 accumulation; activations (the dispatched input rows and
+# Hl) carry one scale per row, weights one scale per output column; a scale is
+# amax / 448 (1 for an all-zero vector) and a code is the e4m3 value nearest to
+# x / scale, ties to the even code, saturating at +-448.  The code decision is
+# taken in fp32 (amax, the division and x / scale are binary32 operations), as
+# on the GPU.  Everything after the decoded codes is fp64.
+# --------------------------------------------------------------------------
+
+_E4M3_MAX = 448.0
+# non-negative finite e4m3 values in code order (codes 0x00..0x7e are increasing)
+_E4M3_POS_VALUES = _E4M3_TABLE[:0x7f]
+
+
+def e4m3_rne(x) -> np.ndarray:
+    """Codes (uint8) of the e4m3 values nearest to x: ties to the even code,
+    magnitudes above 448 (and infinities) saturate to +-448, NaN gives 0x7f."""
+    v = np.asarray(x, dtype=np.float64)
+    a = np.abs(v)
+    sat = np.minimum(np.nan_to_num(a, nan=0.0, posinf=_E4M3_MAX), _E4M3_MAX)
+    hi = np.searchsorted(_E4M3_POS_VALUES, sat, side="left")    # first value >= |x|
+    hi = np.minimum(hi, 0x7e)
+    lo = np.maximum(hi - 1, 0)
+    d_hi = _E4M3_POS_VALUES[hi] - sat
+    d_lo = sat - _E4M3_POS_VALUES[lo]
+    pick_hi = (d_hi < d_lo) | ((d_hi == d_lo) & (hi % 2 == 0))
+    code = np.where(_E4M3_POS_VALUES[hi] == sat, hi, np.where(pick_hi, hi, lo)).astype(np.uint8)
+    code = np.where(np.signbit(v), code | np.uint8(0x80), code).astype(np.uint8)
+    return np.where(np.isnan(v), np.uint8(0x7f), code).astype(np.uint8)
+
+
+def quantize_e4m3(x, axis: int):
+    """e4m3 codes and binary32 scales of x (binary32 values) with one scale per
+    slice along `axis` (axis=1: per row of a [rows, K] matrix; axis=0: per
+    column of a [K, N] matrix)."""
+    x32 = np.asarray(x, dtype=np.float32)
+    amax = np.max(np.abs(x32), axis=axis)
+    scale = np.where(amax > 0, amax / np.float32(_E4M3_MAX), np.float32(1.0)).astype(np.float32)
+    s = scale[:, None] if axis == 1 else scale[None, :]
+    return e4m3_rne((x32 / s).astype(np.float32)), scale
+
+
+def ffn_forward_fp8(sh: FFNShape, inputs, prm: dict, decoded: bool = False) -> np.ndarray:
+    """The A2A FFN forward with both GEMMs on e4m3 operands (see above).
+
+    Same dispatch / LayerNorm-gate / combine as ffn_forward; Z and Hl stay
+    fp64 apart from the quantisation of Hl (per row, from its binary32 value)
+    before GEMM2.  Returns float64 output [P, B, T, D].
+    """
+    f = (lambda a: np.asarray(a, dtype=np.float64)) if decoded else bf16_to_f64
+    x = f(np.asarray(inputs))                                  # [P, B, T, D]
+    p = {k: f(np.asarray(v)) for k, v in prm.items()}
+    P, B, T, D, H, L = sh.P, sh.B, sh.T, sh.D, sh.H, sh.L
+    # per-row quantisation of every input token row (s, b, t)
+    xq, sx = quantize_e4m3(x.reshape(-1, D), axis=1)
+    xd = (e4m3_to_f64(xq) * sx.astype(np.float64)[:, None]).reshape(P, B, T, D)
+    out = np.zeros((P, B, T, D))
+    for r in range(P):
+        for l in range(L):
+            t = r * L + l
+            X = xd[:, :, t, :].reshape(P * B, D)               # dispatched rows n = s*B + b
+            w1q, s1 = quantize_e4m3(p["w1"][r, l], axis=0)     # [D, 2H], one scale per column
+            Z = X @ (e4m3_to_f64(w1q) * s1.astype(np.float64)[None, :]) + p["b1"][r, l]
+            a = layer_norm(Z[:, :H], p["nx_w"][r], p["nx_b"][r], sh.eps)
+            g = layer_norm(Z[:, H:], p["ng_w"][r], p["ng_b"][r], sh.eps)
+            Hl = a * silu(g)
+            hq, sh_ = quantize_e4m3(Hl.astype(np.float32), axis=1)
+            woq, so = quantize_e4m3(p["wout"][r, l], axis=0)   # [H, D]
+            Y = (e4m3_to_f64(hq) * sh_.astype(np.float64)[:, None]) @ \
+                (e4m3_to_f64(woq) * so.astype(np.float64)[None, :]) + p["bout"][r, l]
+            out[:, :, t, :] = Y.reshape(P, B, D)
+    return out

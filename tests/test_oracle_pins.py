@@ -611,3 +611,112 @@ def test_attention_projection_backward_matches_torch_autograd():
     assert np.allclose(np.concatenate(list(g2["da"]), axis=1), A.grad.numpy(), rtol=1e-11, atol=1e-11)
     assert np.allclose(g2["d_weight"], wo.grad.numpy(), rtol=1e-11, atol=1e-11)
     assert np.allclose(g2["d_bias"], bo.grad.numpy(), rtol=1e-11, atol=1e-11)
+
+
+# ------------------------------------------------------------------ FP8 inside the FFN
+
+def test_e4m3_rne_identity_ties_saturation():
+    codes = np.array([c for c in range(256) if c not in (0x7f, 0xff)], dtype=np.uint8)
+    vals = O.e4m3_to_f64(codes)
+    assert np.array_equal(O.e4m3_rne(vals), codes)                  # every value encodes to itself
+    pos = O.e4m3_to_f64(np.arange(0, 0x7f, dtype=np.uint8))
+    mid = (pos[:-1] + pos[1:]) / 2                                    # exact midpoints (binary)
+    got = O.e4m3_rne(mid)
+    lo, hi = np.arange(0, 0x7e), np.arange(1, 0x7f)
+    assert np.array_equal(got, np.where(lo % 2 == 0, lo, hi))         # ties to the even code
+    assert np.array_equal(O.e4m3_rne(np.nextafter(mid, np.inf)), hi)  # just above: the upper value
+    assert np.array_equal(O.e4m3_rne(np.nextafter(mid, -np.inf)), lo)
+    assert list(O.e4m3_rne(np.array([449.0, 1e9, np.inf, -1e9, -np.inf]))) == [0x7e, 0x7e, 0x7e, 0xfe, 0xfe]
+
+
+def test_e4m3_rne_matches_torch_cast():
+    rng = np.random.default_rng(3)
+    x = (rng.standard_normal(200000) * np.exp(rng.uniform(-12, 6, 200000))).astype(np.float32)
+    x = np.clip(x, -448, 448)
+    ref = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    got = O.e4m3_rne(x)
+    same = (got == ref) | ((got & 0x7f) == 0) & ((ref & 0x7f) == 0)  # +-0 may differ in sign only
+    assert same.all()
+
+
+def test_quantize_e4m3_scales_and_error_bound():
+    rng = np.random.default_rng(4)
+    x = (rng.standard_normal((64, 300)) * np.exp(rng.uniform(-3, 3, (64, 1)))).astype(np.float32)
+    x[5] = 0.0
+    q, s = O.quantize_e4m3(x, axis=1)
+    assert s[5] == 1.0 and not q[5].any()
+    amax = np.abs(x).max(axis=1)
+    assert np.array_equal(s[np.arange(64) != 5], (amax / np.float32(448))[np.arange(64) != 5])
+    # the largest magnitude of every row lands on +-448 (within the binary32 division)
+    assert (np.abs(O.e4m3_to_f64(q)).max(axis=1)[np.arange(64) != 5] == 448).all()
+    dq = O.e4m3_to_f64(q) * s.astype(np.float64)[:, None]
+    bound = 2.0 ** -4 * np.abs(x) + 2.0 ** -10 * s[:, None] + 1e-7 * np.abs(x)
+    assert (np.abs(dq - x) <= bound).all()
+    qc, sc = O.quantize_e4m3(x.T.copy(), axis=0)                      # per column of the transpose
+    assert np.array_equal(qc, q.T) and np.array_equal(sc, s)
+
+
+def test_ffn_forward_fp8_closed_form():
+    # The constant-halves setup of the bf16 closed form: Hl = silu(c) on every row, so the
+    # row's amax quantises it to 448 * scale exactly; wout chosen on the e4m3 grid times
+    # 2^-6 with +-448 * 2^-6 in every column quantises exactly too, hence
+    # Y[n] = silu(c) * colsum(wout) + bout as in the bf16 path.
+    sh = O.FFNShape(2, 3, 4, 8, 2)
+    t, b = _ffn_bits(sh)
+    H = sh.H
+    t["w1"].zero_()
+    t["b1"][..., :H] = 0.75
+    t["b1"][..., H:] = -1.5
+    t["nx_b"].fill_(1.0)
+    c = 0.625
+    t["ng_b"].fill_(c)
+    rng = np.random.default_rng(8)
+    grid = O.e4m3_to_f64(rng.integers(0, 0x7f, size=t["wout"].shape).astype(np.uint8))
+    grid = grid * rng.choice([-1.0, 1.0], size=grid.shape)
+    grid[..., 0, :] = 448.0
+    t["wout"] = torch.from_numpy(grid * 2.0 ** -6).to(torch.bfloat16)
+    b = {k: synth.bits(v) for k, v in t.items()}
+    out = O.ffn_forward_fp8(sh, b["inputs"], b)
+    silu_c = c / (1.0 + math.exp(-c))
+    hq, hs = O.quantize_e4m3(np.full((1, H), silu_c, dtype=np.float32), axis=1)
+    silu_q = O.e4m3_to_f64(hq)[0, 0] * float(hs[0])                  # silu(c) after binary32 rounding
+    wout = O.bf16_to_f64(b["wout"]).reshape(sh.P, sh.L, H, sh.D)
+    bout = O.bf16_to_f64(b["bout"]).reshape(sh.P, sh.L, sh.D)
+    for s, bb, tt in itertools.product(range(sh.P), range(sh.B), range(sh.T)):
+        r, l = divmod(tt, sh.L)
+        expect = silu_q * wout[r, l].sum(axis=0) + bout[r, l]
+        assert np.allclose(out[s, bb, tt], expect, rtol=1e-13, atol=1e-13)
+
+
+def test_ffn_forward_fp8_matches_torch_formulation():
+    # independent restatement: torch float8 casts for the codes, torch float64 for the rest
+    sh = O.FFNShape(2, 4, 8, 32, 2)
+    t, b = _ffn_bits(sh, seed=21)
+    P, B, T, D, H, L = sh.P, sh.B, sh.T, sh.D, sh.H, sh.L
+    f64 = {k: torch.from_numpy(O.bf16_to_f64(v)) for k, v in b.items()}
+
+    def q(x32, dim):
+        amax = x32.abs().amax(dim=dim, keepdim=True)
+        s = torch.where(amax > 0, amax / 448.0, torch.ones_like(amax)).to(torch.float32)
+        codes = (x32 / s).to(torch.float8_e4m3fn)
+        return codes.to(torch.float64) * s.to(torch.float64)
+
+    x = q(f64["inputs"].to(torch.float32).reshape(-1, D), 1).reshape(P, B, T, D)
+    out = torch.zeros(P, B, T, D, dtype=torch.float64)
+    w1 = f64["w1"].reshape(P, L, D, 2 * H)
+    wo = f64["wout"].reshape(P, L, H, D)
+    for r in range(P):
+        for l in range(L):
+            tt = r * L + l
+            X = x[:, :, tt].reshape(P * B, D)
+            Z = X @ q(w1[r, l].to(torch.float32), 0) + f64["b1"].reshape(P, L, -1)[r, l]
+            a = F.layer_norm(Z[:, :H], (H,), f64["nx_w"].reshape(P, H)[r], f64["nx_b"].reshape(P, H)[r], sh.eps)
+            g = F.layer_norm(Z[:, H:], (H,), f64["ng_w"].reshape(P, H)[r], f64["ng_b"].reshape(P, H)[r], sh.eps)
+            Hl = a * F.silu(g)
+            Y = q(Hl.to(torch.float32), 1) @ q(wo[r, l].to(torch.float32), 0) + f64["bout"].reshape(P, L, D)[r, l]
+            out[:, :, tt] = Y.reshape(P, B, D)
+    got = O.ffn_forward_fp8(sh, b["inputs"], b)
+    assert np.allclose(got, out.numpy(), rtol=1e-10, atol=1e-10)
+    # and the quantised layer stays within e4m3 precision of the exact one
+    ref = O.ffn_forward(sh, b["inputs"], b)
+    assert np.abs(got - ref).max() / np.abs(ref).max() < 0.15
