@@ -461,6 +461,7 @@ def run_dg(args, rank, world):
     extra = run_fp8_alone(w, args, dev, peaks)
     extra.update(run_tp_backward(w, args, dev, peaks))
     extra.update(run_attn_proj(w, args, dev, peaks))
+    extra.update(run_ffn_fp8(w, args, dev, peaks))
 
     # end to end: inputs from pinned host memory in, results back to pinned host memory
     e2e = run_e2e(w, args, dev, step_flops, world)
@@ -549,6 +550,46 @@ def run_tp_backward(w, args, dev, peaks):
     return {"tp_swiglu_bwd": {
         "ms": round(ms, 4), "tflops": round(tf, 2), "peak_tflops": peaks["bf16_tflops"],
         "frac_of_peak": round(tf / peaks["bf16_tflops"], 4), "iters": iters,
+        "kernels": {e["name"]: {"launches": e["launches"], "ms_per_launch": round(e["total_ms"] / e["launches"], 4)}
+                    for e in trace}}}
+
+
+def run_ffn_fp8(w, args, dev, peaks):
+    """The FFN forward with both GEMMs on e4m3 operands at the step's shape
+    (outside the step; weights packed once, before timing)."""
+    import torch
+    dg = w.dg
+    P, B, T, D = FFN["P"], FFN["B"], FFN["T"], FFN["D"]
+    packed = dg.a2a_ffn_fp8_pack_weights(w.params, P, B, T, D)
+    out = torch.empty_like(w.out)
+    lib = dg._lib.load()
+    import ctypes
+    ws = torch.empty(lib.dg_a2a_ffn_fp8_workspace_bytes(ctypes.byref(dg.ffn_shape(P, B, T, D, FFN["k"]))),
+                     dtype=torch.uint8, device=dev)
+    run = lambda: dg.a2a_ffn_forward_fp8(w.x, w.params, packed, workspace=ws, out=out)
+    for _ in range(max(args.warmup, 2)):
+        run()
+    iters = 5
+    stream = torch.cuda.current_stream(dev)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    torch.cuda.synchronize(dev)
+    dg.trace_begin()
+    ev[0].record(stream)
+    for _ in range(iters):
+        run()
+    ev[1].record(stream)
+    torch.cuda.synchronize(dev)
+    trace = dg.trace_end()
+    st, code = dg.device_status(dev)
+    if st != 0:
+        raise RuntimeError(f"device error word after the FP8 FFN forward: {code:#x}")
+    ms = ev[0].elapsed_time(ev[1]) / iters
+    flops = gemm_flops()["ffn_fwd"]
+    tf = flops / (ms * 1e-3) / 1e12
+    peak = 2.0 * peaks["bf16_tflops"]
+    return {"ffn_fwd_fp8": {
+        "ms": round(ms, 4), "tflops": round(tf, 2), "peak_tflops": peak, "frac_of_peak": round(tf / peak, 4),
+        "peak_note": "2 x measured bf16 burst (nominal fp8:bf16 ratio 2)", "iters": iters,
         "kernels": {e["name"]: {"launches": e["launches"], "ms_per_launch": round(e["total_ms"] / e["launches"], 4)}
                     for e in trace}}}
 

@@ -6,7 +6,8 @@ TMA/mbarrier pipelines):
 
 * gemm_fp8      D = alpha * (A @ B^T) + beta * C, e4m3 inputs, bf16 output
 * a2a_ffn       the all-to-all expert-parallel FFN layer (forward, backward,
-                autograd), P logical ranks in one GPU's memory
+                autograd), P logical ranks in one GPU's memory; a forward with
+                both GEMMs on e4m3 operands (a2a_ffn_forward_fp8)
 * tp_swiglu     the SwiGLU column/row-parallel pair over W shards (forward,
                 backward, autograd)
 * tp_linear     the attention projections (column-parallel QKV, row-parallel
@@ -15,13 +16,13 @@ TMA/mbarrier pipelines):
 The library is loaded lazily on first use and fails loudly if it is missing.
 """
 from .ops import (A2AFFN, FFN_PARAM_NAMES, TPSwiGLU, a2a_combine, a2a_dispatch, a2a_ffn, a2a_ffn_backward,
-                  a2a_ffn_forward, debug_wait_timeout, device_status, ffn_shape, gemm_fp8, tp_swiglu,
+                  a2a_ffn_forward, a2a_ffn_forward_fp8, a2a_ffn_fp8_pack_weights, debug_wait_timeout, device_status, ffn_shape, gemm_fp8, tp_swiglu,
                   tp_linear, tp_linear_backward, tp_linear_layer, TPLinear, tp_swiglu_backward, tp_swiglu_layer,
                   trace_begin, trace_end)
 
 __all__ = [
     "A2AFFN", "FFN_PARAM_NAMES", "a2a_combine", "a2a_dispatch", "a2a_ffn", "a2a_ffn_backward",
-    "a2a_ffn_forward", "debug_wait_timeout", "device_status", "ffn_shape", "gemm_fp8", "tp_swiglu",
+    "a2a_ffn_forward", "a2a_ffn_forward_fp8", "a2a_ffn_fp8_pack_weights", "debug_wait_timeout", "device_status", "ffn_shape", "gemm_fp8", "tp_swiglu",
     "tp_swiglu_backward", "TPSwiGLU", "tp_swiglu_layer", "tp_linear", "tp_linear_backward", "TPLinear",
     "tp_linear_layer", "trace_begin", "trace_end",
 ]

@@ -55,6 +55,10 @@ SIGNATURES = {
     "dg_tp_swiglu_bwd_workspace_bytes": (_sz, [_i64, _i64, _i64, _i32, _i32]),
     "dg_tp_swiglu_bwd": (ctypes.c_int, [_i64, _i64, _i64, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz,
                                         _vp]),
+    "dg_a2a_ffn_fp8_weights_bytes": (_sz, [_PSHAPE]),
+    "dg_a2a_ffn_fp8_workspace_bytes": (_sz, [_PSHAPE]),
+    "dg_a2a_ffn_fp8_pack_weights": (ctypes.c_int, [_PSHAPE, _vp, _vp, _vp, _sz, _vp]),
+    "dg_a2a_ffn_fwd_fp8": (ctypes.c_int, [_PSHAPE, _vp, _vp, _sz, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "dg_tp_linear_fwd": (ctypes.c_int, [_i64, _i64, _i64, _vp, _vp, _vp, _vp, _vp]),
     "dg_tp_linear_bwd": (ctypes.c_int, [_i64, _i64, _i64, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
     "dg_tp_swiglu_noalloc": (ctypes.c_int, [_i64, _i64, _i64, _i32, _i32, _vp, _vp, _vp, _vp, _vp]),

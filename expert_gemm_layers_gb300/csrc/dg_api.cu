@@ -194,6 +194,8 @@ dg_status run_gemm(GemmVariant v, const CUtensorMap& a, const CUtensorMap& b, co
     case GV_BF16_KM_STORE: e = launch_gemm_bf16_km_store(a, b, d, c, p, grid, s); break;
     case GV_FP8_KK_N224: e = launch_gemm_fp8_kk_n224(a, b, d, c, p, grid, s); break;
     case GV_BF16_KK_BIAS: e = launch_gemm_bf16_kk_bias(a, b, d, c, p, grid, s); break;
+    case GV_FP8_KK_LNSTATS: e = launch_gemm_fp8_kk_lnstats(a, b, d, c, p, grid, s); break;
+    case GV_FP8_KK_BIAS: e = launch_gemm_fp8_kk_bias(a, b, d, c, p, grid, s); break;
     default: return fail(DG_ERR_UNSUPPORTED, "unknown GEMM variant");
   }
   if (e != cudaSuccess) return cuda_fail(e, "GEMM launch");
@@ -457,8 +459,8 @@ dg_status dg_a2a_ffn_fwd(const dg_ffn_shape* shape, const void* inputs, const vo
   if (e != cudaSuccess) return cuda_fail(e, "LayerNorm statistics launch");
   {
     TraceScope trace("ffn_ln_gate_fwd", s, 0.0, rows * (2.0 * 2 * H + 2.0 * H + 16.0));
-    e = launch_ln_gate_fwd(Z, stats, nx_w, nx_b, ng_w, ng_b, Hl, static_cast<int>(f.P), static_cast<int>(M),
-                           static_cast<int>(f.L), static_cast<int>(H), dev, s);
+    e = launch_ln_gate_fwd(Z, stats, nx_w, nx_b, ng_w, ng_b, Hl, nullptr, nullptr, static_cast<int>(f.P),
+                           static_cast<int>(M), static_cast<int>(f.L), static_cast<int>(H), dev, s);
   }
   if (e != cudaSuccess) return cuda_fail(e, "LayerNorm-gate launch");
 
@@ -660,6 +662,215 @@ dg_status dg_a2a_combine(int32_t P, int32_t B, int32_t T, int32_t D, const void*
   TraceScope trace("a2a_combine", static_cast<cudaStream_t>(stream), 0.0, 2.0 * bytes);
   cudaError_t e = launch_combine(ylocal, output, P, B, T, D, dev, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? DG_OK : cuda_fail(e, "combine launch");
+}
+
+// ------------------------------------------------------------------ A2A FFN, FP8 GEMMs (forward)
+
+namespace {
+
+// e4m3 copy of the weights: w1 codes [T][2H][D] and scales [T][2H], wout codes
+// [T][D][H] and scales [T][D] (codes K-major for the GEMMs' B operands).
+struct Fp8WeightsLayout {
+  size_t w1q, s1, woq, so, total;
+};
+Fp8WeightsLayout fp8_weights_layout(const FfnDims& f) {
+  Fp8WeightsLayout l;
+  const size_t T = f.T, D = f.D, H = f.H;
+  l.w1q = 0;
+  l.s1 = round_up(T * 2 * H * D, 256);
+  l.woq = round_up(l.s1 + T * 2 * H * 4, 256);
+  l.so = round_up(l.woq + T * D * H, 256);
+  l.total = round_up(l.so + T * D * 4, 256);
+  return l;
+}
+
+// Forward workspace: input codes [P,B,T,D] and row scales [T,M]; Z [T,M,2H]
+// bf16, the per-tile LayerNorm partials and the row statistics (as in the
+// bf16 forward); Hl codes [T,M,H] and row scales [T,M].
+struct Fp8FwdLayout {
+  size_t xq, sx, z, part, stats, hq, sh, total;
+  int tiles_n;
+};
+Fp8FwdLayout fp8_fwd_layout(const FfnDims& f) {
+  Fp8FwdLayout l;
+  const size_t rows = static_cast<size_t>(f.T) * f.M;
+  l.tiles_n = static_cast<int>((2 * f.H + gemm_tile_n(GV_FP8_KK_LNSTATS) - 1) / gemm_tile_n(GV_FP8_KK_LNSTATS));
+  l.xq = 0;
+  l.sx = round_up(rows * f.D, 256);
+  l.z = round_up(l.sx + rows * 4, 256);
+  l.part = round_up(l.z + rows * 2 * f.H * 2, 256);
+  l.stats = round_up(l.part + rows * l.tiles_n * 16, 256);
+  l.hq = round_up(l.stats + rows * 16, 256);
+  l.sh = round_up(l.hq + rows * f.H, 256);
+  l.total = round_up(l.sh + rows * 4, 256);
+  return l;
+}
+
+dg_status check_fp8_shape(const dg_ffn_shape* shape, FfnDims* f, const char* what) {
+  dg_status st = check_ffn_shape(shape, f);
+  if (st != DG_OK) return st;
+  if (f->D % 16 || f->H % 16)
+    return fail(DG_ERR_INVALID_ARGUMENT, "%s: D and H = D*k must be multiples of 16 (16-byte e4m3 rows)", what);
+  if (f->H > 8192) return fail(DG_ERR_UNSUPPORTED, "%s: H = %lld > 8192 (an e4m3 Hl row is scaled in one CTA)", what,
+                               (long long)f->H);
+  return DG_OK;
+}
+
+}  // namespace
+
+size_t dg_a2a_ffn_fp8_weights_bytes(const dg_ffn_shape* shape) {
+  FfnDims f{};
+  if (check_fp8_shape(shape, &f, "a2a_ffn_fp8_weights_bytes") != DG_OK) return 0;
+  return fp8_weights_layout(f).total;
+}
+
+size_t dg_a2a_ffn_fp8_workspace_bytes(const dg_ffn_shape* shape) {
+  FfnDims f{};
+  if (check_fp8_shape(shape, &f, "a2a_ffn_fp8_workspace_bytes") != DG_OK) return 0;
+  return fp8_fwd_layout(f).total;
+}
+
+dg_status dg_a2a_ffn_fp8_pack_weights(const dg_ffn_shape* shape, const void* w1, const void* wout, void* packed,
+                                      size_t packed_bytes, void* stream) {
+  FfnDims f{};
+  dg_status st = check_fp8_shape(shape, &f, "a2a_ffn_fp8_pack_weights");
+  if (st != DG_OK) return st;
+  const void* ptrs[] = {w1, wout, packed};
+  const char* names[] = {"w1", "wout", "packed"};
+  if (const char* n = ptr_name_null(ptrs, names, 3))
+    return fail(DG_ERR_INVALID_ARGUMENT, "a2a_ffn_fp8_pack_weights: %s is NULL", n);
+  if (const char* n = ptr_name_unaligned(ptrs, names, 3))
+    return fail(DG_ERR_INVALID_ARGUMENT, "a2a_ffn_fp8_pack_weights: %s is not 16-byte aligned", n);
+  const Fp8WeightsLayout wl = fp8_weights_layout(f);
+  if (packed_bytes < wl.total)
+    return fail(DG_ERR_WORKSPACE, "a2a_ffn_fp8_pack_weights: packed buffer has %zu bytes, needs %zu", packed_bytes,
+                wl.total);
+  const size_t wbytes = static_cast<size_t>(f.T) * f.D * 2 * f.H * 2, wobytes = static_cast<size_t>(f.T) * f.H * f.D * 2;
+  if (overlaps(packed, wl.total, w1, wbytes) || overlaps(packed, wl.total, wout, wobytes))
+    return fail(DG_ERR_INVALID_ARGUMENT, "a2a_ffn_fp8_pack_weights: packed overlaps a weight");
+  DeviceInfo dev;
+  if ((st = device_info(&dev)) != DG_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* pk = static_cast<uint8_t*>(packed);
+  cudaError_t e;
+  {
+    TraceScope trace("ffn_fp8_pack_w1", s, 0.0, 2.0 * wbytes);
+    e = launch_quant_weight(w1, reinterpret_cast<float*>(pk + wl.s1), pk + wl.w1q, static_cast<int>(f.T),
+                            static_cast<int>(f.D), static_cast<int>(2 * f.H), dev, s);
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "w1 quantisation launch");
+  {
+    TraceScope trace("ffn_fp8_pack_wout", s, 0.0, 2.0 * wobytes);
+    e = launch_quant_weight(wout, reinterpret_cast<float*>(pk + wl.so), pk + wl.woq, static_cast<int>(f.T),
+                            static_cast<int>(f.H), static_cast<int>(f.D), dev, s);
+  }
+  return e == cudaSuccess ? DG_OK : cuda_fail(e, "wout quantisation launch");
+}
+
+dg_status dg_a2a_ffn_fwd_fp8(const dg_ffn_shape* shape, const void* inputs, const void* packed, size_t packed_bytes,
+                             const void* b1, const void* bout, const void* nx_w, const void* nx_b, const void* ng_w,
+                             const void* ng_b, void* output, void* ws, size_t ws_bytes, void* stream) {
+  FfnDims f{};
+  dg_status st = check_fp8_shape(shape, &f, "a2a_ffn_fwd_fp8");
+  if (st != DG_OK) return st;
+  const void* ptrs[] = {inputs, packed, b1, bout, nx_w, nx_b, ng_w, ng_b, output, ws};
+  const char* names[] = {"inputs", "packed", "b1", "bout", "nx_w", "nx_b", "ng_w", "ng_b", "output", "ws"};
+  if (const char* n = ptr_name_null(ptrs, names, 10))
+    return fail(DG_ERR_INVALID_ARGUMENT, "a2a_ffn_fwd_fp8: %s is NULL", n);
+  if (const char* n = ptr_name_unaligned(ptrs, names, 10))
+    return fail(DG_ERR_INVALID_ARGUMENT, "a2a_ffn_fwd_fp8: %s is not 16-byte aligned", n);
+  const Fp8WeightsLayout wl = fp8_weights_layout(f);
+  const Fp8FwdLayout fl = fp8_fwd_layout(f);
+  if (packed_bytes < wl.total)
+    return fail(DG_ERR_WORKSPACE, "a2a_ffn_fwd_fp8: packed weights have %zu bytes, need %zu", packed_bytes, wl.total);
+  if (ws_bytes < fl.total)
+    return fail(DG_ERR_WORKSPACE, "a2a_ffn_fwd_fp8: workspace has %zu bytes, needs %zu", ws_bytes, fl.total);
+  const size_t act = static_cast<size_t>(f.P) * f.B * f.T * f.D * 2;
+  if (overlaps(output, act, inputs, act) || overlaps(output, act, ws, fl.total) || overlaps(ws, fl.total, inputs, act) ||
+      overlaps(ws, fl.total, packed, wl.total) || overlaps(output, act, packed, wl.total))
+    return fail(DG_ERR_INVALID_ARGUMENT, "a2a_ffn_fwd_fp8: output / workspace / inputs / packed weights overlap");
+  DeviceInfo dev;
+  if ((st = device_info(&dev)) != DG_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const uint8_t* pk = static_cast<const uint8_t*>(packed);
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  const uint64_t T = f.T, M = f.M, D = f.D, H = f.H;
+  const double rows = static_cast<double>(T) * M;
+  cudaError_t e;
+
+  // e4m3 input rows, one scale per row
+  {
+    TraceScope trace("ffn_fp8_quant_inputs", s, 0.0, rows * D * 2.0 + rows * D + rows * 4.0);
+    e = launch_quant_rows(inputs, w + fl.xq, reinterpret_cast<float*>(w + fl.sx), static_cast<int64_t>(T * M),
+                          static_cast<int>(D), static_cast<int>(T), static_cast<int>(M), dev, s);
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "input quantisation launch");
+
+  // GEMM1 on e4m3 operands (dispatch folded into the input map), dequantised in
+  // the epilogue, + b1, LayerNorm partial statistics, bf16 Z.
+  CUtensorMap mx, mw1, mz;
+  if ((st = make_map_3d(&mx, false, w + fl.xq, D, T, M, D, T * D, 128, 1, 128, "input codes")) != DG_OK) return st;
+  if ((st = make_map_3d(&mw1, false, pk + wl.w1q, D, 2 * H, T, D, 2 * H * D, 128, kKMajorBRows, 1, "w1 codes")) != DG_OK)
+    return st;
+  if ((st = make_map_3d(&mz, true, w + fl.z, 2 * H, M, T, 2 * H * 2, M * 2 * H * 2, 64, 32, 1, "Z")) != DG_OK) return st;
+  GemmParams p1{};
+  p1.G = static_cast<int32_t>(T);
+  p1.M = static_cast<int32_t>(M);
+  p1.N = static_cast<int32_t>(2 * H);
+  p1.K = static_cast<int32_t>(D);
+  p1.a_g = G_MID;
+  p1.b_g = G_OUTER;
+  p1.d_g = G_OUTER;
+  p1.bias = static_cast<const __nv_bfloat16*>(b1);
+  p1.bias_g_stride = static_cast<int64_t>(2 * H);
+  p1.ln_part = reinterpret_cast<float4*>(w + fl.part);
+  p1.ln_H = static_cast<int32_t>(H);
+  p1.row_scale = reinterpret_cast<const float*>(w + fl.sx);
+  p1.row_scale_g = static_cast<int64_t>(M);
+  p1.col_scale = reinterpret_cast<const float*>(pk + wl.s1);
+  p1.col_scale_g = static_cast<int64_t>(2 * H);
+  if ((st = run_gemm(GV_FP8_KK_LNSTATS, mx, mw1, mz, mz, p1, dev, s, "ffn_fp8_gemm1",
+                     rows * D + static_cast<double>(T) * D * 2 * H + rows * 2 * H * 2 + rows * 4 +
+                         rows * fl.tiles_n * 16.0)) != DG_OK)
+    return st;
+
+  {
+    TraceScope trace("ffn_fp8_ln_stats", s, 0.0, rows * fl.tiles_n * 16.0 + rows * 16.0);
+    e = launch_ln_stats_finalize(reinterpret_cast<const float4*>(w + fl.part), w + fl.stats, static_cast<int>(T),
+                                 static_cast<int>(M), static_cast<int>(H), gemm_tile_n(GV_FP8_KK_LNSTATS), fl.tiles_n,
+                                 shape->eps, dev, s);
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "LayerNorm statistics launch");
+  {
+    TraceScope trace("ffn_fp8_ln_gate", s, 0.0, rows * (2.0 * 2 * H + H + 16.0 + 4.0));
+    e = launch_ln_gate_fwd(w + fl.z, w + fl.stats, nx_w, nx_b, ng_w, ng_b, nullptr, w + fl.hq,
+                           reinterpret_cast<float*>(w + fl.sh), static_cast<int>(f.P), static_cast<int>(M),
+                           static_cast<int>(f.L), static_cast<int>(H), dev, s);
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "LayerNorm-gate launch");
+
+  // GEMM2 on e4m3 operands, dequantised, + bout, stored at the combine offsets.
+  CUtensorMap mh, mwo, mo;
+  if ((st = make_map_3d(&mh, false, w + fl.hq, H, M, T, H, M * H, 128, 128, 1, "Hl codes")) != DG_OK) return st;
+  if ((st = make_map_3d(&mwo, false, pk + wl.woq, H, D, T, H, D * H, 128, kKMajorBRows, 1, "wout codes")) != DG_OK)
+    return st;
+  if ((st = make_map_3d(&mo, true, output, D, T, M, D * 2, T * D * 2, 64, 1, 32, "output")) != DG_OK) return st;
+  GemmParams p2{};
+  p2.G = static_cast<int32_t>(T);
+  p2.M = static_cast<int32_t>(M);
+  p2.N = static_cast<int32_t>(D);
+  p2.K = static_cast<int32_t>(H);
+  p2.a_g = G_OUTER;
+  p2.b_g = G_OUTER;
+  p2.d_g = G_MID;
+  p2.bias = static_cast<const __nv_bfloat16*>(bout);
+  p2.bias_g_stride = static_cast<int64_t>(D);
+  p2.row_scale = reinterpret_cast<const float*>(w + fl.sh);
+  p2.row_scale_g = static_cast<int64_t>(M);
+  p2.col_scale = reinterpret_cast<const float*>(pk + wl.so);
+  p2.col_scale_g = static_cast<int64_t>(D);
+  return run_gemm(GV_FP8_KK_BIAS, mh, mwo, mo, mo, p2, dev, s, "ffn_fp8_gemm2",
+                  rows * H + static_cast<double>(T) * H * D + rows * D * 2.0 + rows * 4);
 }
 
 // ------------------------------------------------------------------ TP SwiGLU

@@ -58,6 +58,11 @@ struct GemmParams {
   uint32_t* err;             // device error word
   const __nv_bfloat16* c_ptr; // narrow tiles: C and D as row-major [G][M][N] for the last 32-column chunk
   __nv_bfloat16* d_ptr;
+  // e4m3 variants other than EPI_FP8: acc is dequantised as
+  // acc * row_scale[g*row_scale_g + m] * col_scale[g*col_scale_g + n] before the bias
+  const float* row_scale;
+  const float* col_scale;
+  int64_t row_scale_g, col_scale_g;
 };
 
 // Running (count, mean, M2) of a set of values; merge() is the pairwise
@@ -124,6 +129,7 @@ struct GemmCfg {
   static_assert(NUM_BARS * 8 + 4 <= BAR_BYTES, "barrier area");
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
   static_assert(!(kFp8 && (kAMN || kBMN)), "e4m3 operands are K-major here");
+  static_assert(!kFp8 || kEpi == EPI_FP8 || kEpi == EPI_BIAS || kEpi == EPI_BIAS_LNSTATS, "e4m3 epilogues");
   static_assert(kBN <= ACC_STRIDE && kBN % 32 == 0 && (kBN / CTAS) % 8 == 0, "tile width");
   static_assert(kBN == 256 || kEpi == EPI_FP8, "narrow tiles: the alpha/beta/C epilogue only");
 };
@@ -506,6 +512,22 @@ __global__ void __launch_bounds__(GemmCfg<kFp8, kAMN, kBMN, kEpi, kPair, kBN>::N
           if (kEpi == EPI_FP8) {
 #pragma unroll
             for (int i = 0; i < 64; ++i) v[i] *= p.alpha;
+          }
+          if (kFp8 && kEpi != EPI_FP8) {
+            // per-row scale of the e4m3 A rows, per-column scale of the e4m3 B rows
+            const int row = row0 + lane;
+            const float rsc = row < p.M ? __ldg(p.row_scale + static_cast<int64_t>(g) * p.row_scale_g + row) : 0.0f;
+            const float* cp = p.col_scale + static_cast<int64_t>(g) * p.col_scale_g + n0 + 64 * j;
+#pragma unroll
+            for (int q = 0; q < 16; ++q) {
+              if (n0 + 64 * j + 4 * q < p.N) {
+                const float4 c4 = __ldg(reinterpret_cast<const float4*>(cp + 4 * q));
+                v[4 * q] *= rsc * c4.x;
+                v[4 * q + 1] *= rsc * c4.y;
+                v[4 * q + 2] *= rsc * c4.z;
+                v[4 * q + 3] *= rsc * c4.w;
+              }
+            }
           }
           if (kEpi == EPI_BIAS || kEpi == EPI_BIAS_LNSTATS) {
             const __nv_bfloat16* bp = p.bias + static_cast<int64_t>(g) * p.bias_g_stride + n0 + 64 * j;

@@ -40,7 +40,9 @@ enum GemmVariant : int {
   GV_BF16_KM_LNSTATS = 5, // bf16, A K-major, B MN-major, bias + per-tile LayerNorm statistics
   GV_BF16_KM_STORE = 6,   // bf16, A K-major, B MN-major, plain store
   GV_FP8_KK_N224 = 7,     // GV_FP8_KK with 224-column tiles
-  GV_BF16_KK_BIAS = 8     // bf16, A and B K-major, bias epilogue
+  GV_BF16_KK_BIAS = 8,    // bf16, A and B K-major, bias epilogue
+  GV_FP8_KK_LNSTATS = 9,  // e4m3, A and B K-major, dequantise + bias + per-tile LayerNorm statistics
+  GV_FP8_KK_BIAS = 10     // e4m3, A and B K-major, dequantise + bias
 };
 
 // Tiles along N of one problem for this variant (output columns per tile).
@@ -86,6 +88,10 @@ cudaError_t launch_gemm_bf16_km_store(const CUtensorMap&, const CUtensorMap&, co
                                       const CUtensorMap&, const GemmParams&, int num_sms, cudaStream_t);
 cudaError_t launch_gemm_bf16_kk_bias(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
                                      const CUtensorMap&, const GemmParams&, int num_sms, cudaStream_t);
+cudaError_t launch_gemm_fp8_kk_lnstats(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
+                                       const GemmParams&, int num_sms, cudaStream_t);
+cudaError_t launch_gemm_fp8_kk_bias(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
+                                    const GemmParams&, int num_sms, cudaStream_t);
 cudaError_t launch_gemm_fp8_kk_n224(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
                                     const GemmParams&, int num_sms, cudaStream_t);
 // Co-resident CTA pairs (or CTAs) of the e4m3 GEMM on the current device.
@@ -199,8 +205,17 @@ cudaError_t launch_ln_stats_finalize(const float4* part, void* stats, int T, int
 
 // Normalise and gate: Hl [rows, H] = LN_x(U) * silu(LN_g(G)) from Z [rows, 2H] and stats.
 cudaError_t launch_ln_gate_fwd(const void* Z, const void* stats, const void* nx_w, const void* nx_b, const void* ng_w,
-                               const void* ng_b, void* Hl, int P, int M, int L, int H, const DeviceInfo& dev,
-                               cudaStream_t s);
+                               const void* ng_b, void* Hl, uint8_t* hq, float* hs, int P, int M, int L, int H,
+                               const DeviceInfo& dev, cudaStream_t s);
+
+// e4m3 operands of the FP8 path (scale = amax / 448 per row or output column):
+// input rows [P*B*T, D] -> codes in place of each row and scale[t*M + s*B + b];
+// weight [G][K][N] -> scale[G][N] and codes [G][N][K] (K-major).
+cudaError_t launch_quant_rows(const void* x, void* q, float* scale, int64_t rows, int D, int T, int M,
+                              const DeviceInfo& dev, cudaStream_t s);
+cudaError_t launch_quant_weight(const void* w, float* scale, void* q, int G, int K, int N, const DeviceInfo& dev,
+                                cudaStream_t s);
+
 
 // Backward of the gate and both LayerNorms, pass 1: per-row sums
 // rowsum[row] = (sum dx_u, sum dx_u*x_u, sum dx_g, sum dx_g*x_g), one warp per row.

@@ -8,6 +8,7 @@
 // Hl = LN_x(U) * silu(LN_gate(G)).  Statistics come from the stored bf16 Z
 // (what the page's bmm path normalises), two passes over registers.
 #include <cuda_bf16.h>
+#include <cuda_fp8.h>
 
 #include "dg_gate.cuh"
 #include "dg_internal.h"
@@ -82,6 +83,29 @@ __device__ __forceinline__ void block_sum(float (&v)[N], float (*sm)[kMaxRowWarp
   }
 }
 
+// Block-wide maximum of one value; consecutive calls alternate `slot` (see block_sum).
+__device__ __forceinline__ float block_max(float v, float (*sm)[kMaxRowWarps], int slot) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nwarps = blockDim.x >> 5;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  if (lane == 0) sm[slot][warp] = v;
+  __syncthreads();
+  float w = lane < nwarps ? sm[slot][lane] : 0.0f;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) w = fmaxf(w, __shfl_xor_sync(0xffffffffu, w, o));
+  return w;
+}
+
+// e4m3 code of x / scale: binary32 division, round to nearest even, saturating
+// at +-448 (the code decision of the per-row / per-column quantisation).
+__device__ __forceinline__ uint32_t e4m3_code(float x, float scale) {
+  return static_cast<uint32_t>(__nv_cvt_float_to_fp8(__fdiv_rn(x, scale), __NV_SATFINITE, __NV_E4M3));
+}
+
+// Scale of a vector whose largest magnitude is amax: amax / 448, or 1 for zeros.
+__device__ __forceinline__ float e4m3_scale(float amax) { return amax > 0.0f ? __fdiv_rn(amax, 448.0f) : 1.0f; }
+
 // Per-thread asynchronous copies into shared memory (cp.async): a thread
 // copies exactly the bytes it will read back itself, so a multi-stage ring
 // needs no barrier for the copies, only cp.async.wait_group.
@@ -130,11 +154,15 @@ __global__ void ln_stats_finalize_kernel(const float4* __restrict__ part, float4
 
 constexpr int kFwdStages = 4;
 
-template <int NT, int VPT>
+// kFp8Out: instead of bf16 Hl, write each row as e4m3 codes with one scale per
+// row (row amax / 448) for an e4m3 GEMM2; the whole row is in one CTA.
+template <int NT, int VPT, bool kFp8Out>
 __global__ void __launch_bounds__(NT, 512 / NT) ln_gate_fwd_kernel(
     const __nv_bfloat16* __restrict__ Z, const float4* __restrict__ stats, const __nv_bfloat16* __restrict__ gx,
     const __nv_bfloat16* __restrict__ bx, const __nv_bfloat16* __restrict__ gg, const __nv_bfloat16* __restrict__ bg,
-    __nv_bfloat16* __restrict__ Hl, int M, int L, int H, int ctas_per_rank, int col_blocks, const uint32_t* err) {
+    __nv_bfloat16* __restrict__ Hl, uint8_t* __restrict__ hq, float* __restrict__ hs, int M, int L, int H,
+    int ctas_per_rank, int col_blocks, const uint32_t* err) {
+  __shared__ float red_max[2][kMaxRowWarps];
   extern __shared__ uint4 ring[];  // [kFwdStages][VPT][2][NT]
   griddep_wait();
   if (block_aborted(err)) return;
@@ -193,28 +221,151 @@ __global__ void __launch_bounds__(NT, 512 / NT) ln_gate_fwd_kernel(
     const uint4* st = ring + (i % kFwdStages) * (VPT * 2 * NT);
     const float2 rsu = make_float2(sr.y, sr.y), cu = make_float2(-sr.x * sr.y, -sr.x * sr.y);
     const float2 rsg = make_float2(sr.w, sr.w), cgs = make_float2(-sr.z * sr.w, -sr.z * sr.w);
-    __nv_bfloat16* hrow = Hl + row * static_cast<int64_t>(H);
+    float o[VPT][8];
+    float amax = 0.0f;
 #pragma unroll
     for (int j = 0; j < VPT; ++j) {
       const int v = vbase + threadIdx.x + NT * j;
       if (v < nvec) {
         const uint4 pu = st[(2 * j) * NT + threadIdx.x], pg = st[(2 * j + 1) * NT + threadIdx.x];
         const uint32_t uw[4] = {pu.x, pu.y, pu.z, pu.w}, gw[4] = {pg.x, pg.y, pg.z, pg.w};
-        uint32_t ow[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const float2 a = fma2(fma2(unpack_bf16x2(uw[e]), rsu, cu), wx[j][e], cx[j][e]);
           const float2 sv = fma2(fma2(unpack_bf16x2(gw[e]), rsg, cgs), wg[j][e], cg[j][e]);
           const float2 h = mul2(sv, half2);
           const float2 silu = fma2(h, make_float2(tanh_fast(h.x), tanh_fast(h.y)), h);
-          const float2 o = mul2(a, silu);
-          ow[e] = pack_bf16x2(o.x, o.y);
+          const float2 ov = mul2(a, silu);
+          o[j][2 * e] = ov.x;
+          o[j][2 * e + 1] = ov.y;
+          amax = fmaxf(amax, fmaxf(fabsf(ov.x), fabsf(ov.y)));
         }
-        __stcs(reinterpret_cast<uint4*>(hrow + 8 * v), make_uint4(ow[0], ow[1], ow[2], ow[3]));
       }
+    }
+    if (!kFp8Out) {
+      __nv_bfloat16* hrow = Hl + row * static_cast<int64_t>(H);
+#pragma unroll
+      for (int j = 0; j < VPT; ++j) {
+        const int v = vbase + threadIdx.x + NT * j;
+        if (v < nvec)
+          __stcs(reinterpret_cast<uint4*>(hrow + 8 * v),
+                 make_uint4(pack_bf16x2(o[j][0], o[j][1]), pack_bf16x2(o[j][2], o[j][3]),
+                            pack_bf16x2(o[j][4], o[j][5]), pack_bf16x2(o[j][6], o[j][7])));
+      }
+    } else {
+      const float scale = e4m3_scale(block_max(amax, red_max, static_cast<int>(i & 1)));
+      uint8_t* qrow = hq + row * static_cast<int64_t>(H);
+#pragma unroll
+      for (int j = 0; j < VPT; ++j) {
+        const int v = vbase + threadIdx.x + NT * j;
+        if (v < nvec) {
+          uint32_t c[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) c[e] = e4m3_code(o[j][e], scale);
+          *reinterpret_cast<uint2*>(qrow + 8 * v) =
+              make_uint2(c[0] | (c[1] << 8) | (c[2] << 16) | (c[3] << 24), c[4] | (c[5] << 8) | (c[6] << 16) | (c[7] << 24));
+        }
+      }
+      if (threadIdx.x == 0) hs[row] = scale;
     }
   }
   cp_async_wait<0>();
+}
+
+// ------------------------------------------------------------------ e4m3 operands
+// Quantisation for the FP8 GEMMs of the layer: scale = amax / 448 per row of
+// an activation or per output column of a weight, code = the e4m3 value
+// nearest to x / scale (binary32 division, ties to even, saturating).
+
+// inputs [P*B*T rows of D] -> codes in the same layout, one scale per row,
+// stored per problem: scale[t*M + n] for input row (s, b, t), n = s*B + b.
+// One warp per row.
+__global__ void quant_rows_kernel(const __nv_bfloat16* __restrict__ x, uint8_t* __restrict__ q,
+                                  float* __restrict__ scale, int64_t rows, int D, int T, int M,
+                                  const uint32_t* err) {
+  griddep_wait();
+  if (warp_aborted(err)) return;
+  const int lane = threadIdx.x & 31;
+  const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+  for (int64_t row = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); row < rows;
+       row += warps) {
+    const __nv_bfloat16* xr = x + row * D;
+    float amax = 0.0f;
+    for (int c = 8 * lane; c < D; c += 256) {
+      float f[8];
+      unpack8(__ldg(reinterpret_cast<const uint4*>(xr + c)), f);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(f[e]));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    const float sc = e4m3_scale(amax);
+    uint8_t* qr = q + row * D;
+    for (int c = 8 * lane; c < D; c += 256) {
+      float f[8];
+      unpack8(__ldg(reinterpret_cast<const uint4*>(xr + c)), f);
+      uint32_t k[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) k[e] = e4m3_code(f[e], sc);
+      *reinterpret_cast<uint2*>(qr + c) =
+          make_uint2(k[0] | (k[1] << 8) | (k[2] << 16) | (k[3] << 24), k[4] | (k[5] << 8) | (k[6] << 16) | (k[7] << 24));
+    }
+    if (lane == 0) {
+      const int64_t sb = row / T;  // s*B + b
+      const int t = static_cast<int>(row - sb * T);
+      scale[static_cast<int64_t>(t) * M + sb] = sc;
+    }
+  }
+}
+
+// Weight [G][K][N] (N contiguous): scale[g][n] = amax over k / 448.
+__global__ void col_scale_kernel(const __nv_bfloat16* __restrict__ w, float* __restrict__ scale, int K, int N,
+                                 const uint32_t* err) {
+  griddep_wait();
+  if (ld_volatile_u32(err) != 0u) return;
+  const int g = blockIdx.y;
+  const int n = blockIdx.x * blockDim.x + threadIdx.x;
+  if (n >= N) return;
+  const __nv_bfloat16* p = w + static_cast<int64_t>(g) * K * N + n;
+  float amax = 0.0f;
+  for (int k = 0; k < K; ++k) amax = fmaxf(amax, fabsf(__bfloat162float(p[static_cast<int64_t>(k) * N])));
+  scale[static_cast<int64_t>(g) * N + n] = e4m3_scale(amax);
+}
+
+// Weight [G][K][N] -> codes [G][N][K] (K contiguous: the K-major B operand of
+// an e4m3 GEMM), through a 64 x 64 shared-memory tile.  256 threads.
+__global__ void transpose_quant_kernel(const __nv_bfloat16* __restrict__ w, const float* __restrict__ scale,
+                                       uint8_t* __restrict__ q, int K, int N, const uint32_t* err) {
+  __shared__ float tile[64][65];
+  griddep_wait();
+  if (block_aborted(err)) return;
+  const int g = blockIdx.z;
+  const int k0 = blockIdx.y * 64, n0 = blockIdx.x * 64;
+  const __nv_bfloat16* wg = w + static_cast<int64_t>(g) * K * N;
+  {
+    // load: 64 k-rows of 64 n-columns, 16 values per thread
+    const int kr = threadIdx.x >> 2, nc = (threadIdx.x & 3) * 16;
+#pragma unroll
+    for (int e = 0; e < 16; ++e) {
+      const int k = k0 + kr, n = n0 + nc + e;
+      tile[kr][nc + e] = (k < K && n < N) ? __bfloat162float(wg[static_cast<int64_t>(k) * N + n]) : 0.0f;
+    }
+  }
+  __syncthreads();
+  {
+    // store: 64 n-rows of 64 k-codes, 16 per thread
+    const int nr = threadIdx.x >> 2, kc = (threadIdx.x & 3) * 16;
+    const int n = n0 + nr;
+    if (n < N) {
+      const float sc = scale[static_cast<int64_t>(g) * N + n];
+      uint8_t* qn = q + (static_cast<int64_t>(g) * N + n) * K;
+#pragma unroll
+      for (int e = 0; e < 16; ++e) {
+        const int k = k0 + kc + e;
+        if (k < K) qn[k] = static_cast<uint8_t>(e4m3_code(tile[kc + e][nr], sc));
+      }
+    }
+  }
 }
 
 // ------------------------------------------------------------------ backward
@@ -576,10 +727,11 @@ cudaError_t launch_ln_stats_finalize(const float4* part, void* stats, int T, int
 }
 
 cudaError_t launch_ln_gate_fwd(const void* Z, const void* stats, const void* nx_w, const void* nx_b, const void* ng_w,
-                               const void* ng_b, void* Hl, int P, int M, int L, int H, const DeviceInfo& dev,
-                               cudaStream_t s) {
+                               const void* ng_b, void* Hl, uint8_t* hq, float* hs, int P, int M, int L, int H,
+                               const DeviceInfo& dev, cudaStream_t s) {
   int nt = 0, vpt = 0, cb = 1;
   row_shape(H, &nt, &vpt, &cb);
+  if (hq && cb != 1) return cudaErrorInvalidValue;  // e4m3 rows need the whole row in one CTA
   auto run = [&](auto kern) {
     const size_t smem = static_cast<size_t>(kFwdStages) * vpt * 2 * nt * 16;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
@@ -590,12 +742,35 @@ cudaError_t launch_ln_gate_fwd(const void* Z, const void* stats, const void* nx_
     return launch_pdl(kern, dim3(P * cpr * cb), dim3(nt), smem, s, static_cast<const __nv_bfloat16*>(Z),
                       static_cast<const float4*>(stats), static_cast<const __nv_bfloat16*>(nx_w),
                       static_cast<const __nv_bfloat16*>(nx_b), static_cast<const __nv_bfloat16*>(ng_w),
-                      static_cast<const __nv_bfloat16*>(ng_b), static_cast<__nv_bfloat16*>(Hl), M, L, H, cpr, cb,
-                      dev.err);
+                      static_cast<const __nv_bfloat16*>(ng_b), static_cast<__nv_bfloat16*>(Hl), hq, hs, M, L, H, cpr,
+                      cb, dev.err);
   };
-  if (nt == 256 && vpt == 1) return run(ln_gate_fwd_kernel<256, 1>);
-  if (nt == 256) return run(ln_gate_fwd_kernel<256, 2>);
-  return run(ln_gate_fwd_kernel<512, 2>);
+  if (hq) {
+    if (nt == 256 && vpt == 1) return run(ln_gate_fwd_kernel<256, 1, true>);
+    if (nt == 256) return run(ln_gate_fwd_kernel<256, 2, true>);
+    return run(ln_gate_fwd_kernel<512, 2, true>);
+  }
+  if (nt == 256 && vpt == 1) return run(ln_gate_fwd_kernel<256, 1, false>);
+  if (nt == 256) return run(ln_gate_fwd_kernel<256, 2, false>);
+  return run(ln_gate_fwd_kernel<512, 2, false>);
+}
+
+cudaError_t launch_quant_rows(const void* x, void* q, float* scale, int64_t rows, int D, int T, int M,
+                              const DeviceInfo& dev, cudaStream_t s) {
+  int64_t blocks = (rows + 7) / 8;
+  if (blocks > 16 * dev.num_sms) blocks = 16 * dev.num_sms;
+  return launch_pdl(quant_rows_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, s,
+                    static_cast<const __nv_bfloat16*>(x), static_cast<uint8_t*>(q), scale, rows, D, T, M, dev.err);
+}
+
+cudaError_t launch_quant_weight(const void* w, float* scale, void* q, int G, int K, int N, const DeviceInfo& dev,
+                                cudaStream_t s) {
+  cudaError_t e = launch_pdl(col_scale_kernel, dim3((N + 255) / 256, G), dim3(256), 0, s,
+                             static_cast<const __nv_bfloat16*>(w), scale, K, N, dev.err);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(transpose_quant_kernel, dim3((N + 63) / 64, (K + 63) / 64, G), dim3(256), 0, s,
+                    static_cast<const __nv_bfloat16*>(w), static_cast<const float*>(scale), static_cast<uint8_t*>(q), K,
+                    N, dev.err);
 }
 
 cudaError_t launch_ln_gate_bwd_rowsum(const void* Z, const void* stats, const void* dHl, const void* nx_w,

@@ -13,7 +13,7 @@ import torch
 from ._lib import FFNShape, TraceEntry, check, load
 
 __all__ = [
-    "gemm_fp8", "ffn_shape", "a2a_ffn_forward", "a2a_ffn_backward", "A2AFFN", "a2a_ffn",
+    "gemm_fp8", "ffn_shape", "a2a_ffn_forward", "a2a_ffn_backward", "a2a_ffn_fp8_pack_weights", "a2a_ffn_forward_fp8", "A2AFFN", "a2a_ffn",
     "a2a_dispatch", "a2a_combine", "tp_swiglu", "tp_swiglu_backward", "TPSwiGLU", "tp_swiglu_layer",
     "tp_linear", "tp_linear_backward", "TPLinear", "tp_linear_layer", "device_status", "debug_wait_timeout",
     "FFN_PARAM_NAMES", "trace_begin", "trace_end",
@@ -108,6 +108,57 @@ def a2a_ffn_forward(inputs: torch.Tensor, params: dict, eps: float = 1e-5, saved
         check(lib.dg_a2a_ffn_fwd(ctypes.byref(sh), _ptr(inputs), *[_ptr(params[n]) for n in FFN_PARAM_NAMES],
                                  _ptr(out), _ptr(saved), saved.numel(), ctypes.c_void_p(_stream(dev))))
     return out, saved
+
+
+def a2a_ffn_fp8_pack_weights(params: dict, P: int, B: int, T: int, D: int, eps: float = 1e-5,
+                             packed: torch.Tensor | None = None) -> torch.Tensor:
+    """e4m3 copy of w1 and wout (per output column scales) for a2a_ffn_forward_fp8."""
+    lib = load()
+    k = params["w1"].shape[-1] // (2 * D)
+    shapes = _ffn_param_shapes(P, B, T, D, k)
+    dev = params["w1"].device
+    _need(params["w1"], "w1", torch.bfloat16, shapes["w1"], dev)
+    _need(params["wout"], "wout", torch.bfloat16, shapes["wout"], dev)
+    sh = FFNShape(P, B, T, D, k, eps)
+    nbytes = lib.dg_a2a_ffn_fp8_weights_bytes(ctypes.byref(sh))
+    if nbytes == 0:
+        check(lib.dg_a2a_ffn_fp8_pack_weights(ctypes.byref(sh), None, None, None, 0, None))
+    if packed is None:
+        packed = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    with torch.cuda.device(dev):
+        check(lib.dg_a2a_ffn_fp8_pack_weights(ctypes.byref(sh), _ptr(params["w1"]), _ptr(params["wout"]), _ptr(packed),
+                                              packed.numel(), ctypes.c_void_p(_stream(dev))))
+    return packed
+
+
+def a2a_ffn_forward_fp8(inputs: torch.Tensor, params: dict, packed: torch.Tensor, eps: float = 1e-5,
+                        workspace: torch.Tensor | None = None, out: torch.Tensor | None = None) -> torch.Tensor:
+    """The A2A FFN forward with both GEMMs on e4m3 operands (inference).
+
+    `packed` comes from a2a_ffn_fp8_pack_weights; b1, bout and the LayerNorm
+    parameters are taken from `params` (bf16).  Returns output [P,B,T,D] bf16."""
+    lib = load()
+    P, B, T, D = inputs.shape
+    k = params["w1"].shape[-1] // (2 * D)
+    shapes = _ffn_param_shapes(P, B, T, D, k)
+    dev = inputs.device
+    _need(inputs, "inputs", torch.bfloat16, shapes["inputs"])
+    names = ("b1", "bout", "nx_w", "nx_b", "ng_w", "ng_b")
+    for name in names:
+        _need(params[name], name, torch.bfloat16, shapes[name], dev)
+    sh = FFNShape(P, B, T, D, k, eps)
+    nbytes = lib.dg_a2a_ffn_fp8_workspace_bytes(ctypes.byref(sh))
+    if nbytes == 0:
+        check(lib.dg_a2a_ffn_fwd_fp8(ctypes.byref(sh), *([None] * 3), *([None] * 7), None, 0, None))
+    if workspace is None:
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    if out is None:
+        out = torch.empty(shapes["inputs"], dtype=torch.bfloat16, device=dev)
+    with torch.cuda.device(dev):
+        check(lib.dg_a2a_ffn_fwd_fp8(ctypes.byref(sh), _ptr(inputs), _ptr(packed), packed.numel(),
+                                     *[_ptr(params[n]) for n in names], _ptr(out), _ptr(workspace), workspace.numel(),
+                                     ctypes.c_void_p(_stream(dev))))
+    return out
 
 
 def a2a_ffn_backward(inputs: torch.Tensor, params: dict, saved: torch.Tensor, dY: torch.Tensor,

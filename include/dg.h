@@ -156,6 +156,47 @@ dg_status dg_a2a_combine(int32_t P, int32_t B, int32_t T, int32_t D,
                          const void* ylocal, void* output, void* stream);
 
 /* ------------------------------------------------------------------------
+ * A2A FFN forward with both GEMMs on e4m3 operands.
+ *
+ * Source: the A2A-FFN project statement (problems/p04), "Public checks and
+ * instructor coverage", which lists optional FP8 paths of the layer without a
+ * recipe.  Reading taken here: GEMM1 and GEMM2 run on e4m3 operands with fp32
+ * accumulation and dequantise in their epilogues; everything else (bias,
+ * LayerNorm statistics and normalise-and-gate, dispatch/combine) is the bf16
+ * forward's.  Activations (the input rows and Hl) carry one scale per row,
+ * weights one scale per output column; a scale is amax / 448 (1 for an
+ * all-zero vector) and a code is the e4m3 value nearest to x / scale
+ * (binary32 division, ties to even, saturating at +-448).
+ *
+ * dg_a2a_ffn_fp8_pack_weights quantises w1 and wout once into `packed`
+ * (dg_a2a_ffn_fp8_weights_bytes), laid out with 256-byte aligned regions:
+ *   w1 codes [T, 2H, D] e4m3, w1 scales [T, 2H] f32,
+ *   wout codes [T, D, H] e4m3, wout scales [T, D] f32
+ * (T = P*L problems in the order of w1's [P, L] leading dimensions).
+ * dg_a2a_ffn_fwd_fp8 computes `output` (bf16 [P,B,T,D]) from bf16 inputs,
+ * the packed weights, and the bf16 b1, bout and LayerNorm parameters (layouts
+ * of dg_a2a_ffn_fwd).  Its workspace (dg_a2a_ffn_fp8_workspace_bytes) starts
+ * with the input codes [P,B,T,D] e4m3 followed, at the next 256-byte
+ * boundary, by their scales [T, P*B] f32 (scale of input row (s, b, t) at
+ * t*P*B + s*B + b); both are left there after the call.
+ * Requirements: those of dg_a2a_ffn_fwd, D % 16 == 0, H % 16 == 0, H <= 8192
+ * (an e4m3 Hl row is scaled inside one CTA); otherwise the query functions
+ * return 0 and the calls fail with DG_ERR_INVALID_ARGUMENT / UNSUPPORTED.
+ * No backward: training uses the bf16 path.
+ * ------------------------------------------------------------------------ */
+size_t dg_a2a_ffn_fp8_weights_bytes(const dg_ffn_shape* shape);
+size_t dg_a2a_ffn_fp8_workspace_bytes(const dg_ffn_shape* shape);
+
+dg_status dg_a2a_ffn_fp8_pack_weights(const dg_ffn_shape* shape, const void* w1, const void* wout,
+                                      void* packed, size_t packed_bytes, void* stream);
+
+dg_status dg_a2a_ffn_fwd_fp8(const dg_ffn_shape* shape, const void* inputs,
+                             const void* packed, size_t packed_bytes,
+                             const void* b1, const void* bout,
+                             const void* nx_w, const void* nx_b, const void* ng_w, const void* ng_b,
+                             void* output, void* ws, size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
  * (c) SwiGLU column/row-parallel pair over W tensor-parallel shards.
  *
  * Source: "Add dist GEMM attention and FFN backend" (torchtitan PR #4044),

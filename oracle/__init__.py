@@ -782,3 +782,32 @@ def ffn_forward_fp8(sh: FFNShape, inputs, prm: dict, decoded: bool = False) -> n
                 (e4m3_to_f64(woq) * so.astype(np.float64)[None, :]) + p["bout"][r, l]
             out[:, :, t, :] = Y.reshape(P, B, D)
     return out
+
+
+def ffn_forward_fp8_rows(sh: FFNShape, inputs_bits, prm: dict, out_rows) -> np.ndarray:
+    """Selected output rows (flat indices into [P, B, T]) of ffn_forward_fp8.
+
+    An output row (s, b, t) needs its own input row (scaled on its own), the
+    problem t's weights (scaled per column over the whole weight) and its own
+    Hl row (scaled on its own), so a row subset is exact.
+    """
+    P, B, T, D, H, L = sh.P, sh.B, sh.T, sh.D, sh.H, sh.L
+    x = bf16_to_f64(np.asarray(inputs_bits)).reshape(P * B * T, D)
+    rows = np.asarray(out_rows, dtype=np.int64)
+    res = np.zeros((rows.size, D))
+    p = {k: bf16_to_f64(np.asarray(v)) for k, v in prm.items()}
+    ts = rows % T
+    for t in np.unique(ts):
+        r, l = divmod(int(t), L)
+        sel = np.nonzero(ts == t)[0]
+        xq, sx = quantize_e4m3(x[rows[sel]], axis=1)
+        X = e4m3_to_f64(xq) * sx.astype(np.float64)[:, None]
+        w1q, s1 = quantize_e4m3(p["w1"][r, l], axis=0)
+        Z = X @ (e4m3_to_f64(w1q) * s1.astype(np.float64)[None, :]) + p["b1"][r, l]
+        a = layer_norm(Z[:, :H], p["nx_w"][r], p["nx_b"][r], sh.eps)
+        g = layer_norm(Z[:, H:], p["ng_w"][r], p["ng_b"][r], sh.eps)
+        hq, shs = quantize_e4m3((a * silu(g)).astype(np.float32), axis=1)
+        woq, so = quantize_e4m3(p["wout"][r, l], axis=0)
+        res[sel] = (e4m3_to_f64(hq) * shs.astype(np.float64)[:, None]) @ \
+            (e4m3_to_f64(woq) * so.astype(np.float64)[None, :]) + p["bout"][r, l]
+    return res

@@ -720,3 +720,11 @@ def test_ffn_forward_fp8_matches_torch_formulation():
     # and the quantised layer stays within e4m3 precision of the exact one
     ref = O.ffn_forward(sh, b["inputs"], b)
     assert np.abs(got - ref).max() / np.abs(ref).max() < 0.15
+
+
+def test_ffn_forward_fp8_rows_match_full():
+    sh = O.FFNShape(2, 3, 8, 32, 3)
+    t, b = _ffn_bits(sh, seed=22)
+    full = O.ffn_forward_fp8(sh, b["inputs"], b).reshape(-1, sh.D)
+    rows = np.array([0, 5, 17, 18, 31, sh.P * sh.B * sh.T - 1])
+    assert np.allclose(O.ffn_forward_fp8_rows(sh, b["inputs"], b, rows), full[rows], rtol=1e-13, atol=1e-13)
