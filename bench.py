@@ -666,6 +666,7 @@ PROFILE_CASES = {
     "ffn_fwd_small": "A2A FFN forward, P=8, B=512, T=8, D=1280, k=6 (the full shape with 8 token positions)",
     "ffn_small": "A2A FFN forward + backward, P=8, B=512, T=8, D=1280, k=6",
     "tp": "TP SwiGLU, S=8192, d=4096, ffn=14336, W=8",
+    "ffn_fp8_small": "A2A FFN forward on e4m3 GEMMs, P=8, B=512, T=8, D=1280, k=6",
 }
 
 
@@ -692,6 +693,12 @@ def run_profile_case(args):
             out, saved = dg.a2a_ffn_forward(x, params)
             if case == "ffn_small":
                 dg.a2a_ffn_backward(x, params, saved, dY)
+    elif case == "ffn_fp8_small":
+        t = synth.ffn_inputs(8, 512, 8, 1280, 6, seed=42, device=dev)
+        params = {n: t[n] for n in dg.FFN_PARAM_NAMES}
+        x = t["inputs"]
+        packed = dg.a2a_ffn_fp8_pack_weights(params, 8, 512, 8, 1280)
+        run = lambda: dg.a2a_ffn_forward_fp8(x, params, packed)
     elif case == "tp":
         xs, w13, w2 = synth.tp_swiglu_inputs(8192, 4096, 14336, 8, seed=7, device=dev)
         run = lambda: dg.tp_swiglu(xs, w13, w2)
