@@ -671,7 +671,7 @@ namespace {
 // e4m3 copy of the weights: w1 codes [T][2H][D] and scales [T][2H], wout codes
 // [T][D][H] and scales [T][D] (codes K-major for the GEMMs' B operands).
 struct Fp8WeightsLayout {
-  size_t w1q, s1, woq, so, total;
+  size_t w1q, s1, woq, so, i1, io, total;
 };
 Fp8WeightsLayout fp8_weights_layout(const FfnDims& f) {
   Fp8WeightsLayout l;
@@ -680,7 +680,9 @@ Fp8WeightsLayout fp8_weights_layout(const FfnDims& f) {
   l.s1 = round_up(T * 2 * H * D, 256);
   l.woq = round_up(l.s1 + T * 2 * H * 4, 256);
   l.so = round_up(l.woq + T * D * H, 256);
-  l.total = round_up(l.so + T * D * 4, 256);
+  l.i1 = round_up(l.so + T * D * 4, 256);  // inverse scales, used while packing
+  l.io = round_up(l.i1 + T * 2 * H * 4, 256);
+  l.total = round_up(l.io + T * D * 4, 256);
   return l;
 }
 
@@ -755,14 +757,14 @@ dg_status dg_a2a_ffn_fp8_pack_weights(const dg_ffn_shape* shape, const void* w1,
   cudaError_t e;
   {
     TraceScope trace("ffn_fp8_pack_w1", s, 0.0, 2.0 * wbytes);
-    e = launch_quant_weight(w1, reinterpret_cast<float*>(pk + wl.s1), pk + wl.w1q, static_cast<int>(f.T),
-                            static_cast<int>(f.D), static_cast<int>(2 * f.H), dev, s);
+    e = launch_quant_weight(w1, reinterpret_cast<float*>(pk + wl.s1), reinterpret_cast<float*>(pk + wl.i1),
+                            pk + wl.w1q, static_cast<int>(f.T), static_cast<int>(f.D), static_cast<int>(2 * f.H), dev, s);
   }
   if (e != cudaSuccess) return cuda_fail(e, "w1 quantisation launch");
   {
     TraceScope trace("ffn_fp8_pack_wout", s, 0.0, 2.0 * wobytes);
-    e = launch_quant_weight(wout, reinterpret_cast<float*>(pk + wl.so), pk + wl.woq, static_cast<int>(f.T),
-                            static_cast<int>(f.H), static_cast<int>(f.D), dev, s);
+    e = launch_quant_weight(wout, reinterpret_cast<float*>(pk + wl.so), reinterpret_cast<float*>(pk + wl.io),
+                            pk + wl.woq, static_cast<int>(f.T), static_cast<int>(f.H), static_cast<int>(f.D), dev, s);
   }
   return e == cudaSuccess ? DG_OK : cuda_fail(e, "wout quantisation launch");
 }

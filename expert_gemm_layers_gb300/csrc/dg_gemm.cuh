@@ -517,15 +517,18 @@ __global__ void __launch_bounds__(GemmCfg<kFp8, kAMN, kBMN, kEpi, kPair, kBN>::N
             // per-row scale of the e4m3 A rows, per-column scale of the e4m3 B rows
             const int row = row0 + lane;
             const float rsc = row < p.M ? __ldg(p.row_scale + static_cast<int64_t>(g) * p.row_scale_g + row) : 0.0f;
+            const float2 rs2 = make_float2(rsc, rsc);
             const float* cp = p.col_scale + static_cast<int64_t>(g) * p.col_scale_g + n0 + 64 * j;
 #pragma unroll
             for (int q = 0; q < 16; ++q) {
               if (n0 + 64 * j + 4 * q < p.N) {
                 const float4 c4 = __ldg(reinterpret_cast<const float4*>(cp + 4 * q));
-                v[4 * q] *= rsc * c4.x;
-                v[4 * q + 1] *= rsc * c4.y;
-                v[4 * q + 2] *= rsc * c4.z;
-                v[4 * q + 3] *= rsc * c4.w;
+                const float2 a = mul2(mul2(make_float2(v[4 * q], v[4 * q + 1]), rs2), make_float2(c4.x, c4.y));
+                const float2 b = mul2(mul2(make_float2(v[4 * q + 2], v[4 * q + 3]), rs2), make_float2(c4.z, c4.w));
+                v[4 * q] = a.x;
+                v[4 * q + 1] = a.y;
+                v[4 * q + 2] = b.x;
+                v[4 * q + 3] = b.y;
               }
             }
           }
@@ -538,9 +541,9 @@ __global__ void __launch_bounds__(GemmCfg<kFp8, kAMN, kBMN, kEpi, kPair, kBN>::N
                 const uint32_t bw[4] = {bv.x, bv.y, bv.z, bv.w};
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                  const float2 b2 = unpack_bf16x2(bw[e]);
-                  v[8 * q + 2 * e] += b2.x;
-                  v[8 * q + 2 * e + 1] += b2.y;
+                  const float2 sum = add2(make_float2(v[8 * q + 2 * e], v[8 * q + 2 * e + 1]), unpack_bf16x2(bw[e]));
+                  v[8 * q + 2 * e] = sum.x;
+                  v[8 * q + 2 * e + 1] = sum.y;
                 }
               }
             }
@@ -557,15 +560,26 @@ __global__ void __launch_bounds__(GemmCfg<kFp8, kAMN, kBMN, kEpi, kPair, kBN>::N
           const int usplit = min(max(p.ln_H - c0, 0), nvalid);  // columns [0, usplit) are U
           float mean, m2;
           if (nvalid == 64 && (usplit == 0 || usplit == 64)) {
-            float sum = 0.0f, q = 0.0f;
+            // two passes over the chunk, each with four independent packed
+            // accumulators (short dependency chains)
+            float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                             make_float2(0.f, 0.f)};
 #pragma unroll
-            for (int i = 0; i < 64; ++i) sum += v[i];
-            mean = sum * (1.0f / 64.0f);
+            for (int i = 0; i < 32; ++i) acc[i & 3] = add2(acc[i & 3], make_float2(v[2 * i], v[2 * i + 1]));
+            const float2 s01 = add2(acc[0], acc[1]), s23 = add2(acc[2], acc[3]);
+            const float2 s4 = add2(s01, s23);
+            mean = (s4.x + s4.y) * (1.0f / 64.0f);
+            const float2 nm = make_float2(-mean, -mean);
+            float2 sq[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                            make_float2(0.f, 0.f)};
 #pragma unroll
-            for (int i = 0; i < 64; ++i) {
-              const float d = v[i] - mean;
-              q = fmaf(d, d, q);
+            for (int i = 0; i < 32; ++i) {
+              const float2 d = add2(make_float2(v[2 * i], v[2 * i + 1]), nm);
+              sq[i & 3] = fma2(d, d, sq[i & 3]);
             }
+            const float2 q01 = add2(sq[0], sq[1]), q23 = add2(sq[2], sq[3]);
+            const float2 q4 = add2(q01, q23);
+            const float q = q4.x + q4.y;
             (usplit == 64 ? st_u : st_g).merge(64.0f, mean, q);
           } else {
             if (usplit > 0) {

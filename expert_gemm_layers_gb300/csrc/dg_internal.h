@@ -208,13 +208,14 @@ cudaError_t launch_ln_gate_fwd(const void* Z, const void* stats, const void* nx_
                                const void* ng_b, void* Hl, uint8_t* hq, float* hs, int P, int M, int L, int H,
                                const DeviceInfo& dev, cudaStream_t s);
 
-// e4m3 operands of the FP8 path (scale = amax / 448 per row or output column):
-// input rows [P*B*T, D] -> codes in place of each row and scale[t*M + s*B + b];
-// weight [G][K][N] -> scale[G][N] and codes [G][N][K] (K-major).
+// e4m3 operands of the FP8 path (per row or output column: scale = amax / 448,
+// code = e4m3(x * 448 / amax)): input rows [P*B*T, D] -> codes in place of
+// each row and scale[t*M + s*B + b]; weight [G][K][N] -> scale and inverse
+// scale [G][N] and codes [G][N][K] (K-major).
 cudaError_t launch_quant_rows(const void* x, void* q, float* scale, int64_t rows, int D, int T, int M,
                               const DeviceInfo& dev, cudaStream_t s);
-cudaError_t launch_quant_weight(const void* w, float* scale, void* q, int G, int K, int N, const DeviceInfo& dev,
-                                cudaStream_t s);
+cudaError_t launch_quant_weight(const void* w, float* scale, float* inv, void* q, int G, int K, int N,
+                                const DeviceInfo& dev, cudaStream_t s);
 
 
 // Backward of the gate and both LayerNorms, pass 1: per-row sums

@@ -97,14 +97,17 @@ __device__ __forceinline__ float block_max(float v, float (*sm)[kMaxRowWarps], i
   return w;
 }
 
-// e4m3 code of x / scale: binary32 division, round to nearest even, saturating
-// at +-448 (the code decision of the per-row / per-column quantisation).
-__device__ __forceinline__ uint32_t e4m3_code(float x, float scale) {
-  return static_cast<uint32_t>(__nv_cvt_float_to_fp8(__fdiv_rn(x, scale), __NV_SATFINITE, __NV_E4M3));
+// e4m3 code of x * inv (inv = 448 / amax): binary32 product, round to
+// nearest even, saturating at +-448 (the code decision of the per-row /
+// per-column quantisation).
+__device__ __forceinline__ uint32_t e4m3_code(float x, float inv) {
+  return static_cast<uint32_t>(__nv_cvt_float_to_fp8(__fmul_rn(x, inv), __NV_SATFINITE, __NV_E4M3));
 }
 
-// Scale of a vector whose largest magnitude is amax: amax / 448, or 1 for zeros.
+// Scale (amax / 448) and inverse scale (448 / amax) of a vector whose largest
+// magnitude is amax; both 1 for an all-zero vector.
 __device__ __forceinline__ float e4m3_scale(float amax) { return amax > 0.0f ? __fdiv_rn(amax, 448.0f) : 1.0f; }
+__device__ __forceinline__ float e4m3_inv(float amax) { return amax > 0.0f ? __fdiv_rn(448.0f, amax) : 1.0f; }
 
 // Per-thread asynchronous copies into shared memory (cp.async): a thread
 // copies exactly the bytes it will read back itself, so a multi-stage ring
@@ -253,7 +256,8 @@ __global__ void __launch_bounds__(NT, 512 / NT) ln_gate_fwd_kernel(
                             pack_bf16x2(o[j][4], o[j][5]), pack_bf16x2(o[j][6], o[j][7])));
       }
     } else {
-      const float scale = e4m3_scale(block_max(amax, red_max, static_cast<int>(i & 1)));
+      const float rmax = block_max(amax, red_max, static_cast<int>(i & 1));
+      const float inv = e4m3_inv(rmax);
       uint8_t* qrow = hq + row * static_cast<int64_t>(H);
 #pragma unroll
       for (int j = 0; j < VPT; ++j) {
@@ -261,12 +265,12 @@ __global__ void __launch_bounds__(NT, 512 / NT) ln_gate_fwd_kernel(
         if (v < nvec) {
           uint32_t c[8];
 #pragma unroll
-          for (int e = 0; e < 8; ++e) c[e] = e4m3_code(o[j][e], scale);
+          for (int e = 0; e < 8; ++e) c[e] = e4m3_code(o[j][e], inv);
           *reinterpret_cast<uint2*>(qrow + 8 * v) =
               make_uint2(c[0] | (c[1] << 8) | (c[2] << 16) | (c[3] << 24), c[4] | (c[5] << 8) | (c[6] << 16) | (c[7] << 24));
         }
       }
-      if (threadIdx.x == 0) hs[row] = scale;
+      if (threadIdx.x == 0) hs[row] = e4m3_scale(rmax);
     }
   }
   cp_async_wait<0>();
@@ -299,28 +303,29 @@ __global__ void quant_rows_kernel(const __nv_bfloat16* __restrict__ x, uint8_t* 
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-    const float sc = e4m3_scale(amax);
+    const float inv = e4m3_inv(amax);
     uint8_t* qr = q + row * D;
     for (int c = 8 * lane; c < D; c += 256) {
       float f[8];
       unpack8(__ldg(reinterpret_cast<const uint4*>(xr + c)), f);
       uint32_t k[8];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) k[e] = e4m3_code(f[e], sc);
+      for (int e = 0; e < 8; ++e) k[e] = e4m3_code(f[e], inv);
       *reinterpret_cast<uint2*>(qr + c) =
           make_uint2(k[0] | (k[1] << 8) | (k[2] << 16) | (k[3] << 24), k[4] | (k[5] << 8) | (k[6] << 16) | (k[7] << 24));
     }
     if (lane == 0) {
       const int64_t sb = row / T;  // s*B + b
       const int t = static_cast<int>(row - sb * T);
-      scale[static_cast<int64_t>(t) * M + sb] = sc;
+      scale[static_cast<int64_t>(t) * M + sb] = e4m3_scale(amax);
     }
   }
 }
 
-// Weight [G][K][N] (N contiguous): scale[g][n] = amax over k / 448.
-__global__ void col_scale_kernel(const __nv_bfloat16* __restrict__ w, float* __restrict__ scale, int K, int N,
-                                 const uint32_t* err) {
+// Weight [G][K][N] (N contiguous): scale[g][n] = amax over k / 448 and
+// inv[g][n] = 448 / amax.
+__global__ void col_scale_kernel(const __nv_bfloat16* __restrict__ w, float* __restrict__ scale,
+                                 float* __restrict__ inv, int K, int N, const uint32_t* err) {
   griddep_wait();
   if (ld_volatile_u32(err) != 0u) return;
   const int g = blockIdx.y;
@@ -330,11 +335,12 @@ __global__ void col_scale_kernel(const __nv_bfloat16* __restrict__ w, float* __r
   float amax = 0.0f;
   for (int k = 0; k < K; ++k) amax = fmaxf(amax, fabsf(__bfloat162float(p[static_cast<int64_t>(k) * N])));
   scale[static_cast<int64_t>(g) * N + n] = e4m3_scale(amax);
+  inv[static_cast<int64_t>(g) * N + n] = e4m3_inv(amax);
 }
 
 // Weight [G][K][N] -> codes [G][N][K] (K contiguous: the K-major B operand of
 // an e4m3 GEMM), through a 64 x 64 shared-memory tile.  256 threads.
-__global__ void transpose_quant_kernel(const __nv_bfloat16* __restrict__ w, const float* __restrict__ scale,
+__global__ void transpose_quant_kernel(const __nv_bfloat16* __restrict__ w, const float* __restrict__ inv,
                                        uint8_t* __restrict__ q, int K, int N, const uint32_t* err) {
   __shared__ float tile[64][65];
   griddep_wait();
@@ -357,12 +363,12 @@ __global__ void transpose_quant_kernel(const __nv_bfloat16* __restrict__ w, cons
     const int nr = threadIdx.x >> 2, kc = (threadIdx.x & 3) * 16;
     const int n = n0 + nr;
     if (n < N) {
-      const float sc = scale[static_cast<int64_t>(g) * N + n];
+      const float iv = inv[static_cast<int64_t>(g) * N + n];
       uint8_t* qn = q + (static_cast<int64_t>(g) * N + n) * K;
 #pragma unroll
       for (int e = 0; e < 16; ++e) {
         const int k = k0 + kc + e;
-        if (k < K) qn[k] = static_cast<uint8_t>(e4m3_code(tile[kc + e][nr], sc));
+        if (k < K) qn[k] = static_cast<uint8_t>(e4m3_code(tile[kc + e][nr], iv));
       }
     }
   }
@@ -763,13 +769,13 @@ cudaError_t launch_quant_rows(const void* x, void* q, float* scale, int64_t rows
                     static_cast<const __nv_bfloat16*>(x), static_cast<uint8_t*>(q), scale, rows, D, T, M, dev.err);
 }
 
-cudaError_t launch_quant_weight(const void* w, float* scale, void* q, int G, int K, int N, const DeviceInfo& dev,
-                                cudaStream_t s) {
+cudaError_t launch_quant_weight(const void* w, float* scale, float* inv, void* q, int G, int K, int N,
+                                const DeviceInfo& dev, cudaStream_t s) {
   cudaError_t e = launch_pdl(col_scale_kernel, dim3((N + 255) / 256, G), dim3(256), 0, s,
-                             static_cast<const __nv_bfloat16*>(w), scale, K, N, dev.err);
+                             static_cast<const __nv_bfloat16*>(w), scale, inv, K, N, dev.err);
   if (e != cudaSuccess) return e;
   return launch_pdl(transpose_quant_kernel, dim3((N + 63) / 64, (K + 63) / 64, G), dim3(256), 0, s,
-                    static_cast<const __nv_bfloat16*>(w), static_cast<const float*>(scale), static_cast<uint8_t*>(q), K,
+                    static_cast<const __nv_bfloat16*>(w), static_cast<const float*>(inv), static_cast<uint8_t*>(q), K,
                     N, dev.err);
 }
 

@@ -165,13 +165,14 @@ dg_status dg_a2a_combine(int32_t P, int32_t B, int32_t T, int32_t D,
  * LayerNorm statistics and normalise-and-gate, dispatch/combine) is the bf16
  * forward's.  Activations (the input rows and Hl) carry one scale per row,
  * weights one scale per output column; a scale is amax / 448 (1 for an
- * all-zero vector) and a code is the e4m3 value nearest to x / scale
- * (binary32 division, ties to even, saturating at +-448).
+ * all-zero vector) and a code is the e4m3 value nearest to x * (448 / amax)
+ * (binary32 quotient and product, ties to even, saturating at +-448).
  *
  * dg_a2a_ffn_fp8_pack_weights quantises w1 and wout once into `packed`
  * (dg_a2a_ffn_fp8_weights_bytes), laid out with 256-byte aligned regions:
  *   w1 codes [T, 2H, D] e4m3, w1 scales [T, 2H] f32,
- *   wout codes [T, D, H] e4m3, wout scales [T, D] f32
+ *   wout codes [T, D, H] e4m3, wout scales [T, D] f32,
+ *   w1 inverse scales [T, 2H] f32, wout inverse scales [T, D] f32
  * (T = P*L problems in the order of w1's [P, L] leading dimensions).
  * dg_a2a_ffn_fwd_fp8 computes `output` (bf16 [P,B,T,D]) from bf16 inputs,
  * the packed weights, and the bf16 b1, bout and LayerNorm parameters (layouts

@@ -714,9 +714,10 @@ def linear_reduce_scatter_backward(a_ranks, weight, dy_shards, W: int, decoded: 
 # operands with fp32 accumulation; activations (the dispatched input rows and
 # Hl) carry one scale per row, weights one scale per output column; a scale is
 # amax / 448 (1 for an all-zero vector) and a code is the e4m3 value nearest to
-# x / scale, ties to the even code, saturating at +-448.  The code decision is
-# taken in fp32 (amax, the division and x / scale are binary32 operations), as
-# on the GPU.  Everything after the decoded codes is fp64.
+# x * (448 / amax), ties to the even code, saturating at +-448.  The code
+# decision is taken in binary32 (amax, the quotient 448 / amax and the product
+# are binary32 operations), as on the GPU.  Everything after the decoded codes
+# is fp64.
 # --------------------------------------------------------------------------
 
 _E4M3_MAX = 448.0
@@ -744,12 +745,16 @@ def e4m3_rne(x) -> np.ndarray:
 def quantize_e4m3(x, axis: int):
     """e4m3 codes and binary32 scales of x (binary32 values) with one scale per
     slice along `axis` (axis=1: per row of a [rows, K] matrix; axis=0: per
-    column of a [K, N] matrix)."""
+    column of a [K, N] matrix).  code = e4m3_rne(x * inv), inv = 448 / amax,
+    scale = amax / 448 (inv = scale = 1 for an all-zero slice)."""
     x32 = np.asarray(x, dtype=np.float32)
     amax = np.max(np.abs(x32), axis=axis)
-    scale = np.where(amax > 0, amax / np.float32(_E4M3_MAX), np.float32(1.0)).astype(np.float32)
-    s = scale[:, None] if axis == 1 else scale[None, :]
-    return e4m3_rne((x32 / s).astype(np.float32)), scale
+    nz = amax > 0
+    safe = np.where(nz, amax, np.float32(1.0)).astype(np.float32)
+    scale = np.where(nz, safe / np.float32(_E4M3_MAX), np.float32(1.0)).astype(np.float32)
+    inv = np.where(nz, np.float32(_E4M3_MAX) / safe, np.float32(1.0)).astype(np.float32)
+    iv = inv[:, None] if axis == 1 else inv[None, :]
+    return e4m3_rne((x32 * iv).astype(np.float32)), scale
 
 
 def ffn_forward_fp8(sh: FFNShape, inputs, prm: dict, decoded: bool = False) -> np.ndarray:

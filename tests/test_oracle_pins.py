@@ -696,9 +696,14 @@ def test_ffn_forward_fp8_matches_torch_formulation():
     f64 = {k: torch.from_numpy(O.bf16_to_f64(v)) for k, v in b.items()}
 
     def q(x32, dim):
-        amax = x32.abs().amax(dim=dim, keepdim=True)
-        s = torch.where(amax > 0, amax / 448.0, torch.ones_like(amax)).to(torch.float32)
-        codes = (x32 / s).to(torch.float8_e4m3fn)
+        # torch's float32 division on the CPU is not correctly rounded, so the
+        # two quotients are taken in numpy binary32; torch casts to e4m3
+        amax = x32.abs().amax(dim=dim, keepdim=True).numpy()
+        nz = amax > 0
+        a = np.where(nz, amax, np.float32(1)).astype(np.float32)
+        s = torch.from_numpy(np.where(nz, a / np.float32(448), np.float32(1)).astype(np.float32))
+        inv = torch.from_numpy(np.where(nz, np.float32(448) / a, np.float32(1)).astype(np.float32))
+        codes = (x32 * inv).to(torch.float8_e4m3fn)
         return codes.to(torch.float64) * s.to(torch.float64)
 
     x = q(f64["inputs"].to(torch.float32).reshape(-1, D), 1).reshape(P, B, T, D)
