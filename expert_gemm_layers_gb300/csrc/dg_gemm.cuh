@@ -41,7 +41,7 @@ enum Epi : int32_t {
 
 // Wait-site codes recorded with a timeout.
 enum WaitSite : uint32_t {
-  SITE_EMPTY = 1, SITE_FULL = 2, SITE_TEMPTY = 3, SITE_TFULL = 4, SITE_CLOAD = 5, SITE_DRAIN = 6
+  SITE_EMPTY = 1, SITE_FULL = 2, SITE_TEMPTY = 3, SITE_TFULL = 4, SITE_CLOAD = 5, SITE_DRAIN = 6, SITE_PARAM = 7
 };
 
 struct GemmParams {
@@ -110,7 +110,10 @@ struct GemmCfg {
   static constexpr int ROW_BYTES = 128;               // K-block = one 128-byte swizzle row
   static constexpr int BK = kFp8 ? 128 : 64;          // K elements per stage
   static constexpr int K_STEPS = 4;                   // UMMA K = 32 bytes: 16 bf16 / 32 e4m3
-  static constexpr int STAGES = kPair ? 6 : 4;
+  // per-tile epilogue parameters staged in shared memory (bias, e4m3 column scales)
+  static constexpr bool HAS_BIAS = kEpi == EPI_BIAS || kEpi == EPI_BIAS_LNSTATS;
+  static constexpr bool HAS_SCALES = kFp8 && kEpi != EPI_FP8;
+  static constexpr int STAGES = kPair ? (HAS_SCALES ? 5 : 6) : 4;
   static constexpr int A_BYTES = BM * ROW_BYTES;      // 16 KB
   static constexpr int B_BYTES = B_ROWS * ROW_BYTES;  // 16 KB (pair) or 32 KB
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
@@ -122,9 +125,12 @@ struct GemmCfg {
   static constexpr int NACC = 2;                      // TMEM accumulators (double buffered)
   static constexpr uint32_t TMEM_COLS = NACC * ACC_STRIDE;
   static constexpr bool HALF_CHUNK = (BN_OUT % 64) == 32;  // a last 32-column chunk per tile
-  static constexpr int NUM_BARS = 2 * STAGES + 4 + 2 * EPI_WARPS + 1;
+  static constexpr int BIAS_BYTES = HAS_BIAS ? BN_OUT * 2 : 0;    // one tile's bias, bf16
+  static constexpr int SCALE_BYTES = HAS_SCALES ? BN_OUT * 4 : 0; // one tile's column scales, f32
+  static constexpr int PARAM_BYTES = 2 * (BIAS_BYTES + SCALE_BYTES);  // double buffered
+  static constexpr int NUM_BARS = 2 * STAGES + 4 + 2 * EPI_WARPS + 1 + 2;
   static constexpr int BAR_BYTES = 256;
-  static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + EPI_BYTES + BAR_BYTES;
+  static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + EPI_BYTES + PARAM_BYTES + BAR_BYTES;
   static constexpr uint32_t IDESC = umma_idesc(kFp8 ? 0u : 1u, kAMN, kBMN, BN, UMMA_M);
   static_assert(NUM_BARS * 8 + 4 <= BAR_BYTES, "barrier area");
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
@@ -182,14 +188,16 @@ __global__ void __launch_bounds__(GemmCfg<kFp8, kAMN, kBMN, kEpi, kPair, kBN>::N
   uint8_t* smem = smem_raw + pad;
   uint8_t* stage_base = smem;
   uint8_t* epi_base = smem + Cfg::STAGES * Cfg::STAGE_BYTES;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(epi_base + Cfg::EPI_BYTES);
+  uint8_t* param_base = epi_base + Cfg::EPI_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(param_base + Cfg::PARAM_BYTES);
   uint64_t* full = bars;
   uint64_t* empty = bars + Cfg::STAGES;
   uint64_t* tfull = bars + 2 * Cfg::STAGES;
   uint64_t* tempty = tfull + 2;
   uint64_t* cbar = tempty + 2;
   uint64_t* drain = cbar + 2 * Cfg::EPI_WARPS;
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* pready = drain + 1;  // [2]: a tile's epilogue parameters are in shared memory
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(pready + 2);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -210,6 +218,8 @@ __global__ void __launch_bounds__(GemmCfg<kFp8, kAMN, kBMN, kEpi, kPair, kBN>::N
     }
     for (int i = 0; i < 2 * Cfg::EPI_WARPS; ++i) mbar_init(&cbar[i], 1);
     mbar_init(drain, 1);
+    mbar_init(&pready[0], Cfg::EPI_WARPS);
+    mbar_init(&pready[1], Cfg::EPI_WARPS);
     fence_mbar_init();
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
@@ -446,6 +456,40 @@ __global__ void __launch_bounds__(GemmCfg<kFp8, kAMN, kBMN, kEpi, kPair, kBN>::N
       };
       if (use_c && nchunks > 0) issue_load(0, static_cast<int>(chunk_ctr & 1u));
 
+      // This tile's bias and column scales into shared memory (while the MMA
+      // runs); buffer `local & 1`, published by pready after every warp wrote
+      // its part.  A buffer is rewritten two tiles later, after every warp has
+      // passed the next tile's pready, i.e. finished reading it.
+      const int pb = local & 1;
+      const uint4* sbias = reinterpret_cast<const uint4*>(param_base + pb * Cfg::BIAS_BYTES);
+      const float4* sscale = reinterpret_cast<const float4*>(param_base + 2 * Cfg::BIAS_BYTES + pb * Cfg::SCALE_BYTES);
+      float rsc = 0.0f;
+      if (Cfg::HAS_BIAS || Cfg::HAS_SCALES) {
+        const int et = static_cast<int>(threadIdx.x) - 64;  // epilogue thread 0..127
+        if (Cfg::HAS_BIAS && et < Cfg::BN_OUT / 8) {
+          const int c = n0 + 8 * et;
+          const uint4 b = c < p.N ? __ldg(reinterpret_cast<const uint4*>(p.bias + static_cast<int64_t>(g) * p.bias_g_stride + c))
+                                  : make_uint4(0u, 0u, 0u, 0u);
+          const_cast<uint4*>(sbias)[et] = b;
+        }
+        if (Cfg::HAS_SCALES) {
+          if (et < Cfg::BN_OUT / 4) {
+            const int c = n0 + 4 * et;
+            const float4 sc = c < p.N ? __ldg(reinterpret_cast<const float4*>(p.col_scale + static_cast<int64_t>(g) * p.col_scale_g + c))
+                                      : make_float4(0.f, 0.f, 0.f, 0.f);
+            const_cast<float4*>(sscale)[et] = sc;
+          }
+          const int row = row0 + lane;
+          rsc = row < p.M ? __ldg(p.row_scale + static_cast<int64_t>(g) * p.row_scale_g + row) : 0.0f;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&pready[pb]);
+        if (!mbar_wait(&pready[pb], static_cast<uint32_t>(local >> 1) & 1u, p.err, SITE_PARAM)) {
+          ok = false;
+          break;
+        }
+      }
+
       if (!mbar_wait(&tfull[acc], (tphase >> acc) & 1u, p.err, SITE_TFULL)) {
         ok = false;
         break;
@@ -513,16 +557,13 @@ __global__ void __launch_bounds__(GemmCfg<kFp8, kAMN, kBMN, kEpi, kPair, kBN>::N
 #pragma unroll
             for (int i = 0; i < 64; ++i) v[i] *= p.alpha;
           }
-          if (kFp8 && kEpi != EPI_FP8) {
+          if (Cfg::HAS_SCALES) {
             // per-row scale of the e4m3 A rows, per-column scale of the e4m3 B rows
-            const int row = row0 + lane;
-            const float rsc = row < p.M ? __ldg(p.row_scale + static_cast<int64_t>(g) * p.row_scale_g + row) : 0.0f;
             const float2 rs2 = make_float2(rsc, rsc);
-            const float* cp = p.col_scale + static_cast<int64_t>(g) * p.col_scale_g + n0 + 64 * j;
 #pragma unroll
             for (int q = 0; q < 16; ++q) {
-              if (n0 + 64 * j + 4 * q < p.N) {
-                const float4 c4 = __ldg(reinterpret_cast<const float4*>(cp + 4 * q));
+              {
+                const float4 c4 = sscale[16 * j + q];
                 const float2 a = mul2(mul2(make_float2(v[4 * q], v[4 * q + 1]), rs2), make_float2(c4.x, c4.y));
                 const float2 b = mul2(mul2(make_float2(v[4 * q + 2], v[4 * q + 3]), rs2), make_float2(c4.z, c4.w));
                 v[4 * q] = a.x;
@@ -532,12 +573,11 @@ __global__ void __launch_bounds__(GemmCfg<kFp8, kAMN, kBMN, kEpi, kPair, kBN>::N
               }
             }
           }
-          if (kEpi == EPI_BIAS || kEpi == EPI_BIAS_LNSTATS) {
-            const __nv_bfloat16* bp = p.bias + static_cast<int64_t>(g) * p.bias_g_stride + n0 + 64 * j;
+          if (Cfg::HAS_BIAS) {
 #pragma unroll
             for (int q = 0; q < 8; ++q) {
-              if (n0 + 64 * j + 8 * q < p.N) {
-                const uint4 bv = __ldg(reinterpret_cast<const uint4*>(bp + 8 * q));
+              {
+                const uint4 bv = sbias[8 * j + q];
                 const uint32_t bw[4] = {bv.x, bv.y, bv.z, bv.w};
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
