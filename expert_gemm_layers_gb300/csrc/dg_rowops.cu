@@ -54,49 +54,6 @@ __device__ __forceinline__ bool block_aborted(const uint32_t* err) {
   return flag != 0u;
 }
 
-// Block-wide sums of N values (N <= 4); consecutive calls must alternate
-// `slot`, which makes a trailing barrier unnecessary.  After the barrier each
-// warp reduces the per-warp partials lane-parallel, so no second barrier and
-// no per-thread loop over all warps.
-template <int N>
-__device__ __forceinline__ void block_sum(float (&v)[N], float (*sm)[kMaxRowWarps][4], int slot) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nwarps = blockDim.x >> 5;
-#pragma unroll
-  for (int i = 0; i < N; ++i) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v[i] += __shfl_xor_sync(0xffffffffu, v[i], o);
-  }
-  if (lane == 0) {
-#pragma unroll
-    for (int i = 0; i < N; ++i) sm[slot][warp][i] = v[i];
-  }
-  __syncthreads();
-  float w[N];
-#pragma unroll
-  for (int i = 0; i < N; ++i) w[i] = lane < nwarps ? sm[slot][lane][i] : 0.0f;
-#pragma unroll
-  for (int i = 0; i < N; ++i) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) w[i] += __shfl_xor_sync(0xffffffffu, w[i], o);
-    v[i] = w[i];
-  }
-}
-
-// Block-wide maximum of one value; consecutive calls alternate `slot` (see block_sum).
-__device__ __forceinline__ float block_max(float v, float (*sm)[kMaxRowWarps], int slot) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nwarps = blockDim.x >> 5;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-  if (lane == 0) sm[slot][warp] = v;
-  __syncthreads();
-  float w = lane < nwarps ? sm[slot][lane] : 0.0f;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) w = fmaxf(w, __shfl_xor_sync(0xffffffffu, w, o));
-  return w;
-}
-
 // e4m3 code of x * inv (inv = 448 / amax): binary32 product, round to
 // nearest even, saturating at +-448 (the code decision of the per-row /
 // per-column quantisation).
@@ -158,14 +115,23 @@ __global__ void ln_stats_finalize_kernel(const float4* __restrict__ part, float4
 constexpr int kFwdStages = 4;
 
 // kFp8Out: instead of bf16 Hl, write each row as e4m3 codes with one scale per
-// row (row amax / 448) for an e4m3 GEMM2; the whole row is in one CTA.
+// row (row amax / 448) for an e4m3 GEMM2; the whole row is in one CTA.  The
+// row amax is a lagged block reduction: each warp publishes its share of row
+// i through one of four mbarrier-guarded slots and meanwhile quantises row
+// i - 1, whose shares are complete by then (a slot is reused four rows later,
+// after every warp has published row i - 2, so it has read row i - 4).
 template <int NT, int VPT, bool kFp8Out>
 __global__ void __launch_bounds__(NT, 512 / NT) ln_gate_fwd_kernel(
     const __nv_bfloat16* __restrict__ Z, const float4* __restrict__ stats, const __nv_bfloat16* __restrict__ gx,
     const __nv_bfloat16* __restrict__ bx, const __nv_bfloat16* __restrict__ gg, const __nv_bfloat16* __restrict__ bg,
     __nv_bfloat16* __restrict__ Hl, uint8_t* __restrict__ hq, float* __restrict__ hs, int M, int L, int H,
-    int ctas_per_rank, int col_blocks, const uint32_t* err) {
-  __shared__ float red_max[2][kMaxRowWarps];
+    int ctas_per_rank, int col_blocks, uint32_t* err) {
+  __shared__ float red_max[4][kMaxRowWarps];
+  __shared__ uint64_t rbar[4];
+  if (kFp8Out && threadIdx.x == 0) {
+    for (int b = 0; b < 4; ++b) mbar_init(&rbar[b], NT / 32);
+    fence_mbar_init();
+  }
   extern __shared__ uint4 ring[];  // [kFwdStages][VPT][2][NT]
   griddep_wait();
   if (block_aborted(err)) return;
@@ -215,6 +181,32 @@ __global__ void __launch_bounds__(NT, 512 / NT) ln_gate_fwd_kernel(
   for (int i = 0; i < kFwdStages - 1; ++i) issue(i);
   float4 st_next = n_mine > 0 ? stats[row0] : make_float4(0.f, 0.f, 0.f, 0.f);
   const float2 half2 = make_float2(0.5f, 0.5f);
+  // e4m3 output: the previous row's values wait here for its amax
+  float o_prev[VPT][8];
+  int64_t prev_row = 0;
+  auto finish_row = [&](int64_t k, int64_t krow) -> bool {
+    const int slot = static_cast<int>(k & 3);
+    const uint32_t parity = static_cast<uint32_t>(k >> 2) & 1u;
+    if (!__all_sync(0xffffffffu, mbar_wait(&rbar[slot], parity, err, 0x41u))) return false;  // warp-uniform
+    float m = (threadIdx.x & 31) < NT / 32 ? red_max[slot][threadIdx.x & 31] : 0.0f;
+#pragma unroll
+    for (int o2 = 16; o2 > 0; o2 >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o2));
+    const float inv = e4m3_inv(m);
+    uint8_t* qrow = hq + krow * static_cast<int64_t>(H);
+#pragma unroll
+    for (int j = 0; j < VPT; ++j) {
+      const int v = vbase + threadIdx.x + NT * j;
+      if (v < nvec) {
+        uint32_t c[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) c[e] = e4m3_code(o_prev[j][e], inv);
+        *reinterpret_cast<uint2*>(qrow + 8 * v) =
+            make_uint2(c[0] | (c[1] << 8) | (c[2] << 16) | (c[3] << 24), c[4] | (c[5] << 8) | (c[6] << 16) | (c[7] << 24));
+      }
+    }
+    if (threadIdx.x == 0) hs[krow] = e4m3_scale(m);
+    return true;
+  };
   for (int64_t i = 0; i < n_mine; ++i) {
     issue(i + kFwdStages - 1);
     const int64_t row = row0 + i * stride;
@@ -256,23 +248,23 @@ __global__ void __launch_bounds__(NT, 512 / NT) ln_gate_fwd_kernel(
                             pack_bf16x2(o[j][4], o[j][5]), pack_bf16x2(o[j][6], o[j][7])));
       }
     } else {
-      const float rmax = block_max(amax, red_max, static_cast<int>(i & 1));
-      const float inv = e4m3_inv(rmax);
-      uint8_t* qrow = hq + row * static_cast<int64_t>(H);
+      float wmax = amax;
 #pragma unroll
-      for (int j = 0; j < VPT; ++j) {
-        const int v = vbase + threadIdx.x + NT * j;
-        if (v < nvec) {
-          uint32_t c[8];
-#pragma unroll
-          for (int e = 0; e < 8; ++e) c[e] = e4m3_code(o[j][e], inv);
-          *reinterpret_cast<uint2*>(qrow + 8 * v) =
-              make_uint2(c[0] | (c[1] << 8) | (c[2] << 16) | (c[3] << 24), c[4] | (c[5] << 8) | (c[6] << 16) | (c[7] << 24));
-        }
+      for (int o2 = 16; o2 > 0; o2 >>= 1) wmax = fmaxf(wmax, __shfl_xor_sync(0xffffffffu, wmax, o2));
+      const int slot = static_cast<int>(i & 3);
+      if ((threadIdx.x & 31) == 0) {
+        red_max[slot][threadIdx.x >> 5] = wmax;
+        mbar_arrive(&rbar[slot]);
       }
-      if (threadIdx.x == 0) hs[row] = e4m3_scale(rmax);
+      if (i > 0 && !finish_row(i - 1, prev_row)) return;
+#pragma unroll
+      for (int j = 0; j < VPT; ++j)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) o_prev[j][e] = o[j][e];
+      prev_row = row;
     }
   }
+  if (kFp8Out && n_mine > 0 && !finish_row(n_mine - 1, prev_row)) return;
   cp_async_wait<0>();
 }
 
