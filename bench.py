@@ -209,12 +209,6 @@ class Workload:
         self.dqkv = torch.randn_like(self.qkv, dtype=torch.float32).to(bf)
         self.dattn_y = torch.randn_like(self.attn_y, dtype=torch.float32).to(bf)
 
-    def inputs(self):
-        return [self.A, self.B, self.C, self.x, *self.params.values(), self.dY, self.xs, self.w13, self.w2]
-
-    def outputs(self):
-        return [self.D, self.out, *self.grads.values(), self.y]
-
     def step(self, marks=None):
         dg = self.dg
         dg.gemm_fp8(self.A, self.B, self.C, FP8["alpha"], FP8["beta"], out=self.D)
@@ -627,28 +621,80 @@ def run_attn_proj(w, args, dev, peaks):
                     for e in trace}}}
 
 
+# Per-step data of the end-to-end run: the step's activations come from the
+# host and its outputs go back; weights and weight gradients stay resident.
+E2E_INPUTS = ("A", "B", "C", "x", "dY", "xs")
+E2E_OUTPUTS = ("D", "out", "d_inputs", "y")
+
+
+def _io_get(w, name):
+    return w.grads["inputs"] if name == "d_inputs" else getattr(w, name)
+
+
+def _io_set(w, name, t):
+    if name == "d_inputs":
+        w.grads["inputs"] = t
+    else:
+        setattr(w, name, t)
+
+
 def run_e2e(w, args, dev, step_flops, world):
+    """The step through the public API with its data streamed in and out.
+
+    Each step copies its activations host -> device (pinned) and its outputs
+    device -> host; two device buffer sets and two copy streams let the upload
+    of step i+1 and the download of step i-1 overlap the compute of step i.
+    The timed region runs from the first upload to the last download."""
     import torch
-    ins = w.inputs()
-    outs = w.outputs()
-    h_in = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in ins]
-    for h, t in zip(h_in, ins):
-        h.copy_(t)
-    h_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
-    stream = torch.cuda.current_stream(dev)
+    sets = [{n: _io_get(w, n) for n in E2E_INPUTS + E2E_OUTPUTS}]
+    sets.append({n: torch.empty_like(t) for n, t in sets[0].items()})
+    h_in = {n: torch.empty(sets[0][n].shape, dtype=sets[0][n].dtype, pin_memory=True) for n in E2E_INPUTS}
+    for n in E2E_INPUTS:
+        h_in[n].copy_(sets[0][n])
+    h_out = {n: torch.empty(sets[0][n].shape, dtype=sets[0][n].dtype, pin_memory=True) for n in E2E_OUTPUTS}
+    compute = torch.cuda.current_stream(dev)
+    up, down = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
     steps = max(1, min(args.steps, 10))
+    ev = lambda: torch.cuda.Event(enable_timing=False)
+    in_ready, out_free, comp_done = [ev(), ev()], [ev(), ev()], [ev(), ev()]
+
+    def upload(k):
+        with torch.cuda.stream(up):
+            for n in E2E_INPUTS:
+                sets[k % 2][n].copy_(h_in[n], non_blocking=True)
+            in_ready[k % 2].record(up)
+
+    def download(k):
+        down.wait_event(comp_done[k % 2])
+        with torch.cuda.stream(down):
+            for n in E2E_OUTPUTS:
+                h_out[n].copy_(sets[k % 2][n], non_blocking=True)
+            out_free[k % 2].record(down)
+
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize(dev)
-    e0.record(stream)
-    for _ in range(steps):
-        for h, t in zip(h_in, ins):
-            t.copy_(h, non_blocking=True)
+    e0.record(compute)
+    up.wait_event(e0)
+    down.wait_event(e0)
+    upload(0)
+    for i in range(steps):
+        if i + 1 < steps:
+            if i >= 1:
+                up.wait_event(comp_done[(i + 1) % 2])   # step i-1 has read that set's inputs
+            upload(i + 1)
+        compute.wait_event(in_ready[i % 2])
+        if i >= 2:
+            compute.wait_event(out_free[i % 2])         # step i-2's outputs are on the host
+        for n, t in sets[i % 2].items():
+            _io_set(w, n, t)
         w.step()
-        for h, t in zip(h_out, outs):
-            h.copy_(t, non_blocking=True)
-    e1.record(stream)
+        comp_done[i % 2].record(compute)
+        download(i)
+    e1.record(down)
     torch.cuda.synchronize(dev)
+    for n, t in sets[0].items():
+        _io_set(w, n, t)
     ms = e0.elapsed_time(e1) / steps
     if world > 1:
         import torch.distributed as dist
@@ -657,8 +703,12 @@ def run_e2e(w, args, dev, step_flops, world):
         ms = float(tt.item())
     return {"value": round(world * step_flops / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
             "ms_per_step": round(ms, 3), "steps": steps,
-            "h2d_bytes_per_step": int(sum(t.numel() * t.element_size() for t in ins)),
-            "d2h_bytes_per_step": int(sum(t.numel() * t.element_size() for t in outs))}
+            "h2d_bytes_per_step": int(sum(h_in[n].numel() * h_in[n].element_size() for n in E2E_INPUTS)),
+            "d2h_bytes_per_step": int(sum(h_out[n].numel() * h_out[n].element_size() for n in E2E_OUTPUTS)),
+            "copies": "per step: activations (FP8 A, B, C; FFN inputs and dY; TP x) uploaded from pinned host "
+                      "memory, outputs (FP8 D, FFN output and d_inputs, TP y) downloaded; weights and weight "
+                      "gradients resident on the device; uploads/downloads on two copy streams overlap the "
+                      "previous/next step's compute (two device buffer sets)"}
 
 
 PROFILE_CASES = {
