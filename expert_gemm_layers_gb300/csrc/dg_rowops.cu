@@ -10,6 +10,9 @@
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
 
+#include <mutex>
+#include <vector>
+
 #include "dg_gate.cuh"
 #include "dg_internal.h"
 
@@ -691,6 +694,27 @@ __global__ void debug_wait_kernel(uint32_t* err, uint64_t limit_ns) {
 
 }  // namespace
 
+// The dynamic shared-memory limit of a kernel, raised once per device and
+// kernel (a host-side attribute: kept off the launch path, and out of the way
+// of stream capture).
+static cudaError_t smem_attr_once(const void* kern, int bytes) {
+  struct Entry {
+    const void* kern;
+    int device, bytes;
+  };
+  static std::mutex mu;
+  static std::vector<Entry> done;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> g(mu);
+  for (const Entry& x : done)
+    if (x.kern == kern && x.device == dev && x.bytes >= bytes) return cudaSuccess;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) done.push_back(Entry{kern, dev, bytes});
+  return e;
+}
+
 // CTAs per rank so that the row kernels fill every SM (each CTA stays on one rank).
 static int ctas_per_rank(const DeviceInfo& dev, const void* kernel, int threads, size_t smem, int P,
                          int64_t rank_rows) {
@@ -732,7 +756,7 @@ cudaError_t launch_ln_gate_fwd(const void* Z, const void* stats, const void* nx_
   if (hq && cb != 1) return cudaErrorInvalidValue;  // e4m3 rows need the whole row in one CTA
   auto run = [&](auto kern) {
     const size_t smem = static_cast<size_t>(kFwdStages) * vpt * 2 * nt * 16;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    cudaError_t e = smem_attr_once(reinterpret_cast<const void*>(kern), static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     // CTAs per rank and column block, so that the grid fills every SM
     const int cpr =
@@ -804,7 +828,7 @@ cudaError_t launch_ln_gate_bwd_apply(const void* Z, const void* stats, const voi
                                      cudaStream_t s) {
   dim3 grid((H + 8 * kApplyThreads - 1) / (8 * kApplyThreads), T, nsplit);
   const int smem = kApplyStages * (3 * kApplyThreads + 2 * (kApplyThreads / 32)) * 16;
-  cudaError_t e = cudaFuncSetAttribute(ln_gate_bwd_apply_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaError_t e = smem_attr_once(reinterpret_cast<const void*>(ln_gate_bwd_apply_kernel), smem);
   if (e != cudaSuccess) return e;
   return launch_pdl(ln_gate_bwd_apply_kernel, grid, dim3(kApplyThreads), smem, s,
       static_cast<const __nv_bfloat16*>(Z), static_cast<const float4*>(stats), static_cast<const float4*>(rowsum),
