@@ -343,6 +343,22 @@ def workload_config():
             "l2": "inputs larger than L2 (5.2 GB of operands per step; no L2 flush)"}
 
 
+def max_over_ranks(ms: float, world: int, device) -> float:
+    """The slowest rank's time (all ranks get it); the identity on one rank."""
+    if world <= 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+    tt = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+    return float(tt.item())
+
+
+def job_tflops(world: int, step_flops: float, ms: float) -> float:
+    """Whole-job throughput: every rank's step of work over the slowest rank's step time."""
+    return world * step_flops / (ms * 1e-3) / 1e12
+
+
 def run_dg(args, rank, world):
     import torch
     import torch.distributed as dist
@@ -398,11 +414,7 @@ def run_dg(args, rank, world):
     trace = dg.trace_end()
     clk = clocks.stop()
     barrier()
-    ms = t_start.elapsed_time(t_end) / args.steps
-    if world > 1:
-        tt = torch.tensor([ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms = float(tt.item())
+    ms = max_over_ranks(t_start.elapsed_time(t_end) / args.steps, world, dev)
     st, code = dg.device_status(dev)
     if st != 0:
         raise RuntimeError(f"device error word after the timed steps: {code:#x}")
@@ -460,7 +472,7 @@ def run_dg(args, rank, world):
     # end to end: inputs from pinned host memory in, results back to pinned host memory
     e2e = run_e2e(w, args, dev, step_flops, world)
 
-    value = world * step_flops / (ms * 1e-3) / 1e12
+    value = job_tflops(world, step_flops, ms)
     line = {
         "metric": "hot-path GEMM TFLOP/s (FP8 GEMM + A2A FFN fwd+bwd + TP SwiGLU)",
         "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
@@ -695,13 +707,8 @@ def run_e2e(w, args, dev, step_flops, world):
     torch.cuda.synchronize(dev)
     for n, t in sets[0].items():
         _io_set(w, n, t)
-    ms = e0.elapsed_time(e1) / steps
-    if world > 1:
-        import torch.distributed as dist
-        tt = torch.tensor([ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms = float(tt.item())
-    return {"value": round(world * step_flops / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+    ms = max_over_ranks(e0.elapsed_time(e1) / steps, world, dev)
+    return {"value": round(job_tflops(world, step_flops, ms), 2), "unit": "TFLOP/s",
             "ms_per_step": round(ms, 3), "steps": steps,
             "h2d_bytes_per_step": int(sum(h_in[n].numel() * h_in[n].element_size() for n in E2E_INPUTS)),
             "d2h_bytes_per_step": int(sum(h_out[n].numel() * h_out[n].element_size() for n in E2E_OUTPUTS)),
