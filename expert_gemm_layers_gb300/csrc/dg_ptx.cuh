@@ -98,6 +98,16 @@ static __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map)
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
+// Bulk (non-tensor) copy of `bytes` contiguous bytes global -> this CTA's
+// shared memory, completing on `bar` (addresses 16-byte aligned, size a
+// multiple of 16).
+static __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   smem_u32(dst)),
+               "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
+               : "memory");
+}
+
 static __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, uint64_t* bar,
                                                    int32_t c0, int32_t c1, int32_t c2) {
   asm volatile(

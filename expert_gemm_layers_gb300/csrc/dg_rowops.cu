@@ -438,6 +438,157 @@ __global__ void __launch_bounds__(kRowsumThreads, 2) ln_gate_bwd_rowsum_kernel(
   }
 }
 
+// Pass 1 for rows of up to 8192 columns, as a bulk-copy pipeline: one
+// producer warp streams whole rows (the U|G row of Z, the dHl row, the row's
+// statistics) into a ring of shared-memory slots with cp.async.bulk; eight
+// consumer warps each take every eighth 8-column vector of the row and
+// publish per-warp partial sums; when the producer recycles a slot it adds the
+// warps' partials in a fixed order and writes the row's four sums.  Each CTA
+// takes a contiguous range of rows (so the rank, and the affines kept in
+// registers, change at most a few times).
+constexpr int kRsRing = 4;
+constexpr int kRsConsumers = 8;
+constexpr int kRsThreads = 32 * (kRsConsumers + 1);
+
+__global__ void __launch_bounds__(kRsThreads, 1) ln_gate_bwd_rowsum_bulk_kernel(
+    const __nv_bfloat16* __restrict__ Z, const float4* __restrict__ stats, const __nv_bfloat16* __restrict__ dHl,
+    const __nv_bfloat16* __restrict__ gx, const __nv_bfloat16* __restrict__ bx, const __nv_bfloat16* __restrict__ gg,
+    const __nv_bfloat16* __restrict__ bg, float4* __restrict__ rowsum, int64_t rows, int M, int L, int H,
+    int slot_bytes, uint32_t* err) {
+  extern __shared__ __align__(128) uint8_t rs_smem[];
+  float4* part = reinterpret_cast<float4*>(rs_smem + kRsRing * slot_bytes);  // [kRsRing][kRsConsumers]
+  uint64_t* full = reinterpret_cast<uint64_t*>(part + kRsRing * kRsConsumers);
+  uint64_t* empty = full + kRsRing;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kRsRing; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kRsConsumers);
+    }
+    fence_mbar_init();
+  }
+  griddep_wait();
+  if (block_aborted(err)) return;  // (its barrier also publishes the barrier initialisation)
+  const int64_t per = (rows + gridDim.x - 1) / gridDim.x;
+  const int64_t r0 = min(rows, static_cast<int64_t>(blockIdx.x) * per);
+  const int n = static_cast<int>(min(rows, r0 + per) - r0);
+  const uint32_t zbytes = 4u * H, hbytes = 2u * H;
+  const int nvec = H >> 3;
+
+  if (warp == kRsConsumers) {
+    // ---------------------------------------------------------------- producer
+    if (lane == 0) {
+      auto finish = [&](int i) {  // the row's four sums from the warps' partials, in warp order
+        const float4* pp = part + (i % kRsRing) * kRsConsumers;
+        float4 a = pp[0];
+        for (int w = 1; w < kRsConsumers; ++w) {
+          a.x += pp[w].x;
+          a.y += pp[w].y;
+          a.z += pp[w].z;
+          a.w += pp[w].w;
+        }
+        rowsum[r0 + i] = a;
+      };
+      bool ok = true;
+      int issued = 0;
+      for (int i = 0; i < n && ok; ++i) {
+        const int s = i % kRsRing;
+        if (i >= kRsRing) {
+          if (!mbar_wait(&empty[s], static_cast<uint32_t>(i / kRsRing - 1) & 1u, err, 0x50u)) {
+            ok = false;
+            break;
+          }
+          finish(i - kRsRing);
+        }
+        uint8_t* slot = rs_smem + s * slot_bytes;
+        const int64_t row = r0 + i;
+        mbar_arrive_expect_tx(&full[s], zbytes + hbytes + 16u);
+        bulk_load(slot, Z + row * 2 * static_cast<int64_t>(H), zbytes, &full[s]);
+        bulk_load(slot + zbytes, dHl + row * static_cast<int64_t>(H), hbytes, &full[s]);
+        bulk_load(slot + zbytes + hbytes, stats + row, 16u, &full[s]);
+        issued = i + 1;
+      }
+      for (int i = max(0, issued - kRsRing); i < issued && ok; ++i) {
+        if (!mbar_wait(&empty[i % kRsRing], static_cast<uint32_t>(i / kRsRing) & 1u, err, 0x51u)) {
+          ok = false;
+          break;
+        }
+        finish(i);
+      }
+      // every copy issued has landed before the CTA may exit
+      for (int i = max(0, issued - kRsRing); i < issued; ++i) {
+        uint32_t dummy = 0;
+        if (!mbar_try_wait(&full[i % kRsRing], static_cast<uint32_t>(i / kRsRing) & 1u))
+          mbar_wait_slow(&full[i % kRsRing], static_cast<uint32_t>(i / kRsRing) & 1u, &dummy, 0x52u, kWaitLimitNs);
+      }
+    }
+  } else {
+    // ---------------------------------------------------------------- consumers
+    int t = static_cast<int>(r0 / M), nt = static_cast<int>(r0 - static_cast<int64_t>(t) * M);
+    int rank = -1;
+    Affine8 af[4];
+    for (int i = 0; i < n; ++i) {
+      const int s = i % kRsRing;
+      const bool ok = mbar_wait(&full[s], static_cast<uint32_t>(i / kRsRing) & 1u, err, 0x53u);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      if (t / L != rank) {
+        rank = t / L;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int v = warp * 32 + lane + 32 * kRsConsumers * j;
+          if (v < nvec) af[j] = load_affine8(gx, bx, gg, bg, static_cast<int64_t>(rank) * H + 8 * v);
+        }
+      }
+      const uint8_t* slot = rs_smem + s * slot_bytes;
+      const uint4* zrow = reinterpret_cast<const uint4*>(slot);
+      const uint4* hrow = reinterpret_cast<const uint4*>(slot + zbytes);
+      const float4 sr = *reinterpret_cast<const float4*>(slot + zbytes + hbytes);
+      const float2 rsu = splat2(sr.y), cu = splat2(-sr.x * sr.y), rsg = splat2(sr.w), cgs = splat2(-sr.z * sr.w);
+      float2 s1u = splat2(0.f), s2u = splat2(0.f), s1g = splat2(0.f), s2g = splat2(0.f);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int v = warp * 32 + lane + 32 * kRsConsumers * j;
+        if (v < nvec) {
+          const uint4 pu = zrow[v], pg = zrow[nvec + v], ph = hrow[v];
+          const uint32_t uw[4] = {pu.x, pu.y, pu.z, pu.w}, gw[4] = {pg.x, pg.y, pg.z, pg.w};
+          const uint32_t hw[4] = {ph.x, ph.y, ph.z, ph.w};
+          const uint32_t wxw[4] = {af[j].wx.x, af[j].wx.y, af[j].wx.z, af[j].wx.w};
+          const uint32_t cxw[4] = {af[j].cx.x, af[j].cx.y, af[j].cx.z, af[j].cx.w};
+          const uint32_t wgw[4] = {af[j].wg.x, af[j].wg.y, af[j].wg.z, af[j].wg.w};
+          const uint32_t cgw[4] = {af[j].cg.x, af[j].cg.y, af[j].cg.z, af[j].cg.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float2 wx = unpack_bf16x2(wxw[e]), wg = unpack_bf16x2(wgw[e]);
+            const GatePair gp = gate_pair(unpack_bf16x2(uw[e]), unpack_bf16x2(gw[e]), rsu, cu, rsg, cgs, wx,
+                                          unpack_bf16x2(cxw[e]), wg, unpack_bf16x2(cgw[e]));
+            const float2 d = unpack_bf16x2(hw[e]);
+            const float2 dxu = mul2(mul2(d, gp.q), wx);
+            const float2 dxg = mul2(mul2(mul2(d, gp.a), gp.dsil), wg);
+            s1u = add2(s1u, dxu);
+            s2u = fma2(dxu, gp.xu, s2u);
+            s1g = add2(s1g, dxg);
+            s2g = fma2(dxg, gp.xg, s2g);
+          }
+        }
+      }
+      float acc[4] = {s1u.x + s1u.y, s2u.x + s2u.y, s1g.x + s1g.y, s2g.x + s2g.y};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) acc[q] += __shfl_xor_sync(0xffffffffu, acc[q], o);
+      }
+      if (lane == 0) {
+        part[s * kRsConsumers + warp] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+        mbar_arrive(&empty[s]);
+      }
+      if (++nt == M) {
+        nt = 0;
+        ++t;
+      }
+    }
+  }
+}
+
 constexpr int kApplyThreads = 128;  // 8 columns per thread
 constexpr int kApplyStages = 6;
 
@@ -799,6 +950,26 @@ cudaError_t launch_ln_gate_bwd_rowsum(const void* Z, const void* stats, const vo
                                       const void* nx_b, const void* ng_w, const void* ng_b, void* rowsum, int T, int M,
                                       int L, int H, const DeviceInfo& dev, cudaStream_t s) {
   const int64_t rows = static_cast<int64_t>(T) * M;
+  if (H <= 8192) {
+    // bulk-copy pipeline: kRsRing row slots of the U|G row, the dHl row and the statistics
+    const int slot_bytes = (6 * H + 16 + 127) / 128 * 128;
+    const int smem = kRsRing * slot_bytes + kRsRing * kRsConsumers * 16 + 2 * kRsRing * 8;
+    cudaError_t e = smem_attr_once(reinterpret_cast<const void*>(ln_gate_bwd_rowsum_bulk_kernel), smem);
+    if (e != cudaSuccess) return e;
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, ln_gate_bwd_rowsum_bulk_kernel, kRsThreads, smem) !=
+            cudaSuccess ||
+        per_sm < 1)
+      per_sm = 1;
+    int64_t blocks = static_cast<int64_t>(per_sm) * dev.num_sms;
+    if (blocks > rows) blocks = rows;
+    return launch_pdl(ln_gate_bwd_rowsum_bulk_kernel, dim3(static_cast<unsigned>(blocks)), dim3(kRsThreads),
+                      static_cast<size_t>(smem), s, static_cast<const __nv_bfloat16*>(Z),
+                      static_cast<const float4*>(stats), static_cast<const __nv_bfloat16*>(dHl),
+                      static_cast<const __nv_bfloat16*>(nx_w), static_cast<const __nv_bfloat16*>(nx_b),
+                      static_cast<const __nv_bfloat16*>(ng_w), static_cast<const __nv_bfloat16*>(ng_b),
+                      static_cast<float4*>(rowsum), rows, M, L, H, slot_bytes, dev.err);
+  }
   int per_sm = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, ln_gate_bwd_rowsum_kernel, kRowsumThreads, 0) !=
           cudaSuccess ||
