@@ -438,16 +438,20 @@ __global__ void __launch_bounds__(kRowsumThreads, 2) ln_gate_bwd_rowsum_kernel(
   }
 }
 
-// Pass 1 for rows of up to 8192 columns, as a bulk-copy pipeline: one
+// Pass 1 for rows of up to 7680 columns, as a bulk-copy pipeline: one
 // producer warp streams whole rows (the U|G row of Z, the dHl row, the row's
-// statistics) into a ring of shared-memory slots with cp.async.bulk; eight
-// consumer warps each take every eighth 8-column vector of the row and
-// publish per-warp partial sums; when the producer recycles a slot it adds the
-// warps' partials in a fixed order and writes the row's four sums.  Each CTA
-// takes a contiguous range of rows (so the rank, and the affines kept in
-// registers, change at most a few times).
+// statistics) into a ring of shared-memory slots with cp.async.bulk; fifteen
+// consumer warps each take every fifteenth 8-column vector of the row (two
+// vectors a thread, their affines held in fp32 registers) and publish per-warp
+// partial sums; when the producer recycles a slot it adds the warps' partials
+// in a fixed order and writes the row's four sums.  Each CTA takes a
+// contiguous range of rows (so the rank, and with it the affines, change at
+// most a few times).
 constexpr int kRsRing = 4;
-constexpr int kRsConsumers = 8;
+// Sixteen warps in all: four per SM sub-partition leave 128 registers a thread.
+constexpr int kRsConsumers = 15;
+constexpr int kRsVec = 2;  // 8-column vectors per consumer thread: 15 * 32 * 2 * 8 = 7680 columns
+constexpr int kRsMaxH = 8 * 32 * kRsConsumers * kRsVec;
 constexpr int kRsThreads = 32 * (kRsConsumers + 1);
 
 __global__ void __launch_bounds__(kRsThreads, 1) ln_gate_bwd_rowsum_bulk_kernel(
@@ -463,7 +467,7 @@ __global__ void __launch_bounds__(kRsThreads, 1) ln_gate_bwd_rowsum_bulk_kernel(
   if (threadIdx.x == 0) {
     for (int s = 0; s < kRsRing; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], kRsConsumers);
+      mbar_init(&empty[s], 4 * kRsConsumers);  // four publishing lanes per consumer warp
     }
     fence_mbar_init();
   }
@@ -526,7 +530,10 @@ __global__ void __launch_bounds__(kRsThreads, 1) ln_gate_bwd_rowsum_bulk_kernel(
     // ---------------------------------------------------------------- consumers
     int t = static_cast<int>(r0 / M), nt = static_cast<int>(r0 - static_cast<int64_t>(t) * M);
     int rank = -1;
-    Affine8 af[4];
+    AffineF af[kRsVec];
+    float* pf = reinterpret_cast<float*>(part);
+    // which of the four sums this lane ends up holding after the reduce-scatter below
+    const bool hi = (lane & 16) != 0, mid = (lane & 8) != 0;
     for (int i = 0; i < n; ++i) {
       const int s = i % kRsRing;
       const bool ok = mbar_wait(&full[s], static_cast<uint32_t>(i / kRsRing) & 1u, err, 0x53u);
@@ -534,9 +541,9 @@ __global__ void __launch_bounds__(kRsThreads, 1) ln_gate_bwd_rowsum_bulk_kernel(
       if (t / L != rank) {
         rank = t / L;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
+        for (int j = 0; j < kRsVec; ++j) {
           const int v = warp * 32 + lane + 32 * kRsConsumers * j;
-          if (v < nvec) af[j] = load_affine8(gx, bx, gg, bg, static_cast<int64_t>(rank) * H + 8 * v);
+          if (v < nvec) af[j] = load_affine_f(gx, bx, gg, bg, static_cast<int64_t>(rank) * H + 8 * v);
         }
       }
       const uint8_t* slot = rs_smem + s * slot_bytes;
@@ -546,21 +553,17 @@ __global__ void __launch_bounds__(kRsThreads, 1) ln_gate_bwd_rowsum_bulk_kernel(
       const float2 rsu = splat2(sr.y), cu = splat2(-sr.x * sr.y), rsg = splat2(sr.w), cgs = splat2(-sr.z * sr.w);
       float2 s1u = splat2(0.f), s2u = splat2(0.f), s1g = splat2(0.f), s2g = splat2(0.f);
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
+      for (int j = 0; j < kRsVec; ++j) {
         const int v = warp * 32 + lane + 32 * kRsConsumers * j;
         if (v < nvec) {
           const uint4 pu = zrow[v], pg = zrow[nvec + v], ph = hrow[v];
           const uint32_t uw[4] = {pu.x, pu.y, pu.z, pu.w}, gw[4] = {pg.x, pg.y, pg.z, pg.w};
           const uint32_t hw[4] = {ph.x, ph.y, ph.z, ph.w};
-          const uint32_t wxw[4] = {af[j].wx.x, af[j].wx.y, af[j].wx.z, af[j].wx.w};
-          const uint32_t cxw[4] = {af[j].cx.x, af[j].cx.y, af[j].cx.z, af[j].cx.w};
-          const uint32_t wgw[4] = {af[j].wg.x, af[j].wg.y, af[j].wg.z, af[j].wg.w};
-          const uint32_t cgw[4] = {af[j].cg.x, af[j].cg.y, af[j].cg.z, af[j].cg.w};
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            const float2 wx = unpack_bf16x2(wxw[e]), wg = unpack_bf16x2(wgw[e]);
+            const float2 wx = af[j].wx[e], wg = af[j].wg[e];
             const GatePair gp = gate_pair(unpack_bf16x2(uw[e]), unpack_bf16x2(gw[e]), rsu, cu, rsg, cgs, wx,
-                                          unpack_bf16x2(cxw[e]), wg, unpack_bf16x2(cgw[e]));
+                                          af[j].cx[e], wg, af[j].cg[e]);
             const float2 d = unpack_bf16x2(hw[e]);
             const float2 dxu = mul2(mul2(d, gp.q), wx);
             const float2 dxg = mul2(mul2(mul2(d, gp.a), gp.dsil), wg);
@@ -571,14 +574,18 @@ __global__ void __launch_bounds__(kRsThreads, 1) ln_gate_bwd_rowsum_bulk_kernel(
           }
         }
       }
-      float acc[4] = {s1u.x + s1u.y, s2u.x + s2u.y, s1g.x + s1g.y, s2g.x + s2g.y};
+      // Reduce-scatter of the four sums over the warp: after the xor-16 step a
+      // lane keeps two of them (0,1 or 2,3), after the xor-8 step one, and the
+      // last three steps complete that one over all 32 lanes.  Lanes 0, 8, 16
+      // and 24 then hold sums 0, 1, 2 and 3.
+      const float a0 = s1u.x + s1u.y, a1 = s2u.x + s2u.y, a2 = s1g.x + s1g.y, a3 = s2g.x + s2g.y;
+      const float k0 = (hi ? a2 : a0) + __shfl_xor_sync(0xffffffffu, hi ? a0 : a2, 16);
+      const float k1 = (hi ? a3 : a1) + __shfl_xor_sync(0xffffffffu, hi ? a1 : a3, 16);
+      float acc = (mid ? k1 : k0) + __shfl_xor_sync(0xffffffffu, mid ? k0 : k1, 8);
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) acc[q] += __shfl_xor_sync(0xffffffffu, acc[q], o);
-      }
-      if (lane == 0) {
-        part[s * kRsConsumers + warp] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+      for (int o = 4; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+      if ((lane & 7) == 0) {
+        pf[(s * kRsConsumers + warp) * 4 + (lane >> 3)] = acc;
         mbar_arrive(&empty[s]);
       }
       if (++nt == M) {
@@ -950,7 +957,7 @@ cudaError_t launch_ln_gate_bwd_rowsum(const void* Z, const void* stats, const vo
                                       const void* nx_b, const void* ng_w, const void* ng_b, void* rowsum, int T, int M,
                                       int L, int H, const DeviceInfo& dev, cudaStream_t s) {
   const int64_t rows = static_cast<int64_t>(T) * M;
-  if (H <= 8192) {
+  if (H <= kRsMaxH) {
     // bulk-copy pipeline: kRsRing row slots of the U|G row, the dHl row and the statistics
     const int slot_bytes = (6 * H + 16 + 127) / 128 * 128;
     const int smem = kRsRing * slot_bytes + kRsRing * kRsConsumers * 16 + 2 * kRsRing * 8;
