@@ -257,7 +257,7 @@ struct BwdLayout {
 BwdLayout bwd_layout(const FfnDims& f) {
   BwdLayout l;
   const size_t rows = static_cast<size_t>(f.T) * f.M;
-  l.nsplit = ffn_bwd_row_splits(static_cast<int>(f.T), static_cast<int>(f.M));
+  l.nsplit = ffn_bwd_row_splits(static_cast<int>(f.T), static_cast<int>(f.M), static_cast<int>(f.H));
   l.dhl = 0;
   l.dz = round_up(rows * f.H * 2, 256);
   l.rowsum = round_up(l.dz + rows * 2 * f.H * 2, 256);

@@ -232,7 +232,7 @@ cudaError_t launch_ln_gate_bwd_apply(const void* Z, const void* stats, const voi
                                      cudaStream_t s);
 
 // Row ranges per token position used by pass 2.
-int ffn_bwd_row_splits(int T, int M);
+int ffn_bwd_row_splits(int T, int M, int H);
 
 // db1 [T, 2H] and d_nx_w, d_nx_b, d_ng_w, d_ng_b [P, H] from the partials, in a fixed order.
 cudaError_t launch_grad_reduce(const float* part, void* d_b1, void* d_nx_w, void* d_nx_b, void* d_ng_w, void* d_ng_b,

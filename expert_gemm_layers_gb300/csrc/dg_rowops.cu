@@ -33,15 +33,6 @@ __device__ __forceinline__ void unpack8(const uint4 v, float (&f)[8]) {
 }
 
 
-__device__ __forceinline__ void store8_stream(__nv_bfloat16* p, const float (&f)[8]) {
-  uint4 v;
-  v.x = pack_bf16x2(f[0], f[1]);
-  v.y = pack_bf16x2(f[2], f[3]);
-  v.z = pack_bf16x2(f[4], f[5]);
-  v.w = pack_bf16x2(f[6], f[7]);
-  __stcs(reinterpret_cast<uint4*>(p), v);
-}
-
 // Warp-uniform read of the error word (these kernels use full-warp barriers
 // and shuffles, so a warp must not split on it).
 __device__ __forceinline__ bool warp_aborted(const uint32_t* err) {
@@ -528,8 +519,10 @@ __global__ void __launch_bounds__(kRsThreads, 1) ln_gate_bwd_rowsum_bulk_kernel(
     }
   } else {
     // ---------------------------------------------------------------- consumers
-    int t = static_cast<int>(r0 / M), nt = static_cast<int>(r0 - static_cast<int64_t>(t) * M);
-    int rank = -1;
+    // position of the current row: rank, token position within the rank, row within the token position
+    const int t0 = static_cast<int>(r0 / M);
+    int nt = static_cast<int>(r0 - static_cast<int64_t>(t0) * M), rank = t0 / L, tl = t0 - rank * L;
+    bool reload = true;
     AffineF af[kRsVec];
     float* pf = reinterpret_cast<float*>(part);
     // which of the four sums this lane ends up holding after the reduce-scatter below
@@ -538,8 +531,8 @@ __global__ void __launch_bounds__(kRsThreads, 1) ln_gate_bwd_rowsum_bulk_kernel(
       const int s = i % kRsRing;
       const bool ok = mbar_wait(&full[s], static_cast<uint32_t>(i / kRsRing) & 1u, err, 0x53u);
       if (!__all_sync(0xffffffffu, ok)) break;
-      if (t / L != rank) {
-        rank = t / L;
+      if (reload) {
+        reload = false;
 #pragma unroll
         for (int j = 0; j < kRsVec; ++j) {
           const int v = warp * 32 + lane + 32 * kRsConsumers * j;
@@ -590,97 +583,153 @@ __global__ void __launch_bounds__(kRsThreads, 1) ln_gate_bwd_rowsum_bulk_kernel(
       }
       if (++nt == M) {
         nt = 0;
-        ++t;
+        if (++tl == L) {
+          tl = 0;
+          ++rank;
+          reload = true;
+        }
       }
     }
   }
 }
 
-constexpr int kApplyThreads = 128;  // 8 columns per thread
-constexpr int kApplyStages = 6;
+// Pass 2 as a bulk-copy pipeline: one producer thread streams, per row, the
+// CTA's column segments of U, G and dHl plus the row's statistics and row
+// sums into a ring of shared-memory stages with cp.async.bulk; three consumer
+// warps (8 columns a thread) hold the fp32 affines and the six column sums in
+// registers, write dZ, and release each stage as soon as they have read it.
+// Four warps a CTA keep the SM's four sub-partitions evenly loaded.
+constexpr int kApConsumers = 3;
+constexpr int kApCols = 8 * 32 * kApConsumers;  // columns of one CTA: 768
+constexpr int kApThreads = 32 * (kApConsumers + 1);
+constexpr int kApRing = 8;
+constexpr int kApSeg = 2 * kApCols;                 // bytes of one bf16 row segment
+constexpr int kApStageBytes = 3 * kApSeg + 32;      // U, G, dHl segments, statistics, row sums
+constexpr int kApSmem = kApRing * kApStageBytes + 2 * kApRing * 8;
 
-// grid: (column blocks of 8*kApplyThreads, T, row splits).
-__global__ void __launch_bounds__(kApplyThreads) ln_gate_bwd_apply_kernel(
+// grid: (column blocks of kApCols, T, row splits).
+__global__ void __launch_bounds__(kApThreads, 4) ln_gate_bwd_apply_kernel(
     const __nv_bfloat16* __restrict__ Z, const float4* __restrict__ stats, const float4* __restrict__ rowsum,
     const __nv_bfloat16* __restrict__ dHl, const __nv_bfloat16* __restrict__ gx, const __nv_bfloat16* __restrict__ bx,
     const __nv_bfloat16* __restrict__ gg, const __nv_bfloat16* __restrict__ bg, __nv_bfloat16* __restrict__ dZ,
-    float* __restrict__ part, int M, int L, int H, const uint32_t* err) {
-  // per stage: u, g, dh of each thread (16 B each), then the row's statistics
-  // and row sums once per warp (copied by lanes 0 and 1)
-  extern __shared__ uint4 ring_raw[];
-  auto ring = reinterpret_cast<uint4(*)[3][kApplyThreads]>(ring_raw);
-  auto slot = reinterpret_cast<uint4(*)[kApplyThreads / 32][2]>(ring_raw + kApplyStages * 3 * kApplyThreads);
+    float* __restrict__ part, int M, int L, int H, uint32_t* err) {
+  extern __shared__ __align__(128) uint8_t ap_smem[];
+  uint64_t* full = reinterpret_cast<uint64_t*>(ap_smem + kApRing * kApStageBytes);
+  uint64_t* empty = full + kApRing;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kApRing; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 32 * kApConsumers);
+    }
+    fence_mbar_init();
+  }
   griddep_wait();
-  if (warp_aborted(err)) return;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (block_aborted(err)) return;  // (its barrier also publishes the barrier initialisation)
   const int t = blockIdx.y, rsp = blockIdx.z, nsplit = gridDim.z;
-  const int r = t / L;
-  const int c0 = blockIdx.x * (8 * kApplyThreads) + 8 * threadIdx.x;
-  const bool active = c0 < H;
-  const int cc = active ? c0 : 0;
-  const float inv_h = 1.0f / static_cast<float>(H);
-  const AffineF aff = load_affine_f(gx, bx, gg, bg, static_cast<int64_t>(r) * H + cc);
-  float2 s_du[4], s_dg[4], s_gx[4], s_bx[4], s_gg[4], s_bg[4];
-#pragma unroll
-  for (int e = 0; e < 4; ++e) s_du[e] = s_dg[e] = s_gx[e] = s_bx[e] = s_gg[e] = s_bg[e] = splat2(0.0f);
+  const int col0 = blockIdx.x * kApCols;
+  const int wc = min(kApCols, H - col0);  // columns of this block, a multiple of 8
   const int rows_per = (M + nsplit - 1) / nsplit;
   const int n_begin = min(M, rsp * rows_per), n_end = min(M, n_begin + rows_per);
   const int n_rows = n_end - n_begin;
   const int64_t rowbase = static_cast<int64_t>(t) * M + n_begin;
   const int64_t zstride = 2 * static_cast<int64_t>(H);
-  auto issue = [&](int i) {
-    if (i < n_rows) {
-      const int64_t row = rowbase + i;
-      const int s = i % kApplyStages;
-      cp_async16(&ring[s][0][threadIdx.x], Z + row * zstride + cc, active);
-      cp_async16(&ring[s][1][threadIdx.x], Z + row * zstride + H + cc, active);
-      cp_async16(&ring[s][2][threadIdx.x], dHl + row * H + cc, active);
-      if (lane == 0) cp_async16(&slot[s][warp][0], stats + row, true);
-      if (lane == 1) cp_async16(&slot[s][warp][1], rowsum + row, true);
+
+  if (warp == kApConsumers) {
+    // ---------------------------------------------------------------- producer
+    if (lane == 0) {
+      const uint32_t seg = 2u * static_cast<uint32_t>(wc);
+      const __nv_bfloat16* zp = Z + rowbase * zstride + col0;
+      const __nv_bfloat16* hp = dHl + rowbase * H + col0;
+      int stage = 0, issued = 0;
+      uint32_t phase = 0;
+      for (int i = 0; i < n_rows; ++i) {
+        // stage reuse waits for the consumers' release of row i - kApRing
+        if (i >= kApRing && !mbar_wait(&empty[stage], phase ^ 1u, err, 0x54u)) break;
+        uint8_t* slot = ap_smem + stage * kApStageBytes;
+        mbar_arrive_expect_tx(&full[stage], 3u * seg + 32u);
+        bulk_load(slot, zp, seg, &full[stage]);
+        bulk_load(slot + kApSeg, zp + H, seg, &full[stage]);
+        bulk_load(slot + 2 * kApSeg, hp, seg, &full[stage]);
+        bulk_load(slot + 3 * kApSeg, stats + rowbase + i, 16u, &full[stage]);
+        bulk_load(slot + 3 * kApSeg + 16, rowsum + rowbase + i, 16u, &full[stage]);
+        zp += zstride;
+        hp += H;
+        issued = i + 1;
+        if (++stage == kApRing) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      // every copy issued has landed before the CTA may exit
+      for (int i = max(0, issued - kApRing); i < issued; ++i) {
+        uint32_t dummy = 0;
+        if (!mbar_try_wait(&full[i % kApRing], static_cast<uint32_t>(i / kApRing) & 1u))
+          mbar_wait_slow(&full[i % kApRing], static_cast<uint32_t>(i / kApRing) & 1u, &dummy, 0x55u, kWaitLimitNs);
+      }
     }
-    cp_async_commit();
-  };
-#pragma unroll
-  for (int i = 0; i < kApplyStages - 1; ++i) issue(i);
-  for (int i = 0; i < n_rows; ++i) {
-    issue(i + kApplyStages - 1);
-    cp_async_wait<kApplyStages - 1>();
-    __syncwarp();  // lanes 0 and 1 copied this row's scalars for the whole warp
-    const int s = i % kApplyStages;
-    if (!active) continue;
-    const int64_t row = rowbase + i;
-    const uint4 pu = ring[s][0][threadIdx.x], pg = ring[s][1][threadIdx.x], ph = ring[s][2][threadIdx.x];
-    const uint4 stv = slot[s][warp][0], rsv = slot[s][warp][1];
-    const float mu_u = __uint_as_float(stv.x), rs_u = __uint_as_float(stv.y);
-    const float mu_g = __uint_as_float(stv.z), rs_g = __uint_as_float(stv.w);
-    const float2 rsu = splat2(rs_u), cu = splat2(-mu_u * rs_u), rsg = splat2(rs_g), cgs = splat2(-mu_g * rs_g);
-    const float2 m1u = splat2(-__uint_as_float(rsv.x) * inv_h), m2u = splat2(-__uint_as_float(rsv.y) * inv_h);
-    const float2 m1g = splat2(-__uint_as_float(rsv.z) * inv_h), m2g = splat2(-__uint_as_float(rsv.w) * inv_h);
-    const uint32_t uw[4] = {pu.x, pu.y, pu.z, pu.w}, gw[4] = {pg.x, pg.y, pg.z, pg.w}, hw[4] = {ph.x, ph.y, ph.z, ph.w};
-    uint32_t ou[4], og[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const GatePair gp = gate_pair(unpack_bf16x2(uw[e]), unpack_bf16x2(gw[e]), rsu, cu, rsg, cgs, aff.wx[e], aff.cx[e],
-                                    aff.wg[e], aff.cg[e]);
-      const float2 dh = unpack_bf16x2(hw[e]);
-      const float2 da = mul2(dh, gp.q);
-      const float2 ds = mul2(mul2(dh, gp.a), gp.dsil);
-      // dU = rstd_u * (da*gx - mean(dx_u) - x_u*mean(dx_u*x_u)); same for dG
-      const float2 du = mul2(rsu, fma2(gp.xu, m2u, fma2(da, aff.wx[e], m1u)));
-      const float2 dg = mul2(rsg, fma2(gp.xg, m2g, fma2(ds, aff.wg[e], m1g)));
-      s_du[e] = add2(s_du[e], du);
-      s_dg[e] = add2(s_dg[e], dg);
-      s_gx[e] = fma2(da, gp.xu, s_gx[e]);
-      s_bx[e] = add2(s_bx[e], da);
-      s_gg[e] = fma2(ds, gp.xg, s_gg[e]);
-      s_bg[e] = add2(s_bg[e], ds);
-      ou[e] = pack_bf16x2(du.x, du.y);
-      og[e] = pack_bf16x2(dg.x, dg.y);
-    }
-    __stcs(reinterpret_cast<uint4*>(dZ + row * zstride + c0), make_uint4(ou[0], ou[1], ou[2], ou[3]));
-    __stcs(reinterpret_cast<uint4*>(dZ + row * zstride + H + c0), make_uint4(og[0], og[1], og[2], og[3]));
+    return;
   }
-  cp_async_wait<0>();
+
+  // ---------------------------------------------------------------- consumers
+  const int v = warp * 32 + lane;
+  const bool active = 8 * v < wc;
+  const int c0 = col0 + (active ? 8 * v : 0);
+  const float inv_h = 1.0f / static_cast<float>(H);
+  const AffineF aff = load_affine_f(gx, bx, gg, bg, static_cast<int64_t>(t / L) * H + c0);
+  float2 s_du[4], s_dg[4], s_gx[4], s_bx[4], s_gg[4], s_bg[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) s_du[e] = s_dg[e] = s_gx[e] = s_bx[e] = s_gg[e] = s_bg[e] = splat2(0.0f);
+  __nv_bfloat16* dzp = dZ + rowbase * zstride + c0;
+  int stage = 0;
+  uint32_t phase = 0;
+  for (int i = 0; i < n_rows; ++i) {
+    const bool ok = mbar_wait(&full[stage], phase, err, 0x56u);
+    if (!__all_sync(0xffffffffu, ok)) break;
+    const uint8_t* slot = ap_smem + stage * kApStageBytes;
+    uint4 pu = make_uint4(0u, 0u, 0u, 0u), pg = pu, ph = pu;
+    if (active) {
+      pu = reinterpret_cast<const uint4*>(slot)[v];
+      pg = reinterpret_cast<const uint4*>(slot + kApSeg)[v];
+      ph = reinterpret_cast<const uint4*>(slot + 2 * kApSeg)[v];
+    }
+    const float4 stv = *reinterpret_cast<const float4*>(slot + 3 * kApSeg);
+    const float4 rsv = *reinterpret_cast<const float4*>(slot + 3 * kApSeg + 16);
+    mbar_arrive(&empty[stage]);
+    if (++stage == kApRing) {
+      stage = 0;
+      phase ^= 1u;
+    }
+    if (active) {
+      const float2 rsu = splat2(stv.y), cu = splat2(-stv.x * stv.y), rsg = splat2(stv.w), cgs = splat2(-stv.z * stv.w);
+      const float2 m1u = splat2(-rsv.x * inv_h), m2u = splat2(-rsv.y * inv_h);
+      const float2 m1g = splat2(-rsv.z * inv_h), m2g = splat2(-rsv.w * inv_h);
+      const uint32_t uw[4] = {pu.x, pu.y, pu.z, pu.w}, gw[4] = {pg.x, pg.y, pg.z, pg.w}, hw[4] = {ph.x, ph.y, ph.z, ph.w};
+      uint32_t ou[4], og[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const GatePair gp = gate_pair(unpack_bf16x2(uw[e]), unpack_bf16x2(gw[e]), rsu, cu, rsg, cgs, aff.wx[e],
+                                      aff.cx[e], aff.wg[e], aff.cg[e]);
+        const float2 dh = unpack_bf16x2(hw[e]);
+        const float2 da = mul2(dh, gp.q);
+        const float2 ds = mul2(mul2(dh, gp.a), gp.dsil);
+        // dU = rstd_u * (da*gx - mean(dx_u) - x_u*mean(dx_u*x_u)); same for dG
+        const float2 du = mul2(rsu, fma2(gp.xu, m2u, fma2(da, aff.wx[e], m1u)));
+        const float2 dg = mul2(rsg, fma2(gp.xg, m2g, fma2(ds, aff.wg[e], m1g)));
+        s_du[e] = add2(s_du[e], du);
+        s_dg[e] = add2(s_dg[e], dg);
+        s_gx[e] = fma2(da, gp.xu, s_gx[e]);
+        s_bx[e] = add2(s_bx[e], da);
+        s_gg[e] = fma2(ds, gp.xg, s_gg[e]);
+        s_bg[e] = add2(s_bg[e], ds);
+        ou[e] = pack_bf16x2(du.x, du.y);
+        og[e] = pack_bf16x2(dg.x, dg.y);
+      }
+      __stcs(reinterpret_cast<uint4*>(dzp), make_uint4(ou[0], ou[1], ou[2], ou[3]));
+      __stcs(reinterpret_cast<uint4*>(dzp + H), make_uint4(og[0], og[1], og[2], og[3]));
+    }
+    dzp += zstride;
+  }
   if (!active) return;
   // part[t][split][q][c], q: dU, dG, da*x_u, da, ds*x_g, ds
   float* pp = part + (static_cast<int64_t>(t) * nsplit + rsp) * 6 * H + c0;
@@ -992,10 +1041,12 @@ cudaError_t launch_ln_gate_bwd_rowsum(const void* Z, const void* stats, const vo
       rows, M, L, H, dev.err);
 }
 
-int ffn_bwd_row_splits(int T, int M) {
-  // enough (t, column block, row range) items to fill the GPU several times over
-  int splits = (4096 + T - 1) / T;
-  const int cap = (M + 63) / 64;
+int ffn_bwd_row_splits(int T, int M, int H) {
+  // about sixteen waves of (t, column block, row range) items at four CTAs per
+  // SM, and no fewer than 128 rows an item where M allows
+  const int blocks = (H + kApCols - 1) / kApCols;
+  int splits = (10240 + T * blocks - 1) / (T * blocks);
+  const int cap = (M + 127) / 128;
   if (splits > cap) splits = cap;
   return splits < 1 ? 1 : splits;
 }
@@ -1004,11 +1055,10 @@ cudaError_t launch_ln_gate_bwd_apply(const void* Z, const void* stats, const voi
                                      const void* nx_w, const void* nx_b, const void* ng_w, const void* ng_b, void* dZ,
                                      float* part, int T, int M, int L, int H, int nsplit, const DeviceInfo& dev,
                                      cudaStream_t s) {
-  dim3 grid((H + 8 * kApplyThreads - 1) / (8 * kApplyThreads), T, nsplit);
-  const int smem = kApplyStages * (3 * kApplyThreads + 2 * (kApplyThreads / 32)) * 16;
-  cudaError_t e = smem_attr_once(reinterpret_cast<const void*>(ln_gate_bwd_apply_kernel), smem);
+  dim3 grid((H + kApCols - 1) / kApCols, T, nsplit);
+  cudaError_t e = smem_attr_once(reinterpret_cast<const void*>(ln_gate_bwd_apply_kernel), kApSmem);
   if (e != cudaSuccess) return e;
-  return launch_pdl(ln_gate_bwd_apply_kernel, grid, dim3(kApplyThreads), smem, s,
+  return launch_pdl(ln_gate_bwd_apply_kernel, grid, dim3(kApThreads), kApSmem, s,
       static_cast<const __nv_bfloat16*>(Z), static_cast<const float4*>(stats), static_cast<const float4*>(rowsum),
       static_cast<const __nv_bfloat16*>(dHl), static_cast<const __nv_bfloat16*>(nx_w),
       static_cast<const __nv_bfloat16*>(nx_b), static_cast<const __nv_bfloat16*>(ng_w),
