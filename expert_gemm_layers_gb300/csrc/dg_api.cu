@@ -167,6 +167,29 @@ dg_status make_map_3d(CUtensorMap* map, bool is_bf16, const void* base, uint64_t
   return DG_OK;
 }
 
+dg_status make_map_mn(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
+                      uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t b1, uint32_t b2, uint32_t blocks,
+                      int32_t* mn4, const char* what) {
+  *mn4 = 0;
+  if (d0 % 64 == 0 && d1 > 0 && d2 > 0 && aligned16(base) && !(stride1_bytes & 15u) && !(stride2_bytes & 15u)) {
+    EncodeTiledFn enc = encode_fn();
+    if (enc) {
+      const cuuint64_t dims[4] = {64, d1, d2, d0 / 64};
+      const cuuint64_t strides[3] = {stride1_bytes, stride2_bytes, 128};
+      const cuuint32_t box[4] = {64, b1, b2, blocks};
+      const cuuint32_t estr[4] = {1, 1, 1, 1};
+      CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
+                       CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+      if (r == CUDA_SUCCESS) {
+        *mn4 = 1;
+        return DG_OK;
+      }
+    }
+  }
+  return make_map_3d(map, true, base, d0, d1, d2, stride1_bytes, stride2_bytes, 64, b1, b2, what);
+}
+
 int gemm_tile_m() { return kUsePairs ? 256 : 128; }
 
 int gemm_tile_n(GemmVariant v) { return v == GV_BF16_KK_SWIGLU ? 128 : v == GV_FP8_KK_N224 ? 224 : 256; }
@@ -429,7 +452,9 @@ dg_status dg_a2a_ffn_fwd(const dg_ffn_shape* shape, const void* inputs, const vo
   // The epilogue also writes each row's per-tile mean and M2 of its U and G columns.
   CUtensorMap mx, mw1, mz;
   if ((st = make_map_3d(&mx, true, inputs, D, T, M, D * 2, T * D * 2, 64, 1, 128, "inputs")) != DG_OK) return st;
-  if ((st = make_map_3d(&mw1, true, w1, 2 * H, D, T, 2 * H * 2, D * 2 * H * 2, 64, 64, 1, "w1")) != DG_OK) return st;
+  int32_t w1_mn4 = 0;
+  if ((st = make_map_mn(&mw1, w1, 2 * H, D, T, 2 * H * 2, D * 2 * H * 2, 64, 1, kMnBlocksB, &w1_mn4, "w1")) != DG_OK)
+    return st;
   if ((st = make_map_3d(&mz, true, Z, 2 * H, M, T, 2 * H * 2, M * 2 * H * 2, 64, 32, 1, "Z")) != DG_OK) return st;
   GemmParams p1{};
   p1.G = static_cast<int32_t>(T);
@@ -443,6 +468,7 @@ dg_status dg_a2a_ffn_fwd(const dg_ffn_shape* shape, const void* inputs, const vo
   p1.bias_g_stride = static_cast<int64_t>(2 * H);
   p1.ln_part = static_cast<float4*>(part);
   p1.ln_H = static_cast<int32_t>(H);
+  p1.b_mn4 = w1_mn4;
   const double rows = static_cast<double>(T) * M;
   if ((st = run_gemm(GV_BF16_KM_LNSTATS, mx, mw1, mz, mz, p1, dev, s, "ffn_gemm1",
                      2.0 * (rows * D + static_cast<double>(T) * D * 2 * H + rows * 2 * H) +
@@ -467,9 +493,12 @@ dg_status dg_a2a_ffn_fwd(const dg_ffn_shape* shape, const void* inputs, const vo
   // GEMM2: output rows (s, b, t) = Hl_t @ wout_t + bout_t at the combine offsets.
   CUtensorMap mh, mwo, mo;
   if ((st = make_map_3d(&mh, true, Hl, H, M, T, H * 2, M * H * 2, 64, 128, 1, "Hl")) != DG_OK) return st;
-  if ((st = make_map_3d(&mwo, true, wout, D, H, T, D * 2, H * D * 2, 64, 64, 1, "wout")) != DG_OK) return st;
+  int32_t wo_mn4 = 0;
+  if ((st = make_map_mn(&mwo, wout, D, H, T, D * 2, H * D * 2, 64, 1, kMnBlocksB, &wo_mn4, "wout")) != DG_OK)
+    return st;
   if ((st = make_map_3d(&mo, true, output, D, T, M, D * 2, T * D * 2, 64, 1, 32, "output")) != DG_OK) return st;
   GemmParams p2{};
+  p2.b_mn4 = wo_mn4;
   p2.G = static_cast<int32_t>(T);
   p2.M = static_cast<int32_t>(M);
   p2.N = static_cast<int32_t>(D);
@@ -545,8 +574,11 @@ dg_status dg_a2a_ffn_bwd(const dg_ffn_shape* shape, const void* inputs, const vo
 
   // (2) dwout_t = Hl_t^T @ dY_t     [H, D], contraction over the M rows
   CUtensorMap mhl_t, mdy_n, mdwo;
-  if ((st = make_map_3d(&mhl_t, true, Hl, H, M, T, H * 2, M * H * 2, 64, 64, 1, "Hl^T")) != DG_OK) return st;
-  if ((st = make_map_3d(&mdy_n, true, dY, D, T, M, D * 2, T * D * 2, 64, 1, 64, "dY (N-major)")) != DG_OK) return st;
+  int32_t hl_mn4 = 0, dyn_mn4 = 0;
+  if ((st = make_map_mn(&mhl_t, Hl, H, M, T, H * 2, M * H * 2, 64, 1, kMnBlocksA, &hl_mn4, "Hl^T")) != DG_OK)
+    return st;
+  if ((st = make_map_mn(&mdy_n, dY, D, T, M, D * 2, T * D * 2, 1, 64, kMnBlocksB, &dyn_mn4, "dY (N-major)")) != DG_OK)
+    return st;
   if ((st = make_map_3d(&mdwo, true, d_wout, D, H, T, D * 2, H * D * 2, 64, 32, 1, "d_wout")) != DG_OK) return st;
   p = GemmParams{};
   p.G = static_cast<int32_t>(T);
@@ -556,6 +588,8 @@ dg_status dg_a2a_ffn_bwd(const dg_ffn_shape* shape, const void* inputs, const vo
   p.a_g = G_OUTER;
   p.b_g = G_MID;
   p.d_g = G_OUTER;
+  p.a_mn4 = hl_mn4;
+  p.b_mn4 = dyn_mn4;
   if ((st = run_gemm(GV_BF16_MM_STORE, mhl_t, mdy_n, mdwo, mdwo, p, dev, s, "ffn_bwd_dwout",
                      2.0 * (rows * H + rows * D + static_cast<double>(T) * H * D))) != DG_OK)
     return st;
@@ -615,8 +649,11 @@ dg_status dg_a2a_ffn_bwd(const dg_ffn_shape* shape, const void* inputs, const vo
 
   // (7) dw1_t = Xlocal_t^T @ dZ_t   [D, 2H], contraction over the M rows
   CUtensorMap mx_t, mdz_n, mdw1;
-  if ((st = make_map_3d(&mx_t, true, inputs, D, T, M, D * 2, T * D * 2, 64, 1, 64, "inputs^T")) != DG_OK) return st;
-  if ((st = make_map_3d(&mdz_n, true, dZ, 2 * H, M, T, 2 * H * 2, M * 2 * H * 2, 64, 64, 1, "dZ (N-major)")) != DG_OK)
+  int32_t xt_mn4 = 0, dzn_mn4 = 0;
+  if ((st = make_map_mn(&mx_t, inputs, D, T, M, D * 2, T * D * 2, 1, 64, kMnBlocksA, &xt_mn4, "inputs^T")) != DG_OK)
+    return st;
+  if ((st = make_map_mn(&mdz_n, dZ, 2 * H, M, T, 2 * H * 2, M * 2 * H * 2, 64, 1, kMnBlocksB, &dzn_mn4,
+                        "dZ (N-major)")) != DG_OK)
     return st;
   if ((st = make_map_3d(&mdw1, true, d_w1, 2 * H, D, T, 2 * H * 2, D * 2 * H * 2, 64, 32, 1, "d_w1")) != DG_OK)
     return st;
@@ -628,6 +665,8 @@ dg_status dg_a2a_ffn_bwd(const dg_ffn_shape* shape, const void* inputs, const vo
   p.a_g = G_MID;
   p.b_g = G_OUTER;
   p.d_g = G_OUTER;
+  p.a_mn4 = xt_mn4;
+  p.b_mn4 = dzn_mn4;
   return run_gemm(GV_BF16_MM_STORE, mx_t, mdz_n, mdw1, mdw1, p, dev, s, "ffn_bwd_dw1",
                   2.0 * (rows * D + rows * 2 * H + static_cast<double>(T) * D * 2 * H));
 }
@@ -1012,7 +1051,9 @@ dg_status dg_tp_swiglu_bwd(int64_t S, int64_t d, int64_t ffn, int32_t W, int32_t
   CUtensorMap mdy_k, mw2_n, mdh;
   if ((st = make_map_3d(&mdy_k, true, dy_shards, Dm, R, 1, Dm * 2, R * Dm * 2, 64, 128, 1, "dy_shards")) != DG_OK)
     return st;
-  if ((st = make_map_3d(&mw2_n, true, w2, FF, Dm, 1, FF * 2, Dm * FF * 2, 64, 64, 1, "w2 (N-major)")) != DG_OK) return st;
+  int32_t w2n_mn4 = 0;
+  if ((st = make_map_mn(&mw2_n, w2, FF, Dm, 1, FF * 2, Dm * FF * 2, 64, 1, kMnBlocksB, &w2n_mn4, "w2 (N-major)")) != DG_OK)
+    return st;
   if ((st = make_map_3d(&mdh, true, dh, FF, R, 1, FF * 2, R * FF * 2, 64, 32, 1, "dh")) != DG_OK) return st;
   p = GemmParams{};
   p.G = 1;
@@ -1020,6 +1061,7 @@ dg_status dg_tp_swiglu_bwd(int64_t S, int64_t d, int64_t ffn, int32_t W, int32_t
   p.N = static_cast<int32_t>(ffn);
   p.K = static_cast<int32_t>(d);
   p.a_g = p.b_g = p.d_g = G_OUTER;
+  p.b_mn4 = w2n_mn4;
   if ((st = run_gemm(GV_BF16_KM_STORE, mdy_k, mw2_n, mdh, mdh, p, dev, s, "tp_bwd_dh",
                      2.0 * (r * dd + ff * dd + r * ff))) != DG_OK)
     return st;
@@ -1033,8 +1075,11 @@ dg_status dg_tp_swiglu_bwd(int64_t S, int64_t d, int64_t ffn, int32_t W, int32_t
 
   // 4. d_w2 = dY^T h: [d, ffn], contraction over the gathered rows.
   CUtensorMap mdy_t, mh_n, mdw2;
-  if ((st = make_map_3d(&mdy_t, true, dy_shards, Dm, R, 1, Dm * 2, R * Dm * 2, 64, 64, 1, "dy^T")) != DG_OK) return st;
-  if ((st = make_map_3d(&mh_n, true, dh, FF, R, 1, FF * 2, R * FF * 2, 64, 64, 1, "h (N-major)")) != DG_OK) return st;
+  int32_t dyt_mn4 = 0, hn_mn4 = 0;
+  if ((st = make_map_mn(&mdy_t, dy_shards, Dm, R, 1, Dm * 2, R * Dm * 2, 64, 1, kMnBlocksA, &dyt_mn4, "dy^T")) != DG_OK)
+    return st;
+  if ((st = make_map_mn(&mh_n, dh, FF, R, 1, FF * 2, R * FF * 2, 64, 1, kMnBlocksB, &hn_mn4, "h (N-major)")) != DG_OK)
+    return st;
   if ((st = make_map_3d(&mdw2, true, d_w2, FF, Dm, 1, FF * 2, Dm * FF * 2, 64, 32, 1, "d_w2")) != DG_OK) return st;
   p = GemmParams{};
   p.G = 1;
@@ -1042,6 +1087,8 @@ dg_status dg_tp_swiglu_bwd(int64_t S, int64_t d, int64_t ffn, int32_t W, int32_t
   p.N = static_cast<int32_t>(ffn);
   p.K = static_cast<int32_t>(R);
   p.a_g = p.b_g = p.d_g = G_OUTER;
+  p.a_mn4 = dyt_mn4;
+  p.b_mn4 = hn_mn4;
   if ((st = run_gemm(GV_BF16_MM_STORE, mdy_t, mh_n, mdw2, mdw2, p, dev, s, "tp_bwd_dw2",
                      2.0 * (r * dd + r * ff + dd * ff))) != DG_OK)
     return st;
@@ -1050,7 +1097,9 @@ dg_status dg_tp_swiglu_bwd(int64_t S, int64_t d, int64_t ffn, int32_t W, int32_t
   //    K = 2*ffn, so the shard sum (the row-parallel reduction) is the K loop.
   CUtensorMap mdab_k, mw13_n, mdx;
   if ((st = make_map_3d(&mdab_k, true, ab, F2, R, 1, F2 * 2, R * F2 * 2, 64, 128, 1, "[da|db]")) != DG_OK) return st;
-  if ((st = make_map_3d(&mw13_n, true, w13, Dm, F2, 1, Dm * 2, F2 * Dm * 2, 64, 64, 1, "w13 (N-major)")) != DG_OK)
+  int32_t w13n_mn4 = 0;
+  if ((st = make_map_mn(&mw13_n, w13, Dm, F2, 1, Dm * 2, F2 * Dm * 2, 64, 1, kMnBlocksB, &w13n_mn4, "w13 (N-major)")) !=
+      DG_OK)
     return st;
   if ((st = make_map_3d(&mdx, true, dx_shards, Dm, R, 1, Dm * 2, R * Dm * 2, 64, 32, 1, "dx_shards")) != DG_OK) return st;
   p = GemmParams{};
@@ -1059,14 +1108,18 @@ dg_status dg_tp_swiglu_bwd(int64_t S, int64_t d, int64_t ffn, int32_t W, int32_t
   p.N = static_cast<int32_t>(d);
   p.K = static_cast<int32_t>(F2);
   p.a_g = p.b_g = p.d_g = G_OUTER;
+  p.b_mn4 = w13n_mn4;
   if ((st = run_gemm(GV_BF16_KM_STORE, mdab_k, mw13_n, mdx, mdx, p, dev, s, "tp_bwd_dx",
                      2.0 * (2.0 * r * ff + 2.0 * ff * dd + r * dd))) != DG_OK)
     return st;
 
   // 6. d_w13 = [da|db]^T X: [2*ffn, d] in w13's own row order.
   CUtensorMap mdab_t, mx_n, mdw13;
-  if ((st = make_map_3d(&mdab_t, true, ab, F2, R, 1, F2 * 2, R * F2 * 2, 64, 64, 1, "[da|db]^T")) != DG_OK) return st;
-  if ((st = make_map_3d(&mx_n, true, x_shards, Dm, R, 1, Dm * 2, R * Dm * 2, 64, 64, 1, "x (N-major)")) != DG_OK) return st;
+  int32_t dabt_mn4 = 0, xn_mn4 = 0;
+  if ((st = make_map_mn(&mdab_t, ab, F2, R, 1, F2 * 2, R * F2 * 2, 64, 1, kMnBlocksA, &dabt_mn4, "[da|db]^T")) != DG_OK)
+    return st;
+  if ((st = make_map_mn(&mx_n, x_shards, Dm, R, 1, Dm * 2, R * Dm * 2, 64, 1, kMnBlocksB, &xn_mn4, "x (N-major)")) != DG_OK)
+    return st;
   if ((st = make_map_3d(&mdw13, true, d_w13, Dm, F2, 1, Dm * 2, F2 * Dm * 2, 64, 32, 1, "d_w13")) != DG_OK) return st;
   p = GemmParams{};
   p.G = 1;
@@ -1074,6 +1127,8 @@ dg_status dg_tp_swiglu_bwd(int64_t S, int64_t d, int64_t ffn, int32_t W, int32_t
   p.N = static_cast<int32_t>(d);
   p.K = static_cast<int32_t>(R);
   p.a_g = p.b_g = p.d_g = G_OUTER;
+  p.a_mn4 = dabt_mn4;
+  p.b_mn4 = xn_mn4;
   return run_gemm(GV_BF16_MM_STORE, mdab_t, mx_n, mdw13, mdw13, p, dev, s, "tp_bwd_dw13",
                   2.0 * (2.0 * r * ff + r * dd + 2.0 * ff * dd));
 }
@@ -1162,7 +1217,9 @@ dg_status dg_tp_linear_bwd(int64_t rows, int64_t in_f, int64_t out_f, const void
     // dx = dy weight: B = weight read N-major ([out, in], in contiguous)
     CUtensorMap mdy, mw, mdx;
     if ((st = make_map_3d(&mdy, true, dy, O, R, 1, O * 2, R * O * 2, 64, 128, 1, "dy")) != DG_OK) return st;
-    if ((st = make_map_3d(&mw, true, weight, I, O, 1, I * 2, O * I * 2, 64, 64, 1, "weight (N-major)")) != DG_OK)
+    int32_t w_mn4 = 0;
+    if ((st = make_map_mn(&mw, weight, I, O, 1, I * 2, O * I * 2, 64, 1, kMnBlocksB, &w_mn4, "weight (N-major)")) !=
+        DG_OK)
       return st;
     if ((st = make_map_3d(&mdx, true, dx, I, R, 1, I * 2, R * I * 2, 64, 32, 1, "dx")) != DG_OK) return st;
     GemmParams p{};
@@ -1171,6 +1228,7 @@ dg_status dg_tp_linear_bwd(int64_t rows, int64_t in_f, int64_t out_f, const void
     p.N = static_cast<int32_t>(in_f);
     p.K = static_cast<int32_t>(out_f);
     p.a_g = p.b_g = p.d_g = G_OUTER;
+    p.b_mn4 = w_mn4;
     if ((st = run_gemm(GV_BF16_KM_STORE, mdy, mw, mdx, mdx, p, dev, s, "tp_linear_bwd_dx",
                        2.0 * (r * fo + fo * fi + r * fi))) != DG_OK)
       return st;
@@ -1178,8 +1236,11 @@ dg_status dg_tp_linear_bwd(int64_t rows, int64_t in_f, int64_t out_f, const void
   if (d_weight) {
     // d_weight = dy^T x: both operands MN-major, the contraction over rows
     CUtensorMap mdy_t, mx_n, mdw;
-    if ((st = make_map_3d(&mdy_t, true, dy, O, R, 1, O * 2, R * O * 2, 64, 64, 1, "dy^T")) != DG_OK) return st;
-    if ((st = make_map_3d(&mx_n, true, x, I, R, 1, I * 2, R * I * 2, 64, 64, 1, "x (N-major)")) != DG_OK) return st;
+    int32_t dyt_mn4 = 0, xn_mn4 = 0;
+    if ((st = make_map_mn(&mdy_t, dy, O, R, 1, O * 2, R * O * 2, 64, 1, kMnBlocksA, &dyt_mn4, "dy^T")) != DG_OK)
+      return st;
+    if ((st = make_map_mn(&mx_n, x, I, R, 1, I * 2, R * I * 2, 64, 1, kMnBlocksB, &xn_mn4, "x (N-major)")) != DG_OK)
+      return st;
     if ((st = make_map_3d(&mdw, true, d_weight, I, O, 1, I * 2, O * I * 2, 64, 32, 1, "d_weight")) != DG_OK)
       return st;
     GemmParams p{};
@@ -1188,6 +1249,8 @@ dg_status dg_tp_linear_bwd(int64_t rows, int64_t in_f, int64_t out_f, const void
     p.N = static_cast<int32_t>(in_f);
     p.K = static_cast<int32_t>(rows);
     p.a_g = p.b_g = p.d_g = G_OUTER;
+    p.a_mn4 = dyt_mn4;
+    p.b_mn4 = xn_mn4;
     if ((st = run_gemm(GV_BF16_MM_STORE, mdy_t, mx_n, mdw, mdw, p, dev, s, "tp_linear_bwd_dw",
                        2.0 * (r * fo + r * fi + fo * fi))) != DG_OK)
       return st;

@@ -63,6 +63,10 @@ struct GemmParams {
   const float* row_scale;
   const float* col_scale;
   int64_t row_scale_g, col_scale_g;
+  // MN-major A / B described by a 4-D map (mn mod 64, the two other
+  // coordinates, mn / 64): one copy fetches all 64-wide MN blocks of a stage.
+  // Set only when the operand's MN extent is a multiple of 64.
+  int32_t a_mn4, b_mn4;
 };
 
 // Running (count, mean, M2) of a set of values; merge() is the pairwise
@@ -307,8 +311,25 @@ __global__ void __launch_bounds__(GemmCfg<kFp8, kAMN, kBMN, kEpi, kPair, kBN>::N
             else
               tma_load_3d(dst, map, &full[stage], x, c1, c2);
           };
+          // MN-major, one copy: coordinates (0, k, g, mn/64) in the map's order
+          auto load_mn4 = [&](void* dst, const CUtensorMap* map, int32_t k, int32_t mn_blk, int32_t g3,
+                              int32_t mode) {
+            int32_t c1 = k, c2 = g3;
+            if (mode == G_MID) {
+              c1 = g3;
+              c2 = k;
+            } else if (mode == G_NONE) {
+              c2 = 0;
+            }
+            if (kPair)
+              tma_load_4d_pair(dst, map, bar_c, 0, c1, c2, mn_blk);
+            else
+              tma_load_4d(dst, map, &full[stage], 0, c1, c2, mn_blk);
+          };
           if (!kAMN) {
             load(sa, &tmA, k0, m0, g, p.a_g);
+          } else if (p.a_mn4) {
+            load_mn4(sa, &tmA, k0, m0 / 64, g, p.a_g);
           } else {
 #pragma unroll
             for (int i = 0; i < Cfg::BM / 64; ++i) load(sa + i * Cfg::MN_BOX_BYTES, &tmA, m0 + 64 * i, k0, g, p.a_g);
@@ -323,6 +344,8 @@ __global__ void __launch_bounds__(GemmCfg<kFp8, kAMN, kBMN, kEpi, kPair, kBN>::N
             }
           } else if (!kBMN) {
             load(sb, &tmB, k0, n0 + static_cast<int>(rank) * Cfg::B_ROWS, g, p.b_g);
+          } else if (p.b_mn4) {
+            load_mn4(sb, &tmB, k0, (n0 + static_cast<int>(rank) * Cfg::B_ROWS) / 64, g, p.b_g);
           } else {
 #pragma unroll
             for (int i = 0; i < Cfg::B_ROWS / 64; ++i)

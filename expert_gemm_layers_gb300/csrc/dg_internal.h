@@ -31,6 +31,17 @@ dg_status make_map_3d(CUtensorMap* map, bool is_bf16, const void* base, uint64_t
                       uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t b0, uint32_t b1, uint32_t b2,
                       const char* what);
 
+// The map of an MN-major GEMM operand (MN = d0, the contiguous dimension;
+// d1, d2, strides and the box's b1, b2 as for make_map_3d with b0 = 64).
+// When MN is a multiple of 64 the map is 4-D, (mn % 64, d1, d2, mn / 64)
+// with a last stride of 128 bytes, and its box (64, b1, b2, blocks) fetches
+// `blocks` 64-element MN blocks in one copy, stacked in shared memory
+// exactly like `blocks` separate 3-D boxes; *mn4 is set to 1.  Otherwise (or
+// if the driver rejects the 4-D form) it is the 3-D map and *mn4 = 0.
+dg_status make_map_mn(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
+                      uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t b1, uint32_t b2, uint32_t blocks,
+                      int32_t* mn4, const char* what);
+
 enum GemmVariant : int {
   GV_FP8_KK = 0,        // e4m3, A and B K-major, alpha/beta/C epilogue
   GV_BF16_KK_STORE = 1, // bf16, A and B K-major, plain store
@@ -106,6 +117,10 @@ constexpr bool kUsePairs = true;
 
 // Rows of a K-major B tile each CTA loads (the TMA box height of such B maps).
 constexpr int kKMajorBRows = kUsePairs ? 128 : 256;
+// 64-element MN blocks per stage of an MN-major operand: A (128 rows a CTA)
+// and B (a CTA's share of the tile's columns).
+constexpr uint32_t kMnBlocksA = 2;
+constexpr uint32_t kMnBlocksB = kKMajorBRows / 64;
 
 // Per device, once: the kernel's shared-memory attribute and the number of
 // co-resident CTA pairs (CTAs) -- host-side work kept off the launch path.
