@@ -778,6 +778,65 @@ __global__ void grad_reduce_kernel(const float* __restrict__ part, __nv_bfloat16
   }
 }
 
+// out[g, c] = sum over rows n of src[g*g_stride + n*row_stride + c] for a slab
+// of 256 columns per CTA: each lane owns 8 columns (one 16-byte load a row),
+// the CTA's warps take interleaved rows, and their fp32 partials are added in
+// warp order through shared memory.  Columns and row stride multiples of 8.
+constexpr int kColSumWarps = 16;
+__global__ void __launch_bounds__(32 * kColSumWarps) column_sum_slab_kernel(
+    const __nv_bfloat16* __restrict__ src, __nv_bfloat16* __restrict__ out, int rows, int ncols, int64_t g_stride,
+    int64_t row_stride, const uint32_t* err) {
+  __shared__ float part[kColSumWarps][256 + 4];
+  griddep_wait();
+  if (ld_volatile_u32(err) != 0u) return;
+  const int g = blockIdx.y;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int c = blockIdx.x * 256 + 8 * lane;
+  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  if (c < ncols) {
+    const __nv_bfloat16* p = src + g * g_stride + c;
+    int n = warp;
+    for (; n + 3 * kColSumWarps < rows; n += 4 * kColSumWarps) {
+      uint4 v[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) v[i] = __ldcs(reinterpret_cast<const uint4*>(p + (n + i * kColSumWarps) * row_stride));
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 f = unpack_bf16x2(w[e]);
+          acc[2 * e] += f.x;
+          acc[2 * e + 1] += f.y;
+        }
+      }
+    }
+    for (; n < rows; n += kColSumWarps) {
+      const uint4 v = __ldcs(reinterpret_cast<const uint4*>(p + n * row_stride));
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 f = unpack_bf16x2(w[e]);
+        acc[2 * e] += f.x;
+        acc[2 * e + 1] += f.y;
+      }
+    }
+  }
+#pragma unroll
+  for (int e = 0; e < 8; ++e) part[warp][8 * lane + e] = acc[e];
+  __syncthreads();
+  if (threadIdx.x < 128) {
+    const int cc = blockIdx.x * 256 + 2 * threadIdx.x;
+    float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+    for (int w = 0; w < kColSumWarps; ++w) {
+      s0 += part[w][2 * threadIdx.x];
+      s1 += part[w][2 * threadIdx.x + 1];
+    }
+    if (cc < ncols) *reinterpret_cast<uint32_t*>(out + static_cast<int64_t>(g) * ncols + cc) = pack_bf16x2(s0, s1);
+  }
+}
+
 // out[g, c] = sum over rows n of src[g*g_stride + n*row_stride + c]; two columns per thread.
 __global__ void column_sum_kernel(const __nv_bfloat16* __restrict__ src, __nv_bfloat16* __restrict__ out, int rows,
                                   int ncols, int64_t g_stride, int64_t row_stride, const uint32_t* err) {
@@ -1077,6 +1136,10 @@ cudaError_t launch_grad_reduce(const float* part, void* d_b1, void* d_nx_w, void
 
 cudaError_t launch_column_sum(const void* src, void* out, int G, int rows, int ncols, int64_t g_stride,
                               int64_t row_stride, const DeviceInfo& dev, cudaStream_t s) {
+  if (ncols % 8 == 0 && row_stride % 8 == 0 && g_stride % 8 == 0 && (reinterpret_cast<uintptr_t>(src) & 15u) == 0)
+    return launch_pdl(column_sum_slab_kernel, dim3((ncols + 255) / 256, G), dim3(32 * kColSumWarps), 0, s,
+                      static_cast<const __nv_bfloat16*>(src), static_cast<__nv_bfloat16*>(out), rows, ncols, g_stride,
+                      row_stride, dev.err);
   const int threads = 128;
   dim3 grid((ncols / 2 + threads - 1) / threads, G);
   return launch_pdl(column_sum_kernel, grid, dim3(threads), 0, s, static_cast<const __nv_bfloat16*>(src),
