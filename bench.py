@@ -47,15 +47,18 @@ FALLBACK_PEAKS = dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=
 # kernel whose sources changed since reports null.  Capture summary:
 # profiles/ffn_layer_kernels_traffic_T8.md.
 TRAFFIC = {
-    "ffn_gemm1": {"bytes_per_launch": 8 * 1.384868e+09, "sources": ["expert_gemm_layers_gb300/csrc/dg_gemm.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh", "expert_gemm_layers_gb300/csrc/dg_gemm_bf16_km_lnstats.cu"], "sha256": "b123a40f933bda2c0ab1c5011008851688923a307da03bd8ebded7ca0535a83f"},
-    "ffn_ln_gate_fwd": {"bytes_per_launch": 8 * 1.472826e+09, "sources": ["expert_gemm_layers_gb300/csrc/dg_rowops.cu", "expert_gemm_layers_gb300/csrc/dg_gate.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh"], "sha256": "898882bb8f87985a51ae9ba812b3d3f613cba2892fe48da6044ff2f77735bca5"},
-    "ffn_gemm2": {"bytes_per_launch": 8 * 1.170274e+09, "sources": ["expert_gemm_layers_gb300/csrc/dg_gemm.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh", "expert_gemm_layers_gb300/csrc/dg_gemm_bf16_km_bias.cu"], "sha256": "2d9a88fb5baeac441676751484ffebb16656647fbae4594fab1170dd0fa06cd6"},
-    "ffn_bwd_dhl": {"bytes_per_launch": 8 * 6.904627e+08, "sources": ["expert_gemm_layers_gb300/csrc/dg_gemm.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh", "expert_gemm_layers_gb300/csrc/dg_gemm_bf16_kk_store.cu"], "sha256": "dd10d6be8829e588a6c479b3fcca3d7188e9ba2ae99b70492cacaf08bc82e008"},
-    "ffn_bwd_dwout": {"bytes_per_launch": 8 * 1.121104e+09, "sources": ["expert_gemm_layers_gb300/csrc/dg_gemm.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh", "expert_gemm_layers_gb300/csrc/dg_gemm_bf16_mm_store.cu"], "sha256": "8f421cda73a0cccf49d2638dfbabcfa3cd33347bb10b0350baa017ea8c1fe572"},
-    "ffn_bwd_ln_rowsum": {"bytes_per_launch": 8 * 1.512092e+09, "sources": ["expert_gemm_layers_gb300/csrc/dg_rowops.cu", "expert_gemm_layers_gb300/csrc/dg_gate.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh"], "sha256": "898882bb8f87985a51ae9ba812b3d3f613cba2892fe48da6044ff2f77735bca5"},
-    "ffn_bwd_ln_apply": {"bytes_per_launch": 8 * 2.566492e+09, "sources": ["expert_gemm_layers_gb300/csrc/dg_rowops.cu", "expert_gemm_layers_gb300/csrc/dg_gate.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh"], "sha256": "898882bb8f87985a51ae9ba812b3d3f613cba2892fe48da6044ff2f77735bca5"},
-    "ffn_bwd_dx": {"bytes_per_launch": 8 * 2.750209e+09, "sources": ["expert_gemm_layers_gb300/csrc/dg_gemm.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh", "expert_gemm_layers_gb300/csrc/dg_gemm_bf16_kk_store.cu"], "sha256": "dd10d6be8829e588a6c479b3fcca3d7188e9ba2ae99b70492cacaf08bc82e008"},
-    "ffn_bwd_dw1": {"bytes_per_launch": 8 * 1.440493e+09, "sources": ["expert_gemm_layers_gb300/csrc/dg_gemm.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh", "expert_gemm_layers_gb300/csrc/dg_gemm_bf16_mm_store.cu"], "sha256": "8f421cda73a0cccf49d2638dfbabcfa3cd33347bb10b0350baa017ea8c1fe572"},
+    "ffn_gemm1": {"bytes_per_launch": 8 * 1.386433e+09, "sources": ["expert_gemm_layers_gb300/csrc/dg_gemm.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh", "expert_gemm_layers_gb300/csrc/dg_gemm_bf16_km_lnstats.cu"], "sha256": "8afcdd4a6a7f50b4d133b6653fb98d0fb0912dcbb06f440eaf87c018b4311422"},
+    "ffn_ln_stats": {"bytes_per_launch": 8 * 3.147315e+07, "sources": ["expert_gemm_layers_gb300/csrc/dg_rowops.cu", "expert_gemm_layers_gb300/csrc/dg_gate.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh"], "sha256": "c9d095c924206468119dc51d886b81df656a121343a7c0380d6df90e0fcad20a"},
+    "ffn_ln_gate_fwd": {"bytes_per_launch": 8 * 1.470545e+09, "sources": ["expert_gemm_layers_gb300/csrc/dg_rowops.cu", "expert_gemm_layers_gb300/csrc/dg_gate.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh"], "sha256": "c9d095c924206468119dc51d886b81df656a121343a7c0380d6df90e0fcad20a"},
+    "ffn_gemm2": {"bytes_per_launch": 8 * 1.152860e+09, "sources": ["expert_gemm_layers_gb300/csrc/dg_gemm.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh", "expert_gemm_layers_gb300/csrc/dg_gemm_bf16_km_bias.cu"], "sha256": "867afd998f8341c8d9725c3f61ae54b0384195f80931051ba151635de51bce1e"},
+    "ffn_bwd_dhl": {"bytes_per_launch": 8 * 6.894390e+08, "sources": ["expert_gemm_layers_gb300/csrc/dg_gemm.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh", "expert_gemm_layers_gb300/csrc/dg_gemm_bf16_kk_store.cu"], "sha256": "4a709c084460bdf230ac1fe092786e1865f6acc894cf42ae97ee2a04aad6271f"},
+    "ffn_bwd_dwout": {"bytes_per_launch": 8 * 1.078520e+09, "sources": ["expert_gemm_layers_gb300/csrc/dg_gemm.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh", "expert_gemm_layers_gb300/csrc/dg_gemm_bf16_mm_store.cu"], "sha256": "24bcf80e6b036856953a14c9d35431e74eba23c1e63c5bc9ec014e6d7d156351"},
+    "ffn_bwd_dbout": {"bytes_per_launch": 8 * 8.404147e+07, "sources": ["expert_gemm_layers_gb300/csrc/dg_rowops.cu", "expert_gemm_layers_gb300/csrc/dg_gate.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh"], "sha256": "c9d095c924206468119dc51d886b81df656a121343a7c0380d6df90e0fcad20a"},
+    "ffn_bwd_ln_rowsum": {"bytes_per_launch": 8 * 1.512003e+09, "sources": ["expert_gemm_layers_gb300/csrc/dg_rowops.cu", "expert_gemm_layers_gb300/csrc/dg_gate.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh"], "sha256": "c9d095c924206468119dc51d886b81df656a121343a7c0380d6df90e0fcad20a"},
+    "ffn_bwd_ln_apply": {"bytes_per_launch": 8 * 2.525803e+09, "sources": ["expert_gemm_layers_gb300/csrc/dg_rowops.cu", "expert_gemm_layers_gb300/csrc/dg_gate.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh"], "sha256": "c9d095c924206468119dc51d886b81df656a121343a7c0380d6df90e0fcad20a"},
+    "ffn_bwd_grad_reduce": {"bytes_per_launch": 8 * 4.722867e+07, "sources": ["expert_gemm_layers_gb300/csrc/dg_rowops.cu", "expert_gemm_layers_gb300/csrc/dg_gate.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh"], "sha256": "c9d095c924206468119dc51d886b81df656a121343a7c0380d6df90e0fcad20a"},
+    "ffn_bwd_dx": {"bytes_per_launch": 8 * 2.304352e+09, "sources": ["expert_gemm_layers_gb300/csrc/dg_gemm.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh", "expert_gemm_layers_gb300/csrc/dg_gemm_bf16_kk_store.cu"], "sha256": "4a709c084460bdf230ac1fe092786e1865f6acc894cf42ae97ee2a04aad6271f"},
+    "ffn_bwd_dw1": {"bytes_per_launch": 8 * 1.426068e+09, "sources": ["expert_gemm_layers_gb300/csrc/dg_gemm.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh", "expert_gemm_layers_gb300/csrc/dg_gemm_bf16_mm_store.cu"], "sha256": "24bcf80e6b036856953a14c9d35431e74eba23c1e63c5bc9ec014e6d7d156351"},
 }
 
 
