@@ -452,6 +452,50 @@ __global__ void __launch_bounds__(GemmCfg<kFp8, kAMN, kBMN, kEpi, kPair, kBN>::N
     uint32_t pending = 0, pending_parity = 0;  // async loads in flight, per staging buffer
     bool ok = true;
     const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(32 * lg) << 16);
+    // Epilogue parameters of one tile held by this thread: its part of the
+    // bias and of the e4m3 column scales, and its row's e4m3 scale.
+    struct TileParams {
+      uint4 b;
+      float4 sc;
+      float rs;
+    };
+    const int et = static_cast<int>(threadIdx.x) - 64;  // epilogue thread 0..127
+    auto fetch_params = [&](int t, TileParams& q) {
+      q.b = make_uint4(0u, 0u, 0u, 0u);
+      q.sc = make_float4(0.f, 0.f, 0.f, 0.f);
+      q.rs = 0.0f;
+      if (t >= total_tiles) return;
+      const int g = t / tiles_per_group;
+      int mt, nt;
+      tile_coords(p, t - g * tiles_per_group, mt, nt);
+      const int n0 = nt * Cfg::BN_OUT;
+      if (Cfg::HAS_BIAS && et < Cfg::BN_OUT / 8) {
+        const int c = n0 + 8 * et;
+        if (c < p.N) q.b = __ldg(reinterpret_cast<const uint4*>(p.bias + static_cast<int64_t>(g) * p.bias_g_stride + c));
+      }
+      if (Cfg::HAS_SCALES) {
+        if (et < Cfg::BN_OUT / 4) {
+          const int c = n0 + 4 * et;
+          if (c < p.N)
+            q.sc = __ldg(reinterpret_cast<const float4*>(p.col_scale + static_cast<int64_t>(g) * p.col_scale_g + c));
+        }
+        const int row = mt * Cfg::UMMA_M + static_cast<int>(rank) * Cfg::BM + 32 * lg + lane;
+        if (row < p.M) q.rs = __ldg(p.row_scale + static_cast<int64_t>(g) * p.row_scale_g + row);
+      }
+    };
+    auto publish_params = [&](const TileParams& q, int buf) {
+      if (Cfg::HAS_BIAS && et < Cfg::BN_OUT / 8)
+        reinterpret_cast<uint4*>(param_base + buf * Cfg::BIAS_BYTES)[et] = q.b;
+      if (Cfg::HAS_SCALES && et < Cfg::BN_OUT / 4)
+        reinterpret_cast<float4*>(param_base + 2 * Cfg::BIAS_BYTES + buf * Cfg::SCALE_BYTES)[et] = q.sc;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&pready[buf]);
+    };
+    TileParams prm;
+    if (Cfg::HAS_BIAS || Cfg::HAS_SCALES) {
+      fetch_params(unit, prm);
+      publish_params(prm, 0);
+    }
     int local = 0;
     for (int tile = unit; tile < total_tiles && ok; tile += num_units, ++local) {
       const int g = tile / tiles_per_group;
@@ -479,34 +523,19 @@ __global__ void __launch_bounds__(GemmCfg<kFp8, kAMN, kBMN, kEpi, kPair, kBN>::N
       };
       if (use_c && nchunks > 0) issue_load(0, static_cast<int>(chunk_ctr & 1u));
 
-      // This tile's bias and column scales into shared memory (while the MMA
-      // runs); buffer `local & 1`, published by pready after every warp wrote
-      // its part.  A buffer is rewritten two tiles later, after every warp has
-      // passed the next tile's pready, i.e. finished reading it.
+      // This tile's bias and column scales sit in shared-memory buffer
+      // `local & 1`, published by pready at the end of the previous tile (or
+      // before the first); the next tile's are fetched into registers now and
+      // published once this tile's chunks are done.  A buffer is rewritten
+      // two tiles later, after every warp has passed the next tile's pready,
+      // i.e. finished reading it.
       const int pb = local & 1;
       const uint4* sbias = reinterpret_cast<const uint4*>(param_base + pb * Cfg::BIAS_BYTES);
       const float4* sscale = reinterpret_cast<const float4*>(param_base + 2 * Cfg::BIAS_BYTES + pb * Cfg::SCALE_BYTES);
-      float rsc = 0.0f;
+      const float rsc = prm.rs;
+      TileParams nxt;
       if (Cfg::HAS_BIAS || Cfg::HAS_SCALES) {
-        const int et = static_cast<int>(threadIdx.x) - 64;  // epilogue thread 0..127
-        if (Cfg::HAS_BIAS && et < Cfg::BN_OUT / 8) {
-          const int c = n0 + 8 * et;
-          const uint4 b = c < p.N ? __ldg(reinterpret_cast<const uint4*>(p.bias + static_cast<int64_t>(g) * p.bias_g_stride + c))
-                                  : make_uint4(0u, 0u, 0u, 0u);
-          const_cast<uint4*>(sbias)[et] = b;
-        }
-        if (Cfg::HAS_SCALES) {
-          if (et < Cfg::BN_OUT / 4) {
-            const int c = n0 + 4 * et;
-            const float4 sc = c < p.N ? __ldg(reinterpret_cast<const float4*>(p.col_scale + static_cast<int64_t>(g) * p.col_scale_g + c))
-                                      : make_float4(0.f, 0.f, 0.f, 0.f);
-            const_cast<float4*>(sscale)[et] = sc;
-          }
-          const int row = row0 + lane;
-          rsc = row < p.M ? __ldg(p.row_scale + static_cast<int64_t>(g) * p.row_scale_g + row) : 0.0f;
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&pready[pb]);
+        fetch_params(tile + num_units, nxt);
         if (!mbar_wait(&pready[pb], static_cast<uint32_t>(local >> 1) & 1u, p.err, SITE_PARAM)) {
           ok = false;
           break;
@@ -712,6 +741,10 @@ __global__ void __launch_bounds__(GemmCfg<kFp8, kAMN, kBMN, kEpi, kPair, kBN>::N
             make_float4(st_u.mean, st_u.m2, st_g.mean, st_g.m2);
       }
       chunk_ctr += static_cast<uint32_t>(nchunks);
+      if (Cfg::HAS_BIAS || Cfg::HAS_SCALES) {
+        publish_params(nxt, pb ^ 1);
+        prm = nxt;
+      }
       tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) {
