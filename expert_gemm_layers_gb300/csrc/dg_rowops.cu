@@ -55,6 +55,19 @@ __device__ __forceinline__ uint32_t e4m3_code(float x, float inv) {
   return static_cast<uint32_t>(__nv_cvt_float_to_fp8(__fmul_rn(x, inv), __NV_SATFINITE, __NV_E4M3));
 }
 
+// Codes of eight values, packed little-endian into two words: the same
+// binary32 products and round-to-nearest-even saturating conversions as
+// e4m3_code, two values per multiply and per conversion.
+__device__ __forceinline__ uint2 e4m3_code8(const float (&x)[8], float inv) {
+  const float2 iv = make_float2(inv, inv);
+  uint32_t h[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e)
+    h[e] = static_cast<uint32_t>(
+        __nv_cvt_float2_to_fp8x2(mul2(make_float2(x[2 * e], x[2 * e + 1]), iv), __NV_SATFINITE, __NV_E4M3));
+  return make_uint2(h[0] | (h[1] << 16), h[2] | (h[3] << 16));
+}
+
 // Scale (amax / 448) and inverse scale (448 / amax) of a vector whose largest
 // magnitude is amax; both 1 for an all-zero vector.
 __device__ __forceinline__ float e4m3_scale(float amax) { return amax > 0.0f ? __fdiv_rn(amax, 448.0f) : 1.0f; }
@@ -191,11 +204,7 @@ __global__ void __launch_bounds__(NT, 512 / NT) ln_gate_fwd_kernel(
     for (int j = 0; j < VPT; ++j) {
       const int v = vbase + threadIdx.x + NT * j;
       if (v < nvec) {
-        uint32_t c[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) c[e] = e4m3_code(o_prev[j][e], inv);
-        *reinterpret_cast<uint2*>(qrow + 8 * v) =
-            make_uint2(c[0] | (c[1] << 8) | (c[2] << 16) | (c[3] << 24), c[4] | (c[5] << 8) | (c[6] << 16) | (c[7] << 24));
+        *reinterpret_cast<uint2*>(qrow + 8 * v) = e4m3_code8(o_prev[j], inv);
       }
     }
     if (threadIdx.x == 0) hs[krow] = e4m3_scale(m);
@@ -294,11 +303,7 @@ __global__ void quant_rows_kernel(const __nv_bfloat16* __restrict__ x, uint8_t* 
     for (int c = 8 * lane; c < D; c += 256) {
       float f[8];
       unpack8(__ldg(reinterpret_cast<const uint4*>(xr + c)), f);
-      uint32_t k[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) k[e] = e4m3_code(f[e], inv);
-      *reinterpret_cast<uint2*>(qr + c) =
-          make_uint2(k[0] | (k[1] << 8) | (k[2] << 16) | (k[3] << 24), k[4] | (k[5] << 8) | (k[6] << 16) | (k[7] << 24));
+      *reinterpret_cast<uint2*>(qr + c) = e4m3_code8(f, inv);
     }
     if (lane == 0) {
       const int64_t sb = row / T;  // s*B + b
