@@ -47,18 +47,18 @@ FALLBACK_PEAKS = dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=
 # kernel whose sources changed since reports null.  Capture summary:
 # profiles/ffn_layer_kernels_traffic_T8.md.
 TRAFFIC = {
-    "ffn_gemm1": {"bytes_per_launch": 8 * 1.386433e+09, "sources": ["expert_gemm_layers_gb300/csrc/dg_gemm.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh", "expert_gemm_layers_gb300/csrc/dg_gemm_bf16_km_lnstats.cu"], "sha256": "8afcdd4a6a7f50b4d133b6653fb98d0fb0912dcbb06f440eaf87c018b4311422"},
-    "ffn_ln_stats": {"bytes_per_launch": 8 * 3.147315e+07, "sources": ["expert_gemm_layers_gb300/csrc/dg_rowops.cu", "expert_gemm_layers_gb300/csrc/dg_gate.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh"], "sha256": "c9d095c924206468119dc51d886b81df656a121343a7c0380d6df90e0fcad20a"},
-    "ffn_ln_gate_fwd": {"bytes_per_launch": 8 * 1.470545e+09, "sources": ["expert_gemm_layers_gb300/csrc/dg_rowops.cu", "expert_gemm_layers_gb300/csrc/dg_gate.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh"], "sha256": "c9d095c924206468119dc51d886b81df656a121343a7c0380d6df90e0fcad20a"},
-    "ffn_gemm2": {"bytes_per_launch": 8 * 1.152860e+09, "sources": ["expert_gemm_layers_gb300/csrc/dg_gemm.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh", "expert_gemm_layers_gb300/csrc/dg_gemm_bf16_km_bias.cu"], "sha256": "867afd998f8341c8d9725c3f61ae54b0384195f80931051ba151635de51bce1e"},
-    "ffn_bwd_dhl": {"bytes_per_launch": 8 * 6.894390e+08, "sources": ["expert_gemm_layers_gb300/csrc/dg_gemm.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh", "expert_gemm_layers_gb300/csrc/dg_gemm_bf16_kk_store.cu"], "sha256": "4a709c084460bdf230ac1fe092786e1865f6acc894cf42ae97ee2a04aad6271f"},
-    "ffn_bwd_dwout": {"bytes_per_launch": 8 * 1.078520e+09, "sources": ["expert_gemm_layers_gb300/csrc/dg_gemm.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh", "expert_gemm_layers_gb300/csrc/dg_gemm_bf16_mm_store.cu"], "sha256": "24bcf80e6b036856953a14c9d35431e74eba23c1e63c5bc9ec014e6d7d156351"},
-    "ffn_bwd_dbout": {"bytes_per_launch": 8 * 8.404147e+07, "sources": ["expert_gemm_layers_gb300/csrc/dg_rowops.cu", "expert_gemm_layers_gb300/csrc/dg_gate.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh"], "sha256": "c9d095c924206468119dc51d886b81df656a121343a7c0380d6df90e0fcad20a"},
-    "ffn_bwd_ln_rowsum": {"bytes_per_launch": 8 * 1.512003e+09, "sources": ["expert_gemm_layers_gb300/csrc/dg_rowops.cu", "expert_gemm_layers_gb300/csrc/dg_gate.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh"], "sha256": "c9d095c924206468119dc51d886b81df656a121343a7c0380d6df90e0fcad20a"},
-    "ffn_bwd_ln_apply": {"bytes_per_launch": 8 * 2.525803e+09, "sources": ["expert_gemm_layers_gb300/csrc/dg_rowops.cu", "expert_gemm_layers_gb300/csrc/dg_gate.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh"], "sha256": "c9d095c924206468119dc51d886b81df656a121343a7c0380d6df90e0fcad20a"},
-    "ffn_bwd_grad_reduce": {"bytes_per_launch": 8 * 4.722867e+07, "sources": ["expert_gemm_layers_gb300/csrc/dg_rowops.cu", "expert_gemm_layers_gb300/csrc/dg_gate.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh"], "sha256": "c9d095c924206468119dc51d886b81df656a121343a7c0380d6df90e0fcad20a"},
-    "ffn_bwd_dx": {"bytes_per_launch": 8 * 2.304352e+09, "sources": ["expert_gemm_layers_gb300/csrc/dg_gemm.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh", "expert_gemm_layers_gb300/csrc/dg_gemm_bf16_kk_store.cu"], "sha256": "4a709c084460bdf230ac1fe092786e1865f6acc894cf42ae97ee2a04aad6271f"},
-    "ffn_bwd_dw1": {"bytes_per_launch": 8 * 1.426068e+09, "sources": ["expert_gemm_layers_gb300/csrc/dg_gemm.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh", "expert_gemm_layers_gb300/csrc/dg_gemm_bf16_mm_store.cu"], "sha256": "24bcf80e6b036856953a14c9d35431e74eba23c1e63c5bc9ec014e6d7d156351"},
+    "ffn_gemm1": {"bytes_per_launch": 8 * 1.386334e+09, "sources": ["expert_gemm_layers_gb300/csrc/dg_gemm.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh", "expert_gemm_layers_gb300/csrc/dg_gemm_bf16_km_lnstats.cu"], "sha256": "186e43b2f6bf1c3cebf6b3fdec451cabed49f45423acc6488abee9e06c70f85d"},
+    "ffn_ln_stats": {"bytes_per_launch": 8 * 3.147955e+07, "sources": ["expert_gemm_layers_gb300/csrc/dg_rowops.cu", "expert_gemm_layers_gb300/csrc/dg_gate.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh"], "sha256": "334d414edec8c93714706014a1041942a1d018f0cf7442a6edd7923129906b9b"},
+    "ffn_ln_gate_fwd": {"bytes_per_launch": 8 * 1.469441e+09, "sources": ["expert_gemm_layers_gb300/csrc/dg_rowops.cu", "expert_gemm_layers_gb300/csrc/dg_gate.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh"], "sha256": "334d414edec8c93714706014a1041942a1d018f0cf7442a6edd7923129906b9b"},
+    "ffn_gemm2": {"bytes_per_launch": 8 * 1.160083e+09, "sources": ["expert_gemm_layers_gb300/csrc/dg_gemm.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh", "expert_gemm_layers_gb300/csrc/dg_gemm_bf16_km_bias.cu"], "sha256": "5f41e3664194d21d2f63d7ea3aeb955b6a3f413aec6269dbfcb6881e6d3b2544"},
+    "ffn_bwd_dhl": {"bytes_per_launch": 8 * 6.902103e+08, "sources": ["expert_gemm_layers_gb300/csrc/dg_gemm.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh", "expert_gemm_layers_gb300/csrc/dg_gemm_bf16_kk_store.cu"], "sha256": "78533b6c63d882685b2d39f300cf98762b9ffa59ba9216ab44f4f5794f2a8227"},
+    "ffn_bwd_dwout": {"bytes_per_launch": 8 * 1.102403e+09, "sources": ["expert_gemm_layers_gb300/csrc/dg_gemm.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh", "expert_gemm_layers_gb300/csrc/dg_gemm_bf16_mm_store.cu"], "sha256": "1c23c5d6678819154a72c8ee86301c60c888845f06dabd6adee88a1d1e7659be"},
+    "ffn_bwd_dbout": {"bytes_per_launch": 8 * 8.391731e+07, "sources": ["expert_gemm_layers_gb300/csrc/dg_rowops.cu", "expert_gemm_layers_gb300/csrc/dg_gate.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh"], "sha256": "334d414edec8c93714706014a1041942a1d018f0cf7442a6edd7923129906b9b"},
+    "ffn_bwd_ln_rowsum": {"bytes_per_launch": 8 * 1.512054e+09, "sources": ["expert_gemm_layers_gb300/csrc/dg_rowops.cu", "expert_gemm_layers_gb300/csrc/dg_gate.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh"], "sha256": "334d414edec8c93714706014a1041942a1d018f0cf7442a6edd7923129906b9b"},
+    "ffn_bwd_ln_apply": {"bytes_per_launch": 8 * 2.526297e+09, "sources": ["expert_gemm_layers_gb300/csrc/dg_rowops.cu", "expert_gemm_layers_gb300/csrc/dg_gate.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh"], "sha256": "334d414edec8c93714706014a1041942a1d018f0cf7442a6edd7923129906b9b"},
+    "ffn_bwd_grad_reduce": {"bytes_per_launch": 8 * 4.722867e+07, "sources": ["expert_gemm_layers_gb300/csrc/dg_rowops.cu", "expert_gemm_layers_gb300/csrc/dg_gate.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh"], "sha256": "334d414edec8c93714706014a1041942a1d018f0cf7442a6edd7923129906b9b"},
+    "ffn_bwd_dx": {"bytes_per_launch": 8 * 2.519801e+09, "sources": ["expert_gemm_layers_gb300/csrc/dg_gemm.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh", "expert_gemm_layers_gb300/csrc/dg_gemm_bf16_kk_store.cu"], "sha256": "78533b6c63d882685b2d39f300cf98762b9ffa59ba9216ab44f4f5794f2a8227"},
+    "ffn_bwd_dw1": {"bytes_per_launch": 8 * 1.489717e+09, "sources": ["expert_gemm_layers_gb300/csrc/dg_gemm.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh", "expert_gemm_layers_gb300/csrc/dg_gemm_bf16_mm_store.cu"], "sha256": "1c23c5d6678819154a72c8ee86301c60c888845f06dabd6adee88a1d1e7659be"},
 }
 
 
