@@ -188,10 +188,11 @@ __global__ void __launch_bounds__(NT, 512 / NT) ln_gate_fwd_kernel(
   for (int i = 0; i < kFwdStages - 1; ++i) issue(i);
   float4 st_next = n_mine > 0 ? stats[row0] : make_float4(0.f, 0.f, 0.f, 0.f);
   const float2 half2 = make_float2(0.5f, 0.5f);
-  // e4m3 output: the previous row's values wait here for its amax
-  float o_prev[VPT][8];
+  // e4m3 output: the previous row's values wait in the other of two arrays
+  // (the rows alternate between them) for that row's amax
+  float oa[VPT][8], ob[VPT][8];
   int64_t prev_row = 0;
-  auto finish_row = [&](int64_t k, int64_t krow) -> bool {
+  auto finish_row = [&](int64_t k, int64_t krow, const float (&o_prev)[VPT][8]) -> bool {
     const int slot = static_cast<int>(k & 3);
     const uint32_t parity = static_cast<uint32_t>(k >> 2) & 1u;
     if (!__all_sync(0xffffffffu, mbar_wait(&rbar[slot], parity, err, 0x41u))) return false;  // warp-uniform
@@ -210,7 +211,7 @@ __global__ void __launch_bounds__(NT, 512 / NT) ln_gate_fwd_kernel(
     if (threadIdx.x == 0) hs[krow] = e4m3_scale(m);
     return true;
   };
-  for (int64_t i = 0; i < n_mine; ++i) {
+  auto do_row = [&](int64_t i, float (&o)[VPT][8], const float (&o_prev)[VPT][8]) -> bool {
     issue(i + kFwdStages - 1);
     const int64_t row = row0 + i * stride;
     const float4 sr = st_next;
@@ -219,7 +220,6 @@ __global__ void __launch_bounds__(NT, 512 / NT) ln_gate_fwd_kernel(
     const uint4* st = ring + (i % kFwdStages) * (VPT * 2 * NT);
     const float2 rsu = make_float2(sr.y, sr.y), cu = make_float2(-sr.x * sr.y, -sr.x * sr.y);
     const float2 rsg = make_float2(sr.w, sr.w), cgs = make_float2(-sr.z * sr.w, -sr.z * sr.w);
-    float o[VPT][8];
     float amax = 0.0f;
 #pragma unroll
     for (int j = 0; j < VPT; ++j) {
@@ -259,15 +259,20 @@ __global__ void __launch_bounds__(NT, 512 / NT) ln_gate_fwd_kernel(
         red_max[slot][threadIdx.x >> 5] = wmax;
         mbar_arrive(&rbar[slot]);
       }
-      if (i > 0 && !finish_row(i - 1, prev_row)) return;
-#pragma unroll
-      for (int j = 0; j < VPT; ++j)
-#pragma unroll
-        for (int e = 0; e < 8; ++e) o_prev[j][e] = o[j][e];
+      if (i > 0 && !finish_row(i - 1, prev_row, o_prev)) return false;
       prev_row = row;
     }
+    return true;
+  };
+  if (kFp8Out) {
+    for (int64_t i = 0; i < n_mine; i += 2) {
+      if (!do_row(i, oa, ob)) return;
+      if (i + 1 < n_mine && !do_row(i + 1, ob, oa)) return;
+    }
+  } else {
+    for (int64_t i = 0; i < n_mine; ++i) do_row(i, oa, ob);
   }
-  if (kFp8Out && n_mine > 0 && !finish_row(n_mine - 1, prev_row)) return;
+  if (kFp8Out && n_mine > 0 && !finish_row(n_mine - 1, prev_row, ((n_mine - 1) & 1) ? ob : oa)) return;
   cp_async_wait<0>();
 }
 
