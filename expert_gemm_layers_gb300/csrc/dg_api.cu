@@ -508,6 +508,7 @@ dg_status dg_a2a_ffn_fwd(const dg_ffn_shape* shape, const void* inputs, const vo
   p2.d_g = G_MID;
   p2.bias = static_cast<const __nv_bfloat16*>(bout);
   p2.bias_g_stride = static_cast<int64_t>(D);
+  p2.n_fastest = 1;
   return run_gemm(GV_BF16_KM_BIAS, mh, mwo, mo, mo, p2, dev, s, "ffn_gemm2",
                   2.0 * (rows * H + static_cast<double>(T) * H * D + rows * D));
 }
@@ -590,6 +591,7 @@ dg_status dg_a2a_ffn_bwd(const dg_ffn_shape* shape, const void* inputs, const vo
   p.d_g = G_OUTER;
   p.a_mn4 = hl_mn4;
   p.b_mn4 = dyn_mn4;
+  p.n_fastest = 1;
   if ((st = run_gemm(GV_BF16_MM_STORE, mhl_t, mdy_n, mdwo, mdwo, p, dev, s, "ffn_bwd_dwout",
                      2.0 * (rows * H + rows * D + static_cast<double>(T) * H * D))) != DG_OK)
     return st;
@@ -643,6 +645,7 @@ dg_status dg_a2a_ffn_bwd(const dg_ffn_shape* shape, const void* inputs, const vo
   p.a_g = G_OUTER;
   p.b_g = G_OUTER;
   p.d_g = G_MID;
+  p.n_fastest = 1;
   if ((st = run_gemm(GV_BF16_KK_STORE, mdz_k, mw1_k, mdx, mdx, p, dev, s, "ffn_bwd_dx",
                      2.0 * (rows * 2 * H + static_cast<double>(T) * D * 2 * H + rows * D))) != DG_OK)
     return st;
