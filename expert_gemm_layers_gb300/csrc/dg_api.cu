@@ -913,6 +913,7 @@ dg_status dg_a2a_ffn_fwd_fp8(const dg_ffn_shape* shape, const void* inputs, cons
   p2.row_scale_g = static_cast<int64_t>(M);
   p2.col_scale = reinterpret_cast<const float*>(pk + wl.so);
   p2.col_scale_g = static_cast<int64_t>(D);
+  p2.n_fastest = 1;
   return run_gemm(GV_FP8_KK_BIAS, mh, mwo, mo, mo, p2, dev, s, "ffn_fp8_gemm2",
                   rows * H + static_cast<double>(T) * H * D + rows * D * 2.0 + rows * 4);
 }
