@@ -199,6 +199,10 @@ dg_status run_gemm(GemmVariant v, const CUtensorMap& a, const CUtensorMap& b, co
                    double bytes) {
   p.tiles_m = (p.M + gemm_tile_m() - 1) / gemm_tile_m();
   p.tiles_n = (p.N + gemm_tile_n(v) - 1) / gemm_tile_n(v);
+  // Tile order within a problem: along the longer side fastest, so the tiles
+  // that share a panel of the larger operand run on neighbouring CTA pairs at
+  // the same time (measured on every FFN and TP launch of the benchmark).
+  p.n_fastest = p.tiles_n < p.tiles_m ? 1 : 0;
   p.err = dev.err;
   const int64_t tiles = static_cast<int64_t>(p.G) * p.tiles_m * p.tiles_n;
   if (tiles == 0) return DG_OK;
@@ -508,7 +512,6 @@ dg_status dg_a2a_ffn_fwd(const dg_ffn_shape* shape, const void* inputs, const vo
   p2.d_g = G_MID;
   p2.bias = static_cast<const __nv_bfloat16*>(bout);
   p2.bias_g_stride = static_cast<int64_t>(D);
-  p2.n_fastest = 1;
   return run_gemm(GV_BF16_KM_BIAS, mh, mwo, mo, mo, p2, dev, s, "ffn_gemm2",
                   2.0 * (rows * H + static_cast<double>(T) * H * D + rows * D));
 }
@@ -591,7 +594,6 @@ dg_status dg_a2a_ffn_bwd(const dg_ffn_shape* shape, const void* inputs, const vo
   p.d_g = G_OUTER;
   p.a_mn4 = hl_mn4;
   p.b_mn4 = dyn_mn4;
-  p.n_fastest = 1;
   if ((st = run_gemm(GV_BF16_MM_STORE, mhl_t, mdy_n, mdwo, mdwo, p, dev, s, "ffn_bwd_dwout",
                      2.0 * (rows * H + rows * D + static_cast<double>(T) * H * D))) != DG_OK)
     return st;
@@ -645,7 +647,6 @@ dg_status dg_a2a_ffn_bwd(const dg_ffn_shape* shape, const void* inputs, const vo
   p.a_g = G_OUTER;
   p.b_g = G_OUTER;
   p.d_g = G_MID;
-  p.n_fastest = 1;
   if ((st = run_gemm(GV_BF16_KK_STORE, mdz_k, mw1_k, mdx, mdx, p, dev, s, "ffn_bwd_dx",
                      2.0 * (rows * 2 * H + static_cast<double>(T) * D * 2 * H + rows * D))) != DG_OK)
     return st;
@@ -913,7 +914,6 @@ dg_status dg_a2a_ffn_fwd_fp8(const dg_ffn_shape* shape, const void* inputs, cons
   p2.row_scale_g = static_cast<int64_t>(M);
   p2.col_scale = reinterpret_cast<const float*>(pk + wl.so);
   p2.col_scale_g = static_cast<int64_t>(D);
-  p2.n_fastest = 1;
   return run_gemm(GV_FP8_KK_BIAS, mh, mwo, mo, mo, p2, dev, s, "ffn_fp8_gemm2",
                   rows * H + static_cast<double>(T) * H * D + rows * D * 2.0 + rows * 4);
 }
