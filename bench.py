@@ -43,22 +43,23 @@ FALLBACK_PEAKS = dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=
 # Per-launch DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) from
 # one ncu capture of each kernel of the FFN layer at T=8 token positions (an
 # eighth of the benchmark's problems; traffic grows in proportion, so it is
-# scaled by 8), with the sha256 of the kernel's sources at capture time; a
-# kernel whose sources changed since reports null.  Capture summary:
+# scaled by 8), with the sha256 of the kernel's sources (for a GEMM also the
+# launch code, which picks its tile order) at capture time; a kernel whose
+# sources changed since reports null.  Capture summary:
 # profiles/ffn_layer_kernels_traffic_T8.md.
 TRAFFIC = {
-    "ffn_gemm1": {"bytes_per_launch": 8 * 1.386334e+09, "sources": ["expert_gemm_layers_gb300/csrc/dg_gemm.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh", "expert_gemm_layers_gb300/csrc/dg_gemm_bf16_km_lnstats.cu"], "sha256": "186e43b2f6bf1c3cebf6b3fdec451cabed49f45423acc6488abee9e06c70f85d"},
-    "ffn_ln_stats": {"bytes_per_launch": 8 * 3.147955e+07, "sources": ["expert_gemm_layers_gb300/csrc/dg_rowops.cu", "expert_gemm_layers_gb300/csrc/dg_gate.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh"], "sha256": "334d414edec8c93714706014a1041942a1d018f0cf7442a6edd7923129906b9b"},
-    "ffn_ln_gate_fwd": {"bytes_per_launch": 8 * 1.469441e+09, "sources": ["expert_gemm_layers_gb300/csrc/dg_rowops.cu", "expert_gemm_layers_gb300/csrc/dg_gate.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh"], "sha256": "334d414edec8c93714706014a1041942a1d018f0cf7442a6edd7923129906b9b"},
-    "ffn_gemm2": {"bytes_per_launch": 8 * 1.160083e+09, "sources": ["expert_gemm_layers_gb300/csrc/dg_gemm.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh", "expert_gemm_layers_gb300/csrc/dg_gemm_bf16_km_bias.cu"], "sha256": "5f41e3664194d21d2f63d7ea3aeb955b6a3f413aec6269dbfcb6881e6d3b2544"},
-    "ffn_bwd_dhl": {"bytes_per_launch": 8 * 6.902103e+08, "sources": ["expert_gemm_layers_gb300/csrc/dg_gemm.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh", "expert_gemm_layers_gb300/csrc/dg_gemm_bf16_kk_store.cu"], "sha256": "78533b6c63d882685b2d39f300cf98762b9ffa59ba9216ab44f4f5794f2a8227"},
-    "ffn_bwd_dwout": {"bytes_per_launch": 8 * 1.102403e+09, "sources": ["expert_gemm_layers_gb300/csrc/dg_gemm.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh", "expert_gemm_layers_gb300/csrc/dg_gemm_bf16_mm_store.cu"], "sha256": "1c23c5d6678819154a72c8ee86301c60c888845f06dabd6adee88a1d1e7659be"},
-    "ffn_bwd_dbout": {"bytes_per_launch": 8 * 8.391731e+07, "sources": ["expert_gemm_layers_gb300/csrc/dg_rowops.cu", "expert_gemm_layers_gb300/csrc/dg_gate.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh"], "sha256": "334d414edec8c93714706014a1041942a1d018f0cf7442a6edd7923129906b9b"},
-    "ffn_bwd_ln_rowsum": {"bytes_per_launch": 8 * 1.512054e+09, "sources": ["expert_gemm_layers_gb300/csrc/dg_rowops.cu", "expert_gemm_layers_gb300/csrc/dg_gate.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh"], "sha256": "334d414edec8c93714706014a1041942a1d018f0cf7442a6edd7923129906b9b"},
-    "ffn_bwd_ln_apply": {"bytes_per_launch": 8 * 2.526297e+09, "sources": ["expert_gemm_layers_gb300/csrc/dg_rowops.cu", "expert_gemm_layers_gb300/csrc/dg_gate.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh"], "sha256": "334d414edec8c93714706014a1041942a1d018f0cf7442a6edd7923129906b9b"},
-    "ffn_bwd_grad_reduce": {"bytes_per_launch": 8 * 4.722867e+07, "sources": ["expert_gemm_layers_gb300/csrc/dg_rowops.cu", "expert_gemm_layers_gb300/csrc/dg_gate.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh"], "sha256": "334d414edec8c93714706014a1041942a1d018f0cf7442a6edd7923129906b9b"},
-    "ffn_bwd_dx": {"bytes_per_launch": 8 * 2.519801e+09, "sources": ["expert_gemm_layers_gb300/csrc/dg_gemm.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh", "expert_gemm_layers_gb300/csrc/dg_gemm_bf16_kk_store.cu"], "sha256": "78533b6c63d882685b2d39f300cf98762b9ffa59ba9216ab44f4f5794f2a8227"},
-    "ffn_bwd_dw1": {"bytes_per_launch": 8 * 1.489717e+09, "sources": ["expert_gemm_layers_gb300/csrc/dg_gemm.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh", "expert_gemm_layers_gb300/csrc/dg_gemm_bf16_mm_store.cu"], "sha256": "1c23c5d6678819154a72c8ee86301c60c888845f06dabd6adee88a1d1e7659be"},
+    "ffn_gemm1": {"bytes_per_launch": 8 * 1.386331e+09, "sources": ["expert_gemm_layers_gb300/csrc/dg_gemm.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh", "expert_gemm_layers_gb300/csrc/dg_gemm_bf16_km_lnstats.cu", "expert_gemm_layers_gb300/csrc/dg_api.cu"], "sha256": "9a8d652b487a6045c7a01af36f6aad7f2b3fdd8afb7c475083de1fcdd13039ba"},
+    "ffn_ln_stats": {"bytes_per_launch": 8 * 3.147341e+07, "sources": ["expert_gemm_layers_gb300/csrc/dg_rowops.cu", "expert_gemm_layers_gb300/csrc/dg_gate.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh"], "sha256": "11cc40550008b41dcf95458ed76c0e31aa48bd4716d58882e0e1f39376e83dbe"},
+    "ffn_ln_gate_fwd": {"bytes_per_launch": 8 * 1.470191e+09, "sources": ["expert_gemm_layers_gb300/csrc/dg_rowops.cu", "expert_gemm_layers_gb300/csrc/dg_gate.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh"], "sha256": "11cc40550008b41dcf95458ed76c0e31aa48bd4716d58882e0e1f39376e83dbe"},
+    "ffn_gemm2": {"bytes_per_launch": 8 * 9.025352e+08, "sources": ["expert_gemm_layers_gb300/csrc/dg_gemm.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh", "expert_gemm_layers_gb300/csrc/dg_gemm_bf16_km_bias.cu", "expert_gemm_layers_gb300/csrc/dg_api.cu"], "sha256": "b8c6368e8b96cd576fbe627a8a6e840d66f81aaf8ac5654d34f3f1d4215a570e"},
+    "ffn_bwd_dhl": {"bytes_per_launch": 8 * 6.895360e+08, "sources": ["expert_gemm_layers_gb300/csrc/dg_gemm.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh", "expert_gemm_layers_gb300/csrc/dg_gemm_bf16_kk_store.cu", "expert_gemm_layers_gb300/csrc/dg_api.cu"], "sha256": "25eb58162d935448137220d78d25e63b37fc905fdcb956c46c30a89007734750"},
+    "ffn_bwd_dwout": {"bytes_per_launch": 8 * 7.440929e+08, "sources": ["expert_gemm_layers_gb300/csrc/dg_gemm.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh", "expert_gemm_layers_gb300/csrc/dg_gemm_bf16_mm_store.cu", "expert_gemm_layers_gb300/csrc/dg_api.cu"], "sha256": "53055a267e1afe8abbf59d99048ba8b65a9a3bacc8e69fb656cadaadec1acaab"},
+    "ffn_bwd_dbout": {"bytes_per_launch": 8 * 8.390656e+07, "sources": ["expert_gemm_layers_gb300/csrc/dg_rowops.cu", "expert_gemm_layers_gb300/csrc/dg_gate.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh"], "sha256": "11cc40550008b41dcf95458ed76c0e31aa48bd4716d58882e0e1f39376e83dbe"},
+    "ffn_bwd_ln_rowsum": {"bytes_per_launch": 8 * 1.512175e+09, "sources": ["expert_gemm_layers_gb300/csrc/dg_rowops.cu", "expert_gemm_layers_gb300/csrc/dg_gate.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh"], "sha256": "11cc40550008b41dcf95458ed76c0e31aa48bd4716d58882e0e1f39376e83dbe"},
+    "ffn_bwd_ln_apply": {"bytes_per_launch": 8 * 2.525985e+09, "sources": ["expert_gemm_layers_gb300/csrc/dg_rowops.cu", "expert_gemm_layers_gb300/csrc/dg_gate.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh"], "sha256": "11cc40550008b41dcf95458ed76c0e31aa48bd4716d58882e0e1f39376e83dbe"},
+    "ffn_bwd_grad_reduce": {"bytes_per_launch": 8 * 4.722842e+07, "sources": ["expert_gemm_layers_gb300/csrc/dg_rowops.cu", "expert_gemm_layers_gb300/csrc/dg_gate.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh"], "sha256": "11cc40550008b41dcf95458ed76c0e31aa48bd4716d58882e0e1f39376e83dbe"},
+    "ffn_bwd_dx": {"bytes_per_launch": 8 * 1.930475e+09, "sources": ["expert_gemm_layers_gb300/csrc/dg_gemm.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh", "expert_gemm_layers_gb300/csrc/dg_gemm_bf16_kk_store.cu", "expert_gemm_layers_gb300/csrc/dg_api.cu"], "sha256": "25eb58162d935448137220d78d25e63b37fc905fdcb956c46c30a89007734750"},
+    "ffn_bwd_dw1": {"bytes_per_launch": 8 * 1.409192e+09, "sources": ["expert_gemm_layers_gb300/csrc/dg_gemm.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh", "expert_gemm_layers_gb300/csrc/dg_gemm_bf16_mm_store.cu", "expert_gemm_layers_gb300/csrc/dg_api.cu"], "sha256": "53055a267e1afe8abbf59d99048ba8b65a9a3bacc8e69fb656cadaadec1acaab"},
 }
 
 
