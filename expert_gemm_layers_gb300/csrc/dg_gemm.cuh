@@ -549,6 +549,23 @@ __global__ void __launch_bounds__(GemmCfg<kFp8, kAMN, kBMN, kEpi, kPair, kBN>::N
       tphase ^= 1u << acc;
       tc_fence_after_sync();
 
+      // The accumulator goes back to the MMA warp as soon as this warp's last
+      // TMEM load of the tile has completed (the rest of the tile's epilogue
+      // works from registers and shared memory).
+      bool released = false;
+      auto release_acc = [&]() {
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) {
+          if (kPair)
+            mbar_arrive_cluster(mapa_shared(smem_u32(&tempty[acc]), 0));
+          else
+            mbar_arrive(&tempty[acc]);
+        }
+        released = true;
+      };
+      const bool last_ld_in_loop = !Cfg::HALF_CHUNK || !(row0 < p.M && n0 + Cfg::BN_OUT - 32 < p.N);
+
       MeanM2 st_u{0.0f, 0.0f, 0.0f}, st_g{0.0f, 0.0f, 0.0f};
       for (int j = 0; j < nchunks; ++j) {
         const int buf = static_cast<int>((chunk_ctr + j) & 1u);
@@ -563,6 +580,7 @@ __global__ void __launch_bounds__(GemmCfg<kFp8, kAMN, kBMN, kEpi, kPair, kBN>::N
             tmem_ld_32x32b_x32(lane_addr + col, ra);
             tmem_ld_32x32b_x32(lane_addr + col + Cfg::BN / 2, rb);
             tmem_ld_wait();
+            if (h == 1 && j + 1 == nchunks && last_ld_in_loop) release_acc();
 #pragma unroll
             for (int i = 0; i < 32; ++i)
               v[32 * h + i] = silu_f(__uint_as_float(ra[i])) * __uint_as_float(rb[i]);
@@ -573,6 +591,7 @@ __global__ void __launch_bounds__(GemmCfg<kFp8, kAMN, kBMN, kEpi, kPair, kBN>::N
           tmem_ld_32x32b_x32(lane_addr + col, r0);
           tmem_ld_32x32b_x32(lane_addr + col + 32, r1);
           tmem_ld_wait();
+          if (j + 1 == nchunks && last_ld_in_loop) release_acc();
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
             v[i] = __uint_as_float(r0[i]);
@@ -709,6 +728,7 @@ __global__ void __launch_bounds__(GemmCfg<kFp8, kAMN, kBMN, kEpi, kPair, kBN>::N
           uint32_t r0[32];
           tmem_ld_32x32b_x32(lane_addr + static_cast<uint32_t>(acc * Cfg::ACC_STRIDE + Cfg::BN_OUT - 32), r0);
           tmem_ld_wait();
+          release_acc();
           const int row = row0 + lane;
           if (row < p.M) {
             const int64_t off = (static_cast<int64_t>(g) * p.M + row) * p.N + c0;
@@ -745,14 +765,7 @@ __global__ void __launch_bounds__(GemmCfg<kFp8, kAMN, kBMN, kEpi, kPair, kBN>::N
         publish_params(nxt, pb ^ 1);
         prm = nxt;
       }
-      tc_fence_before_sync();
-      __syncwarp();
-      if (lane == 0) {
-        if (kPair)
-          mbar_arrive_cluster(mapa_shared(smem_u32(&tempty[acc]), 0));
-        else
-          mbar_arrive(&tempty[acc]);
-      }
+      if (!released) release_acc();
     }
     // Outstanding copies of this warp must finish before the CTA exits.
     if (lane == 0) bulk_wait_group<0>();
