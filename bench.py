@@ -48,18 +48,18 @@ FALLBACK_PEAKS = dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=
 # sources changed since reports null.  Capture summary:
 # profiles/ffn_layer_kernels_traffic_T8.md.
 TRAFFIC = {
-    "ffn_gemm1": {"bytes_per_launch": 8 * 1.386331e+09, "sources": ["expert_gemm_layers_gb300/csrc/dg_gemm.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh", "expert_gemm_layers_gb300/csrc/dg_gemm_bf16_km_lnstats.cu", "expert_gemm_layers_gb300/csrc/dg_api.cu"], "sha256": "9a8d652b487a6045c7a01af36f6aad7f2b3fdd8afb7c475083de1fcdd13039ba"},
-    "ffn_ln_stats": {"bytes_per_launch": 8 * 3.147341e+07, "sources": ["expert_gemm_layers_gb300/csrc/dg_rowops.cu", "expert_gemm_layers_gb300/csrc/dg_gate.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh"], "sha256": "11cc40550008b41dcf95458ed76c0e31aa48bd4716d58882e0e1f39376e83dbe"},
-    "ffn_ln_gate_fwd": {"bytes_per_launch": 8 * 1.470191e+09, "sources": ["expert_gemm_layers_gb300/csrc/dg_rowops.cu", "expert_gemm_layers_gb300/csrc/dg_gate.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh"], "sha256": "11cc40550008b41dcf95458ed76c0e31aa48bd4716d58882e0e1f39376e83dbe"},
-    "ffn_gemm2": {"bytes_per_launch": 8 * 9.025352e+08, "sources": ["expert_gemm_layers_gb300/csrc/dg_gemm.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh", "expert_gemm_layers_gb300/csrc/dg_gemm_bf16_km_bias.cu", "expert_gemm_layers_gb300/csrc/dg_api.cu"], "sha256": "b8c6368e8b96cd576fbe627a8a6e840d66f81aaf8ac5654d34f3f1d4215a570e"},
-    "ffn_bwd_dhl": {"bytes_per_launch": 8 * 6.895360e+08, "sources": ["expert_gemm_layers_gb300/csrc/dg_gemm.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh", "expert_gemm_layers_gb300/csrc/dg_gemm_bf16_kk_store.cu", "expert_gemm_layers_gb300/csrc/dg_api.cu"], "sha256": "25eb58162d935448137220d78d25e63b37fc905fdcb956c46c30a89007734750"},
-    "ffn_bwd_dwout": {"bytes_per_launch": 8 * 7.440929e+08, "sources": ["expert_gemm_layers_gb300/csrc/dg_gemm.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh", "expert_gemm_layers_gb300/csrc/dg_gemm_bf16_mm_store.cu", "expert_gemm_layers_gb300/csrc/dg_api.cu"], "sha256": "53055a267e1afe8abbf59d99048ba8b65a9a3bacc8e69fb656cadaadec1acaab"},
-    "ffn_bwd_dbout": {"bytes_per_launch": 8 * 8.390656e+07, "sources": ["expert_gemm_layers_gb300/csrc/dg_rowops.cu", "expert_gemm_layers_gb300/csrc/dg_gate.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh"], "sha256": "11cc40550008b41dcf95458ed76c0e31aa48bd4716d58882e0e1f39376e83dbe"},
-    "ffn_bwd_ln_rowsum": {"bytes_per_launch": 8 * 1.512175e+09, "sources": ["expert_gemm_layers_gb300/csrc/dg_rowops.cu", "expert_gemm_layers_gb300/csrc/dg_gate.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh"], "sha256": "11cc40550008b41dcf95458ed76c0e31aa48bd4716d58882e0e1f39376e83dbe"},
-    "ffn_bwd_ln_apply": {"bytes_per_launch": 8 * 2.525985e+09, "sources": ["expert_gemm_layers_gb300/csrc/dg_rowops.cu", "expert_gemm_layers_gb300/csrc/dg_gate.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh"], "sha256": "11cc40550008b41dcf95458ed76c0e31aa48bd4716d58882e0e1f39376e83dbe"},
+    "ffn_gemm1": {"bytes_per_launch": 8 * 1.385788e+09, "sources": ["expert_gemm_layers_gb300/csrc/dg_gemm.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh", "expert_gemm_layers_gb300/csrc/dg_gemm_bf16_km_lnstats.cu", "expert_gemm_layers_gb300/csrc/dg_api.cu"], "sha256": "f820ee9c205118e5c77c4348a05dbafa5c20e656b6cb35d63f98a50b4a033570"},
+    "ffn_ln_stats": {"bytes_per_launch": 8 * 3.147264e+07, "sources": ["expert_gemm_layers_gb300/csrc/dg_rowops.cu", "expert_gemm_layers_gb300/csrc/dg_gate.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh"], "sha256": "11cc40550008b41dcf95458ed76c0e31aa48bd4716d58882e0e1f39376e83dbe"},
+    "ffn_ln_gate_fwd": {"bytes_per_launch": 8 * 1.468731e+09, "sources": ["expert_gemm_layers_gb300/csrc/dg_rowops.cu", "expert_gemm_layers_gb300/csrc/dg_gate.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh"], "sha256": "11cc40550008b41dcf95458ed76c0e31aa48bd4716d58882e0e1f39376e83dbe"},
+    "ffn_gemm2": {"bytes_per_launch": 8 * 9.025536e+08, "sources": ["expert_gemm_layers_gb300/csrc/dg_gemm.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh", "expert_gemm_layers_gb300/csrc/dg_gemm_bf16_km_bias.cu", "expert_gemm_layers_gb300/csrc/dg_api.cu"], "sha256": "3165c0331fcdc3e20a96895c2c45caa6468692bb0ce06a00f8f24a294681a465"},
+    "ffn_bwd_dhl": {"bytes_per_launch": 8 * 6.893960e+08, "sources": ["expert_gemm_layers_gb300/csrc/dg_gemm.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh", "expert_gemm_layers_gb300/csrc/dg_gemm_bf16_kk_store.cu", "expert_gemm_layers_gb300/csrc/dg_api.cu"], "sha256": "9b9a38ce6844d6316d1cefa105634b841688cf0a84f08d23aa03320cd33ef1d7"},
+    "ffn_bwd_dwout": {"bytes_per_launch": 8 * 7.516895e+08, "sources": ["expert_gemm_layers_gb300/csrc/dg_gemm.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh", "expert_gemm_layers_gb300/csrc/dg_gemm_bf16_mm_store.cu", "expert_gemm_layers_gb300/csrc/dg_api.cu"], "sha256": "4bccd4e11fb08277b811d3fc4d118c999b819cba2a43a0404720b47d6656e8a1"},
+    "ffn_bwd_dbout": {"bytes_per_launch": 8 * 8.403840e+07, "sources": ["expert_gemm_layers_gb300/csrc/dg_rowops.cu", "expert_gemm_layers_gb300/csrc/dg_gate.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh"], "sha256": "11cc40550008b41dcf95458ed76c0e31aa48bd4716d58882e0e1f39376e83dbe"},
+    "ffn_bwd_ln_rowsum": {"bytes_per_launch": 8 * 1.512215e+09, "sources": ["expert_gemm_layers_gb300/csrc/dg_rowops.cu", "expert_gemm_layers_gb300/csrc/dg_gate.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh"], "sha256": "11cc40550008b41dcf95458ed76c0e31aa48bd4716d58882e0e1f39376e83dbe"},
+    "ffn_bwd_ln_apply": {"bytes_per_launch": 8 * 2.526112e+09, "sources": ["expert_gemm_layers_gb300/csrc/dg_rowops.cu", "expert_gemm_layers_gb300/csrc/dg_gate.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh"], "sha256": "11cc40550008b41dcf95458ed76c0e31aa48bd4716d58882e0e1f39376e83dbe"},
     "ffn_bwd_grad_reduce": {"bytes_per_launch": 8 * 4.722842e+07, "sources": ["expert_gemm_layers_gb300/csrc/dg_rowops.cu", "expert_gemm_layers_gb300/csrc/dg_gate.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh"], "sha256": "11cc40550008b41dcf95458ed76c0e31aa48bd4716d58882e0e1f39376e83dbe"},
-    "ffn_bwd_dx": {"bytes_per_launch": 8 * 1.930475e+09, "sources": ["expert_gemm_layers_gb300/csrc/dg_gemm.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh", "expert_gemm_layers_gb300/csrc/dg_gemm_bf16_kk_store.cu", "expert_gemm_layers_gb300/csrc/dg_api.cu"], "sha256": "25eb58162d935448137220d78d25e63b37fc905fdcb956c46c30a89007734750"},
-    "ffn_bwd_dw1": {"bytes_per_launch": 8 * 1.409192e+09, "sources": ["expert_gemm_layers_gb300/csrc/dg_gemm.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh", "expert_gemm_layers_gb300/csrc/dg_gemm_bf16_mm_store.cu", "expert_gemm_layers_gb300/csrc/dg_api.cu"], "sha256": "53055a267e1afe8abbf59d99048ba8b65a9a3bacc8e69fb656cadaadec1acaab"},
+    "ffn_bwd_dx": {"bytes_per_launch": 8 * 1.775118e+09, "sources": ["expert_gemm_layers_gb300/csrc/dg_gemm.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh", "expert_gemm_layers_gb300/csrc/dg_gemm_bf16_kk_store.cu", "expert_gemm_layers_gb300/csrc/dg_api.cu"], "sha256": "9b9a38ce6844d6316d1cefa105634b841688cf0a84f08d23aa03320cd33ef1d7"},
+    "ffn_bwd_dw1": {"bytes_per_launch": 8 * 1.426813e+09, "sources": ["expert_gemm_layers_gb300/csrc/dg_gemm.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh", "expert_gemm_layers_gb300/csrc/dg_gemm_bf16_mm_store.cu", "expert_gemm_layers_gb300/csrc/dg_api.cu"], "sha256": "4bccd4e11fb08277b811d3fc4d118c999b819cba2a43a0404720b47d6656e8a1"},
 }
 
 
