@@ -439,6 +439,7 @@ def run_dg(args, rank, world):
     if st != 0:
         raise RuntimeError(f"device error word after the timed steps: {code:#x}")
 
+    step_ms = [starts[i].elapsed_time(ends[i]) for i in range(args.steps)]
     part_ms = {"fp8_gemm": [], "ffn_fwd": [], "ffn_bwd": [], "tp_swiglu": []}
     for i in range(args.steps):
         m = marks[i]
@@ -453,8 +454,8 @@ def run_dg(args, rank, world):
         pm = statistics.mean(vals)
         tf = flops[name] / (pm * 1e-3) / 1e12
         peak = (2.0 * peaks["bf16_tflops"]) if name == "fp8_gemm" else peaks["bf16_tflops"]
-        parts[name] = {"ms": round(pm, 4), "tflops": round(tf, 2), "peak_tflops": peak,
-                       "frac_of_peak": round(tf / peak, 4)}
+        parts[name] = {"ms": round(pm, 4), "ms_min": round(min(vals), 4), "ms_max": round(max(vals), 4),
+                       "tflops": round(tf, 2), "peak_tflops": peak, "frac_of_peak": round(tf / peak, 4)}
     parts["fp8_gemm"]["peak_note"] = "2 x measured bf16 burst (nominal fp8:bf16 ratio 2)"
 
     # roofline of the dominant kernel (largest share of device time in the traced steps)
@@ -496,7 +497,9 @@ def run_dg(args, rank, world):
     line = {
         "metric": "hot-path GEMM TFLOP/s (FP8 GEMM + A2A FFN fwd+bwd + TP SwiGLU)",
         "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
+        "warmup": args.warmup, "ms_per_step": round(ms, 4),
+        "ms_per_step_min": round(min(step_ms), 4), "ms_per_step_max": round(max(step_ms), 4),
+        "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16+e4m3 (fp32 accumulate)", "data": "synthetic",
         "config": workload_config(), "parts": parts, "roofline": roof, "kernels": kernel_table,
         "gpu_launches": launches, "e2e": e2e, "clocks": clk, "outside_step": extra,
