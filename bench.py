@@ -45,8 +45,8 @@ FALLBACK_PEAKS = dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=
 # eighth of the benchmark's problems; traffic grows in proportion, so it is
 # scaled by 8), with the sha256 of the kernel's sources (for a GEMM also the
 # launch code, which picks its tile order) at capture time; a kernel whose
-# sources changed since reports null.  Capture summary:
-# profiles/ffn_layer_kernels_traffic_T8.md.
+# sources changed since reports null.  The capture's summary is committed with
+# the other ncu summaries of this repository.
 TRAFFIC = {
     "ffn_gemm1": {"bytes_per_launch": 8 * 1.385788e+09, "sources": ["expert_gemm_layers_gb300/csrc/dg_gemm.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh", "expert_gemm_layers_gb300/csrc/dg_gemm_bf16_km_lnstats.cu", "expert_gemm_layers_gb300/csrc/dg_api.cu"], "sha256": "f820ee9c205118e5c77c4348a05dbafa5c20e656b6cb35d63f98a50b4a033570"},
     "ffn_ln_stats": {"bytes_per_launch": 8 * 3.147264e+07, "sources": ["expert_gemm_layers_gb300/csrc/dg_rowops.cu", "expert_gemm_layers_gb300/csrc/dg_gate.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh"], "sha256": "11cc40550008b41dcf95458ed76c0e31aa48bd4716d58882e0e1f39376e83dbe"},
@@ -187,19 +187,19 @@ class Workload:
         lib = dg._lib.load()
         import ctypes
         self.saved = torch.empty(lib.dg_a2a_ffn_saved_bytes(ctypes.byref(sh)), dtype=torch.uint8, device=dev)
-        self.ws = torch.empty(lib.dg_a2a_ffn_bwd_workspace_bytes(ctypes.byref(sh)), dtype=torch.uint8, device=dev)
+        self.ws = dg.alloc_workspace(lib.dg_a2a_ffn_bwd_workspace_bytes(ctypes.byref(sh), 0), dev)
         self.grads = {n: torch.empty_like(v) for n, v in self.params.items()}
         self.grads["inputs"] = torch.empty_like(self.x)
         self.xs, self.w13, self.w2 = synth.tp_swiglu_inputs(TP["S"], TP["d"], TP["ffn"], TP["W"], seed=TP["seed"],
                                                             device=dev)
         self.y = torch.empty_like(self.xs)
-        self.tp_ws = torch.empty(lib.dg_tp_swiglu_workspace_bytes(TP["S"], TP["d"], TP["ffn"], TP["W"], 1),
-                                 dtype=torch.uint8, device=dev)
+        self.tp_ws = dg.alloc_workspace(lib.dg_tp_swiglu_workspace_bytes(TP["S"], TP["d"], TP["ffn"], TP["W"], 1),
+                                        dev)
         # the TP SwiGLU backward, timed on its own after the step
         self.tp_dy = synth.tp_swiglu_inputs(TP["S"], TP["d"], TP["ffn"], TP["W"], seed=TP["seed"] + 1,
                                             device=dev)[0]
-        self.tp_bws = torch.empty(lib.dg_tp_swiglu_bwd_workspace_bytes(TP["S"], TP["d"], TP["ffn"], TP["W"], 1),
-                                  dtype=torch.uint8, device=dev)
+        self.tp_bws = dg.alloc_workspace(
+            lib.dg_tp_swiglu_bwd_workspace_bytes(TP["S"], TP["d"], TP["ffn"], TP["W"], 1), dev)
         self.tp_grads = dict(x=torch.empty_like(self.xs), w13=torch.empty_like(self.w13), w2=torch.empty_like(self.w2))
         # attention projections at the same Llama-3-8B shape (32 query / 8 key-value heads of 128), no bias
         S, W, d = TP["S"], TP["W"], TP["d"]
@@ -212,6 +212,14 @@ class Workload:
         self.attn_y = torch.empty((W, 1, S // W, d), dtype=bf, device=dev)
         self.dqkv = torch.randn_like(self.qkv, dtype=torch.float32).to(bf)
         self.dattn_y = torch.randn_like(self.attn_y, dtype=torch.float32).to(bf)
+
+    def status(self):
+        """Reads and clears the error word of every workspace the step uses: (status, raw code)."""
+        for ws in (None, self.ws, self.tp_ws, self.tp_bws):
+            st, code = self.dg.device_status(self.dev, workspace=ws)
+            if st != 0:
+                return st, code
+        return 0, 0
 
     def step(self, marks=None):
         dg = self.dg
@@ -259,9 +267,13 @@ class Workload:
 class OracleSample:
     """A bounded sample of the same workload run by the CPU oracle (fp64 numpy).
 
-    Per step: 64 rows of the FP8 GEMM, 32 seeded output rows of the FFN
-    forward, 16 seeded rows of d_inputs, 8 rows of the TP SwiGLU output.
-    Its FLOPs are the GEMM FLOPs of exactly those rows.
+    Per step: rows 0-255 of the FP8 GEMM; 256 FFN output rows, 64 from each of
+    4 seeded token positions; 64 rows of d_inputs, 32 from each of 2 seeded
+    token positions; 32 seeded rows of the TP SwiGLU output.  Its FLOPs are the
+    GEMM FLOPs of exactly those rows.  The oracle decodes the weights of every
+    problem it touches once per call, so the rows are grouped into few
+    problems to keep that decode a small part of the sample; decode_seconds()
+    times those decodes alone.
     """
 
     def __init__(self, host):
@@ -270,18 +282,22 @@ class OracleSample:
         self.h = host
         rng = np.random.default_rng(0)
         P, B, T, D, k = FFN["P"], FFN["B"], FFN["T"], FFN["D"], FFN["k"]
+        M = P * B
         self.sh = O.FFNShape(P, B, T, D, k)
-        self.fp8_rows = np.arange(64)
-        self.ffn_rows = rng.choice(P * B * T, size=32, replace=False)
-        self.dx_rows = rng.choice(P * B * T, size=16, replace=False)
-        self.tp_rows = rng.choice(TP["S"], size=8, replace=False)
+        self.fp8_rows = np.arange(256)
+        self.ffn_t = rng.choice(T, size=4, replace=False)
+        self.ffn_rows = np.concatenate([rng.choice(M, size=64, replace=False) * T + t for t in self.ffn_t])
+        self.dx_t = rng.choice(T, size=2, replace=False)
+        self.dx_rows = np.concatenate([rng.choice(M, size=32, replace=False) * T + t for t in self.dx_t])
+        self.tp_rows = rng.choice(TP["S"], size=32, replace=False)
         H = D * k
         row_fwd = 2.0 * D * 2 * H + 2.0 * H * D
         self.flops = (2.0 * len(self.fp8_rows) * FP8["N"] * FP8["K"] + len(self.ffn_rows) * row_fwd
                       + len(self.dx_rows) * (row_fwd + 2.0 * H * D + 2.0 * 2 * H * D)
                       + len(self.tp_rows) * (2.0 * TP["d"] * 2 * TP["ffn"] + 2.0 * TP["ffn"] * TP["d"]))
-        self.desc = ("per step: FP8 GEMM rows 0-63 of 4096; 32 seeded FFN output rows; 16 seeded d_inputs rows; "
-                     "8 seeded TP SwiGLU rows (GEMM FLOPs of those rows only)")
+        self.desc = ("per step: FP8 GEMM rows 0-255 of 4096; 256 FFN output rows (64 from each of 4 seeded token "
+                     "positions); 64 d_inputs rows (32 from each of 2 seeded token positions); 32 seeded TP SwiGLU "
+                     "rows (GEMM FLOPs of those rows only)")
 
     def step(self):
         O, h = self.O, self.h
@@ -289,6 +305,22 @@ class OracleSample:
         O.ffn_forward_rows(self.sh, h["inputs"], h, self.ffn_rows)
         O.ffn_backward_dx_rows(self.sh, h["inputs"], h, h["dY"], self.dx_rows)
         O.tp_swiglu_rows(h["xs"], h["w13"], h["w2"], TP["W"], self.tp_rows)
+
+    def decode_seconds(self):
+        """Time of the exact decodes of the operands one step touches (part of step())."""
+        O, h = self.O, self.h
+        sh = self.sh
+        P, L, D, H = sh.P, sh.L, sh.D, sh.H
+        t0 = time.perf_counter()
+        O.e4m3_to_f64(h["B"])
+        O.e4m3_to_f64(np.asarray(h["A"]).reshape(FP8["M"], FP8["K"])[self.fp8_rows])
+        for t in list(self.ffn_t) + list(self.dx_t):
+            r, l = divmod(int(t), L)
+            O.bf16_to_f64(np.asarray(h["w1"]).reshape(P, L, D, 2 * H)[r, l])
+            O.bf16_to_f64(np.asarray(h["wout"]).reshape(P, L, H, D)[r, l])
+        O.bf16_to_f64(h["w13"])
+        O.bf16_to_f64(h["w2"])
+        return time.perf_counter() - t0
 
 
 def host_bits(w):
@@ -395,7 +427,7 @@ def run_dg(args, rank, world):
     for _ in range(args.warmup):
         w.step()
     torch.cuda.synchronize(dev)
-    st, code = dg.device_status(dev)
+    st, code = w.status()
     if st != 0:
         raise RuntimeError(f"device error word after warm-up: {code:#x}")
 
@@ -435,7 +467,7 @@ def run_dg(args, rank, world):
     clk = clocks.stop()
     barrier()
     ms = max_over_ranks(t_start.elapsed_time(t_end) / args.steps, world, dev)
-    st, code = dg.device_status(dev)
+    st, code = w.status()
     if st != 0:
         raise RuntimeError(f"device error word after the timed steps: {code:#x}")
 
@@ -475,7 +507,7 @@ def run_dg(args, rank, world):
     roof["peak_source"] = peaks["source"] + (" sustained bf16" if top["flops"] > 0 else " HBM copy")
     roof["traffic"] = traffic_for(top["name"])
     if roof["traffic"] is not None:
-        roof["traffic_source"] = "ncu dram__bytes_read+write at T=8 token positions, x8 (profiles/ffn_layer_kernels_traffic_T8.md)"
+        roof["traffic_source"] = "ncu dram__bytes_read+write of the kernel at T=8 token positions, scaled x8"
     roof["launches_timed"] = top["launches"]
     total_ms = sum(e["total_ms"] for e in table)
     kernel_table = {e["name"]: {"launches_per_step": e["launches"] // 2,
@@ -489,6 +521,8 @@ def run_dg(args, rank, world):
     extra.update(run_tp_backward(w, args, dev, peaks))
     extra.update(run_attn_proj(w, args, dev, peaks))
     extra.update(run_ffn_fp8(w, args, dev, peaks))
+    extra.update(run_ffn_forward_variants(w, args, dev, peaks))
+    extra.update(run_tiny_latency(args, dev))
 
     # end to end: inputs from pinned host memory in, results back to pinned host memory
     e2e = run_e2e(w, args, dev, step_flops, world)
@@ -501,15 +535,18 @@ def run_dg(args, rank, world):
         "ms_per_step_min": round(min(step_ms), 4), "ms_per_step_max": round(max(step_ms), 4),
         "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16+e4m3 (fp32 accumulate)", "data": "synthetic",
-        "config": workload_config(), "parts": parts, "roofline": roof, "kernels": kernel_table,
+        "config": workload_config(), "parts": dict(parts, ffn_tiny_latency=extra["ffn_tiny_latency"]),
+        "roofline": roof, "kernels": kernel_table,
         "gpu_launches": launches, "e2e": e2e, "clocks": clk, "outside_step": extra,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         sample = OracleSample(host_bits(w))
         sec = time_oracle(sample, 1)
+        dec = sample.decode_seconds()
         line["cpu_baseline"] = {"value": round(sample.flops / sec / 1e12, 6), "unit": "TFLOP/s",
                                 "cores": oracle_threads(), "kind": "oracle", "sample": sample.desc,
-                                "seconds": round(sec, 2)}
+                                "seconds": round(sec, 2), "decode_seconds": round(dec, 2),
+                                "arith_tflops": round(sample.flops / max(sec - dec, 1e-9) / 1e12, 6)}
     if rank == 0:
         print(json.dumps(line), flush=True)
 
@@ -536,7 +573,7 @@ def run_fp8_alone(w, args, dev, peaks):
         e1.record(stream)
     torch.cuda.synchronize(dev)
     del flush_sum
-    st, code = dg.device_status(dev)
+    st, code = w.status()
     if st != 0:
         raise RuntimeError(f"device error word after the FP8 GEMM: {code:#x}")
     ms = sorted(e0.elapsed_time(e1) for e0, e1 in ev)
@@ -569,7 +606,7 @@ def run_tp_backward(w, args, dev, peaks):
     ev[1].record(stream)
     torch.cuda.synchronize(dev)
     trace = dg.trace_end()
-    st, code = dg.device_status(dev)
+    st, code = w.status()
     if st != 0:
         raise RuntimeError(f"device error word after the TP backward: {code:#x}")
     ms = ev[0].elapsed_time(ev[1]) / iters
@@ -593,8 +630,8 @@ def run_ffn_fp8(w, args, dev, peaks):
     out = torch.empty_like(w.out)
     lib = dg._lib.load()
     import ctypes
-    ws = torch.empty(lib.dg_a2a_ffn_fp8_workspace_bytes(ctypes.byref(dg.ffn_shape(P, B, T, D, FFN["k"]))),
-                     dtype=torch.uint8, device=dev)
+    ws = dg.alloc_workspace(lib.dg_a2a_ffn_fp8_workspace_bytes(ctypes.byref(dg.ffn_shape(P, B, T, D, FFN["k"]))),
+                            dev)
     run = lambda: dg.a2a_ffn_forward_fp8(w.x, w.params, packed, workspace=ws, out=out)
     for _ in range(max(args.warmup, 2)):
         run()
@@ -609,7 +646,7 @@ def run_ffn_fp8(w, args, dev, peaks):
     ev[1].record(stream)
     torch.cuda.synchronize(dev)
     trace = dg.trace_end()
-    st, code = dg.device_status(dev)
+    st, code = dg.device_status(dev, workspace=ws)
     if st != 0:
         raise RuntimeError(f"device error word after the FP8 FFN forward: {code:#x}")
     ms = ev[0].elapsed_time(ev[1]) / iters
@@ -621,6 +658,113 @@ def run_ffn_fp8(w, args, dev, peaks):
         "peak_note": "2 x measured bf16 burst (nominal fp8:bf16 ratio 2)", "iters": iters,
         "kernels": {e["name"]: {"launches": e["launches"], "ms_per_launch": round(e["total_ms"] / e["launches"], 4)}
                     for e in trace}}}
+
+
+def _timed(run, iters, dev):
+    """Mean device time (ms) of `iters` back-to-back calls, and the kernel table of those calls."""
+    import torch
+    from expert_gemm_layers_gb300 import trace_begin, trace_end
+    stream = torch.cuda.current_stream(dev)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    torch.cuda.synchronize(dev)
+    ev[0].record(stream)
+    for _ in range(iters):
+        run()
+    ev[1].record(stream)
+    torch.cuda.synchronize(dev)
+    ms = ev[0].elapsed_time(ev[1]) / iters
+    trace_begin()
+    run()
+    torch.cuda.synchronize(dev)
+    table = trace_end()
+    return ms, {e["name"]: round(e["total_ms"] / e["launches"], 4) for e in table}
+
+
+def run_ffn_forward_variants(w, args, dev, peaks):
+    """The FFN forward at the step's shape in four forms, timed alone (outside
+    the step, same box and run): training with the separate normalise-and-gate
+    pass (the default, as in the step) and with the normalise-and-gate computed
+    by the second GEMM's producer warps; inference (nothing saved) in both
+    forms, the fused one without Hl scratch."""
+    import ctypes
+    dg = w.dg
+    lib = dg._lib.load()
+    sh = dg.ffn_shape(FFN["P"], FFN["B"], FFN["T"], FFN["D"], FFN["k"])
+    ws_inf = dg.alloc_workspace(lib.dg_a2a_ffn_fwd_workspace_bytes(ctypes.byref(sh), 1, 0), dev)
+    ws_inf_fused = dg.alloc_workspace(lib.dg_a2a_ffn_fwd_workspace_bytes(ctypes.byref(sh), 1, dg.DG_FFN_FUSED_GATE),
+                                      dev)
+    variants = {
+        "separate_gate": lambda: dg.a2a_ffn_forward(w.x, w.params, saved=w.saved, out=w.out),
+        "fused_gate": lambda: dg.a2a_ffn_forward(w.x, w.params, saved=w.saved, out=w.out,
+                                                 flags=dg.DG_FFN_FUSED_GATE),
+        "inference": lambda: dg.a2a_ffn_forward(w.x, w.params, out=w.out, inference=True, ws=ws_inf),
+        "inference_fused_gate": lambda: dg.a2a_ffn_forward(w.x, w.params, out=w.out, inference=True, ws=ws_inf_fused,
+                                                           flags=dg.DG_FFN_FUSED_GATE),
+    }
+    flops = gemm_flops()["ffn_fwd"]
+    res = {}
+    for _ in range(2):                                    # two rounds, alternating the variants
+        for name, run in variants.items():
+            run()
+            ms, kernels = _timed(run, 5, dev)
+            tf = flops / (ms * 1e-3) / 1e12
+            prev = res.get(name)
+            if prev is None or ms < prev["ms"]:
+                res[name] = {"ms": round(ms, 4), "tflops": round(tf, 2), "peak_tflops": peaks["bf16_tflops"],
+                             "frac_of_peak": round(tf / peaks["bf16_tflops"], 4), "kernels_ms": kernels}
+    for wsx in (ws_inf, ws_inf_fused):
+        st, code = dg.device_status(dev, workspace=wsx)
+        if st != 0:
+            raise RuntimeError(f"device error word after the FFN forward variants: {code:#x}")
+    st, code = w.status()
+    if st != 0:
+        raise RuntimeError(f"device error word after the FFN forward variants: {code:#x}")
+    del ws_inf, ws_inf_fused
+    return {"ffn_fwd_variants": dict(res, note="best of two rounds of 5 back-to-back calls each")}
+
+
+def run_tiny_latency(args, dev):
+    """Latency of the tiny A2A FFN workload (P=2, B=4, T=16, D=128, k=2, seed 42):
+    device time of each forward and each forward + backward call, in microseconds."""
+    import torch
+
+    import expert_gemm_layers_gb300 as dg
+    from expert_gemm_layers_gb300 import synth
+    t = synth.ffn_inputs(2, 4, 16, 128, 2, seed=42, device=dev)
+    params = {n: t[n] for n in dg.FFN_PARAM_NAMES}
+    x = t["inputs"]
+    dY = synth.ffn_grad_output(2, 4, 16, 128, seed=43, device=dev)
+    import ctypes
+    lib = dg._lib.load()
+    sh = dg.ffn_shape(2, 4, 16, 128, 2)
+    saved = torch.empty(lib.dg_a2a_ffn_saved_bytes(ctypes.byref(sh)), dtype=torch.uint8, device=dev)
+    ws = dg.alloc_workspace(lib.dg_a2a_ffn_bwd_workspace_bytes(ctypes.byref(sh), 0), dev)
+    out = torch.empty_like(x)
+    grads = {n: torch.empty_like(v) for n, v in params.items()}
+    grads["inputs"] = torch.empty_like(x)
+    stream = torch.cuda.current_stream(dev)
+    iters = 100
+    res = {}
+    for name, with_bwd in (("forward", False), ("forward_backward", True)):
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(iters)]
+        for i in range(iters + 10):
+            if i >= 10:
+                ev[i - 10][0].record(stream)
+            dg.a2a_ffn_forward(x, params, saved=saved, out=out)
+            if with_bwd:
+                dg.a2a_ffn_backward(x, params, saved, dY, workspace=ws, grads=grads)
+            if i >= 10:
+                ev[i - 10][1].record(stream)
+        torch.cuda.synchronize(dev)
+        us = [1e3 * a.elapsed_time(b) for a, b in ev]
+        res[name] = {"us_mean": round(statistics.mean(us), 2), "us_min": round(min(us), 2),
+                     "us_max": round(max(us), 2), "iters": iters}
+    for wsx in (None, ws):
+        st, code = dg.device_status(dev, workspace=wsx)
+        if st != 0:
+            raise RuntimeError(f"device error word after the tiny workload: {code:#x}")
+    return {"ffn_tiny_latency": dict(res, workload="A2A FFN P=2, B=4, T=16, D=128, k=2 (H=256), seed 42",
+                                     timing="CUDA events around each call, back to back, 10 untimed first")}
 
 
 def run_attn_proj(w, args, dev, peaks):
@@ -641,7 +785,7 @@ def run_attn_proj(w, args, dev, peaks):
     ev[1].record(stream)
     torch.cuda.synchronize(dev)
     trace = dg.trace_end()
-    st, code = dg.device_status(dev)
+    st, code = w.status()
     if st != 0:
         raise RuntimeError(f"device error word after the attention projections: {code:#x}")
     ms = ev[0].elapsed_time(ev[1]) / iters
@@ -763,6 +907,7 @@ def run_e2e(w, args, dev, step_flops, world):
 PROFILE_CASES = {
     "fp8": "FP8 GEMM 4096^3 (alpha 0.5, beta 1)",
     "ffn_fwd_small": "A2A FFN forward, P=8, B=512, T=8, D=1280, k=6 (the full shape with 8 token positions)",
+    "ffn_fwd_small_fused": "the same forward with the normalise-and-gate in the second GEMM's producer warps",
     "ffn_small": "A2A FFN forward + backward, P=8, B=512, T=8, D=1280, k=6",
     "tp": "TP SwiGLU, S=8192, d=4096, ffn=14336, W=8",
     "ffn_fp8_small": "A2A FFN forward on e4m3 GEMMs, P=8, B=512, T=8, D=1280, k=6",
@@ -782,14 +927,15 @@ def run_profile_case(args):
         A, B, C = synth.fp8_gemm_inputs(4096, 4096, 4096, seed=1, device=dev)
         D = torch.empty((4096, 4096), dtype=torch.bfloat16, device=dev)
         run = lambda: dg.gemm_fp8(A, B, C, 0.5, 1.0, out=D)
-    elif case in ("ffn_fwd_small", "ffn_small"):
+    elif case in ("ffn_fwd_small", "ffn_small", "ffn_fwd_small_fused"):
         t = synth.ffn_inputs(8, 512, 8, 1280, 6, seed=42, device=dev)
         params = {n: t[n] for n in dg.FFN_PARAM_NAMES}
         x = t["inputs"]
         dY = synth.ffn_grad_output(8, 512, 8, 1280, seed=43, device=dev)
+        flags = dg.DG_FFN_FUSED_GATE if case == "ffn_fwd_small_fused" else 0
 
         def run():
-            out, saved = dg.a2a_ffn_forward(x, params)
+            out, saved = dg.a2a_ffn_forward(x, params, flags=flags)
             if case == "ffn_small":
                 dg.a2a_ffn_backward(x, params, saved, dY)
     elif case == "ffn_fp8_small":

@@ -38,16 +38,23 @@ class TraceEntry(ctypes.Structure):
     _fields_ = [("name", ctypes.c_char * 40), ("launches", ctypes.c_int64), ("total_ms", ctypes.c_double),
                 ("flops", ctypes.c_double), ("bytes", ctypes.c_double)]
 
+DG_ERROR_BLOCK_BYTES = 256
+DG_FFN_COMP_ONLY = 1
+DG_FFN_FUSED_GATE = 2
+
 SIGNATURES = {
     "dg_last_error": (ctypes.c_char_p, []),
     "dg_version": (ctypes.c_char_p, []),
-    "dg_device_status": (ctypes.c_int, [_vp, ctypes.POINTER(ctypes.c_uint32)]),
-    "dg_debug_wait_timeout": (ctypes.c_int, [_u32, _vp]),
-    "dg_gemm_fp8": (ctypes.c_int, [_i64, _i64, _i64, _vp, _vp, _vp, _vp, _f32, _f32, _vp]),
+    "dg_workspace_init": (ctypes.c_int, [_vp, _sz, _vp]),
+    "dg_check_device_error": (ctypes.c_int, [_vp, _vp, ctypes.POINTER(ctypes.c_uint32)]),
+    "dg_debug_wait_timeout": (ctypes.c_int, [_vp, _sz, _u32, _vp]),
+    "dg_gemm_fp8_workspace_bytes": (_sz, [_i64, _i64, _i64]),
+    "dg_gemm_fp8": (ctypes.c_int, [_i64, _i64, _i64, _vp, _vp, _vp, _vp, _f32, _f32, _vp, _sz, _vp]),
     "dg_a2a_ffn_saved_bytes": (_sz, [_PSHAPE]),
-    "dg_a2a_ffn_fwd": (ctypes.c_int, [_PSHAPE] + [_vp] * 10 + [_vp, _sz, _vp]),
-    "dg_a2a_ffn_bwd_workspace_bytes": (_sz, [_PSHAPE]),
-    "dg_a2a_ffn_bwd": (ctypes.c_int, [_PSHAPE] + [_vp] * 9 + [_vp, _sz, _vp] + [_vp] * 9 + [_vp, _sz, _vp]),
+    "dg_a2a_ffn_fwd_workspace_bytes": (_sz, [_PSHAPE, _i32, _u32]),
+    "dg_a2a_ffn_fwd": (ctypes.c_int, [_PSHAPE] + [_vp] * 10 + [_vp, _sz, _vp, _sz, _u32, _vp]),
+    "dg_a2a_ffn_bwd_workspace_bytes": (_sz, [_PSHAPE, _u32]),
+    "dg_a2a_ffn_bwd": (ctypes.c_int, [_PSHAPE] + [_vp] * 9 + [_vp, _sz, _vp] + [_vp] * 9 + [_vp, _sz, _u32, _vp]),
     "dg_a2a_dispatch": (ctypes.c_int, [_i32, _i32, _i32, _i32, _vp, _vp, _vp]),
     "dg_a2a_combine": (ctypes.c_int, [_i32, _i32, _i32, _i32, _vp, _vp, _vp]),
     "dg_tp_swiglu_workspace_bytes": (_sz, [_i64, _i64, _i64, _i32, _i32]),
@@ -59,8 +66,9 @@ SIGNATURES = {
     "dg_a2a_ffn_fp8_workspace_bytes": (_sz, [_PSHAPE]),
     "dg_a2a_ffn_fp8_pack_weights": (ctypes.c_int, [_PSHAPE, _vp, _vp, _vp, _sz, _vp]),
     "dg_a2a_ffn_fwd_fp8": (ctypes.c_int, [_PSHAPE, _vp, _vp, _sz, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
-    "dg_tp_linear_fwd": (ctypes.c_int, [_i64, _i64, _i64, _vp, _vp, _vp, _vp, _vp]),
-    "dg_tp_linear_bwd": (ctypes.c_int, [_i64, _i64, _i64, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
+    "dg_tp_linear_workspace_bytes": (_sz, [_i64, _i64, _i64]),
+    "dg_tp_linear_fwd": (ctypes.c_int, [_i64, _i64, _i64, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
+    "dg_tp_linear_bwd": (ctypes.c_int, [_i64, _i64, _i64, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "dg_tp_swiglu_noalloc": (ctypes.c_int, [_i64, _i64, _i64, _i32, _i32, _vp, _vp, _vp, _vp, _vp]),
     "dg_trace_begin": (ctypes.c_int, []),
     "dg_trace_begin_only": (ctypes.c_int, [ctypes.c_char_p]),

@@ -16,13 +16,33 @@ namespace dg {
 // Records a thread-local message and returns `s`.
 dg_status fail(dg_status s, const char* fmt, ...);
 
-// Per-device facts, cached on first use of each device.
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// True if [a, a+na) and [b, b+nb) overlap (a NULL or empty range overlaps nothing).
+inline bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
+  if (!a || !b || na == 0 || nb == 0) return false;
+  const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+  return x < y + nb && y < x + na;
+}
+
+// Per-device facts, cached on first use of each device.  `err` is the
+// error word the kernels of one call record a failed wait in: each entry point
+// points it at the error block of its caller's workspace (device_info leaves
+// it NULL).  `builtin_err` is the library's own word, which only the call
+// that takes no workspace (dg_tp_swiglu_noalloc) uses.
 struct DeviceInfo {
   int device;
   int num_sms;
-  uint32_t* err;  // device address of this device's error word
+  uint32_t* err;
+  uint32_t* builtin_err;
 };
 dg_status device_info(DeviceInfo* out);
+
+// Checks that `ws` holds at least the error block (DG_ERROR_BLOCK_BYTES,
+// 16-byte aligned), before any device call.
+dg_status check_error_block(const void* ws, size_t ws_bytes, const char* what);
+// check_error_block, then device_info, with dev->err pointed at the first word of `ws`.
+dg_status device_info_ws(DeviceInfo* dev, void* ws, size_t ws_bytes, const char* what);
 
 // A 3-D TMA tensor map over a row-major tensor.  dims are in elements,
 // innermost first; strides (bytes) are those of dims 1 and 2; box in
@@ -30,6 +50,12 @@ dg_status device_info(DeviceInfo* out);
 dg_status make_map_3d(CUtensorMap* map, bool is_bf16, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
                       uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t b0, uint32_t b1, uint32_t b2,
                       const char* what);
+
+// make_map_3d with a 64- or 128-byte swizzle (the box's inner extent must not
+// exceed it).
+dg_status make_map_3d_sw(CUtensorMap* map, bool is_bf16, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
+                         uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t b0, uint32_t b1, uint32_t b2,
+                         int swizzle_bytes, const char* what);
 
 // The map of an MN-major GEMM operand (MN = d0, the contiguous dimension;
 // d1, d2, strides and the box's b1, b2 as for make_map_3d with b0 = 64).
@@ -61,10 +87,32 @@ int gemm_tile_n(GemmVariant v);
 int gemm_tile_m();
 
 // Enqueue one persistent GEMM launch.  `p.tiles_*` and the grid are filled in
-// here.  `name` and `bytes` (algorithmic HBM bytes) label the launch for tracing.
+// here.  `name` and `bytes` (algorithmic HBM bytes) label the launch for
+// tracing; a NULL name launches it untraced (no events are created).
 dg_status run_gemm(GemmVariant v, const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& d,
                    const CUtensorMap& c, GemmParams p, const DeviceInfo& dev, cudaStream_t s, const char* name,
                    double bytes);
+
+// The FFN's second GEMM with the normalise-and-gate folded into its A operand
+// (launch_gemm_gated), traced like run_gemm.
+struct GateSrc;
+dg_status run_gemm_gated(const CUtensorMap& b, const CUtensorMap& d, const CUtensorMap& z, GemmParams p,
+                         const GateSrc& q, const DeviceInfo& dev, cudaStream_t s, const char* name, double bytes);
+
+// Argument checks of the TP SwiGLU pair (sizes, NULL, alignment, overlaps of
+// the output and of the scratch region [scratch, scratch + scratch_bytes)
+// with the tensors); the same for every entry point of the pair.
+dg_status tp_swiglu_check_sizes(int64_t S, int64_t d, int64_t ffn, int32_t W, int32_t bsz, const char* what);
+dg_status tp_swiglu_check(int64_t S, int64_t d, int64_t ffn, int32_t W, int32_t bsz, const void* x_shards,
+                          const void* w13, const void* w2, const void* y_shards, const void* scratch,
+                          size_t scratch_bytes, const char* what);
+
+// The two GEMMs of the TP SwiGLU pair with h [S*bsz, ffn] bf16 at `h`; the
+// arguments have been validated by the caller.  traced = false creates no
+// events (the entry point that must not allocate anything).
+dg_status tp_swiglu_enqueue(int64_t S, int64_t d, int64_t ffn, int32_t W, int32_t bsz, const void* x_shards,
+                            const void* w13, const void* w2, void* y_shards, void* h, const DeviceInfo& dev,
+                            cudaStream_t s, bool traced);
 
 // Brackets one kernel launch with CUDA events while tracing is on (dg_trace_begin).
 class TraceScope {
@@ -107,6 +155,26 @@ cudaError_t launch_gemm_fp8_kk_n224(const CUtensorMap&, const CUtensorMap&, cons
                                     const GemmParams&, int num_sms, cudaStream_t);
 // Co-resident CTA pairs (or CTAs) of the e4m3 GEMM on the current device.
 cudaError_t gemm_fp8_units(int num_sms, int* units);
+
+// Sources of the normalise-and-gate folded into the A operand of the FFN's
+// second GEMM (dg_gemm_gated.cu): A[m, k] = LN_x(U)[m, k] * silu(LN_g(G))[m, k]
+// of problem g, computed from Z and the row statistics.
+struct GateSrc {
+  const __nv_bfloat16* Z;                  // [G][M][2H]: U = columns [0, H), G = [H, 2H)
+  const float4* stats;                     // [G][M]: (mean_u, rstd_u, mean_g, rstd_g)
+  const __nv_bfloat16 *gx, *bx, *gg, *bg;  // [P][H]: LayerNorm weight and bias of U and of G
+  __nv_bfloat16* Hl;                       // [G][M][H], written by the units of column pass 0; or NULL
+  int32_t H, L;                            // half width of Z; problems per rank (rank of problem g = g / L)
+};
+// Output columns per work unit of the gated GEMM (two 256-column UMMAs), and
+// the K elements of one of its pipeline stages (32 or 64).
+int gemm_gated_tile_n();
+int gemm_gated_bk();
+// One persistent launch of the gated GEMM: B = wout (MN-major map, p.b_mn4),
+// D = the output map with p.d_g, Z = the map of q.Z ([G][M][2H], box 64 x 128
+// rows), p.bias [G][N] with p.bias_g_stride.
+cudaError_t launch_gemm_gated(const CUtensorMap& b, const CUtensorMap& d, const CUtensorMap& z, const GemmParams& p,
+                              const GateSrc& q, int num_sms, cudaStream_t s);
 
 // Widest FFN hidden size H = D*k accepted (GEMM N = 2H stays far inside int32
 // tile arithmetic; the row kernels split wider rows into column blocks).
@@ -249,7 +317,8 @@ cudaError_t launch_ln_gate_bwd_apply(const void* Z, const void* stats, const voi
 // Row ranges per token position used by pass 2.
 int ffn_bwd_row_splits(int T, int M, int H);
 
-// db1 [T, 2H] and d_nx_w, d_nx_b, d_ng_w, d_ng_b [P, H] from the partials, in a fixed order.
+// db1 [T, 2H] and d_nx_w, d_nx_b, d_ng_w, d_ng_b [P, H] from the partials, in a
+// fixed order; a NULL output is skipped.
 cudaError_t launch_grad_reduce(const float* part, void* d_b1, void* d_nx_w, void* d_nx_b, void* d_ng_w, void* d_ng_b,
                                int P, int L, int H, int nsplit, const DeviceInfo& dev, cudaStream_t s);
 
@@ -260,6 +329,11 @@ cudaError_t launch_column_sum(const void* src, void* out, int G, int rows, int n
 // Backward of the SwiGLU gate, in place: ab [rows, W, 2F] holds (a_s | b_s)
 // and becomes (da_s | db_s); dh [rows, W*F] becomes h = silu(a)*b.
 cudaError_t launch_swiglu_gate_bwd(void* ab, void* dh_h, int64_t rows, int W, int F, const DeviceInfo& dev,
+                                   cudaStream_t s);
+
+// comp_only layout: out[p][b][r*L + l] = in[r][b][p*L + l] for tensors
+// [P, B, T, D] with T = P*L (an involution; 16-byte vector copies).
+cudaError_t launch_swap_rank_slice(const void* in, void* out, int P, int B, int T, int D, const DeviceInfo& dev,
                                    cudaStream_t s);
 
 // Row permutations of the exchange (16-byte vector copies).

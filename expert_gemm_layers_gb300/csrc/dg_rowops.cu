@@ -33,17 +33,21 @@ __device__ __forceinline__ void unpack8(const uint4 v, float (&f)[8]) {
 }
 
 
+// True if the call's error word records a failure.  A kernel without bounded
+// waits may be given no error word (NULL), which reads as no failure.
+__device__ __forceinline__ bool err_set(const uint32_t* err) { return err != nullptr && ld_volatile_u32(err) != 0u; }
+
 // Warp-uniform read of the error word (these kernels use full-warp barriers
 // and shuffles, so a warp must not split on it).
 __device__ __forceinline__ bool warp_aborted(const uint32_t* err) {
-  return __shfl_sync(0xffffffffu, ld_volatile_u32(err), 0) != 0u;
+  return __shfl_sync(0xffffffffu, err_set(err) ? 1u : 0u, 0) != 0u;
 }
 
 // Block-uniform read of the error word (a divergent early return ahead of a
 // barrier would be undefined).
 __device__ __forceinline__ bool block_aborted(const uint32_t* err) {
   __shared__ uint32_t flag;
-  if (threadIdx.x == 0) flag = ld_volatile_u32(err);
+  if (threadIdx.x == 0) flag = err_set(err) ? 1u : 0u;
   __syncthreads();
   return flag != 0u;
 }
@@ -100,7 +104,7 @@ __device__ __forceinline__ void cp_async_wait() {
 __global__ void ln_stats_finalize_kernel(const float4* __restrict__ part, float4* __restrict__ stats, int T, int M,
                                          int H, int tile_n, int tiles_n, float eps, const uint32_t* err) {
   griddep_wait();
-  if (ld_volatile_u32(err) != 0u) return;
+  if (err_set(err)) return;
   const int64_t rows = static_cast<int64_t>(T) * M;
   const int N = 2 * H;
   for (int64_t row = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; row < rows;
@@ -323,7 +327,7 @@ __global__ void quant_rows_kernel(const __nv_bfloat16* __restrict__ x, uint8_t* 
 __global__ void col_scale_kernel(const __nv_bfloat16* __restrict__ w, float* __restrict__ scale,
                                  float* __restrict__ inv, int K, int N, const uint32_t* err) {
   griddep_wait();
-  if (ld_volatile_u32(err) != 0u) return;
+  if (err_set(err)) return;
   const int g = blockIdx.y;
   const int n = blockIdx.x * blockDim.x + threadIdx.x;
   if (n >= N) return;
@@ -759,13 +763,14 @@ __global__ void grad_reduce_kernel(const float* __restrict__ part, __nv_bfloat16
                                    __nv_bfloat16* __restrict__ d_ng_w, __nv_bfloat16* __restrict__ d_ng_b, int P,
                                    int L, int H, int nsplit, const uint32_t* err) {
   griddep_wait();
-  if (ld_volatile_u32(err) != 0u) return;
+  if (err_set(err)) return;
   const int T = P * L;
   const int64_t n_b1 = static_cast<int64_t>(T) * 2 * H;
   const int64_t n_norm = static_cast<int64_t>(P) * 4 * H;
   for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n_b1 + n_norm;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     if (i < n_b1) {
+      if (d_b1 == nullptr) continue;
       const int t = static_cast<int>(i / (2 * H));
       const int c2 = static_cast<int>(i - static_cast<int64_t>(t) * 2 * H);
       const int q = c2 >= H ? 1 : 0;
@@ -778,12 +783,13 @@ __global__ void grad_reduce_kernel(const float* __restrict__ part, __nv_bfloat16
       const int r = static_cast<int>(j / (4 * H));
       const int q = static_cast<int>((j / H) % 4);  // 0: nx_w, 1: nx_b, 2: ng_w, 3: ng_b
       const int c = static_cast<int>(j % H);
+      if ((q == 0 ? d_nx_w : q == 1 ? d_nx_b : q == 2 ? d_ng_w : d_ng_b) == nullptr) continue;
       float s = 0.0f;
       for (int l = 0; l < L; ++l)
         for (int k = 0; k < nsplit; ++k)
           s += part[((static_cast<int64_t>(r * L + l) * nsplit + k) * 6 + 2 + q) * H + c];
       __nv_bfloat16* out = q == 0 ? d_nx_w : q == 1 ? d_nx_b : q == 2 ? d_ng_w : d_ng_b;
-      out[static_cast<int64_t>(r) * H + c] = __float2bfloat16_rn(s);
+      if (out != nullptr) out[static_cast<int64_t>(r) * H + c] = __float2bfloat16_rn(s);
     }
   }
 }
@@ -798,7 +804,7 @@ __global__ void __launch_bounds__(32 * kColSumWarps) column_sum_slab_kernel(
     int64_t row_stride, const uint32_t* err) {
   __shared__ float part[kColSumWarps][256 + 4];
   griddep_wait();
-  if (ld_volatile_u32(err) != 0u) return;
+  if (err_set(err)) return;
   const int g = blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int c = blockIdx.x * 256 + 8 * lane;
@@ -851,7 +857,7 @@ __global__ void __launch_bounds__(32 * kColSumWarps) column_sum_slab_kernel(
 __global__ void column_sum_kernel(const __nv_bfloat16* __restrict__ src, __nv_bfloat16* __restrict__ out, int rows,
                                   int ncols, int64_t g_stride, int64_t row_stride, const uint32_t* err) {
   griddep_wait();
-  if (ld_volatile_u32(err) != 0u) return;
+  if (err_set(err)) return;
   const int g = blockIdx.y;
   const int c = 2 * (blockIdx.x * blockDim.x + threadIdx.x);
   if (c >= ncols) return;
@@ -884,7 +890,7 @@ __global__ void column_sum_kernel(const __nv_bfloat16* __restrict__ src, __nv_bf
 __global__ void swiglu_gate_bwd_kernel(__nv_bfloat16* __restrict__ ab, __nv_bfloat16* __restrict__ dh_h, int64_t rows,
                                        int W, int F, const uint32_t* err) {
   griddep_wait();
-  if (ld_volatile_u32(err) != 0u) return;
+  if (err_set(err)) return;
   const int fv = F / 8;
   const int64_t total = rows * W * fv;
   for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
@@ -920,11 +926,12 @@ __global__ void swiglu_gate_bwd_kernel(__nv_bfloat16* __restrict__ ab, __nv_bflo
   }
 }
 
-// Exchange permutations, 16 bytes per thread.
+// Exchange permutations, 16 bytes per thread.  A NULL error word (the explicit
+// permutation calls, which have no workspace) is not read.
 __global__ void dispatch_kernel(const uint4* __restrict__ in, uint4* __restrict__ out, int P, int B, int T,
                                 int vec_per_row, const uint32_t* err) {
   griddep_wait();
-  if (ld_volatile_u32(err) != 0u) return;
+  if (err_set(err)) return;
   const int L = T / P, PB = P * B;
   const int64_t total = static_cast<int64_t>(P) * PB * L * vec_per_row;
   for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
@@ -942,7 +949,7 @@ __global__ void dispatch_kernel(const uint4* __restrict__ in, uint4* __restrict_
 __global__ void combine_kernel(const uint4* __restrict__ in, uint4* __restrict__ out, int P, int B, int T,
                                int vec_per_row, const uint32_t* err) {
   griddep_wait();
-  if (ld_volatile_u32(err) != 0u) return;
+  if (err_set(err)) return;
   const int L = T / P, PB = P * B;
   const int64_t total = static_cast<int64_t>(PB) * T * vec_per_row;
   for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
@@ -952,6 +959,27 @@ __global__ void combine_kernel(const uint4* __restrict__ in, uint4* __restrict__
     const int n = static_cast<int>(q / T), t = static_cast<int>(q - (q / T) * T);
     const int r = t / L, l = t - (t / L) * L;
     const int64_t src_row = (static_cast<int64_t>(r) * PB + n) * L + l;  // Ylocal[r][n][l]
+    out[i] = in[src_row * vec_per_row + c];
+  }
+}
+
+// comp_only layout (the exchange with the roles of rank and slice swapped):
+// out row (p, b, r*L + l) = in row (r, b, p*L + l) of [P, B, T, D] tensors.
+__global__ void swap_rank_slice_kernel(const uint4* __restrict__ in, uint4* __restrict__ out, int P, int B, int T,
+                                       int vec_per_row, const uint32_t* err) {
+  griddep_wait();
+  if (err_set(err)) return;
+  const int L = T / P;
+  const int64_t total = static_cast<int64_t>(P) * B * T * vec_per_row;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t q = i / vec_per_row;  // destination row (p, b, t)
+    const int c = static_cast<int>(i - q * vec_per_row);
+    const int t = static_cast<int>(q % T);
+    const int64_t pb = q / T;
+    const int b = static_cast<int>(pb % B), p = static_cast<int>(pb / B);
+    const int r = t / L, l = t - (t / L) * L;
+    const int64_t src_row = (static_cast<int64_t>(r) * B + b) * T + static_cast<int64_t>(p) * L + l;
     out[i] = in[src_row * vec_per_row + c];
   }
 }
@@ -1180,6 +1208,15 @@ cudaError_t launch_combine(const void* in, void* out, int P, int B, int T, int D
   int64_t blocks = (total + 255) / 256;
   if (blocks > 16 * dev.num_sms) blocks = 16 * dev.num_sms;
   return launch_pdl(combine_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, s,
+                    static_cast<const uint4*>(in), static_cast<uint4*>(out), P, B, T, D / 8, dev.err);
+}
+
+cudaError_t launch_swap_rank_slice(const void* in, void* out, int P, int B, int T, int D, const DeviceInfo& dev,
+                                   cudaStream_t s) {
+  const int64_t total = static_cast<int64_t>(P) * B * T * (D / 8);
+  int64_t blocks = (total + 255) / 256;
+  if (blocks > 16 * dev.num_sms) blocks = 16 * dev.num_sms;
+  return launch_pdl(swap_rank_slice_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, s,
                     static_cast<const uint4*>(in), static_cast<uint4*>(out), P, B, T, D / 8, dev.err);
 }
 

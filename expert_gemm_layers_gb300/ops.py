@@ -10,13 +10,14 @@ import ctypes
 
 import torch
 
-from ._lib import FFNShape, TraceEntry, check, load
+from ._lib import DG_ERROR_BLOCK_BYTES, DG_FFN_COMP_ONLY, DG_FFN_FUSED_GATE, FFNShape, TraceEntry, check, load
 
 __all__ = [
     "gemm_fp8", "ffn_shape", "a2a_ffn_forward", "a2a_ffn_backward", "a2a_ffn_fp8_pack_weights", "a2a_ffn_forward_fp8", "A2AFFN", "a2a_ffn",
     "a2a_dispatch", "a2a_combine", "tp_swiglu", "tp_swiglu_backward", "TPSwiGLU", "tp_swiglu_layer",
     "tp_linear", "tp_linear_backward", "TPLinear", "tp_linear_layer", "device_status", "debug_wait_timeout",
-    "FFN_PARAM_NAMES", "trace_begin", "trace_end",
+    "FFN_PARAM_NAMES", "trace_begin", "trace_end", "alloc_workspace", "error_block", "DG_FFN_COMP_ONLY",
+    "DG_FFN_FUSED_GATE",
 ]
 
 FFN_PARAM_NAMES = ("w1", "b1", "wout", "bout", "nx_w", "nx_b", "ng_w", "ng_b")
@@ -28,6 +29,31 @@ def _stream(dev: torch.device) -> int:
 
 def _ptr(t):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+_error_blocks: dict = {}
+
+
+def alloc_workspace(nbytes: int, device) -> torch.Tensor:
+    """A workspace of `nbytes` bytes on `device` whose error block (its first
+    DG_ERROR_BLOCK_BYTES bytes) is zeroed on the current stream."""
+    ws = torch.empty(max(int(nbytes), DG_ERROR_BLOCK_BYTES), dtype=torch.uint8, device=device)
+    ws[:DG_ERROR_BLOCK_BYTES].zero_()
+    return ws
+
+
+def error_block(device=None) -> torch.Tensor:
+    """The zeroed error block this module gives calls that need no other
+    scratch, one per (device, current stream): calls on different streams
+    do not share an error word."""
+    dev = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
+    key = (dev.index, _stream(dev))
+    blk = _error_blocks.get(key)
+    if blk is None:
+        with torch.cuda.device(dev):
+            blk = torch.zeros(DG_ERROR_BLOCK_BYTES, dtype=torch.uint8, device=dev)
+        _error_blocks[key] = blk
+    return blk
 
 
 def _need(t: torch.Tensor, name: str, dtype: torch.dtype, shape=None, device=None):
@@ -48,8 +74,9 @@ def _need(t: torch.Tensor, name: str, dtype: torch.dtype, shape=None, device=Non
 # ------------------------------------------------------------------ FP8 GEMM
 
 def gemm_fp8(A: torch.Tensor, B: torch.Tensor, C: torch.Tensor | None = None, alpha: float = 1.0,
-             beta: float = 0.0, out: torch.Tensor | None = None) -> torch.Tensor:
-    """D = alpha * (A @ B^T) + beta * C with A [M,K], B [N,K] in float8_e4m3fn, C/D bf16 [M,N]."""
+             beta: float = 0.0, out: torch.Tensor | None = None, ws: torch.Tensor | None = None) -> torch.Tensor:
+    """D = alpha * (A @ B^T) + beta * C with A [M,K], B [N,K] in float8_e4m3fn, C/D bf16 [M,N].
+    `ws` holds the call's error block (default: this stream's error_block())."""
     lib = load()
     M, K = A.shape
     N = B.shape[0]
@@ -60,9 +87,11 @@ def gemm_fp8(A: torch.Tensor, B: torch.Tensor, C: torch.Tensor | None = None, al
     if out is None:
         out = torch.empty((M, N), dtype=torch.bfloat16, device=A.device)
     _need(out, "out", torch.bfloat16, (M, N), A.device)
+    if ws is None:
+        ws = error_block(A.device)
     with torch.cuda.device(A.device):
         check(lib.dg_gemm_fp8(M, N, K, _ptr(A), _ptr(B), _ptr(C), _ptr(out), float(alpha), float(beta),
-                              ctypes.c_void_p(_stream(A.device))))
+                              _ptr(ws), ws.numel(), ctypes.c_void_p(_stream(A.device))))
     return out
 
 
@@ -79,13 +108,15 @@ def _ffn_param_shapes(P, B, T, D, k):
 
 
 def a2a_ffn_forward(inputs: torch.Tensor, params: dict, eps: float = 1e-5, saved: torch.Tensor | None = None,
-                    out: torch.Tensor | None = None):
+                    out: torch.Tensor | None = None, inference: bool = False, flags: int = 0,
+                    ws: torch.Tensor | None = None):
     """The A2A FFN layer for all P ranks at once.
 
     inputs [P,B,T,D] bf16; params: w1 [P,L,D,2H], b1 [P,L,2H], wout [P,L,H,D],
     bout [P,L,D], nx_w/nx_b/ng_w/ng_b [P,H] (bf16), where k = 2H/(2D) is read
     from w1.  Returns (output [P,B,T,D], saved) where `saved` is the opaque
-    byte buffer the backward needs.
+    byte buffer the backward needs (None with inference=True: nothing is
+    kept).  flags: DG_FFN_COMP_ONLY, DG_FFN_FUSED_GATE.
     """
     lib = load()
     P, B, T, D = inputs.shape
@@ -97,16 +128,22 @@ def a2a_ffn_forward(inputs: torch.Tensor, params: dict, eps: float = 1e-5, saved
         _need(params[name], name, torch.bfloat16, shapes[name], dev)
     sh = FFNShape(P, B, T, D, k, eps)
     nbytes = lib.dg_a2a_ffn_saved_bytes(ctypes.byref(sh))
-    if nbytes == 0:
-        check(lib.dg_a2a_ffn_fwd(ctypes.byref(sh), *([None] * 10), None, 0, None))
-    if saved is None:
+    wsb = lib.dg_a2a_ffn_fwd_workspace_bytes(ctypes.byref(sh), int(inference), int(flags))
+    if nbytes == 0 or wsb == 0:
+        check(lib.dg_a2a_ffn_fwd(ctypes.byref(sh), *([None] * 10), None, 0, None, 0, int(flags), None))
+    if saved is None and not inference:
         saved = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    if inference:
+        saved = None
+    if ws is None:
+        ws = error_block(dev) if wsb <= DG_ERROR_BLOCK_BYTES else alloc_workspace(wsb, dev)
     if out is None:
         out = torch.empty(shapes["inputs"], dtype=torch.bfloat16, device=dev)
     _need(out, "out", torch.bfloat16, shapes["inputs"], dev)
     with torch.cuda.device(dev):
         check(lib.dg_a2a_ffn_fwd(ctypes.byref(sh), _ptr(inputs), *[_ptr(params[n]) for n in FFN_PARAM_NAMES],
-                                 _ptr(out), _ptr(saved), saved.numel(), ctypes.c_void_p(_stream(dev))))
+                                 _ptr(out), _ptr(saved), 0 if saved is None else saved.numel(), _ptr(ws),
+                                 ws.numel(), int(flags), ctypes.c_void_p(_stream(dev))))
     return out, saved
 
 
@@ -151,7 +188,7 @@ def a2a_ffn_forward_fp8(inputs: torch.Tensor, params: dict, packed: torch.Tensor
     if nbytes == 0:
         check(lib.dg_a2a_ffn_fwd_fp8(ctypes.byref(sh), *([None] * 3), *([None] * 7), None, 0, None))
     if workspace is None:
-        workspace = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+        workspace = alloc_workspace(nbytes, dev)
     if out is None:
         out = torch.empty(shapes["inputs"], dtype=torch.bfloat16, device=dev)
     with torch.cuda.device(dev):
@@ -162,10 +199,14 @@ def a2a_ffn_forward_fp8(inputs: torch.Tensor, params: dict, packed: torch.Tensor
 
 
 def a2a_ffn_backward(inputs: torch.Tensor, params: dict, saved: torch.Tensor, dY: torch.Tensor,
-                     eps: float = 1e-5, workspace: torch.Tensor | None = None, grads: dict | None = None) -> dict:
+                     eps: float = 1e-5, workspace: torch.Tensor | None = None, grads: dict | None = None,
+                     flags: int = 0, need: tuple | None = None) -> dict:
     """Gradients of the layer w.r.t. inputs and every parameter (overwritten, bf16).
 
-    Returns a dict with keys "inputs" and the names in FFN_PARAM_NAMES.
+    Returns a dict with keys "inputs" and the names in FFN_PARAM_NAMES.  With
+    `need` (a subset of those keys) only those gradients are computed (the
+    others are None and their work is skipped); `grads` may hold None entries
+    for the same effect.  flags: DG_FFN_COMP_ONLY (as given to the forward).
     """
     lib = load()
     P, B, T, D = inputs.shape
@@ -174,20 +215,21 @@ def a2a_ffn_backward(inputs: torch.Tensor, params: dict, saved: torch.Tensor, dY
     dev = inputs.device
     _need(dY, "dY", torch.bfloat16, shapes["inputs"], dev)
     sh = FFNShape(P, B, T, D, k, eps)
-    wsb = lib.dg_a2a_ffn_bwd_workspace_bytes(ctypes.byref(sh))
+    wsb = lib.dg_a2a_ffn_bwd_workspace_bytes(ctypes.byref(sh), int(flags))
     if workspace is None:
-        workspace = torch.empty(max(wsb, 1), dtype=torch.uint8, device=dev)
+        workspace = alloc_workspace(wsb, dev)
+    names = ("inputs",) + FFN_PARAM_NAMES
     if grads is None:
-        grads = {name: torch.empty(shapes[name], dtype=torch.bfloat16, device=dev)
-                 for name in ("inputs",) + FFN_PARAM_NAMES}
+        grads = {name: (torch.empty(shapes[name], dtype=torch.bfloat16, device=dev)
+                        if need is None or name in need else None) for name in names}
     g = grads
     with torch.cuda.device(dev):
         check(lib.dg_a2a_ffn_bwd(
             ctypes.byref(sh), _ptr(inputs), *[_ptr(params[n]) for n in FFN_PARAM_NAMES],
-            _ptr(saved), saved.numel(), _ptr(dY),
-            _ptr(g["inputs"]), _ptr(g["w1"]), _ptr(g["b1"]), _ptr(g["wout"]), _ptr(g["bout"]),
-            _ptr(g["nx_w"]), _ptr(g["nx_b"]), _ptr(g["ng_w"]), _ptr(g["ng_b"]),
-            _ptr(workspace), workspace.numel(), ctypes.c_void_p(_stream(dev))))
+            _ptr(saved), 0 if saved is None else saved.numel(), _ptr(dY),
+            _ptr(g.get("inputs")), _ptr(g.get("w1")), _ptr(g.get("b1")), _ptr(g.get("wout")), _ptr(g.get("bout")),
+            _ptr(g.get("nx_w")), _ptr(g.get("nx_b")), _ptr(g.get("ng_w")), _ptr(g.get("ng_b")),
+            _ptr(workspace), workspace.numel(), int(flags), ctypes.c_void_p(_stream(dev))))
     return grads
 
 
@@ -206,9 +248,10 @@ class A2AFFN(torch.autograd.Function):
     def backward(ctx, dY):
         inputs, w1, b1, wout, bout, nx_w, nx_b, ng_w, ng_b, saved = ctx.saved_tensors
         params = dict(w1=w1, b1=b1, wout=wout, bout=bout, nx_w=nx_w, nx_b=nx_b, ng_w=ng_w, ng_b=ng_b)
-        g = a2a_ffn_backward(inputs, params, saved, dY.contiguous(), ctx.eps)
-        return (g["inputs"], g["w1"], g["b1"], g["wout"], g["bout"], g["nx_w"], g["nx_b"], g["ng_w"],
-                g["ng_b"], None)
+        names = ("inputs",) + FFN_PARAM_NAMES
+        need = tuple(n for n, want in zip(names, ctx.needs_input_grad[:9]) if want)
+        g = a2a_ffn_backward(inputs, params, saved, dY.contiguous(), ctx.eps, need=need)
+        return tuple(g[n] for n in names) + (None,)
 
 
 def a2a_ffn(inputs, params: dict, eps: float = 1e-5):
@@ -256,7 +299,7 @@ def tp_swiglu(x_shards: torch.Tensor, w13: torch.Tensor, w2: torch.Tensor,
     S = W * sl
     wsb = lib.dg_tp_swiglu_workspace_bytes(S, d, ffn, W, bsz)
     if workspace is None:
-        workspace = torch.empty(max(wsb, 1), dtype=torch.uint8, device=dev)
+        workspace = alloc_workspace(wsb, dev)
     if out is None:
         out = torch.empty_like(x_shards)
     with torch.cuda.device(dev):
@@ -282,7 +325,7 @@ def tp_swiglu_backward(x_shards: torch.Tensor, w13: torch.Tensor, w2: torch.Tens
     S = W * sl
     wsb = lib.dg_tp_swiglu_bwd_workspace_bytes(S, d, ffn, W, bsz)
     if workspace is None:
-        workspace = torch.empty(max(wsb, 1), dtype=torch.uint8, device=dev)
+        workspace = alloc_workspace(wsb, dev)
     if grads is None:
         grads = dict(x=torch.empty_like(x_shards), w13=torch.empty_like(w13), w2=torch.empty_like(w2))
     with torch.cuda.device(dev):
@@ -334,9 +377,11 @@ def tp_linear(x: torch.Tensor, weight: torch.Tensor, bias: torch.Tensor | None =
     rows = x.numel() // in_f
     if out is None:
         out = torch.empty((*x.shape[:-1], out_f), dtype=torch.bfloat16, device=dev)
+    ws = error_block(dev)
     with torch.cuda.device(dev):
         check(lib.dg_tp_linear_fwd(rows, in_f, out_f, _ptr(x), _ptr(weight),
-                                   None if bias is None else _ptr(bias), _ptr(out), ctypes.c_void_p(_stream(dev))))
+                                   None if bias is None else _ptr(bias), _ptr(out), _ptr(ws), ws.numel(),
+                                   ctypes.c_void_p(_stream(dev))))
     return out
 
 
@@ -356,9 +401,10 @@ def tp_linear_backward(x: torch.Tensor, weight: torch.Tensor, dy: torch.Tensor, 
     g["weight"] = torch.empty_like(weight) if need_dw else None
     g["bias"] = torch.empty(out_f, dtype=torch.bfloat16, device=dev) if need_db else None
     p = lambda t: None if t is None else _ptr(t)
+    ws = error_block(dev)
     with torch.cuda.device(dev):
         check(lib.dg_tp_linear_bwd(rows, in_f, out_f, _ptr(x), _ptr(weight), _ptr(dy), p(g["x"]), p(g["weight"]),
-                                   p(g["bias"]), ctypes.c_void_p(_stream(dev))))
+                                   p(g["bias"]), _ptr(ws), ws.numel(), ctypes.c_void_p(_stream(dev))))
     return g
 
 
@@ -386,21 +432,30 @@ def tp_linear_layer(x, weight, bias=None):
 
 # ------------------------------------------------------------------ diagnostics
 
-def device_status(device=None):
-    """Synchronise the current stream and read/clear the device error word: (status, raw code)."""
+def device_status(device=None, workspace: torch.Tensor | None = None, builtin: bool = False):
+    """Synchronise the current stream and read/clear an error word: that of
+    `workspace`, else this stream's error_block() (builtin=True: the library's
+    own word, written only by dg_tp_swiglu_noalloc).  Returns (status, raw code)."""
     lib = load()
     dev = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
+    if builtin:
+        ws = None
+    else:
+        ws = workspace if workspace is not None else error_block(dev)
     site = ctypes.c_uint32(0)
     with torch.cuda.device(dev):
-        st = lib.dg_device_status(ctypes.c_void_p(_stream(dev)), ctypes.byref(site))
+        st = lib.dg_check_device_error(_ptr(ws), ctypes.c_void_p(_stream(dev)), ctypes.byref(site))
     return st, site.value
 
 
-def debug_wait_timeout(limit_us: int, device=None) -> None:
+def debug_wait_timeout(limit_us: int, device=None, workspace: torch.Tensor | None = None) -> None:
+    """Expire one bounded wait on purpose; the failure lands in `workspace`'s error block
+    (default: this stream's error_block())."""
     lib = load()
     dev = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
+    ws = workspace if workspace is not None else error_block(dev)
     with torch.cuda.device(dev):
-        check(lib.dg_debug_wait_timeout(int(limit_us), ctypes.c_void_p(_stream(dev))))
+        check(lib.dg_debug_wait_timeout(_ptr(ws), ws.numel(), int(limit_us), ctypes.c_void_p(_stream(dev))))
 
 
 def trace_begin(only: str | None = None) -> None:

@@ -11,18 +11,22 @@
  *    e4m3 means OCP E4M3FN bit patterns (uint8, the element format of
  *    cutlass::float_e4m3_t and torch.float8_e4m3fn).
  *  - The library never allocates device memory.  Scratch space comes from
- *    the caller through a (pointer, bytes) pair whose required size is given
- *    by the matching *_bytes() query; too small a buffer is an error.
+ *    the caller through a (pointer `ws`, bytes) pair whose required size is
+ *    given by the matching *_bytes() query; too small a buffer is an error.
  *  - Inputs are never written.  Outputs must not overlap inputs or scratch.
  *  - Calls are asynchronous and stream-ordered on `stream` (a cudaStream_t,
  *    NULL = legacy default stream): they return once the work is enqueued.
  *  - Every call returns a dg_status.  On failure nothing is enqueued and
  *    dg_last_error() names the offending argument (thread-local message).
  *    There is no silent fallback: an unsupported case is an error.
- *  - Device-side failures (a pipeline wait that exceeded its time limit) are
- *    recorded in a per-device error word instead of trapping; once set, the
- *    library's kernels return early without touching memory until
- *    dg_device_status() reads and clears it.  Poll it after synchronising.
+ *  - Error block.  The first DG_ERROR_BLOCK_BYTES bytes of every workspace
+ *    hold that workspace's device-side error word.  A kernel whose bounded
+ *    pipeline wait runs out of time records the failure there instead of
+ *    trapping, and later kernels of calls given the same workspace return
+ *    early without touching memory until dg_check_device_error() reads and
+ *    clears the word.  Calls with different workspaces (for example one per
+ *    stream) do not see each other's failures.  The word must be zero before
+ *    a workspace's first use: zero-filled memory, or dg_workspace_init().
  *  - Tensor cores accumulate in fp32; bf16 results are rounded to nearest
  *    even once, at the end.
  */
@@ -35,6 +39,9 @@
 #ifdef __cplusplus
 extern "C" {
 #endif
+
+/* Bytes at the start of every workspace that hold its error word. */
+#define DG_ERROR_BLOCK_BYTES 256
 
 typedef enum {
   DG_OK = 0,
@@ -53,12 +60,20 @@ const char* dg_last_error(void);
 const char* dg_version(void);
 
 /*
- * Synchronises `stream`, then reads and clears the current device's error
- * word.  Returns DG_OK, DG_ERR_TIMEOUT (a bounded pipeline wait expired),
+ * Zeroes the error block of a freshly allocated workspace (stream-ordered;
+ * ws_bytes >= DG_ERROR_BLOCK_BYTES).  Not needed for zero-filled memory.
+ */
+dg_status dg_workspace_init(void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Synchronises `stream`, then reads and clears the error word in the error
+ * block of `ws` (a workspace given to earlier calls), or, with ws = NULL, the
+ * library's own error word, which only dg_tp_swiglu_noalloc writes.  Returns
+ * DG_OK, DG_ERR_TIMEOUT (a bounded pipeline wait expired),
  * DG_ERR_DEVICE_CHECK, or DG_ERR_CUDA.  When not DG_OK, *site (if non-NULL)
  * receives the raw code, whose low byte names the wait that expired.
  */
-dg_status dg_device_status(void* stream, uint32_t* site);
+dg_status dg_check_device_error(void* ws, void* stream, uint32_t* site);
 
 /* ------------------------------------------------------------------------
  * (a) FP8 GEMM   D = alpha * (A @ B^T) + beta * C
@@ -74,11 +89,13 @@ dg_status dg_device_status(void* stream, uint32_t* site);
  *   D      bf16 [M, N]         output, D = bf16_rne(alpha*acc + beta*C),
  *                              acc = sum_k A[m,k]*B[n,k] exact products, fp32 sum
  *   M, N >= 0 (0 = nothing to do); K >= 0 (K == 0 gives D = beta*C).
- * No scratch is needed.
+ *   ws     the error block only (dg_gemm_fp8_workspace_bytes = 256 bytes)
  * ------------------------------------------------------------------------ */
+size_t dg_gemm_fp8_workspace_bytes(int64_t M, int64_t N, int64_t K);
+
 dg_status dg_gemm_fp8(int64_t M, int64_t N, int64_t K,
                       const void* A, const void* B, const void* C, void* D,
-                      float alpha, float beta, void* stream);
+                      float alpha, float beta, void* ws, size_t ws_bytes, void* stream);
 
 /* ------------------------------------------------------------------------
  * (b) All-to-all expert-parallel FFN layer, P logical ranks on one GPU.
@@ -104,16 +121,32 @@ dg_status dg_gemm_fp8(int64_t M, int64_t N, int64_t K,
  * Requirements: T % P == 0, D % 8 == 0, P*B >= 1; H = D*k <= 65536 (larger H
  * returns DG_ERR_UNSUPPORTED).
  *
- * `saved` (size dg_a2a_ffn_saved_bytes) is required: the forward writes Z,
- * Hl and the per-row LayerNorm statistics there, and the backward reads
- * them.  It is also the forward's only scratch.
+ * saved  (size dg_a2a_ffn_saved_bytes) training: the forward writes Z, Hl
+ *        and the per-row LayerNorm statistics there, and the backward reads
+ *        them.  NULL = inference: nothing is kept, and Z, the statistics
+ *        (and Hl, unless DG_FFN_FUSED_GATE) live in the workspace instead.
+ * ws     size dg_a2a_ffn_fwd_workspace_bytes(shape, saved == NULL, flags):
+ *        the error block, plus the inference scratch and the comp_only
+ *        buffers when they apply.
+ * flags  DG_FFN_COMP_ONLY: no exchange; each rank's own [B, T, D] rows, viewed
+ *        as [B, P, L, D], feed its L slices (the project statement's
+ *        comp_only mode of forward_ffn; the output keeps the input's layout).
+ *        DG_FFN_FUSED_GATE: compute Hl inside the second GEMM, by producer
+ *        warps that normalise and gate Z while building its A operand,
+ *        instead of in a separate pass through HBM.  Same results bit for
+ *        bit; slower at the page's shapes, but an inference call then needs
+ *        no Hl scratch (rows x H bf16 less workspace).
  * ------------------------------------------------------------------------ */
 typedef struct {
   int32_t P, B, T, D, k;
   float eps; /* LayerNorm epsilon, 1e-5 on the page */
 } dg_ffn_shape;
 
+#define DG_FFN_COMP_ONLY 1u
+#define DG_FFN_FUSED_GATE 2u
+
 size_t dg_a2a_ffn_saved_bytes(const dg_ffn_shape* shape);
+size_t dg_a2a_ffn_fwd_workspace_bytes(const dg_ffn_shape* shape, int32_t inference, uint32_t flags);
 
 dg_status dg_a2a_ffn_fwd(const dg_ffn_shape* shape,
                          const void* inputs, const void* w1, const void* b1,
@@ -121,17 +154,23 @@ dg_status dg_a2a_ffn_fwd(const dg_ffn_shape* shape,
                          const void* nx_w, const void* nx_b,
                          const void* ng_w, const void* ng_b,
                          void* output, void* saved, size_t saved_bytes,
-                         void* stream);
+                         void* ws, size_t ws_bytes, uint32_t flags, void* stream);
 
 /*
- * Backward of dg_a2a_ffn_fwd for the same shape and parameters, given the
- * upstream gradient dY [P,B,T,D] and the `saved` buffer the forward filled.
- * Gradient outputs are OVERWRITTEN (not accumulated), bf16, same layouts as
- * the tensors they belong to; d_nx_* / d_ng_* of rank r sum over its rows
- * and its L slices.  Scratch: `ws` of dg_a2a_ffn_bwd_workspace_bytes.
- * All gradient pointers are required.
+ * Backward of dg_a2a_ffn_fwd for the same shape, parameters and flags, given
+ * the upstream gradient dY [P,B,T,D] and the `saved` buffer the forward
+ * filled.  Gradient outputs are OVERWRITTEN (not accumulated), bf16, same
+ * layouts as the tensors they belong to; d_nx_* / d_ng_* of rank r sum over
+ * its rows and its L slices.  Any gradient pointer may be NULL: that gradient
+ * is not computed, nothing is written there, and work that only it needs is
+ * skipped (d_inputs: the dX GEMM; d_w1: the dw1 GEMM; d_wout: the dwout GEMM;
+ * d_bout: its column sum; with d_inputs, d_w1, d_b1 and the four norm
+ * gradients all NULL, also the dHl GEMM and the LayerNorm-gate backward).
+ * Inputs only a skipped gradient needs may be NULL too (inputs for d_w1, w1
+ * for d_inputs, saved for all but d_bout).  flags: DG_FFN_COMP_ONLY or 0.
+ * Scratch: `ws` of dg_a2a_ffn_bwd_workspace_bytes(shape, flags).
  */
-size_t dg_a2a_ffn_bwd_workspace_bytes(const dg_ffn_shape* shape);
+size_t dg_a2a_ffn_bwd_workspace_bytes(const dg_ffn_shape* shape, uint32_t flags);
 
 dg_status dg_a2a_ffn_bwd(const dg_ffn_shape* shape,
                          const void* inputs, const void* w1, const void* b1,
@@ -142,7 +181,7 @@ dg_status dg_a2a_ffn_bwd(const dg_ffn_shape* shape,
                          void* d_inputs, void* d_w1, void* d_b1,
                          void* d_wout, void* d_bout,
                          void* d_nx_w, void* d_nx_b, void* d_ng_w, void* d_ng_b,
-                         void* ws, size_t ws_bytes, void* stream);
+                         void* ws, size_t ws_bytes, uint32_t flags, void* stream);
 
 /*
  * The two exchanges as explicit permutation copies (bit-exact bf16 moves),
@@ -177,9 +216,9 @@ dg_status dg_a2a_combine(int32_t P, int32_t B, int32_t T, int32_t D,
  * dg_a2a_ffn_fwd_fp8 computes `output` (bf16 [P,B,T,D]) from bf16 inputs,
  * the packed weights, and the bf16 b1, bout and LayerNorm parameters (layouts
  * of dg_a2a_ffn_fwd).  Its workspace (dg_a2a_ffn_fp8_workspace_bytes) starts
- * with the input codes [P,B,T,D] e4m3 followed, at the next 256-byte
- * boundary, by their scales [T, P*B] f32 (scale of input row (s, b, t) at
- * t*P*B + s*B + b); both are left there after the call.
+ * with the error block, then the input codes [P,B,T,D] e4m3 followed, at the
+ * next 256-byte boundary, by their scales [T, P*B] f32 (scale of input row
+ * (s, b, t) at t*P*B + s*B + b); both are left there after the call.
  * Requirements: those of dg_a2a_ffn_fwd, D % 16 == 0, H % 16 == 0, H <= 8192
  * (an e4m3 Hl row is scaled inside one CTA); otherwise the query functions
  * return 0 and the calls fail with DG_ERR_INVALID_ARGUMENT / UNSUPPORTED.
@@ -213,7 +252,8 @@ dg_status dg_a2a_ffn_fwd_fp8(const dg_ffn_shape* shape, const void* inputs,
  * scattering them back is the identity on memory order.  The shard sum is
  * the K loop of one GEMM accumulating in TMEM.
  * Requirements: S % W == 0, ffn % W == 0, d % 8 == 0, (ffn/W) % 8 == 0.
- * Scratch: h [W*bsz*S/W, ffn] bf16 in `ws` (dg_tp_swiglu_workspace_bytes).
+ * Scratch (dg_tp_swiglu_workspace_bytes): the error block, then h
+ * [W*bsz*S/W, ffn] bf16.
  * ------------------------------------------------------------------------ */
 size_t dg_tp_swiglu_workspace_bytes(int64_t S, int64_t d, int64_t ffn, int32_t W, int32_t bsz);
 
@@ -241,8 +281,9 @@ dg_status dg_tp_swiglu(int64_t S, int64_t d, int64_t ffn, int32_t W, int32_t bsz
  *   dx_shards [W, bsz, S/W, d]   dL/dx (output, overwritten)
  *   d_w13     [W, 2*ffn/W, d]    dL/dw13 in w13's layout (output, overwritten)
  *   d_w2      [d, ffn]           dL/dw2 (output, overwritten)
- * Scratch: [a|b] [rows, 2*ffn] and dh [rows, ffn] bf16 in `ws`
- * (dg_tp_swiglu_bwd_workspace_bytes); no written buffer may overlap any other.
+ * Scratch: the error block, then [a|b] [rows, 2*ffn] and dh [rows, ffn] bf16
+ * in `ws` (dg_tp_swiglu_bwd_workspace_bytes); no written buffer may overlap
+ * any other.
  * Requirements and errors are those of dg_tp_swiglu.
  */
 size_t dg_tp_swiglu_bwd_workspace_bytes(int64_t S, int64_t d, int64_t ffn, int32_t W, int32_t bsz);
@@ -265,6 +306,8 @@ dg_status dg_tp_swiglu_bwd(int64_t S, int64_t d, int64_t ffn, int32_t W, int32_t
  * nothing: S*bsz*ffn*2 bytes must not exceed 32 MiB (33554432), otherwise
  * the call returns DG_ERR_UNSUPPORTED without enqueuing anything.  Every
  * device that loads the library holds that array until the process exits.
+ * Having no workspace, it records device-side failures in the library's own
+ * error word: read it with dg_check_device_error(NULL, stream, site).
  * The first call on a device looks up the array's device address
  * (cudaGetSymbolAddress) with that device current; make that first call
  * before any stream capture.  All calls on a device share the one array, so
@@ -303,25 +346,30 @@ dg_status dg_tp_swiglu_noalloc(int64_t S, int64_t d, int64_t ffn, int32_t W, int
  * (not computed).  Outputs are overwritten.
  * Requirements: rows, in_features, out_features >= 1; in_features and
  * out_features multiples of 8; 16-byte aligned tensors; outputs disjoint from
- * each other and from the inputs.
+ * each other and from the inputs.  ws: the error block only
+ * (dg_tp_linear_workspace_bytes = 256 bytes).
  * ------------------------------------------------------------------------ */
+size_t dg_tp_linear_workspace_bytes(int64_t rows, int64_t in_features, int64_t out_features);
+
 dg_status dg_tp_linear_fwd(int64_t rows, int64_t in_features, int64_t out_features,
                            const void* x, const void* weight, const void* bias,
-                           void* y, void* stream);
+                           void* y, void* ws, size_t ws_bytes, void* stream);
 
 dg_status dg_tp_linear_bwd(int64_t rows, int64_t in_features, int64_t out_features,
                            const void* x, const void* weight, const void* dy,
-                           void* dx, void* d_weight, void* d_bias, void* stream);
+                           void* dx, void* d_weight, void* d_bias,
+                           void* ws, size_t ws_bytes, void* stream);
 
 /* ------------------------------------------------------------------------
  * Diagnostics.
  * dg_debug_wait_timeout launches one small kernel that waits, with the
  * library's bounded wait, on a barrier nothing will ever arrive at; after
  * `limit_us` microseconds the wait gives up and records DG_ERR_TIMEOUT in the
- * error word, which dg_device_status() then reports.  It exists to test the
+ * error block of `ws` (ws_bytes >= DG_ERROR_BLOCK_BYTES), which
+ * dg_check_device_error(ws, ...) then reports.  It exists to test the
  * failure path without faulting or hanging the GPU.
  * ------------------------------------------------------------------------ */
-dg_status dg_debug_wait_timeout(uint32_t limit_us, void* stream);
+dg_status dg_debug_wait_timeout(void* ws, size_t ws_bytes, uint32_t limit_us, void* stream);
 
 /* ------------------------------------------------------------------------
  * Launch tracing.

@@ -47,7 +47,7 @@ __all__ = [
     "a2a_dispatch", "a2a_combine", "dispatch_source_row", "combine_source_row",
     "layer_norm", "silu", "FFNShape", "ffn_forward", "ffn_forward_rows",
     "ffn_problem_backward", "ffn_backward", "ffn_backward_dx_rows",
-    "ffn_backward_problem", "ffn_backward_norm_rank",
+    "ffn_backward_problem", "ffn_backward_norm_rank", "ffn_forward_comp_only", "ffn_backward_comp_only",
     "tp_swiglu", "tp_swiglu_rows", "tp_swiglu_backward", "tp_swiglu_backward_rows",
     "tp_swiglu_backward_weight_cols",
 ]
@@ -441,14 +441,109 @@ def ffn_backward_problem(sh: FFNShape, inputs_bits, prm: dict, dY_bits, t: int) 
     return _run_problem(sh, inputs_bits, prm, dY_bits, r, l, range(sh.M))
 
 
+def _problem_norm_grads(X, dY, w1, b1, wout, nxw, nxb, ngw, ngb, eps, H):
+    """The LayerNorm weight/bias gradients of one (rank, slice) problem alone.
+
+    The same chain rule as ffn_problem_backward, stopped where these four
+    gradients are complete: Z = X w1 + b1, a = LN_x(U), s = LN_g(G),
+    dHl = dY wout^T, da = dHl*silu(s), ds = dHl*a*silu'(s); then
+    dgamma_x = sum_n da*xhat_u, dbeta_x = sum_n da, and the same with ds and
+    xhat_g (xhat the normalised half before the affine).
+    """
+    Z = X @ w1 + b1
+    U, G = Z[:, :H], Z[:, H:]
+    a = layer_norm(U, nxw, nxb, eps)
+    s = layer_norm(G, ngw, ngb, eps)
+    sig = 1.0 / (1.0 + np.exp(-s))
+    dHl = dY @ wout.T
+    da = dHl * (s * sig)
+    ds = dHl * a * (sig * (1.0 + s * (1.0 - sig)))
+    xu = layer_norm(U, 1.0, 0.0, eps)
+    xg = layer_norm(G, 1.0, 0.0, eps)
+    return dict(dnx_w=(da * xu).sum(axis=0), dnx_b=da.sum(axis=0),
+                dng_w=(ds * xg).sum(axis=0), dng_b=ds.sum(axis=0))
+
+
 def ffn_backward_norm_rank(sh: FFNShape, inputs_bits, prm: dict, dY_bits, r: int) -> dict:
     """Rank r's LayerNorm weight/bias gradients: sums over its L slices and all rows."""
+    P, B, T, D, H = sh.P, sh.B, sh.T, sh.D, sh.H
+    x_all = np.asarray(inputs_bits).reshape(P * B * T, D)
+    dy_all = np.asarray(dY_bits).reshape(P * B * T, D)
     acc = None
     for l in range(sh.L):
-        o = _run_problem(sh, inputs_bits, prm, dY_bits, r, l, range(sh.M))
-        part = {k: o[k] for k in ("dnx_w", "dnx_b", "dng_w", "dng_b")}
+        src = _problem_rows(sh, x_all, r, l, range(sh.M))
+        p = _problem_params(sh, prm, r, l)
+        part = _problem_norm_grads(bf16_to_f64(x_all[src]), bf16_to_f64(dy_all[src]), p["w1"], p["b1"], p["wout"],
+                                   p["nxw"], p["nxb"], p["ngw"], p["ngb"], sh.eps, H)
         acc = part if acc is None else {k: acc[k] + part[k] for k in acc}
     return acc
+
+
+# ---------------------------------------------------------------------------
+# comp_only: the layer without the exchange
+# ---------------------------------------------------------------------------
+#
+# The project statement's forward_ffn(ffn, inputs, *, comp_only=False)
+# ("Interface, layout, and parameters") names a compute-only mode without
+# defining it.  Reading: no exchange -- rank r's own inputs [B, T, D] are
+# viewed as [B, P, L, D] (token t = p*L + l), i.e. [B*P, L, D] with row
+# n = b*P + p, and slice l of that view goes through rank r's problem l
+# (w1[r][l], ..., the rank's norm_x / norm_gate); the result is viewed back
+# to [B, T, D] at the same place.  Every row is still processed on its own.
+
+def _comp_only_view(x_r, sh: FFNShape):
+    """[B, T, D] -> [B*P, L, D] (row n = b*P + p holds token t = p*L + l)."""
+    return x_r.reshape(sh.B, sh.P, sh.L, -1).reshape(sh.B * sh.P, sh.L, -1)
+
+
+def _comp_only_unview(y_r, sh: FFNShape):
+    """[B*P, L, D] -> [B, T, D], the inverse of _comp_only_view."""
+    return y_r.reshape(sh.B, sh.P, sh.L, -1).reshape(sh.B, sh.T, -1)
+
+
+def ffn_forward_comp_only(sh: FFNShape, inputs, prm: dict, decoded: bool = False) -> np.ndarray:
+    """The layer in comp_only mode (no exchange), float64 [P, B, T, D]."""
+    P, L, D, H = sh.P, sh.L, sh.D, sh.H
+    x = np.asarray(inputs, dtype=np.float64) if decoded else bf16_to_f64(inputs)
+    x = x.reshape(P, sh.B, sh.T, D)
+    p = prm if decoded else _decode_ffn_params(sh, prm)
+    out = np.empty_like(x)
+    for r in range(P):
+        Xr = _comp_only_view(x[r], sh)
+        Yr = np.empty_like(Xr)
+        for l in range(L):
+            _, _, Yr[:, l, :] = _ffn_problem_forward(
+                Xr[:, l, :], p["w1"][r, l], p["b1"][r, l], p["wout"][r, l], p["bout"][r, l],
+                p["nxw"][r], p["nxb"][r], p["ngw"][r], p["ngb"][r], sh.eps, H)
+        out[r] = _comp_only_unview(Yr, sh)
+    return out
+
+
+def ffn_backward_comp_only(sh: FFNShape, inputs, prm: dict, dY, decoded: bool = False) -> dict:
+    """All gradients of the comp_only layer, float64 (keys as ffn_backward)."""
+    P, L, D, H = sh.P, sh.L, sh.D, sh.H
+    x = np.asarray(inputs, dtype=np.float64) if decoded else bf16_to_f64(inputs)
+    dy = np.asarray(dY, dtype=np.float64) if decoded else bf16_to_f64(dY)
+    x = x.reshape(P, sh.B, sh.T, D)
+    dy = dy.reshape(P, sh.B, sh.T, D)
+    p = prm if decoded else _decode_ffn_params(sh, prm)
+    g = dict(d_inputs=np.empty_like(x), dw1=np.empty((P, L, D, 2 * H)), db1=np.empty((P, L, 2 * H)),
+             dwout=np.empty((P, L, H, D)), dbout=np.empty((P, L, D)),
+             dnx_w=np.zeros((P, H)), dnx_b=np.zeros((P, H)), dng_w=np.zeros((P, H)), dng_b=np.zeros((P, H)))
+    for r in range(P):
+        Xr, dYr = _comp_only_view(x[r], sh), _comp_only_view(dy[r], sh)
+        dXr = np.empty_like(Xr)
+        for l in range(L):
+            o = ffn_problem_backward(Xr[:, l, :], dYr[:, l, :], p["w1"][r, l], p["b1"][r, l], p["wout"][r, l],
+                                     p["bout"][r, l], p["nxw"][r], p["nxb"][r], p["ngw"][r], p["ngb"][r],
+                                     sh.eps, H)
+            dXr[:, l, :] = o["dX"]
+            for key in ("dw1", "db1", "dwout", "dbout"):
+                g[key][r, l] = o[key]
+            for key in ("dnx_w", "dnx_b", "dng_w", "dng_b"):
+                g[key][r] += o[key]
+        g["d_inputs"][r] = _comp_only_unview(dXr, sh)
+    return g
 
 
 # ---------------------------------------------------------------------------

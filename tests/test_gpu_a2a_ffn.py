@@ -12,8 +12,9 @@ import pytest
 import torch
 
 import oracle as O
-from expert_gemm_layers_gb300 import (FFN_PARAM_NAMES, a2a_combine, a2a_dispatch, a2a_ffn, a2a_ffn_backward,
-                                      a2a_ffn_forward, synth)
+import expert_gemm_layers_gb300 as dg
+from expert_gemm_layers_gb300 import (DG_FFN_COMP_ONLY, DG_FFN_FUSED_GATE, FFN_PARAM_NAMES, a2a_combine,
+                                      a2a_dispatch, a2a_ffn, a2a_ffn_backward, a2a_ffn_forward, synth)
 from _compare import TOL_BF16, assert_close, err_fro
 
 pytestmark = pytest.mark.gpu
@@ -208,6 +209,14 @@ def test_backward_full_size_subsets():
             got = grads[name][r, l]
             assert_close(got, o[key], TOL_BF16, f"{name}[t={t}]")
             assert err_fro(got, o[key]) <= TOL_BF16, name
+    # the LayerNorm weight/bias gradients of one seeded rank, in full: sums over
+    # its 8 slices x 4096 rows (the row-range partials of every slice reduced)
+    r = int(rng.integers(P))
+    nr = O.ffn_backward_norm_rank(sh, xb, pb, dyb, r)
+    for key, name in (("dnx_w", "nx_w"), ("dnx_b", "nx_b"), ("dng_w", "ng_w"), ("dng_b", "ng_b")):
+        got = grads[name][r]
+        assert_close(got, nr[key], TOL_BF16, f"{name}[rank {r}]")
+        assert err_fro(got, nr[key]) <= TOL_BF16, name
 
 
 def test_backward_full_width_one_row_per_rank():
@@ -243,3 +252,126 @@ def test_shape_sweep_forward_backward(P, B, T, D, k):
         got = grads[name].reshape(r.shape)
         assert_close(got, r, TOL_BF16, f"grad {name} {P,B,T,D,k}")
         assert err_fro(got, r) <= TOL_BF16, name
+
+
+# ------------------------------------------------------------------ normalise-and-gate in GEMM2's producer (DG_FFN_FUSED_GATE)
+
+FOLD_SHAPES = SMALL_SHAPES + [
+    (2, 300, 4, 1280, 2),   # M = 600 (three row tiles, the last ragged), N = 1280 (passes of 512, 512, 256)
+    (2, 128, 2, 1280, 6),   # H = 7680, the full width of the page's default workload
+]
+
+
+@pytest.mark.parametrize("P,B,T,D,k", FOLD_SHAPES)
+def test_fused_gate_equals_separate_pass_bit_for_bit(P, B, T, D, k):
+    # with DG_FFN_FUSED_GATE the producer warps of GEMM2 compute Hl with the same
+    # fp32 operations as the separate pass, so the output, and everything the
+    # forward saves, match exactly
+    inputs, params = _inputs(P, B, T, D, k, seed=91 + D + k, device=DEV)
+    sh = dg._lib.FFNShape(P, B, T, D, k, 1e-5)
+    nbytes = dg._lib.load().dg_a2a_ffn_saved_bytes(__import__("ctypes").byref(sh))
+    sv_sep = torch.zeros(nbytes, dtype=torch.uint8, device=DEV)
+    sv_fused = torch.zeros(nbytes, dtype=torch.uint8, device=DEV)
+    out_sep, _ = a2a_ffn_forward(inputs, params, saved=sv_sep)
+    out_fused, _ = a2a_ffn_forward(inputs, params, saved=sv_fused, flags=DG_FFN_FUSED_GATE)
+    torch.cuda.synchronize()
+    assert torch.equal(out_fused, out_sep)
+    assert torch.equal(sv_fused, sv_sep)
+    # inference (nothing saved; with the fused gate, Hl is never written) gives the same output
+    out_i, none = a2a_ffn_forward(inputs, params, inference=True)
+    assert none is None
+    assert torch.equal(out_i, out_sep)
+    out_if, _ = a2a_ffn_forward(inputs, params, inference=True, flags=DG_FFN_FUSED_GATE)
+    assert torch.equal(out_if, out_sep)
+
+
+# ------------------------------------------------------------------ comp_only
+
+def _swap_rank_slice(x, P):
+    """out[p][b][r*L + l] = x[r][b][p*L + l] (rank and slice block exchanged)."""
+    Pn, B, T, D = x.shape
+    return x.view(P, B, P, T // P, D).permute(2, 1, 0, 3, 4).reshape(P, B, T, D)
+
+
+@pytest.mark.parametrize("P,B,T,D,k", [(2, 4, 16, 128, 2), (4, 3, 16, 136, 3), (1, 5, 16, 128, 6),
+                                       (8, 20, 64, 64, 2)])
+def test_comp_only_forward_backward(P, B, T, D, k):
+    inputs, params = _inputs(P, B, T, D, k, seed=81 + P + D, device="cpu")
+    dY = synth.ffn_grad_output(P, B, T, D, seed=82 + P)
+    xd, pd = inputs.to(DEV), {n: v.to(DEV) for n, v in params.items()}
+    out, saved = a2a_ffn_forward(xd, pd, flags=DG_FFN_COMP_ONLY)
+    grads = a2a_ffn_backward(xd, pd, saved, dY.to(DEV), flags=DG_FFN_COMP_ONLY)
+    torch.cuda.synchronize()
+    xb, pb = _bits(inputs, params)
+    sh = O.FFNShape(P, B, T, D, k)
+    assert_close(out, O.ffn_forward_comp_only(sh, xb, pb), TOL_BF16, f"comp_only forward {P,B,T,D,k}")
+    ref = O.ffn_backward_comp_only(sh, xb, pb, synth.bits(dY))
+    keys = dict(inputs="d_inputs", w1="dw1", b1="db1", wout="dwout", bout="dbout",
+                nx_w="dnx_w", nx_b="dnx_b", ng_w="dng_w", ng_b="dng_b")
+    for name, key in keys.items():
+        r = ref[key]
+        got = grads[name].reshape(r.shape)
+        assert_close(got, r, TOL_BF16, f"comp_only grad {name} {P,B,T,D,k}")
+        assert err_fro(got, r) <= TOL_BF16, name
+    # layout, bit for bit: comp_only is the exchange layer on the rank/slice-swapped input, swapped back
+    out_x, saved_x = a2a_ffn_forward(_swap_rank_slice(xd, P).contiguous(), pd)
+    assert torch.equal(out, _swap_rank_slice(out_x, P))
+    gx = a2a_ffn_backward(_swap_rank_slice(xd, P).contiguous(), pd, saved_x,
+                          _swap_rank_slice(dY.to(DEV), P).contiguous())
+    assert torch.equal(grads["inputs"], _swap_rank_slice(gx["inputs"], P))
+    for n in FFN_PARAM_NAMES:
+        assert torch.equal(grads[n], gx[n]), n
+
+
+# ------------------------------------------------------------------ gradients on request
+
+SUBSETS = [("inputs",), ("w1",), ("b1",), ("wout",), ("bout",), ("wout", "bout"),
+           ("nx_w", "nx_b", "ng_w", "ng_b"), ("ng_b",), ("inputs", "w1", "wout")]
+
+# kernels each gradient needs (the dHl GEMM and the LayerNorm-gate backward for everything built on dZ)
+_DZ = {"ffn_bwd_dhl", "ffn_bwd_ln_rowsum", "ffn_bwd_ln_apply"}
+_KERNELS = {"inputs": _DZ | {"ffn_bwd_dx"}, "w1": _DZ | {"ffn_bwd_dw1"}, "b1": _DZ | {"ffn_bwd_grad_reduce"},
+            "wout": {"ffn_bwd_dwout"}, "bout": {"ffn_bwd_dbout"}}
+for _n in ("nx_w", "nx_b", "ng_w", "ng_b"):
+    _KERNELS[_n] = _DZ | {"ffn_bwd_grad_reduce"}
+
+
+@pytest.mark.parametrize("need", SUBSETS)
+def test_backward_computes_only_what_is_asked(need):
+    P, B, T, D, k = 2, 3, 4, 136, 3
+    inputs, params = _inputs(P, B, T, D, k, seed=61, device=DEV)
+    dY = synth.ffn_grad_output(P, B, T, D, seed=62, device=DEV)
+    _, saved = a2a_ffn_forward(inputs, params)
+    full = a2a_ffn_backward(inputs, params, saved, dY)
+    names = ("inputs",) + FFN_PARAM_NAMES
+    # every gradient buffer the caller owns starts as a sentinel; only the requested ones are passed
+    owned = {n: torch.full_like(full[n], float("nan")) for n in names}
+    grads = {n: (owned[n] if n in need else None) for n in names}
+    dg.trace_begin()
+    a2a_ffn_backward(inputs, params, saved, dY, grads=grads)
+    torch.cuda.synchronize()
+    launched = {e["name"] for e in dg.trace_end()}
+    for n in names:
+        if n in need:
+            assert torch.equal(owned[n], full[n]), n        # the same kernels, the same bits
+        else:
+            assert bool(torch.isnan(owned[n].float()).all()), n
+    expect = set().union(*(_KERNELS[n] for n in need))
+    assert launched == expect, (sorted(launched), sorted(expect))
+
+
+def test_autograd_asks_only_for_the_gradients_it_needs():
+    P, B, T, D, k = 2, 4, 16, 128, 2
+    inputs, params = _inputs(P, B, T, D, k, seed=63, device=DEV)
+    frozen = {n: v.clone() for n, v in params.items()}
+    w1 = params["w1"].clone().requires_grad_(True)
+    frozen["w1"] = w1
+    out = a2a_ffn(inputs, frozen)                  # only w1 needs a gradient
+    dY = synth.ffn_grad_output(P, B, T, D, seed=64, device=DEV)
+    dg.trace_begin()
+    out.backward(dY)
+    torch.cuda.synchronize()
+    launched = {e["name"] for e in dg.trace_end()}
+    assert "ffn_bwd_dx" not in launched and "ffn_bwd_dwout" not in launched and "ffn_bwd_dw1" in launched
+    _, saved = a2a_ffn_forward(inputs, params)
+    assert torch.equal(w1.grad, a2a_ffn_backward(inputs, params, saved, dY)["w1"])

@@ -69,7 +69,7 @@ def test_input_codes_bit_exact():
     ws = torch.zeros(nbytes, dtype=torch.uint8, device=DEV)
     a2a_ffn_forward_fp8(x, params, packed, workspace=ws)
     torch.cuda.synchronize()
-    w = ws.cpu().numpy()
+    w = ws.cpu().numpy()[256:]          # past the error block
     rows = P * B * T
     q, s = O.quantize_e4m3(O.bf16_to_f64(synth.bits(x)).reshape(rows, D), axis=1)
     assert np.array_equal(w[:rows * D].reshape(rows, D), q)

@@ -15,8 +15,8 @@ DEV = torch.device("cuda")
 
 def _step(t):
     out = {}
-    out["D"] = dg.gemm_fp8(t["A"], t["B"], t["C"], 0.5, 1.0, out=t["D"])
-    y, saved = dg.a2a_ffn_forward(t["x"], t["params"], saved=t["saved"], out=t["out"])
+    out["D"] = dg.gemm_fp8(t["A"], t["B"], t["C"], 0.5, 1.0, out=t["D"], ws=t["err"])
+    y, saved = dg.a2a_ffn_forward(t["x"], t["params"], saved=t["saved"], out=t["out"], ws=t["err"])
     g = dg.a2a_ffn_backward(t["x"], t["params"], t["saved"], t["dY"], workspace=t["ws"], grads=t["grads"])
     dg.tp_swiglu(t["xs"], t["w13"], t["w2"], workspace=t["tp_ws"], out=t["y"])
     dg.tp_swiglu_backward(t["xs"], t["w13"], t["w2"], t["tp_dy"], workspace=t["tp_bws"], grads=t["tp_grads"])
@@ -38,13 +38,13 @@ def _tensors():
              x=f["inputs"], params=params, dY=synth.ffn_grad_output(P, B, T, D, seed=9, device=DEV),
              out=torch.empty_like(f["inputs"]),
              saved=torch.empty(lib.dg_a2a_ffn_saved_bytes(ctypes.byref(sh)), dtype=torch.uint8, device=DEV),
-             ws=torch.empty(lib.dg_a2a_ffn_bwd_workspace_bytes(ctypes.byref(sh)), dtype=torch.uint8, device=DEV),
+             ws=dg.alloc_workspace(lib.dg_a2a_ffn_bwd_workspace_bytes(ctypes.byref(sh), 0), DEV),
              grads={**{n: torch.empty_like(v) for n, v in params.items()}, "inputs": torch.empty_like(f["inputs"])},
              xs=xs, w13=w13, w2=w2, y=torch.empty_like(xs),
-             tp_ws=torch.empty(lib.dg_tp_swiglu_workspace_bytes(256, 128, 512, 4, 1), dtype=torch.uint8, device=DEV),
+             tp_ws=dg.alloc_workspace(lib.dg_tp_swiglu_workspace_bytes(256, 128, 512, 4, 1), DEV),
              tp_dy=torch.randn(xs.shape, generator=g, device=DEV).to(torch.bfloat16),
-             tp_bws=torch.empty(lib.dg_tp_swiglu_bwd_workspace_bytes(256, 128, 512, 4, 1), dtype=torch.uint8,
-                                device=DEV),
+             tp_bws=dg.alloc_workspace(lib.dg_tp_swiglu_bwd_workspace_bytes(256, 128, 512, 4, 1), DEV),
+             err=dg.alloc_workspace(256, DEV),
              tp_grads=dict(x=torch.empty_like(xs), w13=torch.empty_like(w13), w2=torch.empty_like(w2)),
              wq=(torch.randn((384, 128), generator=g, device=DEV) / 12).to(torch.bfloat16),
              bq=torch.randn((384,), generator=g, device=DEV).to(torch.bfloat16))
@@ -83,5 +83,6 @@ def test_captured_step_replays_bit_identical():
     eager = _results(t)
     for name in eager:
         assert torch.equal(replayed[name], eager[name]), name
-    st, code = dg.device_status()
-    assert st == 0, hex(code)
+    for ws in (t["err"], t["ws"], t["tp_ws"], t["tp_bws"]):
+        st, code = dg.device_status(workspace=ws)
+        assert st == 0, hex(code)

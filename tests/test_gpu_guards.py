@@ -36,6 +36,12 @@ class Guarded:
         self.bufs.append((buf, nbytes))
         return buf[PAD:PAD + nbytes]
 
+    def workspace(self, nbytes: int) -> torch.Tensor:
+        """A guarded workspace whose error block (the first 256 bytes) is zero."""
+        ws = self.raw(max(nbytes, 256))
+        ws[:256].zero_()
+        return ws
+
     def tensor(self, shape, dtype) -> torch.Tensor:
         n = 1
         for s in shape:
@@ -67,7 +73,7 @@ def test_gemm_fp8_writes_only_d(M, N, K, beta):
     A, B, C = synth.fp8_gemm_inputs(M, N, K, seed=M + N + K, device=DEV)
     g = Guarded()
     D = g.tensor((M, N), torch.bfloat16)
-    dg.gemm_fp8(A, B, C if beta != 0.0 else None, 0.5, beta, out=D)
+    dg.gemm_fp8(A, B, C if beta != 0.0 else None, 0.5, beta, out=D, ws=g.workspace(256))
     g.check(f"gemm_fp8 {M}x{N}x{K}")
     assert torch.isfinite(D.float()).all()
 
@@ -83,8 +89,8 @@ def test_a2a_ffn_forward_backward_write_only_their_buffers(P, B, T, D, k):
     g = Guarded()
     out = g.like(x)
     saved = g.raw(lib.dg_a2a_ffn_saved_bytes(ctypes.byref(sh)))
-    dg.a2a_ffn_forward(x, params, saved=saved, out=out)
-    ws = g.raw(max(lib.dg_a2a_ffn_bwd_workspace_bytes(ctypes.byref(sh)), 1))
+    dg.a2a_ffn_forward(x, params, saved=saved, out=out, ws=g.workspace(256))
+    ws = g.workspace(lib.dg_a2a_ffn_bwd_workspace_bytes(ctypes.byref(sh), 0))
     grads = {"inputs": g.like(x)}
     grads.update({n: g.like(params[n]) for n in dg.FFN_PARAM_NAMES})
     dg.a2a_ffn_backward(x, params, saved, dY, workspace=ws, grads=grads)
@@ -101,7 +107,7 @@ def test_a2a_ffn_fp8_forward_writes_only_its_buffers(P, B, T, D, k):
     g = Guarded()
     packed = g.raw(lib.dg_a2a_ffn_fp8_weights_bytes(ctypes.byref(sh)))
     dg.a2a_ffn_fp8_pack_weights(params, P, B, T, D, packed=packed)
-    ws = g.raw(lib.dg_a2a_ffn_fp8_workspace_bytes(ctypes.byref(sh)))
+    ws = g.workspace(lib.dg_a2a_ffn_fp8_workspace_bytes(ctypes.byref(sh)))
     out = g.like(x)
     dg.a2a_ffn_forward_fp8(x, params, packed, workspace=ws, out=out)
     g.check(f"a2a_ffn_fp8 {P, B, T, D, k}")
@@ -128,10 +134,10 @@ def test_tp_swiglu_forward_backward_write_only_their_buffers(S, d, ffn, W, bsz):
     dy = synth.tp_swiglu_inputs(S, d, ffn, W, bsz=bsz, seed=S + d + 1, device=DEV)[0]
     lib = _lib.load()
     g = Guarded()
-    ws = g.raw(max(lib.dg_tp_swiglu_workspace_bytes(S, d, ffn, W, bsz), 1))
+    ws = g.workspace(lib.dg_tp_swiglu_workspace_bytes(S, d, ffn, W, bsz))
     y = g.like(xs)
     dg.tp_swiglu(xs, w13, w2, workspace=ws, out=y)
-    bws = g.raw(max(lib.dg_tp_swiglu_bwd_workspace_bytes(S, d, ffn, W, bsz), 1))
+    bws = g.workspace(lib.dg_tp_swiglu_bwd_workspace_bytes(S, d, ffn, W, bsz))
     grads = dict(x=g.like(xs), w13=g.like(w13), w2=g.like(w2))
     dg.tp_swiglu_backward(xs, w13, w2, dy, workspace=bws, grads=grads)
     g.check(f"tp_swiglu {S, d, ffn, W, bsz}")
@@ -151,7 +157,34 @@ def test_tp_linear_forward_backward_write_only_their_outputs(rows, fin, fout):
     dg.tp_linear(x, w, b, out=y)
     dx, dw, db = g.like(x), g.like(w), g.like(b)
     p = lambda t: ctypes.c_void_p(t.data_ptr())
-    st = lib.dg_tp_linear_bwd(rows, fin, fout, p(x), p(w), p(dy), p(dx), p(dw), p(db),
+    ws = g.workspace(256)
+    st = lib.dg_tp_linear_bwd(rows, fin, fout, p(x), p(w), p(dy), p(dx), p(dw), p(db), p(ws), 256,
                               ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
     assert st == 0, lib.dg_last_error()
     g.check(f"tp_linear {rows, fin, fout}")
+
+
+@pytest.mark.parametrize("P,B,T,D,k", [(2, 4, 16, 128, 2), (2, 3, 4, 136, 3), (4, 40, 16, 64, 2)])
+@pytest.mark.parametrize("flags", [0, dg.DG_FFN_COMP_ONLY, dg.DG_FFN_FUSED_GATE,
+                                   dg.DG_FFN_COMP_ONLY | dg.DG_FFN_FUSED_GATE])
+def test_a2a_ffn_inference_and_comp_only_write_only_their_buffers(P, B, T, D, k, flags):
+    t = synth.ffn_inputs(P, B, T, D, k, seed=P + B + T + D + k + 1, device=DEV)
+    params = {n: t[n] for n in dg.FFN_PARAM_NAMES}
+    x = t["inputs"]
+    lib = _lib.load()
+    sh = _lib.FFNShape(P, B, T, D, k, 1e-5)
+    g = Guarded()
+    out = g.like(x)
+    ws = g.workspace(lib.dg_a2a_ffn_fwd_workspace_bytes(ctypes.byref(sh), 1, flags))
+    dg.a2a_ffn_forward(x, params, out=out, inference=True, flags=flags, ws=ws)
+    g.check(f"a2a_ffn inference {P, B, T, D, k} flags={flags}")
+    if flags & dg.DG_FFN_COMP_ONLY:
+        saved = g.raw(lib.dg_a2a_ffn_saved_bytes(ctypes.byref(sh)))
+        fws = g.workspace(lib.dg_a2a_ffn_fwd_workspace_bytes(ctypes.byref(sh), 0, flags))
+        dg.a2a_ffn_forward(x, params, saved=saved, out=g.like(x), flags=flags, ws=fws)
+        dY = synth.ffn_grad_output(P, B, T, D, seed=8, device=DEV)
+        bws = g.workspace(lib.dg_a2a_ffn_bwd_workspace_bytes(ctypes.byref(sh), dg.DG_FFN_COMP_ONLY))
+        grads = {"inputs": g.like(x)}
+        grads.update({n: g.like(params[n]) for n in dg.FFN_PARAM_NAMES})
+        dg.a2a_ffn_backward(x, params, saved, dY, workspace=bws, grads=grads, flags=dg.DG_FFN_COMP_ONLY)
+        g.check(f"a2a_ffn comp_only backward {P, B, T, D, k}")

@@ -365,6 +365,149 @@ def test_ffn_backward_subset_functions_match_full():
         assert np.allclose(nr[key], full[key][1], rtol=1e-12, atol=1e-12), key
 
 
+def test_ffn_norm_rank_helper_matches_full_backward():
+    # the norm-only helper behind ffn_backward_norm_rank against the full backward of each problem
+    sh = O.FFNShape(4, 2, 16, 8, 3)
+    _, b = _ffn_bits(sh, seed=61)
+    dY = synth.bits(synth.ffn_grad_output(sh.P, sh.B, sh.T, sh.D, seed=62))
+    full = O.ffn_backward(sh, b["inputs"], b, dY)
+    for r in (0, 3):
+        nr = O.ffn_backward_norm_rank(sh, b["inputs"], b, dY, r)
+        for key in ("dnx_w", "dnx_b", "dng_w", "dng_b"):
+            assert np.allclose(nr[key], full[key][r], rtol=1e-12, atol=1e-12), key
+
+
+# --------------------------------------------------------------------------
+# comp_only (no exchange)
+# --------------------------------------------------------------------------
+
+def test_comp_only_is_the_layer_when_one_rank():
+    # with P = 1 both exchanges are the identity, so both modes are the same map
+    sh = O.FFNShape(1, 3, 8, 8, 2)
+    _, b = _ffn_bits(sh, seed=71)
+    dY = synth.bits(synth.ffn_grad_output(sh.P, sh.B, sh.T, sh.D, seed=72))
+    assert np.array_equal(O.ffn_forward_comp_only(sh, b["inputs"], b), O.ffn_forward(sh, b["inputs"], b))
+    g1, g2 = O.ffn_backward_comp_only(sh, b["inputs"], b, dY), O.ffn_backward(sh, b["inputs"], b, dY)
+    for key in g2:
+        assert np.array_equal(g1[key], g2[key]), key
+
+
+def test_comp_only_closed_form_uses_own_rank_and_slice():
+    # constant halves (as in the exchange closed form): output row (r, b, t) is
+    # silu(c) * colsum(wout[r, t % L]) + bout[r, t % L] -- rank r's own problem
+    sh = O.FFNShape(2, 3, 8, 8, 2)
+    t, _ = _ffn_bits(sh, seed=73)
+    H = sh.H
+    t["w1"].zero_()
+    t["b1"][..., :H] = 0.5
+    t["b1"][..., H:] = 2.0
+    t["nx_b"].fill_(1.0)
+    c = -0.875
+    t["ng_b"].fill_(c)
+    b = {k: synth.bits(v) for k, v in t.items()}
+    out = O.ffn_forward_comp_only(sh, b["inputs"], b)
+    silu_c = c / (1.0 + math.exp(-c))
+    wout = O.bf16_to_f64(b["wout"]).reshape(sh.P, sh.L, H, sh.D)
+    bout = O.bf16_to_f64(b["bout"]).reshape(sh.P, sh.L, sh.D)
+    for r, bb, tt in itertools.product(range(sh.P), range(sh.B), range(sh.T)):
+        l = tt % sh.L
+        expect = silu_c * wout[r, l].sum(axis=0) + bout[r, l]
+        assert np.allclose(out[r, bb, tt], expect, rtol=1e-13, atol=1e-13)
+
+
+def test_comp_only_forward_brute_force_scalar_loops():
+    sh = O.FFNShape(2, 2, 4, 4, 1)     # H = 4, L = 2
+    _, b = _ffn_bits(sh, seed=74)
+    f = {k: O.bf16_to_f64(v) for k, v in b.items()}
+    P, B, T, D, H, L = sh.P, sh.B, sh.T, sh.D, sh.H, sh.L
+    x = f["inputs"].reshape(P, B, T, D)
+    w1, b1 = f["w1"].reshape(P, L, D, 2 * H), f["b1"].reshape(P, L, 2 * H)
+    wo, bo = f["wout"].reshape(P, L, H, D), f["bout"].reshape(P, L, D)
+    out = O.ffn_forward_comp_only(sh, b["inputs"], b)
+    for r in range(P):
+        for bb in range(B):
+            for tt in range(T):
+                l = tt % L                       # slice of token tt = p*L + l in the [B, P, L, D] view
+                xin = [float(v) for v in x[r, bb, tt]]
+                z = [sum(xin[d] * w1[r, l, d, j] for d in range(D)) + b1[r, l, j] for j in range(2 * H)]
+
+                def ln(v, gam, bet):
+                    m = sum(v) / len(v)
+                    var = sum((vi - m) ** 2 for vi in v) / len(v)
+                    return [(vi - m) / math.sqrt(var + 1e-5) * gam[i] + bet[i] for i, vi in enumerate(v)]
+                a = ln(z[:H], f["nx_w"].reshape(P, H)[r], f["nx_b"].reshape(P, H)[r])
+                g = ln(z[H:], f["ng_w"].reshape(P, H)[r], f["ng_b"].reshape(P, H)[r])
+                h = [a[i] * (g[i] / (1.0 + math.exp(-g[i]))) for i in range(H)]
+                y = [sum(h[i] * wo[r, l, i, e] for i in range(H)) + bo[r, l, e] for e in range(D)]
+                assert np.allclose(out[r, bb, tt], y, rtol=1e-12, atol=1e-12)
+
+
+def _torch_ffn_comp_only(sh, f64):
+    """Independent float64 formulation of comp_only: torch view/reshape, bmm, F.layer_norm, F.silu."""
+    P, B, T, D, H, L = sh.P, sh.B, sh.T, sh.D, sh.H, sh.L
+    outs = []
+    for r in range(P):
+        Xr = f64["inputs"][r].view(B, P, L, D).reshape(B * P, L, D)
+        Z = torch.bmm(Xr.transpose(0, 1), f64["w1"][r]) + f64["b1"][r][:, None, :]
+        U, G = torch.chunk(Z, 2, dim=-1)
+        a = F.layer_norm(U, (H,), f64["nx_w"][r], f64["nx_b"][r], eps=sh.eps)
+        s_ = F.layer_norm(G, (H,), f64["ng_w"][r], f64["ng_b"][r], eps=sh.eps)
+        Y = torch.bmm(a * F.silu(s_), f64["wout"][r]) + f64["bout"][r][:, None, :]
+        outs.append(Y.transpose(0, 1).reshape(B, P, L, D).reshape(B, T, D))
+    return torch.stack(outs)
+
+
+def test_comp_only_matches_torch_formulation_and_autograd():
+    sh = O.FFNShape(4, 2, 16, 8, 2)
+    _, b = _ffn_bits(sh, seed=75)
+    t = _f64_tensors(sh, b)
+    for v in t.values():
+        v.requires_grad_(True)
+    out = _torch_ffn_comp_only(sh, t)
+    assert np.allclose(O.ffn_forward_comp_only(sh, b["inputs"], b), out.detach().numpy(), rtol=1e-11, atol=1e-11)
+    dY = torch.randn(out.shape, dtype=torch.float64, generator=torch.Generator().manual_seed(76))
+    out.backward(dY)
+    prm = dict(w1=t["w1"].detach().numpy(), b1=t["b1"].detach().numpy(), wout=t["wout"].detach().numpy(),
+               bout=t["bout"].detach().numpy(), nxw=t["nx_w"].detach().numpy(), nxb=t["nx_b"].detach().numpy(),
+               ngw=t["ng_w"].detach().numpy(), ngb=t["ng_b"].detach().numpy())
+    g = O.ffn_backward_comp_only(sh, t["inputs"].detach().numpy(), prm, dY.numpy(), decoded=True)
+    pairs = dict(inputs="d_inputs", w1="dw1", b1="db1", wout="dwout", bout="dbout",
+                 nx_w="dnx_w", nx_b="dnx_b", ng_w="dng_w", ng_b="dng_b")
+    for key, gkey in pairs.items():
+        assert np.allclose(g[gkey], t[key].grad.numpy(), rtol=1e-10, atol=1e-10), key
+
+
+def test_comp_only_backward_finite_differences():
+    sh = O.FFNShape(2, 1, 4, 4, 1)
+    _, b = _ffn_bits(sh, seed=77)
+    f = {k: v.numpy().copy() for k, v in _f64_tensors(sh, b).items()}
+    dY = np.random.default_rng(78).standard_normal(f["inputs"].shape)
+
+    def params(ff):
+        return dict(w1=ff["w1"], b1=ff["b1"], wout=ff["wout"], bout=ff["bout"],
+                    nxw=ff["nx_w"], nxb=ff["nx_b"], ngw=ff["ng_w"], ngb=ff["ng_b"])
+
+    def loss(ff):
+        return float((O.ffn_forward_comp_only(sh, ff["inputs"], params(ff), decoded=True) * dY).sum())
+
+    g = O.ffn_backward_comp_only(sh, f["inputs"], params(f), dY, decoded=True)
+    names = dict(inputs="d_inputs", w1="dw1", b1="db1", wout="dwout", bout="dbout",
+                 nx_w="dnx_w", nx_b="dnx_b", ng_w="dng_w", ng_b="dng_b")
+    h = 1e-6
+    for key, gkey in names.items():
+        flat = f[key].reshape(-1)
+        ana = g[gkey].reshape(-1)
+        for i in range(flat.size):
+            old = flat[i]
+            flat[i] = old + h
+            lp = loss(f)
+            flat[i] = old - h
+            lm = loss(f)
+            flat[i] = old
+            num = (lp - lm) / (2 * h)
+            assert abs(num - ana[i]) <= 1e-6 * max(1.0, abs(num)), (key, i, num, ana[i])
+
+
 # --------------------------------------------------------------------------
 # TP SwiGLU
 # --------------------------------------------------------------------------
