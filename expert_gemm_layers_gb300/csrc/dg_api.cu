@@ -317,10 +317,10 @@ SavedLayout saved_layout(const FfnDims& f) {
 
 // Carving of the backward's workspace: the error block, then
 // (DG_FFN_COMP_ONLY) the rank/slice-swapped inputs, dY and d_inputs, then
-// dHl [T,M,H] bf16, dZ [T,M,2H] bf16, rowsum [T,M] float4 and the column
-// partials [T,nsplit,6,H] fp32.
+// dHl [T,M,H] bf16, dZ [T,M,2H] bf16, the per-row coefficient records
+// [T,M] x 32 bytes and the column partials [T,nsplit,6,H] fp32.
 struct BwdLayout {
-  size_t perm_x, perm_dy, perm_dx, dhl, dz, rowsum, part, total;
+  size_t perm_x, perm_dy, perm_dx, dhl, dz, rowcoef, part, total;
   int nsplit;
 };
 BwdLayout bwd_layout(const FfnDims& f, uint32_t flags) {
@@ -339,8 +339,8 @@ BwdLayout bwd_layout(const FfnDims& f, uint32_t flags) {
   }
   l.dhl = off;
   l.dz = round_up(l.dhl + rows * f.H * 2, 256);
-  l.rowsum = round_up(l.dz + rows * 2 * f.H * 2, 256);
-  l.part = round_up(l.rowsum + rows * 16, 256);
+  l.rowcoef = round_up(l.dz + rows * 2 * f.H * 2, 256);
+  l.part = round_up(l.rowcoef + rows * 32, 256);
   l.total = round_up(l.part + static_cast<size_t>(f.T) * l.nsplit * 6 * f.H * 4, 256);
   return l;
 }
@@ -765,7 +765,7 @@ dg_status dg_a2a_ffn_bwd(const dg_ffn_shape* shape, const void* inputs, const vo
   uint8_t* w = static_cast<uint8_t*>(ws);
   void* dHl = w + bl.dhl;
   void* dZ = w + bl.dz;
-  void* rowsum = w + bl.rowsum;
+  void* rowcoef = w + bl.rowcoef;
   float* part = reinterpret_cast<float*>(w + bl.part);
   const uint64_t T = f.T, M = f.M, D = f.D, H = f.H;
   const double rows = static_cast<double>(T) * M;
@@ -846,8 +846,8 @@ dg_status dg_a2a_ffn_bwd(const dg_ffn_shape* shape, const void* inputs, const vo
   if (need_dz) {
     // (4) gate + LayerNorm backward: per-row sums, then dZ with db1 and the norm column sums
     {
-      TraceScope trace("ffn_bwd_ln_rowsum", s, 0.0, rows * (2.0 * 2 * H + 2.0 * H + 32.0));
-      e = launch_ln_gate_bwd_rowsum(Z, stats, dHl, nx_w, nx_b, ng_w, ng_b, rowsum, static_cast<int>(T),
+      TraceScope trace("ffn_bwd_ln_rowsum", s, 0.0, rows * (2.0 * 2 * H + 2.0 * H + 16.0 + 32.0));
+      e = launch_ln_gate_bwd_rowsum(Z, stats, dHl, nx_w, nx_b, ng_w, ng_b, rowcoef, static_cast<int>(T),
                                     static_cast<int>(M), static_cast<int>(f.L), static_cast<int>(H), dev, s);
     }
     if (e != cudaSuccess) return cuda_fail(e, "LayerNorm-gate backward (row sums) launch");
@@ -855,7 +855,7 @@ dg_status dg_a2a_ffn_bwd(const dg_ffn_shape* shape, const void* inputs, const vo
       TraceScope trace("ffn_bwd_ln_apply", s, 0.0,
                        rows * (2.0 * 2 * H + 2.0 * H + 32.0 + 2.0 * 2 * H) +
                            static_cast<double>(T) * bl.nsplit * 6 * H * 4);
-      e = launch_ln_gate_bwd_apply(Z, stats, rowsum, dHl, nx_w, nx_b, ng_w, ng_b, dZ, part, static_cast<int>(T),
+      e = launch_ln_gate_bwd_apply(Z, rowcoef, dHl, nx_w, nx_b, ng_w, ng_b, dZ, part, static_cast<int>(T),
                                    static_cast<int>(M), static_cast<int>(f.L), static_cast<int>(H), bl.nsplit, dev, s);
     }
     if (e != cudaSuccess) return cuda_fail(e, "LayerNorm-gate backward (apply) launch");

@@ -69,6 +69,39 @@ static __device__ __forceinline__ GatePair gate_pair(float2 u, float2 g, float2 
 }
 
 
+// The same quantities with the gate norm's affine pre-halved (wg2 = gg/2,
+// cg2 = bg/2), so that h = s/2 comes out of one fma.  With t = tanh(h):
+// q = silu(s) = h*(1 + t), and silu'(s) = sig*(1 + s*(1 - sig)) with
+// sig = (1 + t)/2 gives dsil2 = 2*silu'(s) = (1 + t)*w, w = 1 + 2h - q.
+// Callers use dsil2 with the halved gg, so d*a*dsil2*wg2 = d*a*silu'(s)*gg.
+struct GatePairH {
+  float2 xu, xg, a, q, dsil2;
+};
+
+static __device__ __forceinline__ GatePairH gate_pair_h(float2 u, float2 g, float2 rsu, float2 cu, float2 rsg,
+                                                       float2 cg_, float2 wx, float2 cx, float2 wg2, float2 cg2) {
+  GatePairH r;
+  r.xu = fma2(u, rsu, cu);
+  r.xg = fma2(g, rsg, cg_);
+  r.a = fma2(r.xu, wx, cx);
+  const float2 h = fma2(r.xg, wg2, cg2);
+  const float2 t = make_float2(tanh_fast(h.x), tanh_fast(h.y));
+  r.q = fma2(h, t, h);
+  const float2 w = fma2(r.q, splat2(-1.0f), fma2(h, splat2(2.0f), splat2(1.0f)));
+  r.dsil2 = fma2(t, w, w);
+  return r;
+}
+
+// Per-row coefficients of the backward, stored by the row-sum pass as two
+// float4: (rstd_u, -mean_u*rstd_u, rstd_g, -mean_g*rstd_g) and
+// (-mean(dx_u), -mean(dx_u*x_u), -mean(dx_g), -mean(dx_g*x_g)), the means
+// over the row's H columns.
+static __device__ __forceinline__ void store_row_coef(float4* rc, float4 stats, float4 sums, float inv_h) {
+  rc[0] = make_float4(stats.y, -stats.x * stats.y, stats.w, -stats.z * stats.w);
+  rc[1] = make_float4(-sums.x * inv_h, -sums.y * inv_h, -sums.z * inv_h, -sums.w * inv_h);
+}
+
+
 // bf16x2-packed affine parameters of one 8-column vector (held for all rows).
 struct Affine8 {
   uint4 wx, cx, wg, cg;
@@ -103,6 +136,15 @@ static __device__ __forceinline__ AffineF load_affine_f(const __nv_bfloat16* gx,
     f.cg[e] = unpack_bf16x2(w3[e]);
   }
   return f;
+}
+
+// The gate norm's affine halved (exact), for gate_pair_h.
+static __device__ __forceinline__ void halve_gate_affine(AffineF& f) {
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    f.wg[e] = mul2(f.wg[e], splat2(0.5f));
+    f.cg[e] = mul2(f.cg[e], splat2(0.5f));
+  }
 }
 
 }  // namespace dg

@@ -301,18 +301,19 @@ cudaError_t launch_quant_weight(const void* w, float* scale, float* inv, void* q
                                 const DeviceInfo& dev, cudaStream_t s);
 
 
-// Backward of the gate and both LayerNorms, pass 1: per-row sums
-// rowsum[row] = (sum dx_u, sum dx_u*x_u, sum dx_g, sum dx_g*x_g), one warp per row.
+// Backward of the gate and both LayerNorms, pass 1: per row, the sums of
+// dx_u, dx_u*x_u, dx_g and dx_g*x_g over its H columns, stored with the row's
+// statistics as a coefficient record rc[2*row], rc[2*row+1] (two float4: see
+// store_row_coef).
 cudaError_t launch_ln_gate_bwd_rowsum(const void* Z, const void* stats, const void* dHl, const void* nx_w,
-                                      const void* nx_b, const void* ng_w, const void* ng_b, void* rowsum, int T, int M,
+                                      const void* nx_b, const void* ng_w, const void* ng_b, void* rc, int T, int M,
                                       int L, int H, const DeviceInfo& dev, cudaStream_t s);
 
-// Pass 2: dZ [rows, 2H] and per-(t, row range) column partial sums
-// part [T, nsplit, 6, H] fp32 (dU, dG, da*x_u, da, ds*x_g, ds).
-cudaError_t launch_ln_gate_bwd_apply(const void* Z, const void* stats, const void* rowsum, const void* dHl,
-                                     const void* nx_w, const void* nx_b, const void* ng_w, const void* ng_b, void* dZ,
-                                     float* part, int T, int M, int L, int H, int nsplit, const DeviceInfo& dev,
-                                     cudaStream_t s);
+// Pass 2: dZ [rows, 2H] from the records and per-(t, row range) column partial
+// sums part [T, nsplit, 6, H] fp32 (dU, dG, da*x_u, da, ds*x_g, ds).
+cudaError_t launch_ln_gate_bwd_apply(const void* Z, const void* rc, const void* dHl, const void* nx_w,
+                                     const void* nx_b, const void* ng_w, const void* ng_b, void* dZ, float* part, int T,
+                                     int M, int L, int H, int nsplit, const DeviceInfo& dev, cudaStream_t s);
 
 // Row ranges per token position used by pass 2.
 int ffn_bwd_row_splits(int T, int M, int H);

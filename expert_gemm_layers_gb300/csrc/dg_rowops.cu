@@ -396,10 +396,11 @@ constexpr int kRowsumThreads = 256;
 __global__ void __launch_bounds__(kRowsumThreads, 2) ln_gate_bwd_rowsum_kernel(
     const __nv_bfloat16* __restrict__ Z, const float4* __restrict__ stats, const __nv_bfloat16* __restrict__ dHl,
     const __nv_bfloat16* __restrict__ gx, const __nv_bfloat16* __restrict__ bx, const __nv_bfloat16* __restrict__ gg,
-    const __nv_bfloat16* __restrict__ bg, float4* __restrict__ rowsum, int64_t rows, int M, int L, int H,
+    const __nv_bfloat16* __restrict__ bg, float4* __restrict__ rc, int64_t rows, int M, int L, int H,
     const uint32_t* err) {
   griddep_wait();
   if (warp_aborted(err)) return;
+  const float inv_h = 1.0f / static_cast<float>(H);
   const int lane = threadIdx.x & 31;
   const int64_t warps = static_cast<int64_t>(gridDim.x) * (kRowsumThreads / 32);
   const int64_t zstride = 2 * static_cast<int64_t>(H);
@@ -439,7 +440,7 @@ __global__ void __launch_bounds__(kRowsumThreads, 2) ln_gate_bwd_rowsum_kernel(
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) acc[i] += __shfl_xor_sync(0xffffffffu, acc[i], o);
     }
-    if (lane == 0) rowsum[row] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    if (lane == 0) store_row_coef(rc + 2 * row, sr, make_float4(acc[0], acc[1], acc[2], acc[3]), inv_h);
   }
 }
 
@@ -449,9 +450,9 @@ __global__ void __launch_bounds__(kRowsumThreads, 2) ln_gate_bwd_rowsum_kernel(
 // consumer warps each take every fifteenth 8-column vector of the row (two
 // vectors a thread, their affines held in fp32 registers) and publish per-warp
 // partial sums; when the producer recycles a slot it adds the warps' partials
-// in a fixed order and writes the row's four sums.  Each CTA takes a
-// contiguous range of rows (so the rank, and with it the affines, change at
-// most a few times).
+// in a fixed order and writes the row's coefficient record (store_row_coef).
+// Each CTA takes a contiguous range of rows (so the rank, and with it the
+// affines, change at most a few times).
 constexpr int kRsRing = 4;
 // Sixteen warps in all: four per SM sub-partition leave 128 registers a thread.
 constexpr int kRsConsumers = 15;
@@ -462,7 +463,7 @@ constexpr int kRsThreads = 32 * (kRsConsumers + 1);
 __global__ void __launch_bounds__(kRsThreads, 1) ln_gate_bwd_rowsum_bulk_kernel(
     const __nv_bfloat16* __restrict__ Z, const float4* __restrict__ stats, const __nv_bfloat16* __restrict__ dHl,
     const __nv_bfloat16* __restrict__ gx, const __nv_bfloat16* __restrict__ bx, const __nv_bfloat16* __restrict__ gg,
-    const __nv_bfloat16* __restrict__ bg, float4* __restrict__ rowsum, int64_t rows, int M, int L, int H,
+    const __nv_bfloat16* __restrict__ bg, float4* __restrict__ rc, int64_t rows, int M, int L, int H,
     int slot_bytes, uint32_t* err) {
   extern __shared__ __align__(128) uint8_t rs_smem[];
   float4* part = reinterpret_cast<float4*>(rs_smem + kRsRing * slot_bytes);  // [kRsRing][kRsConsumers]
@@ -472,7 +473,7 @@ __global__ void __launch_bounds__(kRsThreads, 1) ln_gate_bwd_rowsum_bulk_kernel(
   if (threadIdx.x == 0) {
     for (int s = 0; s < kRsRing; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 4 * kRsConsumers);  // four publishing lanes per consumer warp
+      mbar_init(&empty[s], kRsConsumers);  // one release per consumer warp
     }
     fence_mbar_init();
   }
@@ -483,11 +484,14 @@ __global__ void __launch_bounds__(kRsThreads, 1) ln_gate_bwd_rowsum_bulk_kernel(
   const int n = static_cast<int>(min(rows, r0 + per) - r0);
   const uint32_t zbytes = 4u * H, hbytes = 2u * H;
   const int nvec = H >> 3;
+  const float inv_h = 1.0f / static_cast<float>(H);
 
   if (warp == kRsConsumers) {
     // ---------------------------------------------------------------- producer
     if (lane == 0) {
-      auto finish = [&](int i) {  // the row's four sums from the warps' partials, in warp order
+      // the row's four sums from the warps' partials, in warp order, and its
+      // record; the slot still holds the row's statistics
+      auto finish = [&](int i) {
         const float4* pp = part + (i % kRsRing) * kRsConsumers;
         float4 a = pp[0];
         for (int w = 1; w < kRsConsumers; ++w) {
@@ -496,7 +500,8 @@ __global__ void __launch_bounds__(kRsThreads, 1) ln_gate_bwd_rowsum_bulk_kernel(
           a.z += pp[w].z;
           a.w += pp[w].w;
         }
-        rowsum[r0 + i] = a;
+        const float4 sr = *reinterpret_cast<const float4*>(rs_smem + (i % kRsRing) * slot_bytes + zbytes + hbytes);
+        store_row_coef(rc + 2 * (r0 + i), sr, a, inv_h);
       };
       bool ok = true;
       int issued = 0;
@@ -533,9 +538,10 @@ __global__ void __launch_bounds__(kRsThreads, 1) ln_gate_bwd_rowsum_bulk_kernel(
     }
   } else {
     // ---------------------------------------------------------------- consumers
-    // position of the current row: rank, token position within the rank, row within the token position
-    const int t0 = static_cast<int>(r0 / M);
-    int nt = static_cast<int>(r0 - static_cast<int64_t>(t0) * M), rank = t0 / L, tl = t0 - rank * L;
+    // rank of the current row, and the local index of the first row of the next rank
+    const int64_t rank_rows = static_cast<int64_t>(L) * M;
+    int rank = static_cast<int>(r0 / rank_rows);
+    int next_rank_at = static_cast<int>(min(static_cast<int64_t>(n), (rank + 1) * rank_rows - r0));
     bool reload = true;
     AffineF af[kRsVec];
     float* pf = reinterpret_cast<float*>(part);
@@ -545,12 +551,20 @@ __global__ void __launch_bounds__(kRsThreads, 1) ln_gate_bwd_rowsum_bulk_kernel(
       const int s = i % kRsRing;
       const bool ok = mbar_wait(&full[s], static_cast<uint32_t>(i / kRsRing) & 1u, err, 0x53u);
       if (!__all_sync(0xffffffffu, ok)) break;
+      if (i == next_rank_at) {
+        ++rank;
+        next_rank_at = static_cast<int>(min(static_cast<int64_t>(n), next_rank_at + rank_rows));
+        reload = true;
+      }
       if (reload) {
         reload = false;
 #pragma unroll
         for (int j = 0; j < kRsVec; ++j) {
           const int v = warp * 32 + lane + 32 * kRsConsumers * j;
-          if (v < nvec) af[j] = load_affine_f(gx, bx, gg, bg, static_cast<int64_t>(rank) * H + 8 * v);
+          if (v < nvec) {
+            af[j] = load_affine_f(gx, bx, gg, bg, static_cast<int64_t>(rank) * H + 8 * v);
+            halve_gate_affine(af[j]);
+          }
         }
       }
       const uint8_t* slot = rs_smem + s * slot_bytes;
@@ -568,12 +582,12 @@ __global__ void __launch_bounds__(kRsThreads, 1) ln_gate_bwd_rowsum_bulk_kernel(
           const uint32_t hw[4] = {ph.x, ph.y, ph.z, ph.w};
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            const float2 wx = af[j].wx[e], wg = af[j].wg[e];
-            const GatePair gp = gate_pair(unpack_bf16x2(uw[e]), unpack_bf16x2(gw[e]), rsu, cu, rsg, cgs, wx,
-                                          af[j].cx[e], wg, af[j].cg[e]);
+            const float2 wx = af[j].wx[e], wg2 = af[j].wg[e];
+            const GatePairH gp = gate_pair_h(unpack_bf16x2(uw[e]), unpack_bf16x2(gw[e]), rsu, cu, rsg, cgs, wx,
+                                             af[j].cx[e], wg2, af[j].cg[e]);
             const float2 d = unpack_bf16x2(hw[e]);
             const float2 dxu = mul2(mul2(d, gp.q), wx);
-            const float2 dxg = mul2(mul2(mul2(d, gp.a), gp.dsil), wg);
+            const float2 dxg = mul2(mul2(mul2(d, gp.a), gp.dsil2), wg2);
             s1u = add2(s1u, dxu);
             s2u = fma2(dxu, gp.xu, s2u);
             s1g = add2(s1g, dxg);
@@ -591,42 +605,34 @@ __global__ void __launch_bounds__(kRsThreads, 1) ln_gate_bwd_rowsum_bulk_kernel(
       float acc = (mid ? k1 : k0) + __shfl_xor_sync(0xffffffffu, mid ? k0 : k1, 8);
 #pragma unroll
       for (int o = 4; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-      if ((lane & 7) == 0) {
-        pf[(s * kRsConsumers + warp) * 4 + (lane >> 3)] = acc;
-        mbar_arrive(&empty[s]);
-      }
-      if (++nt == M) {
-        nt = 0;
-        if (++tl == L) {
-          tl = 0;
-          ++rank;
-          reload = true;
-        }
-      }
+      if ((lane & 7) == 0) pf[(s * kRsConsumers + warp) * 4 + (lane >> 3)] = acc;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);
     }
   }
 }
 
 // Pass 2 as a bulk-copy pipeline: one producer thread streams, per row, the
-// CTA's column segments of U, G and dHl plus the row's statistics and row
-// sums into a ring of shared-memory stages with cp.async.bulk; three consumer
+// CTA's column segments of U, G and dHl plus the row's coefficient record
+// into a ring of shared-memory stages with cp.async.bulk; three consumer
 // warps (8 columns a thread) hold the fp32 affines and the six column sums in
-// registers, write dZ, and release each stage as soon as they have read it.
-// Four warps a CTA keep the SM's four sub-partitions evenly loaded.
+// registers, write dZ, and release each stage (one arrival a warp) as soon as
+// they have read it.  Four warps a CTA keep the SM's four sub-partitions
+// evenly loaded.
 constexpr int kApConsumers = 3;
 constexpr int kApCols = 8 * 32 * kApConsumers;  // columns of one CTA: 768
 constexpr int kApThreads = 32 * (kApConsumers + 1);
 constexpr int kApRing = 8;
 constexpr int kApSeg = 2 * kApCols;                 // bytes of one bf16 row segment
-constexpr int kApStageBytes = 3 * kApSeg + 32;      // U, G, dHl segments, statistics, row sums
+constexpr int kApStageBytes = 3 * kApSeg + 32;      // U, G, dHl segments, the row's coefficient record
 constexpr int kApSmem = kApRing * kApStageBytes + 2 * kApRing * 8;
 
 // grid: (column blocks of kApCols, T, row splits).
 __global__ void __launch_bounds__(kApThreads, 4) ln_gate_bwd_apply_kernel(
-    const __nv_bfloat16* __restrict__ Z, const float4* __restrict__ stats, const float4* __restrict__ rowsum,
-    const __nv_bfloat16* __restrict__ dHl, const __nv_bfloat16* __restrict__ gx, const __nv_bfloat16* __restrict__ bx,
-    const __nv_bfloat16* __restrict__ gg, const __nv_bfloat16* __restrict__ bg, __nv_bfloat16* __restrict__ dZ,
-    float* __restrict__ part, int M, int L, int H, uint32_t* err) {
+    const __nv_bfloat16* __restrict__ Z, const float4* __restrict__ rc, const __nv_bfloat16* __restrict__ dHl,
+    const __nv_bfloat16* __restrict__ gx, const __nv_bfloat16* __restrict__ bx, const __nv_bfloat16* __restrict__ gg,
+    const __nv_bfloat16* __restrict__ bg, __nv_bfloat16* __restrict__ dZ, float* __restrict__ part, int M, int L, int H,
+    uint32_t* err) {
   extern __shared__ __align__(128) uint8_t ap_smem[];
   uint64_t* full = reinterpret_cast<uint64_t*>(ap_smem + kApRing * kApStageBytes);
   uint64_t* empty = full + kApRing;
@@ -634,7 +640,7 @@ __global__ void __launch_bounds__(kApThreads, 4) ln_gate_bwd_apply_kernel(
   if (threadIdx.x == 0) {
     for (int i = 0; i < kApRing; ++i) {
       mbar_init(&full[i], 1);
-      mbar_init(&empty[i], 32 * kApConsumers);
+      mbar_init(&empty[i], kApConsumers);
     }
     fence_mbar_init();
   }
@@ -665,8 +671,7 @@ __global__ void __launch_bounds__(kApThreads, 4) ln_gate_bwd_apply_kernel(
         bulk_load(slot, zp, seg, &full[stage]);
         bulk_load(slot + kApSeg, zp + H, seg, &full[stage]);
         bulk_load(slot + 2 * kApSeg, hp, seg, &full[stage]);
-        bulk_load(slot + 3 * kApSeg, stats + rowbase + i, 16u, &full[stage]);
-        bulk_load(slot + 3 * kApSeg + 16, rowsum + rowbase + i, 16u, &full[stage]);
+        bulk_load(slot + 3 * kApSeg, rc + 2 * (rowbase + i), 32u, &full[stage]);
         zp += zstride;
         hp += H;
         issued = i + 1;
@@ -689,8 +694,8 @@ __global__ void __launch_bounds__(kApThreads, 4) ln_gate_bwd_apply_kernel(
   const int v = warp * 32 + lane;
   const bool active = 8 * v < wc;
   const int c0 = col0 + (active ? 8 * v : 0);
-  const float inv_h = 1.0f / static_cast<float>(H);
-  const AffineF aff = load_affine_f(gx, bx, gg, bg, static_cast<int64_t>(t / L) * H + c0);
+  AffineF aff = load_affine_f(gx, bx, gg, bg, static_cast<int64_t>(t / L) * H + c0);
+  halve_gate_affine(aff);
   float2 s_du[4], s_dg[4], s_gx[4], s_bx[4], s_gg[4], s_bg[4];
 #pragma unroll
   for (int e = 0; e < 4; ++e) s_du[e] = s_dg[e] = s_gx[e] = s_bx[e] = s_gg[e] = s_bg[e] = splat2(0.0f);
@@ -707,26 +712,26 @@ __global__ void __launch_bounds__(kApThreads, 4) ln_gate_bwd_apply_kernel(
       pg = reinterpret_cast<const uint4*>(slot + kApSeg)[v];
       ph = reinterpret_cast<const uint4*>(slot + 2 * kApSeg)[v];
     }
-    const float4 stv = *reinterpret_cast<const float4*>(slot + 3 * kApSeg);
-    const float4 rsv = *reinterpret_cast<const float4*>(slot + 3 * kApSeg + 16);
-    mbar_arrive(&empty[stage]);
+    const float4* rcs = reinterpret_cast<const float4*>(slot + 3 * kApSeg);
+    const float4 cst = rcs[0], csum = rcs[1];
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[stage]);
     if (++stage == kApRing) {
       stage = 0;
       phase ^= 1u;
     }
     if (active) {
-      const float2 rsu = splat2(stv.y), cu = splat2(-stv.x * stv.y), rsg = splat2(stv.w), cgs = splat2(-stv.z * stv.w);
-      const float2 m1u = splat2(-rsv.x * inv_h), m2u = splat2(-rsv.y * inv_h);
-      const float2 m1g = splat2(-rsv.z * inv_h), m2g = splat2(-rsv.w * inv_h);
+      const float2 rsu = splat2(cst.x), cu = splat2(cst.y), rsg = splat2(cst.z), cgs = splat2(cst.w);
+      const float2 m1u = splat2(csum.x), m2u = splat2(csum.y), m1g = splat2(csum.z), m2g = splat2(csum.w);
       const uint32_t uw[4] = {pu.x, pu.y, pu.z, pu.w}, gw[4] = {pg.x, pg.y, pg.z, pg.w}, hw[4] = {ph.x, ph.y, ph.z, ph.w};
       uint32_t ou[4], og[4];
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const GatePair gp = gate_pair(unpack_bf16x2(uw[e]), unpack_bf16x2(gw[e]), rsu, cu, rsg, cgs, aff.wx[e],
-                                      aff.cx[e], aff.wg[e], aff.cg[e]);
+        const GatePairH gp = gate_pair_h(unpack_bf16x2(uw[e]), unpack_bf16x2(gw[e]), rsu, cu, rsg, cgs, aff.wx[e],
+                                         aff.cx[e], aff.wg[e], aff.cg[e]);
         const float2 dh = unpack_bf16x2(hw[e]);
         const float2 da = mul2(dh, gp.q);
-        const float2 ds = mul2(mul2(dh, gp.a), gp.dsil);
+        const float2 ds = mul2(mul2(dh, gp.a), gp.dsil2);  // twice ds: aff.wg is halved, ds*gg = this*wg
         // dU = rstd_u * (da*gx - mean(dx_u) - x_u*mean(dx_u*x_u)); same for dG
         const float2 du = mul2(rsu, fma2(gp.xu, m2u, fma2(da, aff.wx[e], m1u)));
         const float2 dg = mul2(rsg, fma2(gp.xg, m2g, fma2(ds, aff.wg[e], m1g)));
@@ -745,7 +750,12 @@ __global__ void __launch_bounds__(kApThreads, 4) ln_gate_bwd_apply_kernel(
     dzp += zstride;
   }
   if (!active) return;
-  // part[t][split][q][c], q: dU, dG, da*x_u, da, ds*x_g, ds
+  // part[t][split][q][c], q: dU, dG, da*x_u, da, ds*x_g, ds (the last two were summed twice over)
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    s_gg[e] = mul2(s_gg[e], splat2(0.5f));
+    s_bg[e] = mul2(s_bg[e], splat2(0.5f));
+  }
   float* pp = part + (static_cast<int64_t>(t) * nsplit + rsp) * 6 * H + c0;
   const float2* src[6] = {s_du, s_dg, s_gx, s_bx, s_gg, s_bg};
 #pragma unroll
@@ -1100,7 +1110,7 @@ cudaError_t launch_quant_weight(const void* w, float* scale, float* inv, void* q
 }
 
 cudaError_t launch_ln_gate_bwd_rowsum(const void* Z, const void* stats, const void* dHl, const void* nx_w,
-                                      const void* nx_b, const void* ng_w, const void* ng_b, void* rowsum, int T, int M,
+                                      const void* nx_b, const void* ng_w, const void* ng_b, void* rc, int T, int M,
                                       int L, int H, const DeviceInfo& dev, cudaStream_t s) {
   const int64_t rows = static_cast<int64_t>(T) * M;
   if (H <= kRsMaxH) {
@@ -1121,7 +1131,7 @@ cudaError_t launch_ln_gate_bwd_rowsum(const void* Z, const void* stats, const vo
                       static_cast<const float4*>(stats), static_cast<const __nv_bfloat16*>(dHl),
                       static_cast<const __nv_bfloat16*>(nx_w), static_cast<const __nv_bfloat16*>(nx_b),
                       static_cast<const __nv_bfloat16*>(ng_w), static_cast<const __nv_bfloat16*>(ng_b),
-                      static_cast<float4*>(rowsum), rows, M, L, H, slot_bytes, dev.err);
+                      static_cast<float4*>(rc), rows, M, L, H, slot_bytes, dev.err);
   }
   int per_sm = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, ln_gate_bwd_rowsum_kernel, kRowsumThreads, 0) !=
@@ -1134,7 +1144,7 @@ cudaError_t launch_ln_gate_bwd_rowsum(const void* Z, const void* stats, const vo
   return launch_pdl(ln_gate_bwd_rowsum_kernel, dim3(static_cast<unsigned>(blocks)), dim3(kRowsumThreads), 0, s,
       static_cast<const __nv_bfloat16*>(Z), static_cast<const float4*>(stats), static_cast<const __nv_bfloat16*>(dHl),
       static_cast<const __nv_bfloat16*>(nx_w), static_cast<const __nv_bfloat16*>(nx_b),
-      static_cast<const __nv_bfloat16*>(ng_w), static_cast<const __nv_bfloat16*>(ng_b), static_cast<float4*>(rowsum),
+      static_cast<const __nv_bfloat16*>(ng_w), static_cast<const __nv_bfloat16*>(ng_b), static_cast<float4*>(rc),
       rows, M, L, H, dev.err);
 }
 
@@ -1148,18 +1158,17 @@ int ffn_bwd_row_splits(int T, int M, int H) {
   return splits < 1 ? 1 : splits;
 }
 
-cudaError_t launch_ln_gate_bwd_apply(const void* Z, const void* stats, const void* rowsum, const void* dHl,
-                                     const void* nx_w, const void* nx_b, const void* ng_w, const void* ng_b, void* dZ,
-                                     float* part, int T, int M, int L, int H, int nsplit, const DeviceInfo& dev,
-                                     cudaStream_t s) {
+cudaError_t launch_ln_gate_bwd_apply(const void* Z, const void* rc, const void* dHl, const void* nx_w,
+                                     const void* nx_b, const void* ng_w, const void* ng_b, void* dZ, float* part, int T,
+                                     int M, int L, int H, int nsplit, const DeviceInfo& dev, cudaStream_t s) {
   dim3 grid((H + kApCols - 1) / kApCols, T, nsplit);
   cudaError_t e = smem_attr_once(reinterpret_cast<const void*>(ln_gate_bwd_apply_kernel), kApSmem);
   if (e != cudaSuccess) return e;
   return launch_pdl(ln_gate_bwd_apply_kernel, grid, dim3(kApThreads), kApSmem, s,
-      static_cast<const __nv_bfloat16*>(Z), static_cast<const float4*>(stats), static_cast<const float4*>(rowsum),
-      static_cast<const __nv_bfloat16*>(dHl), static_cast<const __nv_bfloat16*>(nx_w),
-      static_cast<const __nv_bfloat16*>(nx_b), static_cast<const __nv_bfloat16*>(ng_w),
-      static_cast<const __nv_bfloat16*>(ng_b), static_cast<__nv_bfloat16*>(dZ), part, M, L, H, dev.err);
+      static_cast<const __nv_bfloat16*>(Z), static_cast<const float4*>(rc), static_cast<const __nv_bfloat16*>(dHl),
+      static_cast<const __nv_bfloat16*>(nx_w), static_cast<const __nv_bfloat16*>(nx_b),
+      static_cast<const __nv_bfloat16*>(ng_w), static_cast<const __nv_bfloat16*>(ng_b),
+      static_cast<__nv_bfloat16*>(dZ), part, M, L, H, dev.err);
 }
 
 cudaError_t launch_grad_reduce(const float* part, void* d_b1, void* d_nx_w, void* d_nx_b, void* d_ng_w, void* d_ng_b,
