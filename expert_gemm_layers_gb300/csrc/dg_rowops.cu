@@ -59,17 +59,29 @@ __device__ __forceinline__ uint32_t e4m3_code(float x, float inv) {
   return static_cast<uint32_t>(__nv_cvt_float_to_fp8(__fmul_rn(x, inv), __NV_SATFINITE, __NV_E4M3));
 }
 
+// Four e4m3 codes packed little-endian into a word: the binary32 values a.x,
+// a.y, b.x, b.y rounded to nearest even, saturating (cvt ... e4m3x2 puts its
+// first source operand in the upper byte of its 16-bit result).
+__device__ __forceinline__ uint32_t e4m3x4(float2 a, float2 b) {
+  uint32_t r;
+  asm("{\n\t.reg .b16 lo, hi;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 lo, %2, %1;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 hi, %4, %3;\n\t"
+      "mov.b32 %0, {lo, hi};\n\t}"
+      : "=r"(r)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return r;
+}
+
 // Codes of eight values, packed little-endian into two words: the same
 // binary32 products and round-to-nearest-even saturating conversions as
 // e4m3_code, two values per multiply and per conversion.
 __device__ __forceinline__ uint2 e4m3_code8(const float (&x)[8], float inv) {
   const float2 iv = make_float2(inv, inv);
-  uint32_t h[4];
+  float2 p[4];
 #pragma unroll
-  for (int e = 0; e < 4; ++e)
-    h[e] = static_cast<uint32_t>(
-        __nv_cvt_float2_to_fp8x2(mul2(make_float2(x[2 * e], x[2 * e + 1]), iv), __NV_SATFINITE, __NV_E4M3));
-  return make_uint2(h[0] | (h[1] << 16), h[2] | (h[3] << 16));
+  for (int e = 0; e < 4; ++e) p[e] = mul2(make_float2(x[2 * e], x[2 * e + 1]), iv);
+  return make_uint2(e4m3x4(p[0], p[1]), e4m3x4(p[2], p[3]));
 }
 
 // Scale (amax / 448) and inverse scale (448 / amax) of a vector whose largest
@@ -278,6 +290,176 @@ __global__ void __launch_bounds__(NT, 512 / NT) ln_gate_fwd_kernel(
   }
   if (kFp8Out && n_mine > 0 && !finish_row(n_mine - 1, prev_row, ((n_mine - 1) & 1) ? ob : oa)) return;
   cp_async_wait<0>();
+}
+
+// The e4m3 gate pass for rows of up to 7680 columns as a bulk-copy
+// pipeline: one producer thread streams whole rows of Z (U | G, 4H bytes)
+// and their statistics into a ring of shared-memory slots with
+// cp.async.bulk; fifteen consumer warps take two 8-column vectors a thread
+// (affines in fp32 registers), compute the row's values and its largest
+// magnitude, park the values in one of two fp32 row buffers in shared memory
+// (each thread its own columns) and release the slot.  The row amax is the
+// same lagged block reduction as in ln_gate_fwd_kernel (four mbarrier-guarded
+// slots, row i - 1 quantised while row i's shares arrive), with the warp and
+// block maxima
+// taken by redux.sync on the bit patterns: the per-thread amax is a
+// non-negative float that is never NaN (fmaxf drops NaNs), and for those
+// the unsigned order of the bits is the order of the values.  Values and
+// codes are those of ln_gate_fwd_kernel<..., true>.  Each CTA takes a
+// contiguous range of rows.
+constexpr int kGfRing = 5;
+constexpr int kGfConsumers = 15;
+constexpr int kGfVec = 2;
+constexpr int kGfMaxH = 8 * 32 * kGfConsumers * kGfVec;
+constexpr int kGfThreads = 32 * (kGfConsumers + 1);
+
+template <bool kFull>  // kFull: H == kGfMaxH, so every consumer thread owns two whole vectors
+__global__ void __launch_bounds__(kGfThreads, 1) ln_gate_fwd_fp8_bulk_kernel(
+    const __nv_bfloat16* __restrict__ Z, const float4* __restrict__ stats, const __nv_bfloat16* __restrict__ gx,
+    const __nv_bfloat16* __restrict__ bx, const __nv_bfloat16* __restrict__ gg, const __nv_bfloat16* __restrict__ bg,
+    uint8_t* __restrict__ hq, float* __restrict__ hs, int64_t rows, int M, int L, int H, int slot_bytes,
+    uint32_t* err) {
+  extern __shared__ __align__(128) uint8_t gf_smem[];
+  float* vbuf = reinterpret_cast<float*>(gf_smem + kGfRing * slot_bytes);  // [2][H] row values
+  uint64_t* full = reinterpret_cast<uint64_t*>(vbuf + 2 * H);
+  uint64_t* empty = full + kGfRing;
+  uint64_t* rbar = empty + kGfRing;                            // [4]
+  uint32_t* red = reinterpret_cast<uint32_t*>(rbar + 4);      // [4][kGfConsumers]
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kGfRing; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], kGfConsumers);
+    }
+    for (int b = 0; b < 4; ++b) mbar_init(&rbar[b], kGfConsumers);
+    fence_mbar_init();
+  }
+  griddep_wait();
+  if (block_aborted(err)) return;  // (its barrier also publishes the barrier initialisation)
+  const int64_t per = (rows + gridDim.x - 1) / gridDim.x;
+  const int64_t r0 = min(rows, static_cast<int64_t>(blockIdx.x) * per);
+  const int n = static_cast<int>(min(rows, r0 + per) - r0);
+  const uint32_t zbytes = 4u * H;
+  const int nvec = H >> 3;
+
+  if (warp == kGfConsumers) {
+    // ---------------------------------------------------------------- producer
+    if (lane == 0) {
+      int issued = 0;
+      for (int i = 0; i < n; ++i) {
+        const int s = i % kGfRing;
+        if (i >= kGfRing && !mbar_wait(&empty[s], static_cast<uint32_t>(i / kGfRing - 1) & 1u, err, 0x42u)) break;
+        uint8_t* slot = gf_smem + s * slot_bytes;
+        const int64_t row = r0 + i;
+        mbar_arrive_expect_tx(&full[s], zbytes + 16u);
+        bulk_load(slot, Z + row * 2 * static_cast<int64_t>(H), zbytes, &full[s]);
+        bulk_load(slot + zbytes, stats + row, 16u, &full[s]);
+        issued = i + 1;
+      }
+      // every copy issued has landed before the CTA may exit
+      for (int i = max(0, issued - kGfRing); i < issued; ++i) {
+        uint32_t dummy = 0;
+        if (!mbar_try_wait(&full[i % kGfRing], static_cast<uint32_t>(i / kGfRing) & 1u))
+          mbar_wait_slow(&full[i % kGfRing], static_cast<uint32_t>(i / kGfRing) & 1u, &dummy, 0x43u, kWaitLimitNs);
+      }
+    }
+    return;
+  }
+
+  // ---------------------------------------------------------------- consumers
+  const int64_t rank_rows = static_cast<int64_t>(L) * M;
+  int rank = static_cast<int>(r0 / rank_rows);
+  int next_rank_at = static_cast<int>(min(static_cast<int64_t>(n), (rank + 1) * rank_rows - r0));
+  bool reload = true;
+  AffineF af[kGfVec];
+  // this thread's vectors: v0 + 32 * kGfConsumers * j
+  const int v0 = warp * 32 + lane;
+  int s = 0;           // ring slot of the row being computed
+  uint32_t ph = 0;     // and its phase parity
+  uint8_t* qrow = hq + r0 * static_cast<int64_t>(H);  // code row of the row being quantised
+  // quantise row k (local index) once every warp's share of its amax is in
+  auto finish_row = [&](int k) -> bool {
+    const int slot = k & 3;
+    if (!__all_sync(0xffffffffu, mbar_wait(&rbar[slot], static_cast<uint32_t>(k >> 2) & 1u, err, 0x44u)))
+      return false;
+    const uint32_t mb = __reduce_max_sync(0xffffffffu, lane < kGfConsumers ? red[slot * kGfConsumers + lane] : 0u);
+    const float m = __uint_as_float(mb);
+    const float inv = e4m3_inv(m);
+    const float* vrow = vbuf + (k & 1) * H;
+#pragma unroll
+    for (int j = 0; j < kGfVec; ++j) {
+      const int v = v0 + 32 * kGfConsumers * j;
+      if (kFull || v < nvec) {
+        const float4 x0 = reinterpret_cast<const float4*>(vrow)[2 * v];
+        const float4 x1 = reinterpret_cast<const float4*>(vrow)[2 * v + 1];
+        const float x[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+        *reinterpret_cast<uint2*>(qrow + 8 * v) = e4m3_code8(x, inv);
+      }
+    }
+    if (warp == 0 && lane == 0) hs[r0 + k] = e4m3_scale(m);
+    qrow += H;
+    return true;
+  };
+  auto do_row = [&](int i) -> bool {
+    if (!__all_sync(0xffffffffu, mbar_wait(&full[s], ph, err, 0x45u))) return false;
+    if (i == next_rank_at) {
+      ++rank;
+      next_rank_at = static_cast<int>(min(static_cast<int64_t>(n), next_rank_at + rank_rows));
+      reload = true;
+    }
+    if (reload) {
+      reload = false;
+#pragma unroll
+      for (int j = 0; j < kGfVec; ++j) {
+        const int v = v0 + 32 * kGfConsumers * j;
+        if (kFull || v < nvec) af[j] = load_affine_f(gx, bx, gg, bg, static_cast<int64_t>(rank) * H + 8 * v);
+      }
+    }
+    const uint8_t* slot = gf_smem + s * slot_bytes;
+    const uint4* zrow = reinterpret_cast<const uint4*>(slot);
+    const float4 sr = *reinterpret_cast<const float4*>(slot + zbytes);
+    const float2 rsu = splat2(sr.y), cu = splat2(-sr.x * sr.y), rsg = splat2(sr.w), cgs = splat2(-sr.z * sr.w);
+    const float2 half2 = splat2(0.5f);
+    float* vrow = vbuf + (i & 1) * H;
+    float amax = 0.0f;
+#pragma unroll
+    for (int j = 0; j < kGfVec; ++j) {
+      const int v = v0 + 32 * kGfConsumers * j;
+      if (kFull || v < nvec) {
+        const uint4 pu = zrow[v], pg = zrow[nvec + v];
+        const uint32_t uw[4] = {pu.x, pu.y, pu.z, pu.w}, gw[4] = {pg.x, pg.y, pg.z, pg.w};
+        float o[8];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 a = fma2(fma2(unpack_bf16x2(uw[e]), rsu, cu), af[j].wx[e], af[j].cx[e]);
+          const float2 sv = fma2(fma2(unpack_bf16x2(gw[e]), rsg, cgs), af[j].wg[e], af[j].cg[e]);
+          const float2 h = mul2(sv, half2);
+          const float2 silu = fma2(h, make_float2(tanh_fast(h.x), tanh_fast(h.y)), h);
+          const float2 ov = mul2(a, silu);
+          o[2 * e] = ov.x;
+          o[2 * e + 1] = ov.y;
+          amax = fmaxf(amax, fmaxf(fabsf(ov.x), fabsf(ov.y)));
+        }
+        reinterpret_cast<float4*>(vrow)[2 * v] = make_float4(o[0], o[1], o[2], o[3]);
+        reinterpret_cast<float4*>(vrow)[2 * v + 1] = make_float4(o[4], o[5], o[6], o[7]);
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[s]);  // the slot has been read
+    if (++s == kGfRing) {
+      s = 0;
+      ph ^= 1u;
+    }
+    const uint32_t wmax = __reduce_max_sync(0xffffffffu, __float_as_uint(amax));
+    if (lane == 0) {
+      red[(i & 3) * kGfConsumers + warp] = wmax;
+      mbar_arrive(&rbar[i & 3]);
+    }
+    return i == 0 || finish_row(i - 1);
+  };
+  for (int i = 0; i < n; ++i)
+    if (!do_row(i)) return;
+  if (n > 0) finish_row(n - 1);
 }
 
 // ------------------------------------------------------------------ e4m3 operands
@@ -1081,6 +1263,23 @@ cudaError_t launch_ln_gate_fwd(const void* Z, const void* stats, const void* nx_
                       static_cast<const __nv_bfloat16*>(ng_b), static_cast<__nv_bfloat16*>(Hl), hq, hs, M, L, H, cpr,
                       cb, dev.err);
   };
+  if (hq && H <= kGfMaxH) {
+    // bulk-copy pipeline: kGfRing slots of a Z row and its statistics
+    const int64_t rows = static_cast<int64_t>(P) * L * M;
+    if (rows == 0) return cudaSuccess;
+    const int slot_bytes = (4 * H + 16 + 127) / 128 * 128;
+    const int smem = kGfRing * slot_bytes + 2 * H * 4 + (2 * kGfRing + 4) * 8 + 4 * kGfConsumers * 4;
+    auto kern = H == kGfMaxH ? ln_gate_fwd_fp8_bulk_kernel<true> : ln_gate_fwd_fp8_bulk_kernel<false>;
+    cudaError_t e = smem_attr_once(reinterpret_cast<const void*>(kern), smem);
+    if (e != cudaSuccess) return e;
+    int64_t blocks = dev.num_sms;
+    if (blocks > rows) blocks = rows;
+    return launch_pdl(kern, dim3(static_cast<unsigned>(blocks)), dim3(kGfThreads),
+                      static_cast<size_t>(smem), s, static_cast<const __nv_bfloat16*>(Z),
+                      static_cast<const float4*>(stats), static_cast<const __nv_bfloat16*>(nx_w),
+                      static_cast<const __nv_bfloat16*>(nx_b), static_cast<const __nv_bfloat16*>(ng_w),
+                      static_cast<const __nv_bfloat16*>(ng_b), hq, hs, rows, M, L, H, slot_bytes, dev.err);
+  }
   if (hq) {
     if (nt == 256 && vpt == 1) return run(ln_gate_fwd_kernel<256, 1, true>);
     if (nt == 256) return run(ln_gate_fwd_kernel<256, 2, true>);
