@@ -517,12 +517,14 @@ def run_dg(args, rank, world):
 
     # outside the step: the FP8 GEMM alone (L2 flushed before each launch) and
     # the TP SwiGLU backward (recompute [a|b], dh, gate backward, dw2, dX, dw13)
-    extra = run_fp8_alone(w, args, dev, peaks)
-    extra.update(run_tp_backward(w, args, dev, peaks))
-    extra.update(run_attn_proj(w, args, dev, peaks))
-    extra.update(run_ffn_fp8(w, args, dev, peaks))
-    extra.update(run_ffn_forward_variants(w, args, dev, peaks))
-    extra.update(run_tiny_latency(args, dev))
+    extra = {}
+    if not args.step_only:
+        extra = run_fp8_alone(w, args, dev, peaks)
+        extra.update(run_tp_backward(w, args, dev, peaks))
+        extra.update(run_attn_proj(w, args, dev, peaks))
+        extra.update(run_ffn_fp8(w, args, dev, peaks))
+        extra.update(run_ffn_forward_variants(w, args, dev, peaks))
+        extra.update(run_tiny_latency(args, dev))
 
     # end to end: inputs from pinned host memory in, results back to pinned host memory
     e2e = run_e2e(w, args, dev, step_flops, world)
@@ -535,7 +537,8 @@ def run_dg(args, rank, world):
         "ms_per_step_min": round(min(step_ms), 4), "ms_per_step_max": round(max(step_ms), 4),
         "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16+e4m3 (fp32 accumulate)", "data": "synthetic",
-        "config": workload_config(), "parts": dict(parts, ffn_tiny_latency=extra["ffn_tiny_latency"]),
+        "config": workload_config(),
+        "parts": dict(parts, **({"ffn_tiny_latency": extra["ffn_tiny_latency"]} if "ffn_tiny_latency" in extra else {})),
         "roofline": roof, "kernels": kernel_table,
         "gpu_launches": launches, "e2e": e2e, "clocks": clk, "outside_step": extra,
     }
@@ -965,6 +968,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=("dg", "reference"), default="dg")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--step-only", action="store_true",
+                    help="skip the measurements outside the step (for a launch list of the step alone)")
     ap.add_argument("--profile-case", choices=sorted(PROFILE_CASES), default=None,
                     help="run one small part of the path (for ncu captures) instead of the benchmark")
     args = ap.parse_args()

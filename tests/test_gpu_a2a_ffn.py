@@ -121,6 +121,55 @@ def test_forward_closed_form_constant_halves():
     assert_close(out, ref, 1e-2, "closed form")
 
 
+@pytest.mark.parametrize("flags", [0, DG_FFN_FUSED_GATE])
+@pytest.mark.parametrize("half", [0, 1])
+def test_gate_elementwise_error_bound(half, flags):
+    """Every gate value Hl against the fp64 gate, with an elementwise bound.
+
+    The gate's sigmoid is (1 + tanh(s/2)) / 2 on the hardware tanh
+    (tanh.approx.f32, absolute error below 2^-10), so silu(s) = h + h*tanh(h),
+    h = s/2, carries an absolute error up to |h| * 2^-10: a large relative
+    error where silu(s) is tiny (s << 0).  The inputs make Z exact in bf16
+    (small integers), and wout copies one half of Hl's columns to the output
+    unchanged (Y = Hl[:, c] exactly), so the output shows every gate value of
+    that half.  Bound per element: 2^-8 |Hl| (Hl rounded to bf16) +
+    |a| (|h| 2^-10 + 2^-20 (|s| + 1)) (the tanh and the fp32 normalisation).
+    """
+    P, B, T, D, k = 2, 4, 4, 128, 2
+    H, L = D * k, T // P
+    g = torch.Generator().manual_seed(11 + half)
+    ints = lambda *shape, lo, hi: torch.randint(lo, hi + 1, shape, generator=g).to(torch.bfloat16)
+    inputs = ints(P, B, T, D, lo=-1, hi=1)
+    params = {
+        "w1": ints(P, L, D, 2 * H, lo=-1, hi=1), "b1": ints(P, L, 2 * H, lo=-4, hi=4),
+        "wout": torch.zeros((P, L, H, D), dtype=torch.bfloat16), "bout": torch.zeros((P, L, D), dtype=torch.bfloat16),
+        "nx_w": torch.randn((P, H), generator=g).to(torch.bfloat16),
+        "nx_b": (0.5 * torch.randn((P, H), generator=g)).to(torch.bfloat16),
+        "ng_w": torch.full((P, H), 4.0, dtype=torch.bfloat16),
+        "ng_b": (2.0 * torch.rand((P, H), generator=g) - 1.0).to(torch.bfloat16),
+    }
+    off = half * D
+    params["wout"][:, :, off + torch.arange(D), torch.arange(D)] = 1.0
+    out, _ = a2a_ffn_forward(inputs.to(DEV), {n: v.to(DEV) for n, v in params.items()}, flags=flags)
+    torch.cuda.synchronize()
+    xb, pb = _bits(inputs, params)
+    sh = O.FFNShape(P, B, T, D, k)
+    _, Zs, Hs = O.ffn_forward(sh, xb, pb, intermediates=True)
+    got = O.a2a_dispatch(out.float().cpu().numpy().astype(np.float64))   # [P, P*B, L, D], per problem
+    a = np.empty_like(Hs)
+    sg = np.empty_like(Hs)
+    for r in range(P):
+        a[r] = O.layer_norm(Zs[r, ..., :H], O.bf16_to_f64(pb["nx_w"])[r], O.bf16_to_f64(pb["nx_b"])[r], sh.eps)
+        sg[r] = O.layer_norm(Zs[r, ..., H:], O.bf16_to_f64(pb["ng_w"])[r], O.bf16_to_f64(pb["ng_b"])[r], sh.eps)
+    hl, a, sg = Hs[..., off:off + D], a[..., off:off + D], sg[..., off:off + D]
+    bound = 2.0 ** -8 * np.abs(hl) + np.abs(a) * (np.abs(sg / 2) * 2.0 ** -10 + 2.0 ** -20 * (np.abs(sg) + 1.0))
+    err = np.abs(got - hl)
+    assert (sg < -6).any() and (sg > 6).any()       # both tails of the gate are exercised
+    worst = np.unravel_index(np.argmax(err - bound), err.shape)
+    assert np.all(err <= bound), (f"gate value {got[worst]} vs {hl[worst]} at s={sg[worst]}, a={a[worst]}: "
+                                  f"error {err[worst]:.3g} > bound {bound[worst]:.3g}")
+
+
 def test_forward_full_size_row_subset():
     # the page-3 default workload: P=8, B=512, T=64, D=1280, k=6, seed 42
     P, B, T, D, k = 8, 512, 64, 1280, 6
