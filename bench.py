@@ -48,18 +48,18 @@ FALLBACK_PEAKS = dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=
 # sources changed since reports null.  The capture's summary is committed with
 # the other ncu summaries of this repository.
 TRAFFIC = {
-    "ffn_gemm1": {"bytes_per_launch": 8 * 1.385788e+09, "sources": ["expert_gemm_layers_gb300/csrc/dg_gemm.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh", "expert_gemm_layers_gb300/csrc/dg_gemm_bf16_km_lnstats.cu", "expert_gemm_layers_gb300/csrc/dg_api.cu"], "sha256": "f820ee9c205118e5c77c4348a05dbafa5c20e656b6cb35d63f98a50b4a033570"},
-    "ffn_ln_stats": {"bytes_per_launch": 8 * 3.147264e+07, "sources": ["expert_gemm_layers_gb300/csrc/dg_rowops.cu", "expert_gemm_layers_gb300/csrc/dg_gate.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh"], "sha256": "11cc40550008b41dcf95458ed76c0e31aa48bd4716d58882e0e1f39376e83dbe"},
-    "ffn_ln_gate_fwd": {"bytes_per_launch": 8 * 1.468731e+09, "sources": ["expert_gemm_layers_gb300/csrc/dg_rowops.cu", "expert_gemm_layers_gb300/csrc/dg_gate.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh"], "sha256": "11cc40550008b41dcf95458ed76c0e31aa48bd4716d58882e0e1f39376e83dbe"},
-    "ffn_gemm2": {"bytes_per_launch": 8 * 9.025536e+08, "sources": ["expert_gemm_layers_gb300/csrc/dg_gemm.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh", "expert_gemm_layers_gb300/csrc/dg_gemm_bf16_km_bias.cu", "expert_gemm_layers_gb300/csrc/dg_api.cu"], "sha256": "3165c0331fcdc3e20a96895c2c45caa6468692bb0ce06a00f8f24a294681a465"},
-    "ffn_bwd_dhl": {"bytes_per_launch": 8 * 6.893960e+08, "sources": ["expert_gemm_layers_gb300/csrc/dg_gemm.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh", "expert_gemm_layers_gb300/csrc/dg_gemm_bf16_kk_store.cu", "expert_gemm_layers_gb300/csrc/dg_api.cu"], "sha256": "9b9a38ce6844d6316d1cefa105634b841688cf0a84f08d23aa03320cd33ef1d7"},
-    "ffn_bwd_dwout": {"bytes_per_launch": 8 * 7.516895e+08, "sources": ["expert_gemm_layers_gb300/csrc/dg_gemm.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh", "expert_gemm_layers_gb300/csrc/dg_gemm_bf16_mm_store.cu", "expert_gemm_layers_gb300/csrc/dg_api.cu"], "sha256": "4bccd4e11fb08277b811d3fc4d118c999b819cba2a43a0404720b47d6656e8a1"},
-    "ffn_bwd_dbout": {"bytes_per_launch": 8 * 8.403840e+07, "sources": ["expert_gemm_layers_gb300/csrc/dg_rowops.cu", "expert_gemm_layers_gb300/csrc/dg_gate.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh"], "sha256": "11cc40550008b41dcf95458ed76c0e31aa48bd4716d58882e0e1f39376e83dbe"},
-    "ffn_bwd_ln_rowsum": {"bytes_per_launch": 8 * 1.512215e+09, "sources": ["expert_gemm_layers_gb300/csrc/dg_rowops.cu", "expert_gemm_layers_gb300/csrc/dg_gate.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh"], "sha256": "11cc40550008b41dcf95458ed76c0e31aa48bd4716d58882e0e1f39376e83dbe"},
-    "ffn_bwd_ln_apply": {"bytes_per_launch": 8 * 2.526112e+09, "sources": ["expert_gemm_layers_gb300/csrc/dg_rowops.cu", "expert_gemm_layers_gb300/csrc/dg_gate.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh"], "sha256": "11cc40550008b41dcf95458ed76c0e31aa48bd4716d58882e0e1f39376e83dbe"},
-    "ffn_bwd_grad_reduce": {"bytes_per_launch": 8 * 4.722842e+07, "sources": ["expert_gemm_layers_gb300/csrc/dg_rowops.cu", "expert_gemm_layers_gb300/csrc/dg_gate.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh"], "sha256": "11cc40550008b41dcf95458ed76c0e31aa48bd4716d58882e0e1f39376e83dbe"},
-    "ffn_bwd_dx": {"bytes_per_launch": 8 * 1.775118e+09, "sources": ["expert_gemm_layers_gb300/csrc/dg_gemm.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh", "expert_gemm_layers_gb300/csrc/dg_gemm_bf16_kk_store.cu", "expert_gemm_layers_gb300/csrc/dg_api.cu"], "sha256": "9b9a38ce6844d6316d1cefa105634b841688cf0a84f08d23aa03320cd33ef1d7"},
-    "ffn_bwd_dw1": {"bytes_per_launch": 8 * 1.426813e+09, "sources": ["expert_gemm_layers_gb300/csrc/dg_gemm.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh", "expert_gemm_layers_gb300/csrc/dg_gemm_bf16_mm_store.cu", "expert_gemm_layers_gb300/csrc/dg_api.cu"], "sha256": "4bccd4e11fb08277b811d3fc4d118c999b819cba2a43a0404720b47d6656e8a1"},
+    "ffn_gemm1": {"bytes_per_launch": 8 * 1.387412e+09, "sources": ["expert_gemm_layers_gb300/csrc/dg_gemm.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh", "expert_gemm_layers_gb300/csrc/dg_gemm_bf16_km_lnstats.cu", "expert_gemm_layers_gb300/csrc/dg_api.cu"], "sha256": "8af1a1e83e62c16914bb6c50cf736df46517636c57125c66e1e8d33436f1c6b9"},
+    "ffn_ln_stats": {"bytes_per_launch": 8 * 3.148058e+07, "sources": ["expert_gemm_layers_gb300/csrc/dg_rowops.cu", "expert_gemm_layers_gb300/csrc/dg_gate.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh"], "sha256": "bb77f856ab24f2d31376afce4833087011278392c561d3202948e3dbdf23873f"},
+    "ffn_ln_gate_fwd": {"bytes_per_launch": 8 * 1.470775e+09, "sources": ["expert_gemm_layers_gb300/csrc/dg_rowops.cu", "expert_gemm_layers_gb300/csrc/dg_gate.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh"], "sha256": "bb77f856ab24f2d31376afce4833087011278392c561d3202948e3dbdf23873f"},
+    "ffn_gemm2": {"bytes_per_launch": 8 * 9.039542e+08, "sources": ["expert_gemm_layers_gb300/csrc/dg_gemm.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh", "expert_gemm_layers_gb300/csrc/dg_gemm_bf16_km_bias.cu", "expert_gemm_layers_gb300/csrc/dg_api.cu"], "sha256": "1a42a166a43d464666f78e5b0c69e4f778e61d58820bade39421e79b852abf9d"},
+    "ffn_bwd_dhl": {"bytes_per_launch": 8 * 6.892237e+08, "sources": ["expert_gemm_layers_gb300/csrc/dg_gemm.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh", "expert_gemm_layers_gb300/csrc/dg_gemm_bf16_kk_store.cu", "expert_gemm_layers_gb300/csrc/dg_api.cu"], "sha256": "cb09ae5300c95f1679f8d6eee9fceed5f3f495ad332b153aa023173889f34842"},
+    "ffn_bwd_dwout": {"bytes_per_launch": 8 * 7.431660e+08, "sources": ["expert_gemm_layers_gb300/csrc/dg_gemm.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh", "expert_gemm_layers_gb300/csrc/dg_gemm_bf16_mm_store.cu", "expert_gemm_layers_gb300/csrc/dg_api.cu"], "sha256": "0d345dfcbed84061302bf57ad74c765f52f38be776a0a7d40b4415a03f3eaacd"},
+    "ffn_bwd_dbout": {"bytes_per_launch": 8 * 8.398950e+07, "sources": ["expert_gemm_layers_gb300/csrc/dg_rowops.cu", "expert_gemm_layers_gb300/csrc/dg_gate.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh"], "sha256": "bb77f856ab24f2d31376afce4833087011278392c561d3202948e3dbdf23873f"},
+    "ffn_bwd_ln_rowsum": {"bytes_per_launch": 8 * 1.512460e+09, "sources": ["expert_gemm_layers_gb300/csrc/dg_rowops.cu", "expert_gemm_layers_gb300/csrc/dg_gate.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh"], "sha256": "bb77f856ab24f2d31376afce4833087011278392c561d3202948e3dbdf23873f"},
+    "ffn_bwd_ln_apply": {"bytes_per_launch": 8 * 2.524076e+09, "sources": ["expert_gemm_layers_gb300/csrc/dg_rowops.cu", "expert_gemm_layers_gb300/csrc/dg_gate.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh"], "sha256": "bb77f856ab24f2d31376afce4833087011278392c561d3202948e3dbdf23873f"},
+    "ffn_bwd_grad_reduce": {"bytes_per_launch": 8 * 4.725504e+07, "sources": ["expert_gemm_layers_gb300/csrc/dg_rowops.cu", "expert_gemm_layers_gb300/csrc/dg_gate.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh"], "sha256": "bb77f856ab24f2d31376afce4833087011278392c561d3202948e3dbdf23873f"},
+    "ffn_bwd_dx": {"bytes_per_launch": 8 * 1.852506e+09, "sources": ["expert_gemm_layers_gb300/csrc/dg_gemm.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh", "expert_gemm_layers_gb300/csrc/dg_gemm_bf16_kk_store.cu", "expert_gemm_layers_gb300/csrc/dg_api.cu"], "sha256": "cb09ae5300c95f1679f8d6eee9fceed5f3f495ad332b153aa023173889f34842"},
+    "ffn_bwd_dw1": {"bytes_per_launch": 8 * 1.409293e+09, "sources": ["expert_gemm_layers_gb300/csrc/dg_gemm.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh", "expert_gemm_layers_gb300/csrc/dg_gemm_bf16_mm_store.cu", "expert_gemm_layers_gb300/csrc/dg_api.cu"], "sha256": "0d345dfcbed84061302bf57ad74c765f52f38be776a0a7d40b4415a03f3eaacd"},
 }
 
 

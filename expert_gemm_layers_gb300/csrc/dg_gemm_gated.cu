@@ -16,9 +16,11 @@
 // same time, so Z is read from HBM about once.
 //
 // Warp roles (512 threads):
-//   warp 0      Z producer: per K block of 32, this CTA's 128 rows of the U
-//               and G columns of Z (two 64-byte-swizzled boxes, the U box
-//               landing in the stage's A tile), on a per-CTA barrier
+//   warp 0      Z producer: per K block (64 columns, or 32 when built with
+//               DG_GATED_BK=32), this CTA's 128 rows of the U and G columns
+//               of Z (two boxes swizzled at the K block's row width, 128 or
+//               64 bytes, the U box landing in the stage's A tile), on a
+//               per-CTA barrier
 //   warp 14     B producer: the CTA's half of the block's B (wout, MN-major)
 //               columns, on the pair leader's barrier
 //   warp 15     parameter producer: the block's LayerNorm weights and biases
@@ -36,8 +38,8 @@
 // transform warps of both CTAs have arrived on the leader's barrier (after a
 // generic-to-async proxy fence; the arrive is a CTA-scope release, which a
 // cluster-scope one would stall for up to a microsecond per stage).  Each stage therefore passes through copy,
-// transform and MMA in turn; six stages of 32 K values keep enough of them in
-// flight for that chain.  The arithmetic is the same sequence of fp32
+// transform and MMA in turn; three stages of 64 K values (six of 32) keep
+// enough of them in flight for that chain.  The arithmetic is the same sequence of fp32
 // operations as the separate normalise-and-gate pass, so the A operand equals
 // that pass's Hl bit for bit.
 #include "dg_internal.h"

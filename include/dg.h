@@ -48,7 +48,7 @@ typedef enum {
   DG_ERR_INVALID_ARGUMENT = 1, /* a size, pointer, alignment or overlap rule was broken */
   DG_ERR_UNSUPPORTED = 2,      /* a valid request this build does not implement */
   DG_ERR_CUDA = 3,             /* a CUDA runtime/driver call failed */
-  DG_ERR_TIMEOUT = 4,          /* a device-side wait exceeded its limit (see dg_device_status) */
+  DG_ERR_TIMEOUT = 4,          /* a device-side wait exceeded its limit (see dg_check_device_error) */
   DG_ERR_DEVICE_CHECK = 5,     /* a device-side consistency check failed */
   DG_ERR_WORKSPACE = 6         /* the scratch buffer is missing or smaller than the query says */
 } dg_status;
