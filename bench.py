@@ -515,8 +515,14 @@ def run_dg(args, rank, world):
                                 "share": round(e["total_ms"] / total_ms, 4)} for e in table}
     launches = int(launches_per_step * args.steps)
 
-    # outside the step: the FP8 GEMM alone (L2 flushed before each launch) and
-    # the TP SwiGLU backward (recompute [a|b], dh, gate backward, dw2, dX, dw13)
+    # end to end: inputs from pinned host memory in, results back to pinned
+    # host memory; right after the device-timed steps, in the same state of the GPU
+    e2e = run_e2e(w, args, dev, step_flops, world)
+
+    # outside the step: the FP8 GEMM alone (L2 flushed before each launch),
+    # the TP SwiGLU backward (recompute [a|b], dh, gate backward, dw2, dX,
+    # dw13), the attention projections, the e4m3 FFN forward, the FFN forward
+    # variants and the tiny workload's latency
     extra = {}
     if not args.step_only:
         extra = run_fp8_alone(w, args, dev, peaks)
@@ -525,9 +531,6 @@ def run_dg(args, rank, world):
         extra.update(run_ffn_fp8(w, args, dev, peaks))
         extra.update(run_ffn_forward_variants(w, args, dev, peaks))
         extra.update(run_tiny_latency(args, dev))
-
-    # end to end: inputs from pinned host memory in, results back to pinned host memory
-    e2e = run_e2e(w, args, dev, step_flops, world)
 
     value = job_tflops(world, step_flops, ms)
     line = {

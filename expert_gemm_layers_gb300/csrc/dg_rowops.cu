@@ -630,11 +630,14 @@ __global__ void __launch_bounds__(kRowsumThreads, 2) ln_gate_bwd_rowsum_kernel(
 // producer warp streams whole rows (the U|G row of Z, the dHl row, the row's
 // statistics) into a ring of shared-memory slots with cp.async.bulk; fifteen
 // consumer warps each take every fifteenth 8-column vector of the row (two
-// vectors a thread, their affines held in fp32 registers) and publish per-warp
-// partial sums; when the producer recycles a slot it adds the warps' partials
-// in a fixed order and writes the row's coefficient record (store_row_coef).
-// Each CTA takes a contiguous range of rows (so the rank, and with it the
-// affines, change at most a few times).
+// vectors a thread, their affines held in fp32 registers) and publish each
+// lane's four partial sums; when the producer warp recycles a slot its lanes
+// add the partials of their lane position over the warps in a fixed order,
+// reduce the four sums over the lanes, and lane 0 writes the row's
+// coefficient record (store_row_coef).  The producer warp, which otherwise
+// only issues copies, thus does the row reduction the consumers would each
+// have done.  Each CTA takes a contiguous range of rows (so the rank, and
+// with it the affines, change at most a few times).
 constexpr int kRsRing = 4;
 // Sixteen warps in all: four per SM sub-partition leave 128 registers a thread.
 constexpr int kRsConsumers = 15;
@@ -648,8 +651,8 @@ __global__ void __launch_bounds__(kRsThreads, 1) ln_gate_bwd_rowsum_bulk_kernel(
     const __nv_bfloat16* __restrict__ bg, float4* __restrict__ rc, int64_t rows, int M, int L, int H,
     int slot_bytes, uint32_t* err) {
   extern __shared__ __align__(128) uint8_t rs_smem[];
-  float4* part = reinterpret_cast<float4*>(rs_smem + kRsRing * slot_bytes);  // [kRsRing][kRsConsumers]
-  uint64_t* full = reinterpret_cast<uint64_t*>(part + kRsRing * kRsConsumers);
+  float4* part = reinterpret_cast<float4*>(rs_smem + kRsRing * slot_bytes);  // [kRsRing][kRsConsumers][32]
+  uint64_t* full = reinterpret_cast<uint64_t*>(part + kRsRing * kRsConsumers * 32);
   uint64_t* empty = full + kRsRing;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -670,48 +673,70 @@ __global__ void __launch_bounds__(kRsThreads, 1) ln_gate_bwd_rowsum_bulk_kernel(
 
   if (warp == kRsConsumers) {
     // ---------------------------------------------------------------- producer
-    if (lane == 0) {
-      // the row's four sums from the warps' partials, in warp order, and its
-      // record; the slot still holds the row's statistics
-      auto finish = [&](int i) {
-        const float4* pp = part + (i % kRsRing) * kRsConsumers;
-        float4 a = pp[0];
-        for (int w = 1; w < kRsConsumers; ++w) {
-          a.x += pp[w].x;
-          a.y += pp[w].y;
-          a.z += pp[w].z;
-          a.w += pp[w].w;
+    // The whole warp: lane 0 issues the copies, every lane takes part in the
+    // reduction of a recycled row.  The row's four sums: each lane adds the
+    // partials of its lane position over the consumer warps in warp order,
+    // then a reduce-scatter over the lanes (after the xor-16 step a lane keeps
+    // two of the sums, after the xor-8 step one; lanes 0, 8, 16 and 24 end
+    // with sums 0 to 3), and lane 0 writes the record; the slot still holds
+    // the row's statistics.
+    const bool hi = (lane & 16) != 0, mid = (lane & 8) != 0;
+    auto finish = [&](int i) {
+      const int sl = i % kRsRing;
+      const float4* pp = part + sl * kRsConsumers * 32 + lane;
+      float4 a = pp[0];
+      for (int w = 1; w < kRsConsumers; ++w) {
+        const float4 b = pp[32 * w];
+        a.x += b.x;
+        a.y += b.y;
+        a.z += b.z;
+        a.w += b.w;
+      }
+      const float k0 = (hi ? a.z : a.x) + __shfl_xor_sync(0xffffffffu, hi ? a.x : a.z, 16);
+      const float k1 = (hi ? a.w : a.y) + __shfl_xor_sync(0xffffffffu, hi ? a.y : a.w, 16);
+      float t = (mid ? k1 : k0) + __shfl_xor_sync(0xffffffffu, mid ? k0 : k1, 8);
+#pragma unroll
+      for (int o = 4; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+      const float t1 = __shfl_sync(0xffffffffu, t, 8), t2 = __shfl_sync(0xffffffffu, t, 16);
+      const float t3 = __shfl_sync(0xffffffffu, t, 24);
+      if (lane == 0) {
+        const float4 sr = *reinterpret_cast<const float4*>(rs_smem + sl * slot_bytes + zbytes + hbytes);
+        store_row_coef(rc + 2 * (r0 + i), sr, make_float4(t, t1, t2, t3), inv_h);
+      }
+      __syncwarp();
+    };
+    bool ok = true;
+    int issued = 0;
+    for (int i = 0; i < n && ok; ++i) {
+      const int s = i % kRsRing;
+      if (i >= kRsRing) {
+        if (!__all_sync(0xffffffffu, mbar_wait(&empty[s], static_cast<uint32_t>(i / kRsRing - 1) & 1u, err, 0x50u))) {
+          ok = false;
+          break;
         }
-        const float4 sr = *reinterpret_cast<const float4*>(rs_smem + (i % kRsRing) * slot_bytes + zbytes + hbytes);
-        store_row_coef(rc + 2 * (r0 + i), sr, a, inv_h);
-      };
-      bool ok = true;
-      int issued = 0;
-      for (int i = 0; i < n && ok; ++i) {
-        const int s = i % kRsRing;
-        if (i >= kRsRing) {
-          if (!mbar_wait(&empty[s], static_cast<uint32_t>(i / kRsRing - 1) & 1u, err, 0x50u)) {
-            ok = false;
-            break;
-          }
-          finish(i - kRsRing);
-        }
+        finish(i - kRsRing);
+      }
+      if (lane == 0) {
         uint8_t* slot = rs_smem + s * slot_bytes;
         const int64_t row = r0 + i;
         mbar_arrive_expect_tx(&full[s], zbytes + hbytes + 16u);
         bulk_load(slot, Z + row * 2 * static_cast<int64_t>(H), zbytes, &full[s]);
         bulk_load(slot + zbytes, dHl + row * static_cast<int64_t>(H), hbytes, &full[s]);
         bulk_load(slot + zbytes + hbytes, stats + row, 16u, &full[s]);
-        issued = i + 1;
       }
-      for (int i = max(0, issued - kRsRing); i < issued && ok; ++i) {
-        if (!mbar_wait(&empty[i % kRsRing], static_cast<uint32_t>(i / kRsRing) & 1u, err, 0x51u)) {
-          ok = false;
-          break;
-        }
-        finish(i);
+      __syncwarp();
+      issued = i + 1;
+    }
+    for (int i = max(0, issued - kRsRing); i < issued && ok; ++i) {
+      if (!__all_sync(0xffffffffu,
+                      mbar_wait(&empty[i % kRsRing], static_cast<uint32_t>(i / kRsRing) & 1u, err, 0x51u))) {
+        ok = false;
+        break;
       }
-      // every copy issued has landed before the CTA may exit
+      finish(i);
+    }
+    // every copy issued has landed before the CTA may exit
+    if (lane == 0) {
       for (int i = max(0, issued - kRsRing); i < issued; ++i) {
         uint32_t dummy = 0;
         if (!mbar_try_wait(&full[i % kRsRing], static_cast<uint32_t>(i / kRsRing) & 1u))
@@ -726,9 +751,6 @@ __global__ void __launch_bounds__(kRsThreads, 1) ln_gate_bwd_rowsum_bulk_kernel(
     int next_rank_at = static_cast<int>(min(static_cast<int64_t>(n), (rank + 1) * rank_rows - r0));
     bool reload = true;
     AffineF af[kRsVec];
-    float* pf = reinterpret_cast<float*>(part);
-    // which of the four sums this lane ends up holding after the reduce-scatter below
-    const bool hi = (lane & 16) != 0, mid = (lane & 8) != 0;
     for (int i = 0; i < n; ++i) {
       const int s = i % kRsRing;
       const bool ok = mbar_wait(&full[s], static_cast<uint32_t>(i / kRsRing) & 1u, err, 0x53u);
@@ -754,10 +776,13 @@ __global__ void __launch_bounds__(kRsThreads, 1) ln_gate_bwd_rowsum_bulk_kernel(
       const uint4* hrow = reinterpret_cast<const uint4*>(slot + zbytes);
       const float4 sr = *reinterpret_cast<const float4*>(slot + zbytes + hbytes);
       const float2 rsu = splat2(sr.y), cu = splat2(-sr.x * sr.y), rsg = splat2(sr.w), cgs = splat2(-sr.z * sr.w);
-      float2 s1u = splat2(0.f), s2u = splat2(0.f), s1g = splat2(0.f), s2g = splat2(0.f);
+      // the four sums start from the first column pair's terms (no zeroing and
+      // no first additions); a thread without any vector of this row holds zeros
+      float2 s1u, s2u, s1g, s2g;
 #pragma unroll
       for (int j = 0; j < kRsVec; ++j) {
         const int v = warp * 32 + lane + 32 * kRsConsumers * j;
+        if (j == 0 && v >= nvec) s1u = s2u = s1g = s2g = splat2(0.f);
         if (v < nvec) {
           const uint4 pu = zrow[v], pg = zrow[nvec + v], ph = hrow[v];
           const uint32_t uw[4] = {pu.x, pu.y, pu.z, pu.w}, gw[4] = {pg.x, pg.y, pg.z, pg.w};
@@ -770,24 +795,23 @@ __global__ void __launch_bounds__(kRsThreads, 1) ln_gate_bwd_rowsum_bulk_kernel(
             const float2 d = unpack_bf16x2(hw[e]);
             const float2 dxu = mul2(mul2(d, gp.q), wx);
             const float2 dxg = mul2(mul2(mul2(d, gp.a), gp.dsil2), wg2);
-            s1u = add2(s1u, dxu);
-            s2u = fma2(dxu, gp.xu, s2u);
-            s1g = add2(s1g, dxg);
-            s2g = fma2(dxg, gp.xg, s2g);
+            if (j == 0 && e == 0) {
+              s1u = dxu;
+              s2u = mul2(dxu, gp.xu);
+              s1g = dxg;
+              s2g = mul2(dxg, gp.xg);
+            } else {
+              s1u = add2(s1u, dxu);
+              s2u = fma2(dxu, gp.xu, s2u);
+              s1g = add2(s1g, dxg);
+              s2g = fma2(dxg, gp.xg, s2g);
+            }
           }
         }
       }
-      // Reduce-scatter of the four sums over the warp: after the xor-16 step a
-      // lane keeps two of them (0,1 or 2,3), after the xor-8 step one, and the
-      // last three steps complete that one over all 32 lanes.  Lanes 0, 8, 16
-      // and 24 then hold sums 0, 1, 2 and 3.
-      const float a0 = s1u.x + s1u.y, a1 = s2u.x + s2u.y, a2 = s1g.x + s1g.y, a3 = s2g.x + s2g.y;
-      const float k0 = (hi ? a2 : a0) + __shfl_xor_sync(0xffffffffu, hi ? a0 : a2, 16);
-      const float k1 = (hi ? a3 : a1) + __shfl_xor_sync(0xffffffffu, hi ? a1 : a3, 16);
-      float acc = (mid ? k1 : k0) + __shfl_xor_sync(0xffffffffu, mid ? k0 : k1, 8);
-#pragma unroll
-      for (int o = 4; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-      if ((lane & 7) == 0) pf[(s * kRsConsumers + warp) * 4 + (lane >> 3)] = acc;
+      // this lane's four partial sums, for the producer warp to reduce
+      part[(s * kRsConsumers + warp) * 32 + lane] =
+          make_float4(s1u.x + s1u.y, s2u.x + s2u.y, s1g.x + s1g.y, s2g.x + s2g.y);
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);
     }
@@ -1315,7 +1339,7 @@ cudaError_t launch_ln_gate_bwd_rowsum(const void* Z, const void* stats, const vo
   if (H <= kRsMaxH) {
     // bulk-copy pipeline: kRsRing row slots of the U|G row, the dHl row and the statistics
     const int slot_bytes = (6 * H + 16 + 127) / 128 * 128;
-    const int smem = kRsRing * slot_bytes + kRsRing * kRsConsumers * 16 + 2 * kRsRing * 8;
+    const int smem = kRsRing * slot_bytes + kRsRing * kRsConsumers * 32 * 16 + 2 * kRsRing * 8;
     cudaError_t e = smem_attr_once(reinterpret_cast<const void*>(ln_gate_bwd_rowsum_bulk_kernel), smem);
     if (e != cudaSuccess) return e;
     int per_sm = 0;
