@@ -46,7 +46,7 @@ extern "C" {
 typedef enum {
   DG_OK = 0,
   DG_ERR_INVALID_ARGUMENT = 1, /* a size, pointer, alignment or overlap rule was broken */
-  DG_ERR_UNSUPPORTED = 2,      /* a valid request this build does not implement */
+  DG_ERR_UNSUPPORTED = 2,      /* a valid request the library does not implement */
   DG_ERR_CUDA = 3,             /* a CUDA runtime/driver call failed */
   DG_ERR_TIMEOUT = 4,          /* a device-side wait exceeded its limit (see dg_check_device_error) */
   DG_ERR_DEVICE_CHECK = 5,     /* a device-side consistency check failed */
