@@ -44,6 +44,11 @@ static __device__ __forceinline__ float2 add2(float2 a, float2 b) {
   asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(f2u(a)), "l"(f2u(b)));
   return u2f(d);
 }
+static __device__ __forceinline__ float2 sub2(float2 a, float2 b) {
+  unsigned long long d;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(f2u(a)), "l"(f2u(b)));
+  return u2f(d);
+}
 static __device__ __forceinline__ float2 splat2(float x) { return make_float2(x, x); }
 
 
@@ -72,7 +77,8 @@ static __device__ __forceinline__ GatePair gate_pair(float2 u, float2 g, float2 
 // The same quantities with the gate norm's affine pre-halved (wg2 = gg/2,
 // cg2 = bg/2), so that h = s/2 comes out of one fma.  With t = tanh(h):
 // q = silu(s) = h*(1 + t), and silu'(s) = sig*(1 + s*(1 - sig)) with
-// sig = (1 + t)/2 gives dsil2 = 2*silu'(s) = (1 + t)*w, w = 1 + 2h - q.
+// sig = (1 + t)/2 gives dsil2 = 2*silu'(s) = (1 + t)*w, w = 1 + h*(1 - t),
+// which needs the single constant 1 (a register pair the loops keep).
 // Callers use dsil2 with the halved gg, so d*a*dsil2*wg2 = d*a*silu'(s)*gg.
 struct GatePairH {
   float2 xu, xg, a, q, dsil2;
@@ -87,7 +93,8 @@ static __device__ __forceinline__ GatePairH gate_pair_h(float2 u, float2 g, floa
   const float2 h = fma2(r.xg, wg2, cg2);
   const float2 t = make_float2(tanh_fast(h.x), tanh_fast(h.y));
   r.q = fma2(h, t, h);
-  const float2 w = fma2(r.q, splat2(-1.0f), fma2(h, splat2(2.0f), splat2(1.0f)));
+  const float2 one = splat2(1.0f);
+  const float2 w = fma2(h, sub2(one, t), one);
   r.dsil2 = fma2(t, w, w);
   return r;
 }

@@ -39,9 +39,10 @@
 // generic-to-async proxy fence; the arrive is a CTA-scope release, which a
 // cluster-scope one would stall for up to a microsecond per stage).  Each stage therefore passes through copy,
 // transform and MMA in turn; three stages of 64 K values (six of 32) keep
-// enough of them in flight for that chain.  The arithmetic is the same sequence of fp32
-// operations as the separate normalise-and-gate pass, so the A operand equals
-// that pass's Hl bit for bit.
+// enough of them in flight for that chain.  The arithmetic is that of the separate
+// normalise-and-gate pass (that pass folds the 1/2 of h = s/2 into the gate
+// norm's affine instead of multiplying by 0.5, which rounds to the same
+// value), so the A operand equals that pass's Hl bit for bit.
 #include "dg_internal.h"
 
 #ifndef DG_GATED_BK

@@ -182,8 +182,10 @@ __global__ void __launch_bounds__(NT, 512 / NT) ln_gate_fwd_kernel(
     for (int e = 0; e < 4; ++e) {
       wx[j][e] = unpack_bf16x2(w0[e]);
       cx[j][e] = unpack_bf16x2(w1[e]);
-      wg[j][e] = unpack_bf16x2(w2[e]);
-      cg[j][e] = unpack_bf16x2(w3[e]);
+      // the gate norm's affine halved (exact): h = s/2 = x_g*(gg/2) + bg/2
+      // rounds to exactly half of fma(x_g, gg, bg), so Hl is unchanged
+      wg[j][e] = mul2(unpack_bf16x2(w2[e]), splat2(0.5f));
+      cg[j][e] = mul2(unpack_bf16x2(w3[e]), splat2(0.5f));
     }
   }
   auto issue = [&](int64_t i) {
@@ -203,7 +205,6 @@ __global__ void __launch_bounds__(NT, 512 / NT) ln_gate_fwd_kernel(
 #pragma unroll
   for (int i = 0; i < kFwdStages - 1; ++i) issue(i);
   float4 st_next = n_mine > 0 ? stats[row0] : make_float4(0.f, 0.f, 0.f, 0.f);
-  const float2 half2 = make_float2(0.5f, 0.5f);
   // e4m3 output: the previous row's values wait in the other of two arrays
   // (the rows alternate between them) for that row's amax
   float oa[VPT][8], ob[VPT][8];
@@ -246,8 +247,7 @@ __global__ void __launch_bounds__(NT, 512 / NT) ln_gate_fwd_kernel(
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const float2 a = fma2(fma2(unpack_bf16x2(uw[e]), rsu, cu), wx[j][e], cx[j][e]);
-          const float2 sv = fma2(fma2(unpack_bf16x2(gw[e]), rsg, cgs), wg[j][e], cg[j][e]);
-          const float2 h = mul2(sv, half2);
+          const float2 h = fma2(fma2(unpack_bf16x2(gw[e]), rsg, cgs), wg[j][e], cg[j][e]);
           const float2 silu = fma2(h, make_float2(tanh_fast(h.x), tanh_fast(h.y)), h);
           const float2 ov = mul2(a, silu);
           o[j][2 * e] = ov.x;
@@ -412,14 +412,16 @@ __global__ void __launch_bounds__(kGfThreads, 1) ln_gate_fwd_fp8_bulk_kernel(
 #pragma unroll
       for (int j = 0; j < kGfVec; ++j) {
         const int v = v0 + 32 * kGfConsumers * j;
-        if (kFull || v < nvec) af[j] = load_affine_f(gx, bx, gg, bg, static_cast<int64_t>(rank) * H + 8 * v);
+        if (kFull || v < nvec) {
+          af[j] = load_affine_f(gx, bx, gg, bg, static_cast<int64_t>(rank) * H + 8 * v);
+          halve_gate_affine(af[j]);  // h = s/2 from one fma, exactly as in ln_gate_fwd_kernel
+        }
       }
     }
     const uint8_t* slot = gf_smem + s * slot_bytes;
     const uint4* zrow = reinterpret_cast<const uint4*>(slot);
     const float4 sr = *reinterpret_cast<const float4*>(slot + zbytes);
     const float2 rsu = splat2(sr.y), cu = splat2(-sr.x * sr.y), rsg = splat2(sr.w), cgs = splat2(-sr.z * sr.w);
-    const float2 half2 = splat2(0.5f);
     float* vrow = vbuf + (i & 1) * H;
     float amax = 0.0f;
 #pragma unroll
@@ -432,8 +434,7 @@ __global__ void __launch_bounds__(kGfThreads, 1) ln_gate_fwd_fp8_bulk_kernel(
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const float2 a = fma2(fma2(unpack_bf16x2(uw[e]), rsu, cu), af[j].wx[e], af[j].cx[e]);
-          const float2 sv = fma2(fma2(unpack_bf16x2(gw[e]), rsg, cgs), af[j].wg[e], af[j].cg[e]);
-          const float2 h = mul2(sv, half2);
+          const float2 h = fma2(fma2(unpack_bf16x2(gw[e]), rsg, cgs), af[j].wg[e], af[j].cg[e]);
           const float2 silu = fma2(h, make_float2(tanh_fast(h.x), tanh_fast(h.y)), h);
           const float2 ov = mul2(a, silu);
           o[2 * e] = ov.x;
