@@ -297,17 +297,29 @@ __global__ void __launch_bounds__(NT, 512 / NT) ln_gate_fwd_kernel(
 // and their statistics into a ring of shared-memory slots with
 // cp.async.bulk; fifteen consumer warps take two 8-column vectors a thread
 // (affines in fp32 registers), compute the row's values and its largest
-// magnitude, park the values in one of two fp32 row buffers in shared memory
-// (each thread its own columns) and release the slot.  The row amax is the
-// same lagged block reduction as in ln_gate_fwd_kernel (four mbarrier-guarded
-// slots, row i - 1 quantised while row i's shares arrive), with the warp and
-// block maxima
-// taken by redux.sync on the bit patterns: the per-thread amax is a
+// magnitude, park the values in one of kGfVbuf fp32 row buffers in shared
+// memory (each thread its own columns) and release the slot.  The row amax
+// is a lagged block reduction: each warp publishes its share of row i
+// through one of kGfSlots mbarrier-guarded slots and then quantises row
+// i - kGfLag, whose shares are complete by then unless a warp is more than
+// kGfLag rows behind (two rows of lag instead of one measured 11 % faster:
+// the warps drift apart by about a row).  A slot is rewritten kGfSlots rows
+// later; a warp publishing row j has seen every warp publish row
+// j - 1 - kGfLag, so every warp has quantised row j - 2 - 2 * kGfLag, which
+// kGfSlots >= 2 + 2 * kGfLag makes old enough.  The warp and block maxima
+// are taken by redux.sync on the bit patterns: the per-thread amax is a
 // non-negative float that is never NaN (fmaxf drops NaNs), and for those
 // the unsigned order of the bits is the order of the values.  Values and
 // codes are those of ln_gate_fwd_kernel<..., true>.  Each CTA takes a
 // contiguous range of rows.
-constexpr int kGfRing = 5;
+#ifndef DG_GF_LAG
+#define DG_GF_LAG 2
+#endif
+constexpr int kGfLag = DG_GF_LAG;                  // rows between computing a row and quantising it
+constexpr int kGfRing = kGfLag == 1 ? 5 : 4;       // Z row slots
+constexpr int kGfVbuf = kGfLag + 1;                // parked rows of fp32 values
+constexpr int kGfSlots = 8;                        // amax slots (at least 2 + 2 * kGfLag)
+static_assert(kGfSlots >= 2 + 2 * kGfLag, "amax slots");
 constexpr int kGfConsumers = 15;
 constexpr int kGfVec = 2;
 constexpr int kGfMaxH = 8 * 32 * kGfConsumers * kGfVec;
@@ -320,18 +332,18 @@ __global__ void __launch_bounds__(kGfThreads, 1) ln_gate_fwd_fp8_bulk_kernel(
     uint8_t* __restrict__ hq, float* __restrict__ hs, int64_t rows, int M, int L, int H, int slot_bytes,
     uint32_t* err) {
   extern __shared__ __align__(128) uint8_t gf_smem[];
-  float* vbuf = reinterpret_cast<float*>(gf_smem + kGfRing * slot_bytes);  // [2][H] row values
-  uint64_t* full = reinterpret_cast<uint64_t*>(vbuf + 2 * H);
+  float* vbuf = reinterpret_cast<float*>(gf_smem + kGfRing * slot_bytes);  // [kGfVbuf][H] row values
+  uint64_t* full = reinterpret_cast<uint64_t*>(vbuf + kGfVbuf * H);
   uint64_t* empty = full + kGfRing;
-  uint64_t* rbar = empty + kGfRing;                            // [4]
-  uint32_t* red = reinterpret_cast<uint32_t*>(rbar + 4);      // [4][kGfConsumers]
+  uint64_t* rbar = empty + kGfRing;                            // [kGfSlots]
+  uint32_t* red = reinterpret_cast<uint32_t*>(rbar + kGfSlots);  // [kGfSlots][kGfConsumers]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int i = 0; i < kGfRing; ++i) {
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], kGfConsumers);
     }
-    for (int b = 0; b < 4; ++b) mbar_init(&rbar[b], kGfConsumers);
+    for (int b = 0; b < kGfSlots; ++b) mbar_init(&rbar[b], kGfConsumers);
     fence_mbar_init();
   }
   griddep_wait();
@@ -379,13 +391,13 @@ __global__ void __launch_bounds__(kGfThreads, 1) ln_gate_fwd_fp8_bulk_kernel(
   uint8_t* qrow = hq + r0 * static_cast<int64_t>(H);  // code row of the row being quantised
   // quantise row k (local index) once every warp's share of its amax is in
   auto finish_row = [&](int k) -> bool {
-    const int slot = k & 3;
-    if (!__all_sync(0xffffffffu, mbar_wait(&rbar[slot], static_cast<uint32_t>(k >> 2) & 1u, err, 0x44u)))
+    const int slot = k % kGfSlots;
+    if (!__all_sync(0xffffffffu, mbar_wait(&rbar[slot], static_cast<uint32_t>(k / kGfSlots) & 1u, err, 0x44u)))
       return false;
     const uint32_t mb = __reduce_max_sync(0xffffffffu, lane < kGfConsumers ? red[slot * kGfConsumers + lane] : 0u);
     const float m = __uint_as_float(mb);
     const float inv = e4m3_inv(m);
-    const float* vrow = vbuf + (k & 1) * H;
+    const float* vrow = vbuf + (k % kGfVbuf) * H;
 #pragma unroll
     for (int j = 0; j < kGfVec; ++j) {
       const int v = v0 + 32 * kGfConsumers * j;
@@ -422,7 +434,7 @@ __global__ void __launch_bounds__(kGfThreads, 1) ln_gate_fwd_fp8_bulk_kernel(
     const uint4* zrow = reinterpret_cast<const uint4*>(slot);
     const float4 sr = *reinterpret_cast<const float4*>(slot + zbytes);
     const float2 rsu = splat2(sr.y), cu = splat2(-sr.x * sr.y), rsg = splat2(sr.w), cgs = splat2(-sr.z * sr.w);
-    float* vrow = vbuf + (i & 1) * H;
+    float* vrow = vbuf + (i % kGfVbuf) * H;
     float amax = 0.0f;
 #pragma unroll
     for (int j = 0; j < kGfVec; ++j) {
@@ -453,14 +465,15 @@ __global__ void __launch_bounds__(kGfThreads, 1) ln_gate_fwd_fp8_bulk_kernel(
     }
     const uint32_t wmax = __reduce_max_sync(0xffffffffu, __float_as_uint(amax));
     if (lane == 0) {
-      red[(i & 3) * kGfConsumers + warp] = wmax;
-      mbar_arrive(&rbar[i & 3]);
+      red[(i % kGfSlots) * kGfConsumers + warp] = wmax;
+      mbar_arrive(&rbar[i % kGfSlots]);
     }
-    return i == 0 || finish_row(i - 1);
+    return i < kGfLag || finish_row(i - kGfLag);
   };
   for (int i = 0; i < n; ++i)
     if (!do_row(i)) return;
-  if (n > 0) finish_row(n - 1);
+  for (int k = max(0, n - kGfLag); k < n; ++k)
+    if (!finish_row(k)) return;
 }
 
 // ------------------------------------------------------------------ e4m3 operands
@@ -1293,7 +1306,7 @@ cudaError_t launch_ln_gate_fwd(const void* Z, const void* stats, const void* nx_
     const int64_t rows = static_cast<int64_t>(P) * L * M;
     if (rows == 0) return cudaSuccess;
     const int slot_bytes = (4 * H + 16 + 127) / 128 * 128;
-    const int smem = kGfRing * slot_bytes + 2 * H * 4 + (2 * kGfRing + 4) * 8 + 4 * kGfConsumers * 4;
+    const int smem = kGfRing * slot_bytes + kGfVbuf * H * 4 + (2 * kGfRing + kGfSlots) * 8 + kGfSlots * kGfConsumers * 4;
     auto kern = H == kGfMaxH ? ln_gate_fwd_fp8_bulk_kernel<true> : ln_gate_fwd_fp8_bulk_kernel<false>;
     cudaError_t e = smem_attr_once(reinterpret_cast<const void*>(kern), smem);
     if (e != cudaSuccess) return e;
