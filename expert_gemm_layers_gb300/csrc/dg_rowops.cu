@@ -577,13 +577,14 @@ __global__ void transpose_quant_kernel(const __nv_bfloat16* __restrict__ w, cons
 // silu'(s) = sig(s) + s*sig(s)*(1 - sig(s)), dx_u = da*gx,
 // dU = rstd_u * (dx_u - mean(dx_u) - x_u*mean(dx_u*x_u)), and the same for G.
 //
-// Pass 1 (row sums): one warp per row sums dx_u, dx_u*x_u, dx_g, dx_g*x_g.
+// Pass 1 (row sums): per row, the sums of dx_u, dx_u*x_u, dx_g and dx_g*x_g,
+// stored with the row's statistics as a 32-byte coefficient record.
 // Pass 2 (apply): a CTA owns a column block of one token position t and a
 // range of its rows: it writes dZ and sums, per column, dU, dG (db1),
 // da*x_u, da (norm_x grads), ds*x_g, ds (norm_gate grads) in registers; the
 // per-(t, row range) partial sums are added in a fixed order afterwards.
 
-// Pass 1: one warp per row, no block barrier.  The warp walks the row in
+// Pass 1 for rows wider than 7680 columns: one warp per row, no block barrier.  The warp walks the row in
 // 256-column steps (8 columns per lane), two steps in flight, and reduces
 // the four sums with shuffles.  The affines come through L1 (a CTA's warps
 // work on consecutive rows, hence mostly on one rank).
