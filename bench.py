@@ -38,6 +38,12 @@ TP = dict(S=8192, d=4096, ffn=14336, W=8, seed=7)
 ATTN = dict(qkv_out=4096 + 2 * 1024)  # fused QKV rows of Llama-3-8B: 32 query + 2 x 8 key/value heads of 128
 
 MEASURED_PEAKS = os.path.join(ROOT, "MEASURED_PEAKS.json")
+# GB300 nominal dense tensor rates (TFLOP/s; the vendor's figures without 2:4
+# sparsity) and the maximum SM clock they are quoted at, for the second and
+# third denominators of each part: the nominal rate, and the nominal rate
+# scaled to the SM clock the step ran at.
+NOMINAL_TFLOPS = {"bf16": 2250.0, "fp8": 4500.0}
+NOMINAL_MAX_MHZ = 2070.0
 FALLBACK_PEAKS = dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0)
 
 # Per-launch DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) from
@@ -481,13 +487,18 @@ def run_dg(args, rank, world):
         part_ms["tp_swiglu"].append(m[2].elapsed_time(ends[i]))
 
     peaks = load_peaks()
+    run_mhz = (clk or {}).get("sm_mhz")
     parts = {}
     for name, vals in part_ms.items():
         pm = statistics.mean(vals)
         tf = flops[name] / (pm * 1e-3) / 1e12
         peak = (2.0 * peaks["bf16_tflops"]) if name == "fp8_gemm" else peaks["bf16_tflops"]
+        nominal = NOMINAL_TFLOPS["fp8" if name == "fp8_gemm" else "bf16"]
         parts[name] = {"ms": round(pm, 4), "ms_min": round(min(vals), 4), "ms_max": round(max(vals), 4),
-                       "tflops": round(tf, 2), "peak_tflops": peak, "frac_of_peak": round(tf / peak, 4)}
+                       "tflops": round(tf, 2), "peak_tflops": peak, "frac_of_peak": round(tf / peak, 4),
+                       "frac_of_nominal": round(tf / nominal, 4)}
+        if run_mhz:
+            parts[name]["frac_of_nominal_at_run_clock"] = round(tf / (nominal * run_mhz / NOMINAL_MAX_MHZ), 4)
     parts["fp8_gemm"]["peak_note"] = "2 x measured bf16 burst (nominal fp8:bf16 ratio 2)"
 
     # roofline of the dominant kernel (largest share of device time in the traced steps)
