@@ -39,11 +39,8 @@ ATTN = dict(qkv_out=4096 + 2 * 1024)  # fused QKV rows of Llama-3-8B: 32 query +
 
 MEASURED_PEAKS = os.path.join(ROOT, "MEASURED_PEAKS.json")
 # GB300 nominal dense tensor rates (TFLOP/s; the vendor's figures without 2:4
-# sparsity) and the maximum SM clock they are quoted at, for the second and
-# third denominators of each part: the nominal rate, and the nominal rate
-# scaled to the SM clock the step ran at.
+# sparsity), the second denominator of each part.
 NOMINAL_TFLOPS = {"bf16": 2250.0, "fp8": 4500.0}
-NOMINAL_MAX_MHZ = 2070.0
 FALLBACK_PEAKS = dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0)
 
 # Per-launch DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) from
@@ -54,18 +51,18 @@ FALLBACK_PEAKS = dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=
 # sources changed since reports null.  The capture's summary is committed with
 # the other ncu summaries of this repository.
 TRAFFIC = {
-    "ffn_gemm1": {"bytes_per_launch": 8 * 1.387412e+09, "sources": ["expert_gemm_layers_gb300/csrc/dg_gemm.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh", "expert_gemm_layers_gb300/csrc/dg_gemm_bf16_km_lnstats.cu", "expert_gemm_layers_gb300/csrc/dg_api.cu"], "sha256": "8af1a1e83e62c16914bb6c50cf736df46517636c57125c66e1e8d33436f1c6b9"},
-    "ffn_ln_stats": {"bytes_per_launch": 8 * 3.148058e+07, "sources": ["expert_gemm_layers_gb300/csrc/dg_rowops.cu", "expert_gemm_layers_gb300/csrc/dg_gate.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh"], "sha256": "bb77f856ab24f2d31376afce4833087011278392c561d3202948e3dbdf23873f"},
-    "ffn_ln_gate_fwd": {"bytes_per_launch": 8 * 1.470775e+09, "sources": ["expert_gemm_layers_gb300/csrc/dg_rowops.cu", "expert_gemm_layers_gb300/csrc/dg_gate.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh"], "sha256": "bb77f856ab24f2d31376afce4833087011278392c561d3202948e3dbdf23873f"},
-    "ffn_gemm2": {"bytes_per_launch": 8 * 9.039542e+08, "sources": ["expert_gemm_layers_gb300/csrc/dg_gemm.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh", "expert_gemm_layers_gb300/csrc/dg_gemm_bf16_km_bias.cu", "expert_gemm_layers_gb300/csrc/dg_api.cu"], "sha256": "1a42a166a43d464666f78e5b0c69e4f778e61d58820bade39421e79b852abf9d"},
-    "ffn_bwd_dhl": {"bytes_per_launch": 8 * 6.892237e+08, "sources": ["expert_gemm_layers_gb300/csrc/dg_gemm.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh", "expert_gemm_layers_gb300/csrc/dg_gemm_bf16_kk_store.cu", "expert_gemm_layers_gb300/csrc/dg_api.cu"], "sha256": "cb09ae5300c95f1679f8d6eee9fceed5f3f495ad332b153aa023173889f34842"},
-    "ffn_bwd_dwout": {"bytes_per_launch": 8 * 7.431660e+08, "sources": ["expert_gemm_layers_gb300/csrc/dg_gemm.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh", "expert_gemm_layers_gb300/csrc/dg_gemm_bf16_mm_store.cu", "expert_gemm_layers_gb300/csrc/dg_api.cu"], "sha256": "0d345dfcbed84061302bf57ad74c765f52f38be776a0a7d40b4415a03f3eaacd"},
-    "ffn_bwd_dbout": {"bytes_per_launch": 8 * 8.398950e+07, "sources": ["expert_gemm_layers_gb300/csrc/dg_rowops.cu", "expert_gemm_layers_gb300/csrc/dg_gate.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh"], "sha256": "bb77f856ab24f2d31376afce4833087011278392c561d3202948e3dbdf23873f"},
-    "ffn_bwd_ln_rowsum": {"bytes_per_launch": 8 * 1.512460e+09, "sources": ["expert_gemm_layers_gb300/csrc/dg_rowops.cu", "expert_gemm_layers_gb300/csrc/dg_gate.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh"], "sha256": "bb77f856ab24f2d31376afce4833087011278392c561d3202948e3dbdf23873f"},
-    "ffn_bwd_ln_apply": {"bytes_per_launch": 8 * 2.524076e+09, "sources": ["expert_gemm_layers_gb300/csrc/dg_rowops.cu", "expert_gemm_layers_gb300/csrc/dg_gate.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh"], "sha256": "bb77f856ab24f2d31376afce4833087011278392c561d3202948e3dbdf23873f"},
-    "ffn_bwd_grad_reduce": {"bytes_per_launch": 8 * 4.725504e+07, "sources": ["expert_gemm_layers_gb300/csrc/dg_rowops.cu", "expert_gemm_layers_gb300/csrc/dg_gate.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh"], "sha256": "bb77f856ab24f2d31376afce4833087011278392c561d3202948e3dbdf23873f"},
-    "ffn_bwd_dx": {"bytes_per_launch": 8 * 1.852506e+09, "sources": ["expert_gemm_layers_gb300/csrc/dg_gemm.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh", "expert_gemm_layers_gb300/csrc/dg_gemm_bf16_kk_store.cu", "expert_gemm_layers_gb300/csrc/dg_api.cu"], "sha256": "cb09ae5300c95f1679f8d6eee9fceed5f3f495ad332b153aa023173889f34842"},
-    "ffn_bwd_dw1": {"bytes_per_launch": 8 * 1.409293e+09, "sources": ["expert_gemm_layers_gb300/csrc/dg_gemm.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh", "expert_gemm_layers_gb300/csrc/dg_gemm_bf16_mm_store.cu", "expert_gemm_layers_gb300/csrc/dg_api.cu"], "sha256": "0d345dfcbed84061302bf57ad74c765f52f38be776a0a7d40b4415a03f3eaacd"},
+    "ffn_gemm1": {"bytes_per_launch": 8 * 1.389358e+09, "sources": ["expert_gemm_layers_gb300/csrc/dg_gemm.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh", "expert_gemm_layers_gb300/csrc/dg_gemm_bf16_km_lnstats.cu", "expert_gemm_layers_gb300/csrc/dg_api.cu"], "sha256": "6f5d5bb788ec31cd4eadff3af767fbf38b2f00fb9e700f83adbe6d37c2e58ce9"},
+    "ffn_ln_stats": {"bytes_per_launch": 8 * 3.147341e+07, "sources": ["expert_gemm_layers_gb300/csrc/dg_rowops.cu", "expert_gemm_layers_gb300/csrc/dg_gate.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh"], "sha256": "070f3ba90f80902fa2dffa524380bba6013dc6dab8f58248a4b7b7ba8daaf711"},
+    "ffn_gemm2_gated": {"bytes_per_launch": 8 * 1.573220e+09, "sources": ["expert_gemm_layers_gb300/csrc/dg_gemm_gated.cu", "expert_gemm_layers_gb300/csrc/dg_gate.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh", "expert_gemm_layers_gb300/csrc/dg_api.cu"], "sha256": "561932b9d744a48b99a81ff6f5d226bcf6b2e1b5f1fc914d9f9b5d8689248ffe"},
+    "ffn_gemm2_rest": {"bytes_per_launch": 8 * 7.041393e+08, "sources": ["expert_gemm_layers_gb300/csrc/dg_gemm.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh", "expert_gemm_layers_gb300/csrc/dg_gemm_bf16_km_bias.cu", "expert_gemm_layers_gb300/csrc/dg_api.cu"], "sha256": "28a307d71a17aa0f8f43cae379bd59bc34f29e25f752988f9e06479f3c2f2dfb"},
+    "ffn_bwd_dhl": {"bytes_per_launch": 8 * 6.898706e+08, "sources": ["expert_gemm_layers_gb300/csrc/dg_gemm.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh", "expert_gemm_layers_gb300/csrc/dg_gemm_bf16_kk_store.cu", "expert_gemm_layers_gb300/csrc/dg_api.cu"], "sha256": "8a59cbfdb1e0196befc7f7a106e94370b22edb6f77dc1414b4ac6962a2e8da17"},
+    "ffn_bwd_dwout": {"bytes_per_launch": 8 * 7.538304e+08, "sources": ["expert_gemm_layers_gb300/csrc/dg_gemm.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh", "expert_gemm_layers_gb300/csrc/dg_gemm_bf16_mm_store.cu", "expert_gemm_layers_gb300/csrc/dg_api.cu"], "sha256": "fbe7eae26e7178c268aabb26011175fee575e881adddf5b70f58aa7f9c0d495c"},
+    "ffn_bwd_dbout": {"bytes_per_launch": 8 * 8.392499e+07, "sources": ["expert_gemm_layers_gb300/csrc/dg_rowops.cu", "expert_gemm_layers_gb300/csrc/dg_gate.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh"], "sha256": "070f3ba90f80902fa2dffa524380bba6013dc6dab8f58248a4b7b7ba8daaf711"},
+    "ffn_bwd_ln_rowsum": {"bytes_per_launch": 8 * 1.512544e+09, "sources": ["expert_gemm_layers_gb300/csrc/dg_rowops.cu", "expert_gemm_layers_gb300/csrc/dg_gate.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh"], "sha256": "070f3ba90f80902fa2dffa524380bba6013dc6dab8f58248a4b7b7ba8daaf711"},
+    "ffn_bwd_ln_apply": {"bytes_per_launch": 8 * 2.524226e+09, "sources": ["expert_gemm_layers_gb300/csrc/dg_rowops.cu", "expert_gemm_layers_gb300/csrc/dg_gate.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh"], "sha256": "070f3ba90f80902fa2dffa524380bba6013dc6dab8f58248a4b7b7ba8daaf711"},
+    "ffn_bwd_grad_reduce": {"bytes_per_launch": 8 * 4.725274e+07, "sources": ["expert_gemm_layers_gb300/csrc/dg_rowops.cu", "expert_gemm_layers_gb300/csrc/dg_gate.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh"], "sha256": "070f3ba90f80902fa2dffa524380bba6013dc6dab8f58248a4b7b7ba8daaf711"},
+    "ffn_bwd_dx": {"bytes_per_launch": 8 * 2.168298e+09, "sources": ["expert_gemm_layers_gb300/csrc/dg_gemm.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh", "expert_gemm_layers_gb300/csrc/dg_gemm_bf16_kk_store.cu", "expert_gemm_layers_gb300/csrc/dg_api.cu"], "sha256": "8a59cbfdb1e0196befc7f7a106e94370b22edb6f77dc1414b4ac6962a2e8da17"},
+    "ffn_bwd_dw1": {"bytes_per_launch": 8 * 1.514869e+09, "sources": ["expert_gemm_layers_gb300/csrc/dg_gemm.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh", "expert_gemm_layers_gb300/csrc/dg_gemm_bf16_mm_store.cu", "expert_gemm_layers_gb300/csrc/dg_api.cu"], "sha256": "fbe7eae26e7178c268aabb26011175fee575e881adddf5b70f58aa7f9c0d495c"},
 }
 
 
@@ -101,8 +98,12 @@ def load_peaks():
     try:
         with open(MEASURED_PEAKS) as fh:
             p = json.load(fh)
-        return dict(hbm_gbs=float(p["hbm_gbs"]), bf16_tflops=float(p["bf16_tflops"]),
-                    bf16_tflops_sustained=float(p["bf16_tflops_sustained"]), source="measured")
+        out = dict(hbm_gbs=float(p["hbm_gbs"]), bf16_tflops=float(p["bf16_tflops"]),
+                   bf16_tflops_sustained=float(p["bf16_tflops_sustained"]), source="measured")
+        mhz = (p.get("clocks_under_load") or {}).get("sm_mhz_median")
+        if mhz:
+            out["sustained_sm_mhz"] = float(mhz)  # median SM clock of the sustained measurement
+        return out
     except Exception:
         return dict(FALLBACK_PEAKS, source="fallback")
 
@@ -497,8 +498,11 @@ def run_dg(args, rank, world):
         parts[name] = {"ms": round(pm, 4), "ms_min": round(min(vals), 4), "ms_max": round(max(vals), 4),
                        "tflops": round(tf, 2), "peak_tflops": peak, "frac_of_peak": round(tf / peak, 4),
                        "frac_of_nominal": round(tf / nominal, 4)}
-        if run_mhz:
-            parts[name]["frac_of_nominal_at_run_clock"] = round(tf / (nominal * run_mhz / NOMINAL_MAX_MHZ), 4)
+        if run_mhz and peaks.get("sustained_sm_mhz"):
+            # the measured sustained rate per MHz of its own clock, at the clock the step ran at
+            at_clock = peaks["bf16_tflops_sustained"] * (2.0 if name == "fp8_gemm" else 1.0) * run_mhz / \
+                peaks["sustained_sm_mhz"]
+            parts[name]["frac_of_sustained_at_run_clock"] = round(tf / at_clock, 4)
     parts["fp8_gemm"]["peak_note"] = "2 x measured bf16 burst (nominal fp8:bf16 ratio 2)"
 
     # roofline of the dominant kernel (largest share of device time in the traced steps)
@@ -699,24 +703,23 @@ def _timed(run, iters, dev):
 
 def run_ffn_forward_variants(w, args, dev, peaks):
     """The FFN forward at the step's shape in four forms, timed alone (outside
-    the step, same box and run): training with the separate normalise-and-gate
-    pass (the default, as in the step) and with the normalise-and-gate computed
-    by the second GEMM's producer warps; inference (nothing saved) in both
-    forms, the fused one without Hl scratch."""
+    the step, same box and run): training with the normalise-and-gate computed
+    by the second GEMM's producer warps (the default, as in the step) and with
+    the separate pass through HBM; inference (nothing saved) in both forms."""
     import ctypes
     dg = w.dg
     lib = dg._lib.load()
     sh = dg.ffn_shape(FFN["P"], FFN["B"], FFN["T"], FFN["D"], FFN["k"])
     ws_inf = dg.alloc_workspace(lib.dg_a2a_ffn_fwd_workspace_bytes(ctypes.byref(sh), 1, 0), dev)
-    ws_inf_fused = dg.alloc_workspace(lib.dg_a2a_ffn_fwd_workspace_bytes(ctypes.byref(sh), 1, dg.DG_FFN_FUSED_GATE),
-                                      dev)
+    ws_inf_sep = dg.alloc_workspace(
+        lib.dg_a2a_ffn_fwd_workspace_bytes(ctypes.byref(sh), 1, dg.DG_FFN_SEPARATE_GATE), dev)
     variants = {
-        "separate_gate": lambda: dg.a2a_ffn_forward(w.x, w.params, saved=w.saved, out=w.out),
-        "fused_gate": lambda: dg.a2a_ffn_forward(w.x, w.params, saved=w.saved, out=w.out,
-                                                 flags=dg.DG_FFN_FUSED_GATE),
-        "inference": lambda: dg.a2a_ffn_forward(w.x, w.params, out=w.out, inference=True, ws=ws_inf),
-        "inference_fused_gate": lambda: dg.a2a_ffn_forward(w.x, w.params, out=w.out, inference=True, ws=ws_inf_fused,
-                                                           flags=dg.DG_FFN_FUSED_GATE),
+        "fused_gate": lambda: dg.a2a_ffn_forward(w.x, w.params, saved=w.saved, out=w.out),
+        "separate_gate": lambda: dg.a2a_ffn_forward(w.x, w.params, saved=w.saved, out=w.out,
+                                                    flags=dg.DG_FFN_SEPARATE_GATE),
+        "inference_fused_gate": lambda: dg.a2a_ffn_forward(w.x, w.params, out=w.out, inference=True, ws=ws_inf),
+        "inference_separate_gate": lambda: dg.a2a_ffn_forward(w.x, w.params, out=w.out, inference=True,
+                                                              ws=ws_inf_sep, flags=dg.DG_FFN_SEPARATE_GATE),
     }
     flops = gemm_flops()["ffn_fwd"]
     res = {}
@@ -729,14 +732,14 @@ def run_ffn_forward_variants(w, args, dev, peaks):
             if prev is None or ms < prev["ms"]:
                 res[name] = {"ms": round(ms, 4), "tflops": round(tf, 2), "peak_tflops": peaks["bf16_tflops"],
                              "frac_of_peak": round(tf / peaks["bf16_tflops"], 4), "kernels_ms": kernels}
-    for wsx in (ws_inf, ws_inf_fused):
+    for wsx in (ws_inf, ws_inf_sep):
         st, code = dg.device_status(dev, workspace=wsx)
         if st != 0:
             raise RuntimeError(f"device error word after the FFN forward variants: {code:#x}")
     st, code = w.status()
     if st != 0:
         raise RuntimeError(f"device error word after the FFN forward variants: {code:#x}")
-    del ws_inf, ws_inf_fused
+    del ws_inf, ws_inf_sep
     return {"ffn_fwd_variants": dict(res, note="best of two rounds of 5 back-to-back calls each")}
 
 
@@ -924,7 +927,7 @@ def run_e2e(w, args, dev, step_flops, world):
 PROFILE_CASES = {
     "fp8": "FP8 GEMM 4096^3 (alpha 0.5, beta 1)",
     "ffn_fwd_small": "A2A FFN forward, P=8, B=512, T=8, D=1280, k=6 (the full shape with 8 token positions)",
-    "ffn_fwd_small_fused": "the same forward with the normalise-and-gate in the second GEMM's producer warps",
+    "ffn_fwd_small_separate": "the same forward with the normalise-and-gate as a separate pass through HBM",
     "ffn_small": "A2A FFN forward + backward, P=8, B=512, T=8, D=1280, k=6",
     "tp": "TP SwiGLU, S=8192, d=4096, ffn=14336, W=8",
     "ffn_fp8_small": "A2A FFN forward on e4m3 GEMMs, P=8, B=512, T=8, D=1280, k=6",
@@ -944,12 +947,12 @@ def run_profile_case(args):
         A, B, C = synth.fp8_gemm_inputs(4096, 4096, 4096, seed=1, device=dev)
         D = torch.empty((4096, 4096), dtype=torch.bfloat16, device=dev)
         run = lambda: dg.gemm_fp8(A, B, C, 0.5, 1.0, out=D)
-    elif case in ("ffn_fwd_small", "ffn_small", "ffn_fwd_small_fused"):
+    elif case in ("ffn_fwd_small", "ffn_small", "ffn_fwd_small_separate"):
         t = synth.ffn_inputs(8, 512, 8, 1280, 6, seed=42, device=dev)
         params = {n: t[n] for n in dg.FFN_PARAM_NAMES}
         x = t["inputs"]
         dY = synth.ffn_grad_output(8, 512, 8, 1280, seed=43, device=dev)
-        flags = dg.DG_FFN_FUSED_GATE if case == "ffn_fwd_small_fused" else 0
+        flags = dg.DG_FFN_SEPARATE_GATE if case == "ffn_fwd_small_separate" else 0
 
         def run():
             out, saved = dg.a2a_ffn_forward(x, params, flags=flags)

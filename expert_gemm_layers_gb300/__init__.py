@@ -15,14 +15,16 @@ TMA/mbarrier pipelines):
 
 The library is loaded lazily on first use and fails loudly if it is missing.
 """
-from .ops import (A2AFFN, DG_FFN_COMP_ONLY, DG_FFN_FUSED_GATE, FFN_PARAM_NAMES, TPSwiGLU, a2a_combine,
+from .ops import (A2AFFN, DG_FFN_COMP_ONLY, DG_FFN_FUSED_GATE, DG_FFN_SEPARATE_GATE, FFN_PARAM_NAMES, TPSwiGLU,
+                  a2a_combine,
                   a2a_dispatch, a2a_ffn, a2a_ffn_backward, a2a_ffn_forward, a2a_ffn_forward_fp8,
                   a2a_ffn_fp8_pack_weights, alloc_workspace, debug_wait_timeout, device_status, error_block,
                   ffn_shape, gemm_fp8, tp_swiglu, tp_linear, tp_linear_backward, tp_linear_layer, TPLinear,
                   tp_swiglu_backward, tp_swiglu_layer, trace_begin, trace_end)
 
 __all__ = [
-    "A2AFFN", "DG_FFN_COMP_ONLY", "DG_FFN_FUSED_GATE", "FFN_PARAM_NAMES", "a2a_combine", "a2a_dispatch",
+    "A2AFFN", "DG_FFN_COMP_ONLY", "DG_FFN_FUSED_GATE", "DG_FFN_SEPARATE_GATE", "FFN_PARAM_NAMES", "a2a_combine",
+    "a2a_dispatch",
     "a2a_ffn", "a2a_ffn_backward", "a2a_ffn_forward", "a2a_ffn_forward_fp8", "a2a_ffn_fp8_pack_weights",
     "alloc_workspace", "debug_wait_timeout", "device_status", "error_block", "ffn_shape", "gemm_fp8", "tp_swiglu",
     "tp_swiglu_backward", "TPSwiGLU", "tp_swiglu_layer", "tp_linear", "tp_linear_backward", "TPLinear",

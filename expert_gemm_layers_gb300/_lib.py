@@ -41,6 +41,7 @@ class TraceEntry(ctypes.Structure):
 DG_ERROR_BLOCK_BYTES = 256
 DG_FFN_COMP_ONLY = 1
 DG_FFN_FUSED_GATE = 2
+DG_FFN_SEPARATE_GATE = 4
 
 SIGNATURES = {
     "dg_last_error": (ctypes.c_char_p, []),

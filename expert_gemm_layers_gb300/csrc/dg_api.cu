@@ -482,18 +482,23 @@ dg_status dg_gemm_fp8(int64_t M, int64_t N, int64_t K, const void* A, const void
 
 namespace {
 
-constexpr uint32_t kFfnFlagsKnown = DG_FFN_COMP_ONLY | DG_FFN_FUSED_GATE;
+constexpr uint32_t kFfnFlagsKnown = DG_FFN_COMP_ONLY | DG_FFN_FUSED_GATE | DG_FFN_SEPARATE_GATE;
 
 dg_status check_ffn_flags(const FfnDims& f, uint32_t flags, uint32_t allowed, const char* what) {
   if (flags & ~allowed) return fail(DG_ERR_INVALID_ARGUMENT, "%s: unknown flags 0x%x", what, flags & ~allowed);
+  if ((flags & DG_FFN_FUSED_GATE) && (flags & DG_FFN_SEPARATE_GATE))
+    return fail(DG_ERR_INVALID_ARGUMENT, "%s: DG_FFN_FUSED_GATE and DG_FFN_SEPARATE_GATE exclude each other", what);
   (void)f;
   return DG_OK;
 }
 
+// The normalise-and-gate runs inside GEMM2 unless the separate pass is asked for.
+inline bool ffn_fused_gate(uint32_t flags) { return !(flags & DG_FFN_SEPARATE_GATE); }
+
 // The forward's workspace: the error block, then (DG_FFN_COMP_ONLY) the
 // rank/slice-swapped input and output, then (inference, saved == NULL) the
 // Z, statistics and per-tile partials that would otherwise live in `saved`,
-// and Hl when the separate normalise-and-gate pass is asked for.
+// and Hl unless the gated GEMM covers all of D in one column pass.
 struct FwdWsLayout {
   size_t perm_in, perm_out, z, stats, part, hl, total;
 };
@@ -516,7 +521,7 @@ FwdWsLayout fwd_ws_layout(const FfnDims& f, bool inference, uint32_t flags) {
     off = round_up(off + rows * 16, 256);
     l.part = off;
     off = round_up(off + rows * tiles_n * 16, 256);
-    if (!(flags & DG_FFN_FUSED_GATE)) {
+    if (!ffn_fused_gate(flags) || f.D > gemm_gated_tile_n()) {
       l.hl = off;
       off = round_up(off + rows * f.H * 2, 256);
     }
@@ -535,7 +540,9 @@ size_t dg_a2a_ffn_saved_bytes(const dg_ffn_shape* shape) {
 
 size_t dg_a2a_ffn_fwd_workspace_bytes(const dg_ffn_shape* shape, int32_t inference, uint32_t flags) {
   FfnDims f{};
-  if (check_ffn_shape(shape, &f) != DG_OK || (flags & ~kFfnFlagsKnown)) return 0;
+  if (check_ffn_shape(shape, &f) != DG_OK || (flags & ~kFfnFlagsKnown) ||
+      ((flags & DG_FFN_FUSED_GATE) && (flags & DG_FFN_SEPARATE_GATE)))
+    return 0;
   return fwd_ws_layout(f, inference != 0, flags).total;
 }
 
@@ -579,7 +586,8 @@ dg_status dg_a2a_ffn_fwd(const dg_ffn_shape* shape, const void* inputs, const vo
   void* Z = inference ? w + wl.z : sv + sl.z;
   void* stats = inference ? w + wl.stats : sv + sl.stats;
   void* part = inference ? w + wl.part : sv + sl.part;
-  void* Hl = inference ? ((flags & DG_FFN_FUSED_GATE) ? nullptr : w + wl.hl) : sv + sl.hl;
+  void* Hl = inference ? (ffn_fused_gate(flags) && f.D <= gemm_gated_tile_n() ? nullptr : w + wl.hl)
+                       : sv + sl.hl;
   const uint64_t T = f.T, M = f.M, D = f.D, H = f.H;
   const double rows = static_cast<double>(T) * M;
   cudaError_t e;
@@ -634,9 +642,12 @@ dg_status dg_a2a_ffn_fwd(const dg_ffn_shape* shape, const void* inputs, const vo
   if (e != cudaSuccess) return cuda_fail(e, "LayerNorm statistics launch");
 
   // GEMM2: output rows (s, b, t) = Hl_t @ wout_t + bout_t at the combine offsets,
-  // with Hl = LN_x(U) * silu(LN_g(G)) either computed by a separate pass
-  // through HBM (the default, the faster of the two) or, with
-  // DG_FFN_FUSED_GATE, by the GEMM's own producer warps from Z.
+  // with Hl = LN_x(U) * silu(LN_g(G)) computed by the GEMM's own producer
+  // warps from Z (the default) or, with DG_FFN_SEPARATE_GATE, by a separate
+  // pass through HBM.  The gated GEMM covers the first column pass (up to
+  // gemm_gated_tile_n() output columns) and stores Hl as it goes; a plain
+  // GEMM2 on that Hl computes the remaining columns, so the gate is computed
+  // once, not once per column pass.
   CUtensorMap mwo, mo;
   int32_t wo_mn4 = 0;
   if ((st = make_map_mn(&mwo, wout, D, H, T, D * 2, H * D * 2, 64, 1, kMnBlocksB, &wo_mn4, "wout")) != DG_OK)
@@ -653,7 +664,7 @@ dg_status dg_a2a_ffn_fwd(const dg_ffn_shape* shape, const void* inputs, const vo
   p2.d_g = G_MID;
   p2.bias = static_cast<const __nv_bfloat16*>(bout);
   p2.bias_g_stride = static_cast<int64_t>(D);
-  if (flags & DG_FFN_FUSED_GATE) {
+  if (ffn_fused_gate(flags)) {
     GateSrc q{};
     q.Z = static_cast<const __nv_bfloat16*>(Z);
     q.stats = static_cast<const float4*>(stats);
@@ -664,7 +675,8 @@ dg_status dg_a2a_ffn_fwd(const dg_ffn_shape* shape, const void* inputs, const vo
     q.Hl = static_cast<__nv_bfloat16*>(Hl);
     q.H = static_cast<int32_t>(H);
     q.L = static_cast<int32_t>(f.L);
-    const double bytes = rows * (2.0 * 2 * H + 16.0 + 2.0 * D) + 2.0 * static_cast<double>(T) * H * D +
+    const int64_t n_fused = D < gemm_gated_tile_n() ? D : gemm_gated_tile_n();
+    const double bytes = rows * (2.0 * 2 * H + 16.0 + 2.0 * n_fused) + 2.0 * static_cast<double>(T) * H * n_fused +
                          (Hl ? rows * 2.0 * H : 0.0);
     // Z by rows, U at x = k and G at x = H + k, and wout, in boxes of the gated
     // GEMM's K block (BK columns of Z with a 2*BK-byte swizzle; BK rows of wout)
@@ -676,7 +688,29 @@ dg_status dg_a2a_ffn_fwd(const dg_ffn_shape* shape, const void* inputs, const vo
     if ((st = make_map_mn(&mwok, wout, D, H, T, D * 2, H * D * 2, bk, 1, kMnBlocksB, &p2.b_mn4, "wout")) != DG_OK)
       return st;
     mwo = mwok;
-    if ((st = run_gemm_gated(mwo, mo, mzk, p2, q, dev, s, "ffn_gemm2_gated", bytes)) != DG_OK) return st;
+    GemmParams pf = p2;
+    pf.N = static_cast<int32_t>(n_fused);
+    if ((st = run_gemm_gated(mwo, mo, mzk, pf, q, dev, s, "ffn_gemm2_gated", bytes)) != DG_OK) return st;
+    if (D > n_fused) {
+      // columns [n_fused, D): a plain GEMM2 on the Hl the gated pass stored
+      const int64_t rest = D - n_fused;
+      CUtensorMap mh, mwor, mor;
+      GemmParams pr = p2;
+      pr.N = static_cast<int32_t>(rest);
+      pr.bias = static_cast<const __nv_bfloat16*>(bout) + n_fused;
+      const __nv_bfloat16* wout_r = static_cast<const __nv_bfloat16*>(wout) + n_fused;
+      __nv_bfloat16* y_r = static_cast<__nv_bfloat16*>(y_out) + n_fused;
+      if ((st = make_map_3d(&mh, true, Hl, H, M, T, H * 2, M * H * 2, 64, 128, 1, "Hl")) != DG_OK) return st;
+      if ((st = make_map_mn(&mwor, wout_r, rest, H, T, D * 2, H * D * 2, 64, 1, kMnBlocksB, &pr.b_mn4,
+                            "wout (remaining columns)")) != DG_OK)
+        return st;
+      if ((st = make_map_3d(&mor, true, y_r, rest, T, M, D * 2, T * D * 2, 64, 1, 32, "output (remaining columns)")) !=
+          DG_OK)
+        return st;
+      if ((st = run_gemm(GV_BF16_KM_BIAS, mh, mwor, mor, mor, pr, dev, s, "ffn_gemm2_rest",
+                         2.0 * (rows * H + static_cast<double>(T) * H * rest + rows * rest))) != DG_OK)
+        return st;
+    }
   } else {
     {
       TraceScope trace("ffn_ln_gate_fwd", s, 0.0, rows * (2.0 * 2 * H + 2.0 * H + 16.0));

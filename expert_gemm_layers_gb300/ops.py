@@ -10,7 +10,8 @@ import ctypes
 
 import torch
 
-from ._lib import DG_ERROR_BLOCK_BYTES, DG_FFN_COMP_ONLY, DG_FFN_FUSED_GATE, FFNShape, TraceEntry, check, load
+from ._lib import (DG_ERROR_BLOCK_BYTES, DG_FFN_COMP_ONLY, DG_FFN_FUSED_GATE, DG_FFN_SEPARATE_GATE, FFNShape,
+                   TraceEntry, check, load)
 
 __all__ = [
     "gemm_fp8", "ffn_shape", "a2a_ffn_forward", "a2a_ffn_backward", "a2a_ffn_fp8_pack_weights", "a2a_ffn_forward_fp8", "A2AFFN", "a2a_ffn",
@@ -18,6 +19,7 @@ __all__ = [
     "tp_linear", "tp_linear_backward", "TPLinear", "tp_linear_layer", "device_status", "debug_wait_timeout",
     "FFN_PARAM_NAMES", "trace_begin", "trace_end", "alloc_workspace", "error_block", "DG_FFN_COMP_ONLY",
     "DG_FFN_FUSED_GATE",
+    "DG_FFN_SEPARATE_GATE",
 ]
 
 FFN_PARAM_NAMES = ("w1", "b1", "wout", "bout", "nx_w", "nx_b", "ng_w", "ng_b")
@@ -116,7 +118,8 @@ def a2a_ffn_forward(inputs: torch.Tensor, params: dict, eps: float = 1e-5, saved
     bout [P,L,D], nx_w/nx_b/ng_w/ng_b [P,H] (bf16), where k = 2H/(2D) is read
     from w1.  Returns (output [P,B,T,D], saved) where `saved` is the opaque
     byte buffer the backward needs (None with inference=True: nothing is
-    kept).  flags: DG_FFN_COMP_ONLY, DG_FFN_FUSED_GATE.
+    kept).  flags: DG_FFN_COMP_ONLY; DG_FFN_SEPARATE_GATE (the gate as a
+    separate pass instead of inside GEMM2) or DG_FFN_FUSED_GATE (the default).
     """
     lib = load()
     P, B, T, D = inputs.shape

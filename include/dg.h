@@ -124,18 +124,23 @@ dg_status dg_gemm_fp8(int64_t M, int64_t N, int64_t K,
  * saved  (size dg_a2a_ffn_saved_bytes) training: the forward writes Z, Hl
  *        and the per-row LayerNorm statistics there, and the backward reads
  *        them.  NULL = inference: nothing is kept, and Z, the statistics
- *        (and Hl, unless DG_FFN_FUSED_GATE) live in the workspace instead.
+ *        and Hl live in the workspace instead (Hl only when D is wider than
+ *        one column pass of the gated GEMM, 512, or with
+ *        DG_FFN_SEPARATE_GATE).
  * ws     size dg_a2a_ffn_fwd_workspace_bytes(shape, saved == NULL, flags):
  *        the error block, plus the inference scratch and the comp_only
  *        buffers when they apply.
  * flags  DG_FFN_COMP_ONLY: no exchange; each rank's own [B, T, D] rows, viewed
  *        as [B, P, L, D], feed its L slices (the project statement's
  *        comp_only mode of forward_ffn; the output keeps the input's layout).
- *        DG_FFN_FUSED_GATE: compute Hl inside the second GEMM, by producer
- *        warps that normalise and gate Z while building its A operand,
- *        instead of in a separate pass through HBM.  Same results bit for
- *        bit; slower at the page's shapes, but an inference call then needs
- *        no Hl scratch (rows x H bf16 less workspace).
+ *        The normalise-and-gate is computed inside the second GEMM by
+ *        default: producer warps normalise and gate Z while building its A
+ *        operand for the first 512 output columns and store Hl as they go,
+ *        and a plain GEMM on that Hl computes the remaining columns.
+ *        DG_FFN_SEPARATE_GATE: compute Hl in a separate pass through HBM
+ *        first, then the whole second GEMM on it.  Same results bit for bit
+ *        (slower at the page's shapes).  DG_FFN_FUSED_GATE asks for the
+ *        default explicitly; giving both is an invalid argument.
  * ------------------------------------------------------------------------ */
 typedef struct {
   int32_t P, B, T, D, k;
@@ -144,6 +149,7 @@ typedef struct {
 
 #define DG_FFN_COMP_ONLY 1u
 #define DG_FFN_FUSED_GATE 2u
+#define DG_FFN_SEPARATE_GATE 4u
 
 size_t dg_a2a_ffn_saved_bytes(const dg_ffn_shape* shape);
 size_t dg_a2a_ffn_fwd_workspace_bytes(const dg_ffn_shape* shape, int32_t inference, uint32_t flags);

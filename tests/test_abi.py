@@ -68,10 +68,18 @@ def test_ffn_saved_and_workspace_sizes(lib):
     assert lib.dg_a2a_ffn_fwd_workspace_bytes(ctypes.byref(sh), 0, 0) == 256
     inf = lib.dg_a2a_ffn_fwd_workspace_bytes(ctypes.byref(sh), 1, 0)
     assert inf >= 256 + rows * (2 * H * 2 + 16 + H * 2)
-    # with the gate fused into the second GEMM, inference needs no Hl scratch
-    assert lib.dg_a2a_ffn_fwd_workspace_bytes(ctypes.byref(sh), 1, 2) <= inf - rows * H * 2
+    # with the gate fused into the second GEMM (the default), inference needs Hl scratch only when D is
+    # wider than one gated column pass (512 columns): the remaining columns come from a plain GEMM on the Hl
+    # it stores; the separate pass (flag 4) always needs it
+    assert lib.dg_a2a_ffn_fwd_workspace_bytes(ctypes.byref(sh), 1, 4) == inf
+    assert lib.dg_a2a_ffn_fwd_workspace_bytes(ctypes.byref(sh), 1, 2) == inf
+    narrow = _shape(2, 4, 16, 512, 2)
+    rows_n, H_n = 16 * 8, 1024
+    inf_n = lib.dg_a2a_ffn_fwd_workspace_bytes(ctypes.byref(narrow), 1, 4)
+    assert lib.dg_a2a_ffn_fwd_workspace_bytes(ctypes.byref(narrow), 1, 0) <= inf_n - rows_n * H_n * 2
+    assert lib.dg_a2a_ffn_fwd_workspace_bytes(ctypes.byref(sh), 1, 2 | 4) == 0         # exclusive flags
     assert lib.dg_a2a_ffn_fwd_workspace_bytes(ctypes.byref(sh), 0, 1) >= 256 + 2 * act
-    assert lib.dg_a2a_ffn_fwd_workspace_bytes(ctypes.byref(sh), 0, 4) == 0             # unknown flag
+    assert lib.dg_a2a_ffn_fwd_workspace_bytes(ctypes.byref(sh), 0, 8) == 0             # unknown flag
 
 
 def _aligned(buf):
@@ -90,9 +98,11 @@ def test_ffn_flags_and_error_block_checked_before_the_device(lib):
     buf = ctypes.create_string_buffer(12 << 16)
     p = [_aligned(buf) + (i << 16) for i in range(11)]   # distinct, non-overlapping stand-ins
     args = [ctypes.byref(sh)] + p[:10]
-    # an unknown flag
-    st = lib.dg_a2a_ffn_fwd(*args, None, 0, p[10], 256, 4, None)
+    # an unknown flag, and the two gate flags together
+    st = lib.dg_a2a_ffn_fwd(*args, None, 0, p[10], 256, 8, None)
     assert STATUS_NAMES[st] == "DG_ERR_INVALID_ARGUMENT" and b"flags" in lib.dg_last_error()
+    st = lib.dg_a2a_ffn_fwd(*args, None, 0, p[10], 256, 2 | 4, None)
+    assert STATUS_NAMES[st] == "DG_ERR_INVALID_ARGUMENT" and b"exclude" in lib.dg_last_error()
     # no workspace at all: the error block is missing
     st = lib.dg_a2a_ffn_fwd(*args, None, 0, None, 0, 0, None)
     assert STATUS_NAMES[st] == "DG_ERR_WORKSPACE" and b"error block" in lib.dg_last_error()

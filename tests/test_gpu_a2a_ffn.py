@@ -13,7 +13,8 @@ import torch
 
 import oracle as O
 import expert_gemm_layers_gb300 as dg
-from expert_gemm_layers_gb300 import (DG_FFN_COMP_ONLY, DG_FFN_FUSED_GATE, FFN_PARAM_NAMES, a2a_combine,
+from expert_gemm_layers_gb300 import (DG_FFN_COMP_ONLY, DG_FFN_FUSED_GATE, DG_FFN_SEPARATE_GATE, FFN_PARAM_NAMES,
+                                      a2a_combine,
                                       a2a_dispatch, a2a_ffn, a2a_ffn_backward, a2a_ffn_forward, synth)
 from _compare import TOL_BF16, assert_close, err_fro
 
@@ -121,7 +122,7 @@ def test_forward_closed_form_constant_halves():
     assert_close(out, ref, 1e-2, "closed form")
 
 
-@pytest.mark.parametrize("flags", [0, DG_FFN_FUSED_GATE])
+@pytest.mark.parametrize("flags", [0, DG_FFN_SEPARATE_GATE])
 @pytest.mark.parametrize("half", [0, 1])
 def test_gate_elementwise_error_bound(half, flags):
     """Every gate value Hl against the fp64 gate, with an elementwise bound.
@@ -303,35 +304,41 @@ def test_shape_sweep_forward_backward(P, B, T, D, k):
         assert err_fro(got, r) <= TOL_BF16, name
 
 
-# ------------------------------------------------------------------ normalise-and-gate in GEMM2's producer (DG_FFN_FUSED_GATE)
+# ------------------------------------------------------------------ normalise-and-gate in GEMM2's producer (the default) or a separate pass
 
 FOLD_SHAPES = SMALL_SHAPES + [
-    (2, 300, 4, 1280, 2),   # M = 600 (three row tiles, the last ragged), N = 1280 (passes of 512, 512, 256)
+    (2, 300, 4, 1280, 2),   # M = 600 (three row tiles, the last ragged), N = 1280 (one gated pass of 512, then 768)
+    (2, 8, 2, 520, 2),      # N = 520: a gated pass of 512 and a plain GEMM over the last 8 columns
     (2, 128, 2, 1280, 6),   # H = 7680, the full width of the page's default workload
 ]
 
 
 @pytest.mark.parametrize("P,B,T,D,k", FOLD_SHAPES)
 def test_fused_gate_equals_separate_pass_bit_for_bit(P, B, T, D, k):
-    # with DG_FFN_FUSED_GATE the producer warps of GEMM2 compute Hl with the same
-    # fp32 operations as the separate pass, so the output, and everything the
-    # forward saves, match exactly
+    # the producer warps of the gated GEMM2 compute Hl to the same values as the
+    # separate pass (DG_FFN_SEPARATE_GATE), and both GEMM2 variants add the same
+    # products in the same order, so the output, and everything the forward
+    # saves, match exactly
     inputs, params = _inputs(P, B, T, D, k, seed=91 + D + k, device=DEV)
     sh = dg._lib.FFNShape(P, B, T, D, k, 1e-5)
     nbytes = dg._lib.load().dg_a2a_ffn_saved_bytes(__import__("ctypes").byref(sh))
     sv_sep = torch.zeros(nbytes, dtype=torch.uint8, device=DEV)
     sv_fused = torch.zeros(nbytes, dtype=torch.uint8, device=DEV)
-    out_sep, _ = a2a_ffn_forward(inputs, params, saved=sv_sep)
-    out_fused, _ = a2a_ffn_forward(inputs, params, saved=sv_fused, flags=DG_FFN_FUSED_GATE)
+    sv_explicit = torch.zeros(nbytes, dtype=torch.uint8, device=DEV)
+    out_sep, _ = a2a_ffn_forward(inputs, params, saved=sv_sep, flags=DG_FFN_SEPARATE_GATE)
+    out_fused, _ = a2a_ffn_forward(inputs, params, saved=sv_fused)
+    out_explicit, _ = a2a_ffn_forward(inputs, params, saved=sv_explicit, flags=DG_FFN_FUSED_GATE)
     torch.cuda.synchronize()
     assert torch.equal(out_fused, out_sep)
     assert torch.equal(sv_fused, sv_sep)
-    # inference (nothing saved; with the fused gate, Hl is never written) gives the same output
+    assert torch.equal(out_explicit, out_sep)
+    assert torch.equal(sv_explicit, sv_sep)
+    # inference (nothing saved; with the fused gate and D <= 512, Hl is never written) gives the same output
     out_i, none = a2a_ffn_forward(inputs, params, inference=True)
     assert none is None
     assert torch.equal(out_i, out_sep)
-    out_if, _ = a2a_ffn_forward(inputs, params, inference=True, flags=DG_FFN_FUSED_GATE)
-    assert torch.equal(out_if, out_sep)
+    out_is, _ = a2a_ffn_forward(inputs, params, inference=True, flags=DG_FFN_SEPARATE_GATE)
+    assert torch.equal(out_is, out_sep)
 
 
 # ------------------------------------------------------------------ comp_only

@@ -165,8 +165,8 @@ def test_tp_linear_forward_backward_write_only_their_outputs(rows, fin, fout):
 
 
 @pytest.mark.parametrize("P,B,T,D,k", [(2, 4, 16, 128, 2), (2, 3, 4, 136, 3), (4, 40, 16, 64, 2)])
-@pytest.mark.parametrize("flags", [0, dg.DG_FFN_COMP_ONLY, dg.DG_FFN_FUSED_GATE,
-                                   dg.DG_FFN_COMP_ONLY | dg.DG_FFN_FUSED_GATE])
+@pytest.mark.parametrize("flags", [0, dg.DG_FFN_COMP_ONLY, dg.DG_FFN_SEPARATE_GATE,
+                                   dg.DG_FFN_COMP_ONLY | dg.DG_FFN_SEPARATE_GATE])
 def test_a2a_ffn_inference_and_comp_only_write_only_their_buffers(P, B, T, D, k, flags):
     t = synth.ffn_inputs(P, B, T, D, k, seed=P + B + T + D + k + 1, device=DEV)
     params = {n: t[n] for n in dg.FFN_PARAM_NAMES}
