@@ -548,7 +548,8 @@ size_t dg_a2a_ffn_fwd_workspace_bytes(const dg_ffn_shape* shape, int32_t inferen
 
 size_t dg_a2a_ffn_bwd_workspace_bytes(const dg_ffn_shape* shape, uint32_t flags) {
   FfnDims f{};
-  if (check_ffn_shape(shape, &f) != DG_OK || (flags & ~DG_FFN_COMP_ONLY)) return 0;
+  if (check_ffn_shape(shape, &f) != DG_OK || (flags & ~kFfnFlagsKnown)) return 0;
+  if ((flags & DG_FFN_FUSED_GATE) && (flags & DG_FFN_SEPARATE_GATE)) return 0;
   return bwd_layout(f, flags).total;
 }
 
@@ -742,7 +743,10 @@ dg_status dg_a2a_ffn_bwd(const dg_ffn_shape* shape, const void* inputs, const vo
   FfnDims f{};
   dg_status st = check_ffn_shape(shape, &f);
   if (st != DG_OK) return st;
-  if ((st = check_ffn_flags(f, flags, DG_FFN_COMP_ONLY, "a2a_ffn_bwd")) != DG_OK) return st;
+  // The forward's flags: comp_only applies; the gate flags are checked the
+  // same way but leave the backward unchanged (its row sums are a pass of
+  // their own either way).
+  if ((st = check_ffn_flags(f, flags, kFfnFlagsKnown, "a2a_ffn_bwd")) != DG_OK) return st;
   (void)b1;
   (void)bout;
   // What each requested gradient needs: dZ (from dHl and the LayerNorm-gate

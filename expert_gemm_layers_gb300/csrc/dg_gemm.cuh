@@ -580,6 +580,8 @@ __global__ void __launch_bounds__(GemmCfg<kFp8, kAMN, kBMN, kEpi, kPair, kBN>::N
             tmem_ld_32x32b_x32(lane_addr + col, ra);
             tmem_ld_32x32b_x32(lane_addr + col + Cfg::BN / 2, rb);
             tmem_ld_wait();
+            tmem_regs_after_wait(ra);
+            tmem_regs_after_wait(rb);
             if (h == 1 && j + 1 == nchunks && last_ld_in_loop) release_acc();
 #pragma unroll
             for (int i = 0; i < 32; ++i)
@@ -591,6 +593,8 @@ __global__ void __launch_bounds__(GemmCfg<kFp8, kAMN, kBMN, kEpi, kPair, kBN>::N
           tmem_ld_32x32b_x32(lane_addr + col, r0);
           tmem_ld_32x32b_x32(lane_addr + col + 32, r1);
           tmem_ld_wait();
+          tmem_regs_after_wait(r0);
+          tmem_regs_after_wait(r1);
           if (j + 1 == nchunks && last_ld_in_loop) release_acc();
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
@@ -728,6 +732,7 @@ __global__ void __launch_bounds__(GemmCfg<kFp8, kAMN, kBMN, kEpi, kPair, kBN>::N
           uint32_t r0[32];
           tmem_ld_32x32b_x32(lane_addr + static_cast<uint32_t>(acc * Cfg::ACC_STRIDE + Cfg::BN_OUT - 32), r0);
           tmem_ld_wait();
+          tmem_regs_after_wait(r0);
           release_acc();
           const int row = row0 + lane;
           if (row < p.M) {

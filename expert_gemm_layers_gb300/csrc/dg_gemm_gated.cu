@@ -404,6 +404,7 @@ __global__ void __launch_bounds__(GatedCfg::NUM_THREADS, 1)
           uint32_t r[32];
           tmem_ld_32x32b_x32(lane_addr + static_cast<uint32_t>(64 * j + 32 * h), r);
           tmem_ld_wait();
+          tmem_regs_after_wait(r);
           if (h == 1 && j + 1 == nchunks) release_acc();
           uint32_t packed[16];
 #pragma unroll

@@ -214,6 +214,17 @@ static __device__ __forceinline__ void tmem_ld_wait() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+// The registers a tcgen05.ld writes hold its data only once tcgen05.wait::ld
+// has completed, but to the compiler they are defined by the load statement,
+// so it may schedule their first use before the wait.  An empty volatile
+// statement that rewrites each of them, placed right after the wait (volatile
+// statements keep their order), makes every use depend on a point after it.
+template <int N>
+static __device__ __forceinline__ void tmem_regs_after_wait(uint32_t (&r)[N]) {
+#pragma unroll
+  for (int i = 0; i < N; ++i) asm volatile("" : "+r"(r[i]));
+}
+
 // Shared-memory matrix descriptor of a 128-byte-swizzled operand tile.
 // start: byte address of the (sub)matrix; lbo / sbo: leading / stride byte
 // offsets.  Bits 46-47 carry the descriptor version used by tcgen05 and bits

@@ -855,6 +855,7 @@ __global__ void __launch_bounds__(kApThreads, 4) ln_gate_bwd_apply_kernel(
     const __nv_bfloat16* __restrict__ bg, __nv_bfloat16* __restrict__ dZ, float* __restrict__ part, int M, int L, int H,
     uint32_t* err) {
   extern __shared__ __align__(128) uint8_t ap_smem[];
+  __shared__ volatile uint32_t ap_sink;  // written only to order slot releases after their loads
   uint64_t* full = reinterpret_cast<uint64_t*>(ap_smem + kApRing * kApStageBytes);
   uint64_t* empty = full + kApRing;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -935,8 +936,17 @@ __global__ void __launch_bounds__(kApThreads, 4) ln_gate_bwd_apply_kernel(
     }
     const float4* rcs = reinterpret_cast<const float4*>(slot + 3 * kApSeg);
     const float4 cst = rcs[0], csum = rcs[1];
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[stage]);
+    // Release the slot only once every lane's loads of it have returned: the
+    // arrive could otherwise overtake a load still being served, and the
+    // producer's next copy overwrite part of what the load reads.  A word of
+    // each load, OR-ed over the warp (which needs every lane's operands) and
+    // stored before the arrive, makes the release wait for them.
+    const uint32_t dep = __reduce_or_sync(0xffffffffu, pu.x | pg.x | ph.x | __float_as_uint(cst.x) |
+                                                           __float_as_uint(csum.x));
+    if (lane == 0) {
+      ap_sink = dep;
+      mbar_arrive(&empty[stage]);
+    }
     if (++stage == kApRing) {
       stage = 0;
       phase ^= 1u;

@@ -209,7 +209,8 @@ def a2a_ffn_backward(inputs: torch.Tensor, params: dict, saved: torch.Tensor, dY
     Returns a dict with keys "inputs" and the names in FFN_PARAM_NAMES.  With
     `need` (a subset of those keys) only those gradients are computed (the
     others are None and their work is skipped); `grads` may hold None entries
-    for the same effect.  flags: DG_FFN_COMP_ONLY (as given to the forward).
+    for the same effect.  flags: those given to the forward (DG_FFN_COMP_ONLY
+    applies; the gate flags are accepted and leave the backward unchanged).
     """
     lib = load()
     P, B, T, D = inputs.shape

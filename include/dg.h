@@ -173,8 +173,13 @@ dg_status dg_a2a_ffn_fwd(const dg_ffn_shape* shape,
  * d_bout: its column sum; with d_inputs, d_w1, d_b1 and the four norm
  * gradients all NULL, also the dHl GEMM and the LayerNorm-gate backward).
  * Inputs only a skipped gradient needs may be NULL too (inputs for d_w1, w1
- * for d_inputs, saved for all but d_bout).  flags: DG_FFN_COMP_ONLY or 0.
- * Scratch: `ws` of dg_a2a_ffn_bwd_workspace_bytes(shape, flags).
+ * for d_inputs, saved for all but d_bout).
+ * flags  the forward's flags.  DG_FFN_COMP_ONLY as in the forward.  The gate
+ *        flags are checked as in the forward (both together are an invalid
+ *        argument) and do not change the backward: its LayerNorm-gate row
+ *        sums are always a pass of their own over Z and dHl.
+ * Scratch: `ws` of dg_a2a_ffn_bwd_workspace_bytes(shape, flags) (0 for
+ * invalid flags).
  */
 size_t dg_a2a_ffn_bwd_workspace_bytes(const dg_ffn_shape* shape, uint32_t flags);
 

@@ -63,7 +63,11 @@ def test_ffn_saved_and_workspace_sizes(lib):
     assert ws >= 256 + rows * (H * 2 + 2 * H * 2)
     act = 8 * 512 * 64 * 1280 * 2
     assert lib.dg_a2a_ffn_bwd_workspace_bytes(ctypes.byref(sh), 1) >= ws + 3 * act     # comp_only buffers
-    assert lib.dg_a2a_ffn_bwd_workspace_bytes(ctypes.byref(sh), 2) == 0                # not a backward flag
+    # the backward takes the forward's flags; the gate flags do not change it
+    assert lib.dg_a2a_ffn_bwd_workspace_bytes(ctypes.byref(sh), 2) == ws
+    assert lib.dg_a2a_ffn_bwd_workspace_bytes(ctypes.byref(sh), 4) == ws
+    assert lib.dg_a2a_ffn_bwd_workspace_bytes(ctypes.byref(sh), 2 | 4) == 0           # exclusive flags
+    assert lib.dg_a2a_ffn_bwd_workspace_bytes(ctypes.byref(sh), 8) == 0               # unknown flag
     # forward: training needs the error block only; inference holds Z, the statistics and partials
     assert lib.dg_a2a_ffn_fwd_workspace_bytes(ctypes.byref(sh), 0, 0) == 256
     inf = lib.dg_a2a_ffn_fwd_workspace_bytes(ctypes.byref(sh), 1, 0)
@@ -114,9 +118,11 @@ def test_ffn_flags_and_error_block_checked_before_the_device(lib):
     st = lib.dg_a2a_ffn_bwd(*bw, p[9], 1 << 12, p[10], p[1], None, None, None, None, None, None, None, None,
                             None, 0, 0, None)
     assert STATUS_NAMES[st] == "DG_ERR_INVALID_ARGUMENT" and b"w1" in lib.dg_last_error()
-    # backward: comp_only is the only flag it takes
-    st = lib.dg_a2a_ffn_bwd(ctypes.byref(sh), *p[:9], p[9], 1 << 12, p[10], *([None] * 9), None, 0, 2, None)
-    assert STATUS_NAMES[st] == "DG_ERR_INVALID_ARGUMENT"
+    # backward: the forward's flags, checked the same way
+    st = lib.dg_a2a_ffn_bwd(ctypes.byref(sh), *p[:9], p[9], 1 << 12, p[10], *([None] * 9), None, 0, 8, None)
+    assert STATUS_NAMES[st] == "DG_ERR_INVALID_ARGUMENT" and b"flags" in lib.dg_last_error()
+    st = lib.dg_a2a_ffn_bwd(ctypes.byref(sh), *p[:9], p[9], 1 << 12, p[10], *([None] * 9), None, 0, 2 | 4, None)
+    assert STATUS_NAMES[st] == "DG_ERR_INVALID_ARGUMENT" and b"exclude" in lib.dg_last_error()
 
 
 def test_error_block_query_functions(lib):

@@ -5,6 +5,7 @@ full-size workload on seeded row / token-position subsets, which is exact
 per row because each output row and each problem's weight gradients depend
 only on their own rows.  The exchange permutations are compared bit for bit.
 """
+import ctypes
 import os
 
 import numpy as np
@@ -339,6 +340,46 @@ def test_fused_gate_equals_separate_pass_bit_for_bit(P, B, T, D, k):
     assert torch.equal(out_i, out_sep)
     out_is, _ = a2a_ffn_forward(inputs, params, inference=True, flags=DG_FFN_SEPARATE_GATE)
     assert torch.equal(out_is, out_sep)
+
+
+@pytest.mark.parametrize("P,B,T,D,k", [(2, 3, 4, 136, 3), (2, 128, 2, 1280, 6)])
+def test_backward_takes_the_forward_gate_flags(P, B, T, D, k):
+    # the backward accepts the flags given to the forward; the gate flags
+    # leave it unchanged, so every gradient is the same bits
+    inputs, params = _inputs(P, B, T, D, k, seed=71 + D + k, device=DEV)
+    dY = synth.ffn_grad_output(P, B, T, D, seed=72 + D, device=DEV)
+    _, saved = a2a_ffn_forward(inputs, params)
+    g0 = a2a_ffn_backward(inputs, params, saved, dY)
+    for flags in (DG_FFN_FUSED_GATE, DG_FFN_SEPARATE_GATE):
+        g = a2a_ffn_backward(inputs, params, saved, dY, flags=flags)
+        for n in g0:
+            assert torch.equal(g0[n], g[n]), (flags, n)
+
+
+def test_backward_full_size_repeats_bit_for_bit():
+    # Five backward passes at P=8, B=512, T=64, D=1280, k=6 into one workspace,
+    # refilled with a non-finite pattern before every other pass, give the
+    # same bits every time.  This caught a stage of the LayerNorm-gate apply
+    # pass's copy ring being released before its loads had returned: the
+    # next row's copy then overwrote part of a load in flight, leaving about
+    # one row of dZ per pass computed from another row's G columns.
+    P, B, T, D, k = 8, 512, 64, 1280, 6
+    inputs, params = _inputs(P, B, T, D, k, seed=42, device=DEV)
+    dY = synth.ffn_grad_output(P, B, T, D, seed=43, device=DEV)
+    _, saved = a2a_ffn_forward(inputs, params)
+    lib = dg._lib.load()
+    sh = dg._lib.FFNShape(P, B, T, D, k, 1e-5)
+    ws = dg.alloc_workspace(lib.dg_a2a_ffn_bwd_workspace_bytes(ctypes.byref(sh), 0), DEV)
+    ref = a2a_ffn_backward(inputs, params, saved, dY, workspace=ws)
+    ref = {n: v.clone() for n, v in ref.items()}
+    grads = {n: torch.empty_like(v) for n, v in ref.items()}
+    for it in range(5):
+        if it % 2 == 0:
+            ws[256:].fill_(0x7F)
+        a2a_ffn_backward(inputs, params, saved, dY, workspace=ws, grads=grads)
+        torch.cuda.synchronize()
+        for n in ref:
+            assert torch.equal(grads[n], ref[n]), (it, n)
 
 
 # ------------------------------------------------------------------ comp_only

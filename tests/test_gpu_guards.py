@@ -183,8 +183,8 @@ def test_a2a_ffn_inference_and_comp_only_write_only_their_buffers(P, B, T, D, k,
         fws = g.workspace(lib.dg_a2a_ffn_fwd_workspace_bytes(ctypes.byref(sh), 0, flags))
         dg.a2a_ffn_forward(x, params, saved=saved, out=g.like(x), flags=flags, ws=fws)
         dY = synth.ffn_grad_output(P, B, T, D, seed=8, device=DEV)
-        bws = g.workspace(lib.dg_a2a_ffn_bwd_workspace_bytes(ctypes.byref(sh), dg.DG_FFN_COMP_ONLY))
+        bws = g.workspace(lib.dg_a2a_ffn_bwd_workspace_bytes(ctypes.byref(sh), flags))
         grads = {"inputs": g.like(x)}
         grads.update({n: g.like(params[n]) for n in dg.FFN_PARAM_NAMES})
-        dg.a2a_ffn_backward(x, params, saved, dY, workspace=bws, grads=grads, flags=dg.DG_FFN_COMP_ONLY)
+        dg.a2a_ffn_backward(x, params, saved, dY, workspace=bws, grads=grads, flags=flags)
         g.check(f"a2a_ffn comp_only backward {P, B, T, D, k}")
