@@ -51,18 +51,18 @@ FALLBACK_PEAKS = dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=
 # sources changed since reports null.  The capture's summary is committed with
 # the other ncu summaries of this repository.
 TRAFFIC = {
-    "ffn_gemm1": {"bytes_per_launch": 8 * 1.389358e+09, "sources": ["expert_gemm_layers_gb300/csrc/dg_gemm.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh", "expert_gemm_layers_gb300/csrc/dg_gemm_bf16_km_lnstats.cu", "expert_gemm_layers_gb300/csrc/dg_api.cu"], "sha256": "6f5d5bb788ec31cd4eadff3af767fbf38b2f00fb9e700f83adbe6d37c2e58ce9"},
-    "ffn_ln_stats": {"bytes_per_launch": 8 * 3.147341e+07, "sources": ["expert_gemm_layers_gb300/csrc/dg_rowops.cu", "expert_gemm_layers_gb300/csrc/dg_gate.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh"], "sha256": "070f3ba90f80902fa2dffa524380bba6013dc6dab8f58248a4b7b7ba8daaf711"},
-    "ffn_gemm2_gated": {"bytes_per_launch": 8 * 1.573220e+09, "sources": ["expert_gemm_layers_gb300/csrc/dg_gemm_gated.cu", "expert_gemm_layers_gb300/csrc/dg_gate.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh", "expert_gemm_layers_gb300/csrc/dg_api.cu"], "sha256": "561932b9d744a48b99a81ff6f5d226bcf6b2e1b5f1fc914d9f9b5d8689248ffe"},
-    "ffn_gemm2_rest": {"bytes_per_launch": 8 * 7.041393e+08, "sources": ["expert_gemm_layers_gb300/csrc/dg_gemm.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh", "expert_gemm_layers_gb300/csrc/dg_gemm_bf16_km_bias.cu", "expert_gemm_layers_gb300/csrc/dg_api.cu"], "sha256": "28a307d71a17aa0f8f43cae379bd59bc34f29e25f752988f9e06479f3c2f2dfb"},
-    "ffn_bwd_dhl": {"bytes_per_launch": 8 * 6.898706e+08, "sources": ["expert_gemm_layers_gb300/csrc/dg_gemm.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh", "expert_gemm_layers_gb300/csrc/dg_gemm_bf16_kk_store.cu", "expert_gemm_layers_gb300/csrc/dg_api.cu"], "sha256": "8a59cbfdb1e0196befc7f7a106e94370b22edb6f77dc1414b4ac6962a2e8da17"},
-    "ffn_bwd_dwout": {"bytes_per_launch": 8 * 7.538304e+08, "sources": ["expert_gemm_layers_gb300/csrc/dg_gemm.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh", "expert_gemm_layers_gb300/csrc/dg_gemm_bf16_mm_store.cu", "expert_gemm_layers_gb300/csrc/dg_api.cu"], "sha256": "fbe7eae26e7178c268aabb26011175fee575e881adddf5b70f58aa7f9c0d495c"},
-    "ffn_bwd_dbout": {"bytes_per_launch": 8 * 8.392499e+07, "sources": ["expert_gemm_layers_gb300/csrc/dg_rowops.cu", "expert_gemm_layers_gb300/csrc/dg_gate.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh"], "sha256": "070f3ba90f80902fa2dffa524380bba6013dc6dab8f58248a4b7b7ba8daaf711"},
-    "ffn_bwd_ln_rowsum": {"bytes_per_launch": 8 * 1.512544e+09, "sources": ["expert_gemm_layers_gb300/csrc/dg_rowops.cu", "expert_gemm_layers_gb300/csrc/dg_gate.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh"], "sha256": "070f3ba90f80902fa2dffa524380bba6013dc6dab8f58248a4b7b7ba8daaf711"},
-    "ffn_bwd_ln_apply": {"bytes_per_launch": 8 * 2.524226e+09, "sources": ["expert_gemm_layers_gb300/csrc/dg_rowops.cu", "expert_gemm_layers_gb300/csrc/dg_gate.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh"], "sha256": "070f3ba90f80902fa2dffa524380bba6013dc6dab8f58248a4b7b7ba8daaf711"},
-    "ffn_bwd_grad_reduce": {"bytes_per_launch": 8 * 4.725274e+07, "sources": ["expert_gemm_layers_gb300/csrc/dg_rowops.cu", "expert_gemm_layers_gb300/csrc/dg_gate.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh"], "sha256": "070f3ba90f80902fa2dffa524380bba6013dc6dab8f58248a4b7b7ba8daaf711"},
-    "ffn_bwd_dx": {"bytes_per_launch": 8 * 2.168298e+09, "sources": ["expert_gemm_layers_gb300/csrc/dg_gemm.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh", "expert_gemm_layers_gb300/csrc/dg_gemm_bf16_kk_store.cu", "expert_gemm_layers_gb300/csrc/dg_api.cu"], "sha256": "8a59cbfdb1e0196befc7f7a106e94370b22edb6f77dc1414b4ac6962a2e8da17"},
-    "ffn_bwd_dw1": {"bytes_per_launch": 8 * 1.514869e+09, "sources": ["expert_gemm_layers_gb300/csrc/dg_gemm.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh", "expert_gemm_layers_gb300/csrc/dg_gemm_bf16_mm_store.cu", "expert_gemm_layers_gb300/csrc/dg_api.cu"], "sha256": "fbe7eae26e7178c268aabb26011175fee575e881adddf5b70f58aa7f9c0d495c"},
+    "ffn_gemm1": {"bytes_per_launch": 8 * 1.385666e+09, "sources": ["expert_gemm_layers_gb300/csrc/dg_gemm.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh", "expert_gemm_layers_gb300/csrc/dg_gemm_bf16_km_lnstats.cu", "expert_gemm_layers_gb300/csrc/dg_api.cu"], "sha256": "07b159e4bbb09f23988902b0bf077ef8b80bf25753960ae9df865d51fe835018"},
+    "ffn_ln_stats": {"bytes_per_launch": 8 * 3.147315e+07, "sources": ["expert_gemm_layers_gb300/csrc/dg_rowops.cu", "expert_gemm_layers_gb300/csrc/dg_gate.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh"], "sha256": "ea365d14712a1ad5be858188fced02f64b83d3ab504a542fd1d29b681c9acb93"},
+    "ffn_gemm2_gated": {"bytes_per_launch": 8 * 1.573281e+09, "sources": ["expert_gemm_layers_gb300/csrc/dg_gemm_gated.cu", "expert_gemm_layers_gb300/csrc/dg_gate.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh", "expert_gemm_layers_gb300/csrc/dg_api.cu"], "sha256": "c3cf68bbbb7cd6b7f06a5b36ba41ec9dbbced9bfb478687bf7ed3481c1a5d275"},
+    "ffn_gemm2_rest": {"bytes_per_launch": 8 * 7.045676e+08, "sources": ["expert_gemm_layers_gb300/csrc/dg_gemm.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh", "expert_gemm_layers_gb300/csrc/dg_gemm_bf16_km_bias.cu", "expert_gemm_layers_gb300/csrc/dg_api.cu"], "sha256": "dde9856cb24d1e3024b1048dc8e39beee94f6dec81c34cbc31c4fff404065c8a"},
+    "ffn_bwd_dhl": {"bytes_per_launch": 8 * 6.893816e+08, "sources": ["expert_gemm_layers_gb300/csrc/dg_gemm.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh", "expert_gemm_layers_gb300/csrc/dg_gemm_bf16_kk_store.cu", "expert_gemm_layers_gb300/csrc/dg_api.cu"], "sha256": "efe94c9ca71d215ebdd5e913e5138fef6ff3499d726d470b4b62b71e9d1aa699"},
+    "ffn_bwd_dwout": {"bytes_per_launch": 8 * 7.416228e+08, "sources": ["expert_gemm_layers_gb300/csrc/dg_gemm.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh", "expert_gemm_layers_gb300/csrc/dg_gemm_bf16_mm_store.cu", "expert_gemm_layers_gb300/csrc/dg_api.cu"], "sha256": "b1b66f1d79739eea6a711feb91d7f7b1457367056fea15b1edada529e34530cc"},
+    "ffn_bwd_dbout": {"bytes_per_launch": 8 * 8.397286e+07, "sources": ["expert_gemm_layers_gb300/csrc/dg_rowops.cu", "expert_gemm_layers_gb300/csrc/dg_gate.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh"], "sha256": "ea365d14712a1ad5be858188fced02f64b83d3ab504a542fd1d29b681c9acb93"},
+    "ffn_bwd_ln_rowsum": {"bytes_per_launch": 8 * 1.512550e+09, "sources": ["expert_gemm_layers_gb300/csrc/dg_rowops.cu", "expert_gemm_layers_gb300/csrc/dg_gate.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh"], "sha256": "ea365d14712a1ad5be858188fced02f64b83d3ab504a542fd1d29b681c9acb93"},
+    "ffn_bwd_ln_apply": {"bytes_per_launch": 8 * 2.522037e+09, "sources": ["expert_gemm_layers_gb300/csrc/dg_rowops.cu", "expert_gemm_layers_gb300/csrc/dg_gate.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh"], "sha256": "ea365d14712a1ad5be858188fced02f64b83d3ab504a542fd1d29b681c9acb93"},
+    "ffn_bwd_grad_reduce": {"bytes_per_launch": 8 * 4.725248e+07, "sources": ["expert_gemm_layers_gb300/csrc/dg_rowops.cu", "expert_gemm_layers_gb300/csrc/dg_gate.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh"], "sha256": "ea365d14712a1ad5be858188fced02f64b83d3ab504a542fd1d29b681c9acb93"},
+    "ffn_bwd_dx": {"bytes_per_launch": 8 * 1.764650e+09, "sources": ["expert_gemm_layers_gb300/csrc/dg_gemm.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh", "expert_gemm_layers_gb300/csrc/dg_gemm_bf16_kk_store.cu", "expert_gemm_layers_gb300/csrc/dg_api.cu"], "sha256": "efe94c9ca71d215ebdd5e913e5138fef6ff3499d726d470b4b62b71e9d1aa699"},
+    "ffn_bwd_dw1": {"bytes_per_launch": 8 * 1.408519e+09, "sources": ["expert_gemm_layers_gb300/csrc/dg_gemm.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh", "expert_gemm_layers_gb300/csrc/dg_gemm_bf16_mm_store.cu", "expert_gemm_layers_gb300/csrc/dg_api.cu"], "sha256": "b1b66f1d79739eea6a711feb91d7f7b1457367056fea15b1edada529e34530cc"},
 }
 
 
