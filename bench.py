@@ -532,7 +532,12 @@ def run_dg(args, rank, world):
 
     # end to end: inputs from pinned host memory in, results back to pinned
     # host memory; right after the device-timed steps, in the same state of the GPU
+    # (with its own clock record: it runs after the device-timed steps, and at
+    # the power cap the SM clock can differ between the two)
+    e2e_clocks = ClockSampler(local)
+    e2e_clocks.start()
     e2e = run_e2e(w, args, dev, step_flops, world)
+    e2e["clocks"] = e2e_clocks.stop()
 
     # outside the step: the FP8 GEMM alone (L2 flushed before each launch),
     # the TP SwiGLU backward (recompute [a|b], dh, gate backward, dw2, dX,
