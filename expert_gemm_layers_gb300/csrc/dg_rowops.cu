@@ -838,8 +838,8 @@ __global__ void __launch_bounds__(kRsThreads, 1) ln_gate_bwd_rowsum_bulk_kernel(
 // into a ring of shared-memory stages with cp.async.bulk; three consumer
 // warps (8 columns a thread) hold the fp32 affines and the six column sums in
 // registers, write dZ, and release each stage (one arrival a warp) as soon as
-// they have read it.  Four warps a CTA keep the SM's four sub-partitions
-// evenly loaded.
+// their loads of it have returned.  Four warps a CTA keep the SM's four
+// sub-partitions evenly loaded.
 constexpr int kApConsumers = 3;
 constexpr int kApCols = 8 * 32 * kApConsumers;  // columns of one CTA: 768
 constexpr int kApThreads = 32 * (kApConsumers + 1);
