@@ -837,8 +837,8 @@ __global__ void __launch_bounds__(kRsThreads, 1) ln_gate_bwd_rowsum_bulk_kernel(
 // CTA's column segments of U, G and dHl plus the row's coefficient record
 // into a ring of shared-memory stages with cp.async.bulk; three consumer
 // warps (8 columns a thread) hold the fp32 affines and the six column sums in
-// registers, write dZ, and release each stage (one arrival a warp) as soon as
-// their loads of it have returned.  Four warps a CTA keep the SM's four
+// registers, write dZ, and release each row's stage (one arrival a warp) at
+// the start of the next row.  Four warps a CTA keep the SM's four
 // sub-partitions evenly loaded.
 constexpr int kApConsumers = 3;
 constexpr int kApCols = 8 * 32 * kApConsumers;  // columns of one CTA: 768
@@ -855,7 +855,6 @@ __global__ void __launch_bounds__(kApThreads, 4) ln_gate_bwd_apply_kernel(
     const __nv_bfloat16* __restrict__ bg, __nv_bfloat16* __restrict__ dZ, float* __restrict__ part, int M, int L, int H,
     uint32_t* err) {
   extern __shared__ __align__(128) uint8_t ap_smem[];
-  __shared__ volatile uint32_t ap_sink;  // written only to order slot releases after their loads
   uint64_t* full = reinterpret_cast<uint64_t*>(ap_smem + kApRing * kApStageBytes);
   uint64_t* empty = full + kApRing;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -927,6 +926,14 @@ __global__ void __launch_bounds__(kApThreads, 4) ln_gate_bwd_apply_kernel(
   for (int i = 0; i < n_rows; ++i) {
     const bool ok = mbar_wait(&full[stage], phase, err, 0x56u);
     if (!__all_sync(0xffffffffu, ok)) break;
+    // Release the previous row's stage: every lane has issued that row's
+    // stores (this warp-wide vote follows them), and they need values
+    // computed from every load of the stage that is used, so those loads have
+    // returned.  (Released right after its loads, a stage could be refilled
+    // while a load of it was still being served, and the next row's copy
+    // overwrote part of what it read.)  The last row's stage is never
+    // released; nothing waits for it.
+    if (i > 0 && lane == 0) mbar_arrive(&empty[stage == 0 ? kApRing - 1 : stage - 1]);
     const uint8_t* slot = ap_smem + stage * kApStageBytes;
     uint4 pu = make_uint4(0u, 0u, 0u, 0u), pg = pu, ph = pu;
     if (active) {
@@ -936,17 +943,6 @@ __global__ void __launch_bounds__(kApThreads, 4) ln_gate_bwd_apply_kernel(
     }
     const float4* rcs = reinterpret_cast<const float4*>(slot + 3 * kApSeg);
     const float4 cst = rcs[0], csum = rcs[1];
-    // Release the slot only once every lane's loads of it have returned: the
-    // arrive could otherwise overtake a load still being served, and the
-    // producer's next copy overwrite part of what the load reads.  A word of
-    // each load, OR-ed over the warp (which needs every lane's operands) and
-    // stored before the arrive, makes the release wait for them.
-    const uint32_t dep = __reduce_or_sync(0xffffffffu, pu.x | pg.x | ph.x | __float_as_uint(cst.x) |
-                                                           __float_as_uint(csum.x));
-    if (lane == 0) {
-      ap_sink = dep;
-      mbar_arrive(&empty[stage]);
-    }
     if (++stage == kApRing) {
       stage = 0;
       phase ^= 1u;
