@@ -51,18 +51,18 @@ FALLBACK_PEAKS = dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=
 # sources changed since reports null.  The capture's summary is committed with
 # the other ncu summaries of this repository.
 TRAFFIC = {
-    "ffn_gemm1": {"bytes_per_launch": 8 * 1.385666e+09, "sources": ["expert_gemm_layers_gb300/csrc/dg_gemm.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh", "expert_gemm_layers_gb300/csrc/dg_gemm_bf16_km_lnstats.cu", "expert_gemm_layers_gb300/csrc/dg_api.cu"], "sha256": "07b159e4bbb09f23988902b0bf077ef8b80bf25753960ae9df865d51fe835018"},
-    "ffn_ln_stats": {"bytes_per_launch": 8 * 3.147315e+07, "sources": ["expert_gemm_layers_gb300/csrc/dg_rowops.cu", "expert_gemm_layers_gb300/csrc/dg_gate.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh"], "sha256": "c54a9cc3b571bcbec42e6420a7d0284686d9c3f9fe7d048a507a14df43fe818d"},
-    "ffn_gemm2_gated": {"bytes_per_launch": 8 * 1.573281e+09, "sources": ["expert_gemm_layers_gb300/csrc/dg_gemm_gated.cu", "expert_gemm_layers_gb300/csrc/dg_gate.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh", "expert_gemm_layers_gb300/csrc/dg_api.cu"], "sha256": "c3cf68bbbb7cd6b7f06a5b36ba41ec9dbbced9bfb478687bf7ed3481c1a5d275"},
-    "ffn_gemm2_rest": {"bytes_per_launch": 8 * 7.045676e+08, "sources": ["expert_gemm_layers_gb300/csrc/dg_gemm.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh", "expert_gemm_layers_gb300/csrc/dg_gemm_bf16_km_bias.cu", "expert_gemm_layers_gb300/csrc/dg_api.cu"], "sha256": "dde9856cb24d1e3024b1048dc8e39beee94f6dec81c34cbc31c4fff404065c8a"},
-    "ffn_bwd_dhl": {"bytes_per_launch": 8 * 6.893816e+08, "sources": ["expert_gemm_layers_gb300/csrc/dg_gemm.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh", "expert_gemm_layers_gb300/csrc/dg_gemm_bf16_kk_store.cu", "expert_gemm_layers_gb300/csrc/dg_api.cu"], "sha256": "efe94c9ca71d215ebdd5e913e5138fef6ff3499d726d470b4b62b71e9d1aa699"},
-    "ffn_bwd_dwout": {"bytes_per_launch": 8 * 7.416228e+08, "sources": ["expert_gemm_layers_gb300/csrc/dg_gemm.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh", "expert_gemm_layers_gb300/csrc/dg_gemm_bf16_mm_store.cu", "expert_gemm_layers_gb300/csrc/dg_api.cu"], "sha256": "b1b66f1d79739eea6a711feb91d7f7b1457367056fea15b1edada529e34530cc"},
-    "ffn_bwd_dbout": {"bytes_per_launch": 8 * 8.397286e+07, "sources": ["expert_gemm_layers_gb300/csrc/dg_rowops.cu", "expert_gemm_layers_gb300/csrc/dg_gate.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh"], "sha256": "c54a9cc3b571bcbec42e6420a7d0284686d9c3f9fe7d048a507a14df43fe818d"},
-    "ffn_bwd_ln_rowsum": {"bytes_per_launch": 8 * 1.512550e+09, "sources": ["expert_gemm_layers_gb300/csrc/dg_rowops.cu", "expert_gemm_layers_gb300/csrc/dg_gate.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh"], "sha256": "c54a9cc3b571bcbec42e6420a7d0284686d9c3f9fe7d048a507a14df43fe818d"},
-    "ffn_bwd_ln_apply": {"bytes_per_launch": 8 * 2.522037e+09, "sources": ["expert_gemm_layers_gb300/csrc/dg_rowops.cu", "expert_gemm_layers_gb300/csrc/dg_gate.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh"], "sha256": "c54a9cc3b571bcbec42e6420a7d0284686d9c3f9fe7d048a507a14df43fe818d"},
-    "ffn_bwd_grad_reduce": {"bytes_per_launch": 8 * 4.725248e+07, "sources": ["expert_gemm_layers_gb300/csrc/dg_rowops.cu", "expert_gemm_layers_gb300/csrc/dg_gate.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh"], "sha256": "c54a9cc3b571bcbec42e6420a7d0284686d9c3f9fe7d048a507a14df43fe818d"},
-    "ffn_bwd_dx": {"bytes_per_launch": 8 * 1.764650e+09, "sources": ["expert_gemm_layers_gb300/csrc/dg_gemm.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh", "expert_gemm_layers_gb300/csrc/dg_gemm_bf16_kk_store.cu", "expert_gemm_layers_gb300/csrc/dg_api.cu"], "sha256": "efe94c9ca71d215ebdd5e913e5138fef6ff3499d726d470b4b62b71e9d1aa699"},
-    "ffn_bwd_dw1": {"bytes_per_launch": 8 * 1.408519e+09, "sources": ["expert_gemm_layers_gb300/csrc/dg_gemm.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh", "expert_gemm_layers_gb300/csrc/dg_gemm_bf16_mm_store.cu", "expert_gemm_layers_gb300/csrc/dg_api.cu"], "sha256": "b1b66f1d79739eea6a711feb91d7f7b1457367056fea15b1edada529e34530cc"},
+    "ffn_gemm1": {"bytes_per_launch": 8 * 1.386602e+09, "sources": ["expert_gemm_layers_gb300/csrc/dg_gemm.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh", "expert_gemm_layers_gb300/csrc/dg_gemm_bf16_km_lnstats.cu", "expert_gemm_layers_gb300/csrc/dg_api.cu"], "sha256": "07b159e4bbb09f23988902b0bf077ef8b80bf25753960ae9df865d51fe835018"},
+    "ffn_ln_stats": {"bytes_per_launch": 8 * 3.147341e+07, "sources": ["expert_gemm_layers_gb300/csrc/dg_rowops.cu", "expert_gemm_layers_gb300/csrc/dg_gate.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh"], "sha256": "34454a0547e4ce1103037b8d8921ba87fd8ba11de4a1f897e625b5b5d8c168bf"},
+    "ffn_gemm2_gated": {"bytes_per_launch": 8 * 1.573366e+09, "sources": ["expert_gemm_layers_gb300/csrc/dg_gemm_gated.cu", "expert_gemm_layers_gb300/csrc/dg_gate.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh", "expert_gemm_layers_gb300/csrc/dg_api.cu"], "sha256": "c3cf68bbbb7cd6b7f06a5b36ba41ec9dbbced9bfb478687bf7ed3481c1a5d275"},
+    "ffn_gemm2_rest": {"bytes_per_launch": 8 * 7.040044e+08, "sources": ["expert_gemm_layers_gb300/csrc/dg_gemm.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh", "expert_gemm_layers_gb300/csrc/dg_gemm_bf16_km_bias.cu", "expert_gemm_layers_gb300/csrc/dg_api.cu"], "sha256": "dde9856cb24d1e3024b1048dc8e39beee94f6dec81c34cbc31c4fff404065c8a"},
+    "ffn_bwd_dhl": {"bytes_per_launch": 8 * 6.894607e+08, "sources": ["expert_gemm_layers_gb300/csrc/dg_gemm.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh", "expert_gemm_layers_gb300/csrc/dg_gemm_bf16_kk_store.cu", "expert_gemm_layers_gb300/csrc/dg_api.cu"], "sha256": "efe94c9ca71d215ebdd5e913e5138fef6ff3499d726d470b4b62b71e9d1aa699"},
+    "ffn_bwd_dwout": {"bytes_per_launch": 8 * 7.436754e+08, "sources": ["expert_gemm_layers_gb300/csrc/dg_gemm.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh", "expert_gemm_layers_gb300/csrc/dg_gemm_bf16_mm_store.cu", "expert_gemm_layers_gb300/csrc/dg_api.cu"], "sha256": "b1b66f1d79739eea6a711feb91d7f7b1457367056fea15b1edada529e34530cc"},
+    "ffn_bwd_dbout": {"bytes_per_launch": 8 * 8.392038e+07, "sources": ["expert_gemm_layers_gb300/csrc/dg_rowops.cu", "expert_gemm_layers_gb300/csrc/dg_gate.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh"], "sha256": "34454a0547e4ce1103037b8d8921ba87fd8ba11de4a1f897e625b5b5d8c168bf"},
+    "ffn_bwd_ln_rowsum": {"bytes_per_launch": 8 * 1.512565e+09, "sources": ["expert_gemm_layers_gb300/csrc/dg_rowops.cu", "expert_gemm_layers_gb300/csrc/dg_gate.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh"], "sha256": "34454a0547e4ce1103037b8d8921ba87fd8ba11de4a1f897e625b5b5d8c168bf"},
+    "ffn_bwd_ln_apply": {"bytes_per_launch": 8 * 2.527671e+09, "sources": ["expert_gemm_layers_gb300/csrc/dg_rowops.cu", "expert_gemm_layers_gb300/csrc/dg_gate.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh"], "sha256": "34454a0547e4ce1103037b8d8921ba87fd8ba11de4a1f897e625b5b5d8c168bf"},
+    "ffn_bwd_grad_reduce": {"bytes_per_launch": 8 * 4.725248e+07, "sources": ["expert_gemm_layers_gb300/csrc/dg_rowops.cu", "expert_gemm_layers_gb300/csrc/dg_gate.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh"], "sha256": "34454a0547e4ce1103037b8d8921ba87fd8ba11de4a1f897e625b5b5d8c168bf"},
+    "ffn_bwd_dx": {"bytes_per_launch": 8 * 1.848908e+09, "sources": ["expert_gemm_layers_gb300/csrc/dg_gemm.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh", "expert_gemm_layers_gb300/csrc/dg_gemm_bf16_kk_store.cu", "expert_gemm_layers_gb300/csrc/dg_api.cu"], "sha256": "efe94c9ca71d215ebdd5e913e5138fef6ff3499d726d470b4b62b71e9d1aa699"},
+    "ffn_bwd_dw1": {"bytes_per_launch": 8 * 1.415758e+09, "sources": ["expert_gemm_layers_gb300/csrc/dg_gemm.cuh", "expert_gemm_layers_gb300/csrc/dg_ptx.cuh", "expert_gemm_layers_gb300/csrc/dg_gemm_bf16_mm_store.cu", "expert_gemm_layers_gb300/csrc/dg_api.cu"], "sha256": "b1b66f1d79739eea6a711feb91d7f7b1457367056fea15b1edada529e34530cc"},
 }
 
 
